@@ -1,0 +1,20 @@
+"""GB300-native `element-scan`: nonlinear per-lane recurrences on sm_103a.
+
+The compute path is the C-ABI library ``libes.so`` (hand-written CUDA kernels
+for sm_103a, declared in ``include/es.h``); ``scan`` and friends are a thin
+ctypes binding over it that only marshals arguments.  The binding loads the
+library on first use and raises if it is missing: there is no CPU fallback.
+"""
+from . import workloads  # noqa: F401  (pure Python: seeded inputs only)
+
+_BINDING_NAMES = {
+    "scan", "scan_into", "scan_host", "lib", "LibraryMissing", "EsError",
+    "TANH_DECAY", "NORMCAP", "MAXPLUS", "device_status", "plan", "status_string",
+}
+
+
+def __getattr__(name):
+    if name in _BINDING_NAMES:
+        from . import binding
+        return getattr(binding, name)
+    raise AttributeError(name)

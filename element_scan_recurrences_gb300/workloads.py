@@ -1,0 +1,128 @@
+"""Seeded synthetic inputs for `element-scan` workloads.
+
+This module only draws random numbers and describes shapes: it holds none of
+the scan's arithmetic, so both the CUDA path and the CPU oracle may be fed
+from it.  Every draw comes from one ``torch.Generator`` seeded per workload,
+in the order x, then the second sequence (decay / gate / cost), then initial.
+
+Distributions: ``("normal", mu, sigma)`` is ``mu + sigma * randn``;
+``("uniform", lo, hi)`` is ``lo + (hi - lo) * rand``; ``("const", v)`` is a
+constant fill.  The five named workloads are the element-scan cases the
+library is measured and checked on: a small TANH_DECAY case, a wide-lane
+TANH_DECAY case, a NORMCAP vector-state case, a reverse MAXPLUS case and a
+TANH_DECAY case whose sequence axis is innermost.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import List, Optional, Sequence, Tuple
+
+import torch
+
+TANH_DECAY = 0
+NORMCAP = 1
+MAXPLUS = 2
+BODY_NAMES = {TANH_DECAY: "TANH_DECAY", NORMCAP: "NORMCAP", MAXPLUS: "MAXPLUS"}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    body: int
+    shape: Tuple[int, ...]            # output shape (= full-width sequence shape)
+    axis: int
+    state_axis: bool
+    seq_widths: Tuple[int, int]       # last width of x and of the second sequence
+    reverse: Tuple[bool, ...]         # directions that are run
+    x_dist: tuple
+    a_dist: tuple
+    init_dist: tuple
+    seed: int = 0
+
+    @property
+    def rank(self) -> int:
+        return len(self.shape)
+
+    @property
+    def ax(self) -> int:
+        return self.axis + self.rank if self.axis < 0 else self.axis
+
+    @property
+    def T(self) -> int:
+        return self.shape[self.ax]
+
+    @property
+    def elements(self) -> int:
+        return math.prod(self.shape)
+
+    def seq_shape(self, k: int) -> Tuple[int, ...]:
+        s = list(self.shape)
+        if self.state_axis:
+            s[-1] = self.seq_widths[k]
+        return tuple(s)
+
+    @property
+    def init_shape(self) -> Tuple[int, ...]:
+        return tuple(d for i, d in enumerate(self.shape) if i != self.ax)
+
+    def algorithmic_bytes(self) -> int:
+        """f32 bytes read (both sequences and initial) plus states written."""
+        reads = sum(math.prod(self.seq_shape(k)) for k in range(2))
+        return 4 * (reads + math.prod(self.init_shape) + self.elements)
+
+    def with_shape(self, shape: Sequence[int], name: Optional[str] = None) -> "Workload":
+        """Same body, axis and distributions at another shape."""
+        return dataclasses.replace(self, shape=tuple(shape), name=name or self.name + "@" + "x".join(map(str, shape)))
+
+
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("tanh_decay_small", TANH_DECAY, (2, 64, 8), 1, False, (8, 8), (False,),
+                 ("normal", 0.0, 1.0), ("uniform", 0.0, 0.9), ("normal", 0.0, 0.1)),
+        Workload("tanh_decay_lanes", TANH_DECAY, (64, 4096, 1024), 1, False, (1024, 1024), (False,),
+                 ("normal", 0.0, 1.0), ("uniform", 0.5, 0.99), ("const", 0.0)),
+        Workload("normcap_vector", NORMCAP, (32, 8192, 64, 16), 1, True, (16, 1), (False,),
+                 ("normal", 0.0, 0.5), ("uniform", 0.8, 1.0), ("const", 0.0)),
+        Workload("maxplus_reverse", MAXPLUS, (128, 16384, 128), 1, False, (128, 128), (True,),
+                 ("uniform", -1.0, 1.0), ("uniform", 0.0, 0.1), ("const", -3.0e38)),
+        Workload("tanh_decay_time_inner", TANH_DECAY, (262144, 1024), -1, False, (1024, 1024), (False, True),
+                 ("normal", 0.0, 1.0), ("uniform", 0.5, 0.99), ("normal", 0.0, 0.1)),
+    ]
+}
+ORDER = ["tanh_decay_small", "tanh_decay_lanes", "normcap_vector", "maxplus_reverse",
+         "tanh_decay_time_inner"]
+
+
+def _draw(dist: tuple, shape, gen: torch.Generator, device) -> torch.Tensor:
+    kind = dist[0]
+    if kind == "normal":
+        t = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+        return t.mul_(dist[2]).add_(dist[1])
+    if kind == "uniform":
+        t = torch.rand(shape, generator=gen, device=device, dtype=torch.float32)
+        return t.mul_(dist[2] - dist[1]).add_(dist[1])
+    if kind == "const":
+        return torch.full(shape, dist[1], device=device, dtype=torch.float32)
+    raise ValueError("unknown distribution %r" % (dist,))
+
+
+def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None):
+    """Draw (initial, [x, second]) for a workload, seeded, on ``device``."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed if seed is None else seed)
+    x = _draw(w.x_dist, w.seq_shape(0), gen, device)
+    a = _draw(w.a_dist, w.seq_shape(1), gen, device)
+    init = _draw(w.init_dist, w.init_shape, gen, device)
+    return init, [x, a]
+
+
+def custom(body: int, shape, axis: int, state_axis: bool = False, seq_widths=None,
+           reverse: bool = False, x_dist=("normal", 0.0, 1.0), a_dist=("uniform", 0.5, 0.99),
+           init_dist=("normal", 0.0, 0.1), seed: int = 0, name: str = "custom") -> Workload:
+    """An ad-hoc workload (tests use it for shapes outside the named five)."""
+    shape = tuple(int(d) for d in shape)
+    if seq_widths is None:
+        seq_widths = (shape[-1], shape[-1])
+    return Workload(name, body, shape, axis, state_axis, tuple(seq_widths), (reverse,),
+                    x_dist, a_dist, init_dist, seed)

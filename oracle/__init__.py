@@ -1,0 +1,163 @@
+"""CPU oracle for `element-scan` -- TEST INFRASTRUCTURE, not the product.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the bench's CPU-baseline
+and reference arms may import this package.  The product path (the CUDA
+library and its Python binding) never imports it and shares no code with it.
+
+The arithmetic lives in ``es_oracle.c`` (a plain lane-by-lane loop, built with
+``gcc -O2 -ffp-contract=off``); this module only compiles it and marshals numpy
+arrays across ctypes.  Semantics follow "Nonlinear element scans"
+(sx.041.io/docs/element-scan.md): intro (forward recurrence, output holds the
+state after every trip), the `:state-axis` example (NORMCAP), the `:reverse`
+paragraph (MAXPLUS, reverse order) and "Arguments and body" (shapes).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "es_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libes_oracle.so")
+
+TANH_DECAY = 0
+NORMCAP = 1
+MAXPLUS = 2
+BODIES = {"TANH_DECAY": TANH_DECAY, "NORMCAP": NORMCAP, "MAXPLUS": MAXPLUS}
+
+_lock = threading.Lock()
+_lib = None
+
+GCC_FLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+
+def compile_source(src: str, lib_path: str) -> str:
+    """Compile an oracle source file into a shared library at ``lib_path``."""
+    os.makedirs(os.path.dirname(lib_path), exist_ok=True)
+    tmp = lib_path + ".%d.tmp" % os.getpid()
+    subprocess.run(["gcc"] + GCC_FLAGS + ["-o", tmp, src, "-lm"], check=True)
+    os.replace(tmp, lib_path)
+    return lib_path
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into a shared library (plain gcc, no fast-math)."""
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        compile_source(_SRC, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(lib_path: str):
+    lib = ctypes.CDLL(lib_path)
+    for name, ft in (("es_oracle_f32", ctypes.c_float),
+                     ("es_oracle_f64", ctypes.c_double)):
+        fn = getattr(lib, name)
+        fn.restype = ctypes.c_int
+        fn.argtypes = [
+            ctypes.c_int,                         # body
+            ctypes.POINTER(ft),                   # initial
+            ctypes.POINTER(ctypes.POINTER(ft)),   # seqs
+            ctypes.c_int,                         # n_seqs
+            ctypes.POINTER(ctypes.c_int64),       # shape
+            ctypes.c_int,                         # rank
+            ctypes.c_int,                         # axis
+            ctypes.c_int,                         # state_width
+            ctypes.POINTER(ctypes.c_int64),       # seq_widths or NULL
+            ctypes.c_int,                         # reverse
+            ctypes.POINTER(ft),                   # out
+        ]
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _bind(_LIB_PATH)
+    return _lib
+
+
+def _body_id(body) -> int:
+    if isinstance(body, str):
+        return BODIES[body.upper()]
+    return int(body)
+
+
+def scan(body, initial, seqs, axis: int = 0, state_axis: bool = False,
+         reverse: bool = False, dtype=np.float32, _lib=None) -> np.ndarray:
+    """Run the oracle on host arrays and return the states after every trip.
+
+    ``initial`` has the output shape with ``axis`` removed; ``seqs`` is a list
+    of two arrays.  Without ``state_axis`` both have the output shape; with it,
+    each may have its own last width (1 or the state width W).
+    ``dtype=np.float64`` runs the double-precision diagnostic twin.
+    """
+    lib = _lib if _lib is not None else _load()
+    ft = ctypes.c_float if dtype == np.float32 else ctypes.c_double
+    fn = lib.es_oracle_f32 if dtype == np.float32 else lib.es_oracle_f64
+    seqs = [np.ascontiguousarray(np.asarray(s, dtype=dtype)) for s in seqs]
+    initial = np.ascontiguousarray(np.asarray(initial, dtype=dtype))
+    if len(seqs) != 2:
+        raise ValueError("every body takes exactly two sequences")
+    # output shape: the first sequence's shape; under a state axis its last
+    # dim is the state width, which is initial's last dim
+    shape = list(seqs[0].shape)
+    rank = len(shape)
+    if state_axis:
+        if initial.ndim < 1 or rank < 2:
+            raise ValueError("a state axis needs rank >= 2")
+        shape[-1] = initial.shape[-1]
+    W = shape[-1] if state_axis else 0
+    ax = axis + rank if axis < 0 else axis
+    if not 0 <= ax < rank:
+        raise ValueError("axis %d out of range for rank %d" % (axis, rank))
+    want_init = shape[:ax] + shape[ax + 1:]
+    if list(initial.shape) != want_init:
+        raise ValueError("initial shape %r, expected %r" % (list(initial.shape), want_init))
+    for s in seqs:
+        want = list(shape)
+        if state_axis and s.ndim == rank and s.shape[-1] == 1:
+            want[-1] = 1
+        if list(s.shape) != want:
+            raise ValueError("sequence shape %r, expected %r" % (list(s.shape), want))
+    widths = None
+    if state_axis:
+        widths = (ctypes.c_int64 * 2)(*[s.shape[-1] for s in seqs])
+    out = np.empty(shape, dtype=dtype)
+    ptrs = (ctypes.POINTER(ft) * 2)(*[s.ctypes.data_as(ctypes.POINTER(ft)) for s in seqs])
+    rc = fn(_body_id(body), initial.ctypes.data_as(ctypes.POINTER(ft)), ptrs, 2,
+            (ctypes.c_int64 * rank)(*shape), rank, int(axis), int(W), widths,
+            int(bool(reverse)), out.ctypes.data_as(ctypes.POINTER(ft)))
+    if rc != 0:
+        raise ValueError("oracle rejected arguments: body=%r shape=%r axis=%r state_axis=%r"
+                         % (body, shape, axis, state_axis))
+    return out
+
+
+class Oracle:
+    """An oracle bound to one compiled library (tests load mutated builds)."""
+
+    def __init__(self, lib_path: str):
+        self._lib = _bind(lib_path)
+
+    def scan(self, body, initial, seqs, axis: int = 0, state_axis: bool = False,
+             reverse: bool = False, dtype=np.float32) -> np.ndarray:
+        return scan(body, initial, seqs, axis=axis, state_axis=state_axis,
+                    reverse=reverse, dtype=dtype, _lib=self._lib)
+
+
+def scan_lanes(body, initial, x, a, reverse: bool = False) -> np.ndarray:
+    """Scalar-state scan over independent lanes laid out as [L, T] rows.
+
+    Convenience for sampled-lane parity: ``x`` and ``a`` are [L, T], ``initial``
+    is [L]; the scan axis is 1.
+    """
+    return scan(body, initial, [x, a], axis=1, state_axis=False, reverse=reverse)

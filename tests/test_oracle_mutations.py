@@ -1,0 +1,69 @@
+"""Plant plausible mistakes in the oracle (on the CPU, in a temporary copy of
+its source) and check that the pins catch every one of them.
+
+A mutant is the oracle's C source with one exact text replacement; it is
+compiled with the oracle's own flags into a temporary directory and run
+through every pin of ``oracle_pins``.  The committed oracle is never touched.
+"""
+import os
+
+import pytest
+
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "es_oracle.c")
+
+# (id, text in the float32 oracle, replacement, which occurrence (0-based))
+MUTATIONS = [
+    ("tanh_sign_of_decay_term", "float v = xv + ah;", "float v = xv - ah;", 0),
+    ("tanh_dropped_decay_term", "float v = xv + ah;", "float v = xv;", 0),
+    ("tanh_transposed_operand", "float ah = av * h[w];", "float ah = av * xv;", 0),
+    ("tanh_missing_tanh", "h[w] = oracle_tanh(v);", "h[w] = v;", 0),
+    ("maxplus_sign_of_cost", "float v = h[w] - cv;", "float v = h[w] + cv;", 0),
+    ("maxplus_dropped_cost", "h[w] = oracle_maximum(v, xv);", "h[w] = oracle_maximum(h[w], xv);", 0),
+    ("maxplus_min_instead_of_max", "if (a > b) return a;", "if (a < b) return a;", 0),
+    ("maximum_zero_sign", "return signbit(a) ? b : a;", "return a;", 0),
+    ("normcap_no_floor_at_one", "float d = oracle_maximum(1.0f, sqrtf(ss));", "float d = sqrtf(ss);", 0),
+    ("normcap_norm_without_square", "float sq = y[w] * y[w];", "float sq = y[w] < 0 ? -y[w] : y[w];", 0),
+    ("normcap_dropped_input", "y[w] = ah + xv;", "y[w] = ah;", 0),
+    ("normcap_gate_on_input", "float ah = av * h[w];", "float ah = av * xv;", 1),
+    ("reverse_ignored", "int64_t t = reverse ? T - 1 - s : s;", "int64_t t = s;", 0),
+    ("output_in_trip_order", "float *ot = out + ((o * T + t) * J + j) * W;",
+     "float *ot = out + ((o * T + s) * J + j) * W;", 0),
+    ("initial_ignored", "h[w] = initial[(o * J + j) * W + w];", "h[w] = 0.0f;", 0),
+    ("initial_lane_index", "h[w] = initial[(o * J + j) * W + w];", "h[w] = initial[(j * O + o) % (O * J) * W + w];", 0),
+    ("second_sequence_time_shift", "const float *at = a + ((o * T + t) * J + j) * sw[1];",
+     "const float *at = a + ((o * T + (t + 1) % T) * J + j) * sw[1];", 0),
+    ("gate_ignores_broadcast", "float av = at[sw[1] == 1 ? 0 : w];", "float av = at[0];", 1),
+]
+
+
+def _mutate(src, old, new, occ):
+    idx = -1
+    for _ in range(occ + 1):
+        idx = src.index(old, idx + 1)
+    return src[:idx] + new + src[idx + len(old):]
+
+
+def test_mutation_targets_exist():
+    src = open(SRC).read()
+    for mid, old, new, occ in MUTATIONS:
+        assert src.count(old) > occ, mid
+
+
+@pytest.mark.parametrize("mid,old,new,occ", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_mutant(mid, old, new, occ, tmp_path, oracle_mod):
+    src = open(SRC).read()
+    mutated = _mutate(src, old, new, occ)
+    assert mutated != src
+    cfile = tmp_path / "mutant.c"
+    cfile.write_text(mutated)
+    lib = oracle_mod.compile_source(str(cfile), str(tmp_path / "libmutant.so"))
+    mutant = oracle_mod.Oracle(lib)
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(mutant.scan)
+        except (AssertionError, ValueError) as e:   # noqa: PERF203
+            caught.append(pin.__name__)
+    assert caught, "no pin caught the planted mistake %s" % mid
