@@ -1,0 +1,444 @@
+#!/usr/bin/env python3
+"""Benchmark of the element-scan library on one GB300 (or N, one process each).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole scan over one batch of the workload (every
+direction the workload names).  Inputs are seeded synthetic tensors already
+resident in HBM when the timed region starts; they are larger than the 129 MB
+L2, so no flush is needed between steps.  Device time comes from CUDA events
+on the launching stream; the timed region is bracketed by a barrier and a
+synchronize on both sides and the slowest rank's time is used.  Rank 0 prints
+one JSON line.
+
+``e2e`` is the same metric end to end through the public API with host
+buffers: every step copies its inputs from pinned host memory, scans, and
+copies the states back.  ``cpu_baseline`` times the CPU oracle (test
+infrastructure, a plain loop) on a bounded sample of the same workload.
+``--impl reference`` times only that oracle, as the comparison arm.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "element-scan elements/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "elements/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+PATH_KERNEL = {"lane_tma": "k_lane_tma", "time_tma": "k_time_tma", "vec_tma": "k_vec_tma", "generic": "k_generic"}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; timing only, no data exchange)
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    """The largest `value` over all ranks (the slowest rank's time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        cmd = ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + ",".join(self.FIELDS),
+               "--format=csv,noheader,nounits", "-lms", str(period_ms)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "nvidia-smi unavailable"}
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        used = inside
+        note = "samples inside the timed region"
+        if len(inside) < 3:
+            # a short timed region: widen to the whole measurement window
+            used = [p for _, p in self.samples]
+            note = "timed region shorter than the sampling period; samples over warm-up and timed steps"
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+
+        sm = sorted(v for v in (num(p[0]) for p in used) if v is not None)
+        mx = [v for v in (num(p[1]) for p in used) if v is not None]
+        reasons = set()
+        for p in used:
+            for name, val in zip(self.REASONS, p[4:8]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(used), "samples_in_timed_region": len(inside),
+                "note": note}
+
+
+# ---------------------------------------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "element_scan_recurrences_gb300", "csrc", "*")))
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None when there is none or the kernel sources changed since."""
+    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, workload))
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    s = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_source_hash():
+        return None
+    return int(m.group(1))
+
+
+def plan_of(es, w, reverse):
+    return es.plan(w.body, w.shape, w.axis, w.shape[-1] if w.state_axis else 0,
+                   w.seq_widths if w.state_axis else None, reverse)
+
+
+def take_sample(w, init, seqs, target_elems: int):
+    """Whole sequences of a leading block of lanes, about `target_elems` output
+    values per direction: the first rows along dim 0 (or, when one row is
+    already larger, the first positions of the last lane axis of row 0)."""
+    x, a = seqs
+    if w.ax == 0:
+        raise ValueError("sampling needs a dimension before the sequence axis")
+    per_row = w.elements // w.shape[0]
+    if per_row <= target_elems:
+        k = max(1, min(w.shape[0], target_elems // per_row))
+        pick = lambda t: t[:k]
+        desc = "first %d of %d rows along dim 0" % (k, w.shape[0])
+        elems = k * per_row
+    else:
+        lane_dim = w.rank - 2 if w.state_axis else w.rank - 1
+        n_last = w.shape[lane_dim]
+        m = max(1, min(n_last, int(n_last * target_elems / per_row)))
+        if w.state_axis:
+            pick = lambda t: t[:1, ..., :m, :]
+        else:
+            pick = lambda t: t[:1, ..., :m]
+        desc = "row 0 along dim 0, first %d of %d positions along dim %d" % (m, n_last, lane_dim)
+        elems = per_row * m // n_last
+    cpu = lambda t: pick(t).contiguous().cpu().numpy()
+    return cpu(init), cpu(x), cpu(a), elems, desc
+
+
+def cpu_oracle_rate(w, init, seqs, budget_s: float):
+    """Time the oracle (as it stands, one thread) on a leading block of lanes
+    of the workload; return (elements/s, description, threads)."""
+    import oracle
+    oracle.build()
+
+    def run(target):
+        ins, xs, as_, elems, desc = take_sample(w, init, seqs, target)
+        t0 = time.perf_counter()
+        for reverse in w.reverse:
+            oracle.scan(w.body, ins, [xs, as_], axis=w.axis, state_axis=w.state_axis, reverse=reverse)
+        return time.perf_counter() - t0, elems * len(w.reverse), desc
+
+    target = 1 << 20
+    t, elems, desc = run(target)
+    if t < budget_s / 4:
+        target = int(target * budget_s / max(t, 1e-3))
+        t, elems, desc = run(target)
+    desc = "%s of the same workload (%d elements, %s), one thread" % (
+        desc, elems, "+".join("reverse" if r else "forward" for r in w.reverse))
+    return elems / t, desc, 1
+
+
+def run_reference(args, w):
+    """--impl reference: the CPU oracle as the comparison arm."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from element_scan_recurrences_gb300 import workloads as wl
+    oracle.build()
+    init, seqs = wl.make_inputs(w, "cpu")
+    # each step scans a bounded sample so that the whole run stays short
+    step_budget = max(0.05, min(1.0, 120.0 / max(1, args.steps + args.warmup)))
+    ins, xs, as_, elems, _ = take_sample(w, init, seqs, 1 << 18)
+    t0 = time.perf_counter()
+    for r in w.reverse:
+        oracle.scan(w.body, ins, [xs, as_], axis=w.axis, state_axis=w.state_axis, reverse=r)
+    t_cal = time.perf_counter() - t0
+    target = max(1, int((1 << 18) * step_budget / max(t_cal, 1e-4)))
+    ins, xs, as_, elems, desc = take_sample(w, init, seqs, target)
+    for _ in range(args.warmup):
+        for r in w.reverse:
+            oracle.scan(w.body, ins, [xs, as_], axis=w.axis, state_axis=w.state_axis, reverse=r)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for r in w.reverse:
+            oracle.scan(w.body, ins, [xs, as_], axis=w.axis, state_axis=w.state_axis, reverse=r)
+    dt = time.perf_counter() - t0
+    elems *= len(w.reverse)
+    value = elems * args.steps / dt
+    sample_desc = "%s of the same workload (%d elements per step), one thread" % (desc, elems)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample_desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w):
+    return {"workload": w.name, "body": ["TANH_DECAY", "NORMCAP", "MAXPLUS"][w.body], "shape": list(w.shape),
+            "axis": w.axis, "state_axis": w.state_axis, "seq_widths": list(w.seq_widths) if w.state_axis else None,
+            "directions": ["reverse" if r else "forward" for r in w.reverse], "elements_per_step": w.elements *
+            len(w.reverse), "algorithmic_bytes_per_step": w.algorithmic_bytes() * len(w.reverse),
+            "l2": "no flush: inputs and outputs (%.2f GB) exceed the 129 MB L2" % (w.algorithmic_bytes() / 1e9)}
+
+
+def run_ours(args, w):
+    import torch
+    from element_scan_recurrences_gb300 import binding as es
+    from element_scan_recurrences_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device; the library has no CPU path")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    es.lib()
+
+    # weak scaling: each rank scans its own batch of the workload (own seed)
+    init, seqs = wl.make_inputs(w, device, seed=w.seed + rank)
+    out = torch.empty(w.shape, device=device, dtype=torch.float32)
+    outs = [out] + [torch.empty_like(out) for _ in w.reverse[1:]]
+    stream = torch.cuda.current_stream(device)
+    plans = [plan_of(es, w, r) for r in w.reverse]
+
+    def step():
+        for o, r in zip(outs, w.reverse):
+            es.scan_into(w.body, init, seqs, o, axis=w.axis, state_axis=w.state_axis, reverse=r, stream=stream)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    for _ in range(max(args.warmup, 0)):
+        step()
+    es.device_status(stream)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    launches0 = es.launch_count()
+    t_host0 = time.time()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(device)
+    t_host1 = time.time()
+    barrier(dist, device)
+    launches = es.launch_count() - launches0
+    es.device_status(stream)
+    per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    region_ms = starts[0].elapsed_time(ends[-1])
+    region_ms = max_over_ranks(dist, region_ms, device)
+    if sampler is not None:
+        sampler.stop()
+        clocks = sampler.summary(t_host0, t_host1)
+    else:
+        clocks = None
+
+    elems_step = w.elements * len(w.reverse)
+    total_elems = sum_over_ranks(dist, float(elems_step * args.steps), device)
+    value = total_elems / (region_ms / 1e3)
+    kernel_ms = sum(per_step_ms) / len(per_step_ms) / len(w.reverse)
+
+    # roofline of the dominant kernel (every launch of a step is the same kernel)
+    peak, peak_kind = measured_peaks()
+    alg_bytes = w.algorithmic_bytes()
+    achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
+    kernel = PATH_KERNEL.get(plans[0]["path"], plans[0]["path"])
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": profiled_traffic(kernel, w.name), "kernel": kernel,
+                "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": kernel_ms,
+                "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs, copy burst)" % peak_kind
+                if peak_kind == "measured" else "fallback 6.8 TB/s"}
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        init_h = init.cpu().pin_memory()
+        seqs_h = [s.cpu().pin_memory() for s in seqs]
+        out_h = [torch.empty(w.shape, dtype=torch.float32).pin_memory() for _ in w.reverse]
+        h2d = (init_h.numel() + sum(s.numel() for s in seqs_h)) * 4
+        d2h = sum(o.numel() for o in out_h) * 4
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+
+        def e2e_step():
+            for oh, od, r in zip(out_h, outs, w.reverse):
+                es.scan_host(w.body, init_h, seqs_h, oh, (init, seqs, od), axis=w.axis, state_axis=w.state_axis,
+                             reverse=r, stream=stream)
+
+        e2e_step()
+        torch.cuda.synchronize(device)
+        barrier(dist, device)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(dist, device)
+        e_ms = max_over_ranks(dist, e0.elapsed_time(e1), device)
+        e2e = {"value": sum_over_ranks(dist, float(elems_step * e2e_steps), device) / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d * (len(w.reverse)), "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "ms_per_step": e_ms / e2e_steps}
+        del init_h, seqs_h, out_h
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, desc, cores = cpu_oracle_rate(w, init, seqs, args.cpu_budget)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": region_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(config_of(w), parallelism="replicas: each GPU scans its own batch" if world > 1
+                           else "single GPU", path=plans[0]["path"]),
+            "achieved_gbs": achieved, "hbm_frac": achieved / peak,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="tanh_decay_lanes")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    from element_scan_recurrences_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -8,8 +8,9 @@ library on first use and raises if it is missing: there is no CPU fallback.
 from . import workloads  # noqa: F401  (pure Python: seeded inputs only)
 
 _BINDING_NAMES = {
-    "scan", "scan_into", "scan_host", "lib", "LibraryMissing", "EsError",
+    "scan", "scan_into", "scan_host", "lib", "LibraryMissing", "EsError", "PATHS",
     "TANH_DECAY", "NORMCAP", "MAXPLUS", "device_status", "plan", "status_string",
+    "launch_count", "set_path_override", "set_wait_limit_ns", "set_drop_tile",
 }
 
 

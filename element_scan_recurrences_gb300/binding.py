@@ -1,0 +1,231 @@
+"""ctypes binding over libes.so (include/es.h).
+
+Argument marshalling only: every step of a scan runs in the library's CUDA
+kernels.  The binding raises ``LibraryMissing`` when libes.so has not been
+built and ``EsError`` (with the library's message) for every non-OK status;
+there is no CPU fallback.  Tensors are PyTorch CUDA tensors (PyTorch supplies
+device memory and streams only).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence
+
+from . import build as _build
+
+TANH_DECAY = 0
+NORMCAP = 1
+MAXPLUS = 2
+_BODIES = {"TANH_DECAY": TANH_DECAY, "NORMCAP": NORMCAP, "MAXPLUS": MAXPLUS}
+
+STATUS = {0: "ES_OK", 1: "ES_E_DIM_001", 2: "ES_E_DIM_002", 3: "ES_E_ARG", 4: "ES_E_UNSUPPORTED",
+          5: "ES_E_CUDA", 6: "ES_E_TIMEOUT"}
+PATHS = {0: "auto", 1: "empty", 2: "generic", 3: "lane_tma", 4: "time_tma", 5: "vec_tma"}
+PATH_IDS = {v: k for k, v in PATHS.items()}
+
+# every function include/es.h declares
+EXPORTS = ("es_scan_f32", "es_plan_f32", "es_device_status", "es_last_error", "es_status_string",
+           "es_launch_count", "es_set_path_override", "es_set_wait_limit_ns", "es_set_drop_tile")
+
+
+class LibraryMissing(ImportError):
+    pass
+
+
+class EsError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (STATUS.get(status, status), message))
+        self.status = status
+        self.message = message
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("O", ctypes.c_int64), ("T", ctypes.c_int64), ("J", ctypes.c_int64), ("W", ctypes.c_int64),
+                ("seq_width", ctypes.c_int64 * 2), ("elements", ctypes.c_int64), ("path", ctypes.c_int),
+                ("reverse", ctypes.c_int)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """Load libes.so (built in-tree); raise LibraryMissing if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise LibraryMissing("libes.so is not built (%s); run __graft_entry__.build() first" % path)
+        L = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        sig = [ctypes.c_int, P, ctypes.POINTER(P), ctypes.c_int, i64p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+               i64p, ctypes.c_int, P]
+        L.es_scan_f32.argtypes = sig + [P]
+        L.es_scan_f32.restype = ctypes.c_int
+        L.es_plan_f32.argtypes = sig + [ctypes.POINTER(PlanInfo)]
+        L.es_plan_f32.restype = ctypes.c_int
+        L.es_device_status.argtypes = [P]
+        L.es_device_status.restype = ctypes.c_int
+        L.es_last_error.argtypes = []
+        L.es_last_error.restype = ctypes.c_char_p
+        L.es_status_string.argtypes = [ctypes.c_int]
+        L.es_status_string.restype = ctypes.c_char_p
+        L.es_launch_count.argtypes = []
+        L.es_launch_count.restype = ctypes.c_uint64
+        L.es_set_path_override.argtypes = [ctypes.c_int]
+        L.es_set_path_override.restype = ctypes.c_int
+        L.es_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        L.es_set_wait_limit_ns.restype = ctypes.c_int
+        L.es_set_drop_tile.argtypes = [ctypes.c_int64]
+        L.es_set_drop_tile.restype = ctypes.c_int
+        _lib = L
+        return L
+
+
+def _check(status: int):
+    if status != 0:
+        raise EsError(status, lib().es_last_error().decode(errors="replace"))
+
+
+def status_string(status: int) -> str:
+    return lib().es_status_string(int(status)).decode()
+
+
+def _body_id(body) -> int:
+    if isinstance(body, str):
+        return _BODIES[body.upper()]
+    return int(body)
+
+
+def _args(body, shape, axis, state_width, seq_widths):
+    rank = len(shape)
+    shp = (ctypes.c_int64 * max(rank, 1))(*shape)
+    sw = None if seq_widths is None else (ctypes.c_int64 * 2)(*seq_widths)
+    return _body_id(body), shp, rank, int(axis), int(state_width), sw
+
+
+def plan(body, shape: Sequence[int], axis: int, state_width: int = 0, seq_widths=None, reverse: bool = False,
+         ptrs: Optional[Sequence[int]] = None) -> dict:
+    """Validate and plan a call without touching a GPU (pure host logic).
+
+    ``ptrs`` are the (initial, x, second, out) addresses to plan for; by
+    default 16-byte aligned, non-overlapping stand-ins.  Raises EsError for an
+    invalid call, else returns the canonical view and the kernel path.
+    """
+    b, shp, rank, ax, sw_, widths = _args(body, shape, axis, state_width, seq_widths)
+    if ptrs is None:
+        ptrs = [(k + 1) << 44 for k in range(4)]
+    seqs = (ctypes.c_void_p * 2)(ptrs[1], ptrs[2])
+    info = PlanInfo()
+    _check(lib().es_plan_f32(b, ptrs[0], seqs, 2, shp, rank, ax, sw_, widths, int(bool(reverse)), ptrs[3],
+                             ctypes.byref(info)))
+    return {"O": info.O, "T": info.T, "J": info.J, "W": info.W, "seq_width": (info.seq_width[0], info.seq_width[1]),
+            "elements": info.elements, "path": PATHS[info.path], "reverse": bool(info.reverse)}
+
+
+def _out_shape(initial, seqs, axis, state_axis):
+    shape = list(seqs[0].shape)
+    if state_axis:
+        shape[-1] = initial.shape[-1]
+    return shape
+
+
+def _require_cuda_f32(t, name):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+        raise TypeError("%s must be a contiguous float32 CUDA tensor (got %s %s, contiguous=%s)"
+                        % (name, t.device, t.dtype, t.is_contiguous()))
+
+
+def scan(body, initial, seqs, axis: int = 0, state_axis: bool = False, reverse: bool = False, out=None,
+         stream=None):
+    """Run one element scan on CUDA tensors; returns ``out`` (allocated if None).
+
+    ``seqs`` is ``[x, a]`` (TANH_DECAY, NORMCAP) or ``[x, c]`` (MAXPLUS).  The
+    call is asynchronous on ``stream`` (default: PyTorch's current stream).
+    """
+    import torch
+    seqs = list(seqs)
+    if len(seqs) != 2:
+        raise EsError(3, "every body takes exactly two sequences")
+    _require_cuda_f32(initial, "initial")
+    for k, s in enumerate(seqs):
+        _require_cuda_f32(s, "sequence %d" % k)
+    shape = _out_shape(initial, seqs, axis, state_axis)
+    if out is None:
+        out = torch.empty(shape, device=seqs[0].device, dtype=torch.float32)
+    else:
+        _require_cuda_f32(out, "out")
+        if list(out.shape) != shape:
+            raise EsError(1, "out shape %s does not match the output shape %s" % (list(out.shape), shape))
+    return scan_into(body, initial, seqs, out, axis=axis, state_axis=state_axis, reverse=reverse, stream=stream)
+
+
+def scan_into(body, initial, seqs, out, axis: int = 0, state_axis: bool = False, reverse: bool = False,
+              stream=None):
+    """es_scan_f32 on tensors the caller has already checked (no allocation)."""
+    import torch
+    shape = list(out.shape)
+    state_width = shape[-1] if state_axis else 0
+    seq_widths = [int(s.shape[-1]) for s in seqs] if state_axis else None
+    b, shp, rank, ax, sw_, widths = _args(body, shape, axis, state_width, seq_widths)
+    ptrs = (ctypes.c_void_p * 2)(seqs[0].data_ptr(), seqs[1].data_ptr())
+    if stream is None:
+        stream = torch.cuda.current_stream(out.device)
+    handle = stream if isinstance(stream, int) else stream.cuda_stream
+    _check(lib().es_scan_f32(b, initial.data_ptr(), ptrs, 2, shp, rank, ax, sw_, widths, int(bool(reverse)),
+                             out.data_ptr(), handle))
+    return out
+
+
+def scan_host(body, initial_h, seqs_h, out_h, dev_bufs, axis: int = 0, state_axis: bool = False,
+              reverse: bool = False, stream=None):
+    """End-to-end call on host tensors: copy the inputs from (pinned) host
+    memory into the caller's device buffers, scan, copy the states back.
+
+    ``dev_bufs`` = (initial_d, [x_d, a_d], out_d), preallocated by the caller.
+    Asynchronous on ``stream``; synchronise before reading ``out_h``.
+    """
+    import torch
+    init_d, seqs_d, out_d = dev_bufs
+    if stream is None:
+        stream = torch.cuda.current_stream(out_d.device)
+    with torch.cuda.stream(stream):
+        init_d.copy_(initial_h, non_blocking=True)
+        for d, h in zip(seqs_d, seqs_h):
+            d.copy_(h, non_blocking=True)
+        scan_into(body, init_d, seqs_d, out_d, axis=axis, state_axis=state_axis, reverse=reverse, stream=stream)
+        out_h.copy_(out_d, non_blocking=True)
+    return out_h
+
+
+def device_status(stream=None):
+    """Synchronise and raise EsError(ES_E_TIMEOUT) if a kernel gave up a wait."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream if isinstance(stream, int) else stream.cuda_stream
+    _check(lib().es_device_status(handle))
+
+
+def launch_count() -> int:
+    return int(lib().es_launch_count())
+
+
+def set_path_override(path) -> None:
+    _check(lib().es_set_path_override(PATH_IDS[path] if isinstance(path, str) else int(path)))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    _check(lib().es_set_wait_limit_ns(int(ns)))
+
+
+def set_drop_tile(k: int) -> None:
+    _check(lib().es_set_drop_tile(int(k)))

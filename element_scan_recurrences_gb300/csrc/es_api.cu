@@ -1,0 +1,335 @@
+// es_api.cu -- the C ABI of libes.so (declared in include/es.h): argument
+// validation, canonicalisation to [O, T, J, W], kernel-path choice and launch.
+//
+// Argument contract: "Nonlinear element scans", "Arguments and body" table
+// (initial = sequence shape minus the axis; sequences share one shape, under
+// a state axis except for their own last width; the axis may be negative and
+// its length is at least one; the state axis is the last axis and holds 1 to
+// 16 values).  Error classes: "Tensor operations", "Errors" (E-DIM-001 shapes
+// do not fit, E-DIM-002 dtypes; messages name both operands with their shapes).
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "es.h"
+#include "es_internal.h"
+
+// One status word per device, in the library's own device memory (module
+// scope), so no call allocates anything.  Kernels OR in ES_DEVICE_TIMEOUT.
+static __device__ unsigned int g_es_device_status;
+
+namespace {
+
+thread_local std::string t_error;
+
+std::atomic<int> g_path_override{ES_PATH_AUTO};
+std::atomic<uint64_t> g_wait_ns{2000000000ull};
+std::atomic<int64_t> g_drop_tile{-1};
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    unsigned int* status = nullptr;
+    int num_sms = 0;
+};
+DeviceState g_dev[kMaxDevices];
+
+std::once_flag g_encode_once;
+es::EncodeTiledFn g_encode = nullptr;
+
+es_status fail(es_status st, const char* fmt, ...) {
+    char buf[1024];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_error = buf;
+    return st;
+}
+
+std::string shape_str(const int64_t* shape, int rank, int replace_last = -1, int64_t last = 0) {
+    std::string s = "[";
+    for (int d = 0; d < rank; ++d) {
+        if (d) s += ", ";
+        s += std::to_string((d == rank - 1 && replace_last >= 0) ? last : shape[d]);
+    }
+    return s + "]";
+}
+
+bool mul_ok(int64_t a, int64_t b, int64_t* r) { return !__builtin_mul_overflow(a, b, r); }
+
+struct Plan {
+    int64_t O, T, J, W;
+    int64_t sw[2];
+    int64_t n_out, n_init, n_seq[2];
+    int path;
+};
+
+const char* kSeqName[3][2] = {{"x", "a"}, {"x", "a"}, {"x", "c"}};
+
+es_status plan_impl(es_body body, const float* initial, const float* const* seqs, int n_seqs, const int64_t* shape,
+                    int rank, int axis, int state_width, const int64_t* seq_widths, const float* out, Plan* P) {
+    if (body != ES_TANH_DECAY && body != ES_NORMCAP && body != ES_MAXPLUS)
+        return fail(ES_E_ARG, "es_scan_f32: unknown body id %d", static_cast<int>(body));
+    if (n_seqs != 2)
+        return fail(ES_E_ARG, "es_scan_f32: body %d takes the state and 2 sequences, got %d sequences",
+                    static_cast<int>(body), n_seqs);
+    if (shape == nullptr || seqs == nullptr) return fail(ES_E_ARG, "es_scan_f32: null shape or sequence list");
+    if (rank < 1 || rank > ES_MAX_RANK)
+        return fail(ES_E_UNSUPPORTED, "es_scan_f32: rank %d outside 1..%d", rank, ES_MAX_RANK);
+    for (int d = 0; d < rank; ++d)
+        if (shape[d] < 0)
+            return fail(ES_E_DIM_001, "E-DIM-001 es_scan_f32: negative dimension in %s",
+                        shape_str(shape, rank).c_str());
+    const std::string xs = shape_str(shape, rank);
+    if (axis < -rank || axis >= rank)
+        return fail(ES_E_DIM_001, "E-DIM-001 es_scan_f32: axis %d out of range for `%s` %s f32", axis,
+                    kSeqName[body][0], xs.c_str());
+    const int ax = axis < 0 ? axis + rank : axis;
+    if (shape[ax] < 1)
+        return fail(ES_E_DIM_001, "E-DIM-001 es_scan_f32: sequence axis %d of `%s` %s f32 has length %lld; it must be "
+                    "at least one", ax, kSeqName[body][0], xs.c_str(), static_cast<long long>(shape[ax]));
+    int64_t W = 1;
+    if (state_width != 0) {
+        if (rank < 2 || ax == rank - 1)
+            return fail(ES_E_DIM_001, "E-DIM-001 es_scan_f32: the state axis is the last axis of `%s` %s f32 and "
+                        "cannot also be the sequence axis %d", kSeqName[body][0], xs.c_str(), ax);
+        if (state_width < 1 || state_width > ES_MAX_STATE || shape[rank - 1] != state_width)
+            return fail(ES_E_DIM_001, "E-DIM-001 es_scan_f32: state width %d does not fit the last axis of `%s` %s "
+                        "f32 (1..%d values)", state_width, kSeqName[body][0], xs.c_str(), ES_MAX_STATE);
+        W = state_width;
+    } else if (body == ES_NORMCAP) {
+        return fail(ES_E_UNSUPPORTED, "es_scan_f32: NORMCAP reduces over its state and needs a state axis "
+                    "(state_width >= 1); a scalar state cannot reduce");
+    }
+    int64_t O = 1, after = 1;
+    for (int d = 0; d < ax; ++d)
+        if (!mul_ok(O, shape[d], &O)) return fail(ES_E_UNSUPPORTED, "es_scan_f32: element count overflows");
+    for (int d = ax + 1; d < rank; ++d)
+        if (!mul_ok(after, shape[d], &after)) return fail(ES_E_UNSUPPORTED, "es_scan_f32: element count overflows");
+    const int64_t T = shape[ax];
+    P->O = O;
+    P->T = T;
+    P->W = W;
+    P->J = after / W;
+    for (int k = 0; k < 2; ++k) {
+        int64_t w = W;
+        if (seq_widths != nullptr) {
+            w = seq_widths[k];
+            const bool fits = state_width != 0 ? (w == 1 || w == W) : (w == shape[rank - 1]);
+            if (!fits)
+                return fail(ES_E_DIM_001, "E-DIM-001 es_scan_f32: `%s` %s f32 does not fit `%s` %s f32%s",
+                            kSeqName[body][k], shape_str(shape, rank, 1, w).c_str(), kSeqName[body][0], xs.c_str(),
+                            state_width != 0 ? " (its last width must be 1 or the state width)" : "");
+        }
+        P->sw[k] = state_width != 0 ? w : 1;
+    }
+    int64_t rows, tmp;
+    if (!mul_ok(O, T, &rows) || !mul_ok(rows, after, &P->n_out) || !mul_ok(O, after, &P->n_init))
+        return fail(ES_E_UNSUPPORTED, "es_scan_f32: element count overflows");
+    for (int k = 0; k < 2; ++k)
+        if (!mul_ok(rows, P->J, &tmp) || !mul_ok(tmp, P->sw[k], &P->n_seq[k]))
+            return fail(ES_E_UNSUPPORTED, "es_scan_f32: element count overflows");
+    if (P->n_out > (int64_t(1) << 60)) return fail(ES_E_UNSUPPORTED, "es_scan_f32: too many elements");
+
+    if (O * P->J == 0) {      // no lanes: nothing to read or write
+        P->path = ES_PATH_EMPTY;
+        return ES_OK;
+    }
+    if (initial == nullptr || out == nullptr || seqs[0] == nullptr || seqs[1] == nullptr)
+        return fail(ES_E_ARG, "es_scan_f32: null data pointer");
+    const void* ptrs[4] = {initial, seqs[0], seqs[1], out};
+    for (int k = 0; k < 4; ++k)
+        if (reinterpret_cast<uintptr_t>(ptrs[k]) % 4 != 0)
+            return fail(ES_E_ARG, "es_scan_f32: pointer %d is not 4-byte aligned", k);
+    // the result is a new value: `out` may not overlap any input
+    const uintptr_t olo = reinterpret_cast<uintptr_t>(out), ohi = olo + static_cast<uintptr_t>(P->n_out) * 4;
+    const int64_t nin[3] = {P->n_init, P->n_seq[0], P->n_seq[1]};
+    const char* nm[3] = {"initial", kSeqName[body][0], kSeqName[body][1]};
+    for (int k = 0; k < 3; ++k) {
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(ptrs[k]), hi = lo + static_cast<uintptr_t>(nin[k]) * 4;
+        if (lo < ohi && olo < hi) return fail(ES_E_ARG, "es_scan_f32: `out` overlaps `%s`", nm[k]);
+    }
+
+    const bool vec_ok = es::vec_tma_ok(body, O, T, P->J, W, P->sw, ptrs);
+    const bool time_ok = es::time_tma_ok(body, O, T, P->J, W, P->sw, ptrs);
+    const bool lane_ok = es::lane_tma_ok(body, O, T, P->J, W, P->sw, ptrs);
+    const int forced = g_path_override.load();
+    if (forced == ES_PATH_AUTO) {
+        P->path = vec_ok ? ES_PATH_VEC_TMA : time_ok ? ES_PATH_TIME_TMA : lane_ok ? ES_PATH_LANE_TMA : ES_PATH_GENERIC;
+        return ES_OK;
+    }
+    const bool ok = forced == ES_PATH_GENERIC || (forced == ES_PATH_VEC_TMA && vec_ok) ||
+                    (forced == ES_PATH_TIME_TMA && time_ok) || (forced == ES_PATH_LANE_TMA && lane_ok);
+    if (!ok) return fail(ES_E_UNSUPPORTED, "es_scan_f32: the forced kernel path %d cannot serve this call", forced);
+    P->path = forced;
+    return ES_OK;
+}
+
+es_status device_state(int* dev_out, DeviceState** st_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(ES_E_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(ES_E_UNSUPPORTED, "device ordinal %d too large", dev);
+    DeviceState& st = g_dev[dev];
+    std::call_once(st.once, [&]() {
+        void* p = nullptr;
+        st.err = cudaGetSymbolAddress(&p, g_es_device_status);
+        if (st.err == cudaSuccess) st.status = static_cast<unsigned int*>(p);
+        if (st.err == cudaSuccess) st.err = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    });
+    if (st.err != cudaSuccess) return fail(ES_E_CUDA, "device set-up: %s", cudaGetErrorString(st.err));
+    *dev_out = dev;
+    *st_out = &st;
+    return ES_OK;
+}
+
+es_status encoder(es::EncodeTiledFn* fn) {
+    std::call_once(g_encode_once, []() {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<es::EncodeTiledFn>(p);
+    });
+    if (g_encode == nullptr) return fail(ES_E_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    *fn = g_encode;
+    return ES_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+es_status es_plan_f32(es_body body, const float* initial, const float* const* seqs, int n_seqs,
+                      const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
+                      int reverse, const float* out, es_plan_info* info) {
+    Plan P{};
+    es_status st = plan_impl(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths, out, &P);
+    if (st != ES_OK) return st;
+    if (info != nullptr) {
+        info->O = P.O;
+        info->T = P.T;
+        info->J = P.J;
+        info->W = P.W;
+        info->seq_width[0] = P.sw[0];
+        info->seq_width[1] = P.sw[1];
+        info->elements = P.n_out;
+        info->path = P.path;
+        info->reverse = reverse ? 1 : 0;
+    }
+    return ES_OK;
+}
+
+es_status es_scan_f32(es_body body, const float* initial, const float* const* seqs, int n_seqs,
+                      const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
+                      int reverse, float* out, es_stream_t stream) {
+    Plan P{};
+    es_status st = plan_impl(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths, out, &P);
+    if (st != ES_OK) return st;
+    if (P.path == ES_PATH_EMPTY) return ES_OK;
+
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&dev, &ds)) != ES_OK) return st;
+
+    es::Launch L{};
+    L.body = static_cast<int>(body);
+    L.init = initial;
+    L.x = seqs[0];
+    L.a = seqs[1];
+    L.out = out;
+    L.O = P.O;
+    L.T = P.T;
+    L.J = P.J;
+    L.W = P.W;
+    L.sw[0] = P.sw[0];
+    L.sw[1] = P.sw[1];
+    L.reverse = reverse ? 1 : 0;
+    L.status = ds->status;
+    L.wait_ns = g_wait_ns.load();
+    L.drop_tile = g_drop_tile.load();
+    L.stream = reinterpret_cast<cudaStream_t>(stream);
+    L.num_sms = ds->num_sms;
+    L.device = dev;
+
+    const char* msg = nullptr;
+    cudaError_t e;
+    if (P.path == ES_PATH_GENERIC) {
+        e = es::launch_generic(L);
+    } else {
+        if ((st = encoder(&L.encode)) != ES_OK) return st;
+        if (P.path == ES_PATH_LANE_TMA) e = es::launch_lane_tma(L, &msg);
+        else if (P.path == ES_PATH_TIME_TMA) e = es::launch_time_tma(L, &msg);
+        else e = es::launch_vec_tma(L, &msg);
+    }
+    if (e != cudaSuccess) {
+        if (msg != nullptr) return fail(ES_E_CUDA, "es_scan_f32: %s", msg);
+        return fail(ES_E_CUDA, "es_scan_f32: kernel launch: %s", cudaGetErrorString(e));
+    }
+    g_launches.fetch_add(1);
+    return ES_OK;
+}
+
+es_status es_device_status(es_stream_t stream) {
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    es_status st = device_state(&dev, &ds);
+    if (st != ES_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(ES_E_CUDA, "es_device_status: %s", cudaGetErrorString(e));
+    unsigned int word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_es_device_status, sizeof(word));
+    if (e == cudaSuccess && word != 0) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_es_device_status, &zero, sizeof(zero));
+    }
+    if (e != cudaSuccess) return fail(ES_E_CUDA, "es_device_status: %s", cudaGetErrorString(e));
+    if (word & ES_DEVICE_TIMEOUT)
+        return fail(ES_E_TIMEOUT, "es_device_status: a kernel gave up a bounded wait; its output is incomplete");
+    return ES_OK;
+}
+
+const char* es_last_error(void) { return t_error.c_str(); }
+
+const char* es_status_string(es_status status) {
+    switch (status) {
+        case ES_OK: return "ES_OK";
+        case ES_E_DIM_001: return "ES_E_DIM_001";
+        case ES_E_DIM_002: return "ES_E_DIM_002";
+        case ES_E_ARG: return "ES_E_ARG";
+        case ES_E_UNSUPPORTED: return "ES_E_UNSUPPORTED";
+        case ES_E_CUDA: return "ES_E_CUDA";
+        case ES_E_TIMEOUT: return "ES_E_TIMEOUT";
+    }
+    return "ES_UNKNOWN_STATUS";
+}
+
+uint64_t es_launch_count(void) { return g_launches.load(); }
+
+es_status es_set_path_override(int path) {
+    if (path != ES_PATH_AUTO && path != ES_PATH_GENERIC && path != ES_PATH_LANE_TMA && path != ES_PATH_TIME_TMA &&
+        path != ES_PATH_VEC_TMA)
+        return fail(ES_E_ARG, "es_set_path_override: unknown path %d", path);
+    g_path_override.store(path);
+    return ES_OK;
+}
+
+es_status es_set_wait_limit_ns(uint64_t ns) {
+    if (ns == 0) return fail(ES_E_ARG, "es_set_wait_limit_ns: the limit must be positive");
+    g_wait_ns.store(ns);
+    return ES_OK;
+}
+
+es_status es_set_drop_tile(int64_t k) {
+    g_drop_tile.store(k < 0 ? -1 : k);
+    return ES_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// es_internal.h -- declarations shared by the host dispatcher (es_api.cu) and
+// the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define ES_BODY_TANH_DECAY 0
+#define ES_BODY_NORMCAP 1
+#define ES_BODY_MAXPLUS 2
+
+// bits of the per-device status word
+#define ES_DEVICE_TIMEOUT 1u
+
+namespace es {
+
+// cuTensorMapEncodeTiled, fetched from the driver at run time
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// One validated call in canonical form: output [O, T, J, W] and sequence k
+// as [O, T, J, sw[k]] (sw[k] == 1 broadcasts over the state).
+struct Launch {
+    int body;
+    const float* init;
+    const float* x;
+    const float* a;
+    float* out;
+    int64_t O, T, J, W;
+    int64_t sw[2];
+    int reverse;
+    unsigned int* status;   // device status word
+    uint64_t wait_ns;       // bounded-wait limit
+    int64_t drop_tile;      // testing hook: producers skip this tile (-1: off)
+    cudaStream_t stream;
+    int num_sms;
+    int device;
+    EncodeTiledFn encode;
+};
+
+// Each launcher enqueues exactly one kernel; it returns cudaSuccess or the
+// launch error.  `err` receives a message for non-CUDA failures (tensor-map
+// encoding).
+cudaError_t launch_generic(const Launch& L);
+cudaError_t launch_lane_tma(const Launch& L, const char** err);
+cudaError_t launch_time_tma(const Launch& L, const char** err);
+cudaError_t launch_vec_tma(const Launch& L, const char** err);
+
+// eligibility of the TMA paths (pure host logic, also used by planning)
+bool lane_tma_ok(int body, int64_t O, int64_t T, int64_t J, int64_t W, const int64_t sw[2],
+                 const void* const ptrs[4]);
+bool time_tma_ok(int body, int64_t O, int64_t T, int64_t J, int64_t W, const int64_t sw[2],
+                 const void* const ptrs[4]);
+bool vec_tma_ok(int body, int64_t O, int64_t T, int64_t J, int64_t W, const int64_t sw[2],
+                const void* const ptrs[4]);
+
+}  // namespace es

@@ -1,0 +1,215 @@
+// k_lane_tma.cu -- element scan with the lanes innermost (ES_PATH_LANE_TMA).
+//
+// Canonical view [O, T, I] with I = J*W contiguous lanes per trip row
+// ("Nonlinear element scans": every lane is an independent recurrence; lanes
+// run in parallel and trips in sequence).  One CTA owns a tile of LI adjacent
+// lanes of one o and walks all T trips:
+//   * warp 0, lane 0 is the producer: it streams time tiles of TT trips of
+//     both sequences (box {LI, TT, 1} of a 3-D tensor map) into an S-stage
+//     SMEM ring with TMA, each stage guarded by a full / empty mbarrier pair;
+//   * LI consumer threads (one per lane) keep the state in a register, run
+//     the serial body over each tile row by row (conflict-free SMEM reads,
+//     one coalesced 4*LI-byte store per trip and warp), then release the stage.
+// Reverse scans walk the tiles from last to first and each tile bottom-up, so
+// no flipped copy is ever made (reverse paragraph of the page).  A ragged
+// last tile is zero-filled by TMA and only its valid rows are used.  Every
+// wait is bounded: on give-up the CTA records ES_DEVICE_TIMEOUT, the producer
+// waits (bounded) for its copies in flight, and all threads return.
+#include <algorithm>
+
+#include "es_device.cuh"
+
+namespace es {
+namespace {
+
+constexpr int kTT = 16;          // trips per time tile
+constexpr int kMaxStages = 8;
+
+template <int BODY, int LI>
+__global__ void __launch_bounds__(32 + LI)
+k_lane_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_a,
+           const float* __restrict__ init, float* __restrict__ out, int T, int I, int tiles_i,
+           int stages, int reverse, unsigned int* status, uint64_t wait_ns, int64_t drop_tile) {
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+    __shared__ int abort_flag;
+
+    float* tiles = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr int kTileFloats = kTT * LI;           // one sequence, one stage
+    constexpr uint32_t kStageBytes = 2u * kTileFloats * 4u;
+
+    const int o = blockIdx.x / tiles_i;
+    const int i0 = (blockIdx.x % tiles_i) * LI;
+    const int ntiles = (T + kTT - 1) / kTT;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], LI / 32);
+        }
+        abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&map_x);
+            tma_prefetch_desc(&map_a);
+            const uint64_t pol = l2_policy_evict_first();
+            int issued = 0;
+            for (int k = 0; k < ntiles; ++k) {
+                const int s = k % stages;
+                const int round = k / stages;
+                if (round > 0 && !mbar_wait_bounded(&empty_bar[s], (round - 1) & 1, wait_ns, &abort_flag)) {
+                    report_timeout(status, &abort_flag);
+                    break;
+                }
+                issued = k + 1;
+                if (k == drop_tile) continue;   // testing hook: this tile never arrives
+                const int j = reverse ? ntiles - 1 - k : k;
+                float* xs = tiles + s * 2 * kTileFloats;
+                mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
+                tma_load_3d(xs, &map_x, i0, j * kTT, o, &full_bar[s], pol);
+                tma_load_3d(xs + kTileFloats, &map_a, i0, j * kTT, o, &full_bar[s], pol);
+            }
+            // no copy may still target SMEM when the CTA exits
+            volatile int never = 0;
+            for (int k = max(0, issued - stages); k < issued; ++k) {
+                if (k == drop_tile) continue;
+                if (!mbar_wait_bounded(&full_bar[k % stages], (k / stages) & 1, wait_ns, &never))
+                    atomicOr(status, ES_DEVICE_TIMEOUT);
+            }
+        }
+        return;
+    }
+
+    // consumers: one lane each
+    const int c = threadIdx.x - 32;
+    const int i = i0 + c;
+    const bool valid = i < I;
+    float h = valid ? init[static_cast<int64_t>(o) * I + i] : 0.0f;
+    float* obase = out + static_cast<int64_t>(o) * T * I + i;
+
+    for (int k = 0; k < ntiles; ++k) {
+        const int s = k % stages;
+        const bool ok = mbar_wait_bounded(&full_bar[s], (k / stages) & 1, wait_ns, &abort_flag);
+        // the whole warp leaves together, so __syncwarp never misses a lane
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (!ok) report_timeout(status, &abort_flag);
+            break;
+        }
+        const int j = reverse ? ntiles - 1 - k : k;
+        const int t0 = j * kTT;
+        const int n = min(kTT, T - t0);
+        const float* xs = tiles + s * 2 * kTileFloats + c;
+        const float* as = xs + kTileFloats;
+        float* op = obase + static_cast<int64_t>(t0) * I;
+        if (n == kTT) {
+            if (!reverse) {
+#pragma unroll
+                for (int tt = 0; tt < kTT; ++tt) {
+                    h = step_pointwise<BODY>(h, xs[tt * LI], as[tt * LI]);
+                    if (valid) __stcs(op + static_cast<int64_t>(tt) * I, h);
+                }
+            } else {
+#pragma unroll
+                for (int tt = kTT - 1; tt >= 0; --tt) {
+                    h = step_pointwise<BODY>(h, xs[tt * LI], as[tt * LI]);
+                    if (valid) __stcs(op + static_cast<int64_t>(tt) * I, h);
+                }
+            }
+        } else {
+            for (int q = 0; q < n; ++q) {
+                const int tt = reverse ? n - 1 - q : q;
+                h = step_pointwise<BODY>(h, xs[tt * LI], as[tt * LI]);
+                if (valid) __stcs(op + static_cast<int64_t>(tt) * I, h);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+    }
+}
+
+template <int BODY, int LI>
+cudaError_t launch_li(const Launch& L, const CUtensorMap& mx, const CUtensorMap& ma, int I, int tiles_i,
+                      int stages) {
+    const size_t smem = static_cast<size_t>(stages) * 2 * kTT * LI * 4 + 1024;
+    auto kern = k_lane_tma<BODY, LI>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int64_t grid = L.O * tiles_i;
+    kern<<<static_cast<unsigned>(grid), 32 + LI, smem, L.stream>>>(
+        mx, ma, L.init, L.out, static_cast<int>(L.T), I, tiles_i, stages, L.reverse, L.status, L.wait_ns,
+        L.drop_tile);
+    return cudaGetLastError();
+}
+
+bool encode_rows(const Launch& L, CUtensorMap* m, const float* base, int64_t I, int LI, const char** err) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(I), static_cast<cuuint64_t>(L.T),
+                                static_cast<cuuint64_t>(L.O)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(I) * 4, static_cast<cuuint64_t>(I) * L.T * 4};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(LI), static_cast<cuuint32_t>(kTT), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = L.encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        *err = "cuTensorMapEncodeTiled failed for the lane-innermost tile map";
+        return false;
+    }
+    return true;
+}
+
+}  // namespace
+
+bool lane_tma_ok(int body, int64_t O, int64_t T, int64_t J, int64_t W, const int64_t sw[2],
+                 const void* const ptrs[4]) {
+    if (body == ES_BODY_NORMCAP) return false;
+    if (W > 1 && (sw[0] != W || sw[1] != W)) return false;   // broadcast sequences: generic path
+    const int64_t I = J * W;
+    if (I < 32 || I % 4 != 0) return false;                  // 16-byte row stride, box <= row
+    if (O >= (int64_t(1) << 31) || T >= (int64_t(1) << 31) || I >= (int64_t(1) << 31)) return false;
+    if (O * ((I + 31) / 32) >= (int64_t(1) << 31)) return false;
+    for (int k = 1; k < 4; ++k)
+        if (reinterpret_cast<uintptr_t>(ptrs[k]) % 16 != 0) return false;
+    return true;
+}
+
+cudaError_t launch_lane_tma(const Launch& L, const char** err) {
+    const int64_t I = L.J * L.W;
+    // Lanes per CTA: the widest tile that still gives at least two CTAs per
+    // SM, so every SM streams; then as many stages as fit when all CTAs are
+    // resident at once.
+    int LI = 32;
+    for (int cand : {128, 64}) {
+        if (I >= cand && L.O * ((I + cand - 1) / cand) >= 2LL * L.num_sms) {
+            LI = cand;
+            break;
+        }
+    }
+    const int64_t tiles_i = (I + LI - 1) / LI;
+    const int64_t ctas = L.O * tiles_i;
+    const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>(8, (ctas + L.num_sms - 1) / L.num_sms));
+    const int64_t budget = std::min<int64_t>(96 * 1024, (200 * 1024) / per_sm);
+    const int64_t stage_bytes = 2LL * kTT * LI * 4;
+    const int stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(kMaxStages, budget / stage_bytes)));
+
+    CUtensorMap mx, ma;
+    if (!encode_rows(L, &mx, L.x, I, LI, err) || !encode_rows(L, &ma, L.a, I, LI, err))
+        return cudaErrorInvalidValue;
+    const int Ii = static_cast<int>(I), ti = static_cast<int>(tiles_i);
+    if (L.body == ES_BODY_TANH_DECAY) {
+        if (LI == 128) return launch_li<ES_BODY_TANH_DECAY, 128>(L, mx, ma, Ii, ti, stages);
+        if (LI == 64) return launch_li<ES_BODY_TANH_DECAY, 64>(L, mx, ma, Ii, ti, stages);
+        return launch_li<ES_BODY_TANH_DECAY, 32>(L, mx, ma, Ii, ti, stages);
+    }
+    if (LI == 128) return launch_li<ES_BODY_MAXPLUS, 128>(L, mx, ma, Ii, ti, stages);
+    if (LI == 64) return launch_li<ES_BODY_MAXPLUS, 64>(L, mx, ma, Ii, ti, stages);
+    return launch_li<ES_BODY_MAXPLUS, 32>(L, mx, ma, Ii, ti, stages);
+}
+
+}  // namespace es

@@ -1,0 +1,162 @@
+/*
+ * es.h -- C ABI of libes.so, a GB300-native (sm_103a) `element-scan` library.
+ *
+ * Operation: "Nonlinear element scans" (sx.041.io/docs/element-scan.md).
+ *   intro        h[t] = f(h[t-1], seq_1[t], ..., seq_n[t]) at every position
+ *                outside one sequence axis, from h[-1] = initial; every
+ *                output position holds the state after its own trip.
+ *   :reverse     trips run from the last position to the first,
+ *                h[t] = f(h[t+1], ...) from h[T] = initial; the final state
+ *                is at position 0 (reverse paragraph of the intro).
+ *   :state-axis  each lane carries a vector of 1..16 values along the last
+ *                axis; a sequence whose last width is 1 is a per-trip value
+ *                broadcast over the whole state ("Arguments and body").
+ *   precision    the recurrence computes in f32 ("Precision and gradients").
+ * Layout: every array is dense, C-contiguous, row-major f32 ("lucid.tensor"
+ * page, contiguity paragraph).
+ *
+ * All pointers passed to es_scan_f32 except `seqs`, `shape` and `seq_widths`
+ * are DEVICE pointers owned by the caller; the library never frees or keeps
+ * them.  Calls are asynchronous on the caller's stream.  No function here
+ * throws; every failure is a status code plus a thread-local message.
+ */
+#ifndef ES_H
+#define ES_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same handle type as cudaStream_t; NULL means the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *es_stream_t;
+
+/* Bodies (element-scan page): each takes the state and two sequences.
+ *   ES_TANH_DECAY  seqs (x, a):  h = tanh(x + a*h)            intro example
+ *   ES_NORMCAP     seqs (x, a):  y = a*h + x; h = y / max(1, ||y||_2)
+ *                                over the whole state vector   :state-axis example
+ *   ES_MAXPLUS     seqs (x, c):  h = maximum(h - c, x)         :reverse example
+ * Each body operation is one f32 operation rounded to nearest, in the order
+ * written (no fused multiply-add); tanh, sqrt and division are CUDA's
+ * tanhf, correctly rounded sqrtf and correctly rounded division; `maximum`
+ * is IEEE 754-2019 maximum (+0 above -0, NaN propagates). */
+typedef enum es_body {
+    ES_TANH_DECAY = 0,
+    ES_NORMCAP = 1,
+    ES_MAXPLUS = 2
+} es_body;
+
+/* Status codes.  The E-DIM codes follow the error table of the "Tensor
+ * operations" page ("Errors"): E-DIM-001 shapes do not fit, E-DIM-002 dtypes
+ * differ. */
+typedef enum es_status {
+    ES_OK = 0,
+    ES_E_DIM_001 = 1,     /* shapes do not fit: axis, widths, T = 0, rank    */
+    ES_E_DIM_002 = 2,     /* dtype (reserved: only f32 entry points exist)   */
+    ES_E_ARG = 3,         /* null / misaligned / overlapping pointer, bad id */
+    ES_E_UNSUPPORTED = 4, /* valid on the pages but not in this library      */
+    ES_E_CUDA = 5,        /* a CUDA runtime or driver call failed            */
+    ES_E_TIMEOUT = 6      /* a kernel gave up a bounded device-side wait     */
+} es_status;
+
+#define ES_MAX_RANK 8
+#define ES_MAX_STATE 16
+
+/* Kernel paths.  es_scan_f32 picks one per call (ES_PATH_AUTO) from the
+ * canonical view [O, T, J, W] (O = product of dims before the axis, T the
+ * axis length, J lanes after it, W the state width, 1 for a scalar state). */
+typedef enum es_path {
+    ES_PATH_AUTO = 0,
+    ES_PATH_EMPTY = 1,     /* no lanes: nothing is launched                    */
+    ES_PATH_GENERIC = 2,   /* one thread per lane, direct loads, any layout    */
+    ES_PATH_LANE_TMA = 3,  /* lanes innermost: TMA/mbarrier time-tile pipeline */
+    ES_PATH_TIME_TMA = 4,  /* time innermost: TMA tiles transposed in SMEM     */
+    ES_PATH_VEC_TMA = 5    /* NORMCAP vector state: TMA pipeline + shuffles    */
+} es_path;
+
+/*
+ * es_scan_f32 -- run one element scan.
+ *
+ *   body        ES_TANH_DECAY, ES_NORMCAP or ES_MAXPLUS.
+ *   initial     device f32, the output shape with `axis` removed (its last
+ *               dim is the state width W under a state axis).
+ *   seqs        HOST array of n_seqs DEVICE pointers, in the body's argument
+ *               order after the state: (x, a) or (x, c).
+ *   n_seqs      must be 2.
+ *   shape, rank HOST array: the output shape, rank 1..ES_MAX_RANK, dims >= 0.
+ *               Without a state axis every sequence has exactly this shape.
+ *   axis        the sequence axis, -rank <= axis < rank (negative counts from
+ *               the end); shape[axis] >= 1.
+ *   state_width 0 for a scalar state; otherwise W = shape[rank-1] in 1..16
+ *               (`:state-axis -1`), and axis may not be the last axis.
+ *               ES_NORMCAP requires W >= 1 (a scalar state cannot reduce);
+ *               the pointwise bodies accept both.
+ *   seq_widths  NULL (every sequence has `shape`), or a HOST array of n_seqs
+ *               last widths, each 1 (broadcast over the state) or W.
+ *   reverse     0 forward; nonzero runs the trips from the last position.
+ *   out         device f32 of `shape`; must not overlap any input.
+ *   stream      the CUDA stream to enqueue on.
+ *
+ * Returns ES_OK once the kernel is enqueued (nothing is launched when a
+ * dimension other than the axis is 0).  Argument errors return before any
+ * CUDA call.  Pointers must be 4-byte aligned; 16-byte alignment (and row
+ * widths that are multiples of 4 floats) selects the TMA paths.  The call
+ * allocates no device memory; it keeps one small per-device status word
+ * that bounded device waits report through es_device_status().
+ */
+es_status es_scan_f32(es_body body, const float *initial, const float *const *seqs,
+                      int n_seqs, const int64_t *shape, int rank, int axis,
+                      int state_width, const int64_t *seq_widths, int reverse,
+                      float *out, es_stream_t stream);
+
+/* The plan of a call: canonical view and chosen kernel.  Pure host logic
+ * (same validation as es_scan_f32, no CUDA call), so it can be used and
+ * tested on machines without a GPU.  Pointers are only inspected for null,
+ * alignment and overlap. */
+typedef struct es_plan_info {
+    int64_t O, T, J, W;        /* canonical [O, T, J, W]                      */
+    int64_t seq_width[2];      /* each sequence's last width (1 or W)         */
+    int64_t elements;          /* O*T*J*W output values                       */
+    int path;                  /* es_path chosen                              */
+    int reverse;
+} es_plan_info;
+
+es_status es_plan_f32(es_body body, const float *initial, const float *const *seqs,
+                      int n_seqs, const int64_t *shape, int rank, int axis,
+                      int state_width, const int64_t *seq_widths, int reverse,
+                      const float *out, es_plan_info *info);
+
+/* Synchronise `stream`, then read and clear this device's status word.
+ * Returns ES_E_TIMEOUT if a kernel since the last check gave up a bounded
+ * wait (its outputs are then incomplete), ES_E_CUDA if the synchronisation
+ * failed, else ES_OK. */
+es_status es_device_status(es_stream_t stream);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char *es_last_error(void);
+
+/* Static name of a status code. */
+const char *es_status_string(es_status status);
+
+/* Kernel launches issued by this process so far (all devices). */
+uint64_t es_launch_count(void);
+
+/* Testing hooks (process-wide).
+ *   es_set_path_override: force a path for later calls (ES_PATH_AUTO undoes
+ *     it); a call the forced path cannot serve returns ES_E_UNSUPPORTED.
+ *   es_set_wait_limit_ns: limit of every bounded device wait (default 2 s).
+ *   es_set_drop_tile: the TMA producers skip the load of pipeline tile k
+ *     (-1: off), so the consumers' bounded wait runs out; used to test the
+ *     timeout path without faulting or hanging the GPU. */
+es_status es_set_path_override(int path);
+es_status es_set_wait_limit_ns(uint64_t ns);
+es_status es_set_drop_tile(int64_t k);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ES_H */
