@@ -430,11 +430,18 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--trips", type=int, default=0,
+                    help="profiling aid: shorten the sequence axis to this many trips (same lanes, same kernel "
+                         "launch shape); lines printed with it are not the workload's bench numbers")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
     from element_scan_recurrences_gb300 import workloads as wl
     w = wl.WORKLOADS[args.workload]
+    if args.trips:
+        shape = list(w.shape)
+        shape[w.ax] = args.trips
+        w = w.with_shape(shape, name="%s_T%d" % (w.name, args.trips))
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -91,6 +91,12 @@ def _body_id(body) -> int:
     return int(body)
 
 
+def _c_array(a, dtype):
+    """A C-contiguous array of `dtype` that keeps the rank (0-d stays 0-d)."""
+    a = np.asarray(a, dtype=dtype)
+    return a if a.flags.c_contiguous else a.copy(order="C")
+
+
 def scan(body, initial, seqs, axis: int = 0, state_axis: bool = False,
          reverse: bool = False, dtype=np.float32, _lib=None) -> np.ndarray:
     """Run the oracle on host arrays and return the states after every trip.
@@ -103,8 +109,8 @@ def scan(body, initial, seqs, axis: int = 0, state_axis: bool = False,
     lib = _lib if _lib is not None else _load()
     ft = ctypes.c_float if dtype == np.float32 else ctypes.c_double
     fn = lib.es_oracle_f32 if dtype == np.float32 else lib.es_oracle_f64
-    seqs = [np.ascontiguousarray(np.asarray(s, dtype=dtype)) for s in seqs]
-    initial = np.ascontiguousarray(np.asarray(initial, dtype=dtype))
+    seqs = [_c_array(s, dtype) for s in seqs]
+    initial = _c_array(initial, dtype)
     if len(seqs) != 2:
         raise ValueError("every body takes exactly two sequences")
     # output shape: the first sequence's shape; under a state axis its last
