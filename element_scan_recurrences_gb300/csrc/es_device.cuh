@@ -18,13 +18,21 @@ namespace es {
 // body is written; the _rn intrinsics keep the compiler from contracting a
 // multiply and an add into one fused operation.
 
-// IEEE 754-2019 maximum: the larger value, +0 above -0, NaN propagates.
+// IEEE 754-2019 maximum: the larger value, +0 above -0, NaN if either
+// operand is NaN.  PTX `max.NaN.f32` has exactly these semantics (the PTX ISA
+// orders +0.0 above -0.0 for max and returns the canonical NaN when an input
+// is NaN) in one instruction on the serial chain.
 __device__ __forceinline__ float ieee_maximum(float a, float b) {
-    if (a != a) return a;
-    if (b != b) return b;
-    if (a > b) return a;
-    if (b > a) return b;
-    return (__float_as_uint(a) & 0x80000000u) ? b : a;
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// IEEE 754-2019 minimum, the mirror of ieee_maximum (-0 below +0, NaN wins).
+__device__ __forceinline__ float ieee_minimum(float a, float b) {
+    float r;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
 }
 
 // h = tanh(x + a*h)
@@ -100,10 +108,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 31u) == 0u) {
-            if (*abort_flag) return false;
+            if (abort_flag != nullptr && *abort_flag) return false;
             if (global_timer_ns() - t0 > limit_ns) return false;
         }
     }
+}
+
+// Byte offset that moves the dynamic SMEM base up to a 1024-byte boundary
+// (tile bases must be 1024-byte aligned for the 128-byte swizzle).  Adding it
+// to the `extern __shared__` array keeps pointers in the shared space, so
+// the compiler emits shared loads and knows they cannot alias global stores.
+__device__ __forceinline__ uint32_t smem_align_pad(const void* base) {
+    return (1024u - (smem_u32(base) & 1023u)) & 1023u;
 }
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

@@ -7,9 +7,12 @@
 //   * warp 0, lane 0 is the producer: it streams time tiles of TT trips of
 //     both sequences (box {LI, TT, 1} of a 3-D tensor map) into an S-stage
 //     SMEM ring with TMA, each stage guarded by a full / empty mbarrier pair;
-//   * LI consumer threads (one per lane) keep the state in a register, run
-//     the serial body over each tile row by row (conflict-free SMEM reads,
-//     one coalesced 4*LI-byte store per trip and warp), then release the stage.
+//   * LI consumer threads (one per lane) copy a whole tile into registers
+//     (conflict-free SMEM reads), hand the stage back to the producer at
+//     once, then run the serial body over the tile with the state in a
+//     register, one coalesced 4*LI-byte store per trip and warp.
+// Handing the stage back before the serial chain runs keeps all S stages in
+// flight while the warp computes, so HBM latency hides behind the chain.
 // Reverse scans walk the tiles from last to first and each tile bottom-up, so
 // no flipped copy is ever made (reverse paragraph of the page).  A ragged
 // last tile is zero-filled by TMA and only its valid rows are used.  Every
@@ -19,13 +22,23 @@
 
 #include "es_device.cuh"
 
+// Tuning overrides (0: chosen per shape in launch_lane_tma).
+#ifndef ES_LANE_TT
+#define ES_LANE_TT 0        // trips per tile: 16 or 32
+#endif
+#ifndef ES_LANE_LI
+#define ES_LANE_LI 0        // lanes per CTA: 32, 64 or 128
+#endif
+#ifndef ES_LANE_STAGES
+#define ES_LANE_STAGES 0    // pipeline depth
+#endif
+
 namespace es {
 namespace {
 
-constexpr int kTT = 16;          // trips per time tile
 constexpr int kMaxStages = 8;
 
-template <int BODY, int LI>
+template <int BODY, int LI, int TT>
 __global__ void __launch_bounds__(32 + LI)
 k_lane_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_a,
            const float* __restrict__ init, float* __restrict__ out, int T, int I, int tiles_i,
@@ -35,13 +48,13 @@ k_lane_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
     __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
     __shared__ int abort_flag;
 
-    float* tiles = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr int kTileFloats = kTT * LI;           // one sequence, one stage
+    float* tiles = reinterpret_cast<float*>(smem_raw + smem_align_pad(smem_raw));
+    constexpr int kTileFloats = TT * LI;            // one sequence, one stage
     constexpr uint32_t kStageBytes = 2u * kTileFloats * 4u;
 
     const int o = blockIdx.x / tiles_i;
     const int i0 = (blockIdx.x % tiles_i) * LI;
-    const int ntiles = (T + kTT - 1) / kTT;
+    const int ntiles = (T + TT - 1) / TT;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -73,14 +86,13 @@ k_lane_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
                 const int j = reverse ? ntiles - 1 - k : k;
                 float* xs = tiles + s * 2 * kTileFloats;
                 mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
-                tma_load_3d(xs, &map_x, i0, j * kTT, o, &full_bar[s], pol);
-                tma_load_3d(xs + kTileFloats, &map_a, i0, j * kTT, o, &full_bar[s], pol);
+                tma_load_3d(xs, &map_x, i0, j * TT, o, &full_bar[s], pol);
+                tma_load_3d(xs + kTileFloats, &map_a, i0, j * TT, o, &full_bar[s], pol);
             }
             // no copy may still target SMEM when the CTA exits
-            volatile int never = 0;
             for (int k = max(0, issued - stages); k < issued; ++k) {
                 if (k == drop_tile) continue;
-                if (!mbar_wait_bounded(&full_bar[k % stages], (k / stages) & 1, wait_ns, &never))
+                if (!mbar_wait_bounded(&full_bar[k % stages], (k / stages) & 1, wait_ns, nullptr))
                     atomicOr(status, ES_DEVICE_TIMEOUT);
             }
         }
@@ -103,42 +115,48 @@ k_lane_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
             break;
         }
         const int j = reverse ? ntiles - 1 - k : k;
-        const int t0 = j * kTT;
-        const int n = min(kTT, T - t0);
+        const int t0 = j * TT;
+        const int n = min(TT, T - t0);          // < TT only for the last time tile
         const float* xs = tiles + s * 2 * kTileFloats + c;
         const float* as = xs + kTileFloats;
+        // the whole tile goes to registers first: the loads overlap each other
+        // and the serial chain below only waits on arithmetic
+        float xr[TT], ar[TT];
+#pragma unroll
+        for (int tt = 0; tt < TT; ++tt) {
+            xr[tt] = xs[tt * LI];
+            ar[tt] = as[tt * LI];
+        }
+        // the stage is free as soon as the tile sits in registers, so the
+        // producer refills it while this warp runs the chain
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
         float* op = obase + static_cast<int64_t>(t0) * I;
-        if (n == kTT) {
-            if (!reverse) {
+        if (!reverse) {
 #pragma unroll
-                for (int tt = 0; tt < kTT; ++tt) {
-                    h = step_pointwise<BODY>(h, xs[tt * LI], as[tt * LI]);
-                    if (valid) __stcs(op + static_cast<int64_t>(tt) * I, h);
-                }
-            } else {
-#pragma unroll
-                for (int tt = kTT - 1; tt >= 0; --tt) {
-                    h = step_pointwise<BODY>(h, xs[tt * LI], as[tt * LI]);
+            for (int tt = 0; tt < TT; ++tt) {
+                if (tt < n) {
+                    h = step_pointwise<BODY>(h, xr[tt], ar[tt]);
                     if (valid) __stcs(op + static_cast<int64_t>(tt) * I, h);
                 }
             }
         } else {
-            for (int q = 0; q < n; ++q) {
-                const int tt = reverse ? n - 1 - q : q;
-                h = step_pointwise<BODY>(h, xs[tt * LI], as[tt * LI]);
-                if (valid) __stcs(op + static_cast<int64_t>(tt) * I, h);
+#pragma unroll
+            for (int tt = TT - 1; tt >= 0; --tt) {
+                if (tt < n) {
+                    h = step_pointwise<BODY>(h, xr[tt], ar[tt]);
+                    if (valid) __stcs(op + static_cast<int64_t>(tt) * I, h);
+                }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
 }
 
-template <int BODY, int LI>
-cudaError_t launch_li(const Launch& L, const CUtensorMap& mx, const CUtensorMap& ma, int I, int tiles_i,
-                      int stages) {
-    const size_t smem = static_cast<size_t>(stages) * 2 * kTT * LI * 4 + 1024;
-    auto kern = k_lane_tma<BODY, LI>;
+template <int BODY, int LI, int TT>
+cudaError_t launch_cfg(const Launch& L, const CUtensorMap& mx, const CUtensorMap& ma, int I, int tiles_i,
+                       int stages) {
+    const size_t smem = static_cast<size_t>(stages) * 2 * TT * LI * 4 + 1024;
+    auto kern = k_lane_tma<BODY, LI, TT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int64_t grid = L.O * tiles_i;
@@ -148,11 +166,26 @@ cudaError_t launch_li(const Launch& L, const CUtensorMap& mx, const CUtensorMap&
     return cudaGetLastError();
 }
 
-bool encode_rows(const Launch& L, CUtensorMap* m, const float* base, int64_t I, int LI, const char** err) {
+template <int BODY, int TT>
+cudaError_t launch_tt(const Launch& L, const CUtensorMap& mx, const CUtensorMap& ma, int I, int tiles_i,
+                      int stages, int LI) {
+    if (LI == 128) return launch_cfg<BODY, 128, TT>(L, mx, ma, I, tiles_i, stages);
+    if (LI == 64) return launch_cfg<BODY, 64, TT>(L, mx, ma, I, tiles_i, stages);
+    return launch_cfg<BODY, 32, TT>(L, mx, ma, I, tiles_i, stages);
+}
+
+template <int BODY>
+cudaError_t launch_body(const Launch& L, const CUtensorMap& mx, const CUtensorMap& ma, int I, int tiles_i,
+                        int stages, int LI, int TT) {
+    if (TT == 32) return launch_tt<BODY, 32>(L, mx, ma, I, tiles_i, stages, LI);
+    return launch_tt<BODY, 16>(L, mx, ma, I, tiles_i, stages, LI);
+}
+
+bool encode_rows(const Launch& L, CUtensorMap* m, const float* base, int64_t I, int LI, int TT, const char** err) {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(I), static_cast<cuuint64_t>(L.T),
                                 static_cast<cuuint64_t>(L.O)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(I) * 4, static_cast<cuuint64_t>(I) * L.T * 4};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(LI), static_cast<cuuint32_t>(kTT), 1};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(LI), static_cast<cuuint32_t>(TT), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = L.encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -181,35 +214,35 @@ bool lane_tma_ok(int body, int64_t O, int64_t T, int64_t J, int64_t W, const int
 
 cudaError_t launch_lane_tma(const Launch& L, const char** err) {
     const int64_t I = L.J * L.W;
-    // Lanes per CTA: the widest tile that still gives at least two CTAs per
-    // SM, so every SM streams; then as many stages as fit when all CTAs are
-    // resident at once.
+    // Lanes per CTA: the widest tile (longest contiguous row segment per TMA
+    // box row, the friendliest pattern for HBM) that still puts a CTA on most
+    // SMs.
     int LI = 32;
     for (int cand : {128, 64}) {
-        if (I >= cand && L.O * ((I + cand - 1) / cand) >= 2LL * L.num_sms) {
+        if (I >= cand && 5 * L.O * ((I + cand - 1) / cand) >= 4LL * L.num_sms) {
             LI = cand;
             break;
         }
     }
+    if (ES_LANE_LI != 0 && I >= ES_LANE_LI) LI = ES_LANE_LI;
     const int64_t tiles_i = (I + LI - 1) / LI;
     const int64_t ctas = L.O * tiles_i;
+    // SMEM per CTA when every CTA is resident at once; 32-trip tiles when at
+    // least four of them fit, else 16-trip tiles.
     const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>(8, (ctas + L.num_sms - 1) / L.num_sms));
-    const int64_t budget = std::min<int64_t>(96 * 1024, (200 * 1024) / per_sm);
-    const int64_t stage_bytes = 2LL * kTT * LI * 4;
-    const int stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(kMaxStages, budget / stage_bytes)));
+    const int64_t budget = (200 * 1024) / per_sm;
+    int TT = (budget / (2LL * 32 * LI * 4) >= 4) ? 32 : 16;
+    if (ES_LANE_TT != 0) TT = ES_LANE_TT;
+    const int64_t stage_bytes = 2LL * TT * LI * 4;
+    int stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(kMaxStages, budget / stage_bytes)));
+    if (ES_LANE_STAGES != 0) stages = ES_LANE_STAGES;
 
     CUtensorMap mx, ma;
-    if (!encode_rows(L, &mx, L.x, I, LI, err) || !encode_rows(L, &ma, L.a, I, LI, err))
+    if (!encode_rows(L, &mx, L.x, I, LI, TT, err) || !encode_rows(L, &ma, L.a, I, LI, TT, err))
         return cudaErrorInvalidValue;
     const int Ii = static_cast<int>(I), ti = static_cast<int>(tiles_i);
-    if (L.body == ES_BODY_TANH_DECAY) {
-        if (LI == 128) return launch_li<ES_BODY_TANH_DECAY, 128>(L, mx, ma, Ii, ti, stages);
-        if (LI == 64) return launch_li<ES_BODY_TANH_DECAY, 64>(L, mx, ma, Ii, ti, stages);
-        return launch_li<ES_BODY_TANH_DECAY, 32>(L, mx, ma, Ii, ti, stages);
-    }
-    if (LI == 128) return launch_li<ES_BODY_MAXPLUS, 128>(L, mx, ma, Ii, ti, stages);
-    if (LI == 64) return launch_li<ES_BODY_MAXPLUS, 64>(L, mx, ma, Ii, ti, stages);
-    return launch_li<ES_BODY_MAXPLUS, 32>(L, mx, ma, Ii, ti, stages);
+    if (L.body == ES_BODY_TANH_DECAY) return launch_body<ES_BODY_TANH_DECAY>(L, mx, ma, Ii, ti, stages, LI, TT);
+    return launch_body<ES_BODY_MAXPLUS>(L, mx, ma, Ii, ti, stages, LI, TT);
 }
 
 }  // namespace es

@@ -7,12 +7,14 @@
 // per row) in SMEM through an S-stage TMA/mbarrier ring, with the 128-byte
 // swizzle so that a thread reading its own row four trips at a time (one
 // 16-byte vector) is conflict-free across the warp.  Each consumer thread owns
-// one row: it runs the serial body over the 32 trips of its segment, writes
-// the states into a swizzled output tile, and one thread stores the tile back
-// with a TMA tensor store (three output buffers, so the stores overlap the
-// next tiles).  Reverse scans take the tiles last-first and the four values of
-// every vector in descending order.  Waits are bounded as in the other
-// pipelines.
+// one row: it copies its 32-trip segment of both sequences into registers,
+// hands the input stage back to the producer at once (so every stage stays
+// in flight while the chain runs), runs the serial body over the segment,
+// and writes the states into a swizzled output tile; one thread stores the
+// tile back with a TMA tensor store (three output buffers, so the stores
+// overlap the next tiles).  Reverse scans take the tiles last-first and the
+// four values of every vector in descending order.  Waits are bounded as in
+// the other pipelines.
 #include <algorithm>
 
 #include "es_device.cuh"
@@ -51,8 +53,7 @@ k_time_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
 
     // every tile is LO rows x 128 bytes and starts on a 1024-byte boundary
     constexpr uint32_t kTileBytes = LO * 128u;
-    unsigned char* base = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* base = smem_raw + smem_align_pad(smem_raw);
     unsigned char* in_tiles = base;                                   // [stages][2][LO][128 B]
     unsigned char* out_tiles = base + static_cast<size_t>(stages) * 2 * kTileBytes;  // [3][LO][128 B]
 
@@ -92,10 +93,9 @@ k_time_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
                 tma_load_2d(xs, &map_x, j * kTT, o0, &full_bar[s], pol);
                 tma_load_2d(xs + kTileBytes, &map_a, j * kTT, o0, &full_bar[s], pol);
             }
-            volatile int never = 0;
             for (int k = max(0, issued - stages); k < issued; ++k) {
                 if (k == drop_tile) continue;
-                if (!mbar_wait_bounded(&full_bar[k % stages], (k / stages) & 1, wait_ns, &never))
+                if (!mbar_wait_bounded(&full_bar[k % stages], (k / stages) & 1, wait_ns, nullptr))
                     atomicOr(status, ES_DEVICE_TIMEOUT);
             }
         }
@@ -136,30 +136,36 @@ k_time_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
         const unsigned char* xrow = in_tiles + static_cast<size_t>(s) * 2 * kTileBytes + row_off;
         const unsigned char* arow = xrow + kTileBytes;
         unsigned char* orow = out_tiles + static_cast<size_t>(k % kOutBufs) * kTileBytes + row_off;
-        if (nq == kTT / 4) {
+        // the row's whole segment goes to registers first, then the serial chain
+        float4 xv[kTT / 4], av[kTT / 4];
 #pragma unroll
-            for (int qq = 0; qq < kTT / 4; ++qq) {
-                const uint32_t q = reverse ? (kTT / 4 - 1 - qq) : qq;
-                const uint32_t off = ((q ^ sw) << 4);
-                const float4 xv = *reinterpret_cast<const float4*>(xrow + off);
-                const float4 av = *reinterpret_cast<const float4*>(arow + off);
-                float4 ov;
-                run_vec<BODY>(h, xv, av, ov, reverse);
-                *reinterpret_cast<float4*>(orow + off) = ov;
-            }
-        } else {
-            for (int qq = 0; qq < nq; ++qq) {
-                const uint32_t q = reverse ? (nq - 1 - qq) : qq;
-                const uint32_t off = ((q ^ sw) << 4);
-                const float4 xv = *reinterpret_cast<const float4*>(xrow + off);
-                const float4 av = *reinterpret_cast<const float4*>(arow + off);
-                float4 ov;
-                run_vec<BODY>(h, xv, av, ov, reverse);
-                *reinterpret_cast<float4*>(orow + off) = ov;
-            }
+        for (int q = 0; q < kTT / 4; ++q) {
+            const uint32_t off = ((static_cast<uint32_t>(q) ^ sw) << 4);
+            xv[q] = *reinterpret_cast<const float4*>(xrow + off);
+            av[q] = *reinterpret_cast<const float4*>(arow + off);
         }
+        // the input stage is free as soon as the segment sits in registers
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
+        if (!reverse) {
+#pragma unroll
+            for (int q = 0; q < kTT / 4; ++q) {
+                if (q < nq) {
+                    float4 ov;
+                    run_vec<BODY>(h, xv[q], av[q], ov, false);
+                    *reinterpret_cast<float4*>(orow + ((static_cast<uint32_t>(q) ^ sw) << 4)) = ov;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int q = kTT / 4 - 1; q >= 0; --q) {
+                if (q < nq) {
+                    float4 ov;
+                    run_vec<BODY>(h, xv[q], av[q], ov, true);
+                    *reinterpret_cast<float4*>(orow + ((static_cast<uint32_t>(q) ^ sw) << 4)) = ov;
+                }
+            }
+        }
     }
     if (storer) bulk_wait_all();
 }

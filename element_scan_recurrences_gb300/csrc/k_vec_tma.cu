@@ -9,41 +9,122 @@
 // CTA owns LV = 128 / W adjacent lanes of one o (128 contiguous values per
 // trip) and walks all T trips.  Warp 0's lane 0 streams time tiles of TT
 // trips of x and of the gate into an S-stage SMEM ring with TMA (full/empty
-// mbarrier pairs); each of the 128 consumer threads holds one state value.
-// The norm is a butterfly of W/2 .. 1 xor-shuffles inside each W-thread group
-// (every thread of a group ends with the same bitwise sum, because each level
-// adds the same two operands), then a correctly rounded sqrt, the floor at
-// one, and a correctly rounded division.  Stores are one coalesced 512-byte
-// row per trip.  Waits are bounded as in the other pipelines.
+// mbarrier pairs).  Each of the 128 / E consumer threads holds E consecutive
+// values of one lane's state (E in {1, 2, 4, 8, 16}); a lane is G = W / E
+// threads.  A trip is a serial chain, so its latency bounds the kernel when
+// lanes are few; the chain is kept short:
+//   * the squared norm adds each thread's E squares pairwise, then a
+//     butterfly of G/2 .. 1 xor-shuffles inside the lane's group (every
+//     thread of a group ends with the same bitwise sum: each level adds the
+//     same two operands); E = 8 leaves one shuffle for W = 16;
+//   * the division by max(1, ||y||) is a multiplication by
+//     min(1, 1/sqrt(ss)) from the hardware reciprocal square root: the same
+//     value up to rounding (exactly y inside the unit ball), one multiply on
+//     the chain instead of a square root followed by a division;
+//   * a tile's inputs go to registers before its chain starts and the stage
+//     is handed back to the producer at once.
+// Stores are one coalesced 512-byte row per trip.  Waits are bounded as in
+// the other pipelines.
 #include <algorithm>
 
 #include "es_device.cuh"
+
+// Tuning overrides.
+#ifndef ES_VEC_VALUES_PER_THREAD
+#define ES_VEC_VALUES_PER_THREAD 0      // 0: min(W, 8)
+#endif
+#ifndef ES_VEC_STAGE_TILE
+#define ES_VEC_STAGE_TILE -1            // -1: chosen from the operand count per trip
+#endif
 
 namespace es {
 namespace {
 
 constexpr int kTT = 16;
 constexpr int kMaxStages = 8;
-constexpr int kThreads = 128;     // consumer threads = values per CTA row
+constexpr int kRow = 128;        // values of x per CTA per trip
 
-template <int W>
-__global__ void __launch_bounds__(32 + kThreads)
+template <int E>
+struct Vec;
+template <>
+struct Vec<1> {
+    static __device__ __forceinline__ void load(float* d, const float* p) { d[0] = p[0]; }
+    static __device__ __forceinline__ void store(float* p, const float* v) { __stcs(p, v[0]); }
+};
+template <>
+struct Vec<2> {
+    static __device__ __forceinline__ void load(float* d, const float* p) {
+        const float2 t = *reinterpret_cast<const float2*>(p);
+        d[0] = t.x;
+        d[1] = t.y;
+    }
+    static __device__ __forceinline__ void store(float* p, const float* v) {
+        __stcs(reinterpret_cast<float2*>(p), make_float2(v[0], v[1]));
+    }
+};
+template <>
+struct Vec<4> {
+    static __device__ __forceinline__ void load(float* d, const float* p) {
+        const float4 t = *reinterpret_cast<const float4*>(p);
+        d[0] = t.x;
+        d[1] = t.y;
+        d[2] = t.z;
+        d[3] = t.w;
+    }
+    static __device__ __forceinline__ void store(float* p, const float* v) {
+        __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
+    }
+};
+template <int E>
+struct VecN {   // E = 8 or 16 values as 16-byte pieces
+    static __device__ __forceinline__ void load(float* d, const float* p) {
+#pragma unroll
+        for (int i = 0; i < E; i += 4) Vec<4>::load(d + i, p + i);
+    }
+    static __device__ __forceinline__ void store(float* p, const float* v) {
+#pragma unroll
+        for (int i = 0; i < E; i += 4) Vec<4>::store(p + i, v + i);
+    }
+};
+template <>
+struct Vec<8> : VecN<8> {};
+template <>
+struct Vec<16> : VecN<16> {};
+
+// 1 / max(1, sqrt(ss)) for ss >= 0, i.e. min(1, 1/sqrt(ss)): the hardware
+// reciprocal square root (relative error below 2^-22) and an IEEE minimum
+// with one.  Inside the unit ball the result is exactly one, so h = y as with
+// the division.  A NaN propagates.
+__device__ __forceinline__ float normcap_scale(float ss) {
+    float r;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(ss));
+    return ieee_minimum(r, 1.0f);
+}
+
+template <int W, int E, bool GW>
+__global__ void __launch_bounds__(32 + kRow / E)
 k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_g,
           const float* __restrict__ init, float* __restrict__ out, int T, int J, int gw, int tiles_j, int stages,
           int reverse, unsigned int* status, uint64_t wait_ns, int64_t drop_tile) {
-    constexpr int LV = kThreads / W;               // lanes per CTA
+    constexpr int LV = kRow / W;                   // lanes per CTA
+    constexpr int NC = kRow / E;                   // consumer threads
+    constexpr int G = W / E;                       // threads per lane
+    // active consumer lanes of a warp (fewer than 32 when E is large)
+    constexpr unsigned kMask = NC >= 32 ? 0xffffffffu : ((1u << NC) - 1u);
+    constexpr int GE = GW ? E : 1;                 // staged gate values per trip
+    // whole-tile staging while a trip's operands fit in about nine registers
+    constexpr bool kStageTile = ES_VEC_STAGE_TILE < 0 ? (E + GE <= 9) : (ES_VEC_STAGE_TILE != 0);
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
     __shared__ int abort_flag;
 
     const int gl = LV * gw;                        // gate floats per trip row
-    const uint32_t x_bytes = kTT * kThreads * 4;
+    const uint32_t x_bytes = kTT * kRow * 4;
     const uint32_t g_bytes = static_cast<uint32_t>(kTT * gl * 4);
     const uint32_t g_pad = (g_bytes + 1023u) & ~1023u;
     const uint32_t stage_bytes = x_bytes + g_pad;
-    unsigned char* base = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* base = smem_raw + smem_align_pad(smem_raw);
 
     const int o = blockIdx.x / tiles_j;
     const int j0 = (blockIdx.x % tiles_j) * LV;
@@ -54,7 +135,7 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], kThreads / 32);
+            mbar_init(&empty_bar[s], (NC + 31) / 32);
         }
         abort_flag = 0;
         mbar_fence_init();
@@ -82,69 +163,145 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
                 tma_load_3d(xs, &map_x, j0 * W, j * kTT, o, &full_bar[s], pol);
                 tma_load_3d(xs + x_bytes, &map_g, j0 * gw, j * kTT, o, &full_bar[s], pol);
             }
-            volatile int never = 0;
             for (int k = max(0, issued - stages); k < issued; ++k) {
                 if (k == drop_tile) continue;
-                if (!mbar_wait_bounded(&full_bar[k % stages], (k / stages) & 1, wait_ns, &never))
+                if (!mbar_wait_bounded(&full_bar[k % stages], (k / stages) & 1, wait_ns, nullptr))
                     atomicOr(status, ES_DEVICE_TIMEOUT);
             }
         }
         return;
     }
 
-    // consumers: thread c holds value w of lane j0 + v
+    // consumers: thread c holds values w0 .. w0+E-1 of lane j0 + v
     const int c = threadIdx.x - 32;
-    const int v = c / W;
-    const int w = c % W;
+    const int v = (c * E) / W;
+    const int w0 = (c * E) % W;
     const bool valid = j0 + v < J;
     const int64_t row = static_cast<int64_t>(J) * W;           // values per trip row
-    float h = valid ? init[(static_cast<int64_t>(o) * J + j0 + v) * W + w] : 0.0f;
-    float* obase = out + static_cast<int64_t>(o) * T * row + static_cast<int64_t>(j0) * W + c;
-    const int gi = v * gw + (gw == 1 ? 0 : w);
+    float h[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+        h[e] = valid ? init[(static_cast<int64_t>(o) * J + j0 + v) * W + w0 + e] : 0.0f;
+    float* obase = out + static_cast<int64_t>(o) * T * row + static_cast<int64_t>(j0) * W + c * E;
+    const int gi = v * gw + (GW ? w0 : 0);
 
     for (int k = 0; k < ntiles; ++k) {
         const int s = k % stages;
         const bool ok = mbar_wait_bounded(&full_bar[s], (k / stages) & 1, wait_ns, &abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) {
+        if (!__all_sync(kMask, ok)) {
             if (!ok) report_timeout(status, &abort_flag);
             break;
         }
         const int j = reverse ? ntiles - 1 - k : k;
         const int t0 = j * kTT;
         const int n = min(kTT, T - t0);
-        const float* xs = reinterpret_cast<const float*>(base + static_cast<size_t>(s) * stage_bytes) + c;
+        const float* xs = reinterpret_cast<const float*>(base + static_cast<size_t>(s) * stage_bytes) + c * E;
         const float* gs = reinterpret_cast<const float*>(base + static_cast<size_t>(s) * stage_bytes + x_bytes) + gi;
         float* op = obase + static_cast<int64_t>(t0) * row;
-        for (int q = 0; q < n; ++q) {
-            const int tt = reverse ? n - 1 - q : q;
-            const float xv = xs[tt * kThreads];
-            const float g = gs[tt * gl];
-            const float y = __fadd_rn(__fmul_rn(g, h), xv);
-            float ss = __fmul_rn(y, y);
+        auto load = [&](const int tt, float* xd, float* gd) {
+            Vec<E>::load(xd, xs + tt * kRow);
 #pragma unroll
-            for (int off = W / 2; off >= 1; off >>= 1)
-                ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
-            const float d = ieee_maximum(1.0f, __fsqrt_rn(ss));
-            h = __fdiv_rn(y, d);
-            if (valid) __stcs(op + static_cast<int64_t>(tt) * row, h);
+            for (int e = 0; e < GE; ++e) gd[e] = gs[tt * gl + e];
+        };
+        // one trip from operands already in registers
+        auto trip = [&](const int tt, const float* xv, const float* gv) {
+            float y[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) y[e] = __fadd_rn(__fmul_rn(gv[GW ? e : 0], h[e]), xv[e]);
+            float sq[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) sq[e] = __fmul_rn(y[e], y[e]);
+#pragma unroll
+            for (int span = 1; span < E; span *= 2)
+#pragma unroll
+                for (int e = 0; e + span < E; e += 2 * span) sq[e] = __fadd_rn(sq[e], sq[e + span]);
+            float ss = sq[0];
+#pragma unroll
+            for (int off = G / 2; off >= 1; off >>= 1)
+                ss = __fadd_rn(ss, __shfl_xor_sync(kMask, ss, off));
+            const float scale = normcap_scale(ss);
+#pragma unroll
+            for (int e = 0; e < E; ++e) h[e] = __fmul_rn(y[e], scale);
+            if (valid) Vec<E>::store(op + static_cast<int64_t>(tt) * row, h);
+        };
+        if constexpr (kStageTile) {
+            // the whole tile goes to registers before the chain starts
+            float xr[kTT][E], gr[kTT][GE];
+#pragma unroll
+            for (int tt = 0; tt < kTT; ++tt) load(tt, xr[tt], gr[tt]);
+            // the stage is free as soon as the tile sits in registers
+            __syncwarp(kMask);
+            if (lane == 0) mbar_arrive(&empty_bar[s]);
+            if (!reverse) {
+#pragma unroll
+                for (int tt = 0; tt < kTT; ++tt)
+                    if (tt < n) trip(tt, xr[tt], gr[tt]);
+            } else {
+#pragma unroll
+                for (int tt = kTT - 1; tt >= 0; --tt)
+                    if (tt < n) trip(tt, xr[tt], gr[tt]);
+            }
+        } else {
+            // wide threads: the next trip's operands are read while a trip runs
+            float xa[E], ga[GE], xb[E], gb[GE];
+            if (!reverse) {
+                load(0, xa, ga);
+#pragma unroll
+                for (int tt = 0; tt < kTT; tt += 2) {
+                    load(tt + 1, xb, gb);
+                    if (tt < n) trip(tt, xa, ga);
+                    if (tt + 2 < kTT) load(tt + 2, xa, ga);
+                    if (tt + 1 < n) trip(tt + 1, xb, gb);
+                }
+            } else {
+                load(kTT - 1, xa, ga);
+#pragma unroll
+                for (int tt = kTT - 1; tt >= 0; tt -= 2) {
+                    load(tt - 1, xb, gb);
+                    if (tt < n) trip(tt, xa, ga);
+                    if (tt - 2 >= 0) load(tt - 2, xa, ga);
+                    if (tt - 1 < n) trip(tt - 1, xb, gb);
+                }
+            }
+            __syncwarp(kMask);
+            if (lane == 0) mbar_arrive(&empty_bar[s]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
+}
+
+template <int W, int E>
+cudaError_t launch_we(const Launch& L, const CUtensorMap& mx, const CUtensorMap& mg, int gw, int tiles_j,
+                      int stages, size_t stage_bytes) {
+    const size_t smem = static_cast<size_t>(stages) * stage_bytes + 1024;
+    auto kern = gw == 1 ? k_vec_tma<W, E, false> : k_vec_tma<W, E, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int64_t grid = L.O * tiles_j;
+    kern<<<static_cast<unsigned>(grid), 32 + kRow / E, smem, L.stream>>>(
+        mx, mg, L.init, L.out, static_cast<int>(L.T), static_cast<int>(L.J), gw, tiles_j, stages, L.reverse,
+        L.status, L.wait_ns, L.drop_tile);
+    return cudaGetLastError();
 }
 
 template <int W>
 cudaError_t launch_w(const Launch& L, const CUtensorMap& mx, const CUtensorMap& mg, int gw, int tiles_j,
                      int stages, size_t stage_bytes) {
-    const size_t smem = static_cast<size_t>(stages) * stage_bytes + 1024;
-    auto kern = k_vec_tma<W>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    const int64_t grid = L.O * tiles_j;
-    kern<<<static_cast<unsigned>(grid), 32 + kThreads, smem, L.stream>>>(
-        mx, mg, L.init, L.out, static_cast<int>(L.T), static_cast<int>(L.J), gw, tiles_j, stages, L.reverse,
-        L.status, L.wait_ns, L.drop_tile);
-    return cudaGetLastError();
+    // values per thread: each halving of a lane's thread group takes one
+    // shuffle off the serial chain and adds one add to the thread's own tree
+    int E = ES_VEC_VALUES_PER_THREAD;
+    if (E == 0) E = W >= 8 ? 8 : W;
+    if (E > W) E = W;
+    if constexpr (W >= 16) {
+        if (E == 16) return launch_we<W, 16>(L, mx, mg, gw, tiles_j, stages, stage_bytes);
+    }
+    if constexpr (W >= 8) {
+        if (E == 8) return launch_we<W, 8>(L, mx, mg, gw, tiles_j, stages, stage_bytes);
+    }
+    if constexpr (W >= 4) {
+        if (E == 4) return launch_we<W, 4>(L, mx, mg, gw, tiles_j, stages, stage_bytes);
+    }
+    if (E == 2) return launch_we<W, 2>(L, mx, mg, gw, tiles_j, stages, stage_bytes);
+    return launch_we<W, 1>(L, mx, mg, gw, tiles_j, stages, stage_bytes);
 }
 
 bool encode_vec(const Launch& L, CUtensorMap* m, const float* base, int64_t row, int box_inner, const char** err) {
@@ -170,9 +327,9 @@ bool vec_tma_ok(int body, int64_t O, int64_t T, int64_t J, int64_t W, const int6
     if (body != ES_BODY_NORMCAP) return false;
     if (W != 2 && W != 4 && W != 8 && W != 16) return false;
     if (sw[0] != W || (sw[1] != 1 && sw[1] != W)) return false;
-    const int64_t LV = kThreads / W;
+    const int64_t LV = kRow / W;
     if (J < LV) return false;                               // a tile never exceeds the row
-    if ((J * sw[1]) % 4 != 0 || (LV * sw[1]) % 4 != 0) return false;   // 16-byte strides and boxes
+    if ((J * W) % 4 != 0 || (J * sw[1]) % 4 != 0 || (LV * sw[1]) % 4 != 0) return false;   // 16-byte strides, boxes
     if (O >= (int64_t(1) << 31) || T >= (int64_t(1) << 31) || J * W >= (int64_t(1) << 31)) return false;
     if (O * ((J + LV - 1) / LV) >= (int64_t(1) << 31)) return false;
     for (int k = 1; k < 4; ++k)
@@ -183,10 +340,10 @@ bool vec_tma_ok(int body, int64_t O, int64_t T, int64_t J, int64_t W, const int6
 cudaError_t launch_vec_tma(const Launch& L, const char** err) {
     const int W = static_cast<int>(L.W);
     const int gw = static_cast<int>(L.sw[1]);
-    const int LV = kThreads / W;
+    const int LV = kRow / W;
     const int64_t tiles_j = (L.J + LV - 1) / LV;
     const int64_t ctas = L.O * tiles_j;
-    const size_t x_bytes = static_cast<size_t>(kTT) * kThreads * 4;
+    const size_t x_bytes = static_cast<size_t>(kTT) * kRow * 4;
     const size_t g_bytes = static_cast<size_t>(kTT) * LV * gw * 4;
     const size_t stage_bytes = x_bytes + ((g_bytes + 1023) & ~size_t(1023));
     const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>(8, (ctas + L.num_sms - 1) / L.num_sms));
@@ -194,7 +351,7 @@ cudaError_t launch_vec_tma(const Launch& L, const char** err) {
     const int stages = static_cast<int>(
         std::max<int64_t>(2, std::min<int64_t>(kMaxStages, budget / static_cast<int64_t>(stage_bytes))));
     CUtensorMap mx, mg;
-    if (!encode_vec(L, &mx, L.x, L.J * W, kThreads, err) || !encode_vec(L, &mg, L.a, L.J * gw, LV * gw, err))
+    if (!encode_vec(L, &mx, L.x, L.J * W, kRow, err) || !encode_vec(L, &mg, L.a, L.J * gw, LV * gw, err))
         return cudaErrorInvalidValue;
     const int tj = static_cast<int>(tiles_j);
     switch (W) {

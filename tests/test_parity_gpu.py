@@ -189,3 +189,46 @@ def test_full_size_reverse_equals_flip_scan_flip():
     fwd = es.scan(w.body, init, [xf, cf], axis=1)
     es.device_status()
     assert torch.equal(rev, fwd.flip(1))
+
+
+@pytest.mark.parametrize("path,shape,axis", [
+    ("lane_tma", (2, 40, 64), 1),
+    ("time_tma", (70, 64), -1),
+    ("generic", (3, 9, 5), 1),
+], ids=["lane_tma", "time_tma", "generic"])
+@pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
+def test_maxplus_signed_zeros_and_ties_bitwise(path, shape, axis, reverse):
+    """MAXPLUS on values drawn from a small set with signed zeros, so ties
+    and +0/-0 meetings are frequent: every path matches the oracle's IEEE
+    maximum bit for bit."""
+    rng = np.random.default_rng(5)
+    x = rng.choice(np.array([-1.0, -0.5, -0.0, 0.0, 0.5, 1.0], np.float32), size=shape).astype(np.float32)
+    c = rng.choice(np.array([0.0, -0.0, 0.25, 0.5], np.float32), size=shape).astype(np.float32)
+    ax = axis % len(shape)
+    ishape = shape[:ax] + shape[ax + 1:]
+    init = rng.choice(np.array([-0.0, 0.0, -3.0e38, 0.5], np.float32), size=ishape).astype(np.float32)
+    p = es.plan(M_, shape, axis, reverse=reverse)
+    assert p["path"] == path
+    out = es.scan(M_, torch.from_numpy(init).cuda(), [torch.from_numpy(x).cuda(), torch.from_numpy(c).cuda()],
+                  axis=axis, reverse=reverse)
+    es.device_status()
+    want = oracle.scan(M_, init, [x, c], axis=axis, reverse=reverse)
+    got = out.cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    # the inputs really exercised both zero signs
+    assert (np.signbit(want) & (want == 0)).any() and (~np.signbit(want) & (want == 0)).any()
+
+
+@pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
+def test_normcap_vector_path_inside_unit_ball_is_exact(reverse):
+    """While every state stays inside the unit ball the cap never acts, and the
+    vector-state kernel then reproduces the oracle bit for bit (its scale is
+    exactly one there)."""
+    w = wl.custom(N_, (2, 40, 24, 16), 1, True, (16, 1), x_dist=("normal", 0.0, 0.01),
+                  a_dist=("uniform", 0.5, 0.9), init_dist=("normal", 0.0, 0.01))
+    init, seqs = wl.make_inputs(w)
+    assert es.plan(N_, w.shape, 1, 16, (16, 1), reverse)["path"] == "vec_tma"
+    got = run_gpu(w, init, seqs, reverse).cpu().numpy()
+    want = run_oracle(w, init, seqs, reverse)
+    assert np.linalg.norm(want.astype(np.float64), axis=-1).max() < 1.0
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
