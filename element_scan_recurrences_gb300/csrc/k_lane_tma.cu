@@ -132,21 +132,29 @@ k_lane_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
         float* op = obase + static_cast<int64_t>(t0) * I;
-        if (!reverse) {
+        auto trip = [&](const int tt) {
+            h = step_pointwise<BODY>(h, xr[tt], ar[tt]);
+            if (valid) __stcs(op + static_cast<int64_t>(tt) * I, h);
+        };
+        // full tiles run unguarded (one basic block, so consecutive trips
+        // overlap); only the ragged last tile checks every trip
+        if (n == TT) {
+            if (!reverse) {
 #pragma unroll
-            for (int tt = 0; tt < TT; ++tt) {
-                if (tt < n) {
-                    h = step_pointwise<BODY>(h, xr[tt], ar[tt]);
-                    if (valid) __stcs(op + static_cast<int64_t>(tt) * I, h);
-                }
+                for (int tt = 0; tt < TT; ++tt) trip(tt);
+            } else {
+#pragma unroll
+                for (int tt = TT - 1; tt >= 0; --tt) trip(tt);
             }
         } else {
+            if (!reverse) {
 #pragma unroll
-            for (int tt = TT - 1; tt >= 0; --tt) {
-                if (tt < n) {
-                    h = step_pointwise<BODY>(h, xr[tt], ar[tt]);
-                    if (valid) __stcs(op + static_cast<int64_t>(tt) * I, h);
-                }
+                for (int tt = 0; tt < TT; ++tt)
+                    if (tt < n) trip(tt);
+            } else {
+#pragma unroll
+                for (int tt = TT - 1; tt >= 0; --tt)
+                    if (tt < n) trip(tt);
             }
         }
     }

@@ -147,24 +147,29 @@ k_time_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
         // the input stage is free as soon as the segment sits in registers
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
-        if (!reverse) {
+        auto quad = [&](const int q, const bool rev) {
+            float4 ov;
+            run_vec<BODY>(h, xv[q], av[q], ov, rev);
+            *reinterpret_cast<float4*>(orow + ((static_cast<uint32_t>(q) ^ sw) << 4)) = ov;
+        };
+        // full tiles run unguarded (one basic block); only a ragged last tile
+        // checks every group of four trips
+        if (nq == kTT / 4) {
+            if (!reverse) {
 #pragma unroll
-            for (int q = 0; q < kTT / 4; ++q) {
-                if (q < nq) {
-                    float4 ov;
-                    run_vec<BODY>(h, xv[q], av[q], ov, false);
-                    *reinterpret_cast<float4*>(orow + ((static_cast<uint32_t>(q) ^ sw) << 4)) = ov;
-                }
+                for (int q = 0; q < kTT / 4; ++q) quad(q, false);
+            } else {
+#pragma unroll
+                for (int q = kTT / 4 - 1; q >= 0; --q) quad(q, true);
             }
+        } else if (!reverse) {
+#pragma unroll
+            for (int q = 0; q < kTT / 4; ++q)
+                if (q < nq) quad(q, false);
         } else {
 #pragma unroll
-            for (int q = kTT / 4 - 1; q >= 0; --q) {
-                if (q < nq) {
-                    float4 ov;
-                    run_vec<BODY>(h, xv[q], av[q], ov, true);
-                    *reinterpret_cast<float4*>(orow + ((static_cast<uint32_t>(q) ^ sw) << 4)) = ov;
-                }
-            }
+            for (int q = kTT / 4 - 1; q >= 0; --q)
+                if (q < nq) quad(q, true);
         }
     }
     if (storer) bulk_wait_all();

@@ -16,7 +16,7 @@
 //   * the squared norm adds each thread's E squares pairwise, then a
 //     butterfly of G/2 .. 1 xor-shuffles inside the lane's group (every
 //     thread of a group ends with the same bitwise sum: each level adds the
-//     same two operands); E = 8 leaves one shuffle for W = 16;
+//     same two operands); E = 4 (two shuffles for W = 16) measured best;
 //   * the division by max(1, ||y||) is a multiplication by
 //     min(1, 1/sqrt(ss)) from the hardware reciprocal square root: the same
 //     value up to rounding (exactly y inside the unit ball), one multiply on
@@ -31,7 +31,7 @@
 
 // Tuning overrides.
 #ifndef ES_VEC_VALUES_PER_THREAD
-#define ES_VEC_VALUES_PER_THREAD 0      // 0: min(W, 8)
+#define ES_VEC_VALUES_PER_THREAD 0      // 0: min(W, 4)
 #endif
 #ifndef ES_VEC_STAGE_TILE
 #define ES_VEC_STAGE_TILE -1            // -1: chosen from the operand count per trip
@@ -232,7 +232,17 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
             // the stage is free as soon as the tile sits in registers
             __syncwarp(kMask);
             if (lane == 0) mbar_arrive(&empty_bar[s]);
-            if (!reverse) {
+            // full tiles run unguarded (one basic block, so consecutive trips
+            // overlap); only the ragged last tile checks every trip
+            if (n == kTT) {
+                if (!reverse) {
+#pragma unroll
+                    for (int tt = 0; tt < kTT; ++tt) trip(tt, xr[tt], gr[tt]);
+                } else {
+#pragma unroll
+                    for (int tt = kTT - 1; tt >= 0; --tt) trip(tt, xr[tt], gr[tt]);
+                }
+            } else if (!reverse) {
 #pragma unroll
                 for (int tt = 0; tt < kTT; ++tt)
                     if (tt < n) trip(tt, xr[tt], gr[tt]);
@@ -289,7 +299,7 @@ cudaError_t launch_w(const Launch& L, const CUtensorMap& mx, const CUtensorMap& 
     // values per thread: each halving of a lane's thread group takes one
     // shuffle off the serial chain and adds one add to the thread's own tree
     int E = ES_VEC_VALUES_PER_THREAD;
-    if (E == 0) E = W >= 8 ? 8 : W;
+    if (E == 0) E = W >= 4 ? 4 : W;
     if (E > W) E = W;
     if constexpr (W >= 16) {
         if (E == 16) return launch_we<W, 16>(L, mx, mg, gw, tiles_j, stages, stage_bytes);
