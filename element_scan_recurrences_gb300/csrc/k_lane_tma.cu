@@ -235,16 +235,19 @@ cudaError_t launch_lane_tma(const Launch& L, const char** err) {
     if (ES_LANE_LI != 0 && I >= ES_LANE_LI) LI = ES_LANE_LI;
     const int64_t tiles_i = (I + LI - 1) / LI;
     const int64_t ctas = L.O * tiles_i;
-    // SMEM per CTA when every CTA is resident at once; 32-trip tiles when at
-    // least four of them fit, else 16-trip tiles.
-    const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>(8, (ctas + L.num_sms - 1) / L.num_sms));
-    const int64_t budget = (200 * 1024) / per_sm;
-    int TT = (budget / (2LL * 32 * LI * 4) >= 4) ? 32 : 16;
+    // Pipeline depth: about 96 trips of both sequences in flight per CTA
+    // (three 32-trip stages), measured best on GB300 for both one CTA per
+    // SM (few lanes) and several (many lanes, even when not all CTAs fit at
+    // once); 16-trip tiles only when 32-trip stages would not fit twice.
+    (void)ctas;
+    int TT = 32;
+    int stages = 3;
+    if (2LL * 32 * LI * 4 * 3 > 200 * 1024) {
+        TT = 16;
+        stages = 6;
+    }
     if (ES_LANE_TT != 0) TT = ES_LANE_TT;
-    const int64_t stage_bytes = 2LL * TT * LI * 4;
-    int stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(kMaxStages, budget / stage_bytes)));
     if (ES_LANE_STAGES != 0) stages = ES_LANE_STAGES;
-
     CUtensorMap mx, ma;
     if (!encode_rows(L, &mx, L.x, I, LI, TT, err) || !encode_rows(L, &ma, L.a, I, LI, TT, err))
         return cudaErrorInvalidValue;

@@ -24,6 +24,14 @@ namespace {
 
 constexpr int kTT = 32;            // trips per tile: 128 bytes per row (swizzle span)
 constexpr int kMaxStages = 6;
+
+// Tuning overrides (0: chosen per shape in launch_time_tma).
+#ifndef ES_TIME_LO
+#define ES_TIME_LO 64       // rows (lanes) per CTA: 64 or 128
+#endif
+#ifndef ES_TIME_STAGES
+#define ES_TIME_STAGES 0    // pipeline depth
+#endif
 constexpr int kOutBufs = 3;
 
 template <int BODY>
@@ -218,12 +226,13 @@ bool time_tma_ok(int body, int64_t O, int64_t T, int64_t J, int64_t W, const int
 }
 
 cudaError_t launch_time_tma(const Launch& L, const char** err) {
-    constexpr int LO = 64;
+    constexpr int LO = ES_TIME_LO;
     const int64_t ctas = (L.O + LO - 1) / LO;
     const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>(3, (ctas + L.num_sms - 1) / L.num_sms));
     const int64_t budget = (210 * 1024) / per_sm - kOutBufs * LO * 128 - 1024;
     const int64_t stage_bytes = 2LL * LO * 128;
-    const int stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(kMaxStages, budget / stage_bytes)));
+    int stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(kMaxStages, budget / stage_bytes)));
+    if (ES_TIME_STAGES != 0) stages = ES_TIME_STAGES;
     CUtensorMap mx, ma, mo;
     if (!encode_time_rows(L, &mx, L.x, LO, err) || !encode_time_rows(L, &ma, L.a, LO, err) ||
         !encode_time_rows(L, &mo, L.out, LO, err))
