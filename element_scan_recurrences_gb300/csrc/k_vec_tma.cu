@@ -7,7 +7,7 @@
 //
 // Canonical view: x and out are [O, T, J*W], the gate is [O, T, J*gw].  One
 // CTA owns LV = 128 / W adjacent lanes of one o (128 contiguous values per
-// trip) and walks all T trips.  Warp 0's lane 0 streams time tiles of TT
+// trip) and walks all T trips.  Warp 0's lane 0 streams time tiles of 32
 // trips of x and of the gate into an S-stage SMEM ring with TMA (full/empty
 // mbarrier pairs).  Each of the 128 / E consumer threads holds E consecutive
 // values of one lane's state (E in {1, 2, 4, 8, 16}); a lane is G = W / E
@@ -26,6 +26,7 @@
 // Stores are one coalesced 512-byte row per trip.  Waits are bounded as in
 // the other pipelines.
 #include <algorithm>
+#include <type_traits>
 
 #include "es_device.cuh"
 
@@ -40,7 +41,7 @@
 namespace es {
 namespace {
 
-constexpr int kTT = 16;
+constexpr int kTT = 32;       // trips per tile
 constexpr int kMaxStages = 8;
 constexpr int kRow = 128;        // values of x per CTA per trip
 
@@ -112,8 +113,8 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
     // active consumer lanes of a warp (fewer than 32 when E is large)
     constexpr unsigned kMask = NC >= 32 ? 0xffffffffu : ((1u << NC) - 1u);
     constexpr int GE = GW ? E : 1;                 // staged gate values per trip
-    // whole-tile staging while a trip's operands fit in about nine registers
-    constexpr bool kStageTile = ES_VEC_STAGE_TILE < 0 ? (E + GE <= 9) : (ES_VEC_STAGE_TILE != 0);
+    // whole-tile staging while the tile's operands fit in about 160 registers
+    constexpr bool kStageTile = ES_VEC_STAGE_TILE < 0 ? (kTT * (E + GE) <= 160) : (ES_VEC_STAGE_TILE != 0);
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
@@ -224,6 +225,18 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
             for (int e = 0; e < E; ++e) h[e] = __fmul_rn(y[e], scale);
             if (valid) Vec<E>::store(op + static_cast<int64_t>(tt) * row, h);
         };
+        // Sum over the lane's W values of u[e]*v[e]: this thread's E products
+        // pairwise, then the xor-shuffle butterfly of the lane's group.
+        auto local_dot = [&](const float* u, const float* v) {
+            float p[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) p[e] = __fmul_rn(u[e], v[e]);
+#pragma unroll
+            for (int span = 1; span < E; span *= 2)
+#pragma unroll
+                for (int e = 0; e + span < E; e += 2 * span) p[e] = __fadd_rn(p[e], p[e + span]);
+            return p[0];
+        };
         if constexpr (kStageTile) {
             // the whole tile goes to registers before the chain starts
             float xr[kTT][E], gr[kTT][GE];
@@ -232,10 +245,65 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
             // the stage is free as soon as the tile sits in registers
             __syncwarp(kMask);
             if (lane == 0) mbar_arrive(&empty_bar[s]);
+            // A full tile with a width-one gate, trips in scan order.  With
+            // h = s*y and a = g'*s, the next trip's y' = g'*h + x' has
+            //     ||y'||^2 = a^2 ||y||^2 + 2a (y . x') + ||x'||^2,
+            // and all three sums depend only on this trip's y and the staged x',
+            // so they are reduced while this trip's scale s is still being formed.
+            // The scale of the next trip then needs a few scalar operations after
+            // s instead of a whole y' -> ||y'||^2 reduction: the serial chain per
+            // trip roughly halves.  The sum is clamped at zero (rounding could
+            // make a vanishing norm slightly negative).  The first trip of a tile
+            // reduces its ||y||^2 directly.
+            auto propagated_tile = [&](auto fwd_tag) {
+                constexpr bool FWD = decltype(fwd_tag)::value;
+                constexpr int first = FWD ? 0 : kTT - 1;
+                float y[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) y[e] = __fadd_rn(__fmul_rn(gr[first][0], h[e]), xr[first][e]);
+                float qf = local_dot(y, y);
+#pragma unroll
+                for (int off = G / 2; off >= 1; off >>= 1) qf = __fadd_rn(qf, __shfl_xor_sync(kMask, qf, off));
+#pragma unroll
+                for (int q = 0; q < kTT; ++q) {
+                    const int tt = FWD ? q : kTT - 1 - q;
+                    const float sc = normcap_scale(qf);
+                    if (q + 1 < kTT) {
+                        const int tn = FWD ? tt + 1 : tt - 1;
+                        float Q = local_dot(y, y);
+                        float D = local_dot(y, xr[tn]);
+                        float P = local_dot(xr[tn], xr[tn]);
+#pragma unroll
+                        for (int off = G / 2; off >= 1; off >>= 1) {
+                            Q = __fadd_rn(Q, __shfl_xor_sync(kMask, Q, off));
+                            D = __fadd_rn(D, __shfl_xor_sync(kMask, D, off));
+                            P = __fadd_rn(P, __shfl_xor_sync(kMask, P, off));
+                        }
+#pragma unroll
+                        for (int e = 0; e < E; ++e) h[e] = __fmul_rn(y[e], sc);
+                        if (valid) Vec<E>::store(op + static_cast<int64_t>(tt) * row, h);
+                        const float gn = gr[tn][0];
+#pragma unroll
+                        for (int e = 0; e < E; ++e) y[e] = __fadd_rn(__fmul_rn(gn, h[e]), xr[tn][e]);
+                        const float a = __fmul_rn(gn, sc);
+                        qf = __fmaf_rn(__fmul_rn(a, a), Q, __fmaf_rn(__fadd_rn(a, a), D, P));
+                        qf = ieee_maximum(qf, 0.0f);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < E; ++e) h[e] = __fmul_rn(y[e], sc);
+                        if (valid) Vec<E>::store(op + static_cast<int64_t>(tt) * row, h);
+                    }
+                }
+            };
             // full tiles run unguarded (one basic block, so consecutive trips
             // overlap); only the ragged last tile checks every trip
             if (n == kTT) {
-                if (!reverse) {
+                if constexpr (!GW) {
+                    // width-one gate: the squared norm of the next trip's y
+                    // follows from this trip's (see propagated_tile)
+                    if (!reverse) propagated_tile(std::true_type{});
+                    else propagated_tile(std::false_type{});
+                } else if (!reverse) {
 #pragma unroll
                     for (int tt = 0; tt < kTT; ++tt) trip(tt, xr[tt], gr[tt]);
                 } else {
