@@ -126,10 +126,13 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// L2 policy for streamed operands that are read exactly once
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+// L2 policy for the streamed TMA loads: normal priority.  An evict-first
+// hint measured worse on GB300: with 256-byte L2 promotion a 128-byte row
+// segment brings in the next tile's half of the line, and evict-first drops
+// it before that tile asks for it, so the data is read from HBM twice.
+__device__ __forceinline__ uint64_t l2_policy_stream() {
     uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
 

@@ -72,7 +72,7 @@ k_lane_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
         if (lane == 0) {
             tma_prefetch_desc(&map_x);
             tma_prefetch_desc(&map_a);
-            const uint64_t pol = l2_policy_evict_first();
+            const uint64_t pol = l2_policy_stream();
             int issued = 0;
             for (int k = 0; k < ntiles; ++k) {
                 const int s = k % stages;
@@ -132,9 +132,14 @@ k_lane_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
         float* op = obase + static_cast<int64_t>(t0) * I;
+        // The state alternates between two registers (by trip parity), so a
+        // trip never overwrites the register the previous trip's store may
+        // still be reading.  Consecutive trips alternate parity in both
+        // directions; the last trip is n-1 forward and 0 in reverse.
+        float hv[2] = {h, h};
         auto trip = [&](const int tt) {
-            h = step_pointwise<BODY>(h, xr[tt], ar[tt]);
-            if (valid) __stcs(op + static_cast<int64_t>(tt) * I, h);
+            hv[tt & 1] = step_pointwise<BODY>(hv[(tt & 1) ^ 1], xr[tt], ar[tt]);
+            if (valid) __stcs(op + static_cast<int64_t>(tt) * I, hv[tt & 1]);
         };
         // full tiles run unguarded (one basic block, so consecutive trips
         // overlap); only the ragged last tile checks every trip
@@ -157,6 +162,7 @@ k_lane_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
                     if (tt < n) trip(tt);
             }
         }
+        h = reverse ? hv[0] : hv[(n - 1) & 1];
     }
 }
 

@@ -84,7 +84,7 @@ k_time_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CU
         if (lane == 0) {
             tma_prefetch_desc(&map_x);
             tma_prefetch_desc(&map_a);
-            const uint64_t pol = l2_policy_evict_first();
+            const uint64_t pol = l2_policy_stream();
             int issued = 0;
             for (int k = 0; k < ntiles; ++k) {
                 const int s = k % stages;

@@ -147,7 +147,7 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
         if (lane == 0) {
             tma_prefetch_desc(&map_x);
             tma_prefetch_desc(&map_g);
-            const uint64_t pol = l2_policy_evict_first();
+            const uint64_t pol = l2_policy_stream();
             int issued = 0;
             for (int k = 0; k < ntiles; ++k) {
                 const int s = k % stages;
@@ -258,6 +258,10 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
             auto propagated_tile = [&](auto fwd_tag) {
                 constexpr bool FWD = decltype(fwd_tag)::value;
                 constexpr int first = FWD ? 0 : kTT - 1;
+                // the state alternates between two register sets, so a trip
+                // never overwrites registers the previous trip's store may
+                // still be reading
+                float hr[2][E];
                 float y[E];
 #pragma unroll
                 for (int e = 0; e < E; ++e) y[e] = __fadd_rn(__fmul_rn(gr[first][0], h[e]), xr[first][e]);
@@ -267,6 +271,7 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
 #pragma unroll
                 for (int q = 0; q < kTT; ++q) {
                     const int tt = FWD ? q : kTT - 1 - q;
+                    float* hs = hr[q & 1];
                     const float sc = normcap_scale(qf);
                     if (q + 1 < kTT) {
                         const int tn = FWD ? tt + 1 : tt - 1;
@@ -280,20 +285,22 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
                             P = __fadd_rn(P, __shfl_xor_sync(kMask, P, off));
                         }
 #pragma unroll
-                        for (int e = 0; e < E; ++e) h[e] = __fmul_rn(y[e], sc);
-                        if (valid) Vec<E>::store(op + static_cast<int64_t>(tt) * row, h);
+                        for (int e = 0; e < E; ++e) hs[e] = __fmul_rn(y[e], sc);
+                        if (valid) Vec<E>::store(op + static_cast<int64_t>(tt) * row, hs);
                         const float gn = gr[tn][0];
 #pragma unroll
-                        for (int e = 0; e < E; ++e) y[e] = __fadd_rn(__fmul_rn(gn, h[e]), xr[tn][e]);
+                        for (int e = 0; e < E; ++e) y[e] = __fadd_rn(__fmul_rn(gn, hs[e]), xr[tn][e]);
                         const float a = __fmul_rn(gn, sc);
                         qf = __fmaf_rn(__fmul_rn(a, a), Q, __fmaf_rn(__fadd_rn(a, a), D, P));
                         qf = ieee_maximum(qf, 0.0f);
                     } else {
 #pragma unroll
-                        for (int e = 0; e < E; ++e) h[e] = __fmul_rn(y[e], sc);
-                        if (valid) Vec<E>::store(op + static_cast<int64_t>(tt) * row, h);
+                        for (int e = 0; e < E; ++e) hs[e] = __fmul_rn(y[e], sc);
+                        if (valid) Vec<E>::store(op + static_cast<int64_t>(tt) * row, hs);
                     }
                 }
+#pragma unroll
+                for (int e = 0; e < E; ++e) h[e] = hr[(kTT - 1) & 1][e];
             };
             // full tiles run unguarded (one basic block, so consecutive trips
             // overlap); only the ragged last tile checks every trip
