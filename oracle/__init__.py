@@ -56,6 +56,13 @@ def build(force: bool = False) -> str:
 
 def _bind(lib_path: str):
     lib = ctypes.CDLL(lib_path)
+    if hasattr(lib, "es_oracle_backward_f32"):
+        fp = ctypes.POINTER(ctypes.c_float)
+        fb = lib.es_oracle_backward_f32
+        fb.restype = ctypes.c_int
+        fb.argtypes = [ctypes.c_int, fp, ctypes.POINTER(fp), ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
+                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
+                       fp, fp, fp, ctypes.POINTER(fp)]
     for name, ft in (("es_oracle_f32", ctypes.c_float),
                      ("es_oracle_f64", ctypes.c_double)):
         fn = getattr(lib, name)
@@ -148,6 +155,47 @@ def scan(body, initial, seqs, axis: int = 0, state_axis: bool = False,
     return out
 
 
+def scan_backward(body, initial, seqs, states, grad_out, axis: int = 0, state_axis: bool = False,
+                  reverse: bool = False, _lib=None):
+    """Gradients of sum(grad_out * scan(...)) with respect to initial and both
+    sequences, from the forward states.  Returns (grad_initial, [gx, ga]) with
+    the shapes of initial and of each sequence."""
+    lib = _lib if _lib is not None else _load()
+    ft = ctypes.c_float
+    fp = ctypes.POINTER(ft)
+    seqs = [_c_array(s, np.float32) for s in seqs]
+    initial = _c_array(initial, np.float32)
+    states = _c_array(states, np.float32)
+    grad_out = _c_array(grad_out, np.float32)
+    shape = list(states.shape)
+    if list(grad_out.shape) != shape:
+        raise ValueError("grad_out shape %r, expected %r" % (list(grad_out.shape), shape))
+    rank = len(shape)
+    W = shape[-1] if state_axis else 0
+    ax = axis + rank if axis < 0 else axis
+    if not 0 <= ax < rank:
+        raise ValueError("axis out of range")
+    if list(initial.shape) != shape[:ax] + shape[ax + 1:]:
+        raise ValueError("initial shape %r does not fit %r" % (list(initial.shape), shape))
+    for s in seqs:
+        want = list(shape)
+        if state_axis and s.shape[-1] == 1:
+            want[-1] = 1
+        if list(s.shape) != want:
+            raise ValueError("sequence shape %r, expected %r" % (list(s.shape), want))
+    widths = (ctypes.c_int64 * 2)(*[s.shape[-1] for s in seqs]) if state_axis else None
+    g_init = np.empty_like(initial)
+    g_seqs = [np.empty_like(s) for s in seqs]
+    sp = (fp * 2)(*[s.ctypes.data_as(fp) for s in seqs])
+    gp = (fp * 2)(*[g.ctypes.data_as(fp) for g in g_seqs])
+    rc = lib.es_oracle_backward_f32(_body_id(body), initial.ctypes.data_as(fp), sp, 2, (ctypes.c_int64 * rank)(*shape),
+                                    rank, int(axis), int(W), widths, int(bool(reverse)), states.ctypes.data_as(fp),
+                                    grad_out.ctypes.data_as(fp), g_init.ctypes.data_as(fp), gp)
+    if rc != 0:
+        raise ValueError("oracle rejected backward arguments")
+    return g_init, g_seqs
+
+
 class Oracle:
     """An oracle bound to one compiled library (tests load mutated builds)."""
 
@@ -158,6 +206,11 @@ class Oracle:
              reverse: bool = False, dtype=np.float32) -> np.ndarray:
         return scan(body, initial, seqs, axis=axis, state_axis=state_axis,
                     reverse=reverse, dtype=dtype, _lib=self._lib)
+
+    def scan_backward(self, body, initial, seqs, states, grad_out, axis: int = 0, state_axis: bool = False,
+                      reverse: bool = False):
+        return scan_backward(body, initial, seqs, states, grad_out, axis=axis, state_axis=state_axis,
+                             reverse=reverse, _lib=self._lib)
 
 
 def scan_lanes(body, initial, x, a, reverse: bool = False) -> np.ndarray:

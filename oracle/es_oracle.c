@@ -242,3 +242,174 @@ int es_oracle_f64(int body, const double *initial, const double *const *seqs,
     }
     return 0;
 }
+
+/*
+ * Backward pass ("Nonlinear element scans", "Precision and gradients"):
+ * gradients flow to `initial` and to every sequence; the gradient of a scan
+ * is another scan that runs the trips in the opposite order and applies the
+ * body's vector-Jacobian product once a trip.  The forward states are given
+ * (`states`, the forward output); `grad_out` is dL/d(states).
+ *
+ * In scan order s = 0..T-1 (trip t(s) = reverse ? T-1-s : s) the state before
+ * trip s is initial for s = 0, else states[t(s-1)].  The cotangent lam of the
+ * state starts at zero; for s = T-1 down to 0: lam += grad_out[t(s)], then
+ * the body's VJP at trip s gives (lam_prev, dx[t], da[t]), and lam = lam_prev.
+ * At the end grad_initial = lam.
+ *
+ * Per body, with h the trip's output and p the state before it:
+ *   TANH_DECAY  mu = lam * (1 - h*h);  dx = mu;  da = mu * p;  lam_prev = mu * a
+ *   MAXPLUS     v = p - c: v > x routes lam to the state (lam_prev = lam,
+ *               dc = -lam), x > v routes it to x (dx = lam); a tie splits it
+ *               evenly (the usual tie rule for maximum)
+ *   NORMCAP     y = a*p + x recomputed, n = sqrt(sum y*y); if n <= 1,
+ *               mu = lam, else mu = (lam - h * (h . lam)) / n; dx = mu;
+ *               da = mu * p (summed over the state for a width-one gate);
+ *               lam_prev = a * mu
+ * A width-one sequence receives the sum over the state of its gradients.
+ * Readings: the MAXPLUS tie rule (even split) and the NORMCAP branch at
+ * n == 1 (the unscaled side) are not fixed by the pages.
+ */
+int es_oracle_backward_f32(int body, const float *initial, const float *const *seqs, int n_seqs,
+                           const int64_t *shape, int rank, int axis, int state_width,
+                           const int64_t *seq_widths, int reverse, const float *states,
+                           const float *grad_out, float *grad_initial, float *const *grad_seqs)
+{
+    if (n_seqs != 2 || rank < 1) return -1;
+    if (axis < 0) axis += rank;
+    if (axis < 0 || axis >= rank) return -1;
+    if (state_width < 0 || state_width > ORACLE_MAX_STATE) return -1;
+    if (state_width > 0 && (axis == rank - 1 || shape[rank - 1] != state_width))
+        return -1;
+    if (body == ORACLE_NORMCAP && state_width == 0) return -1;
+    if (body != ORACLE_TANH_DECAY && body != ORACLE_NORMCAP && body != ORACLE_MAXPLUS)
+        return -1;
+
+    int64_t O = 1, T = shape[axis], after = 1;
+    for (int d = 0; d < axis; d++) O *= shape[d];
+    for (int d = axis + 1; d < rank; d++) after *= shape[d];
+    int64_t W = state_width > 0 ? state_width : 1;
+    int64_t J = after / W;
+    int64_t sw[2];
+    for (int k = 0; k < 2; k++) {
+        sw[k] = W;
+        if (state_width > 0 && seq_widths != NULL) sw[k] = seq_widths[k];
+        if (sw[k] != 1 && sw[k] != W) return -1;
+    }
+
+    const float *x = seqs[0];
+    const float *a = seqs[1];
+    float *gx = grad_seqs[0];
+    float *ga = grad_seqs[1];
+    float lam[ORACLE_MAX_STATE], p[ORACLE_MAX_STATE], mu[ORACLE_MAX_STATE], y[ORACLE_MAX_STATE];
+    float dx[ORACLE_MAX_STATE], da[ORACLE_MAX_STATE];
+
+    for (int64_t o = 0; o < O; o++) {
+        for (int64_t j = 0; j < J; j++) {
+            for (int64_t w = 0; w < W; w++) lam[w] = 0.0f;
+
+            /* scan order backwards: s = T-1 .. 0 */
+            for (int64_t s = T - 1; s >= 0; s--) {
+                int64_t t = reverse ? T - 1 - s : s;
+                const float *ht = states + ((o * T + t) * J + j) * W;
+                const float *gt = grad_out + ((o * T + t) * J + j) * W;
+                /* the state before this trip */
+                if (s == 0) {
+                    for (int64_t w = 0; w < W; w++) p[w] = initial[(o * J + j) * W + w];
+                } else {
+                    int64_t tp = reverse ? t + 1 : t - 1;
+                    const float *hp = states + ((o * T + tp) * J + j) * W;
+                    for (int64_t w = 0; w < W; w++) p[w] = hp[w];
+                }
+                for (int64_t w = 0; w < W; w++) lam[w] = lam[w] + gt[w];
+                const float *xt = x + ((o * T + t) * J + j) * sw[0];
+                const float *at = a + ((o * T + t) * J + j) * sw[1];
+
+                if (body == ORACLE_TANH_DECAY) {
+                    /* h = tanh(v), v = x + a*p:  dh/dv = 1 - h*h */
+                    for (int64_t w = 0; w < W; w++) {
+                        float av = at[sw[1] == 1 ? 0 : w];
+                        float hh = ht[w] * ht[w];
+                        float om = 1.0f - hh;
+                        float m = lam[w] * om;
+                        dx[w] = m;
+                        da[w] = m * p[w];
+                        lam[w] = m * av;
+                    }
+                } else if (body == ORACLE_MAXPLUS) {
+                    /* h = maximum(p - c, x): the larger operand takes the
+                       cotangent, a tie splits it evenly */
+                    for (int64_t w = 0; w < W; w++) {
+                        float v = p[w] - at[sw[1] == 1 ? 0 : w];
+                        float xv = xt[sw[0] == 1 ? 0 : w];
+                        if (v > xv) {
+                            dx[w] = 0.0f;
+                            da[w] = -lam[w];
+                        } else if (xv > v) {
+                            dx[w] = lam[w];
+                            da[w] = 0.0f;
+                            lam[w] = 0.0f;
+                        } else {
+                            float half = lam[w] * 0.5f;
+                            dx[w] = half;
+                            da[w] = -half;
+                            lam[w] = half;
+                        }
+                    }
+                } else {
+                    /* y = a*p + x recomputed; h = y / max(1, |y|) */
+                    float ss = 0.0f;
+                    for (int64_t w = 0; w < W; w++) {
+                        float ap = at[sw[1] == 1 ? 0 : w] * p[w];
+                        y[w] = ap + xt[sw[0] == 1 ? 0 : w];
+                    }
+                    for (int64_t w = 0; w < W; w++) {
+                        float sq = y[w] * y[w];
+                        ss = ss + sq;
+                    }
+                    float nrm = sqrtf(ss);
+                    if (nrm <= 1.0f) {
+                        /* inside the unit ball h = y */
+                        for (int64_t w = 0; w < W; w++) mu[w] = lam[w];
+                    } else {
+                        /* h = y/n: d h = (I - h h^T) d y / n */
+                        float hl = 0.0f;
+                        for (int64_t w = 0; w < W; w++) {
+                            float q = ht[w] * lam[w];
+                            hl = hl + q;
+                        }
+                        for (int64_t w = 0; w < W; w++) {
+                            float r = ht[w] * hl;
+                            float dlt = lam[w] - r;
+                            mu[w] = dlt / nrm;
+                        }
+                    }
+                    for (int64_t w = 0; w < W; w++) {
+                        dx[w] = mu[w];
+                        da[w] = mu[w] * p[w];
+                        lam[w] = at[sw[1] == 1 ? 0 : w] * mu[w];
+                    }
+                }
+
+                /* a width-one sequence gets the sum over the state, in order */
+                float *gxt = gx + ((o * T + t) * J + j) * sw[0];
+                float *gat = ga + ((o * T + t) * J + j) * sw[1];
+                if (sw[0] == 1 && W > 1) {
+                    float acc = 0.0f;
+                    for (int64_t w = 0; w < W; w++) acc = acc + dx[w];
+                    gxt[0] = acc;
+                } else {
+                    for (int64_t w = 0; w < W; w++) gxt[w] = dx[w];
+                }
+                if (sw[1] == 1 && W > 1) {
+                    float acc = 0.0f;
+                    for (int64_t w = 0; w < W; w++) acc = acc + da[w];
+                    gat[0] = acc;
+                } else {
+                    for (int64_t w = 0; w < W; w++) gat[w] = da[w];
+                }
+            }
+            for (int64_t w = 0; w < W; w++) grad_initial[(o * J + j) * W + w] = lam[w];
+        }
+    }
+    return 0;
+}

@@ -421,4 +421,170 @@ def pin_f64_twin_close(scan):
         assert err <= 1e-5, (body, err)
 
 
-ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
+
+
+# ---------------------------------------------------------------------------
+# backward pass ("Precision and gradients": gradients reach initial and every
+# sequence; the gradient is a scan in the opposite direction)
+
+def _fd_case(body, rng, W=None, gate_wide=False):
+    """Small random case in f64-friendly ranges, with no MAXPLUS ties."""
+    if body == "NORMCAP":
+        W = W or 4
+        shape = (2, 6, 3, W)
+        x = rng.normal(0, 0.6, size=shape)
+        g = rng.uniform(0.6, 1.0, size=shape if gate_wide else shape[:-1] + (1,))
+        init = rng.normal(0, 0.3, size=(2, 3, W))
+        return init, x, g, True
+    shape = (2, 6, 3)
+    if body == "MAXPLUS":
+        x = rng.uniform(-1, 1, size=shape)
+        c = rng.uniform(0.0, 0.3, size=shape)
+        init = rng.uniform(-1, 1, size=(2, 3))
+        return init, x, c, False
+    x = rng.normal(0, 1, size=shape)
+    a = rng.uniform(-0.9, 0.9, size=shape)
+    init = rng.normal(0, 0.5, size=(2, 3))
+    return init, x, a, False
+
+
+def _fd_grads(scan, body, init, x, a, G, sa, reverse, eps=1e-6):
+    """Central differences of L = sum(G * scan(...)) in the f64 twin."""
+    def L(i_, x_, a_):
+        return float(np.sum(G * scan(body, i_, [x_, a_], axis=1, state_axis=sa, reverse=reverse,
+                                     dtype=np.float64)))
+    out = []
+    for which, arr in enumerate((init, x, a)):
+        g = np.empty_like(arr)
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            plus = [init.copy(), x.copy(), a.copy()]
+            minus = [init.copy(), x.copy(), a.copy()]
+            plus[which][idx] += eps
+            minus[which][idx] -= eps
+            g[idx] = (L(*plus) - L(*minus)) / (2 * eps)
+        out.append(g)
+    return out
+
+
+def pin_bwd_finite_differences(scan, scan_backward=None):
+    """Every gradient matches central differences of the f64 forward."""
+    if scan_backward is None:
+        return
+    rng = _rng(51)
+    for body, kw in (("TANH_DECAY", {}), ("MAXPLUS", {}), ("NORMCAP", {}), ("NORMCAP", {"gate_wide": True})):
+        for reverse in (False, True):
+            init, x, a, sa = _fd_case(body, rng, **kw)
+            init32, x32, a32 = init.astype(f32), x.astype(f32), a.astype(f32)
+            init, x, a = init32.astype(np.float64), x32.astype(np.float64), a32.astype(np.float64)
+            h = scan(body, init32, [x32, a32], axis=1, state_axis=sa, reverse=reverse)
+            G = rng.normal(size=h.shape).astype(f32)
+            gi, (gx, ga) = scan_backward(body, init32, [x32, a32], h, G, axis=1, state_axis=sa, reverse=reverse)
+            fi, fx, fa = _fd_grads(scan, body, init, x, a, G.astype(np.float64), sa, reverse)
+            for name, got, want in (("initial", gi, fi), ("x", gx, fx), ("a", ga, fa)):
+                err = np.max(np.abs(got - want) / (1.0 + np.abs(want)))
+                assert err <= 2e-4, (body, kw, reverse, name, err)
+
+
+def pin_bwd_torch_autograd(scan, scan_backward=None):
+    """Gradients equal autograd of a plain PyTorch loop of the same bodies
+    (f64); MAXPLUS, whose gradient only routes and halves values, equals
+    autograd in f32 exactly, ties included (maximum splits a tie evenly)."""
+    if scan_backward is None:
+        return
+    import torch
+    rng = _rng(52)
+
+    def torch_scan(body, init, x, a, reverse):
+        T = x.shape[1]
+        h = init
+        outs = [None] * T
+        for s in range(T):
+            t = T - 1 - s if reverse else s
+            if body == "TANH_DECAY":
+                h = torch.tanh(x[:, t] + a[:, t] * h)
+            elif body == "MAXPLUS":
+                h = torch.maximum(h - a[:, t], x[:, t])
+            else:
+                y = a[:, t] * h + x[:, t]
+                n = torch.linalg.vector_norm(y, dim=-1, keepdim=True)
+                h = y / torch.clamp(n, min=1.0)
+            outs[t] = h
+        return torch.stack(outs, 1)
+
+    for body in BODY_LIST:
+        for reverse in (False, True):
+            init, x, a, sa = _fd_case(body, rng)
+            init32, x32, a32 = init.astype(f32), x.astype(f32), a.astype(f32)
+            h = scan(body, init32, [x32, a32], axis=1, state_axis=sa, reverse=reverse)
+            G = rng.normal(size=h.shape).astype(f32)
+            gi, (gx, ga) = scan_backward(body, init32, [x32, a32], h, G, axis=1, state_axis=sa, reverse=reverse)
+            ts = [torch.tensor(v.astype(np.float64), requires_grad=True) for v in (init32, x32, a32)]
+            out = torch_scan(body, *ts, reverse)
+            want = torch.autograd.grad((out * torch.tensor(G.astype(np.float64))).sum(), ts)
+            for name, got, w in zip(("initial", "x", "a"), (gi, gx, ga), want):
+                w = w.numpy()
+                err = np.max(np.abs(got - w) / (1.0 + np.abs(w)))
+                assert err <= 1e-5, (body, reverse, name, err)
+    # MAXPLUS with many ties, f32, exact
+    vals = np.array([-1.0, -0.5, 0.0, 0.5, 1.0], f32)
+    costs = np.array([0.0, 0.5], f32)
+    for reverse in (False, True):
+        x = rng.choice(vals, size=(3, 9, 4)).astype(f32)
+        c = rng.choice(costs, size=(3, 9, 4)).astype(f32)
+        init = rng.choice(vals, size=(3, 4)).astype(f32)
+        h = scan("MAXPLUS", init, [x, c], axis=1, reverse=reverse)
+        G = rng.choice(np.array([-2.0, 1.0, 0.25, 3.0], f32), size=h.shape).astype(f32)
+        gi, (gx, gc) = scan_backward("MAXPLUS", init, [x, c], h, G, axis=1, reverse=reverse)
+        ts = [torch.tensor(v, requires_grad=True) for v in (init, x, c)]
+        out = torch_scan("MAXPLUS", *ts, reverse)
+        want = torch.autograd.grad((out * torch.tensor(G)).sum(), ts)
+        for name, got, w in zip(("initial", "x", "c"), (gi, gx, gc), want):
+            assert np.array_equal(got, w.numpy()), ("maxplus ties", reverse, name)
+
+
+def pin_bwd_tanh_zero_decay(scan, scan_backward=None):
+    """With zero decay every trip is tanh of its own input: no cotangent
+    reaches the initial state and dx = G (1 - h^2)."""
+    if scan_backward is None:
+        return
+    rng = _rng(53)
+    x = rng.normal(0, 1, size=(3, 8)).astype(f32)
+    a = np.zeros_like(x)
+    init = rng.normal(size=3).astype(f32)
+    h = scan("TANH_DECAY", init, [x, a], axis=1)
+    G = rng.normal(size=h.shape).astype(f32)
+    gi, (gx, ga) = scan_backward("TANH_DECAY", init, [x, a], h, G, axis=1)
+    assert np.all(gi == 0)
+    t = np.tanh(x.astype(np.float64))
+    assert np.max(np.abs(gx - G * (1 - t * t))) <= 1e-6
+
+
+def pin_bwd_normcap_linear_adjoint(scan, scan_backward=None):
+    """Inside the unit ball NORMCAP is the linear recurrence h = g h + x; its
+    adjoint is the same first-order filter run backwards over the output
+    gradient (scipy.signal.lfilter on the reversed sequence)."""
+    if scan_backward is None:
+        return
+    rng = _rng(54)
+    B, T, H, W = 2, 12, 3, 4
+    gate = rng.uniform(0.2, 0.9, size=(B, H))
+    x = (1e-3 * rng.normal(size=(B, T, H, W))).astype(f32)
+    g = np.broadcast_to(gate[:, None, :, None], (B, T, H, 1)).astype(f32)
+    init = (1e-3 * rng.normal(size=(B, H, W))).astype(f32)
+    h = scan("NORMCAP", init, [x, g], axis=1, state_axis=True)
+    G = rng.normal(size=h.shape).astype(f32)
+    gi, (gx, gg) = scan_backward("NORMCAP", init, [x, g], h, G, axis=1, state_axis=True)
+    for b in range(B):
+        for hh in range(H):
+            al = float(g[b, 0, hh, 0])
+            for w in range(W):
+                lam = scipy.signal.lfilter([1.0], [1.0, -al], G[b, ::-1, hh, w].astype(np.float64))[::-1]
+                assert np.max(np.abs(gx[b, :, hh, w] - lam)) <= 1e-5 * (1 + np.max(np.abs(lam)))
+                assert abs(gi[b, hh, w] - al * lam[0]) <= 1e-5 * (1 + abs(lam[0]))
+
+
+BWD_PINS = [pin_bwd_finite_differences, pin_bwd_torch_autograd, pin_bwd_tanh_zero_decay,
+            pin_bwd_normcap_linear_adjoint]
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and not k.startswith("pin_bwd_")]

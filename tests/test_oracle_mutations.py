@@ -35,6 +35,18 @@ MUTATIONS = [
     ("second_sequence_time_shift", "const float *at = a + ((o * T + t) * J + j) * sw[1];",
      "const float *at = a + ((o * T + (t + 1) % T) * J + j) * sw[1];", 0),
     ("gate_ignores_broadcast", "float av = at[sw[1] == 1 ? 0 : w];", "float av = at[0];", 1),
+    # backward pass
+    ("bwd_tanh_derivative_sign", "float om = 1.0f - hh;", "float om = 1.0f + hh;", 0),
+    ("bwd_tanh_dropped_decay_factor", "lam[w] = m * av;", "lam[w] = m;", 0),
+    ("bwd_tanh_decay_grad_operand", "da[w] = m * p[w];", "da[w] = m * ht[w];", 0),
+    ("bwd_maxplus_cost_sign", "da[w] = -lam[w];", "da[w] = lam[w];", 0),
+    ("bwd_maxplus_tie_not_split", "float half = lam[w] * 0.5f;", "float half = lam[w];", 0),
+    ("bwd_normcap_projection_sign", "float dlt = lam[w] - r;", "float dlt = lam[w] + r;", 0),
+    ("bwd_normcap_missing_norm", "mu[w] = dlt / nrm;", "mu[w] = dlt;", 0),
+    ("bwd_previous_state_is_own_output", "int64_t tp = reverse ? t + 1 : t - 1;", "int64_t tp = t;", 0),
+    ("bwd_drops_carried_cotangent", "for (int64_t w = 0; w < W; w++) lam[w] = lam[w] + gt[w];",
+     "for (int64_t w = 0; w < W; w++) lam[w] = gt[w];", 0),
+    ("bwd_gate_sum_first_only", "for (int64_t w = 0; w < W; w++) acc = acc + da[w];", "acc = da[0];", 0),
 ]
 
 
@@ -64,6 +76,11 @@ def test_pins_catch_mutant(mid, old, new, occ, tmp_path, oracle_mod):
     for pin in oracle_pins.ALL_PINS:
         try:
             pin(mutant.scan)
-        except (AssertionError, ValueError) as e:   # noqa: PERF203
+        except (AssertionError, ValueError):   # noqa: PERF203
+            caught.append(pin.__name__)
+    for pin in oracle_pins.BWD_PINS:
+        try:
+            pin(mutant.scan, mutant.scan_backward)
+        except (AssertionError, ValueError):   # noqa: PERF203
             caught.append(pin.__name__)
     assert caught, "no pin caught the planted mistake %s" % mid
