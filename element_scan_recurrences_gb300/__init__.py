@@ -10,7 +10,7 @@ from . import workloads  # noqa: F401  (pure Python: seeded inputs only)
 _BINDING_NAMES = {
     "scan", "scan_into", "scan_host", "lib", "LibraryMissing", "EsError", "PATHS",
     "TANH_DECAY", "NORMCAP", "MAXPLUS", "device_status", "plan", "status_string",
-    "launch_count", "set_path_override", "set_wait_limit_ns", "set_drop_tile",
+    "launch_count", "set_path_override", "set_wait_limit_ns", "set_drop_tile", "scan_backward", "plan_backward",
 }
 
 

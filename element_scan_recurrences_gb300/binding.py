@@ -26,8 +26,9 @@ PATHS = {0: "auto", 1: "empty", 2: "generic", 3: "lane_tma", 4: "time_tma", 5: "
 PATH_IDS = {v: k for k, v in PATHS.items()}
 
 # every function include/es.h declares
-EXPORTS = ("es_scan_f32", "es_plan_f32", "es_device_status", "es_last_error", "es_status_string",
-           "es_launch_count", "es_set_path_override", "es_set_wait_limit_ns", "es_set_drop_tile")
+EXPORTS = ("es_scan_f32", "es_plan_f32", "es_scan_backward_f32", "es_plan_backward_f32", "es_device_status",
+           "es_last_error", "es_status_string", "es_launch_count", "es_set_path_override", "es_set_wait_limit_ns",
+           "es_set_drop_tile")
 
 
 class LibraryMissing(ImportError):
@@ -69,6 +70,11 @@ def lib():
         L.es_scan_f32.restype = ctypes.c_int
         L.es_plan_f32.argtypes = sig + [ctypes.POINTER(PlanInfo)]
         L.es_plan_f32.restype = ctypes.c_int
+        bsig = sig[:-1] + [P, P, P, ctypes.POINTER(P)]     # ..., reverse, states, grad_out, grad_init, grad_seqs
+        L.es_scan_backward_f32.argtypes = bsig + [P]
+        L.es_scan_backward_f32.restype = ctypes.c_int
+        L.es_plan_backward_f32.argtypes = bsig + [ctypes.POINTER(PlanInfo)]
+        L.es_plan_backward_f32.restype = ctypes.c_int
         L.es_device_status.argtypes = [P]
         L.es_device_status.restype = ctypes.c_int
         L.es_last_error.argtypes = []
@@ -204,6 +210,59 @@ def scan_host(body, initial_h, seqs_h, out_h, dev_bufs, axis: int = 0, state_axi
         scan_into(body, init_d, seqs_d, out_d, axis=axis, state_axis=state_axis, reverse=reverse, stream=stream)
         out_h.copy_(out_d, non_blocking=True)
     return out_h
+
+
+def plan_backward(body, shape: Sequence[int], axis: int, state_width: int = 0, seq_widths=None,
+                  reverse: bool = False, ptrs: Optional[Sequence[int]] = None) -> dict:
+    """Validate and plan a backward call without a GPU.  ``ptrs`` are the
+    (initial, x, second, states, grad_out, grad_initial, grad_x, grad_second)
+    addresses; by default 16-byte aligned, non-overlapping stand-ins."""
+    b, shp, rank, ax, sw_, widths = _args(body, shape, axis, state_width, seq_widths)
+    if ptrs is None:
+        ptrs = [(k + 1) << 44 for k in range(8)]
+    seqs = (ctypes.c_void_p * 2)(ptrs[1], ptrs[2])
+    gseqs = (ctypes.c_void_p * 2)(ptrs[6], ptrs[7])
+    info = PlanInfo()
+    _check(lib().es_plan_backward_f32(b, ptrs[0], seqs, 2, shp, rank, ax, sw_, widths, int(bool(reverse)), ptrs[3],
+                                      ptrs[4], ptrs[5], gseqs, ctypes.byref(info)))
+    return {"O": info.O, "T": info.T, "J": info.J, "W": info.W, "seq_width": (info.seq_width[0], info.seq_width[1]),
+            "elements": info.elements, "path": PATHS[info.path], "reverse": bool(info.reverse)}
+
+
+def scan_backward(body, initial, seqs, states, grad_out, axis: int = 0, state_axis: bool = False,
+                  reverse: bool = False, grads=None, stream=None):
+    """Gradients of sum(grad_out * scan(...)) on CUDA tensors.
+
+    ``states`` is the forward output.  Returns (grad_initial, [grad_x,
+    grad_second]) shaped like initial and the two sequences; ``grads`` may
+    supply those buffers.  Asynchronous on ``stream``.
+    """
+    import torch
+    seqs = list(seqs)
+    _require_cuda_f32(initial, "initial")
+    for k, t in enumerate(seqs):
+        _require_cuda_f32(t, "sequence %d" % k)
+    _require_cuda_f32(states, "states")
+    _require_cuda_f32(grad_out, "grad_out")
+    shape = list(states.shape)
+    if list(grad_out.shape) != shape:
+        raise EsError(1, "grad_out shape %s does not match the states %s" % (list(grad_out.shape), shape))
+    if grads is None:
+        grads = (torch.empty_like(initial), [torch.empty_like(t) for t in seqs])
+    g_init, g_seqs = grads
+    for t in [g_init] + list(g_seqs):
+        _require_cuda_f32(t, "gradient buffer")
+    state_width = shape[-1] if state_axis else 0
+    seq_widths = [int(t.shape[-1]) for t in seqs] if state_axis else None
+    b, shp, rank, ax, sw_, widths = _args(body, shape, axis, state_width, seq_widths)
+    sp = (ctypes.c_void_p * 2)(seqs[0].data_ptr(), seqs[1].data_ptr())
+    gp = (ctypes.c_void_p * 2)(g_seqs[0].data_ptr(), g_seqs[1].data_ptr())
+    if stream is None:
+        stream = torch.cuda.current_stream(states.device)
+    handle = stream if isinstance(stream, int) else stream.cuda_stream
+    _check(lib().es_scan_backward_f32(b, initial.data_ptr(), sp, 2, shp, rank, ax, sw_, widths, int(bool(reverse)),
+                                      states.data_ptr(), grad_out.data_ptr(), g_init.data_ptr(), gp, handle))
+    return g_init, list(g_seqs)
 
 
 def device_status(stream=None):

@@ -73,7 +73,8 @@ struct Plan {
 const char* kSeqName[3][2] = {{"x", "a"}, {"x", "a"}, {"x", "c"}};
 
 es_status plan_impl(es_body body, const float* initial, const float* const* seqs, int n_seqs, const int64_t* shape,
-                    int rank, int axis, int state_width, const int64_t* seq_widths, const float* out, Plan* P) {
+                    int rank, int axis, int state_width, const int64_t* seq_widths, const float* out, int forced,
+                    Plan* P) {
     if (body != ES_TANH_DECAY && body != ES_NORMCAP && body != ES_MAXPLUS)
         return fail(ES_E_ARG, "es_scan_f32: unknown body id %d", static_cast<int>(body));
     if (n_seqs != 2)
@@ -159,7 +160,6 @@ es_status plan_impl(es_body body, const float* initial, const float* const* seqs
     const bool vec_ok = es::vec_tma_ok(body, O, T, P->J, W, P->sw, ptrs);
     const bool time_ok = es::time_tma_ok(body, O, T, P->J, W, P->sw, ptrs);
     const bool lane_ok = es::lane_tma_ok(body, O, T, P->J, W, P->sw, ptrs);
-    const int forced = g_path_override.load();
     if (forced == ES_PATH_AUTO) {
         P->path = vec_ok ? ES_PATH_VEC_TMA : time_ok ? ES_PATH_TIME_TMA : lane_ok ? ES_PATH_LANE_TMA : ES_PATH_GENERIC;
         return ES_OK;
@@ -169,6 +169,55 @@ es_status plan_impl(es_body body, const float* initial, const float* const* seqs
     if (!ok) return fail(ES_E_UNSUPPORTED, "es_scan_f32: the forced kernel path %d cannot serve this call", forced);
     P->path = forced;
     return ES_OK;
+}
+
+// Backward call: the forward plan for the shapes (the saved states have the
+// output shape), then the gradient buffers: present, aligned, and disjoint
+// from every input and from each other.
+es_status plan_backward_impl(es_body body, const float* initial, const float* const* seqs, int n_seqs,
+                             const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
+                             const float* states, const float* grad_out, const float* grad_initial,
+                             float* const* grad_seqs, Plan* P) {
+    // the forced-path choice happens below, once the gradient buffers are known
+    const int forced = g_path_override.load();
+    es_status st = plan_impl(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths, states,
+                             ES_PATH_AUTO, P);
+    if (st != ES_OK) return st;
+    if (P->path == ES_PATH_EMPTY) return ES_OK;
+    if (grad_seqs == nullptr || grad_out == nullptr || grad_initial == nullptr || grad_seqs[0] == nullptr ||
+        grad_seqs[1] == nullptr)
+        return fail(ES_E_ARG, "es_scan_backward_f32: null gradient pointer");
+    const void* bufs[7] = {initial, seqs[0], seqs[1], states, grad_out, grad_initial, grad_seqs[0]};
+    const void* g1 = grad_seqs[1];
+    const int64_t n[8] = {P->n_init, P->n_seq[0], P->n_seq[1], P->n_out, P->n_out, P->n_init, P->n_seq[0], P->n_seq[1]};
+    const void* all[8] = {bufs[0], bufs[1], bufs[2], bufs[3], bufs[4], bufs[5], bufs[6], g1};
+    const char* nm[8] = {"initial", "x", kSeqName[body][1], "states", "grad_out", "grad_initial", "grad_x",
+                         body == ES_MAXPLUS ? "grad_c" : "grad_a"};
+    for (int k = 0; k < 8; ++k)
+        if (reinterpret_cast<uintptr_t>(all[k]) % 4 != 0)
+            return fail(ES_E_ARG, "es_scan_backward_f32: `%s` is not 4-byte aligned", nm[k]);
+    // outputs (k >= 5) may overlap nothing else
+    for (int k = 5; k < 8; ++k) {
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(all[k]), hi = lo + static_cast<uintptr_t>(n[k]) * 4;
+        for (int q = 0; q < 8; ++q) {
+            if (q == k) continue;
+            const uintptr_t l2 = reinterpret_cast<uintptr_t>(all[q]), h2 = l2 + static_cast<uintptr_t>(n[q]) * 4;
+            if (lo < h2 && l2 < hi) return fail(ES_E_ARG, "es_scan_backward_f32: `%s` overlaps `%s`", nm[k], nm[q]);
+        }
+    }
+    const void* ptrs[4] = {initial, seqs[0], seqs[1], states};
+    bool lane_ok = es::lane_tma_ok(body, P->O, P->T, P->J, P->W, P->sw, ptrs);
+    for (int k = 4; k < 8 && lane_ok; ++k)
+        if (reinterpret_cast<uintptr_t>(all[k]) % 16 != 0) lane_ok = false;
+    if (forced == ES_PATH_AUTO) {
+        P->path = lane_ok ? ES_PATH_LANE_TMA : ES_PATH_GENERIC;
+        return ES_OK;
+    }
+    if (forced == ES_PATH_GENERIC || (forced == ES_PATH_LANE_TMA && lane_ok)) {
+        P->path = forced;
+        return ES_OK;
+    }
+    return fail(ES_E_UNSUPPORTED, "es_scan_backward_f32: the forced kernel path %d cannot serve this call", forced);
 }
 
 es_status device_state(int* dev_out, DeviceState** st_out) {
@@ -211,7 +260,8 @@ es_status es_plan_f32(es_body body, const float* initial, const float* const* se
                       const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
                       int reverse, const float* out, es_plan_info* info) {
     Plan P{};
-    es_status st = plan_impl(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths, out, &P);
+    es_status st = plan_impl(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths, out,
+                             g_path_override.load(), &P);
     if (st != ES_OK) return st;
     if (info != nullptr) {
         info->O = P.O;
@@ -231,7 +281,8 @@ es_status es_scan_f32(es_body body, const float* initial, const float* const* se
                       const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
                       int reverse, float* out, es_stream_t stream) {
     Plan P{};
-    es_status st = plan_impl(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths, out, &P);
+    es_status st = plan_impl(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths, out,
+                             g_path_override.load(), &P);
     if (st != ES_OK) return st;
     if (P.path == ES_PATH_EMPTY) return ES_OK;
 
@@ -272,6 +323,81 @@ es_status es_scan_f32(es_body body, const float* initial, const float* const* se
     if (e != cudaSuccess) {
         if (msg != nullptr) return fail(ES_E_CUDA, "es_scan_f32: %s", msg);
         return fail(ES_E_CUDA, "es_scan_f32: kernel launch: %s", cudaGetErrorString(e));
+    }
+    g_launches.fetch_add(1);
+    return ES_OK;
+}
+
+es_status es_plan_backward_f32(es_body body, const float* initial, const float* const* seqs, int n_seqs,
+                               const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
+                               int reverse, const float* states, const float* grad_out, const float* grad_initial,
+                               float* const* grad_seqs, es_plan_info* info) {
+    Plan P{};
+    es_status st = plan_backward_impl(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths,
+                                      states, grad_out, grad_initial, grad_seqs, &P);
+    if (st != ES_OK) return st;
+    if (info != nullptr) {
+        info->O = P.O;
+        info->T = P.T;
+        info->J = P.J;
+        info->W = P.W;
+        info->seq_width[0] = P.sw[0];
+        info->seq_width[1] = P.sw[1];
+        info->elements = P.n_out;
+        info->path = P.path;
+        info->reverse = reverse ? 1 : 0;
+    }
+    return ES_OK;
+}
+
+es_status es_scan_backward_f32(es_body body, const float* initial, const float* const* seqs, int n_seqs,
+                               const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
+                               int reverse, const float* states, const float* grad_out, float* grad_initial,
+                               float* const* grad_seqs, es_stream_t stream) {
+    Plan P{};
+    es_status st = plan_backward_impl(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths,
+                                      states, grad_out, grad_initial, grad_seqs, &P);
+    if (st != ES_OK) return st;
+    if (P.path == ES_PATH_EMPTY) return ES_OK;
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&dev, &ds)) != ES_OK) return st;
+    es::BackwardLaunch B{};
+    es::Launch& L = B.fwd;
+    L.body = static_cast<int>(body);
+    L.init = initial;
+    L.x = seqs[0];
+    L.a = seqs[1];
+    L.out = nullptr;
+    L.O = P.O;
+    L.T = P.T;
+    L.J = P.J;
+    L.W = P.W;
+    L.sw[0] = P.sw[0];
+    L.sw[1] = P.sw[1];
+    L.reverse = reverse ? 1 : 0;
+    L.status = ds->status;
+    L.wait_ns = g_wait_ns.load();
+    L.drop_tile = g_drop_tile.load();
+    L.stream = reinterpret_cast<cudaStream_t>(stream);
+    L.num_sms = ds->num_sms;
+    L.device = dev;
+    B.states = states;
+    B.gout = grad_out;
+    B.ginit = grad_initial;
+    B.gx = grad_seqs[0];
+    B.ga = grad_seqs[1];
+    const char* msg = nullptr;
+    cudaError_t e;
+    if (P.path == ES_PATH_GENERIC) {
+        e = es::launch_generic_bwd(B);
+    } else {
+        if ((st = encoder(&L.encode)) != ES_OK) return st;
+        e = es::launch_lane_tma_bwd(B, &msg);
+    }
+    if (e != cudaSuccess) {
+        if (msg != nullptr) return fail(ES_E_CUDA, "es_scan_backward_f32: %s", msg);
+        return fail(ES_E_CUDA, "es_scan_backward_f32: kernel launch: %s", cudaGetErrorString(e));
     }
     g_launches.fetch_add(1);
     return ES_OK;

@@ -54,6 +54,26 @@ __device__ __forceinline__ float step_pointwise(float h, float x, float s) {
     }
 }
 
+// Vector-Jacobian product of one MAXPLUS trip h = maximum(v, x), v = p - c,
+// for the state cotangent `lam`: the larger operand takes it, a tie splits
+// it evenly (the usual tie rule for maximum).  Writes dx and dc and leaves in
+// `lam` the cotangent of the previous state.
+__device__ __forceinline__ void maxplus_vjp(float v, float xv, float& lam, float& dx, float& dc) {
+    if (v > xv) {
+        dx = 0.0f;
+        dc = -lam;
+    } else if (xv > v) {
+        dx = lam;
+        dc = 0.0f;
+        lam = 0.0f;
+    } else {
+        const float half = __fmul_rn(lam, 0.5f);
+        dx = half;
+        dc = -half;
+        lam = half;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // shared-memory addresses, mbarriers, TMA
 

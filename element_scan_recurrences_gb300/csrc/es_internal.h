@@ -40,6 +40,17 @@ struct Launch {
     EncodeTiledFn encode;
 };
 
+// A backward call: the forward call's arguments plus the saved states, the
+// output gradient and the gradients to produce (same canonical layouts).
+struct BackwardLaunch {
+    Launch fwd;
+    const float* states;    // forward output [O, T, J, W]
+    const float* gout;      // dL/d states    [O, T, J, W]
+    float* ginit;           // dL/d initial   [O, J, W]
+    float* gx;              // dL/d x         [O, T, J, sw0]
+    float* ga;              // dL/d a or c    [O, T, J, sw1]
+};
+
 // Each launcher enqueues exactly one kernel; it returns cudaSuccess or the
 // launch error.  `err` receives a message for non-CUDA failures (tensor-map
 // encoding).
@@ -47,6 +58,8 @@ cudaError_t launch_generic(const Launch& L);
 cudaError_t launch_lane_tma(const Launch& L, const char** err);
 cudaError_t launch_time_tma(const Launch& L, const char** err);
 cudaError_t launch_vec_tma(const Launch& L, const char** err);
+cudaError_t launch_generic_bwd(const BackwardLaunch& B);
+cudaError_t launch_lane_tma_bwd(const BackwardLaunch& B, const char** err);
 
 // eligibility of the TMA paths (pure host logic, also used by planning)
 bool lane_tma_ok(int body, int64_t O, int64_t T, int64_t J, int64_t W, const int64_t sw[2],

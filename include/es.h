@@ -129,6 +129,47 @@ es_status es_plan_f32(es_body body, const float *initial, const float *const *se
                       int state_width, const int64_t *seq_widths, int reverse,
                       const float *out, es_plan_info *info);
 
+/*
+ * es_scan_backward_f32 -- gradients of one element scan.
+ *
+ * "Nonlinear element scans", "Precision and gradients": gradients flow to
+ * `initial` and to every sequence, and the gradient of a scan is another
+ * element scan over the same lanes in the opposite trip order that applies
+ * the body's vector-Jacobian product once a trip (a forward scan's gradient
+ * runs from the last trip to the first, a reverse scan's from the first to
+ * the last).  Per trip, with h the trip's output, p the state before it and
+ * lam the state's cotangent:
+ *   ES_TANH_DECAY  m = lam*(1 - h*h); dx = m; da = m*p; lam <- m*a
+ *   ES_MAXPLUS     the larger of p - c and x takes lam (dx = lam, or
+ *                  dc = -lam and lam passes on); a tie splits lam evenly
+ *   ES_NORMCAP     y = a*p + x is recomputed; if ||y|| <= 1 mu = lam, else
+ *                  mu = (lam - h (h . lam)) / ||y||; dx = mu; da = mu*p;
+ *                  lam <- a*mu
+ * A width-one sequence receives the sum of its gradients over the state.
+ *
+ *   body .. reverse  exactly the arguments of the forward call.
+ *   states           device f32 of `shape`: the forward output (saved states).
+ *   grad_out         device f32 of `shape`: dL/d(states).
+ *   grad_initial     device f32, the shape of `initial` (written).
+ *   grad_seqs        HOST array of n_seqs DEVICE pointers, each with the
+ *                    shape of its sequence (written).
+ * The written buffers may not overlap any input or each other (ES_E_ARG).
+ * Asynchronous on `stream`; no allocation; statuses as for es_scan_f32.
+ */
+es_status es_scan_backward_f32(es_body body, const float *initial, const float *const *seqs,
+                               int n_seqs, const int64_t *shape, int rank, int axis,
+                               int state_width, const int64_t *seq_widths, int reverse,
+                               const float *states, const float *grad_out, float *grad_initial,
+                               float *const *grad_seqs, es_stream_t stream);
+
+/* Plan of a backward call (validation and kernel path, no CUDA call). */
+es_status es_plan_backward_f32(es_body body, const float *initial, const float *const *seqs,
+                               int n_seqs, const int64_t *shape, int rank, int axis,
+                               int state_width, const int64_t *seq_widths, int reverse,
+                               const float *states, const float *grad_out,
+                               const float *grad_initial, float *const *grad_seqs,
+                               es_plan_info *info);
+
 /* Synchronise `stream`, then read and clear this device's status word.
  * Returns ES_E_TIMEOUT if a kernel since the last check gave up a bounded
  * wait (its outputs are then incomplete), ES_E_CUDA if the synchronisation

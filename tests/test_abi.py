@@ -134,3 +134,26 @@ def test_path_override_is_checked():
     finally:
         es.set_path_override("auto")
     assert _err(lambda: es.set_path_override(99))[0] == 3
+
+
+def test_backward_plans_and_rules():
+    T, N, M = es.TANH_DECAY, es.NORMCAP, es.MAXPLUS
+    assert es.plan_backward(T, [64, 4096, 1024], 1)["path"] == "lane_tma"
+    assert es.plan_backward(M, [128, 16384, 128], 1, reverse=True)["path"] == "lane_tma"
+    assert es.plan_backward(N, [32, 8192, 64, 16], 1, 16, (16, 1))["path"] == "generic"
+    assert es.plan_backward(T, [300, 64], -1)["path"] == "generic"
+    assert es.plan_backward(T, [0, 4, 8], 1, ptrs=[0] * 8)["path"] == "empty"
+    base = 1 << 40
+    ptrs = [base * (k + 1) for k in range(8)]
+    # a gradient buffer overlapping an input is refused
+    bad = list(ptrs)
+    bad[6] = ptrs[1] + 64
+    st, msg = _err(lambda: es.plan_backward(T, [4, 8, 32], 1, ptrs=bad))
+    assert st == 3 and "overlaps" in msg
+    # misaligned gradient buffer: generic path
+    odd = list(ptrs)
+    odd[7] = ptrs[7] + 4
+    assert es.plan_backward(T, [4, 8, 32], 1, ptrs=odd)["path"] == "generic"
+    # shapes are validated exactly as for the forward call
+    assert _err(lambda: es.plan_backward(N, [2, 3, 4], 1))[0] == 4
+    assert _err(lambda: es.plan_backward(T, [2, 3, 4], 5))[0] == 1

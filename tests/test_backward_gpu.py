@@ -1,0 +1,156 @@
+"""Backward pass on the GPU against the oracle's backward, element by element.
+
+Both sides get the same forward states (the oracle's, or the GPU's for the
+full-size runs), so the comparison isolates the backward arithmetic.  The
+backward uses no transcendental and the kernels follow the definition's
+operation order (NORMCAP's sqrt and division correctly rounded), so every
+gradient must match bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from element_scan_recurrences_gb300 import binding as es
+from element_scan_recurrences_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+T_, N_, M_ = wl.TANH_DECAY, wl.NORMCAP, wl.MAXPLUS
+MAXPLUS_DISTS = dict(x_dist=("uniform", -1.0, 1.0), a_dist=("uniform", 0.0, 0.1), init_dist=("uniform", -1.0, 1.0))
+NORMCAP_DISTS = dict(x_dist=("normal", 0.0, 0.5), a_dist=("uniform", 0.8, 1.0), init_dist=("normal", 0.0, 0.2))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_ready():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    es.lib()
+    oracle.build()
+    yield
+    es.set_path_override("auto")
+
+
+def _bits_equal(got, want, what):
+    got = np.asarray(got, np.float32)
+    want = np.asarray(want, np.float32)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all(), "%s: %d of %d differ; first at %s: %r vs %r" % (
+        what, int((~same).sum()), same.size, np.argwhere(~same)[0], got[~same][0], want[~same][0])
+
+
+def _check(w, reverse, path):
+    init, seqs = wl.make_inputs(w, "cpu")
+    i_np, s_np = init.numpy(), [s.numpy() for s in seqs]
+    states = oracle.scan(w.body, i_np, s_np, axis=w.axis, state_axis=w.state_axis, reverse=reverse)
+    G = np.random.default_rng(7).normal(size=states.shape).astype(np.float32)
+    want_i, want_s = oracle.scan_backward(w.body, i_np, s_np, states, G, axis=w.axis, state_axis=w.state_axis,
+                                          reverse=reverse)
+    p = es.plan_backward(w.body, w.shape, w.axis, w.shape[-1] if w.state_axis else 0,
+                         w.seq_widths if w.state_axis else None, reverse)
+    assert p["path"] == path, (w.name, p["path"])
+    dev = "cuda"
+    gi, gs = es.scan_backward(w.body, init.to(dev), [s.to(dev) for s in seqs], torch.from_numpy(states).to(dev),
+                              torch.from_numpy(G).to(dev), axis=w.axis, state_axis=w.state_axis, reverse=reverse)
+    es.device_status()
+    _bits_equal(gi.cpu().numpy(), want_i, w.name + " grad initial")
+    for k in range(2):
+        _bits_equal(gs[k].cpu().numpy(), want_s[k], "%s grad seq %d" % (w.name, k))
+
+
+CASES = [
+    ("lane_tma", wl.custom(T_, (3, 50, 200), 1, name="tanh_lane")),
+    ("lane_tma", wl.custom(T_, (2, 33, 64), 1, name="tanh_lane_T33")),
+    ("lane_tma", wl.custom(M_, (2, 37, 96), 1, name="maxplus_lane", **MAXPLUS_DISTS)),
+    ("lane_tma", wl.custom(M_, (4, 16, 160), 1, name="maxplus_lane_one_tile", **MAXPLUS_DISTS)),
+    ("lane_tma", wl.custom(T_, (300, 40), 0, name="tanh_lane_axis0")),
+    ("lane_tma", wl.custom(T_, (4, 19, 8, 16), 1, state_axis=True, seq_widths=(16, 16), name="tanh_vec_full")),
+    ("generic", wl.custom(T_, (5, 7, 3), 0, name="tanh_generic")),
+    ("generic", wl.custom(M_, (5, 7, 3), 2, name="maxplus_generic", **MAXPLUS_DISTS)),
+    ("generic", wl.custom(T_, (70, 64), -1, name="tanh_time_inner")),
+    ("generic", wl.custom(N_, (3, 30, 7, 16), 1, True, (16, 1), name="normcap_w16", **NORMCAP_DISTS)),
+    ("generic", wl.custom(N_, (2, 25, 5, 4), 1, True, (4, 4), name="normcap_w4_fullgate", **NORMCAP_DISTS)),
+    ("generic", wl.custom(N_, (2, 9, 3, 5), 1, True, (1, 5), name="normcap_bcast_x", **NORMCAP_DISTS)),
+    ("generic", wl.custom(T_, (4, 11, 6, 3), 1, True, (3, 1), name="tanh_vec_gate")),
+    ("generic", wl.custom(T_, (6, 1, 10), 1, name="tanh_T1")),
+]
+
+
+@pytest.mark.parametrize("path,w", CASES, ids=[w.name for _, w in CASES])
+@pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
+def test_backward_matches_oracle_bitwise(path, w, reverse):
+    _check(w, reverse, path)
+
+
+@pytest.mark.parametrize("path,w", [c for c in CASES if c[0] == "lane_tma"],
+                         ids=[w.name for p, w in CASES if p == "lane_tma"])
+def test_generic_backward_agrees_on_lane_shapes(path, w):
+    try:
+        es.set_path_override("generic")
+        _check(w, True, "generic")
+    finally:
+        es.set_path_override("auto")
+
+
+def test_maxplus_backward_with_ties():
+    """Tie-heavy MAXPLUS inputs: every path splits tied cotangents evenly."""
+    rng = np.random.default_rng(3)
+    shape = (2, 40, 64)
+    x = rng.choice(np.array([-1.0, 0.0, 0.5, 1.0], np.float32), size=shape).astype(np.float32)
+    c = rng.choice(np.array([0.0, 0.5], np.float32), size=shape).astype(np.float32)
+    init = rng.choice(np.array([0.0, 0.5], np.float32), size=(2, 64)).astype(np.float32)
+    for reverse in (False, True):
+        states = oracle.scan(M_, init, [x, c], axis=1, reverse=reverse)
+        G = rng.choice(np.array([1.0, -2.0, 0.75], np.float32), size=shape).astype(np.float32)
+        want_i, want_s = oracle.scan_backward(M_, init, [x, c], states, G, axis=1, reverse=reverse)
+        for path in ("lane_tma", "generic"):
+            try:
+                es.set_path_override(path)
+                gi, gs = es.scan_backward(M_, torch.from_numpy(init).cuda(),
+                                          [torch.from_numpy(x).cuda(), torch.from_numpy(c).cuda()],
+                                          torch.from_numpy(states).cuda(), torch.from_numpy(G).cuda(), axis=1,
+                                          reverse=reverse)
+                es.device_status()
+            finally:
+                es.set_path_override("auto")
+            _bits_equal(gi.cpu().numpy(), want_i, path + " ties grad initial")
+            _bits_equal(gs[0].cpu().numpy(), want_s[0], path + " ties grad x")
+            _bits_equal(gs[1].cpu().numpy(), want_s[1], path + " ties grad c")
+
+
+@pytest.mark.parametrize("name", ["tanh_decay_lanes", "maxplus_reverse", "normcap_vector"])
+def test_full_size_backward_sampled_lanes(name):
+    """Full-size backward from the GPU's own forward states, checked on sampled
+    lanes against the oracle's backward of the same lanes."""
+    w = wl.WORKLOADS[name]
+    init, seqs = wl.make_inputs(w, "cuda")
+    reverse = w.reverse[0]
+    states = es.scan(w.body, init, seqs, axis=w.axis, state_axis=w.state_axis, reverse=reverse)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(11)
+    G = torch.randn(states.shape, generator=gen, device="cuda")
+    gi, gs = es.scan_backward(w.body, init, seqs, states, G, axis=w.axis, state_axis=w.state_axis, reverse=reverse)
+    es.device_status()
+    rng = np.random.default_rng(2)
+    O = w.shape[0]
+    if w.state_axis:
+        J = w.shape[2]
+        lanes = [(0, 0), (O - 1, J - 1)] + [(int(rng.integers(O)), int(rng.integers(J))) for _ in range(30)]
+        oi = torch.tensor([l[0] for l in lanes], device="cuda")
+        ji = torch.tensor([l[1] for l in lanes], device="cuda")
+        take = lambda t: t[oi, :, ji, :].cpu().numpy()
+        takei = lambda t: t[oi, ji, :].cpu().numpy()
+    else:
+        J = w.shape[2]
+        lanes = [(0, 0), (O - 1, J - 1)] + [(int(rng.integers(O)), int(rng.integers(J))) for _ in range(30)]
+        oi = torch.tensor([l[0] for l in lanes], device="cuda")
+        ji = torch.tensor([l[1] for l in lanes], device="cuda")
+        take = lambda t: t[oi, :, ji].cpu().numpy()
+        takei = lambda t: t[oi, ji].cpu().numpy()
+    want_i, want_s = oracle.scan_backward(w.body, takei(init), [take(seqs[0]), take(seqs[1])], take(states), take(G),
+                                          axis=1, state_axis=w.state_axis, reverse=reverse)
+    _bits_equal(takei(gi), want_i, name + " grad initial")
+    _bits_equal(take(gs[0]), want_s[0], name + " grad x")
+    _bits_equal(take(gs[1]), want_s[1], name + " grad second")
+    assert bool(torch.isfinite(gs[0]).all()) and bool(torch.isfinite(gi).all())

@@ -51,3 +51,29 @@ def test_dropped_tile_times_out_then_recovers(path, w):
     out = es.scan(w.body, init, seqs, axis=w.axis, state_axis=w.state_axis, reverse=reverse)
     es.device_status()
     compare(w.body, out.cpu().numpy(), run_oracle(w, init, seqs, reverse), "after recovery " + path)
+
+
+def test_backward_dropped_tile_times_out_then_recovers():
+    w = wl.custom(wl.TANH_DECAY, (2, 400, 64), 1, name="bwd")
+    init, seqs = wl.make_inputs(w, "cuda")
+    states = es.scan(w.body, init, seqs, axis=1)
+    G = torch.ones_like(states)
+    assert es.plan_backward(w.body, w.shape, 1)["path"] == "lane_tma"
+    es.device_status()
+    es.set_wait_limit_ns(20_000_000)
+    es.set_drop_tile(2)
+    es.scan_backward(w.body, init, seqs, states, G, axis=1)
+    with pytest.raises(es.EsError) as ei:
+        es.device_status()
+    assert ei.value.status == 6
+    es.set_drop_tile(-1)
+    es.set_wait_limit_ns(2_000_000_000)
+    gi, gs = es.scan_backward(w.body, init, seqs, states, G, axis=1)
+    es.device_status()
+    try:
+        es.set_path_override("generic")
+        gi2, gs2 = es.scan_backward(w.body, init, seqs, states, G, axis=1)
+        es.device_status()
+    finally:
+        es.set_path_override("auto")
+    assert torch.equal(gi, gi2) and torch.equal(gs[0], gs2[0]) and torch.equal(gs[1], gs2[1])
