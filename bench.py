@@ -40,6 +40,7 @@ UNIT = "elements/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 PATH_KERNEL = {"lane_tma": "k_lane_tma", "time_tma": "k_time_tma", "vec_tma": "k_vec_tma", "generic": "k_generic"}
+PATH_KERNEL_BWD = {"lane_tma": "k_lane_bwd", "generic": "k_generic_bwd"}
 
 
 # ---------------------------------------------------------------------------
@@ -223,17 +224,29 @@ def take_sample(w, init, seqs, target_elems: int):
     return cpu(init), cpu(x), cpu(a), elems, desc
 
 
-def cpu_oracle_rate(w, init, seqs, budget_s: float):
+def cpu_oracle_rate(w, init, seqs, budget_s: float, backward: bool = False):
     """Time the oracle (as it stands, one thread) on a leading block of lanes
-    of the workload; return (elements/s, description, threads)."""
+    of the workload; return (elements/s, description, threads).  For the
+    backward pass the oracle's forward states of the sample are made first,
+    untimed."""
+    import numpy as np
     import oracle
     oracle.build()
 
     def run(target):
         ins, xs, as_, elems, desc = take_sample(w, init, seqs, target)
+        prep = []
+        if backward:
+            for reverse in w.reverse:
+                st = oracle.scan(w.body, ins, [xs, as_], axis=w.axis, state_axis=w.state_axis, reverse=reverse)
+                prep.append((st, np.ones_like(st)))
         t0 = time.perf_counter()
-        for reverse in w.reverse:
-            oracle.scan(w.body, ins, [xs, as_], axis=w.axis, state_axis=w.state_axis, reverse=reverse)
+        for k, reverse in enumerate(w.reverse):
+            if backward:
+                oracle.scan_backward(w.body, ins, [xs, as_], prep[k][0], prep[k][1], axis=w.axis,
+                                     state_axis=w.state_axis, reverse=reverse)
+            else:
+                oracle.scan(w.body, ins, [xs, as_], axis=w.axis, state_axis=w.state_axis, reverse=reverse)
         return time.perf_counter() - t0, elems * len(w.reverse), desc
 
     target = 1 << 20
@@ -288,12 +301,13 @@ def run_reference(args, w):
     return 0
 
 
-def config_of(w):
-    return {"workload": w.name, "body": ["TANH_DECAY", "NORMCAP", "MAXPLUS"][w.body], "shape": list(w.shape),
+def config_of(w, backward=False):
+    alg = w.backward_algorithmic_bytes() if backward else w.algorithmic_bytes()
+    return {"workload": w.name + (" (backward pass)" if backward else ""), "pass": "backward" if backward else "forward", "body": ["TANH_DECAY", "NORMCAP", "MAXPLUS"][w.body], "shape": list(w.shape),
             "axis": w.axis, "state_axis": w.state_axis, "seq_widths": list(w.seq_widths) if w.state_axis else None,
             "directions": ["reverse" if r else "forward" for r in w.reverse], "elements_per_step": w.elements *
-            len(w.reverse), "algorithmic_bytes_per_step": w.algorithmic_bytes() * len(w.reverse),
-            "l2": "no flush: inputs and outputs (%.2f GB) exceed the 129 MB L2" % (w.algorithmic_bytes() / 1e9)}
+            len(w.reverse), "algorithmic_bytes_per_step": alg * len(w.reverse),
+            "l2": "no flush: inputs and outputs (%.2f GB) exceed the 129 MB L2" % (alg / 1e9)}
 
 
 def run_ours(args, w):
@@ -316,7 +330,24 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(device)
     plans = [plan_of(es, w, r) for r in w.reverse]
 
+    backward = args.pass_ == "backward"
+    if backward:
+        # saved states and an output gradient per direction (untimed set-up)
+        gen = torch.Generator(device=device)
+        gen.manual_seed(1000 + rank)
+        for o, r in zip(outs, w.reverse):
+            es.scan_into(w.body, init, seqs, o, axis=w.axis, state_axis=w.state_axis, reverse=r, stream=stream)
+        gouts = [torch.randn(w.shape, generator=gen, device=device) for _ in w.reverse]
+        grads = [(torch.empty_like(init), [torch.empty_like(t) for t in seqs]) for _ in w.reverse]
+        plans = [es.plan_backward(w.body, w.shape, w.axis, w.shape[-1] if w.state_axis else 0,
+                                  w.seq_widths if w.state_axis else None, r) for r in w.reverse]
+
     def step():
+        if backward:
+            for o, g, gr, r in zip(outs, gouts, grads, w.reverse):
+                es.scan_backward(w.body, init, seqs, o, g, axis=w.axis, state_axis=w.state_axis, reverse=r,
+                                 grads=gr, stream=stream)
+            return
         for o, r in zip(outs, w.reverse):
             es.scan_into(w.body, init, seqs, o, axis=w.axis, state_axis=w.state_axis, reverse=r, stream=stream)
 
@@ -356,11 +387,12 @@ def run_ours(args, w):
 
     # roofline of the dominant kernel (every launch of a step is the same kernel)
     peak, peak_kind = measured_peaks()
-    alg_bytes = w.algorithmic_bytes()
+    alg_bytes = w.backward_algorithmic_bytes() if backward else w.algorithmic_bytes()
     achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
-    kernel = PATH_KERNEL.get(plans[0]["path"], plans[0]["path"])
+    kernel = (PATH_KERNEL_BWD if backward else PATH_KERNEL).get(plans[0]["path"], plans[0]["path"])
+    prof_name = w.name + ("_backward" if backward else "")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": profiled_traffic(kernel, w.name), "kernel": kernel,
+                "traffic": profiled_traffic(kernel, prof_name), "kernel": kernel,
                 "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": kernel_ms,
                 "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs, copy burst)" % peak_kind
                 if peak_kind == "measured" else "fallback 6.8 TB/s"}
@@ -375,7 +407,31 @@ def run_ours(args, w):
         d2h = sum(o.numel() for o in out_h) * 4
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
 
+        if backward:
+            states_h = [o.cpu().pin_memory() for o in outs]
+            gout_h = [g.cpu().pin_memory() for g in gouts]
+            grads_h = [(torch.empty(init.shape).pin_memory(), [torch.empty(t.shape).pin_memory() for t in seqs])
+                       for _ in w.reverse]
+            h2d = (init_h.numel() + sum(t.numel() for t in seqs_h) + 2 * w.elements) * 4
+            d2h = (init_h.numel() + sum(t.numel() for t in seqs_h)) * 4
+
         def e2e_step():
+            if backward:
+                # inputs, saved states and output gradient in; the three gradients out
+                with torch.cuda.stream(stream):
+                    for sh, gh, od, gd, gr_h, gr_d, r in zip(states_h, gout_h, outs, gouts, grads_h, grads,
+                                                              w.reverse):
+                        init.copy_(init_h, non_blocking=True)
+                        for d, hh in zip(seqs, seqs_h):
+                            d.copy_(hh, non_blocking=True)
+                        od.copy_(sh, non_blocking=True)
+                        gd.copy_(gh, non_blocking=True)
+                        es.scan_backward(w.body, init, seqs, od, gd, axis=w.axis, state_axis=w.state_axis,
+                                         reverse=r, grads=gr_d, stream=stream)
+                        gr_h[0].copy_(gr_d[0], non_blocking=True)
+                        for hh, d in zip(gr_h[1], gr_d[1]):
+                            hh.copy_(d, non_blocking=True)
+                return
             for oh, od, r in zip(out_h, outs, w.reverse):
                 es.scan_host(w.body, init_h, seqs_h, oh, (init, seqs, od), axis=w.axis, state_axis=w.state_axis,
                              reverse=r, stream=stream)
@@ -399,7 +455,7 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, desc, cores = cpu_oracle_rate(w, init, seqs, args.cpu_budget)
+        rate, desc, cores = cpu_oracle_rate(w, init, seqs, args.cpu_budget, backward=backward)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
 
     if rank == 0:
@@ -407,8 +463,8 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": region_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": dict(config_of(w), parallelism="replicas: each GPU scans its own batch" if world > 1
-                           else "single GPU", path=plans[0]["path"]),
+            "config": dict(config_of(w, backward), parallelism="replicas: each GPU scans its own batch"
+                           if world > 1 else "single GPU", path=plans[0]["path"]),
             "achieved_gbs": achieved, "hbm_frac": achieved / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clocks,
@@ -427,6 +483,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="tanh_decay_lanes")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward",
+                    help="time the scan or its backward pass (gradients from saved states)")
     ap.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

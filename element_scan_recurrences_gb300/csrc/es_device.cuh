@@ -55,23 +55,18 @@ __device__ __forceinline__ float step_pointwise(float h, float x, float s) {
 }
 
 // Vector-Jacobian product of one MAXPLUS trip h = maximum(v, x), v = p - c,
-// for the state cotangent `lam`: the larger operand takes it, a tie splits
-// it evenly (the usual tie rule for maximum).  Writes dx and dc and leaves in
-// `lam` the cotangent of the previous state.
+// for the state cotangent `lam`: the larger operand takes it, a tie (or a
+// NaN) splits it evenly (the usual tie rule for maximum).  Writes dx and dc
+// and leaves in `lam` the cotangent of the previous state.  Selects only, so
+// lanes that take different sides do not diverge.
 __device__ __forceinline__ void maxplus_vjp(float v, float xv, float& lam, float& dx, float& dc) {
-    if (v > xv) {
-        dx = 0.0f;
-        dc = -lam;
-    } else if (xv > v) {
-        dx = lam;
-        dc = 0.0f;
-        lam = 0.0f;
-    } else {
-        const float half = __fmul_rn(lam, 0.5f);
-        dx = half;
-        dc = -half;
-        lam = half;
-    }
+    const bool to_state = v > xv;
+    const bool to_x = xv > v;
+    const float half = __fmul_rn(lam, 0.5f);
+    const float keep = to_state ? lam : (to_x ? 0.0f : half);
+    dx = to_x ? lam : (to_state ? 0.0f : half);
+    dc = to_state ? -lam : (to_x ? 0.0f : -half);
+    lam = keep;
 }
 
 // ---------------------------------------------------------------------------

@@ -71,6 +71,16 @@ class Workload:
         reads = sum(math.prod(self.seq_shape(k)) for k in range(2))
         return 4 * (reads + math.prod(self.init_shape) + self.elements)
 
+    def backward_algorithmic_bytes(self) -> int:
+        """f32 bytes of one backward launch: the output gradient, the saved
+        states, the second sequence, x (not for TANH_DECAY, whose gradient
+        never reads it) and initial read; both sequence gradients and the
+        initial gradient written."""
+        n0, n1 = (math.prod(self.seq_shape(k)) for k in range(2))
+        ni = math.prod(self.init_shape)
+        reads = 2 * self.elements + n1 + ni + (0 if self.body == TANH_DECAY else n0)
+        return 4 * (reads + n0 + n1 + ni)
+
     def with_shape(self, shape: Sequence[int], name: Optional[str] = None) -> "Workload":
         """Same body, axis and distributions at another shape."""
         return dataclasses.replace(self, shape=tuple(shape), name=name or self.name + "@" + "x".join(map(str, shape)))
