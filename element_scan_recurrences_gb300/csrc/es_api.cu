@@ -206,14 +206,16 @@ es_status plan_backward_impl(es_body body, const float* initial, const float* co
         }
     }
     const void* ptrs[4] = {initial, seqs[0], seqs[1], states};
-    bool lane_ok = es::lane_tma_ok(body, P->O, P->T, P->J, P->W, P->sw, ptrs);
-    for (int k = 4; k < 8 && lane_ok; ++k)
-        if (reinterpret_cast<uintptr_t>(all[k]) % 16 != 0) lane_ok = false;
+    bool grads_aligned = true;
+    for (int k = 4; k < 8; ++k)
+        if (reinterpret_cast<uintptr_t>(all[k]) % 16 != 0) grads_aligned = false;
+    const bool lane_ok = grads_aligned && es::lane_tma_ok(body, P->O, P->T, P->J, P->W, P->sw, ptrs);
+    const bool vec_ok = grads_aligned && es::vec_tma_ok(body, P->O, P->T, P->J, P->W, P->sw, ptrs);
     if (forced == ES_PATH_AUTO) {
-        P->path = lane_ok ? ES_PATH_LANE_TMA : ES_PATH_GENERIC;
+        P->path = vec_ok ? ES_PATH_VEC_TMA : lane_ok ? ES_PATH_LANE_TMA : ES_PATH_GENERIC;
         return ES_OK;
     }
-    if (forced == ES_PATH_GENERIC || (forced == ES_PATH_LANE_TMA && lane_ok)) {
+    if (forced == ES_PATH_GENERIC || (forced == ES_PATH_LANE_TMA && lane_ok) || (forced == ES_PATH_VEC_TMA && vec_ok)) {
         P->path = forced;
         return ES_OK;
     }
@@ -393,7 +395,7 @@ es_status es_scan_backward_f32(es_body body, const float* initial, const float* 
         e = es::launch_generic_bwd(B);
     } else {
         if ((st = encoder(&L.encode)) != ES_OK) return st;
-        e = es::launch_lane_tma_bwd(B, &msg);
+        e = P.path == ES_PATH_VEC_TMA ? es::launch_vec_tma_bwd(B, &msg) : es::launch_lane_tma_bwd(B, &msg);
     }
     if (e != cudaSuccess) {
         if (msg != nullptr) return fail(ES_E_CUDA, "es_scan_backward_f32: %s", msg);
