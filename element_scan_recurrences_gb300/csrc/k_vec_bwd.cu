@@ -188,7 +188,7 @@ k_vec_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUt
         const float* hs = reinterpret_cast<const float*>(st + kOffH) + c * E;
         const float* as = reinterpret_cast<const float*>(st + kOffA) + gi;
         float* gxp = gx + static_cast<int64_t>(o) * T * row + static_cast<int64_t>(j0) * W + c * E;
-        float* gap = ga + static_cast<int64_t>(o) * T * grow + gi;
+        float* gap = ga + static_cast<int64_t>(o) * T * grow + static_cast<int64_t>(j0) * gw + gi;
 
         struct Ops {
             float g[E], x[E], h[E], p[E], a[GE];
