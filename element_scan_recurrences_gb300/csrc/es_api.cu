@@ -211,11 +211,14 @@ es_status plan_backward_impl(es_body body, const float* initial, const float* co
         if (reinterpret_cast<uintptr_t>(all[k]) % 16 != 0) grads_aligned = false;
     const bool lane_ok = grads_aligned && es::lane_tma_ok(body, P->O, P->T, P->J, P->W, P->sw, ptrs);
     const bool vec_ok = grads_aligned && es::vec_tma_ok(body, P->O, P->T, P->J, P->W, P->sw, ptrs);
+    // the time-innermost backward reads 36-trip state boxes: at least two tiles of trips
+    const bool time_ok = grads_aligned && P->T >= 64 && es::time_tma_ok(body, P->O, P->T, P->J, P->W, P->sw, ptrs);
     if (forced == ES_PATH_AUTO) {
-        P->path = vec_ok ? ES_PATH_VEC_TMA : lane_ok ? ES_PATH_LANE_TMA : ES_PATH_GENERIC;
+        P->path = vec_ok ? ES_PATH_VEC_TMA : time_ok ? ES_PATH_TIME_TMA : lane_ok ? ES_PATH_LANE_TMA : ES_PATH_GENERIC;
         return ES_OK;
     }
-    if (forced == ES_PATH_GENERIC || (forced == ES_PATH_LANE_TMA && lane_ok) || (forced == ES_PATH_VEC_TMA && vec_ok)) {
+    if (forced == ES_PATH_GENERIC || (forced == ES_PATH_LANE_TMA && lane_ok) || (forced == ES_PATH_VEC_TMA && vec_ok) ||
+        (forced == ES_PATH_TIME_TMA && time_ok)) {
         P->path = forced;
         return ES_OK;
     }
@@ -395,7 +398,9 @@ es_status es_scan_backward_f32(es_body body, const float* initial, const float* 
         e = es::launch_generic_bwd(B);
     } else {
         if ((st = encoder(&L.encode)) != ES_OK) return st;
-        e = P.path == ES_PATH_VEC_TMA ? es::launch_vec_tma_bwd(B, &msg) : es::launch_lane_tma_bwd(B, &msg);
+        if (P.path == ES_PATH_VEC_TMA) e = es::launch_vec_tma_bwd(B, &msg);
+        else if (P.path == ES_PATH_TIME_TMA) e = es::launch_time_tma_bwd(B, &msg);
+        else e = es::launch_lane_tma_bwd(B, &msg);
     }
     if (e != cudaSuccess) {
         if (msg != nullptr) return fail(ES_E_CUDA, "es_scan_backward_f32: %s", msg);

@@ -61,6 +61,7 @@ cudaError_t launch_vec_tma(const Launch& L, const char** err);
 cudaError_t launch_generic_bwd(const BackwardLaunch& B);
 cudaError_t launch_lane_tma_bwd(const BackwardLaunch& B, const char** err);
 cudaError_t launch_vec_tma_bwd(const BackwardLaunch& B, const char** err);
+cudaError_t launch_time_tma_bwd(const BackwardLaunch& B, const char** err);
 
 // eligibility of the TMA paths (pure host logic, also used by planning)
 bool lane_tma_ok(int body, int64_t O, int64_t T, int64_t J, int64_t W, const int64_t sw[2],

@@ -142,7 +142,8 @@ def test_backward_plans_and_rules():
     assert es.plan_backward(M, [128, 16384, 128], 1, reverse=True)["path"] == "lane_tma"
     assert es.plan_backward(N, [32, 8192, 64, 16], 1, 16, (16, 1))["path"] == "vec_tma"
     assert es.plan_backward(N, [3, 30, 7, 16], 1, 16, (16, 1))["path"] == "generic"
-    assert es.plan_backward(T, [300, 64], -1)["path"] == "generic"
+    assert es.plan_backward(T, [300, 64], -1)["path"] == "time_tma"
+    assert es.plan_backward(T, [300, 36], -1)["path"] == "generic"
     assert es.plan_backward(T, [0, 4, 8], 1, ptrs=[0] * 8)["path"] == "empty"
     base = 1 << 40
     ptrs = [base * (k + 1) for k in range(8)]

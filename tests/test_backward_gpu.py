@@ -79,7 +79,12 @@ CASES = [
     ("lane_tma", wl.custom(T_, (4, 19, 8, 16), 1, state_axis=True, seq_widths=(16, 16), name="tanh_vec_full")),
     ("generic", wl.custom(T_, (5, 7, 3), 0, name="tanh_generic")),
     ("generic", wl.custom(M_, (5, 7, 3), 2, name="maxplus_generic", **MAXPLUS_DISTS)),
-    ("generic", wl.custom(T_, (70, 64), -1, name="tanh_time_inner")),
+    ("time_tma", wl.custom(T_, (70, 64), -1, name="tanh_time_inner")),
+    ("time_tma", wl.custom(T_, (130, 100), -1, name="tanh_time_ragged")),
+    ("time_tma", wl.custom(M_, (70, 96), 1, name="maxplus_time", **MAXPLUS_DISTS)),
+    ("time_tma", wl.custom(M_, (65, 68), -1, name="maxplus_time_ragged", **MAXPLUS_DISTS)),
+    ("time_tma", wl.custom(T_, (2, 3, 128), 2, name="tanh_time_rank3")),
+    ("generic", wl.custom(T_, (70, 36), -1, name="tanh_time_short")),
     ("generic", wl.custom(N_, (3, 30, 7, 16), 1, True, (16, 1), name="normcap_w16", **NORMCAP_DISTS)),
     ("generic", wl.custom(N_, (2, 25, 5, 4), 1, True, (4, 4), name="normcap_w4_fullgate", **NORMCAP_DISTS)),
     ("generic", wl.custom(N_, (2, 9, 3, 5), 1, True, (1, 5), name="normcap_bcast_x", **NORMCAP_DISTS)),
@@ -147,7 +152,7 @@ def test_maxplus_backward_with_ties():
             _bits_equal(gs[1].cpu().numpy(), want_s[1], path + " ties grad c")
 
 
-@pytest.mark.parametrize("name", ["tanh_decay_lanes", "maxplus_reverse", "normcap_vector"])
+@pytest.mark.parametrize("name", ["tanh_decay_lanes", "maxplus_reverse", "normcap_vector", "tanh_decay_time_inner"])
 def test_full_size_backward_sampled_lanes(name):
     """Full-size backward from the GPU's own forward states, checked on sampled
     lanes against the oracle's backward of the same lanes."""
@@ -162,7 +167,12 @@ def test_full_size_backward_sampled_lanes(name):
     es.device_status()
     rng = np.random.default_rng(2)
     O = w.shape[0]
-    if w.state_axis:
+    if w.ax == w.rank - 1:
+        rows = [0, O - 1] + [int(rng.integers(O)) for _ in range(30)]
+        ri = torch.tensor(rows, device="cuda")
+        take = lambda t: t[ri].cpu().numpy()
+        takei = lambda t: t[ri].cpu().numpy()
+    elif w.state_axis:
         J = w.shape[2]
         lanes = [(0, 0), (O - 1, J - 1)] + [(int(rng.integers(O)), int(rng.integers(J))) for _ in range(30)]
         oi = torch.tensor([l[0] for l in lanes], device="cuda")
