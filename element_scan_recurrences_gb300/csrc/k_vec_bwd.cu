@@ -245,25 +245,66 @@ k_vec_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUt
                 if (valid && lead) __stcs(gap + static_cast<int64_t>(t0 + tt) * grow, dsum);
             }
         };
-        Ops A, B;
+        Ops A;
         if (n == kTT) {
-            if (desc) {
-                load(kTT - 1, A);
+            // Full tile in three passes so the serial chain runs alone:
+            // (1) every trip's 1/|y| and cap flag (they need only saved states
+            //     and inputs), (2) the cotangent chain, keeping each mu,
+            // (3) the gate gradients sum(mu * p) over each lane.
+            float rn[kTT];
+            bool capped[kTT];
 #pragma unroll
-                for (int tt = kTT - 1; tt >= 0; tt -= 2) {
-                    if (tt - 1 >= 0) load(tt - 1, B);
-                    trip(tt, A);
-                    if (tt - 2 >= 0) load(tt - 2, A);
-                    if (tt - 1 >= 0) trip(tt - 1, B);
+            for (int tt = 0; tt < kTT; ++tt) {
+                Ops d;
+                load(tt, d);
+                float q[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float y = __fadd_rn(__fmul_rn(d.a[GW ? e : 0], d.p[e]), d.x[e]);
+                    q[e] = __fmul_rn(y, y);
                 }
-            } else {
-                load(0, A);
+                const float nrm = __fsqrt_rn(lane_sum(local_sum(q)));
+                capped[tt] = nrm > 1.0f;
+                rn[tt] = __frcp_rn(nrm);
+            }
+            float mus[kTT][E];
+            auto chain = [&](const int tt) {
+                float g[E], h[E], q[E];
+                ld_vec<E>(g, gs + tt * kRow);
+                ld_vec<E>(h, hs + (reverse ? tt : tt + 1) * kRow);
 #pragma unroll
-                for (int tt = 0; tt < kTT; tt += 2) {
-                    if (tt + 1 < kTT) load(tt + 1, B);
-                    trip(tt, A);
-                    if (tt + 2 < kTT) load(tt + 2, A);
-                    if (tt + 1 < kTT) trip(tt + 1, B);
+                for (int e = 0; e < E; ++e) {
+                    lam[e] = __fadd_rn(lam[e], g[e]);
+                    q[e] = __fmul_rn(h[e], lam[e]);
+                }
+                const float hl = lane_sum(local_sum(q));
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float m = __fmul_rn(__fsub_rn(lam[e], __fmul_rn(h[e], hl)), rn[tt]);
+                    mus[tt][e] = capped[tt] ? m : lam[e];
+                    lam[e] = __fmul_rn(as[tt * LV * gw + (GW ? e : 0)], mus[tt][e]);
+                }
+                if (valid) st_vec<E>(gxp + static_cast<int64_t>(t0 + tt) * row, mus[tt]);
+            };
+            if (desc) {
+#pragma unroll
+                for (int tt = kTT - 1; tt >= 0; --tt) chain(tt);
+            } else {
+#pragma unroll
+                for (int tt = 0; tt < kTT; ++tt) chain(tt);
+            }
+#pragma unroll
+            for (int tt = 0; tt < kTT; ++tt) {
+                Ops d;
+                load(tt, d);
+                float da[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) da[e] = __fmul_rn(mus[tt][e], d.p[e]);
+                if constexpr (GW) {
+                    if (valid) st_vec<E>(gap + static_cast<int64_t>(t0 + tt) * grow, da);
+                } else {
+                    const float dsum = lane_sum(local_sum(da));
+                    if (valid && lead) __stcs(gap + static_cast<int64_t>(t0 + tt) * grow, dsum);
                 }
             }
         } else if (desc) {
