@@ -250,8 +250,10 @@ k_vec_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUt
             // Full tile in three passes so the serial chain runs alone:
             // (1) every trip's 1/|y| and cap flag (they need only saved states
             //     and inputs), (2) the cotangent chain, keeping each mu,
-            // (3) the gate gradients sum(mu * p) over each lane.
-            float rn[kTT];
+            // (3) the gate gradients sum(mu * p) over each lane.  The lane
+            // sums of passes 1 and 3 go level by level over all trips of the
+            // tile, so their shuffles overlap instead of forming 16 chains.
+            float rn[kTT], ssl[kTT];
             bool capped[kTT];
 #pragma unroll
             for (int tt = 0; tt < kTT; ++tt) {
@@ -263,15 +265,32 @@ k_vec_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUt
                     const float y = __fadd_rn(__fmul_rn(d.a[GW ? e : 0], d.p[e]), d.x[e]);
                     q[e] = __fmul_rn(y, y);
                 }
-                const float nrm = __fsqrt_rn(lane_sum(local_sum(q)));
+                ssl[tt] = local_sum(q);
+            }
+#pragma unroll
+            for (int off = G / 2; off >= 1; off >>= 1)
+#pragma unroll
+                for (int tt = 0; tt < kTT; ++tt) ssl[tt] = __fadd_rn(ssl[tt], __shfl_xor_sync(kMask, ssl[tt], off));
+#pragma unroll
+            for (int tt = 0; tt < kTT; ++tt) {
+                const float nrm = __fsqrt_rn(ssl[tt]);
                 capped[tt] = nrm > 1.0f;
                 rn[tt] = __frcp_rn(nrm);
             }
             float mus[kTT][E];
-            auto chain = [&](const int tt) {
+            float gn[E], hn[E];            // the next trip's operands, read one trip ahead
+            auto fetch = [&](const int tt) {
+                ld_vec<E>(gn, gs + tt * kRow);
+                ld_vec<E>(hn, hs + (reverse ? tt : tt + 1) * kRow);
+            };
+            auto chain = [&](const int tt, const int next) {
                 float g[E], h[E], q[E];
-                ld_vec<E>(g, gs + tt * kRow);
-                ld_vec<E>(h, hs + (reverse ? tt : tt + 1) * kRow);
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    g[e] = gn[e];
+                    h[e] = hn[e];
+                }
+                if (next >= 0) fetch(next);
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                     lam[e] = __fadd_rn(lam[e], g[e]);
@@ -287,12 +306,15 @@ k_vec_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUt
                 if (valid) st_vec<E>(gxp + static_cast<int64_t>(t0 + tt) * row, mus[tt]);
             };
             if (desc) {
+                fetch(kTT - 1);
 #pragma unroll
-                for (int tt = kTT - 1; tt >= 0; --tt) chain(tt);
+                for (int tt = kTT - 1; tt >= 0; --tt) chain(tt, tt - 1);
             } else {
+                fetch(0);
 #pragma unroll
-                for (int tt = 0; tt < kTT; ++tt) chain(tt);
+                for (int tt = 0; tt < kTT; ++tt) chain(tt, tt + 1 < kTT ? tt + 1 : -1);
             }
+            float dl[kTT][GW ? E : 1];
 #pragma unroll
             for (int tt = 0; tt < kTT; ++tt) {
                 Ops d;
@@ -303,9 +325,18 @@ k_vec_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUt
                 if constexpr (GW) {
                     if (valid) st_vec<E>(gap + static_cast<int64_t>(t0 + tt) * grow, da);
                 } else {
-                    const float dsum = lane_sum(local_sum(da));
-                    if (valid && lead) __stcs(gap + static_cast<int64_t>(t0 + tt) * grow, dsum);
+                    dl[tt][0] = local_sum(da);
                 }
+            }
+            if constexpr (!GW) {
+#pragma unroll
+                for (int off = G / 2; off >= 1; off >>= 1)
+#pragma unroll
+                    for (int tt = 0; tt < kTT; ++tt)
+                        dl[tt][0] = __fadd_rn(dl[tt][0], __shfl_xor_sync(kMask, dl[tt][0], off));
+#pragma unroll
+                for (int tt = 0; tt < kTT; ++tt)
+                    if (valid && lead) __stcs(gap + static_cast<int64_t>(t0 + tt) * grow, dl[tt][0]);
             }
         } else if (desc) {
             for (int tt = n - 1; tt >= 0; --tt) {
