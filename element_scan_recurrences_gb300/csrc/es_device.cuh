@@ -54,6 +54,15 @@ __device__ __forceinline__ float step_pointwise(float h, float x, float s) {
     }
 }
 
+// Hardware reciprocal square root (relative error below 2^-22; subnormal
+// inputs are flushed, which only matters where callers use the value for
+// arguments above one).
+__device__ __forceinline__ float rsqrt_approx(float v) {
+    float r;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 // Vector-Jacobian product of one MAXPLUS trip h = maximum(v, x), v = p - c,
 // for the state cotangent `lam`: the larger operand takes it, a tie (or a
 // NaN) splits it evenly (the usual tie rule for maximum).  Writes dx and dc

@@ -10,10 +10,11 @@
 //   dx = mu,  da = mu * p (summed over the state for a width-one gate),
 //   lam <- a * mu.
 // Only (h . lam) sits on the serial chain: |y| and the gate gradient depend
-// on the saved states and inputs alone.  The reciprocal of |y| is formed off
-// the chain and multiplied in (the same value as the division up to
-// rounding); sums over a lane are pairwise within a thread, then xor-shuffles
-// across the lane's W/E threads, as in the forward vector kernel.
+// on the saved states and inputs alone.  1/|y| comes from the hardware
+// reciprocal square root of |y|^2 (relative error below 2^-22) and is
+// multiplied in, the same value as the division up to rounding; sums over a
+// lane are pairwise within a thread, then xor-shuffles across the lane's W/E
+// threads, as in the forward vector kernel.
 //
 // Layout as in the forward vector kernel (x, states, grad_out, grad_x are
 // [O, T, J*W]; the gate and its gradient [O, T, J*gw]); one CTA owns
@@ -216,9 +217,9 @@ k_vec_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUt
                 y[e] = __fadd_rn(__fmul_rn(d.a[GW ? e : 0], d.p[e]), d.x[e]);
                 q[e] = __fmul_rn(y[e], y[e]);
             }
-            const float nrm = __fsqrt_rn(lane_sum(local_sum(q)));
-            const bool capped = nrm > 1.0f;
-            const float rn = __frcp_rn(nrm);
+            const float ss = lane_sum(local_sum(q));
+            const bool capped = ss > 1.0f;
+            const float rn = rsqrt_approx(ss);
             // the chain: lam -> (h . lam) -> mu -> a * mu
 #pragma unroll
             for (int e = 0; e < E; ++e) {
@@ -273,9 +274,8 @@ k_vec_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUt
                 for (int tt = 0; tt < kTT; ++tt) ssl[tt] = __fadd_rn(ssl[tt], __shfl_xor_sync(kMask, ssl[tt], off));
 #pragma unroll
             for (int tt = 0; tt < kTT; ++tt) {
-                const float nrm = __fsqrt_rn(ssl[tt]);
-                capped[tt] = nrm > 1.0f;
-                rn[tt] = __frcp_rn(nrm);
+                capped[tt] = ssl[tt] > 1.0f;
+                rn[tt] = rsqrt_approx(ssl[tt]);
             }
             float mus[kTT][E];
             float gn[E], hn[E];            // the next trip's operands, read one trip ahead
