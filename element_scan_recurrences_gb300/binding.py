@@ -21,14 +21,16 @@ MAXPLUS = 2
 _BODIES = {"TANH_DECAY": TANH_DECAY, "NORMCAP": NORMCAP, "MAXPLUS": MAXPLUS}
 
 STATUS = {0: "ES_OK", 1: "ES_E_DIM_001", 2: "ES_E_DIM_002", 3: "ES_E_ARG", 4: "ES_E_UNSUPPORTED",
-          5: "ES_E_CUDA", 6: "ES_E_TIMEOUT"}
+          5: "ES_E_CUDA", 6: "ES_E_TIMEOUT", 7: "ES_E_BODY"}
+MAX_SEQS = 8
 PATHS = {0: "auto", 1: "empty", 2: "generic", 3: "lane_tma", 4: "time_tma", 5: "vec_tma"}
 PATH_IDS = {v: k for k, v in PATHS.items()}
 
 # every function include/es.h declares
 EXPORTS = ("es_scan_f32", "es_plan_f32", "es_scan_backward_f32", "es_plan_backward_f32", "es_device_status",
            "es_last_error", "es_status_string", "es_launch_count", "es_set_path_override", "es_set_wait_limit_ns",
-           "es_set_drop_tile")
+           "es_set_drop_tile", "es_body_create", "es_body_destroy", "es_body_n_seqs", "es_scan_body_f32",
+           "es_plan_body_f32", "es_body_source", "es_body_prepare", "es_body_compile_count")
 
 
 class LibraryMissing(ImportError):
@@ -44,7 +46,7 @@ class EsError(RuntimeError):
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [("O", ctypes.c_int64), ("T", ctypes.c_int64), ("J", ctypes.c_int64), ("W", ctypes.c_int64),
-                ("seq_width", ctypes.c_int64 * 2), ("elements", ctypes.c_int64), ("path", ctypes.c_int),
+                ("seq_width", ctypes.c_int64 * MAX_SEQS), ("elements", ctypes.c_int64), ("path", ctypes.c_int),
                 ("reverse", ctypes.c_int)]
 
 
@@ -89,6 +91,24 @@ def lib():
         L.es_set_wait_limit_ns.restype = ctypes.c_int
         L.es_set_drop_tile.argtypes = [ctypes.c_int64]
         L.es_set_drop_tile.restype = ctypes.c_int
+        L.es_body_create.argtypes = [ctypes.c_char_p, ctypes.POINTER(P)]
+        L.es_body_create.restype = ctypes.c_int
+        L.es_body_destroy.argtypes = [P]
+        L.es_body_destroy.restype = ctypes.c_int
+        L.es_body_n_seqs.argtypes = [P]
+        L.es_body_n_seqs.restype = ctypes.c_int
+        bodysig = [P] + sig[1:]
+        L.es_scan_body_f32.argtypes = bodysig + [P]
+        L.es_scan_body_f32.restype = ctypes.c_int
+        L.es_plan_body_f32.argtypes = bodysig + [ctypes.POINTER(PlanInfo)]
+        L.es_plan_body_f32.restype = ctypes.c_int
+        L.es_body_source.argtypes = [P, ctypes.c_int, ctypes.c_int, i64p, ctypes.c_char_p, ctypes.c_size_t,
+                                     ctypes.POINTER(ctypes.c_size_t)]
+        L.es_body_source.restype = ctypes.c_int
+        L.es_body_prepare.argtypes = [P, ctypes.c_int, ctypes.c_int, i64p, ctypes.c_int]
+        L.es_body_prepare.restype = ctypes.c_int
+        L.es_body_compile_count.argtypes = []
+        L.es_body_compile_count.restype = ctypes.c_uint64
         _lib = L
         return L
 
@@ -288,3 +308,116 @@ def set_wait_limit_ns(ns: int) -> None:
 
 def set_drop_tile(k: int) -> None:
     _check(lib().es_set_drop_tile(int(k)))
+
+
+# ---------------------------------------------------------------------------
+# body programs
+
+
+def _widths_array(seq_widths):
+    if seq_widths is None:
+        return None
+    return (ctypes.c_int64 * max(len(seq_widths), 1))(*[int(w) for w in seq_widths])
+
+
+class Body:
+    """A body program: an element-scan body given as text in the pages'
+    lambda notation, e.g. ``(lambda (h x a) (tanh (+ x (* a h))))``.
+
+    Created (read and checked) by libes.so; each call signature is compiled
+    into a CUDA kernel at run time on first use.  Raises EsError
+    (ES_E_BODY) for a body the contract rejects.
+    """
+
+    def __init__(self, text: str):
+        handle = ctypes.c_void_p()
+        _check(lib().es_body_create(text.encode(), ctypes.byref(handle)))
+        self._h = handle
+        self.text = text
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value is not None and _lib is not None:
+            _lib.es_body_destroy(h)
+            self._h = None
+
+    @property
+    def n_seqs(self) -> int:
+        return int(lib().es_body_n_seqs(self._h))
+
+    def source(self, state_width: int = 0, seq_widths=None) -> str:
+        """The CUDA functor generated for a signature."""
+        n = self.n_seqs
+        sw = _widths_array(seq_widths)
+        need = ctypes.c_size_t()
+        _check(lib().es_body_source(self._h, int(state_width), n, sw, None, 0, ctypes.byref(need)))
+        buf = ctypes.create_string_buffer(need.value + 1)
+        _check(lib().es_body_source(self._h, int(state_width), n, sw, buf, need.value + 1, ctypes.byref(need)))
+        return buf.value.decode()
+
+    def prepare(self, state_width: int = 0, seq_widths=None, path="auto") -> None:
+        """Compile ahead of time the kernels a signature may use (no GPU needed)."""
+        p = PATH_IDS[path] if isinstance(path, str) else int(path)
+        _check(lib().es_body_prepare(self._h, int(state_width), self.n_seqs, _widths_array(seq_widths), p))
+
+    def plan(self, shape: Sequence[int], axis: int, state_width: int = 0, seq_widths=None, reverse: bool = False,
+             ptrs: Optional[Sequence[int]] = None) -> dict:
+        """Validate and plan a call without a GPU (no kernel is compiled).
+        ``ptrs`` are (initial, seq 0, ..., out); by default 16-byte aligned,
+        non-overlapping stand-ins."""
+        n = self.n_seqs
+        rank = len(shape)
+        shp = (ctypes.c_int64 * max(rank, 1))(*shape)
+        if ptrs is None:
+            ptrs = [(k + 1) << 44 for k in range(n + 2)]
+        seqs = (ctypes.c_void_p * n)(*ptrs[1:n + 1])
+        info = PlanInfo()
+        _check(lib().es_plan_body_f32(self._h, ptrs[0], seqs, n, shp, rank, int(axis), int(state_width),
+                                      _widths_array(seq_widths), int(bool(reverse)), ptrs[n + 1],
+                                      ctypes.byref(info)))
+        return {"O": info.O, "T": info.T, "J": info.J, "W": info.W,
+                "seq_width": tuple(info.seq_width[k] for k in range(n)), "elements": info.elements,
+                "path": PATHS[info.path], "reverse": bool(info.reverse)}
+
+    def scan(self, initial, seqs, axis: int = 0, state_axis: bool = False, reverse: bool = False, out=None,
+             stream=None):
+        """Run the scan on CUDA tensors; returns ``out`` (allocated if None)."""
+        import torch
+        seqs = list(seqs)
+        _require_cuda_f32(initial, "initial")
+        for k, t in enumerate(seqs):
+            _require_cuda_f32(t, "sequence %d" % k)
+        if state_axis:
+            wide = [t for t in seqs if t.shape[-1] == initial.shape[-1]]
+            shape = list((wide[0] if wide else seqs[0]).shape[:-1]) + [int(initial.shape[-1])]
+        else:
+            shape = list(seqs[0].shape)
+        if out is None:
+            out = torch.empty(shape, device=seqs[0].device, dtype=torch.float32)
+        else:
+            _require_cuda_f32(out, "out")
+            if list(out.shape) != shape:
+                raise EsError(1, "out shape %s does not match the output shape %s" % (list(out.shape), shape))
+        return self.scan_into(initial, seqs, out, axis=axis, state_axis=state_axis, reverse=reverse, stream=stream)
+
+    def scan_into(self, initial, seqs, out, axis: int = 0, state_axis: bool = False, reverse: bool = False,
+                  stream=None):
+        """es_scan_body_f32 on tensors the caller has already checked."""
+        import torch
+        shape = list(out.shape)
+        n = len(seqs)
+        rank = len(shape)
+        shp = (ctypes.c_int64 * max(rank, 1))(*shape)
+        state_width = shape[-1] if state_axis else 0
+        sw = _widths_array([int(t.shape[-1]) for t in seqs]) if state_axis else None
+        ptrs = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in seqs])
+        if stream is None:
+            stream = torch.cuda.current_stream(out.device)
+        handle = stream if isinstance(stream, int) else stream.cuda_stream
+        _check(lib().es_scan_body_f32(self._h, initial.data_ptr(), ptrs, n, shp, rank, int(axis), int(state_width),
+                                      sw, int(bool(reverse)), out.data_ptr(), handle))
+        return out
+
+
+def body_compile_count() -> int:
+    return int(lib().es_body_compile_count())

@@ -31,12 +31,7 @@ std::atomic<int64_t> g_drop_tile{-1};
 std::atomic<uint64_t> g_launches{0};
 
 constexpr int kMaxDevices = 64;
-struct DeviceState {
-    std::once_flag once;
-    cudaError_t err = cudaSuccess;
-    unsigned int* status = nullptr;
-    int num_sms = 0;
-};
+using es::DeviceState;
 DeviceState g_dev[kMaxDevices];
 
 std::once_flag g_encode_once;
@@ -80,86 +75,31 @@ es_status plan_impl(es_body body, const float* initial, const float* const* seqs
     if (n_seqs != 2)
         return fail(ES_E_ARG, "es_scan_f32: body %d takes the state and 2 sequences, got %d sequences",
                     static_cast<int>(body), n_seqs);
-    if (shape == nullptr || seqs == nullptr) return fail(ES_E_ARG, "es_scan_f32: null shape or sequence list");
-    if (rank < 1 || rank > ES_MAX_RANK)
-        return fail(ES_E_UNSUPPORTED, "es_scan_f32: rank %d outside 1..%d", rank, ES_MAX_RANK);
-    for (int d = 0; d < rank; ++d)
-        if (shape[d] < 0)
-            return fail(ES_E_DIM_001, "E-DIM-001 es_scan_f32: negative dimension in %s",
-                        shape_str(shape, rank).c_str());
-    const std::string xs = shape_str(shape, rank);
-    if (axis < -rank || axis >= rank)
-        return fail(ES_E_DIM_001, "E-DIM-001 es_scan_f32: axis %d out of range for `%s` %s f32", axis,
-                    kSeqName[body][0], xs.c_str());
-    const int ax = axis < 0 ? axis + rank : axis;
-    if (shape[ax] < 1)
-        return fail(ES_E_DIM_001, "E-DIM-001 es_scan_f32: sequence axis %d of `%s` %s f32 has length %lld; it must be "
-                    "at least one", ax, kSeqName[body][0], xs.c_str(), static_cast<long long>(shape[ax]));
-    int64_t W = 1;
-    if (state_width != 0) {
-        if (rank < 2 || ax == rank - 1)
-            return fail(ES_E_DIM_001, "E-DIM-001 es_scan_f32: the state axis is the last axis of `%s` %s f32 and "
-                        "cannot also be the sequence axis %d", kSeqName[body][0], xs.c_str(), ax);
-        if (state_width < 1 || state_width > ES_MAX_STATE || shape[rank - 1] != state_width)
-            return fail(ES_E_DIM_001, "E-DIM-001 es_scan_f32: state width %d does not fit the last axis of `%s` %s "
-                        "f32 (1..%d values)", state_width, kSeqName[body][0], xs.c_str(), ES_MAX_STATE);
-        W = state_width;
-    } else if (body == ES_NORMCAP) {
+    if (state_width == 0 && body == ES_NORMCAP && shape != nullptr && seqs != nullptr)
         return fail(ES_E_UNSUPPORTED, "es_scan_f32: NORMCAP reduces over its state and needs a state axis "
                     "(state_width >= 1); a scalar state cannot reduce");
-    }
-    int64_t O = 1, after = 1;
-    for (int d = 0; d < ax; ++d)
-        if (!mul_ok(O, shape[d], &O)) return fail(ES_E_UNSUPPORTED, "es_scan_f32: element count overflows");
-    for (int d = ax + 1; d < rank; ++d)
-        if (!mul_ok(after, shape[d], &after)) return fail(ES_E_UNSUPPORTED, "es_scan_f32: element count overflows");
-    const int64_t T = shape[ax];
-    P->O = O;
-    P->T = T;
-    P->W = W;
-    P->J = after / W;
+    es::ShapePlan S{};
+    es_status st = es::plan_shapes("es_scan_f32", kSeqName[body], initial, seqs, n_seqs, shape, rank, axis,
+                                   state_width, seq_widths, out, &S);
+    if (st != ES_OK) return st;
+    P->O = S.O;
+    P->T = S.T;
+    P->J = S.J;
+    P->W = S.W;
+    P->n_out = S.n_out;
+    P->n_init = S.n_init;
     for (int k = 0; k < 2; ++k) {
-        int64_t w = W;
-        if (seq_widths != nullptr) {
-            w = seq_widths[k];
-            const bool fits = state_width != 0 ? (w == 1 || w == W) : (w == shape[rank - 1]);
-            if (!fits)
-                return fail(ES_E_DIM_001, "E-DIM-001 es_scan_f32: `%s` %s f32 does not fit `%s` %s f32%s",
-                            kSeqName[body][k], shape_str(shape, rank, 1, w).c_str(), kSeqName[body][0], xs.c_str(),
-                            state_width != 0 ? " (its last width must be 1 or the state width)" : "");
-        }
-        P->sw[k] = state_width != 0 ? w : 1;
+        P->sw[k] = S.sw[k];
+        P->n_seq[k] = S.n_seq[k];
     }
-    int64_t rows, tmp;
-    if (!mul_ok(O, T, &rows) || !mul_ok(rows, after, &P->n_out) || !mul_ok(O, after, &P->n_init))
-        return fail(ES_E_UNSUPPORTED, "es_scan_f32: element count overflows");
-    for (int k = 0; k < 2; ++k)
-        if (!mul_ok(rows, P->J, &tmp) || !mul_ok(tmp, P->sw[k], &P->n_seq[k]))
-            return fail(ES_E_UNSUPPORTED, "es_scan_f32: element count overflows");
-    if (P->n_out > (int64_t(1) << 60)) return fail(ES_E_UNSUPPORTED, "es_scan_f32: too many elements");
-
-    if (O * P->J == 0) {      // no lanes: nothing to read or write
+    if (S.empty) {      // no lanes: nothing to read or write
         P->path = ES_PATH_EMPTY;
         return ES_OK;
     }
-    if (initial == nullptr || out == nullptr || seqs[0] == nullptr || seqs[1] == nullptr)
-        return fail(ES_E_ARG, "es_scan_f32: null data pointer");
     const void* ptrs[4] = {initial, seqs[0], seqs[1], out};
-    for (int k = 0; k < 4; ++k)
-        if (reinterpret_cast<uintptr_t>(ptrs[k]) % 4 != 0)
-            return fail(ES_E_ARG, "es_scan_f32: pointer %d is not 4-byte aligned", k);
-    // the result is a new value: `out` may not overlap any input
-    const uintptr_t olo = reinterpret_cast<uintptr_t>(out), ohi = olo + static_cast<uintptr_t>(P->n_out) * 4;
-    const int64_t nin[3] = {P->n_init, P->n_seq[0], P->n_seq[1]};
-    const char* nm[3] = {"initial", kSeqName[body][0], kSeqName[body][1]};
-    for (int k = 0; k < 3; ++k) {
-        const uintptr_t lo = reinterpret_cast<uintptr_t>(ptrs[k]), hi = lo + static_cast<uintptr_t>(nin[k]) * 4;
-        if (lo < ohi && olo < hi) return fail(ES_E_ARG, "es_scan_f32: `out` overlaps `%s`", nm[k]);
-    }
-
-    const bool vec_ok = es::vec_tma_ok(body, O, T, P->J, W, P->sw, ptrs);
-    const bool time_ok = es::time_tma_ok(body, O, T, P->J, W, P->sw, ptrs);
-    const bool lane_ok = es::lane_tma_ok(body, O, T, P->J, W, P->sw, ptrs);
+    const bool vec_ok = es::vec_tma_ok(body, S.O, S.T, S.J, S.W, P->sw, ptrs);
+    const bool time_ok = es::time_tma_ok(body, S.O, S.T, S.J, S.W, P->sw, ptrs);
+    const bool lane_ok = es::lane_tma_ok(body, S.O, S.T, S.J, S.W, P->sw, ptrs);
     if (forced == ES_PATH_AUTO) {
         P->path = vec_ok ? ES_PATH_VEC_TMA : time_ok ? ES_PATH_TIME_TMA : lane_ok ? ES_PATH_LANE_TMA : ES_PATH_GENERIC;
         return ES_OK;
@@ -259,6 +199,113 @@ es_status encoder(es::EncodeTiledFn* fn) {
 
 }  // namespace
 
+namespace es {
+
+es_status api_fail(es_status st, const char* fmt, ...) {
+    char buf[1024];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_error = buf;
+    return st;
+}
+
+es_status plan_shapes(const char* fn, const char* const* names, const float* initial, const float* const* seqs,
+                      int n_seqs, const int64_t* shape, int rank, int axis, int state_width,
+                      const int64_t* seq_widths, const float* out, ShapePlan* P) {
+    if (shape == nullptr || seqs == nullptr) return fail(ES_E_ARG, "%s: null shape or sequence list", fn);
+    if (n_seqs < 1 || n_seqs > ES_MAX_SEQS)
+        return fail(ES_E_UNSUPPORTED, "%s: %d sequences; 1..%d are supported", fn, n_seqs, ES_MAX_SEQS);
+    if (rank < 1 || rank > ES_MAX_RANK)
+        return fail(ES_E_UNSUPPORTED, "%s: rank %d outside 1..%d", fn, rank, ES_MAX_RANK);
+    for (int d = 0; d < rank; ++d)
+        if (shape[d] < 0)
+            return fail(ES_E_DIM_001, "E-DIM-001 %s: negative dimension in %s", fn, shape_str(shape, rank).c_str());
+    const std::string xs = shape_str(shape, rank);
+    if (axis < -rank || axis >= rank)
+        return fail(ES_E_DIM_001, "E-DIM-001 %s: axis %d out of range for `%s` %s f32", fn, axis, names[0],
+                    xs.c_str());
+    const int ax = axis < 0 ? axis + rank : axis;
+    if (shape[ax] < 1)
+        return fail(ES_E_DIM_001, "E-DIM-001 %s: sequence axis %d of `%s` %s f32 has length %lld; it must be "
+                    "at least one", fn, ax, names[0], xs.c_str(), static_cast<long long>(shape[ax]));
+    int64_t W = 1;
+    if (state_width != 0) {
+        if (rank < 2 || ax == rank - 1)
+            return fail(ES_E_DIM_001, "E-DIM-001 %s: the state axis is the last axis of `%s` %s f32 and "
+                        "cannot also be the sequence axis %d", fn, names[0], xs.c_str(), ax);
+        if (state_width < 1 || state_width > ES_MAX_STATE || shape[rank - 1] != state_width)
+            return fail(ES_E_DIM_001, "E-DIM-001 %s: state width %d does not fit the last axis of `%s` %s "
+                        "f32 (1..%d values)", fn, state_width, names[0], xs.c_str(), ES_MAX_STATE);
+        W = state_width;
+    }
+    int64_t O = 1, after = 1;
+    for (int d = 0; d < ax; ++d)
+        if (!mul_ok(O, shape[d], &O)) return fail(ES_E_UNSUPPORTED, "%s: element count overflows", fn);
+    for (int d = ax + 1; d < rank; ++d)
+        if (!mul_ok(after, shape[d], &after)) return fail(ES_E_UNSUPPORTED, "%s: element count overflows", fn);
+    const int64_t T = shape[ax];
+    P->O = O;
+    P->T = T;
+    P->W = W;
+    P->J = after / W;
+    P->n_seqs = n_seqs;
+    for (int k = 0; k < n_seqs; ++k) {
+        int64_t w = W;
+        if (seq_widths != nullptr) {
+            w = seq_widths[k];
+            const bool fits = state_width != 0 ? (w == 1 || w == W) : (w == shape[rank - 1]);
+            if (!fits)
+                return fail(ES_E_DIM_001, "E-DIM-001 %s: `%s` %s f32 does not fit `%s` %s f32%s", fn, names[k],
+                            shape_str(shape, rank, 1, w).c_str(), names[0], xs.c_str(),
+                            state_width != 0 ? " (its last width must be 1 or the state width)" : "");
+        }
+        P->sw[k] = state_width != 0 ? w : 1;
+    }
+    int64_t rows, tmp;
+    if (!mul_ok(O, T, &rows) || !mul_ok(rows, after, &P->n_out) || !mul_ok(O, after, &P->n_init))
+        return fail(ES_E_UNSUPPORTED, "%s: element count overflows", fn);
+    for (int k = 0; k < n_seqs; ++k)
+        if (!mul_ok(rows, P->J, &tmp) || !mul_ok(tmp, P->sw[k], &P->n_seq[k]))
+            return fail(ES_E_UNSUPPORTED, "%s: element count overflows", fn);
+    if (P->n_out > (int64_t(1) << 60)) return fail(ES_E_UNSUPPORTED, "%s: too many elements", fn);
+    P->empty = O * P->J == 0;
+    if (P->empty) return ES_OK;
+
+    if (initial == nullptr || out == nullptr) return fail(ES_E_ARG, "%s: null data pointer", fn);
+    for (int k = 0; k < n_seqs; ++k)
+        if (seqs[k] == nullptr) return fail(ES_E_ARG, "%s: null data pointer", fn);
+    if (reinterpret_cast<uintptr_t>(initial) % 4 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0)
+        return fail(ES_E_ARG, "%s: `initial` or `out` is not 4-byte aligned", fn);
+    for (int k = 0; k < n_seqs; ++k)
+        if (reinterpret_cast<uintptr_t>(seqs[k]) % 4 != 0)
+            return fail(ES_E_ARG, "%s: `%s` is not 4-byte aligned", fn, names[k]);
+    // the result is a new value: `out` may not overlap any input
+    const uintptr_t olo = reinterpret_cast<uintptr_t>(out), ohi = olo + static_cast<uintptr_t>(P->n_out) * 4;
+    for (int k = -1; k < n_seqs; ++k) {
+        const void* p = k < 0 ? static_cast<const void*>(initial) : static_cast<const void*>(seqs[k]);
+        const int64_t n = k < 0 ? P->n_init : P->n_seq[k];
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(p), hi = lo + static_cast<uintptr_t>(n) * 4;
+        if (lo < ohi && olo < hi) return fail(ES_E_ARG, "%s: `out` overlaps `%s`", fn, k < 0 ? "initial" : names[k]);
+    }
+    return ES_OK;
+}
+
+es_status api_device(int* dev, DeviceState** st) { return device_state(dev, st); }
+
+es_status api_encoder(EncodeTiledFn* fn) { return encoder(fn); }
+
+void count_launch() { g_launches.fetch_add(1); }
+
+uint64_t api_wait_ns() { return g_wait_ns.load(); }
+
+int64_t api_drop_tile() { return g_drop_tile.load(); }
+
+int api_path_override() { return g_path_override.load(); }
+
+}  // namespace es
+
 extern "C" {
 
 es_status es_plan_f32(es_body body, const float* initial, const float* const* seqs, int n_seqs,
@@ -269,6 +316,7 @@ es_status es_plan_f32(es_body body, const float* initial, const float* const* se
                              g_path_override.load(), &P);
     if (st != ES_OK) return st;
     if (info != nullptr) {
+        std::memset(info, 0, sizeof(*info));
         info->O = P.O;
         info->T = P.T;
         info->J = P.J;
@@ -342,6 +390,7 @@ es_status es_plan_backward_f32(es_body body, const float* initial, const float* 
                                       states, grad_out, grad_initial, grad_seqs, &P);
     if (st != ES_OK) return st;
     if (info != nullptr) {
+        std::memset(info, 0, sizeof(*info));
         info->O = P.O;
         info->T = P.T;
         info->J = P.J;
@@ -440,6 +489,7 @@ const char* es_status_string(es_status status) {
         case ES_E_UNSUPPORTED: return "ES_E_UNSUPPORTED";
         case ES_E_CUDA: return "ES_E_CUDA";
         case ES_E_TIMEOUT: return "ES_E_TIMEOUT";
+        case ES_E_BODY: return "ES_E_BODY";
     }
     return "ES_UNKNOWN_STATUS";
 }

@@ -1,0 +1,362 @@
+// es_body_api.cu -- the body-program entry points of the C ABI (es.h):
+// checking a call, choosing a kernel skeleton, generating the body's functor
+// and launching the kernel compiled from them at run time.
+//
+// Paths ("Nonlinear element scans": lanes in parallel, trips in sequence):
+//   * ES_PATH_LANE_TMA  scalar state (or width one), lanes innermost: the
+//     TMA time-tile pipeline of skel_lane.cuh;
+//   * ES_PATH_TIME_TMA  scalar state with the sequence axis last: TMA tiles
+//     transposed in shared memory (skel_time.cuh);
+//   * ES_PATH_VEC_TMA   vector state of 2, 4, 8 or 16 values: the TMA
+//     pipeline with a lane's state over G threads (skel_vec.cuh);
+//   * ES_PATH_GENERIC   any shape or alignment (skel_generic.cuh).
+#include <cstring>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "es.h"
+#include "es_body_compiler.h"
+#include "es_internal.h"
+#include "es_jit.h"
+#include "skel_common.cuh"
+
+struct es_body_program {
+    std::unique_ptr<es::body::Program> prog;
+    std::mutex mu;
+    // generated functor per (state width, vector state, wide mask)
+    std::map<std::tuple<int, bool, unsigned>, std::string> functors;
+};
+
+namespace es {
+namespace {
+
+using body::Error;
+
+es_status body_fail(const Error& e) { return api_fail(ES_E_BODY, "%s: %s", e.code.c_str(), e.msg.c_str()); }
+
+// the functor for a signature, generated once per program
+es_status functor_for(es_body_program* b, int W, bool vector, unsigned wide_mask, std::string* out) {
+    std::lock_guard<std::mutex> lock(b->mu);
+    const auto key = std::make_tuple(W, vector, wide_mask);
+    auto it = b->functors.find(key);
+    if (it == b->functors.end()) {
+        try {
+            it = b->functors.emplace(key, b->prog->generate(W, vector, wide_mask)).first;
+        } catch (const Error& e) {
+            return body_fail(e);
+        }
+    }
+    *out = it->second;
+    return ES_OK;
+}
+
+bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+
+struct BodyCall {
+    ShapePlan S;
+    bool vector;          // `:state-axis` given
+    unsigned wide_mask;   // bit k: sequence k is as wide as the state
+    int reverse;
+    int path;
+    std::string functor;  // the body's generated functor for this signature
+};
+
+// lanes innermost: I = J contiguous lanes per trip row, 16-byte rows
+bool body_lane_ok(const ShapePlan& S, const float* const* seqs, const float* out) {
+    if (S.W != 1) return false;
+    const int64_t I = S.J;
+    if (I < 32 || I % 4 != 0) return false;
+    if (S.O >= (int64_t(1) << 31) || S.T >= (int64_t(1) << 31) || I >= (int64_t(1) << 31)) return false;
+    if (S.O * ((I + 31) / 32) >= (int64_t(1) << 31)) return false;
+    if (!aligned16(out)) return false;
+    for (int k = 0; k < S.n_seqs; ++k)
+        if (!aligned16(seqs[k])) return false;
+    return true;
+}
+
+es_status plan_body(es_body_t body, const float* initial, const float* const* seqs, int n_seqs,
+                    const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
+                    int reverse, const float* out, BodyCall* C) {
+    if (body == nullptr || !body->prog) return api_fail(ES_E_ARG, "es_scan_body_f32: null body program");
+    const body::Program& p = *body->prog;
+    if (n_seqs != p.n_seqs())
+        return api_fail(ES_E_BODY, "arity: the body takes %d sequence(s), the call passes %d", p.n_seqs(), n_seqs);
+    static const char* const kNames[ES_MAX_SEQS] = {"seq 0", "seq 1", "seq 2", "seq 3",
+                                                    "seq 4", "seq 5", "seq 6", "seq 7"};
+    es_status st = plan_shapes("es_scan_body_f32", kNames, initial, seqs, n_seqs, shape, rank, axis, state_width,
+                               seq_widths, out, &C->S);
+    if (st != ES_OK) return st;
+    C->vector = state_width != 0;
+    C->reverse = reverse ? 1 : 0;
+    C->wide_mask = 0;
+    for (int k = 0; k < n_seqs; ++k)
+        if (C->S.sw[k] == C->S.W) C->wide_mask |= 1u << k;
+    // the body must fit the signature (checked before any path choice)
+    if ((st = functor_for(body, static_cast<int>(C->S.W), C->vector, C->wide_mask, &C->functor)) != ES_OK)
+        return st;
+    if (C->S.empty) {
+        C->path = ES_PATH_EMPTY;
+        return ES_OK;
+    }
+    const bool lane_ok = body_lane_ok(C->S, seqs, out);
+    const int forced = api_path_override();
+    if (forced == ES_PATH_AUTO) {
+        C->path = lane_ok ? ES_PATH_LANE_TMA : ES_PATH_GENERIC;
+        return ES_OK;
+    }
+    if (forced == ES_PATH_GENERIC || (forced == ES_PATH_LANE_TMA && lane_ok)) {
+        C->path = forced;
+        return ES_OK;
+    }
+    return api_fail(ES_E_UNSUPPORTED, "es_scan_body_f32: the forced kernel path %d cannot serve this call", forced);
+}
+
+// ---------------------------------------------------------------------------
+// launchers (one kernel each)
+
+struct BodyLaunch {
+    const BodyCall* C;
+    const float* init;
+    const float* const* seqs;
+    float* out;
+    cudaStream_t stream;
+    DeviceState* dev;
+    EncodeTiledFn encode;
+};
+
+// Kernel sources: a skeleton header, the functor, and the instantiation to
+// compile (template arguments of the launch configuration).
+struct KernelText {
+    std::string source;
+    std::string name;
+};
+
+KernelText generic_text(const std::string& functor, int W) {
+    return {"#include \"skel_generic.cuh\"\n" + functor, "&es::k_body_generic<EsBody, " + std::to_string(W) + ">"};
+}
+
+KernelText lane_text(const std::string& functor, int LI, int TT) {
+    return {"#include \"skel_lane.cuh\"\n" + functor,
+            "&es::k_body_lane<EsBody, " + std::to_string(LI) + ", " + std::to_string(TT) + ">"};
+}
+
+// trips per tile of the lanes-innermost skeleton: every sequence's tile sits
+// in registers
+int lane_trips(int n_seqs) { return n_seqs <= 2 ? 32 : n_seqs <= 4 ? 16 : 8; }
+
+bool launch_body_generic(const BodyLaunch& L, std::string* err) {
+    const BodyCall& C = *L.C;
+    JitKernel k;
+    const KernelText kt = generic_text(C.functor, static_cast<int>(C.S.W));
+    if (!jit_kernel(kt.source, kt.name, &k, err)) return false;
+    SeqPtrs sp{};
+    for (int q = 0; q < C.S.n_seqs; ++q) sp.p[q] = L.seqs[q];
+    const int64_t lanes = C.S.O * C.S.J;
+    const int threads = 128;
+    const int64_t blocks = (lanes + threads - 1) / threads;
+    if (blocks > 0x7fffffffLL) {
+        *err = "too many lanes for one launch";
+        return false;
+    }
+    const float* init = L.init;
+    float* out = L.out;
+    int64_t O = C.S.O, T = C.S.T, J = C.S.J;
+    int reverse = C.reverse;
+    void* args[] = {&sp, &init, &out, &O, &T, &J, &reverse};
+    return jit_launch(k, static_cast<unsigned>(blocks), threads, 0, L.stream, args, err);
+}
+
+// a 3-D map over [O, T, I] with box {LI, TT, 1}
+bool encode_rows(EncodeTiledFn encode, CUtensorMap* m, const float* base, int64_t O, int64_t T, int64_t I, int LI,
+                 int TT) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(I), static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(O)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(I) * 4, static_cast<cuuint64_t>(I) * T * 4};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(LI), static_cast<cuuint32_t>(TT), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool launch_body_lane(const BodyLaunch& L, std::string* err) {
+    const BodyCall& C = *L.C;
+    const int NS = C.S.n_seqs;
+    const int64_t I = C.S.J;
+    // lanes per CTA: the widest tile that still puts a CTA on most SMs
+    int LI = 32;
+    for (int cand : {128, 64}) {
+        if (I >= cand && 5 * C.S.O * ((I + cand - 1) / cand) >= 4LL * L.dev->num_sms) {
+            LI = cand;
+            break;
+        }
+    }
+    const int TT = lane_trips(NS);
+    // about 96 trips in flight, within 200 KB of shared memory
+    const int64_t stage_bytes = static_cast<int64_t>(NS) * TT * LI * 4;
+    int stages = 96 / TT;
+    if (stages > 8) stages = 8;
+    while (stages > 2 && stages * stage_bytes > 200 * 1024) --stages;
+    const int64_t tiles_i = (I + LI - 1) / LI;
+    alignas(64) CUtensorMap maps[ES_MAX_SEQS];
+    for (int q = 0; q < NS; ++q) {
+        if (!encode_rows(L.encode, &maps[q], L.seqs[q], C.S.O, C.S.T, I, LI, TT)) {
+            *err = "cuTensorMapEncodeTiled failed for a lane-innermost tile map";
+            return false;
+        }
+    }
+    JitKernel k;
+    const KernelText kt = lane_text(C.functor, LI, TT);
+    if (!jit_kernel(kt.source, kt.name, &k, err)) return false;
+    const float* init = L.init;
+    float* out = L.out;
+    int T = static_cast<int>(C.S.T), Ii = static_cast<int>(I), ti = static_cast<int>(tiles_i);
+    int reverse = C.reverse;
+    unsigned int* status = L.dev->status;
+    uint64_t wait_ns = api_wait_ns();
+    int64_t drop = api_drop_tile();
+    void* args[] = {maps, &init, &out, &T, &Ii, &ti, &stages, &reverse, &status, &wait_ns, &drop};
+    const size_t smem = static_cast<size_t>(stages * stage_bytes) + 1024;
+    return jit_launch(k, static_cast<unsigned>(C.S.O * tiles_i), 32 + LI, smem, L.stream, args, err);
+}
+
+// the functor of a signature given by widths (no shapes)
+es_status signature_functor(const char* fn, es_body_t body, int state_width, int n_seqs, const int64_t* seq_widths,
+                            std::string* functor, int* W_out) {
+    if (body == nullptr || !body->prog) return api_fail(ES_E_ARG, "%s: null body program", fn);
+    if (n_seqs != body->prog->n_seqs())
+        return api_fail(ES_E_BODY, "arity: the body takes %d sequence(s), not %d", body->prog->n_seqs(), n_seqs);
+    if (state_width < 0 || state_width > ES_MAX_STATE)
+        return api_fail(ES_E_DIM_001, "E-DIM-001 %s: state width %d outside 0..%d", fn, state_width, ES_MAX_STATE);
+    const int W = state_width == 0 ? 1 : state_width;
+    unsigned mask = 0;
+    for (int k = 0; k < n_seqs; ++k) {
+        const int64_t w = seq_widths == nullptr ? W : seq_widths[k];
+        if (state_width != 0 && w != 1 && w != W)
+            return api_fail(ES_E_DIM_001, "E-DIM-001 %s: sequence %d has width %lld", fn, k,
+                            static_cast<long long>(w));
+        if (w == W) mask |= 1u << k;
+    }
+    *W_out = W;
+    return functor_for(body, W, state_width != 0, mask, functor);
+}
+
+void fill_info(const BodyCall& C, es_plan_info* info) {
+    if (info == nullptr) return;
+    std::memset(info, 0, sizeof(*info));
+    info->O = C.S.O;
+    info->T = C.S.T;
+    info->J = C.S.J;
+    info->W = C.S.W;
+    for (int k = 0; k < C.S.n_seqs; ++k) info->seq_width[k] = C.S.sw[k];
+    info->elements = C.S.n_out;
+    info->path = C.path;
+    info->reverse = C.reverse;
+}
+
+}  // namespace
+}  // namespace es
+
+extern "C" {
+
+es_status es_body_create(const char* text, es_body_t* body) {
+    if (text == nullptr || body == nullptr) return es::api_fail(ES_E_ARG, "es_body_create: null argument");
+    *body = nullptr;
+    try {
+        std::unique_ptr<es_body_program> b(new es_body_program());
+        b->prog = es::body::Program::parse(text);
+        *body = b.release();
+    } catch (const es::body::Error& e) {
+        return es::body_fail(e);
+    } catch (const std::bad_alloc&) {
+        return es::api_fail(ES_E_ARG, "es_body_create: out of host memory");
+    }
+    return ES_OK;
+}
+
+es_status es_body_destroy(es_body_t body) {
+    delete body;
+    return ES_OK;
+}
+
+int es_body_n_seqs(es_body_t body) { return body != nullptr && body->prog ? body->prog->n_seqs() : -1; }
+
+es_status es_body_source(es_body_t body, int state_width, int n_seqs, const int64_t* seq_widths, char* buf,
+                         size_t cap, size_t* needed) {
+    std::string src;
+    int W = 1;
+    es_status st = es::signature_functor("es_body_source", body, state_width, n_seqs, seq_widths, &src, &W);
+    if (st != ES_OK) return st;
+    if (needed != nullptr) *needed = src.size();
+    if (buf != nullptr && cap > 0) {
+        const size_t n = src.size() < cap - 1 ? src.size() : cap - 1;
+        std::memcpy(buf, src.data(), n);
+        buf[n] = '\0';
+    }
+    return ES_OK;
+}
+
+es_status es_body_prepare(es_body_t body, int state_width, int n_seqs, const int64_t* seq_widths, int path) {
+    std::string functor;
+    int W = 1;
+    es_status st = es::signature_functor("es_body_prepare", body, state_width, n_seqs, seq_widths, &functor, &W);
+    if (st != ES_OK) return st;
+    std::vector<es::KernelText> todo;
+    if (path == ES_PATH_AUTO || path == ES_PATH_GENERIC) todo.push_back(es::generic_text(functor, W));
+    if ((path == ES_PATH_AUTO || path == ES_PATH_LANE_TMA) && W == 1)
+        for (int LI : {32, 64, 128}) todo.push_back(es::lane_text(functor, LI, es::lane_trips(n_seqs)));
+    if (todo.empty())
+        return es::api_fail(ES_E_UNSUPPORTED, "es_body_prepare: path %d cannot serve this signature", path);
+    for (const es::KernelText& kt : todo) {
+        std::string err;
+        if (!es::jit_compile(kt.source, kt.name, &err)) return es::api_fail(ES_E_CUDA, "es_body_prepare: %s", err.c_str());
+    }
+    return ES_OK;
+}
+
+uint64_t es_body_compile_count(void) { return es::jit_compile_count(); }
+
+es_status es_plan_body_f32(es_body_t body, const float* initial, const float* const* seqs, int n_seqs,
+                           const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
+                           int reverse, const float* out, es_plan_info* info) {
+    es::BodyCall C{};
+    es_status st = es::plan_body(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths, reverse,
+                                 out, &C);
+    if (st != ES_OK) return st;
+    es::fill_info(C, info);
+    return ES_OK;
+}
+
+es_status es_scan_body_f32(es_body_t body, const float* initial, const float* const* seqs, int n_seqs,
+                           const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
+                           int reverse, float* out, es_stream_t stream) {
+    es::BodyCall C{};
+    es_status st = es::plan_body(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths, reverse,
+                                 out, &C);
+    if (st != ES_OK) return st;
+    if (C.path == ES_PATH_EMPTY) return ES_OK;
+    es::BodyLaunch L{};
+    L.C = &C;
+    L.init = initial;
+    L.seqs = seqs;
+    L.out = out;
+    L.stream = reinterpret_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if ((st = es::api_device(&dev, &L.dev)) != ES_OK) return st;
+    std::string err;
+    bool ok;
+    if (C.path == ES_PATH_GENERIC) {
+        ok = es::launch_body_generic(L, &err);
+    } else {
+        if ((st = es::api_encoder(&L.encode)) != ES_OK) return st;
+        ok = es::launch_body_lane(L, &err);
+    }
+    if (!ok) return es::api_fail(ES_E_CUDA, "es_scan_body_f32: %s", err.c_str());
+    es::count_launch();
+    return ES_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,547 @@
+// es_body_compiler.cu -- translate an element-scan body given as text into a
+// CUDA functor (host code).
+//
+// What a body may contain: "Nonlinear element scans", "Arguments and body"
+// (pointwise arithmetic, transcendental functions, comparisons, `where`,
+// scalar constants, boolean intermediates, casts between f32 and bool; with
+// `:state-axis` scalars and vectors of 1..16 values, `sum` and `max` reducing
+// a vector, a one-value vector broadcasting against the state; a scalar
+// state's body cannot reduce).  Operation names and the overloaded
+// arithmetic: "Tensor operations" ("Shapes, dtypes, broadcasting" and
+// "Operations": plain numbers mixed with a tensor become constants, plain
+// numbers at the front of an n-ary `*` fold first).
+//
+// The body is traced once, as the pages describe: every operation on a
+// tensor value appends one statement to the functor, every operation on
+// plain numbers is done here in double precision, and a plain number meeting
+// a tensor becomes the f32 constant nearest to it.  Each tensor statement is
+// one f32 operation rounded to nearest: + - * / and sqrt are the IEEE
+// operations (the _rn intrinsics, which also keep a multiply and an add from
+// fusing), exp, log, tanh, sin, cos, acos, asin, atan2, pow and rsqrt are
+// CUDA's f32 functions, `maximum` / `minimum` are IEEE 754-2019 (PTX
+// max.NaN / min.NaN), comparisons are IEEE (false on NaN except !=).
+// Readings of what the pages leave open: `max` with one tensor argument is the
+// reduction (the elementwise pair is `maximum`); the comparisons are
+// < <= > >= = !=; `and`, `or`, `not` combine booleans; (cast x :bool) is
+// x != 0; `let` binds in order; a `sum` adds a thread's values in state order
+// and then the lane's threads pairwise.
+#include "es_body_compiler.h"
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <sstream>
+
+namespace es {
+namespace body {
+namespace {
+
+[[noreturn]] void fail(const char* code, const std::string& msg) { throw Error{code, msg}; }
+
+// ---------------------------------------------------------------------------
+// reader
+
+bool is_delim(char c) { return c == '(' || c == ')' || c == '[' || c == ']' || c == ';' || std::isspace((unsigned char)c); }
+
+// [+-]? (digits [. digits*] | . digits) ([eE] [+-]? digits)?
+bool parse_number(const std::string& t, double* out) {
+    size_t i = 0;
+    if (i < t.size() && (t[i] == '+' || t[i] == '-')) ++i;
+    size_t int_digits = 0, frac_digits = 0;
+    while (i < t.size() && std::isdigit((unsigned char)t[i])) ++i, ++int_digits;
+    if (i < t.size() && t[i] == '.') {
+        ++i;
+        while (i < t.size() && std::isdigit((unsigned char)t[i])) ++i, ++frac_digits;
+    }
+    if (int_digits == 0 && frac_digits == 0) return false;
+    if (i < t.size() && (t[i] == 'e' || t[i] == 'E')) {
+        ++i;
+        if (i < t.size() && (t[i] == '+' || t[i] == '-')) ++i;
+        size_t exp_digits = 0;
+        while (i < t.size() && std::isdigit((unsigned char)t[i])) ++i, ++exp_digits;
+        if (exp_digits == 0) return false;
+    }
+    if (i != t.size()) return false;
+    *out = std::strtod(t.c_str(), nullptr);   // correctly rounded to double
+    return true;
+}
+
+class Reader {
+public:
+    explicit Reader(const std::string& text) : text_(text) {}
+
+    Form read_all() {
+        Form f = read();
+        skip();
+        if (pos_ != text_.size()) fail("parse", "text after the body");
+        return f;
+    }
+
+private:
+    void skip() {
+        while (pos_ < text_.size()) {
+            if (std::isspace((unsigned char)text_[pos_])) {
+                ++pos_;
+            } else if (text_[pos_] == ';') {
+                while (pos_ < text_.size() && text_[pos_] != '\n') ++pos_;
+            } else {
+                break;
+            }
+        }
+    }
+
+    Form read() {
+        skip();
+        if (pos_ >= text_.size()) fail("parse", "unexpected end of body text");
+        const char c = text_[pos_];
+        if (c == '(' || c == '[') {
+            const char close = c == '(' ? ')' : ']';
+            ++pos_;
+            Form f;
+            f.kind = c == '(' ? Form::kList : Form::kVec;
+            for (;;) {
+                skip();
+                if (pos_ >= text_.size()) fail("parse", std::string("missing '") + close + "'");
+                if (text_[pos_] == close) {
+                    ++pos_;
+                    return f;
+                }
+                if (text_[pos_] == ')' || text_[pos_] == ']')
+                    fail("parse", std::string("mismatched '") + text_[pos_] + "'");
+                f.items.push_back(read());
+            }
+        }
+        if (c == ')' || c == ']') fail("parse", std::string("unexpected '") + c + "'");
+        const size_t start = pos_;
+        while (pos_ < text_.size() && !is_delim(text_[pos_])) ++pos_;
+        const std::string tok = text_.substr(start, pos_ - start);
+        Form f;
+        if (parse_number(tok, &f.num)) {
+            f.kind = Form::kNum;
+        } else if (tok == "true" || tok == "false") {
+            f.kind = Form::kBool;
+            f.b = tok == "true";
+        } else if (tok[0] == ':') {
+            f.kind = Form::kKw;
+            f.s = tok;
+        } else {
+            f.kind = Form::kSym;
+            f.s = tok;
+        }
+        return f;
+    }
+
+    const std::string& text_;
+    size_t pos_ = 0;
+};
+
+// ---------------------------------------------------------------------------
+// values while tracing
+
+struct Val {
+    enum Kind { kNumber, kBoolConst, kTensor } kind = kNumber;
+    double num = 0.0;
+    bool b = false;
+    std::string name;     // tensor: an expression naming it (array name if wide)
+    bool is_bool = false; // tensor dtype: bool or f32
+    bool wide = false;    // tensor width: the state's W (array of E) or one
+};
+
+Val number(double v) {
+    Val r;
+    r.kind = Val::kNumber;
+    r.num = v;
+    return r;
+}
+
+Val bool_const(bool v) {
+    Val r;
+    r.kind = Val::kBoolConst;
+    r.b = v;
+    return r;
+}
+
+std::string f32_literal(double v) {
+    const float f = static_cast<float>(v);   // round to nearest f32
+    uint32_t bits;
+    std::memcpy(&bits, &f, 4);
+    char buf[64];
+    std::snprintf(buf, sizeof(buf), "__uint_as_float(0x%08xu)", bits);
+    return buf;
+}
+
+double num_max(double a, double b) { return (a >= b || std::isnan(a)) ? a : b; }
+
+using Env = std::map<std::string, Val>;
+
+class Tracer {
+public:
+    Tracer(int W, bool vector) : W_(W), vector_(vector) {}
+
+    std::string code;
+
+    Val eval(const Form& f, const Env& env);
+
+    std::string ref(const Val& v) const {
+        if (v.kind == Val::kNumber) return f32_literal(v.num);
+        if (v.kind == Val::kBoolConst) return v.b ? "true" : "false";
+        return v.wide ? v.name + "[e]" : v.name;
+    }
+
+    // a plain number meeting a tensor: an f32 (or bool) constant
+    Val tensor(const Val& v) const {
+        if (v.kind == Val::kTensor) return v;
+        Val r;
+        r.kind = Val::kTensor;
+        r.is_bool = v.kind == Val::kBoolConst;
+        r.name = ref(v);
+        r.wide = false;
+        return r;
+    }
+
+    Val f32(const Val& v, const std::string& what) const {
+        Val t = tensor(v);
+        if (t.is_bool) fail("E-DIM-002", what + " wants f32, got bool");
+        return t;
+    }
+
+    Val boolean(const Val& v, const std::string& what) const {
+        Val t = tensor(v);
+        if (!t.is_bool) fail("E-DIM-002", what + " wants bool, got f32");
+        return t;
+    }
+
+    Val emit(bool is_bool, bool wide, const std::string& expr) {
+        Val r;
+        r.kind = Val::kTensor;
+        r.is_bool = is_bool;
+        r.wide = wide;
+        r.name = "v" + std::to_string(next_++);
+        const char* type = is_bool ? "bool" : "float";
+        if (wide) {
+            code += std::string("        ") + type + " " + r.name + "[E];\n#pragma unroll\n        for (int e = 0; e < E; ++e) " +
+                    r.name + "[e] = " + expr + ";\n";
+        } else {
+            code += std::string("        const ") + type + " " + r.name + " = " + expr + ";\n";
+        }
+        return r;
+    }
+
+    int W() const { return W_; }
+
+private:
+    Val reduce(const std::string& op, const std::vector<Val>& pos, const std::map<std::string, Form>& kws);
+    int W_;
+    bool vector_;
+    int next_ = 0;
+};
+
+const char* kArith[][2] = {{"+", "__fadd_rn"}, {"-", "__fsub_rn"}, {"*", "__fmul_rn"}, {"/", "__fdiv_rn"}};
+const char* kCompare[][2] = {{"<", "<"}, {"<=", "<="}, {">", ">"}, {">=", ">="}, {"=", "=="}, {"!=", "!="}};
+const char* kUnary[][2] = {{"exp", "expf"},   {"log", "logf"},   {"tanh", "tanhf"}, {"sin", "sinf"},
+                           {"cos", "cosf"},   {"acos", "acosf"}, {"asin", "asinf"}, {"rsqrt", "rsqrtf"},
+                           {"abs", "fabsf"},  {"sqrt", "__fsqrt_rn"}};
+const char* kBinaryFn[][2] = {{"pow", "powf"},
+                              {"atan2", "atan2f"},
+                              {"maximum", "es::ieee_maximum"},
+                              {"minimum", "es::ieee_minimum"}};
+
+template <size_t N>
+const char* lookup(const char* (&table)[N][2], const std::string& key) {
+    for (size_t i = 0; i < N; ++i)
+        if (key == table[i][0]) return table[i][1];
+    return nullptr;
+}
+
+double number_arith(const std::string& op, double a, double b) {
+    if (op == "+") return a + b;
+    if (op == "-") return a - b;
+    if (op == "*") return a * b;
+    return a / b;
+}
+
+bool number_compare(const std::string& op, double a, double b) {
+    if (op == "<") return a < b;
+    if (op == "<=") return a <= b;
+    if (op == ">") return a > b;
+    if (op == ">=") return a >= b;
+    if (op == "=") return a == b;
+    return a != b;
+}
+
+Val Tracer::reduce(const std::string& op, const std::vector<Val>& pos, const std::map<std::string, Form>& kws) {
+    if (pos.size() != 1) {
+        if (op == "max") fail("arity", "(max ...) over tensors takes one value; the elementwise pair is maximum");
+        fail("arity", "(sum ...) over tensors takes one value");
+    }
+    if (!vector_) fail("reduce", "a scalar state's body cannot reduce");
+    bool empty_axes = false;
+    auto ax = kws.find(":axes");
+    if (ax != kws.end()) {
+        const Form& a = ax->second;
+        if (a.kind != Form::kVec) fail("E-DIM-001", ":axes takes a vector of integers");
+        std::vector<long> norm;
+        for (const Form& d : a.items) {
+            if (d.kind != Form::kNum || d.num != std::floor(d.num)) fail("E-DIM-001", ":axes takes a vector of integers");
+            const long n = static_cast<long>(d.num) < 0 ? static_cast<long>(d.num) + 1 : static_cast<long>(d.num);
+            if (n != 0) fail("E-DIM-001", "a body value has one axis");
+            for (long m : norm)
+                if (m == n) fail("E-DIM-001", "an axis is listed twice in :axes");
+            norm.push_back(n);
+        }
+        empty_axes = a.items.empty();
+    }
+    auto kd = kws.find(":keepdims");
+    if (kd != kws.end() && kd->second.kind != Form::kBool) fail("arity", ":keepdims takes true or false");
+    Val t = f32(pos[0], "(" + op + " ...)");
+    // a one-value vector (or an empty axis list) reduces to itself
+    if (empty_axes || !t.wide) return t;
+    return emit(false, false, std::string(op == "sum" ? "es::group_sum" : "es::group_max") + "<E, G>(" + t.name +
+                                  ", mask)");
+}
+
+Val Tracer::eval(const Form& f, const Env& env) {
+    switch (f.kind) {
+        case Form::kNum: return number(f.num);
+        case Form::kBool: return bool_const(f.b);
+        case Form::kSym: {
+            auto it = env.find(f.s);
+            if (it == env.end()) fail("E-SCAN-001", "`" + f.s + "` is not an argument of the body or a let binding");
+            return it->second;
+        }
+        case Form::kKw:
+        case Form::kVec: fail("parse", "a keyword or [vector] is not a value here");
+        case Form::kList: break;
+    }
+    if (f.items.empty()) fail("parse", "empty form");
+    if (f.items[0].kind != Form::kSym) fail("parse", "a form starts with an operation name");
+    const std::string& head = f.items[0].s;
+    const std::vector<Form> args(f.items.begin() + 1, f.items.end());
+
+    if (head == "let") {
+        if (args.size() < 2 || args[0].kind != Form::kList) fail("arity", "(let ((name value) ...) body)");
+        Env inner = env;
+        for (const Form& b : args[0].items) {
+            if (b.kind != Form::kList || b.items.size() != 2 || b.items[0].kind != Form::kSym)
+                fail("arity", "a let binding is (name value)");
+            inner[b.items[0].s] = eval(b.items[1], inner);
+        }
+        Val r;
+        for (size_t i = 1; i < args.size(); ++i) r = eval(args[i], inner);
+        return r;
+    }
+
+    if (head == "sum" || head == "max") {
+        std::vector<Val> pos;
+        std::map<std::string, Form> kws;
+        for (size_t i = 0; i < args.size(); ++i) {
+            if (args[i].kind == Form::kKw) {
+                if (args[i].s != ":axes" && args[i].s != ":keepdims") fail("arity", "unknown keyword " + args[i].s);
+                if (i + 1 >= args.size()) fail("arity", "keyword " + args[i].s + " has no value");
+                kws[args[i].s] = args[i + 1];
+                ++i;
+            } else {
+                pos.push_back(eval(args[i], env));
+            }
+        }
+        if (pos.empty()) fail("arity", "(" + head + ") needs a value");
+        bool all_numbers = kws.empty();
+        for (const Val& v : pos) all_numbers = all_numbers && v.kind == Val::kNumber;
+        if (all_numbers) {   // plain numbers: their sum or their maximum
+            double r = pos[0].num;
+            for (size_t i = 1; i < pos.size(); ++i) r = head == "sum" ? r + pos[i].num : num_max(r, pos[i].num);
+            return number(r);
+        }
+        return reduce(head, pos, kws);
+    }
+
+    if (head == "cast") {
+        if (args.size() != 2 || args[1].kind != Form::kKw) fail("arity", "(cast x :f32) or (cast x :bool)");
+        const Val v = tensor(eval(args[0], env));
+        if (args[1].s == ":f32") return v.is_bool ? emit(false, v.wide, "(" + ref(v) + " ? 1.0f : 0.0f)") : v;
+        if (args[1].s == ":bool") return v.is_bool ? v : emit(true, v.wide, "(" + ref(v) + " != 0.0f)");
+        fail("E-DIM-002", "the body casts only between f32 and bool, not to " + args[1].s);
+    }
+
+    if (head == "broadcast-to" || head == "reshape") {
+        if (args.size() != 2 || args[1].kind != Form::kVec) fail("arity", "(" + head + " value [dims...])");
+        for (const Form& d : args[1].items)
+            if (d.kind != Form::kNum) fail("arity", "(" + head + " value [dims...])");
+        const Val v = eval(args[0], env);
+        if (v.kind != Val::kTensor) return v;
+        const auto& dims = args[1].items;
+        if (head == "broadcast-to" && !dims.empty() && !v.wide && vector_ && dims.back().num == W_)
+            return emit(v.is_bool, true, ref(v));
+        return v;
+    }
+
+    std::vector<Val> vals;
+    for (const Form& a : args) vals.push_back(eval(a, env));
+    auto arity = [&](size_t lo, long hi) {
+        if (vals.size() < lo || (hi >= 0 && vals.size() > static_cast<size_t>(hi)))
+            fail("arity", "(" + head + " ...) has a wrong number of arguments: " + std::to_string(vals.size()));
+    };
+
+    if (const char* fn = lookup(kArith, head)) {
+        arity(1, -1);
+        if (vals.size() == 1) {
+            const Val& v = vals[0];
+            if (v.kind == Val::kNumber) {
+                if (head == "-") return number(-v.num);
+                if (head == "/") return number(1.0 / v.num);
+                return v;
+            }
+            const Val t = f32(v, head);
+            if (head == "-") return emit(false, t.wide, "(-" + ref(t) + ")");
+            if (head == "/") return emit(false, t.wide, "__fdiv_rn(1.0f, " + ref(t) + ")");
+            return t;
+        }
+        Val acc = vals[0];
+        for (size_t i = 1; i < vals.size(); ++i) {
+            const Val& v = vals[i];
+            if (acc.kind == Val::kNumber && v.kind == Val::kNumber) {
+                acc = number(number_arith(head, acc.num, v.num));
+            } else {
+                const Val a = f32(acc, head), b = f32(v, head);
+                acc = emit(false, a.wide || b.wide, std::string(fn) + "(" + ref(a) + ", " + ref(b) + ")");
+            }
+        }
+        return acc;
+    }
+    if (const char* op = lookup(kCompare, head)) {
+        arity(2, 2);
+        if (vals[0].kind == Val::kNumber && vals[1].kind == Val::kNumber)
+            return bool_const(number_compare(head, vals[0].num, vals[1].num));
+        const Val a = f32(vals[0], head), b = f32(vals[1], head);
+        return emit(true, a.wide || b.wide, "(" + ref(a) + " " + op + " " + ref(b) + ")");
+    }
+    if (head == "and" || head == "or") {
+        arity(1, -1);
+        Val acc = boolean(vals[0], head);
+        for (size_t i = 1; i < vals.size(); ++i) {
+            const Val b = boolean(vals[i], head);
+            acc = emit(true, acc.wide || b.wide, "(" + ref(acc) + (head == "and" ? " && " : " || ") + ref(b) + ")");
+        }
+        return acc;
+    }
+    if (head == "not") {
+        arity(1, 1);
+        const Val a = boolean(vals[0], "not");
+        return emit(true, a.wide, "(!" + ref(a) + ")");
+    }
+    if (head == "where") {
+        arity(3, 3);
+        const Val m = boolean(vals[0], "where mask");
+        const Val a = tensor(vals[1]), b = tensor(vals[2]);
+        if (a.is_bool != b.is_bool) fail("E-DIM-002", "where: branches of different dtypes");
+        return emit(a.is_bool, m.wide || a.wide || b.wide, "(" + ref(m) + " ? " + ref(a) + " : " + ref(b) + ")");
+    }
+    if (head == "neg") {
+        arity(1, 1);
+        const Val a = f32(vals[0], head);
+        return emit(false, a.wide, "(-" + ref(a) + ")");
+    }
+    if (const char* fn = lookup(kUnary, head)) {
+        arity(1, 1);
+        // sqrt, exp and log are overloaded: on a plain number they stay plain
+        if (vals[0].kind == Val::kNumber && (head == "sqrt" || head == "exp" || head == "log")) {
+            const double x = vals[0].num;
+            return number(head == "sqrt" ? std::sqrt(x) : head == "exp" ? std::exp(x) : std::log(x));
+        }
+        const Val a = f32(vals[0], head);
+        return emit(false, a.wide, std::string(fn) + "(" + ref(a) + ")");
+    }
+    if (const char* fn = lookup(kBinaryFn, head)) {
+        arity(2, 2);
+        if (head == "pow" && vals[0].kind == Val::kNumber && vals[1].kind == Val::kNumber)
+            return number(std::pow(vals[0].num, vals[1].num));
+        const Val a = f32(vals[0], head), b = f32(vals[1], head);
+        return emit(false, a.wide || b.wide, std::string(fn) + "(" + ref(a) + ", " + ref(b) + ")");
+    }
+    fail("op", "`" + head + "` is not an operation a body may use");
+}
+
+std::string comment_safe(const std::string& s) {
+    std::string r;
+    for (size_t i = 0; i < s.size(); ++i) {
+        if (s[i] == '*' && i + 1 < s.size() && s[i + 1] == '/') {
+            r += "* /";
+            ++i;
+        } else {
+            r += s[i];
+        }
+    }
+    return r;
+}
+
+}  // namespace
+
+std::unique_ptr<Program> Program::parse(const std::string& text) {
+    Form f = Reader(text).read_all();
+    if (f.kind != Form::kList || f.items.size() < 3 || f.items[0].kind != Form::kSym || f.items[0].s != "lambda" ||
+        f.items[1].kind != Form::kList)
+        fail("parse", "a body is (lambda (h seq ...) expr)");
+    std::unique_ptr<Program> p(new Program());
+    p->text_ = text;
+    for (const Form& a : f.items[1].items) {
+        if (a.kind != Form::kSym) fail("arity", "the body's arguments are names");
+        for (const std::string& q : p->params_)
+            if (q == a.s) fail("arity", "repeated argument name `" + a.s + "`");
+        p->params_.push_back(a.s);
+    }
+    if (p->params_.size() < 2) fail("arity", "a body takes the state and at least one sequence");
+    p->exprs_.assign(f.items.begin() + 2, f.items.end());
+    return p;
+}
+
+std::string Program::generate(int W, bool vector, unsigned wide_mask) const {
+    const int ns = n_seqs();
+    Tracer tr(W, vector);
+    Env env;
+    Val h;
+    h.kind = Val::kTensor;
+    h.name = "h";
+    h.wide = true;
+    env[params_[0]] = h;
+    int nw = 0, nn = 0;
+    for (int k = 0; k < ns; ++k) {
+        Val s;
+        s.kind = Val::kTensor;
+        s.wide = (wide_mask >> k) & 1u;
+        s.name = s.wide ? "sw[" + std::to_string(nw++) + "]" : "sn[" + std::to_string(nn++) + "]";
+        env[params_[k + 1]] = s;
+    }
+    Val r;
+    for (const Form& e : exprs_) r = tr.eval(e, env);
+    if (r.kind == Val::kBoolConst || (r.kind == Val::kTensor && r.is_bool))
+        fail("E-DIM-002", "the body returns bool; it must return f32");
+    r = tr.tensor(r);
+    if (!r.wide && W != 1)
+        fail("E-DIM-001", "the body returns one value; the state has width " + std::to_string(W));
+
+    std::ostringstream o;
+    o << "// functor for the body\n";
+    std::istringstream lines(comment_safe(text_));
+    for (std::string line; std::getline(lines, line);) o << "//   " << line << "\n";
+    o << "// state width " << W
+      << (vector ? " (vector state)" : " (scalar state)") << ", " << ns << " sequence(s), wide mask 0x" << std::hex
+      << wide_mask << std::dec << "\n";
+    o << "struct EsBody {\n";
+    o << "    static constexpr int kNS = " << ns << ";\n";
+    o << "    static constexpr unsigned kWideMask = 0x" << std::hex << wide_mask << std::dec << "u;\n";
+    o << "    static constexpr int kSW = " << (nw > 0 ? nw : 1) << ";\n";
+    o << "    static constexpr int kSN = " << (nn > 0 ? nn : 1) << ";\n";
+    o << "    template <int E, int G>\n";
+    o << "    __device__ __forceinline__ static void step(float (&r)[E], const float (&h)[E],\n"
+         "                                                const float (&sw)[kSW][E], const float (&sn)[kSN],\n"
+         "                                                const unsigned mask) {\n";
+    o << "        (void)h;\n        (void)sw;\n        (void)sn;\n        (void)mask;\n";
+    o << tr.code;
+    o << "#pragma unroll\n        for (int e = 0; e < E; ++e) r[e] = " << tr.ref(r) << ";\n";
+    o << "    }\n};\n";
+    return o.str();
+}
+
+}  // namespace body
+}  // namespace es

@@ -6,6 +6,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
+#include "es.h"
+
 #define ES_BODY_TANH_DECAY 0
 #define ES_BODY_NORMCAP 1
 #define ES_BODY_MAXPLUS 2
@@ -50,6 +54,40 @@ struct BackwardLaunch {
     float* gx;              // dL/d x         [O, T, J, sw0]
     float* ga;              // dL/d a or c    [O, T, J, sw1]
 };
+
+// Per-device state of the library: the device status word and the SM count.
+struct DeviceState {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    unsigned int* status = nullptr;
+    int num_sms = 0;
+};
+
+// A validated call's shapes in canonical form (shared by every entry point).
+struct ShapePlan {
+    int64_t O, T, J, W;
+    int n_seqs;
+    int64_t sw[ES_MAX_SEQS];
+    int64_t n_out, n_init, n_seq[ES_MAX_SEQS];
+    bool empty;       // no lanes: nothing to read or write
+};
+
+// Check the arguments every scan shares ("Arguments and body": shapes, axis,
+// state axis, sequence widths) and the data pointers (present, 4-byte
+// aligned, `out` disjoint from every input); `names` name the sequences in
+// messages.  Returns ES_OK or the status with es_last_error() set.
+es_status plan_shapes(const char* fn, const char* const* names, const float* initial, const float* const* seqs,
+                      int n_seqs, const int64_t* shape, int rank, int axis, int state_width,
+                      const int64_t* seq_widths, const float* out, ShapePlan* P);
+
+// set es_last_error() and return `st`
+es_status api_fail(es_status st, const char* fmt, ...);
+es_status api_device(int* dev, DeviceState** st);
+es_status api_encoder(EncodeTiledFn* fn);
+void count_launch();
+uint64_t api_wait_ns();
+int64_t api_drop_tile();
+int api_path_override();
 
 // Each launcher enqueues exactly one kernel; it returns cudaSuccess or the
 // launch error.  `err` receives a message for non-CUDA failures (tensor-map

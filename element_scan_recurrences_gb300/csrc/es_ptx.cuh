@@ -1,0 +1,208 @@
+// es_ptx.cuh -- device building blocks of every element-scan kernel, in a
+// form that both nvcc and the run-time compiler (NVRTC) accept: IEEE
+// maximum/minimum, mbarrier and TMA wrappers (inline PTX for sm_103a), the
+// bounded wait every pipeline uses and the device status word's bits.  It
+// includes no host header, so kernels compiled at run time from body
+// programs share it with the kernels built into the library.
+#pragma once
+
+#ifdef __CUDACC_RTC__
+typedef unsigned int uint32_t;
+typedef int int32_t;
+typedef unsigned long long uint64_t;
+typedef long long int64_t;
+// the driver's opaque 128-byte tensor map, passed by value as a kernel argument
+struct alignas(64) CUtensorMap_st {
+    unsigned long long opaque[16];
+};
+typedef CUtensorMap_st CUtensorMap;
+#else
+#include <cuda.h>
+#include <stdint.h>
+#endif
+
+// bits of the per-device status word
+#ifndef ES_DEVICE_TIMEOUT
+#define ES_DEVICE_TIMEOUT 1u
+#endif
+
+namespace es {
+
+// ---------------------------------------------------------------------------
+// IEEE 754-2019 maximum / minimum
+
+// IEEE 754-2019 maximum: the larger value, +0 above -0, NaN if either
+// operand is NaN.  PTX `max.NaN.f32` has exactly these semantics (the PTX ISA
+// orders +0.0 above -0.0 for max and returns the canonical NaN when an input
+// is NaN) in one instruction on the serial chain.
+__device__ __forceinline__ float ieee_maximum(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// IEEE 754-2019 minimum, the mirror of ieee_maximum (-0 below +0, NaN wins).
+__device__ __forceinline__ float ieee_minimum(float a, float b) {
+    float r;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// Hardware reciprocal square root (relative error below 2^-22; subnormal
+// inputs are flushed, which only matters where callers use the value for
+// arguments above one).
+__device__ __forceinline__ float rsqrt_approx(float v) {
+    float r;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// shared-memory addresses, mbarriers, TMA
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// make initialised barriers visible to the async (TMA) proxy
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for the phase with `parity` to complete, giving up after `limit_ns`
+// or when another thread of the CTA has raised `abort_flag`.  Returns false
+// on give-up; the caller then records the failure and leaves its loop.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                                  volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 31u) == 0u) {
+            if (abort_flag != nullptr && *abort_flag) return false;
+            if (global_timer_ns() - t0 > limit_ns) return false;
+        }
+    }
+}
+
+// Byte offset that moves the dynamic SMEM base up to a 1024-byte boundary
+// (tile bases must be 1024-byte aligned for the 128-byte swizzle).  Adding it
+// to the `extern __shared__` array keeps pointers in the shared space, so
+// the compiler emits shared loads and knows they cannot alias global stores.
+__device__ __forceinline__ uint32_t smem_align_pad(const void* base) {
+    return (1024u - (smem_u32(base) & 1023u)) & 1023u;
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// L2 policy for the streamed TMA loads: normal priority.  An evict-first
+// hint measured worse on GB300: with 256-byte L2 promotion a 128-byte row
+// segment brings in the next tile's half of the line, and evict-first drops
+// it before that tile asks for it, so the data is read from HBM twice.
+__device__ __forceinline__ uint64_t l2_policy_stream() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                            uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)),
+          "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                            int32_t c2, uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2),
+          "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t c0, int32_t c1, const void* src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(src))
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// order this thread's generic-proxy SMEM writes before later async-proxy reads
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Barrier 1 over the `nthreads` consumer threads with an OR vote: true when
+// any of them passes `failed`.  Every consumer reaches it once per tile (its
+// own waits are bounded), so it cannot be left waiting.
+__device__ __forceinline__ bool consumer_vote_any_failed(bool failed, uint32_t nthreads) {
+    uint32_t any;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, %2, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(any)
+        : "r"(static_cast<uint32_t>(failed)), "r"(nthreads)
+        : "memory");
+    return any != 0;
+}
+
+// record a give-up in the device status word (read by es_device_status)
+__device__ __forceinline__ void report_timeout(unsigned int* status, volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicOr(status, ES_DEVICE_TIMEOUT);
+}
+
+}  // namespace es

@@ -59,11 +59,13 @@ typedef enum es_status {
     ES_E_ARG = 3,         /* null / misaligned / overlapping pointer, bad id */
     ES_E_UNSUPPORTED = 4, /* valid on the pages but not in this library      */
     ES_E_CUDA = 5,        /* a CUDA runtime or driver call failed            */
-    ES_E_TIMEOUT = 6      /* a kernel gave up a bounded device-side wait     */
+    ES_E_TIMEOUT = 6,     /* a kernel gave up a bounded device-side wait     */
+    ES_E_BODY = 7         /* a body program the contract rejects            */
 } es_status;
 
 #define ES_MAX_RANK 8
 #define ES_MAX_STATE 16
+#define ES_MAX_SEQS 8
 
 /* Kernel paths.  es_scan_f32 picks one per call (ES_PATH_AUTO) from the
  * canonical view [O, T, J, W] (O = product of dims before the axis, T the
@@ -74,7 +76,7 @@ typedef enum es_path {
     ES_PATH_GENERIC = 2,   /* one thread per lane, direct loads, any layout    */
     ES_PATH_LANE_TMA = 3,  /* lanes innermost: TMA/mbarrier time-tile pipeline */
     ES_PATH_TIME_TMA = 4,  /* time innermost: TMA tiles transposed in SMEM     */
-    ES_PATH_VEC_TMA = 5    /* NORMCAP vector state: TMA pipeline + shuffles    */
+    ES_PATH_VEC_TMA = 5    /* vector state: TMA pipeline + xor shuffles        */
 } es_path;
 
 /*
@@ -118,7 +120,7 @@ es_status es_scan_f32(es_body body, const float *initial, const float *const *se
  * alignment and overlap. */
 typedef struct es_plan_info {
     int64_t O, T, J, W;        /* canonical [O, T, J, W]                      */
-    int64_t seq_width[2];      /* each sequence's last width (1 or W)         */
+    int64_t seq_width[ES_MAX_SEQS]; /* each sequence's last width (1 or W); 0 past n_seqs */
     int64_t elements;          /* O*T*J*W output values                       */
     int path;                  /* es_path chosen                              */
     int reverse;
@@ -169,6 +171,81 @@ es_status es_plan_backward_f32(es_body body, const float *initial, const float *
                                const float *states, const float *grad_out,
                                const float *grad_initial, float *const *grad_seqs,
                                es_plan_info *info);
+
+/*
+ * Body programs: an element scan whose body is given as text, in the pages'
+ * notation ("Nonlinear element scans", "Arguments and body"):
+ *
+ *     (lambda (h x a) (tanh (+ x (* a h))))
+ *
+ * The first argument is the incoming state, one argument follows per
+ * sequence.  The body may use pointwise arithmetic (+ - * / pow sqrt exp log
+ * neg abs rsqrt sin cos tanh acos asin atan2 maximum minimum), the six
+ * comparisons (< <= > >= = !=), `and` / `or` / `not`, `where`, `let`,
+ * numbers, `true` / `false`, (cast v :f32) and (cast v :bool), and identity
+ * `reshape` / `broadcast-to`; with a state axis also (sum v) and (max v),
+ * with :axes [-1] and :keepdims, over the state's values ("Tensor
+ * operations": operation names, plain numbers fold in double precision until
+ * they meet a tensor and become f32 constants).  Every tensor operation is
+ * one f32 operation rounded to nearest in the order written (no fused
+ * multiply-add); transcendental functions are CUDA's f32 functions; maximum
+ * and minimum are IEEE 754-2019.  The body must return an f32 value as wide
+ * as the state.  Bodies the contract rejects give ES_E_BODY with a message
+ * naming the problem (E-SCAN-001 for a name that is no argument or binding).
+ *
+ * A program is compiled for each call signature (state width, sequence
+ * widths, kernel path) with NVRTC on first use and cached by its generated
+ * source; later calls launch the cached kernel.
+ */
+typedef struct es_body_program *es_body_t;
+
+/* Read and check `text` (a NUL-terminated host string); on success *body
+ * owns a new program (release it with es_body_destroy). */
+es_status es_body_create(const char *text, es_body_t *body);
+
+/* Release a program (NULL is ignored).  Kernels compiled for it stay cached. */
+es_status es_body_destroy(es_body_t body);
+
+/* The number of sequences the program takes (its arguments minus the state),
+ * or -1 for NULL. */
+int es_body_n_seqs(es_body_t body);
+
+/*
+ * es_scan_body_f32 -- es_scan_f32 with a body program.  The arguments are
+ * those of es_scan_f32 except `body`; n_seqs (1..ES_MAX_SEQS) must match the
+ * program.  A scalar state (state_width 0) cannot use `sum` or `max` over the
+ * state.  The first call of a signature compiles its kernel (host work, no
+ * device synchronisation); statuses as for es_scan_f32 plus ES_E_BODY.
+ */
+es_status es_scan_body_f32(es_body_t body, const float *initial, const float *const *seqs,
+                           int n_seqs, const int64_t *shape, int rank, int axis,
+                           int state_width, const int64_t *seq_widths, int reverse,
+                           float *out, es_stream_t stream);
+
+/* Plan of a body-program call (validation, body check and kernel path; no
+ * CUDA call, nothing compiled). */
+es_status es_plan_body_f32(es_body_t body, const float *initial, const float *const *seqs,
+                           int n_seqs, const int64_t *shape, int rank, int axis,
+                           int state_width, const int64_t *seq_widths, int reverse,
+                           const float *out, es_plan_info *info);
+
+/* The CUDA functor generated for a signature (state_width as in
+ * es_scan_body_f32, seq_widths NULL or n_seqs widths).  Writes at most `cap`
+ * bytes including the NUL into `buf` (may be NULL with cap 0) and the full
+ * length without the NUL into *needed.  No CUDA call. */
+es_status es_body_source(es_body_t body, int state_width, int n_seqs, const int64_t *seq_widths,
+                         char *buf, size_t cap, size_t *needed);
+
+/* Compile ahead of time every kernel a signature (state_width, n_seqs,
+ * seq_widths as in es_body_source) may use on `path` (ES_PATH_AUTO: on every
+ * path it may take), so that later calls only load them.  Host work only
+ * (NVRTC); no device is needed.  A compile failure is ES_E_CUDA with the
+ * compiler's log. */
+es_status es_body_prepare(es_body_t body, int state_width, int n_seqs, const int64_t *seq_widths,
+                          int path);
+
+/* NVRTC compilations so far in this process (kernel cache misses). */
+uint64_t es_body_compile_count(void);
 
 /* Synchronise `stream`, then read and clear this device's status word.
  * Returns ES_E_TIMEOUT if a kernel since the last check gave up a bounded
