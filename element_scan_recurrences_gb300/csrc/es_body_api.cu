@@ -78,6 +78,34 @@ bool body_lane_ok(const ShapePlan& S, const float* const* seqs, const float* out
     return true;
 }
 
+// sequence axis innermost: one row of T values per lane, 16-byte rows
+bool body_time_ok(const ShapePlan& S, const float* const* seqs, const float* out) {
+    if (S.W != 1 || S.J != 1) return false;
+    if (S.T % 4 != 0 || S.T < 32) return false;
+    if (S.O >= (int64_t(1) << 31) || S.T >= (int64_t(1) << 31)) return false;
+    if (!aligned16(out)) return false;
+    for (int k = 0; k < S.n_seqs; ++k)
+        if (!aligned16(seqs[k])) return false;
+    return true;
+}
+
+// vector state of 2, 4, 8 or 16 values: 128 values per CTA and trip, 16-byte
+// rows and boxes for every sequence
+bool body_vec_ok(const ShapePlan& S, const float* const* seqs, const float* out) {
+    const int64_t W = S.W;
+    if (W != 2 && W != 4 && W != 8 && W != 16) return false;
+    const int64_t LV = 128 / W;
+    if (S.J < LV || (S.J * W) % 4 != 0) return false;
+    for (int k = 0; k < S.n_seqs; ++k)
+        if (S.sw[k] == 1 && S.J % 4 != 0) return false;
+    if (S.O >= (int64_t(1) << 31) || S.T >= (int64_t(1) << 31) || S.J * W >= (int64_t(1) << 31)) return false;
+    if (S.O * ((S.J + LV - 1) / LV) >= (int64_t(1) << 31)) return false;
+    if (!aligned16(out)) return false;
+    for (int k = 0; k < S.n_seqs; ++k)
+        if (!aligned16(seqs[k])) return false;
+    return true;
+}
+
 es_status plan_body(es_body_t body, const float* initial, const float* const* seqs, int n_seqs,
                     const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
                     int reverse, const float* out, BodyCall* C) {
@@ -103,12 +131,15 @@ es_status plan_body(es_body_t body, const float* initial, const float* const* se
         return ES_OK;
     }
     const bool lane_ok = body_lane_ok(C->S, seqs, out);
+    const bool time_ok = body_time_ok(C->S, seqs, out);
+    const bool vec_ok = body_vec_ok(C->S, seqs, out);
     const int forced = api_path_override();
     if (forced == ES_PATH_AUTO) {
-        C->path = lane_ok ? ES_PATH_LANE_TMA : ES_PATH_GENERIC;
+        C->path = vec_ok ? ES_PATH_VEC_TMA : time_ok ? ES_PATH_TIME_TMA : lane_ok ? ES_PATH_LANE_TMA : ES_PATH_GENERIC;
         return ES_OK;
     }
-    if (forced == ES_PATH_GENERIC || (forced == ES_PATH_LANE_TMA && lane_ok)) {
+    if (forced == ES_PATH_GENERIC || (forced == ES_PATH_LANE_TMA && lane_ok) || (forced == ES_PATH_TIME_TMA && time_ok) ||
+        (forced == ES_PATH_VEC_TMA && vec_ok)) {
         C->path = forced;
         return ES_OK;
     }
@@ -142,6 +173,34 @@ KernelText generic_text(const std::string& functor, int W) {
 KernelText lane_text(const std::string& functor, int LI, int TT) {
     return {"#include \"skel_lane.cuh\"\n" + functor,
             "&es::k_body_lane<EsBody, " + std::to_string(LI) + ", " + std::to_string(TT) + ">"};
+}
+
+constexpr int kTimeLO = 64;   // rows (lanes) per CTA of the time-innermost skeleton
+
+KernelText time_text(const std::string& functor) {
+    return {"#include \"skel_time.cuh\"\n" + functor, "&es::k_body_time<EsBody, " + std::to_string(kTimeLO) + ">"};
+}
+
+// values of a lane's state per thread in the vector-state skeleton
+int vec_values(int W) { return W >= 4 ? 4 : W; }
+
+KernelText vec_text(const std::string& functor, int W, int TT) {
+    return {"#include \"skel_vec.cuh\"\n" + functor, "&es::k_body_vec<EsBody, " + std::to_string(W) + ", " +
+                                                           std::to_string(vec_values(W)) + ", " +
+                                                           std::to_string(TT) + ">"};
+}
+
+// bytes of one vector-state pipeline stage (every sequence's TT-trip tile)
+int64_t vec_stage_bytes(int W, int TT, int n_wide, int n_narrow) {
+    return static_cast<int64_t>(TT) * (n_wide * 128LL * 4 + n_narrow * (128LL / W) * 4);
+}
+
+// trips per vector-state tile: 32 unless a stage of every sequence would
+// pass 64 KB
+int vec_trips(int W, int n_wide, int n_narrow) {
+    int TT = 32;
+    while (TT > 8 && vec_stage_bytes(W, TT, n_wide, n_narrow) > 64 * 1024) TT /= 2;
+    return TT;
 }
 
 // trips per tile of the lanes-innermost skeleton: every sequence's tile sits
@@ -244,6 +303,93 @@ es_status signature_functor(const char* fn, es_body_t body, int state_width, int
     return functor_for(body, W, state_width != 0, mask, functor);
 }
 
+bool launch_body_time(const BodyLaunch& L, std::string* err) {
+    const BodyCall& C = *L.C;
+    const int NS = C.S.n_seqs;
+    constexpr int LO = kTimeLO;
+    const int64_t ctas = (C.S.O + LO - 1) / LO;
+    int64_t per_sm = (ctas + L.dev->num_sms - 1) / L.dev->num_sms;
+    per_sm = per_sm < 1 ? 1 : per_sm > 3 ? 3 : per_sm;
+    const int64_t budget = (210 * 1024) / per_sm - 3 * LO * 128 - 1024;
+    const int64_t stage_bytes = static_cast<int64_t>(NS) * LO * 128;
+    int64_t st = budget / stage_bytes;
+    const int stages = static_cast<int>(st < 2 ? 2 : st > 6 ? 6 : st);
+    alignas(64) CUtensorMap maps[ES_MAX_SEQS + 1];
+    for (int q = 0; q <= NS; ++q) {
+        const float* basep = q < NS ? L.seqs[q] : L.out;
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(C.S.T), static_cast<cuuint64_t>(C.S.O)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(C.S.T) * 4};
+        const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(LO)};
+        const cuuint32_t estr[2] = {1, 1};
+        if (L.encode(&maps[q], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(basep), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            *err = "cuTensorMapEncodeTiled failed for a time-innermost tile map";
+            return false;
+        }
+    }
+    JitKernel k;
+    const KernelText kt = time_text(C.functor);
+    if (!jit_kernel(kt.source, kt.name, &k, err)) return false;
+    const float* init = L.init;
+    int O = static_cast<int>(C.S.O), T = static_cast<int>(C.S.T);
+    int stg = stages, reverse = C.reverse;
+    unsigned int* status = L.dev->status;
+    uint64_t wait_ns = api_wait_ns();
+    int64_t drop = api_drop_tile();
+    void* args[] = {maps, &init, &O, &T, &stg, &reverse, &status, &wait_ns, &drop};
+    const size_t smem = static_cast<size_t>(stages * stage_bytes) + 3 * LO * 128 + 1024;
+    return jit_launch(k, static_cast<unsigned>(ctas), 32 + LO, smem, L.stream, args, err);
+}
+
+bool launch_body_vec(const BodyLaunch& L, std::string* err) {
+    const BodyCall& C = *L.C;
+    const int NS = C.S.n_seqs;
+    const int W = static_cast<int>(C.S.W);
+    const int LV = 128 / W;
+    int n_wide = 0;
+    for (int q = 0; q < NS; ++q) n_wide += C.S.sw[q] == W ? 1 : 0;
+    const int TT = vec_trips(W, n_wide, NS - n_wide);
+    const int64_t stage_bytes = vec_stage_bytes(W, TT, n_wide, NS - n_wide);
+    const int64_t tiles_j = (C.S.J + LV - 1) / LV;
+    const int64_t ctas = C.S.O * tiles_j;
+    int64_t per_sm = (ctas + L.dev->num_sms - 1) / L.dev->num_sms;
+    per_sm = per_sm < 1 ? 1 : per_sm > 8 ? 8 : per_sm;
+    int64_t budget = (200 * 1024) / per_sm;
+    if (budget > 160 * 1024) budget = 160 * 1024;
+    int64_t st = budget / stage_bytes;
+    const int stages = static_cast<int>(st < 2 ? 2 : st > 8 ? 8 : st);
+    alignas(64) CUtensorMap maps[ES_MAX_SEQS];
+    for (int q = 0; q < NS; ++q) {
+        const bool wide = C.S.sw[q] == W;
+        const int64_t row = wide ? C.S.J * W : C.S.J;
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(row), static_cast<cuuint64_t>(C.S.T),
+                                    static_cast<cuuint64_t>(C.S.O)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row) * 4, static_cast<cuuint64_t>(row) * C.S.T * 4};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(wide ? 128 : LV), static_cast<cuuint32_t>(TT), 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (L.encode(&maps[q], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(L.seqs[q]), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            *err = "cuTensorMapEncodeTiled failed for a vector-state tile map";
+            return false;
+        }
+    }
+    JitKernel k;
+    const KernelText kt = vec_text(C.functor, W, TT);
+    if (!jit_kernel(kt.source, kt.name, &k, err)) return false;
+    const float* init = L.init;
+    float* out = L.out;
+    int T = static_cast<int>(C.S.T), J = static_cast<int>(C.S.J), tj = static_cast<int>(tiles_j);
+    int stg = stages, reverse = C.reverse;
+    unsigned int* status = L.dev->status;
+    uint64_t wait_ns = api_wait_ns();
+    int64_t drop = api_drop_tile();
+    void* args[] = {maps, &init, &out, &T, &J, &tj, &stg, &reverse, &status, &wait_ns, &drop};
+    const size_t smem = static_cast<size_t>(stages * stage_bytes) + 1024;
+    return jit_launch(k, static_cast<unsigned>(ctas), 32 + 128 / vec_values(W), smem, L.stream, args, err);
+}
+
 void fill_info(const BodyCall& C, es_plan_info* info) {
     if (info == nullptr) return;
     std::memset(info, 0, sizeof(*info));
@@ -308,6 +454,12 @@ es_status es_body_prepare(es_body_t body, int state_width, int n_seqs, const int
     if (path == ES_PATH_AUTO || path == ES_PATH_GENERIC) todo.push_back(es::generic_text(functor, W));
     if ((path == ES_PATH_AUTO || path == ES_PATH_LANE_TMA) && W == 1)
         for (int LI : {32, 64, 128}) todo.push_back(es::lane_text(functor, LI, es::lane_trips(n_seqs)));
+    if ((path == ES_PATH_AUTO || path == ES_PATH_TIME_TMA) && W == 1) todo.push_back(es::time_text(functor));
+    if ((path == ES_PATH_AUTO || path == ES_PATH_VEC_TMA) && (W == 2 || W == 4 || W == 8 || W == 16)) {
+        int n_wide = 0;
+        for (int k = 0; k < n_seqs; ++k) n_wide += (seq_widths == nullptr || seq_widths[k] == W) ? 1 : 0;
+        todo.push_back(es::vec_text(functor, W, es::vec_trips(W, n_wide, n_seqs - n_wide)));
+    }
     if (todo.empty())
         return es::api_fail(ES_E_UNSUPPORTED, "es_body_prepare: path %d cannot serve this signature", path);
     for (const es::KernelText& kt : todo) {
@@ -352,7 +504,9 @@ es_status es_scan_body_f32(es_body_t body, const float* initial, const float* co
         ok = es::launch_body_generic(L, &err);
     } else {
         if ((st = es::api_encoder(&L.encode)) != ES_OK) return st;
-        ok = es::launch_body_lane(L, &err);
+        if (C.path == ES_PATH_LANE_TMA) ok = es::launch_body_lane(L, &err);
+        else if (C.path == ES_PATH_TIME_TMA) ok = es::launch_body_time(L, &err);
+        else ok = es::launch_body_vec(L, &err);
     }
     if (!ok) return es::api_fail(ES_E_CUDA, "es_scan_body_f32: %s", err.c_str());
     es::count_launch();

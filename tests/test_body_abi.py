@@ -59,6 +59,25 @@ def test_plan_paths():
     assert e.value.status == 3
     p = es.Body("(lambda (h x y) (+ h x y))").plan([4, 10, 64], 1)
     assert p["seq_width"] == (1, 1) and p["O"] == 4 and p["T"] == 10 and p["J"] == 64
+    # the sequence axis last: time innermost when rows are 16-byte multiples of >= 32 trips
+    assert avg.plan([300, 100], -1)["path"] == "time_tma"
+    assert avg.plan([300, 102], -1)["path"] == "generic"
+    assert avg.plan([300, 16], -1)["path"] == "generic"
+    # vector states of 2, 4, 8, 16 values with enough lanes per CTA
+    nc = es.Body(body_cases.NORMCAP_TEXT)
+    assert nc.plan([2, 70, 48, 16], 1, 16, [16, 1])["path"] == "vec_tma"
+    assert nc.plan([2, 70, 48, 16], 1, 16, [16, 16])["path"] == "vec_tma"
+    assert nc.plan([2, 70, 6, 16], 1, 16, [16, 1])["path"] == "generic"      # fewer lanes than a CTA holds
+    assert nc.plan([2, 70, 50, 16], 1, 16, [16, 1])["path"] == "generic"     # gate rows not 16-byte multiples
+    assert nc.plan([2, 70, 50, 16], 1, 16, [16, 16])["path"] == "vec_tma"
+    assert nc.plan([2, 70, 48, 3], 1, 3, [3, 1])["path"] == "generic"        # odd widths
+    es.set_path_override("vec_tma")
+    try:
+        with pytest.raises(es.EsError) as e:
+            nc.plan([2, 70, 48, 3], 1, 3, [3, 1])
+        assert e.value.status == 4
+    finally:
+        es.set_path_override("auto")
 
 
 def test_arity_and_limits():
@@ -78,8 +97,8 @@ def test_arity_and_limits():
 
 def test_kernels_compile_for_sm103a():
     """NVRTC compiles every kernel variant of each test body's signature."""
-    for cid in ("tanh_decay", "eight_seqs", "count_logic", "normcap_w16", "centre_w4", "odd_width_w3",
-                "width_one_state"):
+    for cid in ("tanh_decay", "eight_seqs", "count_logic", "normcap_w16", "normcap_w4_wide_gate", "centre_w4",
+                "softsign_w2", "row_max_w8", "odd_width_w3", "width_one_state"):
         c = body_cases.case(cid)
         es.Body(c[1]).prepare(c[2], c[3])
 

@@ -63,7 +63,6 @@ def run(c, O, T, J, axis, reverse, path, seed=0):
 
 def tiled_path(c, O, T, J, axis):
     body = es.Body(c[1])
-    initial, seqs, state_axis = body_cases.make_inputs(c, 1, 1, 1)
     W = c[2]
     if W > 0:
         shape = [O, T, J, W]
@@ -88,13 +87,31 @@ def test_body_tiled_path(cid, reverse):
     """The skeleton a lane-rich shape selects: several lane tiles, a ragged
     last lane tile and a ragged last time tile."""
     c = body_cases.case(cid)
-    if c[2] > 0:
-        O, T, J = 2, 70, 48
+    W = c[2]
+    if W > 0:
+        O, T, J = 2, 70, 72
     else:
         O, T, J = 3, 70, 200
     path = tiled_path(c, O, T, J, 1)
+    expected = "vec_tma" if W in (2, 4, 8, 16) else "generic" if W > 1 else "lane_tma"
+    assert path == expected, (cid, path)
     got, want = run(c, O, T, J, 1, reverse, "auto")
     compare(got, want, c[7], "%s %s reverse=%s" % (cid, path, reverse))
+
+
+SCALAR_IDS = [c[0] for c in body_cases.CASES if c[2] == 0]
+
+
+@pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
+@pytest.mark.parametrize("cid", SCALAR_IDS)
+def test_body_time_path(cid, reverse):
+    """The sequence axis last: rows of T trips transposed through shared
+    memory; a ragged last row tile and a ragged last trip tile."""
+    c = body_cases.case(cid)
+    O, J, T = 3, 70, 100
+    assert tiled_path(c, O, T, J, 2) == "time_tma"
+    got, want = run(c, O, T, J, 2, reverse, "auto")
+    compare(got, want, c[7], "%s time_tma reverse=%s" % (cid, reverse))
 
 
 def test_page_bodies_match_fixed_kernels():
