@@ -20,7 +20,6 @@ infrastructure, a plain loop) on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import math
@@ -41,6 +40,9 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 PATH_KERNEL = {"lane_tma": "k_lane_tma", "time_tma": "k_time_tma", "vec_tma": "k_vec_tma", "generic": "k_generic"}
 PATH_KERNEL_BWD = {"lane_tma": "k_lane_bwd", "generic": "k_generic_bwd"}
+# kernels compiled at run time from a body program
+PATH_KERNEL_BODY = {"lane_tma": "k_body_lane", "time_tma": "k_body_time", "vec_tma": "k_body_vec",
+                    "generic": "k_body_generic"}
 
 
 # ---------------------------------------------------------------------------
@@ -168,40 +170,69 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+# the sources each kernel is built from (besides the shared device headers);
+# a body-program kernel also depends on the compiler that writes its functor
+# and on the host code that picks its launch configuration
+_SHARED_SOURCES = ["es_ptx.cuh", "es_device.cuh", "es_internal.h"]
+_BODY_SOURCES = ["skel_common.cuh", "es_body_compiler.cu", "es_body_api.cu", "es_jit.cu"]
+KERNEL_SOURCES = {
+    "k_lane_tma": ["k_lane_tma.cu"], "k_time_tma": ["k_time_tma.cu"], "k_vec_tma": ["k_vec_tma.cu"],
+    "k_generic": ["k_generic.cu"], "k_generic_bwd": ["k_generic.cu"], "k_lane_bwd": ["k_lane_bwd.cu"],
+    "k_vec_bwd": ["k_vec_bwd.cu"], "k_time_bwd": ["k_time_bwd.cu"],
+    "k_body_lane": ["skel_lane.cuh"] + _BODY_SOURCES, "k_body_time": ["skel_time.cuh"] + _BODY_SOURCES,
+    "k_body_vec": ["skel_vec.cuh"] + _BODY_SOURCES, "k_body_generic": ["skel_generic.cuh"] + _BODY_SOURCES,
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the sources a kernel is built from: a profile taken before any
+    of them changed no longer describes the kernel."""
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "element_scan_recurrences_gb300", "csrc", "*")))
-    for f in files:
-        h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
+    csrc = os.path.join(ROOT, "element_scan_recurrences_gb300", "csrc")
+    for name in KERNEL_SOURCES.get(kernel, sorted(os.listdir(csrc))) + _SHARED_SOURCES:
+        h.update(name.encode())
+        with open(os.path.join(csrc, name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary of this kernel and
-    workload, or None when there is none or the kernel sources changed since."""
+    workload, or None when there is none or the kernel's sources changed since."""
     path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, workload))
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
     s = re.search(r"source_hash:\s*([0-9a-f]+)", text)
-    if not m or not s or s.group(1) != kernel_source_hash():
+    if not m or not s or s.group(1) != kernel_source_hash(kernel):
         return None
     return int(m.group(1))
 
 
 def plan_of(es, w, reverse):
+    if w.text is not None:
+        return es.Body(w.text).plan(w.shape, w.axis, w.shape[-1] if w.state_axis else 0,
+                                    w.seq_widths if w.state_axis else None, reverse)
     return es.plan(w.body, w.shape, w.axis, w.shape[-1] if w.state_axis else 0,
                    w.seq_widths if w.state_axis else None, reverse)
+
+
+def oracle_scan(w, init, seqs, reverse):
+    """The CPU oracle on host arrays: the fixed-body oracle, or the body-program
+    oracle for a workload given as text."""
+    if w.text is not None:
+        from oracle.body import scan_body
+        return scan_body(w.text, init, seqs, axis=w.axis, state_axis=w.state_axis, reverse=reverse)
+    import oracle
+    return oracle.scan(w.body, init, seqs, axis=w.axis, state_axis=w.state_axis, reverse=reverse)
 
 
 def take_sample(w, init, seqs, target_elems: int):
     """Whole sequences of a leading block of lanes, about `target_elems` output
     values per direction: the first rows along dim 0 (or, when one row is
-    already larger, the first positions of the last lane axis of row 0)."""
-    x, a = seqs
+    already larger, the first positions of the last lane axis of row 0).
+    Returns (initial, [sequences], elements, description)."""
     if w.ax == 0:
         raise ValueError("sampling needs a dimension before the sequence axis")
     per_row = w.elements // w.shape[0]
@@ -221,7 +252,7 @@ def take_sample(w, init, seqs, target_elems: int):
         desc = "row 0 along dim 0, first %d of %d positions along dim %d" % (m, n_last, lane_dim)
         elems = per_row * m // n_last
     cpu = lambda t: pick(t).contiguous().cpu().numpy()
-    return cpu(init), cpu(x), cpu(a), elems, desc
+    return cpu(init), [cpu(t) for t in seqs], elems, desc
 
 
 def cpu_oracle_rate(w, init, seqs, budget_s: float, backward: bool = False):
@@ -234,19 +265,19 @@ def cpu_oracle_rate(w, init, seqs, budget_s: float, backward: bool = False):
     oracle.build()
 
     def run(target):
-        ins, xs, as_, elems, desc = take_sample(w, init, seqs, target)
+        ins, ss, elems, desc = take_sample(w, init, seqs, target)
         prep = []
         if backward:
             for reverse in w.reverse:
-                st = oracle.scan(w.body, ins, [xs, as_], axis=w.axis, state_axis=w.state_axis, reverse=reverse)
+                st = oracle_scan(w, ins, ss, reverse)
                 prep.append((st, np.ones_like(st)))
         t0 = time.perf_counter()
         for k, reverse in enumerate(w.reverse):
             if backward:
-                oracle.scan_backward(w.body, ins, [xs, as_], prep[k][0], prep[k][1], axis=w.axis,
+                oracle.scan_backward(w.body, ins, ss, prep[k][0], prep[k][1], axis=w.axis,
                                      state_axis=w.state_axis, reverse=reverse)
             else:
-                oracle.scan(w.body, ins, [xs, as_], axis=w.axis, state_axis=w.state_axis, reverse=reverse)
+                oracle_scan(w, ins, ss, reverse)
         return time.perf_counter() - t0, elems * len(w.reverse), desc
 
     target = 1 << 20
@@ -270,20 +301,20 @@ def run_reference(args, w):
     init, seqs = wl.make_inputs(w, "cpu")
     # each step scans a bounded sample so that the whole run stays short
     step_budget = max(0.05, min(1.0, 120.0 / max(1, args.steps + args.warmup)))
-    ins, xs, as_, elems, _ = take_sample(w, init, seqs, 1 << 18)
+    ins, ss, elems, _ = take_sample(w, init, seqs, 1 << 18)
     t0 = time.perf_counter()
     for r in w.reverse:
-        oracle.scan(w.body, ins, [xs, as_], axis=w.axis, state_axis=w.state_axis, reverse=r)
+        oracle_scan(w, ins, ss, r)
     t_cal = time.perf_counter() - t0
     target = max(1, int((1 << 18) * step_budget / max(t_cal, 1e-4)))
-    ins, xs, as_, elems, desc = take_sample(w, init, seqs, target)
+    ins, ss, elems, desc = take_sample(w, init, seqs, target)
     for _ in range(args.warmup):
         for r in w.reverse:
-            oracle.scan(w.body, ins, [xs, as_], axis=w.axis, state_axis=w.state_axis, reverse=r)
+            oracle_scan(w, ins, ss, r)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         for r in w.reverse:
-            oracle.scan(w.body, ins, [xs, as_], axis=w.axis, state_axis=w.state_axis, reverse=r)
+            oracle_scan(w, ins, ss, r)
     dt = time.perf_counter() - t0
     elems *= len(w.reverse)
     value = elems * args.steps / dt
@@ -303,7 +334,9 @@ def run_reference(args, w):
 
 def config_of(w, backward=False):
     alg = w.backward_algorithmic_bytes() if backward else w.algorithmic_bytes()
-    return {"workload": w.name + (" (backward pass)" if backward else ""), "pass": "backward" if backward else "forward", "body": ["TANH_DECAY", "NORMCAP", "MAXPLUS"][w.body], "shape": list(w.shape),
+    body = w.text if w.text is not None else ["TANH_DECAY", "NORMCAP", "MAXPLUS"][w.body]
+    return {"workload": w.name + (" (backward pass)" if backward else ""),
+            "pass": "backward" if backward else "forward", "body": body, "shape": list(w.shape),
             "axis": w.axis, "state_axis": w.state_axis, "seq_widths": list(w.seq_widths) if w.state_axis else None,
             "directions": ["reverse" if r else "forward" for r in w.reverse], "elements_per_step": w.elements *
             len(w.reverse), "algorithmic_bytes_per_step": alg * len(w.reverse),
@@ -329,8 +362,17 @@ def run_ours(args, w):
     outs = [out] + [torch.empty_like(out) for _ in w.reverse[1:]]
     stream = torch.cuda.current_stream(device)
     plans = [plan_of(es, w, r) for r in w.reverse]
+    program = es.Body(w.text) if w.text is not None else None
+
+    def scan_into(o, r):
+        if program is not None:
+            program.scan_into(init, seqs, o, axis=w.axis, state_axis=w.state_axis, reverse=r, stream=stream)
+        else:
+            es.scan_into(w.body, init, seqs, o, axis=w.axis, state_axis=w.state_axis, reverse=r, stream=stream)
 
     backward = args.pass_ == "backward"
+    if backward and program is not None:
+        raise SystemExit("--pass backward: body programs have no backward kernels yet")
     if backward:
         # saved states and an output gradient per direction (untimed set-up)
         gen = torch.Generator(device=device)
@@ -349,7 +391,7 @@ def run_ours(args, w):
                                  grads=gr, stream=stream)
             return
         for o, r in zip(outs, w.reverse):
-            es.scan_into(w.body, init, seqs, o, axis=w.axis, state_axis=w.state_axis, reverse=r, stream=stream)
+            scan_into(o, r)
 
     sampler = ClockSampler(local) if rank == 0 else None
     for _ in range(max(args.warmup, 0)):
@@ -389,7 +431,8 @@ def run_ours(args, w):
     peak, peak_kind = measured_peaks()
     alg_bytes = w.backward_algorithmic_bytes() if backward else w.algorithmic_bytes()
     achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
-    kernel = (PATH_KERNEL_BWD if backward else PATH_KERNEL).get(plans[0]["path"], plans[0]["path"])
+    kernels = PATH_KERNEL_BWD if backward else PATH_KERNEL_BODY if program is not None else PATH_KERNEL
+    kernel = kernels.get(plans[0]["path"], plans[0]["path"])
     prof_name = w.name + ("_backward" if backward else "")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": profiled_traffic(kernel, prof_name), "kernel": kernel,
@@ -433,8 +476,12 @@ def run_ours(args, w):
                             hh.copy_(d, non_blocking=True)
                 return
             for oh, od, r in zip(out_h, outs, w.reverse):
-                es.scan_host(w.body, init_h, seqs_h, oh, (init, seqs, od), axis=w.axis, state_axis=w.state_axis,
-                             reverse=r, stream=stream)
+                if program is not None:
+                    program.scan_host(init_h, seqs_h, oh, (init, seqs, od), axis=w.axis, state_axis=w.state_axis,
+                                      reverse=r, stream=stream)
+                else:
+                    es.scan_host(w.body, init_h, seqs_h, oh, (init, seqs, od), axis=w.axis,
+                                 state_axis=w.state_axis, reverse=r, stream=stream)
 
         e2e_step()
         torch.cuda.synchronize(device)

@@ -418,6 +418,23 @@ class Body:
                                       sw, int(bool(reverse)), out.data_ptr(), handle))
         return out
 
+    def scan_host(self, initial_h, seqs_h, out_h, dev_bufs, axis: int = 0, state_axis: bool = False,
+                  reverse: bool = False, stream=None):
+        """End-to-end call on host tensors (see ``scan_host``): copy the inputs
+        into the caller's device buffers, scan, copy the states back.
+        Asynchronous on ``stream``; synchronise before reading ``out_h``."""
+        import torch
+        init_d, seqs_d, out_d = dev_bufs
+        if stream is None:
+            stream = torch.cuda.current_stream(out_d.device)
+        with torch.cuda.stream(stream):
+            init_d.copy_(initial_h, non_blocking=True)
+            for d, h in zip(seqs_d, seqs_h):
+                d.copy_(h, non_blocking=True)
+            self.scan_into(init_d, seqs_d, out_d, axis=axis, state_axis=state_axis, reverse=reverse, stream=stream)
+            out_h.copy_(out_d, non_blocking=True)
+        return out_h
+
 
 def body_compile_count() -> int:
     return int(lib().es_body_compile_count())

@@ -181,8 +181,13 @@ KernelText time_text(const std::string& functor) {
     return {"#include \"skel_time.cuh\"\n" + functor, "&es::k_body_time<EsBody, " + std::to_string(kTimeLO) + ">"};
 }
 
-// values of a lane's state per thread in the vector-state skeleton
-int vec_values(int W) { return W >= 4 ? 4 : W; }
+// Values of a lane's state per thread in the vector-state skeleton: one.  A
+// trip is a serial chain whose operations on the thread's own values run one
+// after another (an IEEE division or square root is tens of cycles each),
+// while a lane-group shuffle adds about 30 cycles per halving; on GB300 the
+// NORMCAP body took 0.47 / 0.38 / 0.34 ms (2048 trips) at 4 / 2 / 1 values
+// per thread, 0.73 at 8 and 2.1 at 16.
+int vec_values(int) { return 1; }
 
 KernelText vec_text(const std::string& functor, int W, int TT) {
     return {"#include \"skel_vec.cuh\"\n" + functor, "&es::k_body_vec<EsBody, " + std::to_string(W) + ", " +
@@ -254,12 +259,15 @@ bool launch_body_lane(const BodyLaunch& L, std::string* err) {
         }
     }
     const int TT = lane_trips(NS);
-    // about 96 trips in flight, within 200 KB of shared memory
+    // about 96 trips in flight; when there are more CTAs than SMs, at most
+    // about 100 KB of shared memory each, so that two CTAs share an SM (one
+    // consumer group alone cannot keep the serial chains' latency covered)
     const int64_t stage_bytes = static_cast<int64_t>(NS) * TT * LI * 4;
+    const int64_t tiles_i = (I + LI - 1) / LI;
+    const int64_t smem_cap = C.S.O * tiles_i > L.dev->num_sms ? 100 * 1024 : 200 * 1024;
     int stages = 96 / TT;
     if (stages > 8) stages = 8;
-    while (stages > 2 && stages * stage_bytes > 200 * 1024) --stages;
-    const int64_t tiles_i = (I + LI - 1) / LI;
+    while (stages > 2 && stages * stage_bytes > smem_cap) --stages;
     alignas(64) CUtensorMap maps[ES_MAX_SEQS];
     for (int q = 0; q < NS; ++q) {
         if (!encode_rows(L.encode, &maps[q], L.seqs[q], C.S.O, C.S.T, I, LI, TT)) {

@@ -164,12 +164,15 @@ k_body_vec(const __grid_constant__ TmaMaps<Body::kNS> maps, const float* __restr
             }
         };
         float aw[Body::kSW][E], an[Body::kSN], bw[Body::kSW][E], bn[Body::kSN];
-        auto trip = [&](const int tt, const float (&dw)[Body::kSW][E], const float (&dn)[Body::kSN]) {
-            float r[E];
-            Body::template step<E, G>(r, h, dw, dn, kMask);
+        // The state alternates between two register sets by trip parity, so a
+        // trip never overwrites the registers the previous trip's store may
+        // still be reading (consecutive trips alternate parity both ways).
+        float hr[2][E];
 #pragma unroll
-            for (int e = 0; e < E; ++e) h[e] = r[e];
-            if (valid) vec_store<E>(op + static_cast<int64_t>(tt) * row, r);
+        for (int e = 0; e < E; ++e) hr[0][e] = hr[1][e] = h[e];
+        auto trip = [&](const int tt, const float (&dw)[Body::kSW][E], const float (&dn)[Body::kSN]) {
+            Body::template step<E, G>(hr[tt & 1], hr[(tt & 1) ^ 1], dw, dn, kMask);
+            if (valid) vec_store<E>(op + static_cast<int64_t>(tt) * row, hr[tt & 1]);
         };
         // the next trip's operands are read while a trip runs; rows past the
         // valid trips of a ragged tile hold TMA's zero fill and are not used
@@ -192,6 +195,10 @@ k_body_vec(const __grid_constant__ TmaMaps<Body::kNS> maps, const float* __restr
                 if (tt - 1 < n) trip(tt - 1, bw, bn);
             }
         }
+        // the last trip of the tile: n - 1 forward, 0 in reverse
+        const int last = reverse ? 0 : n - 1;
+#pragma unroll
+        for (int e = 0; e < E; ++e) h[e] = hr[last & 1][e];
         __syncwarp(kMask);
         if (lane == 0) mbar_arrive(&empty_bar[s]);
     }

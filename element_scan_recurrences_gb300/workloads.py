@@ -10,7 +10,10 @@ Distributions: ``("normal", mu, sigma)`` is ``mu + sigma * randn``;
 constant fill.  The five named workloads are the element-scan cases the
 library is measured and checked on: a small TANH_DECAY case, a wide-lane
 TANH_DECAY case, a NORMCAP vector-state case, a reverse MAXPLUS case and a
-TANH_DECAY case whose sequence axis is innermost.
+TANH_DECAY case whose sequence axis is innermost.  The ``body_*`` workloads
+run body programs (the body given as text) on the same shapes: the pages'
+bodies, to set the run-time compiled kernels beside the built-in ones, and a
+gated body with three sequences.
 """
 from __future__ import annotations
 
@@ -23,7 +26,16 @@ import torch
 TANH_DECAY = 0
 NORMCAP = 1
 MAXPLUS = 2
-BODY_NAMES = {TANH_DECAY: "TANH_DECAY", NORMCAP: "NORMCAP", MAXPLUS: "MAXPLUS"}
+BODY_PROGRAM = -1
+BODY_NAMES = {TANH_DECAY: "TANH_DECAY", NORMCAP: "NORMCAP", MAXPLUS: "MAXPLUS", BODY_PROGRAM: "program"}
+
+# the pages' bodies as text ("Nonlinear element scans": intro, :state-axis
+# and :reverse examples) and a gated variant with a third sequence
+TANH_DECAY_TEXT = "(lambda (h x a) (tanh (+ x (* a h))))"
+NORMCAP_TEXT = ("(lambda (h x a) (let ((y (+ (* a h) x))) "
+                "(/ y (maximum 1.0 (sqrt (sum (* y y) :axes [-1]))))))")
+MAXPLUS_TEXT = "(lambda (h x c) (maximum (- h c) x))"
+GATED_TEXT = "(lambda (h x a g) (where (> g 0.5) (tanh (+ x (* a h))) h))"
 
 
 @dataclasses.dataclass(frozen=True)
@@ -39,6 +51,12 @@ class Workload:
     a_dist: tuple
     init_dist: tuple
     seed: int = 0
+    text: Optional[str] = None        # a body program (then `body` is BODY_PROGRAM)
+    extra_dists: tuple = ()           # distributions of sequences after the second
+
+    @property
+    def n_seqs(self) -> int:
+        return 2 + len(self.extra_dists)
 
     @property
     def rank(self) -> int:
@@ -67,8 +85,8 @@ class Workload:
         return tuple(d for i, d in enumerate(self.shape) if i != self.ax)
 
     def algorithmic_bytes(self) -> int:
-        """f32 bytes read (both sequences and initial) plus states written."""
-        reads = sum(math.prod(self.seq_shape(k)) for k in range(2))
+        """f32 bytes read (every sequence and initial) plus states written."""
+        reads = sum(math.prod(self.seq_shape(k)) for k in range(self.n_seqs))
         return 4 * (reads + math.prod(self.init_shape) + self.elements)
 
     def backward_algorithmic_bytes(self) -> int:
@@ -98,10 +116,24 @@ WORKLOADS = {
                  ("uniform", -1.0, 1.0), ("uniform", 0.0, 0.1), ("const", -3.0e38)),
         Workload("tanh_decay_time_inner", TANH_DECAY, (262144, 1024), -1, False, (1024, 1024), (False, True),
                  ("normal", 0.0, 1.0), ("uniform", 0.5, 0.99), ("normal", 0.0, 0.1)),
+        Workload("body_tanh_decay_lanes", BODY_PROGRAM, (64, 4096, 1024), 1, False, (1024, 1024), (False,),
+                 ("normal", 0.0, 1.0), ("uniform", 0.5, 0.99), ("const", 0.0), text=TANH_DECAY_TEXT),
+        Workload("body_gated_lanes", BODY_PROGRAM, (64, 4096, 1024), 1, False, (1024, 1024, 1024), (False,),
+                 ("normal", 0.0, 1.0), ("uniform", 0.5, 0.99), ("const", 0.0), text=GATED_TEXT,
+                 extra_dists=(("uniform", 0.0, 1.0),)),
+        Workload("body_normcap_vector", BODY_PROGRAM, (32, 8192, 64, 16), 1, True, (16, 1), (False,),
+                 ("normal", 0.0, 0.5), ("uniform", 0.8, 1.0), ("const", 0.0), text=NORMCAP_TEXT),
+        Workload("body_maxplus_reverse", BODY_PROGRAM, (128, 16384, 128), 1, False, (128, 128), (True,),
+                 ("uniform", -1.0, 1.0), ("uniform", 0.0, 0.1), ("const", -3.0e38), text=MAXPLUS_TEXT),
+        Workload("body_tanh_decay_time_inner", BODY_PROGRAM, (262144, 1024), -1, False, (1024, 1024),
+                 (False, True), ("normal", 0.0, 1.0), ("uniform", 0.5, 0.99), ("normal", 0.0, 0.1),
+                 text=TANH_DECAY_TEXT),
     ]
 }
 ORDER = ["tanh_decay_small", "tanh_decay_lanes", "normcap_vector", "maxplus_reverse",
          "tanh_decay_time_inner"]
+BODY_ORDER = ["body_tanh_decay_lanes", "body_gated_lanes", "body_normcap_vector", "body_maxplus_reverse",
+              "body_tanh_decay_time_inner"]
 
 
 def _draw(dist: tuple, shape, gen: torch.Generator, device) -> torch.Tensor:
@@ -118,13 +150,14 @@ def _draw(dist: tuple, shape, gen: torch.Generator, device) -> torch.Tensor:
 
 
 def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None):
-    """Draw (initial, [x, second]) for a workload, seeded, on ``device``."""
+    """Draw (initial, [x, second, ...]) for a workload, seeded, on ``device``:
+    the sequences in order, then initial."""
     gen = torch.Generator(device=device)
     gen.manual_seed(w.seed if seed is None else seed)
-    x = _draw(w.x_dist, w.seq_shape(0), gen, device)
-    a = _draw(w.a_dist, w.seq_shape(1), gen, device)
+    dists = (w.x_dist, w.a_dist) + tuple(w.extra_dists)
+    seqs = [_draw(d, w.seq_shape(k), gen, device) for k, d in enumerate(dists)]
     init = _draw(w.init_dist, w.init_shape, gen, device)
-    return init, [x, a]
+    return init, seqs
 
 
 def custom(body: int, shape, axis: int, state_axis: bool = False, seq_widths=None,
