@@ -23,14 +23,15 @@ _BODIES = {"TANH_DECAY": TANH_DECAY, "NORMCAP": NORMCAP, "MAXPLUS": MAXPLUS}
 STATUS = {0: "ES_OK", 1: "ES_E_DIM_001", 2: "ES_E_DIM_002", 3: "ES_E_ARG", 4: "ES_E_UNSUPPORTED",
           5: "ES_E_CUDA", 6: "ES_E_TIMEOUT", 7: "ES_E_BODY"}
 MAX_SEQS = 8
-PATHS = {0: "auto", 1: "empty", 2: "generic", 3: "lane_tma", 4: "time_tma", 5: "vec_tma"}
+PATHS = {0: "auto", 1: "empty", 2: "generic", 3: "lane_tma", 4: "time_tma", 5: "vec_tma", 6: "mat_tma"}
 PATH_IDS = {v: k for k, v in PATHS.items()}
 
 # every function include/es.h declares
 EXPORTS = ("es_scan_f32", "es_plan_f32", "es_scan_backward_f32", "es_plan_backward_f32", "es_device_status",
            "es_last_error", "es_status_string", "es_launch_count", "es_set_path_override", "es_set_wait_limit_ns",
            "es_set_drop_tile", "es_body_create", "es_body_destroy", "es_body_n_seqs", "es_scan_body_f32",
-           "es_plan_body_f32", "es_body_source", "es_body_prepare", "es_body_compile_count")
+           "es_plan_body_f32", "es_body_source", "es_body_prepare", "es_body_compile_count", "es_matrix_scan_f32",
+           "es_plan_matrix_scan_f32", "es_linear_scan_f32", "es_plan_linear_scan_f32")
 
 
 class LibraryMissing(ImportError):
@@ -109,6 +110,15 @@ def lib():
         L.es_body_prepare.restype = ctypes.c_int
         L.es_body_compile_count.argtypes = []
         L.es_body_compile_count.restype = ctypes.c_uint64
+        msig = [P, i64p, ctypes.c_int, P, i64p, ctypes.c_int, ctypes.c_int, ctypes.c_int]   # a, b, axis, reverse
+        L.es_matrix_scan_f32.argtypes = msig + [ctypes.c_int, P, P]
+        L.es_matrix_scan_f32.restype = ctypes.c_int
+        L.es_plan_matrix_scan_f32.argtypes = msig + [ctypes.c_int, P, ctypes.POINTER(PlanInfo)]
+        L.es_plan_matrix_scan_f32.restype = ctypes.c_int
+        L.es_linear_scan_f32.argtypes = msig + [P, P]
+        L.es_linear_scan_f32.restype = ctypes.c_int
+        L.es_plan_linear_scan_f32.argtypes = msig + [P, ctypes.POINTER(PlanInfo)]
+        L.es_plan_linear_scan_f32.restype = ctypes.c_int
         _lib = L
         return L
 
@@ -438,3 +448,100 @@ class Body:
 
 def body_compile_count() -> int:
     return int(lib().es_body_compile_count())
+
+
+# ---------------------------------------------------------------------------
+# matrix-scan and linear-scan
+
+
+def _shape_array(shape):
+    shape = [int(d) for d in shape]
+    return (ctypes.c_int64 * max(len(shape), 1))(*shape), len(shape)
+
+
+def _lead_broadcast(sa, sb):
+    r = max(len(sa), len(sb))
+    sa = [1] * (r - len(sa)) + list(sa)
+    sb = [1] * (r - len(sb)) + list(sb)
+    return [y if x == 1 else x for x, y in zip(sa, sb)]
+
+
+def _info(info, path_names=PATHS):
+    return {"O": info.O, "T": info.T, "J": info.J, "W": info.W,
+            "seq_width": (info.seq_width[0], info.seq_width[1]), "elements": info.elements,
+            "path": path_names[info.path], "reverse": bool(info.reverse)}
+
+
+def plan_matrix_scan(a_shape, b_shape, axis: int = 0, reverse: bool = False, projective: bool = False,
+                     ptrs: Optional[Sequence[int]] = None) -> dict:
+    """Validate and plan a matrix-scan without a GPU.  ``ptrs`` = (a, b, out),
+    by default 16-byte aligned, non-overlapping stand-ins."""
+    if ptrs is None:
+        ptrs = [(k + 1) << 44 for k in range(3)]
+    sa, ra = _shape_array(a_shape)
+    sb, rb = _shape_array(b_shape)
+    info = PlanInfo()
+    _check(lib().es_plan_matrix_scan_f32(ptrs[0], sa, ra, ptrs[1], sb, rb, int(axis), int(bool(reverse)),
+                                         int(bool(projective)), ptrs[2], ctypes.byref(info)))
+    return _info(info)
+
+
+def matrix_scan(a, b, axis: int = 0, reverse: bool = False, projective: bool = False, out=None, stream=None):
+    """matrix-scan on CUDA tensors: h[t] = a[t] @ h[t-1] + b[t] along `axis`
+    of the (broadcast) leading dims, from h = 0; returns ``out``."""
+    import torch
+    _require_cuda_f32(a, "a")
+    _require_cuda_f32(b, "b")
+    if a.dim() < 2 or b.dim() < 2:
+        raise EsError(1, "a is [.., n, n] and b [.., n, m]")
+    shape = _lead_broadcast(list(a.shape[:-2]), list(b.shape[:-2])) + [int(b.shape[-2]), int(b.shape[-1])]
+    if out is None:
+        out = torch.empty(shape, device=b.device, dtype=torch.float32)
+    else:
+        _require_cuda_f32(out, "out")
+    sa, ra = _shape_array(a.shape)
+    sb, rb = _shape_array(b.shape)
+    if stream is None:
+        stream = torch.cuda.current_stream(b.device)
+    handle = stream if isinstance(stream, int) else stream.cuda_stream
+    _check(lib().es_matrix_scan_f32(a.data_ptr(), sa, ra, b.data_ptr(), sb, rb, int(axis), int(bool(reverse)),
+                                    int(bool(projective)), out.data_ptr(), handle))
+    return out
+
+
+def plan_linear_scan(a_shape, b_shape, axis: int = 0, reverse: bool = False,
+                     ptrs: Optional[Sequence[int]] = None) -> dict:
+    if ptrs is None:
+        ptrs = [(k + 1) << 44 for k in range(3)]
+    sa, ra = _shape_array(a_shape)
+    sb, rb = _shape_array(b_shape)
+    info = PlanInfo()
+    _check(lib().es_plan_linear_scan_f32(ptrs[0], sa, ra, ptrs[1], sb, rb, int(axis), int(bool(reverse)), ptrs[2],
+                                         ctypes.byref(info)))
+    return _info(info)
+
+
+def linear_scan(a, b, axis: int = 0, reverse: bool = False, out=None, stream=None):
+    """linear-scan: h[t] = a[t] * h[t-1] + b[t] from h = 0, a and b broadcast
+    to one shape (a Python number becomes a one-value device tensor)."""
+    import torch
+    dev = b.device if isinstance(b, torch.Tensor) else a.device
+    if not isinstance(a, torch.Tensor):
+        a = torch.tensor(float(a), device=dev, dtype=torch.float32)
+    if not isinstance(b, torch.Tensor):
+        b = torch.tensor(float(b), device=dev, dtype=torch.float32)
+    _require_cuda_f32(a, "a")
+    _require_cuda_f32(b, "b")
+    shape = _lead_broadcast(list(a.shape), list(b.shape))
+    if out is None:
+        out = torch.empty(shape, device=dev, dtype=torch.float32)
+    else:
+        _require_cuda_f32(out, "out")
+    sa, ra = _shape_array(a.shape)
+    sb, rb = _shape_array(b.shape)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    handle = stream if isinstance(stream, int) else stream.cuda_stream
+    _check(lib().es_linear_scan_f32(a.data_ptr(), sa, ra, b.data_ptr(), sb, rb, int(axis), int(bool(reverse)),
+                                    out.data_ptr(), handle))
+    return out

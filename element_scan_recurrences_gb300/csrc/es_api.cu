@@ -213,7 +213,7 @@ es_status api_fail(es_status st, const char* fmt, ...) {
 
 es_status plan_shapes(const char* fn, const char* const* names, const float* initial, const float* const* seqs,
                       int n_seqs, const int64_t* shape, int rank, int axis, int state_width,
-                      const int64_t* seq_widths, const float* out, ShapePlan* P) {
+                      const int64_t* seq_widths, const float* out, ShapePlan* P, bool zero_initial) {
     if (shape == nullptr || seqs == nullptr) return fail(ES_E_ARG, "%s: null shape or sequence list", fn);
     if (n_seqs < 1 || n_seqs > ES_MAX_SEQS)
         return fail(ES_E_UNSUPPORTED, "%s: %d sequences; 1..%d are supported", fn, n_seqs, ES_MAX_SEQS);
@@ -273,7 +273,7 @@ es_status plan_shapes(const char* fn, const char* const* names, const float* ini
     P->empty = O * P->J == 0;
     if (P->empty) return ES_OK;
 
-    if (initial == nullptr || out == nullptr) return fail(ES_E_ARG, "%s: null data pointer", fn);
+    if ((initial == nullptr) != zero_initial || out == nullptr) return fail(ES_E_ARG, "%s: null data pointer", fn);
     for (int k = 0; k < n_seqs; ++k)
         if (seqs[k] == nullptr) return fail(ES_E_ARG, "%s: null data pointer", fn);
     if (reinterpret_cast<uintptr_t>(initial) % 4 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0)
@@ -283,7 +283,7 @@ es_status plan_shapes(const char* fn, const char* const* names, const float* ini
             return fail(ES_E_ARG, "%s: `%s` is not 4-byte aligned", fn, names[k]);
     // the result is a new value: `out` may not overlap any input
     const uintptr_t olo = reinterpret_cast<uintptr_t>(out), ohi = olo + static_cast<uintptr_t>(P->n_out) * 4;
-    for (int k = -1; k < n_seqs; ++k) {
+    for (int k = zero_initial ? 0 : -1; k < n_seqs; ++k) {
         const void* p = k < 0 ? static_cast<const void*>(initial) : static_cast<const void*>(seqs[k]);
         const int64_t n = k < 0 ? P->n_init : P->n_seq[k];
         const uintptr_t lo = reinterpret_cast<uintptr_t>(p), hi = lo + static_cast<uintptr_t>(n) * 4;
@@ -498,7 +498,7 @@ uint64_t es_launch_count(void) { return g_launches.load(); }
 
 es_status es_set_path_override(int path) {
     if (path != ES_PATH_AUTO && path != ES_PATH_GENERIC && path != ES_PATH_LANE_TMA && path != ES_PATH_TIME_TMA &&
-        path != ES_PATH_VEC_TMA)
+        path != ES_PATH_VEC_TMA && path != ES_PATH_MAT_TMA)
         return fail(ES_E_ARG, "es_set_path_override: unknown path %d", path);
     g_path_override.store(path);
     return ES_OK;

@@ -108,7 +108,7 @@ bool body_vec_ok(const ShapePlan& S, const float* const* seqs, const float* out)
 
 es_status plan_body(es_body_t body, const float* initial, const float* const* seqs, int n_seqs,
                     const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
-                    int reverse, const float* out, BodyCall* C) {
+                    int reverse, const float* out, BodyCall* C, bool zero_initial = false) {
     if (body == nullptr || !body->prog) return api_fail(ES_E_ARG, "es_scan_body_f32: null body program");
     const body::Program& p = *body->prog;
     if (n_seqs != p.n_seqs())
@@ -116,7 +116,7 @@ es_status plan_body(es_body_t body, const float* initial, const float* const* se
     static const char* const kNames[ES_MAX_SEQS] = {"seq 0", "seq 1", "seq 2", "seq 3",
                                                     "seq 4", "seq 5", "seq 6", "seq 7"};
     es_status st = plan_shapes("es_scan_body_f32", kNames, initial, seqs, n_seqs, shape, rank, axis, state_width,
-                               seq_widths, out, &C->S);
+                               seq_widths, out, &C->S, zero_initial);
     if (st != ES_OK) return st;
     C->vector = state_width != 0;
     C->reverse = reverse ? 1 : 0;
@@ -493,9 +493,20 @@ es_status es_plan_body_f32(es_body_t body, const float* initial, const float* co
 es_status es_scan_body_f32(es_body_t body, const float* initial, const float* const* seqs, int n_seqs,
                            const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
                            int reverse, float* out, es_stream_t stream) {
+    return es::scan_body_impl(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths, reverse, out,
+                              reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+}  // extern "C"
+
+namespace es {
+
+es_status scan_body_impl(es_body_t body, const float* initial, const float* const* seqs, int n_seqs,
+                         const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
+                         int reverse, float* out, cudaStream_t stream, bool zero_initial) {
     es::BodyCall C{};
     es_status st = es::plan_body(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths, reverse,
-                                 out, &C);
+                                 out, &C, zero_initial);
     if (st != ES_OK) return st;
     if (C.path == ES_PATH_EMPTY) return ES_OK;
     es::BodyLaunch L{};
@@ -503,7 +514,7 @@ es_status es_scan_body_f32(es_body_t body, const float* initial, const float* co
     L.init = initial;
     L.seqs = seqs;
     L.out = out;
-    L.stream = reinterpret_cast<cudaStream_t>(stream);
+    L.stream = stream;
     int dev = 0;
     if ((st = es::api_device(&dev, &L.dev)) != ES_OK) return st;
     std::string err;
@@ -521,4 +532,15 @@ es_status es_scan_body_f32(es_body_t body, const float* initial, const float* co
     return ES_OK;
 }
 
-}  // extern "C"
+es_status plan_body_impl(es_body_t body, const float* initial, const float* const* seqs, int n_seqs,
+                         const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
+                         int reverse, const float* out, es_plan_info* info, bool zero_initial) {
+    es::BodyCall C{};
+    es_status st = es::plan_body(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths, reverse,
+                                 out, &C, zero_initial);
+    if (st != ES_OK) return st;
+    es::fill_info(C, info);
+    return ES_OK;
+}
+
+}  // namespace es

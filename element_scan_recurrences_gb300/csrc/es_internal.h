@@ -76,9 +76,10 @@ struct ShapePlan {
 // state axis, sequence widths) and the data pointers (present, 4-byte
 // aligned, `out` disjoint from every input); `names` name the sequences in
 // messages.  Returns ES_OK or the status with es_last_error() set.
+// `zero_initial`: the scan starts from zero and `initial` must be null.
 es_status plan_shapes(const char* fn, const char* const* names, const float* initial, const float* const* seqs,
                       int n_seqs, const int64_t* shape, int rank, int axis, int state_width,
-                      const int64_t* seq_widths, const float* out, ShapePlan* P);
+                      const int64_t* seq_widths, const float* out, ShapePlan* P, bool zero_initial = false);
 
 // set es_last_error() and return `st`
 es_status api_fail(es_status st, const char* fmt, ...);
@@ -88,6 +89,15 @@ void count_launch();
 uint64_t api_wait_ns();
 int64_t api_drop_tile();
 int api_path_override();
+
+// The body-program scan (es_scan_body_f32) and its plan, with an optional
+// zero initial state (then `initial` is null), for operations built on it.
+es_status scan_body_impl(struct es_body_program* body, const float* initial, const float* const* seqs, int n_seqs,
+                         const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
+                         int reverse, float* out, cudaStream_t stream, bool zero_initial);
+es_status plan_body_impl(struct es_body_program* body, const float* initial, const float* const* seqs, int n_seqs,
+                         const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
+                         int reverse, const float* out, es_plan_info* info, bool zero_initial);
 
 // Each launcher enqueues exactly one kernel; it returns cudaSuccess or the
 // launch error.  `err` receives a message for non-CUDA failures (tensor-map

@@ -1,0 +1,48 @@
+// es_matrix.h -- matrix-scan launch descriptions shared by the entry points
+// (es_matrix_api.cu) and the kernels (k_matrix.cu).  Not part of the ABI.
+#pragma once
+
+#include "es_internal.h"
+
+namespace es {
+
+// Lanes of a matrix-scan with broadcast leading dims: a lane index splits
+// into the non-axis leading coordinates (row-major over dim[0..nd)); each
+// operand advances by its own stride per coordinate and along the axis, in
+// matrices (0 where the operand is broadcast).
+struct MatGeom {
+    int64_t lanes;
+    int64_t T;
+    int nd;
+    int64_t dim[ES_MAX_RANK];
+    int64_t sa[ES_MAX_RANK], sb[ES_MAX_RANK], so[ES_MAX_RANK];
+    int64_t ta, tb, to;
+};
+
+struct MatLaunch {
+    const float* a;
+    const float* b;
+    float* out;
+    int n, m;
+    int gp;              // threads per lane group: a power of two >= the columns carried
+    bool projective;
+    int reverse;
+    MatGeom g;           // any layout (generic kernel)
+    int64_t O, T, J;     // dense canonical view [O, T, J] of the leading dims (TMA kernel)
+    unsigned int* status;
+    uint64_t wait_ns;
+    int64_t drop_tile;
+    cudaStream_t stream;
+    EncodeTiledFn encode;
+};
+
+cudaError_t launch_mat_generic(const MatLaunch& L);
+cudaError_t launch_mat_tma(const MatLaunch& L, const char** err);
+
+// The TMA kernel serves dense operands with n in {2, 4, 8, 16}, 16-byte
+// aligned bases, n*m a multiple of 4 and at most 256, and a lane group of at
+// most 32 threads.
+bool mat_tma_ok(int n, int m, int gp, bool projective, int64_t O, int64_t T, int64_t J, bool dense, const void* a,
+                const void* b);
+
+}  // namespace es

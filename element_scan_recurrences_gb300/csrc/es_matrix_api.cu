@@ -1,0 +1,299 @@
+// es_matrix_api.cu -- the matrix-scan and linear-scan entry points of the C
+// ABI (es.h): shape checks, broadcasting of the leading dims, kernel choice.
+//
+// Contract ("Tensor operations": the `matrix-scan` row and section): a is
+// lead_a + [n, n] and b lead_b + [n, m], n <= 16; lead_a and lead_b
+// broadcast NumPy-style (right-aligned, each dim equal or 1) to one leading
+// shape, among whose dims `axis` counts (negative from the end, so -1 is the
+// one before the matrices); the result is that shape + [n, m].  linear-scan
+// takes a and b broadcast to one shape, numbers included: the same scan over
+// one-by-one matrices.  Shape errors are E-DIM-001.
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "es.h"
+#include "es_internal.h"
+#include "es_matrix.h"
+
+namespace es {
+namespace {
+
+std::string dims_str(const int64_t* d, int r) {
+    std::string s = "[";
+    for (int i = 0; i < r; ++i) {
+        if (i) s += ", ";
+        s += std::to_string(d[i]);
+    }
+    return s + "]";
+}
+
+bool mul_ok(int64_t a, int64_t b, int64_t* r) { return !__builtin_mul_overflow(a, b, r); }
+
+struct MatPlan {
+    MatLaunch L;
+    int64_t lead[ES_MAX_RANK];
+    int lead_rank;
+    int ax;
+    int64_t n_out, n_a, n_b;     // element counts
+    bool dense;                  // a and b both have the full leading shape
+    bool empty;
+    int path;
+};
+
+// `linear`: a and b have no matrix dims (n = m = 1)
+es_status plan_matrix(const char* fn, const float* a, const int64_t* a_shape, int a_rank, const float* b,
+                      const int64_t* b_shape, int b_rank, int axis, int reverse, int projective, const float* out,
+                      bool linear, MatPlan* P) {
+    if ((a_shape == nullptr && a_rank > 0) || (b_shape == nullptr && b_rank > 0))
+        return api_fail(ES_E_ARG, "%s: null shape", fn);
+    const int mat = linear ? 0 : 2;
+    if (a_rank < mat || b_rank < mat || a_rank - mat > ES_MAX_RANK || b_rank - mat > ES_MAX_RANK)
+        return api_fail(ES_E_DIM_001, "E-DIM-001 %s: a %s and b %s: ranks outside %d..%d", fn,
+                        dims_str(a_shape, a_rank).c_str(), dims_str(b_shape, b_rank).c_str(), mat,
+                        mat + ES_MAX_RANK);
+    for (int d = 0; d < a_rank; ++d)
+        if (a_shape[d] < 0) return api_fail(ES_E_DIM_001, "E-DIM-001 %s: negative dimension in a", fn);
+    for (int d = 0; d < b_rank; ++d)
+        if (b_shape[d] < 0) return api_fail(ES_E_DIM_001, "E-DIM-001 %s: negative dimension in b", fn);
+    int n = 1, m = 1;
+    if (!linear) {
+        const int64_t na = a_shape[a_rank - 1];
+        if (a_shape[a_rank - 2] != na || b_shape[b_rank - 2] != na)
+            return api_fail(ES_E_DIM_001, "E-DIM-001 %s: a %s f32 must be [.., n, n] and b %s f32 [.., n, m]", fn,
+                            dims_str(a_shape, a_rank).c_str(), dims_str(b_shape, b_rank).c_str());
+        if (na < 1 || na > 16)
+            return api_fail(ES_E_DIM_001, "E-DIM-001 %s: n = %lld; matrix-scan takes n from 1 to 16", fn,
+                            static_cast<long long>(na));
+        if (b_shape[b_rank - 1] < 1 || b_shape[b_rank - 1] > (int64_t(1) << 20))
+            return api_fail(ES_E_DIM_001, "E-DIM-001 %s: m = %lld", fn, static_cast<long long>(b_shape[b_rank - 1]));
+        n = static_cast<int>(na);
+        m = static_cast<int>(b_shape[b_rank - 1]);
+    }
+    // NumPy broadcast of the leading shapes
+    const int ra = a_rank - mat, rb = b_rank - mat;
+    const int r = ra > rb ? ra : rb;
+    if (r < 1) return api_fail(ES_E_DIM_001, "E-DIM-001 %s: no leading axis to scan along", fn);
+    int64_t la[ES_MAX_RANK], lb[ES_MAX_RANK];
+    for (int d = 0; d < r; ++d) {
+        la[d] = d < r - ra ? 1 : a_shape[d - (r - ra)];
+        lb[d] = d < r - rb ? 1 : b_shape[d - (r - rb)];
+        if (la[d] != lb[d] && la[d] != 1 && lb[d] != 1)
+            return api_fail(ES_E_DIM_001, "E-DIM-001 %s: the leading dims of a %s and b %s do not broadcast", fn,
+                            dims_str(a_shape, a_rank).c_str(), dims_str(b_shape, b_rank).c_str());
+        P->lead[d] = la[d] == 1 ? lb[d] : la[d];
+    }
+    P->lead_rank = r;
+    if (axis < -r || axis >= r)
+        return api_fail(ES_E_DIM_001, "E-DIM-001 %s: axis %d out of range for the leading shape %s", fn, axis,
+                        dims_str(P->lead, r).c_str());
+    const int ax = axis < 0 ? axis + r : axis;
+    P->ax = ax;
+    const int64_t T = P->lead[ax];
+    if (T < 1) return api_fail(ES_E_DIM_001, "E-DIM-001 %s: the scanned axis has length %lld", fn,
+                               static_cast<long long>(T));
+
+    MatLaunch& L = P->L;
+    L = MatLaunch{};
+    L.a = a;
+    L.b = b;
+    L.out = const_cast<float*>(out);
+    L.n = n;
+    L.m = m;
+    L.projective = projective != 0;
+    L.reverse = reverse ? 1 : 0;
+    int C = m + (L.projective ? n : 0);
+    L.gp = 1;
+    while (L.gp < C && L.gp < 64) L.gp *= 2;
+    if (L.projective && C > 32)
+        return api_fail(ES_E_UNSUPPORTED, "%s: a projective scan carries n + m = %d columns; at most 32", fn, C);
+    // strides in matrices: dense row-major over each operand's own leading shape
+    int64_t sa_all[ES_MAX_RANK], sb_all[ES_MAX_RANK], so_all[ES_MAX_RANK];
+    int64_t ca = 1, cb = 1, co = 1;
+    for (int d = r - 1; d >= 0; --d) {
+        sa_all[d] = la[d] == 1 ? 0 : ca;
+        sb_all[d] = lb[d] == 1 ? 0 : cb;
+        so_all[d] = co;
+        if (!mul_ok(ca, la[d], &ca) || !mul_ok(cb, lb[d], &cb) || !mul_ok(co, P->lead[d], &co))
+            return api_fail(ES_E_UNSUPPORTED, "%s: element count overflows", fn);
+    }
+    MatGeom& g = L.g;
+    g.T = T;
+    g.nd = 0;
+    g.lanes = 1;
+    for (int d = 0; d < r; ++d) {
+        if (d == ax) continue;
+        g.dim[g.nd] = P->lead[d];
+        g.sa[g.nd] = sa_all[d];
+        g.sb[g.nd] = sb_all[d];
+        g.so[g.nd] = so_all[d];
+        ++g.nd;
+        if (!mul_ok(g.lanes, P->lead[d], &g.lanes)) return api_fail(ES_E_UNSUPPORTED, "%s: element count overflows", fn);
+    }
+    g.ta = sa_all[ax];
+    g.tb = sb_all[ax];
+    g.to = so_all[ax];
+    L.O = 1;
+    for (int d = 0; d < ax; ++d) L.O *= P->lead[d];
+    L.T = T;
+    L.J = 1;
+    for (int d = ax + 1; d < r; ++d) L.J *= P->lead[d];
+    if (!mul_ok(co, static_cast<int64_t>(n) * m, &P->n_out) || !mul_ok(ca, static_cast<int64_t>(n) * n, &P->n_a) ||
+        !mul_ok(cb, static_cast<int64_t>(n) * m, &P->n_b) || P->n_out > (int64_t(1) << 60))
+        return api_fail(ES_E_UNSUPPORTED, "%s: element count overflows", fn);
+    P->dense = true;
+    for (int d = 0; d < r; ++d)
+        if (la[d] != P->lead[d] || lb[d] != P->lead[d]) P->dense = false;
+    P->empty = g.lanes == 0;
+    if (P->empty) {
+        P->path = ES_PATH_EMPTY;
+        return ES_OK;
+    }
+    if (a == nullptr || b == nullptr || out == nullptr) return api_fail(ES_E_ARG, "%s: null data pointer", fn);
+    if (reinterpret_cast<uintptr_t>(a) % 4 || reinterpret_cast<uintptr_t>(b) % 4 ||
+        reinterpret_cast<uintptr_t>(out) % 4)
+        return api_fail(ES_E_ARG, "%s: a data pointer is not 4-byte aligned", fn);
+    // the result is a new value: `out` may not overlap a or b
+    const uintptr_t olo = reinterpret_cast<uintptr_t>(out), ohi = olo + static_cast<uintptr_t>(P->n_out) * 4;
+    const uintptr_t alo = reinterpret_cast<uintptr_t>(a), ahi = alo + static_cast<uintptr_t>(P->n_a) * 4;
+    const uintptr_t blo = reinterpret_cast<uintptr_t>(b), bhi = blo + static_cast<uintptr_t>(P->n_b) * 4;
+    if ((alo < ohi && olo < ahi) || (blo < ohi && olo < bhi))
+        return api_fail(ES_E_ARG, "%s: `out` overlaps an input", fn);
+    return ES_OK;
+}
+
+es_status choose_matrix_path(const char* fn, MatPlan* P) {
+    if (P->empty) return ES_OK;
+    const MatLaunch& L = P->L;
+    const bool tma = mat_tma_ok(L.n, L.m, L.gp, L.projective, L.O, L.T, L.J, P->dense, L.a, L.b) &&
+                     reinterpret_cast<uintptr_t>(L.out) % 16 == 0;
+    const int forced = api_path_override();
+    if (forced == ES_PATH_AUTO) {
+        P->path = tma ? ES_PATH_MAT_TMA : ES_PATH_GENERIC;
+        return ES_OK;
+    }
+    if (forced == ES_PATH_GENERIC || (forced == ES_PATH_MAT_TMA && tma)) {
+        P->path = forced;
+        return ES_OK;
+    }
+    return api_fail(ES_E_UNSUPPORTED, "%s: the forced kernel path %d cannot serve this call", fn, forced);
+}
+
+void fill_matrix_info(const MatPlan& P, es_plan_info* info) {
+    if (info == nullptr) return;
+    std::memset(info, 0, sizeof(*info));
+    info->O = P.L.O;
+    info->T = P.L.T;
+    info->J = P.L.J;
+    info->W = static_cast<int64_t>(P.L.n) * P.L.m;
+    info->seq_width[0] = static_cast<int64_t>(P.L.n) * P.L.n;
+    info->seq_width[1] = static_cast<int64_t>(P.L.n) * P.L.m;
+    info->elements = P.n_out;
+    info->path = P.path;
+    info->reverse = P.L.reverse;
+}
+
+es_status launch_matrix(const char* fn, MatPlan* P, cudaStream_t stream) {
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    es_status st = api_device(&dev, &ds);
+    if (st != ES_OK) return st;
+    MatLaunch& L = P->L;
+    L.status = ds->status;
+    L.wait_ns = api_wait_ns();
+    L.drop_tile = api_drop_tile();
+    L.stream = stream;
+    const char* msg = nullptr;
+    cudaError_t e;
+    if (P->path == ES_PATH_MAT_TMA) {
+        if ((st = api_encoder(&L.encode)) != ES_OK) return st;
+        e = launch_mat_tma(L, &msg);
+    } else {
+        e = launch_mat_generic(L);
+    }
+    if (e != cudaSuccess)
+        return api_fail(ES_E_CUDA, "%s: %s", fn, msg != nullptr ? msg : cudaGetErrorString(e));
+    count_launch();
+    return ES_OK;
+}
+
+// linear-scan of operands that share one shape runs as the element scan of
+// the body (+ (* a h) b) from a zero state: per trip one product and one
+// sum, rounded, in that order -- the one-by-one matrix-scan's arithmetic --
+// on the element-scan skeletons
+es_body_t linear_body() {
+    static es_body_t body = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() { es_body_create("(lambda (h a b) (+ (* a h) b))", &body); });
+    return body;
+}
+
+bool same_shape(const int64_t* a_shape, int a_rank, const int64_t* b_shape, int b_rank) {
+    if (a_rank != b_rank) return false;
+    for (int d = 0; d < a_rank; ++d)
+        if (a_shape[d] != b_shape[d]) return false;
+    return true;
+}
+
+}  // namespace
+}  // namespace es
+
+extern "C" {
+
+es_status es_plan_matrix_scan_f32(const float* a, const int64_t* a_shape, int a_rank, const float* b,
+                                  const int64_t* b_shape, int b_rank, int axis, int reverse, int projective,
+                                  const float* out, es_plan_info* info) {
+    es::MatPlan P{};
+    es_status st = es::plan_matrix("es_matrix_scan_f32", a, a_shape, a_rank, b, b_shape, b_rank, axis, reverse,
+                                   projective, out, false, &P);
+    if (st == ES_OK) st = es::choose_matrix_path("es_matrix_scan_f32", &P);
+    if (st != ES_OK) return st;
+    es::fill_matrix_info(P, info);
+    return ES_OK;
+}
+
+es_status es_matrix_scan_f32(const float* a, const int64_t* a_shape, int a_rank, const float* b,
+                             const int64_t* b_shape, int b_rank, int axis, int reverse, int projective, float* out,
+                             es_stream_t stream) {
+    es::MatPlan P{};
+    es_status st = es::plan_matrix("es_matrix_scan_f32", a, a_shape, a_rank, b, b_shape, b_rank, axis, reverse,
+                                   projective, out, false, &P);
+    if (st == ES_OK) st = es::choose_matrix_path("es_matrix_scan_f32", &P);
+    if (st != ES_OK || P.empty) return st;
+    return es::launch_matrix("es_matrix_scan_f32", &P, reinterpret_cast<cudaStream_t>(stream));
+}
+
+es_status es_plan_linear_scan_f32(const float* a, const int64_t* a_shape, int a_rank, const float* b,
+                                  const int64_t* b_shape, int b_rank, int axis, int reverse, const float* out,
+                                  es_plan_info* info) {
+    es::MatPlan P{};
+    es_status st = es::plan_matrix("es_linear_scan_f32", a, a_shape, a_rank, b, b_shape, b_rank, axis, reverse, 0,
+                                   out, true, &P);
+    if (st != ES_OK) return st;
+    if (!P.empty && es::same_shape(a_shape, a_rank, b_shape, b_rank) && es::api_path_override() != ES_PATH_MAT_TMA) {
+        const float* seqs[2] = {a, b};
+        return es::plan_body_impl(es::linear_body(), nullptr, seqs, 2, a_shape, a_rank, axis, 0, nullptr, reverse,
+                                  out, info, true);
+    }
+    if ((st = es::choose_matrix_path("es_linear_scan_f32", &P)) != ES_OK) return st;
+    es::fill_matrix_info(P, info);
+    return ES_OK;
+}
+
+es_status es_linear_scan_f32(const float* a, const int64_t* a_shape, int a_rank, const float* b,
+                             const int64_t* b_shape, int b_rank, int axis, int reverse, float* out,
+                             es_stream_t stream) {
+    es::MatPlan P{};
+    es_status st = es::plan_matrix("es_linear_scan_f32", a, a_shape, a_rank, b, b_shape, b_rank, axis, reverse, 0,
+                                   out, true, &P);
+    if (st != ES_OK || P.empty) return st;
+    if (es::same_shape(a_shape, a_rank, b_shape, b_rank) && es::api_path_override() != ES_PATH_MAT_TMA) {
+        const float* seqs[2] = {a, b};
+        return es::scan_body_impl(es::linear_body(), nullptr, seqs, 2, a_shape, a_rank, axis, 0, nullptr, reverse,
+                                  out, reinterpret_cast<cudaStream_t>(stream), true);
+    }
+    if ((st = es::choose_matrix_path("es_linear_scan_f32", &P)) != ES_OK) return st;
+    return es::launch_matrix("es_linear_scan_f32", &P, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

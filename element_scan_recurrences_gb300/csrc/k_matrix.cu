@@ -1,0 +1,386 @@
+// k_matrix.cu -- matrix-scan kernels ("Tensor operations": the `matrix-scan`
+// row of the operations table and the section "matrix-scan").
+//
+//     h[t] = a[t] @ h[t-1] + b[t]      from h = 0 (h[T] = 0 in reverse)
+//
+// with a [.., n, n] (n <= 16) and b, h [.., n, m].  "Every column of h is its
+// own recurrence on the shared a", so a lane (one leading position off the
+// axis) is m independent column recurrences: each column is one thread,
+// holding its n values in registers.  A product is the plain definition in
+// f32: for row i the terms a[i][j] * h[j] are rounded and added in the order
+// j = 0..n-1, then b[i] is added (no fused multiply-add), which is also the
+// oracle's order, so the results match it bit for bit.
+//
+// `:projective` (same section): the running product P of a, from the
+// identity, is divided by its largest magnitude after every step, and h by
+// the same number.  P's n columns are n more column recurrences on the same
+// a (no b), carried by n more threads of the lane's group; the largest
+// magnitude is an xor-shuffle maximum over the group (IEEE maximum, so a NaN
+// propagates), and every column is divided by it (IEEE division).
+//
+// Two kernels:
+//   * k_mat_generic: any broadcast of the leading dims (per-dim strides, a
+//     stride of 0 repeats an operand), loads straight from global memory;
+//   * k_mat_tma: dense operands; a producer thread streams {lanes x trips}
+//     tiles of a and b with TMA into an mbarrier ring, the lane's column
+//     threads read a's rows from shared memory (broadcast reads) and their own
+//     column of b, and store their column of h.  Waits are bounded as in the
+//     element-scan pipelines.
+#include <algorithm>
+
+#include "es_device.cuh"
+#include "es_matrix.h"
+
+namespace es {
+namespace {
+
+// this column's update hn = a @ h, row by row: the products a[i][j] * h[j]
+// rounded and added in the order j = 0..N-1.  ROW(i, r) fills r with row i.
+template <int N, class Row>
+__device__ __forceinline__ void column_step(float (&hn)[N], const float (&h)[N], Row row) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        float r[N];
+        row(i, r);
+        float acc = __fmul_rn(r[0], h[0]);
+#pragma unroll
+        for (int j = 1; j < N; ++j) acc = __fadd_rn(acc, __fmul_rn(r[j], h[j]));
+        hn[i] = acc;
+    }
+}
+
+// row i of an N x N block in shared memory (16-byte aligned when N is even)
+template <int N>
+__device__ __forceinline__ void smem_row(const float* A, int i, float (&r)[N]) {
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < N; q += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(A + i * N + q);
+            r[q] = v.x;
+            r[q + 1] = v.y;
+            r[q + 2] = v.z;
+            r[q + 3] = v.w;
+        }
+    } else if constexpr (N % 2 == 0) {
+#pragma unroll
+        for (int q = 0; q < N; q += 2) {
+            const float2 v = *reinterpret_cast<const float2*>(A + i * N + q);
+            r[q] = v.x;
+            r[q + 1] = v.y;
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < N; ++q) r[q] = A[i * N + q];
+    }
+}
+
+// the largest |value| over the lane group of `gp` threads (a power of two)
+__device__ __forceinline__ float group_max_abs(float v, int gp, unsigned mask) {
+    for (int off = gp / 2; off >= 1; off >>= 1) v = ieee_maximum(v, __shfl_xor_sync(mask, v, off));
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// any layout
+
+template <int N, bool PROJ>
+__global__ void __launch_bounds__(128)
+k_mat_generic(const float* __restrict__ a, const float* __restrict__ b, float* __restrict__ out, const MatGeom g,
+              int m, int gp, int reverse) {
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    // projective: a lane is a group of gp threads (columns of h, then of P);
+    // else one thread per column of h
+    const int64_t lane = PROJ ? tid / gp : tid / m;
+    const int c = static_cast<int>(PROJ ? tid % gp : tid % m);
+    const bool live = lane < g.lanes;
+    const bool is_h = c < m;
+    const bool is_p = PROJ && !is_h && c < m + N;
+    // offsets of this lane (in matrices) in a, b and out
+    int64_t oa = 0, ob = 0, oo = 0;
+    {
+        int64_t rem = live ? lane : 0;
+        for (int d = g.nd - 1; d >= 0; --d) {
+            const int64_t q = rem % g.dim[d];
+            rem /= g.dim[d];
+            oa += q * g.sa[d];
+            ob += q * g.sb[d];
+            oo += q * g.so[d];
+        }
+    }
+    float h[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) h[i] = (is_p && i == c - m) ? 1.0f : 0.0f;
+    for (int64_t s = 0; s < g.T; ++s) {
+        const int64_t t = reverse ? g.T - 1 - s : s;
+        float hn[N];
+        if (live) {
+            const float* A = a + (oa + t * g.ta) * N * N;
+            column_step<N>(hn, h, [&](int i, float (&r)[N]) {
+#pragma unroll
+                for (int q = 0; q < N; ++q) r[q] = __ldg(A + i * N + q);
+            });
+            if (is_h) {
+                const float* B = b + (ob + t * g.tb) * N * m + c;
+#pragma unroll
+                for (int i = 0; i < N; ++i) hn[i] = __fadd_rn(hn[i], __ldg(B + i * m));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < N; ++i) hn[i] = 0.0f;
+        }
+        if constexpr (PROJ) {
+            float mx = 0.0f;
+            if (is_p) {
+#pragma unroll
+                for (int i = 0; i < N; ++i) mx = ieee_maximum(mx, fabsf(hn[i]));
+            }
+            const float sc = group_max_abs(mx, gp, 0xffffffffu);
+#pragma unroll
+            for (int i = 0; i < N; ++i) hn[i] = __fdiv_rn(hn[i], sc);
+        }
+#pragma unroll
+        for (int i = 0; i < N; ++i) h[i] = hn[i];
+        if (live && is_h) {
+            float* O = out + (oo + t * g.to) * N * m + c;
+#pragma unroll
+            for (int i = 0; i < N; ++i) __stcs(O + i * m, h[i]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dense operands, TMA pipeline
+
+constexpr int kMatMaxStages = 4;
+constexpr int kMatConsumers = 128;
+
+template <int N, bool PROJ>
+__global__ void __launch_bounds__(32 + kMatConsumers)
+k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+          float* __restrict__ out, int T, int J, int m, int gp, int LPC, int tiles_j, int TT, int stages, int reverse,
+          unsigned int* status, uint64_t wait_ns, int64_t drop_tile) {
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kMatMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kMatMaxStages];
+    __shared__ int abort_flag;
+
+    const int consumers = LPC * gp;                         // a multiple of 32, at most kMatConsumers
+    const uint32_t a_floats = static_cast<uint32_t>(TT) * LPC * N * N;
+    const uint32_t b_floats = static_cast<uint32_t>(TT) * LPC * N * m;
+    // every tile starts on a 128-byte boundary
+    const uint32_t a_pad = (a_floats + 31u) & ~31u;
+    const uint32_t stage_floats = (a_pad + b_floats + 31u) & ~31u;
+    const uint32_t stage_bytes = (a_floats + b_floats) * 4u;   // bytes the two copies bring
+    float* tiles = reinterpret_cast<float*>(smem_raw + smem_align_pad(smem_raw));
+
+    const int o = blockIdx.x / tiles_j;
+    const int j0 = (blockIdx.x % tiles_j) * LPC;
+    const int ntiles = (T + TT - 1) / TT;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], consumers / 32);
+        }
+        abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&map_a);
+            tma_prefetch_desc(&map_b);
+            const uint64_t pol = l2_policy_stream();
+            int issued = 0;
+            for (int k = 0; k < ntiles; ++k) {
+                const int s = k % stages;
+                const int round = k / stages;
+                if (round > 0 && !mbar_wait_bounded(&empty_bar[s], (round - 1) & 1, wait_ns, &abort_flag)) {
+                    report_timeout(status, &abort_flag);
+                    break;
+                }
+                issued = k + 1;
+                if (k == drop_tile) continue;   // testing hook: this tile never arrives
+                const int jt = reverse ? ntiles - 1 - k : k;
+                float* st = tiles + static_cast<size_t>(s) * stage_floats;
+                mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
+                tma_load_4d(st, &map_a, 0, j0, jt * TT, o, &full_bar[s], pol);
+                tma_load_4d(st + a_pad, &map_b, 0, j0, jt * TT, o, &full_bar[s], pol);
+            }
+            for (int k = max(0, issued - stages); k < issued; ++k) {
+                if (k == drop_tile) continue;
+                if (!mbar_wait_bounded(&full_bar[k % stages], (k / stages) & 1, wait_ns, nullptr))
+                    atomicOr(status, ES_DEVICE_TIMEOUT);
+            }
+        }
+        return;
+    }
+
+    // consumers: thread (l, c) is column c of lane j0 + l (columns of h, then of P)
+    const int ct = threadIdx.x - 32;
+    (void)consumers;
+    const int l = ct / gp;
+    const int c = ct % gp;
+    const bool valid = j0 + l < J;
+    const bool is_h = c < m;
+    const bool is_p = PROJ && !is_h && c < m + N;
+    const int64_t lane_block = static_cast<int64_t>(N) * m;           // floats of h per lane and trip
+    float* obase = out + (static_cast<int64_t>(o) * T * J + j0 + l) * lane_block + c;
+    const int64_t trip_stride = static_cast<int64_t>(J) * lane_block;
+    float h[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) h[i] = (is_p && i == c - m) ? 1.0f : 0.0f;
+
+    for (int k = 0; k < ntiles; ++k) {
+        const int s = k % stages;
+        const bool ok = mbar_wait_bounded(&full_bar[s], (k / stages) & 1, wait_ns, &abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (!ok) report_timeout(status, &abort_flag);
+            break;
+        }
+        const int jt = reverse ? ntiles - 1 - k : k;
+        const int t0 = jt * TT;
+        const int n = min(TT, T - t0);
+        const float* sa = tiles + static_cast<size_t>(s) * stage_floats;
+        const float* sb = sa + a_pad;
+        for (int q = 0; q < n; ++q) {
+            const int tt = reverse ? n - 1 - q : q;
+            const float* A = sa + (static_cast<uint32_t>(tt) * LPC + l) * (N * N);
+            float hn[N];
+            column_step<N>(hn, h, [&](int i, float (&r)[N]) { smem_row<N>(A, i, r); });
+            if (is_h) {
+                const float* B = sb + (static_cast<uint32_t>(tt) * LPC + l) * (N * m) + c;
+#pragma unroll
+                for (int i = 0; i < N; ++i) hn[i] = __fadd_rn(hn[i], B[i * m]);
+            }
+            if constexpr (PROJ) {
+                float mx = 0.0f;
+                if (is_p) {
+#pragma unroll
+                    for (int i = 0; i < N; ++i) mx = ieee_maximum(mx, fabsf(hn[i]));
+                }
+                const float sc = group_max_abs(mx, gp, 0xffffffffu);
+#pragma unroll
+                for (int i = 0; i < N; ++i) hn[i] = __fdiv_rn(hn[i], sc);
+            }
+#pragma unroll
+            for (int i = 0; i < N; ++i) h[i] = hn[i];
+            if (valid && is_h) {
+                float* op = obase + static_cast<int64_t>(t0 + tt) * trip_stride;
+#pragma unroll
+                for (int i = 0; i < N; ++i) __stcs(op + i * m, h[i]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+    }
+}
+
+template <int N>
+cudaError_t launch_generic_n(const MatLaunch& L) {
+    const int gp = L.gp;
+    const int64_t threads_total = L.projective ? L.g.lanes * gp : L.g.lanes * L.m;
+    const int64_t blocks = (threads_total + 127) / 128;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (L.projective)
+        k_mat_generic<N, true><<<static_cast<unsigned>(blocks), 128, 0, L.stream>>>(L.a, L.b, L.out, L.g, L.m, gp,
+                                                                                   L.reverse);
+    else
+        k_mat_generic<N, false><<<static_cast<unsigned>(blocks), 128, 0, L.stream>>>(L.a, L.b, L.out, L.g, L.m, gp,
+                                                                                    L.reverse);
+    return cudaGetLastError();
+}
+
+template <int N>
+cudaError_t launch_tma_n(const MatLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb, int lpc, int tiles_j,
+                         int TT, int stages, size_t smem) {
+    auto kern = L.projective ? k_mat_tma<N, true> : k_mat_tma<N, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kern<<<static_cast<unsigned>(L.O * tiles_j), 32 + lpc * L.gp, smem, L.stream>>>(
+        ma, mb, L.out, static_cast<int>(L.T), static_cast<int>(L.J), L.m, L.gp, lpc, tiles_j, TT, stages, L.reverse,
+        L.status, L.wait_ns, L.drop_tile);
+    return cudaGetLastError();
+}
+
+// Lanes per CTA: 128 consumer threads, fewer (down to one warp) while one
+// trip of the tile would pass 32 KB; then trips per stage: about 32 KB.
+void mat_tile_shape(int n, int m, int gp, int* lpc, int* TT) {
+    auto per_trip = [&](int l) { return static_cast<int64_t>(l) * (n * n + n * m) * 4; };
+    int l = kMatConsumers / gp;
+    while (l * gp > 32 && per_trip(l) > 32 * 1024) l /= 2;
+    *lpc = l;
+    *TT = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(64, (32 * 1024) / per_trip(l))));
+}
+
+bool encode_blocks(EncodeTiledFn encode, CUtensorMap* map, const float* base, int64_t block, int64_t J, int64_t T,
+                   int64_t O, int LPC, int TT) {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(block), static_cast<cuuint64_t>(J),
+                                static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(O)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(block) * 4, static_cast<cuuint64_t>(block * J) * 4,
+                                   static_cast<cuuint64_t>(block * J * T) * 4};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(block), static_cast<cuuint32_t>(LPC),
+                               static_cast<cuuint32_t>(TT), 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_mat_generic(const MatLaunch& L) {
+    switch (L.n) {
+#define ES_MAT_CASE(K) \
+    case K: return launch_generic_n<K>(L);
+        ES_MAT_CASE(1) ES_MAT_CASE(2) ES_MAT_CASE(3) ES_MAT_CASE(4) ES_MAT_CASE(5) ES_MAT_CASE(6) ES_MAT_CASE(7)
+        ES_MAT_CASE(8) ES_MAT_CASE(9) ES_MAT_CASE(10) ES_MAT_CASE(11) ES_MAT_CASE(12) ES_MAT_CASE(13)
+        ES_MAT_CASE(14) ES_MAT_CASE(15) ES_MAT_CASE(16)
+#undef ES_MAT_CASE
+    }
+    return cudaErrorInvalidValue;
+}
+
+bool mat_tma_ok(int n, int m, int gp, bool projective, int64_t O, int64_t T, int64_t J, bool dense,
+                const void* a, const void* b) {
+    if (!dense) return false;
+    if (n != 2 && n != 4 && n != 8 && n != 16) return false;
+    if ((static_cast<int64_t>(n) * m) % 4 != 0 || static_cast<int64_t>(n) * m > 256) return false;   // boxes, strides
+    if (gp > 32 || (!projective && m > 32)) return false;
+    (void)projective;
+    if (O >= (int64_t(1) << 31) || T >= (int64_t(1) << 31) || J >= (int64_t(1) << 31)) return false;
+    int LPC = 0, TT = 0;
+    mat_tile_shape(n, m, gp, &LPC, &TT);
+    if (O * ((J + LPC - 1) / LPC) >= (int64_t(1) << 31)) return false;
+    return reinterpret_cast<uintptr_t>(a) % 16 == 0 && reinterpret_cast<uintptr_t>(b) % 16 == 0;
+}
+
+cudaError_t launch_mat_tma(const MatLaunch& L, const char** err) {
+    const int n = L.n, m = L.m;
+    int LPC = 0, TT = 0;
+    mat_tile_shape(n, m, L.gp, &LPC, &TT);
+    const int stages = 3;
+    // a stage as the kernel lays it out: each tile on a 128-byte boundary
+    const int64_t a_pad = (static_cast<int64_t>(TT) * LPC * n * n + 31) & ~int64_t(31);
+    const int64_t stage_floats = (a_pad + static_cast<int64_t>(TT) * LPC * n * m + 31) & ~int64_t(31);
+    const int64_t tiles_j = (L.J + LPC - 1) / LPC;
+    CUtensorMap ma, mb;
+    if (!encode_blocks(L.encode, &ma, L.a, static_cast<int64_t>(n) * n, L.J, L.T, L.O, LPC, TT) ||
+        !encode_blocks(L.encode, &mb, L.b, static_cast<int64_t>(n) * m, L.J, L.T, L.O, LPC, TT)) {
+        *err = "cuTensorMapEncodeTiled failed for a matrix-scan tile map";
+        return cudaErrorInvalidValue;
+    }
+    const size_t smem = static_cast<size_t>(stages) * stage_floats * 4 + 1024;
+    const int tj = static_cast<int>(tiles_j);
+    switch (n) {
+        case 2: return launch_tma_n<2>(L, ma, mb, LPC, tj, TT, stages, smem);
+        case 4: return launch_tma_n<4>(L, ma, mb, LPC, tj, TT, stages, smem);
+        case 8: return launch_tma_n<8>(L, ma, mb, LPC, tj, TT, stages, smem);
+        default: return launch_tma_n<16>(L, ma, mb, LPC, tj, TT, stages, smem);
+    }
+}
+
+}  // namespace es

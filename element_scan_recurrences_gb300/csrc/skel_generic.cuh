@@ -24,7 +24,7 @@ k_body_generic(const SeqPtrs seqs, const float* __restrict__ init, float* __rest
 
     float h[W];
 #pragma unroll
-    for (int w = 0; w < W; ++w) h[w] = init[lane * W + w];
+    for (int w = 0; w < W; ++w) h[w] = init != nullptr ? init[lane * W + w] : 0.0f;   // null: from zero
 
     float sw[Body::kSW][W];
     float sn[Body::kSN];

@@ -89,7 +89,7 @@ k_body_lane(const __grid_constant__ TmaMaps<Body::kNS> maps, const float* __rest
     const int c = threadIdx.x - 32;
     const int i = i0 + c;
     const bool valid = i < I;
-    float h = valid ? init[static_cast<int64_t>(o) * I + i] : 0.0f;
+    float h = valid && init != nullptr ? init[static_cast<int64_t>(o) * I + i] : 0.0f;   // null: from zero
     float* obase = out + static_cast<int64_t>(o) * T * I + i;
 
     for (int k = 0; k < ntiles; ++k) {

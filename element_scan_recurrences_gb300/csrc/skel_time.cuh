@@ -92,7 +92,7 @@ k_body_time(const __grid_constant__ TmaMaps<Body::kNS + 1> maps, const float* __
     // consumers: thread r owns row o0 + r
     const int r = threadIdx.x - 32;
     const bool valid = o0 + r < O;
-    float h = valid ? init[o0 + r] : 0.0f;
+    float h = valid && init != nullptr ? init[o0 + r] : 0.0f;   // null: from zero
     const uint32_t row_off = static_cast<uint32_t>(r) * 128u;
     const uint32_t swz = static_cast<uint32_t>(r & 7);   // 128-byte swizzle: chunk q lives at q ^ (row % 8)
     const bool storer = (threadIdx.x == 32);

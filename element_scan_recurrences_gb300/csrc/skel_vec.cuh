@@ -138,7 +138,8 @@ k_body_vec(const __grid_constant__ TmaMaps<Body::kNS> maps, const float* __restr
     const int64_t row = static_cast<int64_t>(J) * W;
     float h[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) h[e] = valid ? init[(static_cast<int64_t>(o) * J + j0 + v) * W + w0 + e] : 0.0f;
+    for (int e = 0; e < E; ++e)   // a null `init`: from zero
+        h[e] = valid && init != nullptr ? init[(static_cast<int64_t>(o) * J + j0 + v) * W + w0 + e] : 0.0f;
     float* obase = out + static_cast<int64_t>(o) * T * row + static_cast<int64_t>(j0) * W + c * E;
 
     for (int k = 0; k < ntiles; ++k) {

@@ -76,7 +76,8 @@ typedef enum es_path {
     ES_PATH_GENERIC = 2,   /* one thread per lane, direct loads, any layout    */
     ES_PATH_LANE_TMA = 3,  /* lanes innermost: TMA/mbarrier time-tile pipeline */
     ES_PATH_TIME_TMA = 4,  /* time innermost: TMA tiles transposed in SMEM     */
-    ES_PATH_VEC_TMA = 5    /* vector state: TMA pipeline + xor shuffles        */
+    ES_PATH_VEC_TMA = 5,   /* vector state: TMA pipeline + xor shuffles        */
+    ES_PATH_MAT_TMA = 6    /* matrix-scan, dense operands: TMA pipeline        */
 } es_path;
 
 /*
@@ -246,6 +247,66 @@ es_status es_body_prepare(es_body_t body, int state_width, int n_seqs, const int
 
 /* NVRTC compilations so far in this process (kernel cache misses). */
 uint64_t es_body_compile_count(void);
+
+/*
+ * es_matrix_scan_f32 -- matrix-scan ("Tensor operations", the `matrix-scan`
+ * row of the operations table and the section "matrix-scan"):
+ *
+ *     h[t] = a[t] @ h[t-1] + b[t]    along `axis`, from h = 0 (so h[0] = b[0])
+ *
+ * and with `reverse` from the last position (h[T] = 0).  Every column of h
+ * is its own recurrence on the shared a.
+ *   a, a_shape, a_rank  device f32, shape lead_a + [n, n], n in 1..16.
+ *   b, b_shape, b_rank  device f32, shape lead_b + [n, m], m >= 1.
+ *                       lead_a and lead_b broadcast NumPy-style (right
+ *                       aligned, each dim equal or 1) to one leading shape
+ *                       of rank 1..ES_MAX_RANK.
+ *   axis                counts among the leading dims (negative from the
+ *                       end: -1 is the one before the matrices); its length
+ *                       is at least one.
+ *   projective          nonzero: the running product P of a, from the
+ *                       identity, is divided by its largest magnitude after
+ *                       every step, and h by the same number (for products of
+ *                       projective maps that would overflow f32); needs
+ *                       n + m <= 32.
+ *   out                 device f32, the broadcast leading shape + [n, m];
+ *                       must not overlap a or b.
+ * Arithmetic: f32; each product a[i][j] * h[j][k] and each sum rounded, the
+ * terms added in the order j = 0..n-1, then b[i][k] added (no fused
+ * multiply-add); the projective scaling is an IEEE maximum of |P| and IEEE
+ * divisions.  Shape errors are ES_E_DIM_001.  Dense operands (no broadcast)
+ * with n in {2, 4, 8, 16}, n*m a multiple of 4 and at most 256, and 16-byte
+ * aligned pointers take the TMA kernel (ES_PATH_MAT_TMA); anything else the
+ * generic one.  Asynchronous on `stream`; no allocation.
+ */
+es_status es_matrix_scan_f32(const float *a, const int64_t *a_shape, int a_rank,
+                             const float *b, const int64_t *b_shape, int b_rank,
+                             int axis, int reverse, int projective, float *out,
+                             es_stream_t stream);
+
+/* Plan of a matrix-scan call (validation and kernel path; no CUDA call).
+ * info: O, T, J the leading dims before, along and after the axis; W = n*m;
+ * seq_width = {n*n, n*m}. */
+es_status es_plan_matrix_scan_f32(const float *a, const int64_t *a_shape, int a_rank,
+                                  const float *b, const int64_t *b_shape, int b_rank,
+                                  int axis, int reverse, int projective, const float *out,
+                                  es_plan_info *info);
+
+/*
+ * es_linear_scan_f32 -- linear-scan, the matrix-scan over one-by-one matrices
+ * ("matrix-scan" section): h[t] = a[t] * h[t-1] + b[t] from h = 0, with a and
+ * b broadcast NumPy-style to one shape (rank 0 is a number), `axis` counting
+ * among its dims.  Same arithmetic (one product and one sum, rounded, in that
+ * order).  Operands of one shape run on the element-scan kernels (lanes or
+ * time innermost); broadcast operands on the generic matrix-scan kernel.
+ */
+es_status es_linear_scan_f32(const float *a, const int64_t *a_shape, int a_rank,
+                             const float *b, const int64_t *b_shape, int b_rank,
+                             int axis, int reverse, float *out, es_stream_t stream);
+
+es_status es_plan_linear_scan_f32(const float *a, const int64_t *a_shape, int a_rank,
+                                  const float *b, const int64_t *b_shape, int b_rank,
+                                  int axis, int reverse, const float *out, es_plan_info *info);
 
 /* Synchronise `stream`, then read and clear this device's status word.
  * Returns ES_E_TIMEOUT if a kernel since the last check gave up a bounded

@@ -1,0 +1,51 @@
+"""matrix-scan and linear-scan through the C ABI without a GPU: the library
+rejects the shapes the oracle rejects and plans the documented kernels."""
+import numpy as np
+import pytest
+
+import matrix_pins
+import oracle.matrix as M
+from element_scan_recurrences_gb300 import binding as es
+
+
+@pytest.mark.parametrize("case", matrix_pins.REJECTED, ids=[str(r) for r in matrix_pins.REJECTED])
+def test_library_rejects_what_the_oracle_rejects(case):
+    sa, sb, axis = case
+    with pytest.raises(ValueError):
+        M.matrix_scan(np.zeros(sa, np.float32), np.zeros(sb, np.float32), axis=axis)
+    with pytest.raises(es.EsError) as e:
+        es.plan_matrix_scan(sa, sb, axis)
+    assert e.value.status == 1
+
+
+def test_matrix_plans():
+    p = es.plan_matrix_scan([64, 1024, 16, 16, 16], [64, 1024, 16, 16, 16], axis=1)
+    assert p["path"] == "mat_tma" and (p["O"], p["T"], p["J"], p["W"]) == (64, 1024, 16, 256)
+    # broadcast a (shared by the batch), odd n, or n*m not a multiple of 4: generic
+    assert es.plan_matrix_scan([1, 1024, 1, 16, 16], [64, 1024, 16, 16, 16], axis=1)["path"] == "generic"
+    assert es.plan_matrix_scan([8, 100, 3, 3], [8, 100, 3, 5], axis=1)["path"] == "generic"
+    assert es.plan_matrix_scan([8, 100, 2, 2], [8, 100, 2, 1], axis=1)["path"] == "generic"
+    assert es.plan_matrix_scan([8, 100, 2, 2], [8, 100, 2, 2], axis=1)["path"] == "mat_tma"
+    # projective: n + m <= 32
+    assert es.plan_matrix_scan([8, 100, 16, 16], [8, 100, 16, 16], axis=1, projective=True)["path"] == "mat_tma"
+    with pytest.raises(es.EsError) as e:
+        es.plan_matrix_scan([8, 100, 16, 16], [8, 100, 16, 17], axis=1, projective=True)
+    assert e.value.status == 4
+    # empty lanes
+    assert es.plan_matrix_scan([0, 100, 4, 4], [0, 100, 4, 4], axis=1)["path"] == "empty"
+    # the axis counts among the leading dims
+    p = es.plan_matrix_scan([5, 7, 4, 4], [5, 7, 4, 3], axis=-1)
+    assert (p["O"], p["T"], p["J"]) == (5, 7, 1)
+    # out may not overlap an input
+    with pytest.raises(es.EsError) as e:
+        es.plan_matrix_scan([5, 7, 4, 4], [5, 7, 4, 4], axis=0, ptrs=[1 << 44, 2 << 44, (1 << 44) + 16])
+    assert e.value.status == 3
+
+
+def test_linear_plans():
+    assert es.plan_linear_scan([64, 4096, 1024], [64, 4096, 1024], axis=1)["path"] == "lane_tma"
+    assert es.plan_linear_scan([262144, 1024], [262144, 1024], axis=-1)["path"] == "time_tma"
+    assert es.plan_linear_scan([], [64, 4096, 1024], axis=1)["path"] == "generic"        # a number
+    assert es.plan_linear_scan([64, 1, 1024], [64, 4096, 1024], axis=1)["path"] == "generic"
+    with pytest.raises(es.EsError):
+        es.plan_linear_scan([3, 4], [4, 4], axis=0)

@@ -1,0 +1,150 @@
+"""matrix-scan and linear-scan on the GPU against the oracle, bit for bit: the
+kernels form every product and sum in the oracle's order (products rounded,
+terms added j = 0..n-1, then b), so nothing is left to a tolerance.  Cases
+span several lane and trip tiles with ragged tails, broadcasts, reverse and
+projective scans, on both the generic and the TMA kernel."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.matrix as M
+from element_scan_recurrences_gb300 import binding as es
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_ready():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    es.lib()
+    yield
+    es.set_path_override("auto")
+
+
+def bitwise(got, want, what):
+    got = np.ascontiguousarray(got, np.float32)
+    want = np.ascontiguousarray(want, np.float32)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    bad = got.view(np.uint32) != want.view(np.uint32)
+    assert not bad.any(), "%s: %d of %d values differ; first at %s: %r vs %r" % (
+        what, int(bad.sum()), bad.size, np.argwhere(bad)[0], got[bad][0], want[bad][0])
+
+
+def contractive(rng, shape, n, norm=0.95):
+    a = rng.standard_normal(shape + (n, n))
+    s = np.linalg.norm(a, ord=2, axis=(-2, -1))[..., None, None]
+    return (a / s * norm).astype(np.float32)
+
+
+def run(a, b, axis, reverse=False, projective=False, path="auto", expect=None):
+    es.set_path_override(path)
+    try:
+        da, db = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+        if expect is not None:
+            assert es.plan_matrix_scan(a.shape, b.shape, axis, reverse, projective)["path"] == expect
+        got = es.matrix_scan(da, db, axis=axis, reverse=reverse, projective=projective)
+        es.device_status()
+        return got.cpu().numpy()
+    finally:
+        es.set_path_override("auto")
+
+
+TMA_CASES = [(2, 2), (4, 1), (4, 4), (8, 4), (8, 8), (16, 1), (16, 4), (16, 16)]
+
+
+@pytest.mark.parametrize("projective", [False, True], ids=["plain", "projective"])
+@pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
+@pytest.mark.parametrize("n,m", TMA_CASES, ids=["n%dm%d" % c for c in TMA_CASES])
+def test_matrix_tma(n, m, reverse, projective):
+    if projective and n + m > 32:
+        pytest.skip("projective scans carry n + m <= 32 columns")
+    rng = np.random.default_rng(n * 100 + m)
+    # several lane tiles with a ragged last one, several trip tiles with a ragged last one
+    O, T, J = 3, 37, 21
+    a = contractive(rng, (O, T, J), n)
+    if projective:
+        a = (a * 3).astype(np.float32)
+    b = rng.standard_normal((O, T, J, n, m)).astype(np.float32)
+    got = run(a, b, 1, reverse, projective, expect="mat_tma")
+    bitwise(got, M.matrix_scan(a, b, axis=1, reverse=reverse, projective=projective), "tma n=%d m=%d" % (n, m))
+
+
+GENERIC_CASES = [(1, 1), (3, 5), (5, 2), (7, 7), (16, 16), (16, 40), (12, 3)]
+
+
+@pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
+@pytest.mark.parametrize("n,m", GENERIC_CASES, ids=["n%dm%d" % c for c in GENERIC_CASES])
+def test_matrix_generic(n, m, reverse):
+    rng = np.random.default_rng(7 * n + m)
+    a = contractive(rng, (2, 23, 3), n)
+    b = rng.standard_normal((2, 23, 3, n, m)).astype(np.float32)
+    got = run(a, b, 1, reverse, path="generic")
+    bitwise(got, M.matrix_scan(a, b, axis=1, reverse=reverse), "generic n=%d m=%d" % (n, m))
+    if n + m <= 32:
+        ap = (a * 3).astype(np.float32)
+        got = run(ap, b, 1, reverse, projective=True, path="generic")
+        bitwise(got, M.matrix_scan(ap, b, axis=1, reverse=reverse, projective=True), "generic projective")
+
+
+def test_matrix_broadcasts_and_axes():
+    rng = np.random.default_rng(3)
+    n, m = 4, 3
+    b = rng.standard_normal((4, 19, 5, n, m)).astype(np.float32)
+    a_full = contractive(rng, (4, 19, 5), n)
+    for a, what in ((a_full[:1], "a shared by the batch"), (a_full[:, :1], "a constant in time"),
+                    (a_full[0, 0], "one a for every lane and trip"), (a_full[:, :, :1], "a shared by the heads")):
+        got = run(np.ascontiguousarray(a), b, 1, expect="generic")
+        bitwise(got, M.matrix_scan(a, b, axis=1), what)
+    # b broadcast, the axis elsewhere, negative axes
+    got = run(a_full, np.ascontiguousarray(b[:1]), 1)
+    bitwise(got, M.matrix_scan(a_full, b[:1], axis=1), "b shared by the batch")
+    for axis in (0, 2, -1, -3):
+        got = run(a_full, b, axis)
+        bitwise(got, M.matrix_scan(a_full, b, axis=axis), "axis %d" % axis)
+
+
+def test_delta_rule_recall():
+    """The pages' delta rule through the TMA kernel: unit keys, beta = 1, so
+    every written value is read back under its key."""
+    rng = np.random.default_rng(4)
+    B, T, n, m = 8, 64, 16, 16
+    k = rng.standard_normal((B, T, n))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, T, m))
+    a = (np.eye(n) - k[..., :, None] * k[..., None, :]).astype(np.float32)
+    b = (k[..., :, None] * v[..., None, :]).astype(np.float32)
+    got = run(a, b, 1, expect="mat_tma")
+    bitwise(got, M.matrix_scan(a, b, axis=1), "delta rule")
+    S = got.astype(np.float64)
+    assert np.allclose(np.einsum("btnm,btn->btm", S, k), v, atol=5e-5)
+
+
+def test_linear_scan_paths():
+    rng = np.random.default_rng(5)
+    a = rng.uniform(0.5, 1.0, (3, 70, 200)).astype(np.float32)
+    b = rng.standard_normal((3, 70, 200)).astype(np.float32)
+    da, db = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    for reverse in (False, True):
+        want = M.linear_scan(a, b, axis=1, reverse=reverse)
+        assert es.plan_linear_scan(a.shape, b.shape, 1, reverse)["path"] == "lane_tma"
+        bitwise(es.linear_scan(da, db, axis=1, reverse=reverse).cpu().numpy(), want, "lanes innermost")
+        es.set_path_override("generic")
+        try:
+            bitwise(es.linear_scan(da, db, axis=1, reverse=reverse).cpu().numpy(), want, "generic")
+        finally:
+            es.set_path_override("auto")
+    # the sequence axis last
+    at, bt = np.ascontiguousarray(a.reshape(600, 70)[:, :68]), np.ascontiguousarray(b.reshape(600, 70)[:, :68])
+    assert es.plan_linear_scan(at.shape, bt.shape, -1)["path"] == "time_tma"
+    got = es.linear_scan(torch.from_numpy(at).cuda(), torch.from_numpy(bt).cuda(), axis=-1)
+    bitwise(got.cpu().numpy(), M.linear_scan(at, bt, axis=-1), "time innermost")
+    # numbers and broadcasts: the generic matrix kernel
+    got = es.linear_scan(0.9, db, axis=1)
+    bitwise(got.cpu().numpy(), M.linear_scan(np.float32(0.9), b, axis=1), "a number")
+    got = es.linear_scan(torch.from_numpy(a[:, :1]).cuda(), db, axis=1, reverse=True)
+    bitwise(got.cpu().numpy(), M.linear_scan(a[:, :1], b, axis=1, reverse=True), "a constant in time")
+    # cumsum
+    got = es.linear_scan(1.0, db, axis=1)
+    bitwise(got.cpu().numpy(), np.add.accumulate(b, axis=1, dtype=np.float32), "cumsum")
+    es.device_status()
