@@ -343,11 +343,81 @@ def config_of(w, backward=False):
             "l2": "no flush: inputs and outputs (%.2f GB) exceed the 129 MB L2" % (alg / 1e9)}
 
 
-def run_ours(args, w):
+def time_device_steps(step, stream, device, dist, args, rank, local, es):
+    """W untimed warm-up steps, then K timed steps bracketed by a barrier and a
+    synchronize on both sides; CUDA events on the launching stream.  Returns
+    (region ms over the slowest rank, per-step ms, kernel launches, clocks)."""
+    import torch
+    sampler = ClockSampler(local) if rank == 0 else None
+    for _ in range(max(args.warmup, 0)):
+        step()
+    es.device_status(stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    launches0 = es.launch_count()
+    t_host0 = time.time()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(device)
+    t_host1 = time.time()
+    barrier(dist, device)
+    launches = es.launch_count() - launches0
+    es.device_status(stream)
+    per_step_ms = [st.elapsed_time(e) for st, e in zip(starts, ends)]
+    region_ms = max_over_ranks(dist, starts[0].elapsed_time(ends[-1]), device)
+    clocks = None
+    if sampler is not None:
+        sampler.stop()
+        clocks = sampler.summary(t_host0, t_host1)
+    return region_ms, per_step_ms, launches, clocks
+
+
+def time_e2e(e2e_step, steps, stream, device, dist):
+    """One untimed end-to-end step, then `steps` timed ones (events on the
+    stream the copies and kernels run on); ms over the slowest rank."""
+    import torch
+    e2e_step()
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    return max_over_ranks(dist, e0.elapsed_time(e1), device)
+
+
+def roofline_of(kernel, prof_name, alg_bytes, kernel_ms):
+    peak, peak_kind = measured_peaks()
+    achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": profiled_traffic(kernel, prof_name), "kernel": kernel,
+            "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": kernel_ms,
+            "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs, copy burst)" % peak_kind
+            if peak_kind == "measured" else "fallback 6.8 TB/s"}
+
+
+def emit_line(args, world, value, region_ms, config, roofline, cpu, e2e, launches, clocks):
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": region_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
+        "achieved_gbs": roofline["achieved"], "hbm_frac": roofline["frac"],
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def gpu_setup():
     import torch
     from element_scan_recurrences_gb300 import binding as es
-    from element_scan_recurrences_gb300 import workloads as wl
-
     rank, world, local = dist_env()
     if not torch.cuda.is_available():
         raise RuntimeError("bench.py needs a CUDA device; the library has no CPU path")
@@ -355,7 +425,14 @@ def run_ours(args, w):
     device = torch.device("cuda", local)
     dist = init_dist(world, "nccl")
     es.lib()
+    return es, rank, world, local, device, dist
 
+
+def run_ours(args, w):
+    import torch
+    from element_scan_recurrences_gb300 import workloads as wl
+
+    es, rank, world, local, device, dist = gpu_setup()
     # weak scaling: each rank scans its own batch of the workload (own seed)
     init, seqs = wl.make_inputs(w, device, seed=w.seed + rank)
     out = torch.empty(w.shape, device=device, dtype=torch.float32)
@@ -393,52 +470,17 @@ def run_ours(args, w):
         for o, r in zip(outs, w.reverse):
             scan_into(o, r)
 
-    sampler = ClockSampler(local) if rank == 0 else None
-    for _ in range(max(args.warmup, 0)):
-        step()
-    es.device_status(stream)
-
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier(dist, device)
-    torch.cuda.synchronize(device)
-    launches0 = es.launch_count()
-    t_host0 = time.time()
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize(device)
-    t_host1 = time.time()
-    barrier(dist, device)
-    launches = es.launch_count() - launches0
-    es.device_status(stream)
-    per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    region_ms = starts[0].elapsed_time(ends[-1])
-    region_ms = max_over_ranks(dist, region_ms, device)
-    if sampler is not None:
-        sampler.stop()
-        clocks = sampler.summary(t_host0, t_host1)
-    else:
-        clocks = None
-
+    region_ms, per_step_ms, launches, clocks = time_device_steps(step, stream, device, dist, args, rank, local, es)
     elems_step = w.elements * len(w.reverse)
     total_elems = sum_over_ranks(dist, float(elems_step * args.steps), device)
     value = total_elems / (region_ms / 1e3)
     kernel_ms = sum(per_step_ms) / len(per_step_ms) / len(w.reverse)
 
     # roofline of the dominant kernel (every launch of a step is the same kernel)
-    peak, peak_kind = measured_peaks()
     alg_bytes = w.backward_algorithmic_bytes() if backward else w.algorithmic_bytes()
-    achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
     kernels = PATH_KERNEL_BWD if backward else PATH_KERNEL_BODY if program is not None else PATH_KERNEL
     kernel = kernels.get(plans[0]["path"], plans[0]["path"])
-    prof_name = w.name + ("_backward" if backward else "")
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": profiled_traffic(kernel, prof_name), "kernel": kernel,
-                "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": kernel_ms,
-                "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs, copy burst)" % peak_kind
-                if peak_kind == "measured" else "fallback 6.8 TB/s"}
+    roofline = roofline_of(kernel, w.name + ("_backward" if backward else ""), alg_bytes, kernel_ms)
 
     # end to end through the public API with host buffers
     e2e = None
@@ -483,18 +525,7 @@ def run_ours(args, w):
                     es.scan_host(w.body, init_h, seqs_h, oh, (init, seqs, od), axis=w.axis,
                                  state_axis=w.state_axis, reverse=r, stream=stream)
 
-        e2e_step()
-        torch.cuda.synchronize(device)
-        barrier(dist, device)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize(device)
-        barrier(dist, device)
-        e_ms = max_over_ranks(dist, e0.elapsed_time(e1), device)
+        e_ms = time_e2e(e2e_step, e2e_steps, stream, device, dist)
         e2e = {"value": sum_over_ranks(dist, float(elems_step * e2e_steps), device) / (e_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": h2d * (len(w.reverse)), "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "ms_per_step": e_ms / e2e_steps}
@@ -506,19 +537,167 @@ def run_ours(args, w):
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
 
     if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": region_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": dict(config_of(w, backward), parallelism="replicas: each GPU scans its own batch"
-                           if world > 1 else "single GPU", path=plans[0]["path"]),
-            "achieved_gbs": achieved, "hbm_frac": achieved / peak,
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clocks,
-        }
-        print(json.dumps(line), flush=True)
+        config = dict(config_of(w, backward), parallelism="replicas: each GPU scans its own batch"
+                      if world > 1 else "single GPU", path=plans[0]["path"])
+        emit_line(args, world, value, region_ms, config, roofline, cpu, e2e, launches, clocks)
     if dist is not None:
         dist.destroy_process_group()
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# matrix-scan / linear-scan workloads
+
+MATRIX_KERNEL = {"mat_tma": "k_mat_tma", "generic": "k_mat_generic", "lane_tma": "k_body_lane",
+                 "time_tma": "k_body_time"}
+KERNEL_SOURCES.update({"k_mat_tma": ["k_matrix.cu", "es_matrix_api.cu"],
+                       "k_mat_generic": ["k_matrix.cu", "es_matrix_api.cu"]})
+
+
+def matrix_scan_call(es, w, a, b, out, reverse, stream):
+    if w.kind == "linear":
+        es.linear_scan(a, b, axis=w.axis, reverse=reverse, out=out, stream=stream)
+    else:
+        es.matrix_scan(a, b, axis=w.axis, reverse=reverse, projective=w.projective, out=out, stream=stream)
+
+
+def matrix_plan(es, w, reverse):
+    if w.kind == "linear":
+        return es.plan_linear_scan(w.a_shape, w.b_shape, w.axis, reverse)
+    return es.plan_matrix_scan(w.a_shape, w.b_shape, w.axis, reverse, w.projective)
+
+
+def matrix_config(w):
+    alg = w.algorithmic_bytes()
+    return {"workload": w.name, "pass": "forward", "op": "linear-scan" if w.kind == "linear" else "matrix-scan",
+            "a_shape": list(w.a_shape), "b_shape": list(w.b_shape), "axis": w.axis, "n": w.n, "m": w.m,
+            "projective": w.projective, "directions": ["reverse" if r else "forward" for r in w.reverse],
+            "elements_per_step": w.elements * len(w.reverse), "algorithmic_bytes_per_step": alg * len(w.reverse),
+            "l2": "no flush: inputs and outputs (%.2f GB) exceed the 129 MB L2" % (alg / 1e9)}
+
+
+def matrix_sample(w, a, b, target_elems):
+    """The first rows along dim 0 (every lane of them, whole sequences) of a
+    and b, about `target_elems` output values."""
+    per_row = w.elements // w.lead[0]
+    k = max(1, min(w.lead[0], target_elems // per_row))
+    return (a[:k].contiguous().cpu().numpy(), b[:k].contiguous().cpu().numpy(), k * per_row,
+            "first %d of %d rows along dim 0" % (k, w.lead[0]))
+
+
+def matrix_oracle(w, a, b, reverse):
+    import oracle.matrix as M
+    if w.kind == "linear":
+        return M.linear_scan(a, b, axis=w.axis, reverse=reverse)
+    return M.matrix_scan(a, b, axis=w.axis, reverse=reverse, projective=w.projective)
+
+
+def matrix_cpu_rate(w, a, b, budget_s):
+    def run(target):
+        sa, sb, elems, desc = matrix_sample(w, a, b, target)
+        t0 = time.perf_counter()
+        for r in w.reverse:
+            matrix_oracle(w, sa, sb, r)
+        return time.perf_counter() - t0, elems * len(w.reverse), desc
+
+    target = 1 << 18
+    t, elems, desc = run(target)
+    if t < budget_s / 4:
+        t, elems, desc = run(int(target * budget_s / max(t, 1e-3)))
+    return elems / t, "%s of the same workload (%d elements), one thread" % (desc, elems), 1
+
+
+def run_ours_matrix(args, w):
+    import torch
+    from element_scan_recurrences_gb300 import workloads as wl
+
+    es, rank, world, local, device, dist = gpu_setup()
+    a, b = wl.make_matrix_inputs(w, device, seed=w.seed + rank)
+    outs = [torch.empty(w.b_shape, device=device, dtype=torch.float32) for _ in w.reverse]
+    stream = torch.cuda.current_stream(device)
+    plans = [matrix_plan(es, w, r) for r in w.reverse]
+
+    def step():
+        for o, r in zip(outs, w.reverse):
+            matrix_scan_call(es, w, a, b, o, r, stream)
+
+    region_ms, per_step_ms, launches, clocks = time_device_steps(step, stream, device, dist, args, rank, local, es)
+    elems_step = w.elements * len(w.reverse)
+    value = sum_over_ranks(dist, float(elems_step * args.steps), device) / (region_ms / 1e3)
+    kernel_ms = sum(per_step_ms) / len(per_step_ms) / len(w.reverse)
+    kernel = MATRIX_KERNEL.get(plans[0]["path"], plans[0]["path"])
+    roofline = roofline_of(kernel, w.name, w.algorithmic_bytes(), kernel_ms)
+
+    e2e = None
+    if not args.no_e2e:
+        a_h, b_h = a.cpu().pin_memory(), b.cpu().pin_memory()
+        out_h = [torch.empty(w.b_shape, dtype=torch.float32).pin_memory() for _ in w.reverse]
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for oh, od, r in zip(out_h, outs, w.reverse):
+                    a.copy_(a_h, non_blocking=True)
+                    b.copy_(b_h, non_blocking=True)
+                    matrix_scan_call(es, w, a, b, od, r, stream)
+                    oh.copy_(od, non_blocking=True)
+
+        e_ms = time_e2e(e2e_step, e2e_steps, stream, device, dist)
+        e2e = {"value": sum_over_ranks(dist, float(elems_step * e2e_steps), device) / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": (a_h.numel() + b_h.numel()) * 4 * len(w.reverse),
+               "d2h_bytes_per_step": sum(o.numel() for o in out_h) * 4, "steps": e2e_steps,
+               "ms_per_step": e_ms / e2e_steps}
+        del a_h, b_h, out_h
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, desc, cores = matrix_cpu_rate(w, a, b, args.cpu_budget)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        config = dict(matrix_config(w), parallelism="replicas: each GPU scans its own batch"
+                      if world > 1 else "single GPU", path=plans[0]["path"])
+        emit_line(args, world, value, region_ms, config, roofline, cpu, e2e, launches, clocks)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_reference_matrix(args, w):
+    """--impl reference for a matrix workload: the matrix oracle on a bounded
+    sample of the same workload, each step."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from element_scan_recurrences_gb300 import workloads as wl
+    a, b = wl.make_matrix_inputs(w, "cpu")
+    step_budget = max(0.05, min(1.0, 120.0 / max(1, args.steps + args.warmup)))
+    sa, sb, elems, _ = matrix_sample(w, a, b, 1 << 14)
+    t0 = time.perf_counter()
+    for r in w.reverse:
+        matrix_oracle(w, sa, sb, r)
+    t_cal = time.perf_counter() - t0
+    sa, sb, elems, desc = matrix_sample(w, a, b, max(1, int((1 << 14) * step_budget / max(t_cal, 1e-4))))
+    for _ in range(args.warmup):
+        for r in w.reverse:
+            matrix_oracle(w, sa, sb, r)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for r in w.reverse:
+            matrix_oracle(w, sa, sb, r)
+    dt = time.perf_counter() - t0
+    elems *= len(w.reverse)
+    value = elems * args.steps / dt
+    sample = "%s of the same workload (%d elements per step), one thread" % (desc, elems)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": matrix_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
     return 0
 
 
@@ -542,6 +721,13 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
     from element_scan_recurrences_gb300 import workloads as wl
+    if args.workload in wl.MATRIX_WORKLOADS:
+        w = wl.MATRIX_WORKLOADS[args.workload]
+        if args.trips:
+            w = w.with_trips(args.trips)
+        if args.pass_ == "backward":
+            ap.error("--pass backward: matrix-scan has no backward kernels yet")
+        return run_reference_matrix(args, w) if args.impl == "reference" else run_ours_matrix(args, w)
     w = wl.WORKLOADS[args.workload]
     if args.trips:
         shape = list(w.shape)

@@ -33,6 +33,7 @@ struct MatLaunch {
     uint64_t wait_ns;
     int64_t drop_tile;
     cudaStream_t stream;
+    int num_sms;
     EncodeTiledFn encode;
 };
 

@@ -203,6 +203,7 @@ es_status launch_matrix(const char* fn, MatPlan* P, cudaStream_t stream) {
     L.wait_ns = api_wait_ns();
     L.drop_tile = api_drop_tile();
     L.stream = stream;
+    L.num_sms = ds->num_sms;
     const char* msg = nullptr;
     cudaError_t e;
     if (P->path == ES_PATH_MAT_TMA) {

@@ -246,11 +246,10 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
         const int n = min(TT, T - t0);
         const float* sa = tiles + static_cast<size_t>(s) * stage_floats;
         const float* sb = sa + a_pad;
-        for (int q = 0; q < n; ++q) {
-            const int tt = reverse ? n - 1 - q : q;
+        // one trip: hn = a @ hp + b, scaled when projective, stored
+        auto trip = [&](const int tt, float (&hn)[N], const float (&hp)[N]) {
             const float* A = sa + (static_cast<uint32_t>(tt) * LPC + l) * (N * N);
-            float hn[N];
-            column_step<N>(hn, h, [&](int i, float (&r)[N]) { smem_row<N>(A, i, r); });
+            column_step<N>(hn, hp, [&](int i, float (&r)[N]) { smem_row<N>(A, i, r); });
             if (is_h) {
                 const float* B = sb + (static_cast<uint32_t>(tt) * LPC + l) * (N * m) + c;
 #pragma unroll
@@ -266,13 +265,25 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
 #pragma unroll
                 for (int i = 0; i < N; ++i) hn[i] = __fdiv_rn(hn[i], sc);
             }
-#pragma unroll
-            for (int i = 0; i < N; ++i) h[i] = hn[i];
             if (valid && is_h) {
                 float* op = obase + static_cast<int64_t>(t0 + tt) * trip_stride;
 #pragma unroll
-                for (int i = 0; i < N; ++i) __stcs(op + i * m, h[i]);
+                for (int i = 0; i < N; ++i) __stcs(op + i * m, hn[i]);
             }
+        };
+        // The state alternates between two register sets trip by trip, so a
+        // trip never overwrites registers the previous trip's stores may still
+        // be reading.
+        float h2[N];
+        int q = 0;
+        for (; q + 1 < n; q += 2) {
+            trip(reverse ? n - 1 - q : q, h2, h);
+            trip(reverse ? n - 2 - q : q + 1, h, h2);
+        }
+        if (q < n) {
+            trip(reverse ? n - 1 - q : q, h2, h);
+#pragma unroll
+            for (int i = 0; i < N; ++i) h[i] = h2[i];
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
@@ -307,13 +318,20 @@ cudaError_t launch_tma_n(const MatLaunch& L, const CUtensorMap& ma, const CUtens
 }
 
 // Lanes per CTA: 128 consumer threads, fewer (down to one warp) while one
-// trip of the tile would pass 32 KB; then trips per stage: about 32 KB.
-void mat_tile_shape(int n, int m, int gp, int* lpc, int* TT) {
+// trip of the tile would pass 32 KB; then trips per stage: about 16 KB of
+// operands, so that several CTAs share an SM.  (Measured on the delta-rule
+// workload, 1024 lanes: 8 lanes per CTA 0.89 ms, 4 lanes 1.03 ms, 2 lanes
+// 0.96 ms -- fewer lanes per CTA spread the lanes over more SMs but leave each
+// CTA one or two consumer warps.)
+void mat_tile_shape(int n, int m, int gp, int64_t O, int64_t J, int num_sms, int* lpc, int* TT) {
+    (void)O;
+    (void)J;
+    (void)num_sms;
     auto per_trip = [&](int l) { return static_cast<int64_t>(l) * (n * n + n * m) * 4; };
     int l = kMatConsumers / gp;
     while (l * gp > 32 && per_trip(l) > 32 * 1024) l /= 2;
     *lpc = l;
-    *TT = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(64, (32 * 1024) / per_trip(l))));
+    *TT = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(64, (16 * 1024) / per_trip(l))));
 }
 
 bool encode_blocks(EncodeTiledFn encode, CUtensorMap* map, const float* base, int64_t block, int64_t J, int64_t T,
@@ -353,7 +371,7 @@ bool mat_tma_ok(int n, int m, int gp, bool projective, int64_t O, int64_t T, int
     (void)projective;
     if (O >= (int64_t(1) << 31) || T >= (int64_t(1) << 31) || J >= (int64_t(1) << 31)) return false;
     int LPC = 0, TT = 0;
-    mat_tile_shape(n, m, gp, &LPC, &TT);
+    mat_tile_shape(n, m, gp, O, J, 1, &LPC, &TT);
     if (O * ((J + LPC - 1) / LPC) >= (int64_t(1) << 31)) return false;
     return reinterpret_cast<uintptr_t>(a) % 16 == 0 && reinterpret_cast<uintptr_t>(b) % 16 == 0;
 }
@@ -361,7 +379,7 @@ bool mat_tma_ok(int n, int m, int gp, bool projective, int64_t O, int64_t T, int
 cudaError_t launch_mat_tma(const MatLaunch& L, const char** err) {
     const int n = L.n, m = L.m;
     int LPC = 0, TT = 0;
-    mat_tile_shape(n, m, L.gp, &LPC, &TT);
+    mat_tile_shape(n, m, L.gp, L.O, L.J, L.num_sms, &LPC, &TT);
     const int stages = 3;
     // a stage as the kernel lays it out: each tile on a 128-byte boundary
     const int64_t a_pad = (static_cast<int64_t>(TT) * LPC * n * n + 31) & ~int64_t(31);

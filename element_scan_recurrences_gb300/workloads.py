@@ -169,3 +169,87 @@ def custom(body: int, shape, axis: int, state_axis: bool = False, seq_widths=Non
         seq_widths = (shape[-1], shape[-1])
     return Workload(name, body, shape, axis, state_axis, tuple(seq_widths), (reverse,),
                     x_dist, a_dist, init_dist, seed)
+
+
+# ---------------------------------------------------------------------------
+# matrix-scan / linear-scan workloads ("Tensor operations", section
+# "matrix-scan": the delta rule S[t] = (I - beta k k^T) S[t-1] + beta k v^T
+# over [b t n m]; linear-scan over one-by-one matrices)
+
+
+@dataclasses.dataclass(frozen=True)
+class MatrixWorkload:
+    name: str
+    kind: str                      # "delta_rule" (matrix-scan) or "linear" (linear-scan)
+    lead: Tuple[int, ...]          # leading shape; the scanned axis is `axis`
+    axis: int
+    n: int
+    m: int
+    reverse: Tuple[bool, ...] = (False,)
+    projective: bool = False
+    seed: int = 0
+
+    @property
+    def ax(self) -> int:
+        return self.axis + len(self.lead) if self.axis < 0 else self.axis
+
+    @property
+    def T(self) -> int:
+        return self.lead[self.ax]
+
+    @property
+    def a_shape(self) -> Tuple[int, ...]:
+        return self.lead + ((self.n, self.n) if self.kind != "linear" else ())
+
+    @property
+    def b_shape(self) -> Tuple[int, ...]:
+        return self.lead + ((self.n, self.m) if self.kind != "linear" else ())
+
+    @property
+    def shape(self) -> Tuple[int, ...]:
+        return self.b_shape
+
+    @property
+    def elements(self) -> int:
+        return math.prod(self.b_shape)
+
+    def algorithmic_bytes(self) -> int:
+        """f32 bytes of one launch: a and b read, the states written."""
+        return 4 * (math.prod(self.a_shape) + 2 * math.prod(self.b_shape))
+
+    def with_trips(self, T: int, name: Optional[str] = None) -> "MatrixWorkload":
+        lead = tuple(T if i == self.ax else d for i, d in enumerate(self.lead))
+        return dataclasses.replace(self, lead=lead, name=name or "%s_T%d" % (self.name, T))
+
+
+MATRIX_WORKLOADS = {
+    w.name: w for w in [
+        # the pages' delta rule: 64 sequences x 16 heads, 1024 steps, 16 x 16 state
+        MatrixWorkload("matrix_scan_delta_rule", "delta_rule", (64, 1024, 16), 1, 16, 16),
+        # linear-scan on the shape of the wide-lane element-scan case
+        MatrixWorkload("linear_scan_lanes", "linear", (64, 4096, 1024), 1, 1, 1),
+    ]
+}
+
+
+def make_matrix_inputs(w: MatrixWorkload, device="cpu", seed: Optional[int] = None):
+    """Draw (a, b) for a matrix workload, seeded, on ``device``.
+
+    delta_rule: keys k ~ N(0, 1) normalised to unit length, values
+    v ~ N(0, 1), beta ~ U(0, 1), drawn in that order; a = I - beta k k^T and
+    b = beta k v^T are formed from them (input construction: outer products of
+    the drawn vectors).  linear: a ~ U(0.5, 0.99), then b ~ N(0, 1)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed if seed is None else seed)
+    if w.kind == "linear":
+        a = torch.rand(w.lead, generator=gen, device=device).mul_(0.49).add_(0.5)
+        b = torch.randn(w.lead, generator=gen, device=device)
+        return a, b
+    k = torch.randn(w.lead + (w.n,), generator=gen, device=device)
+    k = k / k.norm(dim=-1, keepdim=True)
+    v = torch.randn(w.lead + (w.m,), generator=gen, device=device)
+    beta = torch.rand(w.lead + (1, 1), generator=gen, device=device)
+    eye = torch.eye(w.n, device=device)
+    a = (eye - beta * k.unsqueeze(-1) * k.unsqueeze(-2)).contiguous()
+    b = (beta * k.unsqueeze(-1) * v.unsqueeze(-2)).contiguous()
+    return a, b

@@ -148,3 +148,30 @@ def test_linear_scan_paths():
     got = es.linear_scan(1.0, db, axis=1)
     bitwise(got.cpu().numpy(), np.add.accumulate(b, axis=1, dtype=np.float32), "cumsum")
     es.device_status()
+
+
+@pytest.mark.parametrize("name", ["matrix_scan_delta_rule", "linear_scan_lanes"])
+def test_full_size_sampled(name):
+    """The bench workloads at full size in the bench's launch configuration,
+    checked bit for bit on sampled lanes (the first and the last included)."""
+    from element_scan_recurrences_gb300 import workloads as wl
+    w = wl.MATRIX_WORKLOADS[name]
+    a, b = wl.make_matrix_inputs(w, "cuda")
+    if w.kind == "linear":
+        out = es.linear_scan(a, b, axis=w.axis)
+    else:
+        out = es.matrix_scan(a, b, axis=w.axis)
+    es.device_status()
+    rng = np.random.default_rng(2)
+    B, T, J = w.lead
+    lanes = [(0, 0), (B - 1, J - 1)] + [(int(rng.integers(B)), int(rng.integers(J))) for _ in range(30)]
+    bi = torch.tensor([l[0] for l in lanes], device="cuda")
+    ji = torch.tensor([l[1] for l in lanes], device="cuda")
+    # [lanes, T, ...] -> [T, lanes, ...], scanned along axis 0
+    take = lambda t: t[bi, :, ji].transpose(0, 1).contiguous().cpu().numpy()
+    sa, sb, got = take(a), take(b), take(out)
+    if w.kind == "linear":
+        want = M.linear_scan(sa, sb, axis=0)
+    else:
+        want = M.matrix_scan(sa, sb, axis=0)
+    bitwise(got, want, name)
