@@ -567,6 +567,18 @@ def matrix_plan(es, w, reverse):
     return es.plan_matrix_scan(w.a_shape, w.b_shape, w.axis, reverse, w.projective)
 
 
+TABLE_KERNEL = {"time_tma": "k_table_time", "lane_tma": "k_table_lane", "generic": "k_table_generic"}
+KERNEL_SOURCES.update({k: ["k_table.cu", "es_table_api.cu"] for k in TABLE_KERNEL.values()})
+
+
+def table_config(w):
+    alg = w.algorithmic_bytes()
+    return {"workload": w.name, "pass": "forward", "op": "table-scan", "shape": list(w.shape), "axis": w.axis,
+            "states": w.n_states, "symbols": w.n_syms, "dtype": "i32",
+            "elements_per_step": w.elements, "algorithmic_bytes_per_step": alg,
+            "l2": "no flush: symbols and states (%.2f GB) exceed the 129 MB L2" % (alg / 1e9)}
+
+
 def matrix_config(w):
     alg = w.algorithmic_bytes()
     return {"workload": w.name, "pass": "forward", "op": "linear-scan" if w.kind == "linear" else "matrix-scan",
@@ -592,12 +604,34 @@ def matrix_oracle(w, a, b, reverse):
     return M.matrix_scan(a, b, axis=w.axis, reverse=reverse, projective=w.projective)
 
 
-def matrix_cpu_rate(w, a, b, budget_s):
+def op_sample(w, inputs, target_elems):
+    """A bounded sample of an op workload for the oracle: (inputs, elements,
+    description)."""
+    from element_scan_recurrences_gb300 import workloads as wl
+    if isinstance(w, wl.TableWorkload):
+        table, sym = inputs
+        per_row = w.elements // w.shape[0]
+        k = max(1, min(w.shape[0], target_elems // per_row))
+        return ([table.cpu().numpy(), sym[:k].contiguous().cpu().numpy()], k * per_row,
+                "first %d of %d rows along dim 0" % (k, w.shape[0]))
+    sa, sb, elems, desc = matrix_sample(w, inputs[0], inputs[1], target_elems)
+    return [sa, sb], elems, desc
+
+
+def op_oracle(w, inputs, reverse):
+    from element_scan_recurrences_gb300 import workloads as wl
+    if isinstance(w, wl.TableWorkload):
+        import oracle.table as TS
+        return TS.table_scan(inputs[0], inputs[1], axis=w.axis)
+    return matrix_oracle(w, inputs[0], inputs[1], reverse)
+
+
+def op_cpu_rate(w, inputs, budget_s):
     def run(target):
-        sa, sb, elems, desc = matrix_sample(w, a, b, target)
+        sample, elems, desc = op_sample(w, inputs, target)
         t0 = time.perf_counter()
         for r in w.reverse:
-            matrix_oracle(w, sa, sb, r)
+            op_oracle(w, sample, r)
         return time.perf_counter() - t0, elems * len(w.reverse), desc
 
     target = 1 << 18
@@ -607,54 +641,89 @@ def matrix_cpu_rate(w, a, b, budget_s):
     return elems / t, "%s of the same workload (%d elements), one thread" % (desc, elems), 1
 
 
-def run_ours_matrix(args, w):
+class OpJob:
+    """What the bench needs of a matrix-scan, linear-scan or table-scan
+    workload: its device inputs, one launch per direction, the plan, the
+    oracle on a sample, the configuration."""
+
+    def __init__(self, es, w, device, seed):
+        from element_scan_recurrences_gb300 import workloads as wl
+        self.es, self.w = es, w
+        self.table = isinstance(w, wl.TableWorkload)
+        if self.table:
+            self.inputs = list(wl.make_table_inputs(w, device, seed=seed))
+            self.out_shape, self.out_dtype = w.shape, "int32"
+            self.kernels = TABLE_KERNEL
+        else:
+            self.inputs = list(wl.make_matrix_inputs(w, device, seed=seed))
+            self.out_shape, self.out_dtype = w.b_shape, "float32"
+            self.kernels = MATRIX_KERNEL
+
+    def call(self, inputs, out, reverse, stream):
+        es, w = self.es, self.w
+        if self.table:
+            es.table_scan(inputs[0], inputs[1], axis=w.axis, out=out, stream=stream)
+        else:
+            matrix_scan_call(es, w, inputs[0], inputs[1], out, reverse, stream)
+
+    def plan(self, reverse):
+        es, w = self.es, self.w
+        if self.table:
+            return es.plan_table_scan(w.n_states, w.n_syms, w.shape, w.axis)
+        return matrix_plan(es, w, reverse)
+
+    def config(self):
+        return table_config(self.w) if self.table else matrix_config(self.w)
+
+
+def run_ours_op(args, w):
     import torch
-    from element_scan_recurrences_gb300 import workloads as wl
 
     es, rank, world, local, device, dist = gpu_setup()
-    a, b = wl.make_matrix_inputs(w, device, seed=w.seed + rank)
-    outs = [torch.empty(w.b_shape, device=device, dtype=torch.float32) for _ in w.reverse]
+    job = OpJob(es, w, device, w.seed + rank)
+    dtype = getattr(torch, job.out_dtype)
+    outs = [torch.empty(job.out_shape, device=device, dtype=dtype) for _ in w.reverse]
     stream = torch.cuda.current_stream(device)
-    plans = [matrix_plan(es, w, r) for r in w.reverse]
+    plans = [job.plan(r) for r in w.reverse]
 
     def step():
         for o, r in zip(outs, w.reverse):
-            matrix_scan_call(es, w, a, b, o, r, stream)
+            job.call(job.inputs, o, r, stream)
 
     region_ms, per_step_ms, launches, clocks = time_device_steps(step, stream, device, dist, args, rank, local, es)
     elems_step = w.elements * len(w.reverse)
     value = sum_over_ranks(dist, float(elems_step * args.steps), device) / (region_ms / 1e3)
     kernel_ms = sum(per_step_ms) / len(per_step_ms) / len(w.reverse)
-    kernel = MATRIX_KERNEL.get(plans[0]["path"], plans[0]["path"])
+    kernel = job.kernels.get(plans[0]["path"], plans[0]["path"])
     roofline = roofline_of(kernel, w.name, w.algorithmic_bytes(), kernel_ms)
 
     e2e = None
     if not args.no_e2e:
-        a_h, b_h = a.cpu().pin_memory(), b.cpu().pin_memory()
-        out_h = [torch.empty(w.b_shape, dtype=torch.float32).pin_memory() for _ in w.reverse]
+        hosts = [t.cpu().pin_memory() for t in job.inputs]
+        out_h = [torch.empty(job.out_shape, dtype=dtype).pin_memory() for _ in w.reverse]
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
 
         def e2e_step():
             with torch.cuda.stream(stream):
                 for oh, od, r in zip(out_h, outs, w.reverse):
-                    a.copy_(a_h, non_blocking=True)
-                    b.copy_(b_h, non_blocking=True)
-                    matrix_scan_call(es, w, a, b, od, r, stream)
+                    for d, hh in zip(job.inputs, hosts):
+                        d.copy_(hh, non_blocking=True)
+                    job.call(job.inputs, od, r, stream)
                     oh.copy_(od, non_blocking=True)
 
         e_ms = time_e2e(e2e_step, e2e_steps, stream, device, dist)
         e2e = {"value": sum_over_ranks(dist, float(elems_step * e2e_steps), device) / (e_ms / 1e3), "unit": UNIT,
-               "h2d_bytes_per_step": (a_h.numel() + b_h.numel()) * 4 * len(w.reverse),
+               "h2d_bytes_per_step": sum(t.numel() for t in hosts) * 4 * len(w.reverse),
                "d2h_bytes_per_step": sum(o.numel() for o in out_h) * 4, "steps": e2e_steps,
                "ms_per_step": e_ms / e2e_steps}
-        del a_h, b_h, out_h
+        del hosts, out_h
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, desc, cores = matrix_cpu_rate(w, a, b, args.cpu_budget)
+        rate, desc, cores = op_cpu_rate(w, job.inputs, args.cpu_budget)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
     if rank == 0:
-        config = dict(matrix_config(w), parallelism="replicas: each GPU scans its own batch"
+        config = dict(job.config(), parallelism="replicas: each GPU scans its own batch"
                       if world > 1 else "single GPU", path=plans[0]["path"])
         emit_line(args, world, value, region_ms, config, roofline, cpu, e2e, launches, clocks)
     if dist is not None:
@@ -662,28 +731,33 @@ def run_ours_matrix(args, w):
     return 0
 
 
-def run_reference_matrix(args, w):
-    """--impl reference for a matrix workload: the matrix oracle on a bounded
-    sample of the same workload, each step."""
+def run_reference_op(args, w):
+    """--impl reference for a matrix-scan, linear-scan or table-scan
+    workload: its oracle on a bounded sample of the same workload, each step."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     from element_scan_recurrences_gb300 import workloads as wl
-    a, b = wl.make_matrix_inputs(w, "cpu")
+    if isinstance(w, wl.TableWorkload):
+        inputs = list(wl.make_table_inputs(w, "cpu"))
+        config = table_config(w)
+    else:
+        inputs = list(wl.make_matrix_inputs(w, "cpu"))
+        config = matrix_config(w)
     step_budget = max(0.05, min(1.0, 120.0 / max(1, args.steps + args.warmup)))
-    sa, sb, elems, _ = matrix_sample(w, a, b, 1 << 14)
+    sample, elems, _ = op_sample(w, inputs, 1 << 14)
     t0 = time.perf_counter()
     for r in w.reverse:
-        matrix_oracle(w, sa, sb, r)
+        op_oracle(w, sample, r)
     t_cal = time.perf_counter() - t0
-    sa, sb, elems, desc = matrix_sample(w, a, b, max(1, int((1 << 14) * step_budget / max(t_cal, 1e-4))))
+    sample, elems, desc = op_sample(w, inputs, max(1, int((1 << 14) * step_budget / max(t_cal, 1e-4))))
     for _ in range(args.warmup):
         for r in w.reverse:
-            matrix_oracle(w, sa, sb, r)
+            op_oracle(w, sample, r)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         for r in w.reverse:
-            matrix_oracle(w, sa, sb, r)
+            op_oracle(w, sample, r)
     dt = time.perf_counter() - t0
     elems *= len(w.reverse)
     value = elems * args.steps / dt
@@ -692,7 +766,7 @@ def run_reference_matrix(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": matrix_config(w),
+        "config": config,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -721,13 +795,14 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
     from element_scan_recurrences_gb300 import workloads as wl
-    if args.workload in wl.MATRIX_WORKLOADS:
-        w = wl.MATRIX_WORKLOADS[args.workload]
+    ops = dict(wl.MATRIX_WORKLOADS, **wl.TABLE_WORKLOADS)
+    if args.workload in ops:
+        w = ops[args.workload]
         if args.trips:
             w = w.with_trips(args.trips)
         if args.pass_ == "backward":
-            ap.error("--pass backward: matrix-scan has no backward kernels yet")
-        return run_reference_matrix(args, w) if args.impl == "reference" else run_ours_matrix(args, w)
+            ap.error("--pass backward: only the element-scan workloads have backward kernels")
+        return run_reference_op(args, w) if args.impl == "reference" else run_ours_op(args, w)
     w = wl.WORKLOADS[args.workload]
     if args.trips:
         shape = list(w.shape)

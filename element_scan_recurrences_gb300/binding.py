@@ -31,7 +31,8 @@ EXPORTS = ("es_scan_f32", "es_plan_f32", "es_scan_backward_f32", "es_plan_backwa
            "es_last_error", "es_status_string", "es_launch_count", "es_set_path_override", "es_set_wait_limit_ns",
            "es_set_drop_tile", "es_body_create", "es_body_destroy", "es_body_n_seqs", "es_scan_body_f32",
            "es_plan_body_f32", "es_body_source", "es_body_prepare", "es_body_compile_count", "es_matrix_scan_f32",
-           "es_plan_matrix_scan_f32", "es_linear_scan_f32", "es_plan_linear_scan_f32")
+           "es_plan_matrix_scan_f32", "es_linear_scan_f32", "es_plan_linear_scan_f32", "es_table_scan_i32",
+           "es_plan_table_scan_i32")
 
 
 class LibraryMissing(ImportError):
@@ -119,6 +120,11 @@ def lib():
         L.es_linear_scan_f32.restype = ctypes.c_int
         L.es_plan_linear_scan_f32.argtypes = msig + [P, ctypes.POINTER(PlanInfo)]
         L.es_plan_linear_scan_f32.restype = ctypes.c_int
+        tsig = [P, ctypes.c_int64, ctypes.c_int64, P, i64p, ctypes.c_int, ctypes.c_int, ctypes.c_int32]
+        L.es_table_scan_i32.argtypes = tsig + [P, P]
+        L.es_table_scan_i32.restype = ctypes.c_int
+        L.es_plan_table_scan_i32.argtypes = tsig + [P, ctypes.POINTER(PlanInfo)]
+        L.es_plan_table_scan_i32.restype = ctypes.c_int
         _lib = L
         return L
 
@@ -544,4 +550,44 @@ def linear_scan(a, b, axis: int = 0, reverse: bool = False, out=None, stream=Non
     handle = stream if isinstance(stream, int) else stream.cuda_stream
     _check(lib().es_linear_scan_f32(a.data_ptr(), sa, ra, b.data_ptr(), sb, rb, int(axis), int(bool(reverse)),
                                     out.data_ptr(), handle))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# table-scan
+
+
+def plan_table_scan(n_states: int, n_syms: int, shape, axis: int = -1, start: int = 0,
+                    ptrs: Optional[Sequence[int]] = None) -> dict:
+    """Validate and plan a table-scan without a GPU.  ``ptrs`` = (table,
+    symbols, out), by default 16-byte aligned, non-overlapping stand-ins."""
+    if ptrs is None:
+        ptrs = [(k + 1) << 44 for k in range(3)]
+    shp, rank = _shape_array(shape)
+    info = PlanInfo()
+    _check(lib().es_plan_table_scan_i32(ptrs[0], int(n_states), int(n_syms), ptrs[1], shp, rank, int(axis),
+                                        int(start), ptrs[2], ctypes.byref(info)))
+    return _info(info)
+
+
+def table_scan(table, symbols, axis: int = -1, start: int = 0, out=None, stream=None):
+    """table-scan on CUDA tensors: the automaton `table` ([states, symbols],
+    int32) run over int32 `symbols` along `axis` from state `start`; returns
+    the states (int32, `symbols`' shape)."""
+    import torch
+    for name, t in (("table", table), ("symbols", symbols)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise TypeError("%s must be a contiguous CUDA tensor" % name)
+        if t.dtype != torch.int32:
+            raise EsError(2, "E-DIM-002 table-scan: %s is %s; table and symbols must be i32" % (name, t.dtype))
+    if table.dim() != 2:
+        raise EsError(1, "E-DIM-001 table-scan: the table must be [states symbols], got rank %d" % table.dim())
+    if out is None:
+        out = torch.empty(symbols.shape, device=symbols.device, dtype=torch.int32)
+    shp, rank = _shape_array(symbols.shape)
+    if stream is None:
+        stream = torch.cuda.current_stream(symbols.device)
+    handle = stream if isinstance(stream, int) else stream.cuda_stream
+    _check(lib().es_table_scan_i32(table.data_ptr(), int(table.shape[0]), int(table.shape[1]), symbols.data_ptr(),
+                                   shp, rank, int(axis), int(start), out.data_ptr(), handle))
     return out

@@ -253,3 +253,59 @@ def make_matrix_inputs(w: MatrixWorkload, device="cpu", seed: Optional[int] = No
     a = (eye - beta * k.unsqueeze(-1) * k.unsqueeze(-2)).contiguous()
     b = (beta * k.unsqueeze(-1) * v.unsqueeze(-2)).contiguous()
     return a, b
+
+
+# ---------------------------------------------------------------------------
+# table-scan workloads ("Tensor operations", section "table-scan"): a random
+# automaton over random symbols
+
+
+@dataclasses.dataclass(frozen=True)
+class TableWorkload:
+    name: str
+    shape: Tuple[int, ...]         # symbols' shape
+    axis: int
+    n_states: int
+    n_syms: int
+    seed: int = 0
+    reverse: Tuple[bool, ...] = (False,)   # table-scan runs forward only
+
+    @property
+    def ax(self) -> int:
+        return self.axis + len(self.shape) if self.axis < 0 else self.axis
+
+    @property
+    def T(self) -> int:
+        return self.shape[self.ax]
+
+    @property
+    def elements(self) -> int:
+        return math.prod(self.shape)
+
+    def algorithmic_bytes(self) -> int:
+        """i32 bytes of one launch: symbols read, states written, the table."""
+        return 4 * (2 * self.elements + self.n_states * self.n_syms)
+
+    def with_trips(self, T: int, name: Optional[str] = None) -> "TableWorkload":
+        shape = tuple(T if i == self.ax else d for i, d in enumerate(self.shape))
+        return dataclasses.replace(self, shape=shape, name=name or "%s_T%d" % (self.name, T))
+
+
+TABLE_WORKLOADS = {
+    w.name: w for w in [
+        # sequences as rows, the pages' default axis (the last)
+        TableWorkload("table_scan_time_inner", (262144, 1024), -1, 64, 16),
+        # sequences side by side
+        TableWorkload("table_scan_lanes", (64, 4096, 1024), 1, 64, 16),
+    ]
+}
+
+
+def make_table_inputs(w: TableWorkload, device="cpu", seed: Optional[int] = None):
+    """(table, symbols), seeded: table entries uniform in [0, states), then
+    symbols uniform in [0, symbols); both int32."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed if seed is None else seed)
+    table = torch.randint(0, w.n_states, (w.n_states, w.n_syms), generator=gen, device=device, dtype=torch.int32)
+    sym = torch.randint(0, w.n_syms, w.shape, generator=gen, device=device, dtype=torch.int32)
+    return table, sym

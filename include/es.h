@@ -308,6 +308,37 @@ es_status es_plan_linear_scan_f32(const float *a, const int64_t *a_shape, int a_
                                   const float *b, const int64_t *b_shape, int b_rank,
                                   int axis, int reverse, const float *out, es_plan_info *info);
 
+/*
+ * es_table_scan_i32 -- table-scan ("Tensor operations", the `table-scan` row
+ * of the operations table and the section "table-scan"): a deterministic
+ * automaton run along `axis` of `symbols`,
+ *
+ *     h[t] = table[h[t-1], symbols[t]]     from h[-1] = start
+ *
+ * every state kept, in `symbols`' shape (no gradient).
+ *   table             device i32 [n_states, n_syms], row-major; n_states and
+ *                     n_syms >= 1 (else ES_E_DIM_001).
+ *   symbols, shape, rank, axis  device i32 of `shape` (rank 1..ES_MAX_RANK;
+ *                     the pages' default axis is -1, the last).
+ *   start             a state, 0 <= start < n_states (else ES_E_DIM_001).
+ *   out               device i32 of `shape`; must not overlap an input.
+ * As on the pages' CUDA backend, a symbol outside [0, n_syms) and a table
+ * entry outside [0, n_states) are clamped into range (as `gather` clamps an
+ * index); the clamped entry is the state, so every state is a valid row.
+ * One thread per sequence with the table in shared memory when it takes at
+ * most 64 KB (else read through the read-only path); the symbols are
+ * streamed by the TMA pipelines (ES_PATH_TIME_TMA when the axis is last,
+ * ES_PATH_LANE_TMA for >= 32 sequences side by side), else ES_PATH_GENERIC.
+ * An axis of length 0 launches nothing.  Asynchronous on `stream`.
+ */
+es_status es_table_scan_i32(const int32_t *table, int64_t n_states, int64_t n_syms,
+                            const int32_t *symbols, const int64_t *shape, int rank, int axis,
+                            int32_t start, int32_t *out, es_stream_t stream);
+
+es_status es_plan_table_scan_i32(const int32_t *table, int64_t n_states, int64_t n_syms,
+                                 const int32_t *symbols, const int64_t *shape, int rank, int axis,
+                                 int32_t start, const int32_t *out, es_plan_info *info);
+
 /* Synchronise `stream`, then read and clear this device's status word.
  * Returns ES_E_TIMEOUT if a kernel since the last check gave up a bounded
  * wait (its outputs are then incomplete), ES_E_CUDA if the synchronisation
