@@ -31,18 +31,52 @@
 namespace es {
 namespace {
 
-// one step: the clamped symbol `s` (already in range) and the current state
-template <bool SMEM>
-__device__ __forceinline__ int table_step(int h, int s, const int* __restrict__ tab, int n_syms, int hi) {
-    const int e = SMEM ? tab[h * n_syms + s] : __ldg(tab + h * n_syms + s);
-    return min(max(e, 0), hi);
-}
-
 __device__ __forceinline__ int clamp_symbol(int s, int n_syms) { return min(max(s, 0), n_syms - 1); }
 
-// copy the table into shared memory (every thread of the CTA takes part)
-__device__ __forceinline__ void stage_table(int* dst, const int* __restrict__ src, int entries) {
-    for (int q = threadIdx.x; q < entries; q += blockDim.x) dst[q] = __ldg(src + q);
+// The automaton's state is carried as its row offset, state * n_syms.  A
+// table in shared memory is staged once per CTA as two arrays over the
+// entries q = row * n_syms + symbol: the next state, clamped (`state_of`),
+// and that state's row offset (`next_off`).  A step is then
+//     off' = next_off[off + s]      (one add and one load on the chain)
+// with the state read beside it, off the chain: state_of[off + s].
+struct TableSmem {
+    const int* next_off;
+    const int* state_of;
+};
+
+// copy and prepare the table (every thread of the CTA takes part)
+__device__ __forceinline__ TableSmem stage_table(int* dst, const int* __restrict__ src, int n_states, int n_syms) {
+    const int entries = n_states * n_syms;
+    int* next_off = dst;
+    int* state_of = dst + entries;
+    for (int q = threadIdx.x; q < entries; q += blockDim.x) {
+        const int e = min(max(__ldg(src + q), 0), n_states - 1);
+        state_of[q] = e;
+        next_off[q] = e * n_syms;
+    }
+    return TableSmem{next_off, state_of};
+}
+
+// One step of a row-offset-carrying run: returns the state after symbol `s`
+// (already clamped) and advances `off`.  A table left in global memory is
+// read through the read-only path and clamped on the way.
+template <bool SMEM>
+__device__ __forceinline__ int table_step(int& off, int s, const TableSmem& ts, const int* __restrict__ table,
+                                          int n_syms, int hi) {
+    const int q = off + s;
+    if constexpr (SMEM) {
+        off = ts.next_off[q];
+        return ts.state_of[q];
+    } else {
+        const int e = min(max(__ldg(table + q), 0), hi);
+        off = e * n_syms;
+        return e;
+    }
+}
+
+// shared memory a staged table takes
+__host__ __device__ constexpr size_t staged_table_bytes(int64_t n_states, int64_t n_syms) {
+    return static_cast<size_t>(n_states) * static_cast<size_t>(n_syms) * 8;
 }
 
 // ---------------------------------------------------------------------------
@@ -53,22 +87,21 @@ __global__ void __launch_bounds__(128)
 k_table_generic(const int* __restrict__ table, const int* __restrict__ sym, int* __restrict__ out, int64_t O,
                 int64_t T, int64_t J, int n_states, int n_syms, int start) {
     extern __shared__ int tab_s[];
-    const int* tab = table;
+    TableSmem ts{};
     if constexpr (SMEM) {
-        stage_table(tab_s, table, n_states * n_syms);
+        ts = stage_table(tab_s, table, n_states, n_syms);
         __syncthreads();
-        tab = tab_s;
     }
     const int64_t lane = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (lane >= O * J) return;
     const int64_t o = lane / J;
     const int64_t j = lane - o * J;
-    int h = start;
+    int off = start * n_syms;
     const int hi = n_states - 1;
     const int* sp = sym + o * T * J + j;
     int* op = out + o * T * J + j;
     for (int64_t t = 0; t < T; ++t) {
-        h = table_step<SMEM>(h, clamp_symbol(__ldg(sp + t * J), n_syms), tab, n_syms, hi);
+        const int h = table_step<SMEM>(off, clamp_symbol(__ldg(sp + t * J), n_syms), ts, table, n_syms, hi);
         __stcs(op + t * J, h);
     }
 }
@@ -90,12 +123,8 @@ k_table_lane(const __grid_constant__ CUtensorMap map_s, const int* __restrict__ 
     __shared__ int abort_flag;
     constexpr int kTileInts = kTabTT * LI;
     int* tiles = reinterpret_cast<int*>(smem_raw + smem_align_pad(smem_raw));
-    int* tab_s = tiles + stages * kTileInts;
-    const int* tab = table;
-    if constexpr (SMEM) {
-        stage_table(tab_s, table, n_states * n_syms);
-        tab = tab_s;
-    }
+    TableSmem ts{};
+    if constexpr (SMEM) ts = stage_table(tiles + stages * kTileInts, table, n_states, n_syms);
 
     const int o = blockIdx.x / tiles_i;
     const int i0 = (blockIdx.x % tiles_i) * LI;
@@ -142,7 +171,7 @@ k_table_lane(const __grid_constant__ CUtensorMap map_s, const int* __restrict__ 
     const int i = i0 + c;
     const bool valid = i < I;
     const int hi = n_states - 1;
-    int h = start;
+    int off = start * n_syms;
     int* obase = out + static_cast<int64_t>(o) * T * I + i;
     for (int k = 0; k < ntiles; ++k) {
         const int s = k % stages;
@@ -161,11 +190,12 @@ k_table_lane(const __grid_constant__ CUtensorMap map_s, const int* __restrict__ 
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
         int* op = obase + static_cast<int64_t>(t0) * I;
-        // two state registers by trip parity: a lookup never overwrites the
-        // register the previous trip's store may still be reading
-        int hv[2] = {h, h};
+        // the state stored goes to one of two registers by trip parity: a
+        // lookup never overwrites the register the previous trip's store may
+        // still be reading
+        int hv[2];
         auto trip = [&](const int tt) {
-            hv[tt & 1] = table_step<SMEM>(hv[(tt & 1) ^ 1], sr[tt], tab, n_syms, hi);
+            hv[tt & 1] = table_step<SMEM>(off, sr[tt], ts, table, n_syms, hi);
             if (valid) __stcs(op + static_cast<int64_t>(tt) * I, hv[tt & 1]);
         };
         if (n == kTabTT) {
@@ -176,7 +206,6 @@ k_table_lane(const __grid_constant__ CUtensorMap map_s, const int* __restrict__ 
             for (int tt = 0; tt < kTabTT; ++tt)
                 if (tt < n) trip(tt);
         }
-        h = hv[(n - 1) & 1];
     }
 }
 
@@ -199,12 +228,9 @@ k_table_time(const __grid_constant__ CUtensorMap map_s, const __grid_constant__ 
     unsigned char* base = smem_raw + smem_align_pad(smem_raw);
     unsigned char* in_tiles = base;
     unsigned char* out_tiles = base + static_cast<size_t>(stages) * kTileBytes;
-    int* tab_s = reinterpret_cast<int*>(out_tiles + kTabOutBufs * kTileBytes);
-    const int* tab = table;
-    if constexpr (SMEM) {
-        stage_table(tab_s, table, n_states * n_syms);
-        tab = tab_s;
-    }
+    TableSmem ts{};
+    if constexpr (SMEM)
+        ts = stage_table(reinterpret_cast<int*>(out_tiles + kTabOutBufs * kTileBytes), table, n_states, n_syms);
 
     const int o0 = blockIdx.x * kTabLO;
     const int ntiles = (T + 31) / 32;
@@ -248,7 +274,7 @@ k_table_time(const __grid_constant__ CUtensorMap map_s, const __grid_constant__ 
 
     const int r = threadIdx.x - 32;
     const int hi = n_states - 1;
-    int h = start;
+    int off = start * n_syms;
     const uint32_t row_off = static_cast<uint32_t>(r) * 128u;
     const uint32_t swz = static_cast<uint32_t>(r & 7);   // 128-byte swizzle: chunk q lives at q ^ (row % 8)
     const bool storer = (threadIdx.x == 32);
@@ -280,14 +306,10 @@ k_table_time(const __grid_constant__ CUtensorMap map_s, const __grid_constant__ 
         for (int q = 0; q < 8; ++q) {
             if (q < nq) {
                 int4 v;
-                h = table_step<SMEM>(h, clamp_symbol(seg[q].x, n_syms), tab, n_syms, hi);
-                v.x = h;
-                h = table_step<SMEM>(h, clamp_symbol(seg[q].y, n_syms), tab, n_syms, hi);
-                v.y = h;
-                h = table_step<SMEM>(h, clamp_symbol(seg[q].z, n_syms), tab, n_syms, hi);
-                v.z = h;
-                h = table_step<SMEM>(h, clamp_symbol(seg[q].w, n_syms), tab, n_syms, hi);
-                v.w = h;
+                v.x = table_step<SMEM>(off, clamp_symbol(seg[q].x, n_syms), ts, table, n_syms, hi);
+                v.y = table_step<SMEM>(off, clamp_symbol(seg[q].y, n_syms), ts, table, n_syms, hi);
+                v.z = table_step<SMEM>(off, clamp_symbol(seg[q].z, n_syms), ts, table, n_syms, hi);
+                v.w = table_step<SMEM>(off, clamp_symbol(seg[q].w, n_syms), ts, table, n_syms, hi);
                 *reinterpret_cast<int4*>(orow + ((static_cast<uint32_t>(q) ^ swz) << 4)) = v;
             }
         }
@@ -336,8 +358,8 @@ cudaError_t launch_time_t(const TableLaunch& L, const CUtensorMap& ms, const CUt
 
 }  // namespace
 
-// a table of at most 64 KB is staged in shared memory
-bool table_in_smem(int64_t n_states, int64_t n_syms) { return n_states * n_syms * 4 <= 64 * 1024; }
+// a table of at most 32 KB (64 KB staged) goes to shared memory
+bool table_in_smem(int64_t n_states, int64_t n_syms) { return staged_table_bytes(n_states, n_syms) <= 64 * 1024; }
 
 bool table_lane_ok(int64_t O, int64_t T, int64_t J, const void* sym, const void* out) {
     if (J < 32 || J % 4 != 0) return false;
@@ -353,23 +375,21 @@ bool table_time_ok(int64_t O, int64_t T, int64_t J, const void* sym, const void*
 }
 
 cudaError_t launch_table_generic(const TableLaunch& L) {
-    const size_t tb = static_cast<size_t>(L.n_states) * L.n_syms * 4;
+    const size_t tb = staged_table_bytes(L.n_states, L.n_syms);
     return table_in_smem(L.n_states, L.n_syms) ? launch_generic_t<true>(L, tb) : launch_generic_t<false>(L, tb);
 }
 
 cudaError_t launch_table_lane(const TableLaunch& L, const char** err) {
     const bool smem_tab = table_in_smem(L.n_states, L.n_syms);
-    const size_t tb = smem_tab ? static_cast<size_t>(L.n_states) * L.n_syms * 4 : 0;
+    const size_t tb = smem_tab ? staged_table_bytes(L.n_states, L.n_syms) : 0;
+    // 64 sequences per CTA and two stages: a lookup chain per thread leaves
+    // latency that more CTAs per SM cover (on GB300 the lanes workload took
+    // 0.49 / 0.47 / 0.41 ms at 4 / 3 / 2 stages with 128 sequences per CTA,
+    // 0.38 ms with 64)
     const int64_t I = L.J;
-    int LI = 32;
-    for (int cand : {128, 64}) {
-        if (I >= cand && 5 * L.O * ((I + cand - 1) / cand) >= 4LL * L.num_sms) {
-            LI = cand;
-            break;
-        }
-    }
+    const int LI = I >= 64 && 5 * L.O * ((I + 63) / 64) >= 4LL * L.num_sms ? 64 : 32;
     const int64_t tiles_i = (I + LI - 1) / LI;
-    const int stages = 4;
+    const int stages = 2;
     const size_t smem = static_cast<size_t>(stages) * kTabTT * LI * 4 + tb + 1024;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(I), static_cast<cuuint64_t>(L.T), static_cast<cuuint64_t>(L.O)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(I) * 4, static_cast<cuuint64_t>(I) * L.T * 4};
@@ -383,20 +403,15 @@ cudaError_t launch_table_lane(const TableLaunch& L, const char** err) {
         return cudaErrorInvalidValue;
     }
     const int ti = static_cast<int>(tiles_i);
-    if (smem_tab) {
-        if (LI == 128) return launch_lane_t<128, true>(L, ms, ti, stages, smem);
-        if (LI == 64) return launch_lane_t<64, true>(L, ms, ti, stages, smem);
-        return launch_lane_t<32, true>(L, ms, ti, stages, smem);
-    }
-    if (LI == 128) return launch_lane_t<128, false>(L, ms, ti, stages, smem);
-    if (LI == 64) return launch_lane_t<64, false>(L, ms, ti, stages, smem);
-    return launch_lane_t<32, false>(L, ms, ti, stages, smem);
+    if (smem_tab) return LI == 64 ? launch_lane_t<64, true>(L, ms, ti, stages, smem)
+                                  : launch_lane_t<32, true>(L, ms, ti, stages, smem);
+    return LI == 64 ? launch_lane_t<64, false>(L, ms, ti, stages, smem) : launch_lane_t<32, false>(L, ms, ti, stages, smem);
 }
 
 cudaError_t launch_table_time(const TableLaunch& L, const char** err) {
     const bool smem_tab = table_in_smem(L.n_states, L.n_syms);
-    const size_t tb = smem_tab ? static_cast<size_t>(L.n_states) * L.n_syms * 4 : 0;
-    const int stages = 4;
+    const size_t tb = smem_tab ? staged_table_bytes(L.n_states, L.n_syms) : 0;
+    const int stages = 2;   // more CTAs per SM beat a deeper ring (0.43 ms at 4 stages, 0.38 at 2)
     const size_t smem = (static_cast<size_t>(stages) + kTabOutBufs) * kTabLO * 128 + tb + 1024;
     CUtensorMap maps[2];
     const int* bases[2] = {L.sym, L.out};

@@ -325,8 +325,8 @@ es_status es_plan_linear_scan_f32(const float *a, const int64_t *a_shape, int a_
  * As on the pages' CUDA backend, a symbol outside [0, n_syms) and a table
  * entry outside [0, n_states) are clamped into range (as `gather` clamps an
  * index); the clamped entry is the state, so every state is a valid row.
- * One thread per sequence with the table in shared memory when it takes at
- * most 64 KB (else read through the read-only path); the symbols are
+ * One thread per sequence with the table in shared memory when it has at
+ * most 8192 entries (else read through the read-only path); the symbols are
  * streamed by the TMA pipelines (ES_PATH_TIME_TMA when the axis is last,
  * ES_PATH_LANE_TMA for >= 32 sequences side by side), else ES_PATH_GENERIC.
  * An axis of length 0 launches nothing.  Asynchronous on `stream`.
