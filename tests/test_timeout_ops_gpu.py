@@ -1,0 +1,86 @@
+"""Bounded waits in the body-program, matrix-scan and table-scan pipelines:
+a tile that never arrives (the producer is told on the host to skip one
+load) makes the kernel give up after the wait limit, record ES_E_TIMEOUT and
+return; the next call is correct.  Nothing faults or hangs the GPU."""
+import numpy as np
+import pytest
+import torch
+
+import body_cases
+import oracle.matrix as M
+import oracle.table as TS
+from element_scan_recurrences_gb300 import binding as es
+from oracle.body import scan_body
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def restore():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+    es.set_drop_tile(-1)
+    es.set_wait_limit_ns(2_000_000_000)
+    es.set_path_override("auto")
+
+
+def drop_then_recover(run, check):
+    es.device_status()                    # a clean status word
+    es.set_wait_limit_ns(20_000_000)      # 20 ms
+    es.set_drop_tile(3)
+    run()
+    with pytest.raises(es.EsError) as ei:
+        es.device_status()
+    assert ei.value.status == 6           # ES_E_TIMEOUT
+    es.device_status()                    # the word was cleared
+    es.set_drop_tile(-1)
+    es.set_wait_limit_ns(2_000_000_000)
+    out = run()
+    es.device_status()
+    check(out)
+
+
+@pytest.mark.parametrize("cid,shape,axis,path", [
+    ("tanh_decay", (2, 400, 64), 1, "lane_tma"),
+    ("gated_tanh", (2, 64, 400), 2, "time_tma"),
+    ("normcap_w16", (2, 400, 16), 1, "vec_tma"),
+])
+def test_body_program_pipelines(cid, shape, axis, path):
+    c = body_cases.case(cid)
+    O, T, J = (shape[0], shape[1], shape[2]) if axis == 1 else (shape[0], shape[2], shape[1])
+    initial, seqs, state_axis = body_cases.make_inputs(c, O, T, J, axis=axis)
+    body = es.Body(c[1])
+    d_init = torch.from_numpy(initial).cuda()
+    d_seqs = [torch.from_numpy(s).cuda() for s in seqs]
+    es.set_path_override(path)
+    want = scan_body(c[1], initial, seqs, axis=axis, state_axis=state_axis)
+
+    def check(out):
+        err = np.abs(out.cpu().numpy().astype(np.float64) - want) / (1 + np.abs(want.astype(np.float64)))
+        assert err.max() <= 1e-5
+
+    drop_then_recover(lambda: body.scan(d_init, d_seqs, axis=axis, state_axis=state_axis), check)
+
+
+def test_matrix_scan_pipeline():
+    rng = np.random.default_rng(1)
+    a = (rng.standard_normal((2, 400, 8, 4, 4)) * 0.4).astype(np.float32)
+    b = rng.standard_normal((2, 400, 8, 4, 4)).astype(np.float32)
+    assert es.plan_matrix_scan(a.shape, b.shape, 1)["path"] == "mat_tma"
+    da, db = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    want = M.matrix_scan(a, b, axis=1)
+    drop_then_recover(lambda: es.matrix_scan(da, db, axis=1),
+                      lambda out: np.testing.assert_array_equal(out.cpu().numpy(), want))
+
+
+@pytest.mark.parametrize("shape,axis,path", [((130, 400), -1, "time_tma"), ((2, 400, 64), 1, "lane_tma")])
+def test_table_scan_pipelines(shape, axis, path):
+    rng = np.random.default_rng(2)
+    table = rng.integers(0, 16, (16, 4)).astype(np.int32)
+    sym = rng.integers(0, 4, shape).astype(np.int32)
+    assert es.plan_table_scan(16, 4, shape, axis)["path"] == path
+    dt, ds = torch.from_numpy(table).cuda(), torch.from_numpy(sym).cuda()
+    want = TS.table_scan(table, sym, axis=axis)
+    drop_then_recover(lambda: es.table_scan(dt, ds, axis=axis),
+                      lambda out: np.testing.assert_array_equal(out.cpu().numpy(), want))
