@@ -74,6 +74,16 @@ __device__ __forceinline__ void smem_row(const float* A, int i, float (&r)[N]) {
     }
 }
 
+// two IEEE products in one packed instruction (sm_100 and later):
+// (p0, p1) = (a0 * b0, a1 * b1), each rounded to nearest on its own, so the
+// result is that of two __fmul_rn
+__device__ __forceinline__ void mul2_rn(float& p0, float& p1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+        "mul.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(p0), "=f"(p1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // the largest |value| over the lane group of `gp` threads (a power of two)
 __device__ __forceinline__ float group_max_abs(float v, int gp, unsigned mask) {
     for (int off = gp / 2; off >= 1; off >>= 1) v = ieee_maximum(v, __shfl_xor_sync(mask, v, off));
@@ -150,21 +160,34 @@ k_mat_generic(const float* __restrict__ a, const float* __restrict__ b, float* _
 
 // ---------------------------------------------------------------------------
 // dense operands, TMA pipeline
+//
+// A lane's C carried columns (of h, then of P) are gp threads (gp a power of
+// two >= C), and each column's N rows are split over R row groups, so a lane
+// is TPL = gp * R threads (R = min(32 / gp, N): one warp per lane for the
+// wide columns, twice the warps of one thread per column).  Thread (g, c)
+// forms rows i = r * R + g of column c (rows interleaved by group, so the
+// groups' broadcast reads of a's rows fall in different banks), then N
+// shuffles give every thread of the column the whole new column.  Products
+// are formed two at a time with the packed f32x2 multiply (each still one
+// rounded product) and summed in order.  On GB300 the delta-rule workload
+// went from 0.89 ms (one thread per column) to 0.67 ms (two row groups) and
+// 0.65 ms (packed products).
 
 constexpr int kMatMaxStages = 4;
 constexpr int kMatConsumers = 128;
 
-template <int N, bool PROJ>
+template <int N, int R, bool PROJ>
 __global__ void __launch_bounds__(32 + kMatConsumers)
 k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-          float* __restrict__ out, int T, int J, int m, int gp, int LPC, int tiles_j, int TT, int stages, int reverse,
-          unsigned int* status, uint64_t wait_ns, int64_t drop_tile) {
+          float* __restrict__ out, int T, int J, int m, int gp, int LPC, int tiles_j, int TT, int stages,
+          int reverse, unsigned int* status, uint64_t wait_ns, int64_t drop_tile) {
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMatMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kMatMaxStages];
     __shared__ int abort_flag;
 
-    const int consumers = LPC * gp;                         // a multiple of 32, at most kMatConsumers
+    const int TPL = gp * R;                                 // threads per lane
+    const int consumers = LPC * TPL;                        // a multiple of 32, at most kMatConsumers
     const uint32_t a_floats = static_cast<uint32_t>(TT) * LPC * N * N;
     const uint32_t b_floats = static_cast<uint32_t>(TT) * LPC * N * m;
     // every tile starts on a 128-byte boundary
@@ -219,17 +242,22 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
         return;
     }
 
-    // consumers: thread (l, c) is column c of lane j0 + l (columns of h, then of P)
+    // consumers: thread (l, g, c) is row group g of column c of lane j0 + l
     const int ct = threadIdx.x - 32;
-    (void)consumers;
-    const int l = ct / gp;
-    const int c = ct % gp;
+    const int l = ct / TPL;
+    const int w = ct % TPL;
+    const int g = w / gp;
+    const int c = w % gp;
     const bool valid = j0 + l < J;
     const bool is_h = c < m;
     const bool is_p = PROJ && !is_h && c < m + N;
-    const int64_t lane_block = static_cast<int64_t>(N) * m;           // floats of h per lane and trip
+    constexpr int RPT = N / R;                              // rows per thread
+    // warp lane of this column's row group 0
+    const int col_base = (lane & ~(TPL - 1)) + c;
+    const int64_t lane_block = static_cast<int64_t>(N) * m;          // floats of h per lane and trip
     float* obase = out + (static_cast<int64_t>(o) * T * J + j0 + l) * lane_block + c;
     const int64_t trip_stride = static_cast<int64_t>(J) * lane_block;
+    // the column's whole state (every row), the same in all its row groups
     float h[N];
 #pragma unroll
     for (int i = 0; i < N; ++i) h[i] = (is_p && i == c - m) ? 1.0f : 0.0f;
@@ -246,45 +274,52 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
         const int n = min(TT, T - t0);
         const float* sa = tiles + static_cast<size_t>(s) * stage_floats;
         const float* sb = sa + a_pad;
-        // one trip: hn = a @ hp + b, scaled when projective, stored
-        auto trip = [&](const int tt, float (&hn)[N], const float (&hp)[N]) {
+        // one trip: this thread's rows of a @ h + b (scaled when projective),
+        // stored, then the whole new column gathered into h
+        auto trip = [&](const int tt, float (&mine)[RPT]) {
             const float* A = sa + (static_cast<uint32_t>(tt) * LPC + l) * (N * N);
-            column_step<N>(hn, hp, [&](int i, float (&r)[N]) { smem_row<N>(A, i, r); });
-            if (is_h) {
-                const float* B = sb + (static_cast<uint32_t>(tt) * LPC + l) * (N * m) + c;
+            const float* B = sb + (static_cast<uint32_t>(tt) * LPC + l) * (N * m) + c;
 #pragma unroll
-                for (int i = 0; i < N; ++i) hn[i] = __fadd_rn(hn[i], B[i * m]);
+            for (int r = 0; r < RPT; ++r) {
+                const int i = r * R + g;
+                float row[N];
+                smem_row<N>(A, i, row);
+                float prod[N];
+#pragma unroll
+                for (int j = 0; j < N; j += 2) mul2_rn(prod[j], prod[j + 1], row[j], row[j + 1], h[j], h[j + 1]);
+                float acc = prod[0];
+#pragma unroll
+                for (int j = 1; j < N; ++j) acc = __fadd_rn(acc, prod[j]);
+                mine[r] = is_h ? __fadd_rn(acc, B[i * m]) : acc;
             }
             if constexpr (PROJ) {
                 float mx = 0.0f;
                 if (is_p) {
 #pragma unroll
-                    for (int i = 0; i < N; ++i) mx = ieee_maximum(mx, fabsf(hn[i]));
+                    for (int r = 0; r < RPT; ++r) mx = ieee_maximum(mx, fabsf(mine[r]));
                 }
-                const float sc = group_max_abs(mx, gp, 0xffffffffu);
+                const float sc = group_max_abs(mx, TPL, 0xffffffffu);
 #pragma unroll
-                for (int i = 0; i < N; ++i) hn[i] = __fdiv_rn(hn[i], sc);
+                for (int r = 0; r < RPT; ++r) mine[r] = __fdiv_rn(mine[r], sc);
             }
             if (valid && is_h) {
                 float* op = obase + static_cast<int64_t>(t0 + tt) * trip_stride;
 #pragma unroll
-                for (int i = 0; i < N; ++i) __stcs(op + i * m, hn[i]);
+                for (int r = 0; r < RPT; ++r) __stcs(op + (r * R + g) * m, mine[r]);
             }
+            // row i lives in row group i % R at position i / R
+#pragma unroll
+            for (int i = 0; i < N; ++i) h[i] = __shfl_sync(0xffffffffu, mine[i / R], col_base + (i % R) * gp);
         };
-        // The state alternates between two register sets trip by trip, so a
-        // trip never overwrites registers the previous trip's stores may still
-        // be reading.
-        float h2[N];
+        // two register sets by trip parity: a trip never overwrites the
+        // registers the previous trip's stores may still be reading
+        float ma[RPT], mb[RPT];
         int q = 0;
         for (; q + 1 < n; q += 2) {
-            trip(reverse ? n - 1 - q : q, h2, h);
-            trip(reverse ? n - 2 - q : q + 1, h, h2);
+            trip(reverse ? n - 1 - q : q, ma);
+            trip(reverse ? n - 2 - q : q + 1, mb);
         }
-        if (q < n) {
-            trip(reverse ? n - 1 - q : q, h2, h);
-#pragma unroll
-            for (int i = 0; i < N; ++i) h[i] = h2[i];
-        }
+        if (q < n) trip(reverse ? n - 1 - q : q, ma);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
@@ -305,33 +340,46 @@ cudaError_t launch_generic_n(const MatLaunch& L) {
     return cudaGetLastError();
 }
 
-template <int N>
-cudaError_t launch_tma_n(const MatLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb, int lpc, int tiles_j,
-                         int TT, int stages, size_t smem) {
-    auto kern = L.projective ? k_mat_tma<N, true> : k_mat_tma<N, false>;
+template <int N, int R>
+cudaError_t launch_tma_nr(const MatLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb, int lpc, int tiles_j,
+                          int TT, int stages, size_t smem) {
+    auto kern = L.projective ? k_mat_tma<N, R, true> : k_mat_tma<N, R, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(L.O * tiles_j), 32 + lpc * L.gp, smem, L.stream>>>(
-        ma, mb, L.out, static_cast<int>(L.T), static_cast<int>(L.J), L.m, L.gp, lpc, tiles_j, TT, stages, L.reverse,
-        L.status, L.wait_ns, L.drop_tile);
+    kern<<<static_cast<unsigned>(L.O * tiles_j), 32 + lpc * L.gp * R, smem, L.stream>>>(
+        ma, mb, L.out, static_cast<int>(L.T), static_cast<int>(L.J), L.m, L.gp, lpc, tiles_j, TT, stages,
+        L.reverse, L.status, L.wait_ns, L.drop_tile);
     return cudaGetLastError();
 }
 
-// Lanes per CTA: 128 consumer threads, fewer (down to one warp) while one
-// trip of the tile would pass 32 KB; then trips per stage: about 16 KB of
-// operands, so that several CTAs share an SM.  (Measured on the delta-rule
-// workload, 1024 lanes: 8 lanes per CTA 0.89 ms, 4 lanes 1.03 ms, 2 lanes
-// 0.96 ms -- fewer lanes per CTA spread the lanes over more SMs but leave each
-// CTA one or two consumer warps.)
-void mat_tile_shape(int n, int m, int gp, int64_t O, int64_t J, int num_sms, int* lpc, int* TT) {
-    (void)O;
-    (void)J;
-    (void)num_sms;
+template <int N>
+cudaError_t launch_tma_n(const MatLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb, int R, int lpc,
+                         int tiles_j, int TT, int stages, size_t smem) {
+    if constexpr (N >= 16) {
+        if (R == 16) return launch_tma_nr<N, 16>(L, ma, mb, lpc, tiles_j, TT, stages, smem);
+    }
+    if constexpr (N >= 8) {
+        if (R == 8) return launch_tma_nr<N, 8>(L, ma, mb, lpc, tiles_j, TT, stages, smem);
+    }
+    if constexpr (N >= 4) {
+        if (R == 4) return launch_tma_nr<N, 4>(L, ma, mb, lpc, tiles_j, TT, stages, smem);
+    }
+    if (R == 2) return launch_tma_nr<N, 2>(L, ma, mb, lpc, tiles_j, TT, stages, smem);
+    return launch_tma_nr<N, 1>(L, ma, mb, lpc, tiles_j, TT, stages, smem);
+}
+
+// Row groups per column: enough to fill a warp with one lane's threads (at
+// most one row per thread).  Lanes per CTA: 128 consumer threads, fewer (down
+// to one warp) while one trip of the tile would pass 32 KB; trips per stage:
+// about 32 KB of operands.
+void mat_tile_shape(int n, int m, int gp, int* R, int* lpc, int* TT) {
+    *R = std::min(32 / gp, n);
+    const int tpl = gp * *R;
     auto per_trip = [&](int l) { return static_cast<int64_t>(l) * (n * n + n * m) * 4; };
-    int l = kMatConsumers / gp;
-    while (l * gp > 32 && per_trip(l) > 32 * 1024) l /= 2;
+    int l = std::max(1, kMatConsumers / tpl);
+    while (l * tpl > 32 && per_trip(l) > 32 * 1024) l /= 2;
     *lpc = l;
-    *TT = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(64, (16 * 1024) / per_trip(l))));
+    *TT = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(64, (32 * 1024) / per_trip(l))));
 }
 
 bool encode_blocks(EncodeTiledFn encode, CUtensorMap* map, const float* base, int64_t block, int64_t J, int64_t T,
@@ -370,16 +418,16 @@ bool mat_tma_ok(int n, int m, int gp, bool projective, int64_t O, int64_t T, int
     if (gp > 32 || (!projective && m > 32)) return false;
     (void)projective;
     if (O >= (int64_t(1) << 31) || T >= (int64_t(1) << 31) || J >= (int64_t(1) << 31)) return false;
-    int LPC = 0, TT = 0;
-    mat_tile_shape(n, m, gp, O, J, 1, &LPC, &TT);
+    int R = 0, LPC = 0, TT = 0;
+    mat_tile_shape(n, m, gp, &R, &LPC, &TT);
     if (O * ((J + LPC - 1) / LPC) >= (int64_t(1) << 31)) return false;
     return reinterpret_cast<uintptr_t>(a) % 16 == 0 && reinterpret_cast<uintptr_t>(b) % 16 == 0;
 }
 
 cudaError_t launch_mat_tma(const MatLaunch& L, const char** err) {
     const int n = L.n, m = L.m;
-    int LPC = 0, TT = 0;
-    mat_tile_shape(n, m, L.gp, L.O, L.J, L.num_sms, &LPC, &TT);
+    int R = 0, LPC = 0, TT = 0;
+    mat_tile_shape(n, m, L.gp, &R, &LPC, &TT);
     const int stages = 3;
     // a stage as the kernel lays it out: each tile on a 128-byte boundary
     const int64_t a_pad = (static_cast<int64_t>(TT) * LPC * n * n + 31) & ~int64_t(31);
@@ -394,10 +442,10 @@ cudaError_t launch_mat_tma(const MatLaunch& L, const char** err) {
     const size_t smem = static_cast<size_t>(stages) * stage_floats * 4 + 1024;
     const int tj = static_cast<int>(tiles_j);
     switch (n) {
-        case 2: return launch_tma_n<2>(L, ma, mb, LPC, tj, TT, stages, smem);
-        case 4: return launch_tma_n<4>(L, ma, mb, LPC, tj, TT, stages, smem);
-        case 8: return launch_tma_n<8>(L, ma, mb, LPC, tj, TT, stages, smem);
-        default: return launch_tma_n<16>(L, ma, mb, LPC, tj, TT, stages, smem);
+        case 2: return launch_tma_n<2>(L, ma, mb, R, LPC, tj, TT, stages, smem);
+        case 4: return launch_tma_n<4>(L, ma, mb, R, LPC, tj, TT, stages, smem);
+        case 8: return launch_tma_n<8>(L, ma, mb, R, LPC, tj, TT, stages, smem);
+        default: return launch_tma_n<16>(L, ma, mb, R, LPC, tj, TT, stages, smem);
     }
 }
 
