@@ -23,7 +23,8 @@ _BODIES = {"TANH_DECAY": TANH_DECAY, "NORMCAP": NORMCAP, "MAXPLUS": MAXPLUS}
 STATUS = {0: "ES_OK", 1: "ES_E_DIM_001", 2: "ES_E_DIM_002", 3: "ES_E_ARG", 4: "ES_E_UNSUPPORTED",
           5: "ES_E_CUDA", 6: "ES_E_TIMEOUT", 7: "ES_E_BODY"}
 MAX_SEQS = 8
-PATHS = {0: "auto", 1: "empty", 2: "generic", 3: "lane_tma", 4: "time_tma", 5: "vec_tma", 6: "mat_tma"}
+PATHS = {0: "auto", 1: "empty", 2: "generic", 3: "lane_tma", 4: "time_tma", 5: "vec_tma", 6: "mat_tma",
+         7: "mat_chunked"}
 PATH_IDS = {v: k for k, v in PATHS.items()}
 
 # every function include/es.h declares
@@ -32,7 +33,7 @@ EXPORTS = ("es_scan_f32", "es_plan_f32", "es_scan_backward_f32", "es_plan_backwa
            "es_set_drop_tile", "es_body_create", "es_body_destroy", "es_body_n_seqs", "es_scan_body_f32",
            "es_plan_body_f32", "es_body_source", "es_body_prepare", "es_body_compile_count", "es_matrix_scan_f32",
            "es_plan_matrix_scan_f32", "es_linear_scan_f32", "es_plan_linear_scan_f32", "es_table_scan_i32",
-           "es_plan_table_scan_i32")
+           "es_plan_table_scan_i32", "es_matrix_scan_workspace_f32", "es_matrix_scan_ws_f32")
 
 
 class LibraryMissing(ImportError):
@@ -120,6 +121,11 @@ def lib():
         L.es_linear_scan_f32.restype = ctypes.c_int
         L.es_plan_linear_scan_f32.argtypes = msig + [P, ctypes.POINTER(PlanInfo)]
         L.es_plan_linear_scan_f32.restype = ctypes.c_int
+        L.es_matrix_scan_workspace_f32.argtypes = [i64p, ctypes.c_int, i64p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.POINTER(ctypes.c_size_t)]
+        L.es_matrix_scan_workspace_f32.restype = ctypes.c_int
+        L.es_matrix_scan_ws_f32.argtypes = msig + [ctypes.c_int, P, P, ctypes.c_size_t, P]
+        L.es_matrix_scan_ws_f32.restype = ctypes.c_int
         tsig = [P, ctypes.c_int64, ctypes.c_int64, P, i64p, ctypes.c_int, ctypes.c_int, ctypes.c_int32]
         L.es_table_scan_i32.argtypes = tsig + [P, P]
         L.es_table_scan_i32.restype = ctypes.c_int
@@ -512,6 +518,39 @@ def matrix_scan(a, b, axis: int = 0, reverse: bool = False, projective: bool = F
     handle = stream if isinstance(stream, int) else stream.cuda_stream
     _check(lib().es_matrix_scan_f32(a.data_ptr(), sa, ra, b.data_ptr(), sb, rb, int(axis), int(bool(reverse)),
                                     int(bool(projective)), out.data_ptr(), handle))
+    return out
+
+
+def matrix_scan_workspace(a_shape, b_shape, axis: int = 0, projective: bool = False) -> int:
+    """Workspace bytes the chunked path would use for these shapes (0: the
+    call runs lane by lane and needs none).  No GPU needed."""
+    sa, ra = _shape_array(a_shape)
+    sb, rb = _shape_array(b_shape)
+    n = ctypes.c_size_t()
+    _check(lib().es_matrix_scan_workspace_f32(sa, ra, sb, rb, int(axis), int(bool(projective)), ctypes.byref(n)))
+    return int(n.value)
+
+
+def matrix_scan_ws(a, b, workspace, axis: int = 0, reverse: bool = False, projective: bool = False, out=None,
+                   stream=None):
+    """matrix-scan with a caller workspace (a CUDA tensor of at least
+    ``matrix_scan_workspace`` bytes): few long lanes run the chunked scan."""
+    import torch
+    _require_cuda_f32(a, "a")
+    _require_cuda_f32(b, "b")
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA tensor")
+    shape = _lead_broadcast(list(a.shape[:-2]), list(b.shape[:-2])) + [int(b.shape[-2]), int(b.shape[-1])]
+    if out is None:
+        out = torch.empty(shape, device=b.device, dtype=torch.float32)
+    sa, ra = _shape_array(a.shape)
+    sb, rb = _shape_array(b.shape)
+    if stream is None:
+        stream = torch.cuda.current_stream(b.device)
+    handle = stream if isinstance(stream, int) else stream.cuda_stream
+    _check(lib().es_matrix_scan_ws_f32(a.data_ptr(), sa, ra, b.data_ptr(), sb, rb, int(axis), int(bool(reverse)),
+                                       int(bool(projective)), out.data_ptr(), workspace.data_ptr(),
+                                       workspace.numel() * workspace.element_size(), handle))
     return out
 
 

@@ -296,7 +296,7 @@ es_status api_device(int* dev, DeviceState** st) { return device_state(dev, st);
 
 es_status api_encoder(EncodeTiledFn* fn) { return encoder(fn); }
 
-void count_launch() { g_launches.fetch_add(1); }
+void count_launch(int kernels) { g_launches.fetch_add(static_cast<uint64_t>(kernels)); }
 
 uint64_t api_wait_ns() { return g_wait_ns.load(); }
 
@@ -498,7 +498,7 @@ uint64_t es_launch_count(void) { return g_launches.load(); }
 
 es_status es_set_path_override(int path) {
     if (path != ES_PATH_AUTO && path != ES_PATH_GENERIC && path != ES_PATH_LANE_TMA && path != ES_PATH_TIME_TMA &&
-        path != ES_PATH_VEC_TMA && path != ES_PATH_MAT_TMA)
+        path != ES_PATH_VEC_TMA && path != ES_PATH_MAT_TMA && path != ES_PATH_MAT_CHUNKED)
         return fail(ES_E_ARG, "es_set_path_override: unknown path %d", path);
     g_path_override.store(path);
     return ES_OK;

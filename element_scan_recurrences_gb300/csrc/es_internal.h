@@ -85,7 +85,7 @@ es_status plan_shapes(const char* fn, const char* const* names, const float* ini
 es_status api_fail(es_status st, const char* fmt, ...);
 es_status api_device(int* dev, DeviceState** st);
 es_status api_encoder(EncodeTiledFn* fn);
-void count_launch();
+void count_launch(int kernels = 1);
 uint64_t api_wait_ns();
 int64_t api_drop_tile();
 int api_path_override();

@@ -40,6 +40,12 @@ struct MatLaunch {
 cudaError_t launch_mat_generic(const MatLaunch& L);
 cudaError_t launch_mat_tma(const MatLaunch& L, const char** err);
 
+// The chunked scan for few long lanes (three launches, a caller workspace):
+// how to cut T, the workspace it needs, and the launch.
+void mat_chunk_shape(int64_t lanes, int64_t T, int m, int64_t* chunks, int64_t* chunk);
+size_t mat_chunk_workspace_bytes(int n, int m, int64_t lanes, int64_t chunks);
+cudaError_t launch_mat_chunked(const MatLaunch& L, float* ws, int64_t chunks, int64_t chunk);
+
 // The TMA kernel serves dense operands with n in {2, 4, 8, 16}, 16-byte
 // aligned bases, n*m a multiple of 4 and at most 256, and a lane group of at
 // most 32 threads.

@@ -179,6 +179,18 @@ es_status choose_matrix_path(const char* fn, MatPlan* P) {
     return api_fail(ES_E_UNSUPPORTED, "%s: the forced kernel path %d cannot serve this call", fn, forced);
 }
 
+// the chunked scan: few lanes (a lane-by-lane run would leave the GPU
+// idle), many trips, no projective normalisation
+bool chunked_applies(const MatPlan& P) {
+    const MatLaunch& L = P.L;
+    return !P.empty && !L.projective && L.g.lanes * L.m < 8192 && L.T >= 256;
+}
+
+size_t chunked_workspace(const MatPlan& P, int64_t* chunks, int64_t* chunk) {
+    mat_chunk_shape(P.L.g.lanes, P.L.T, P.L.m, chunks, chunk);
+    return mat_chunk_workspace_bytes(P.L.n, P.L.m, P.L.g.lanes, *chunks);
+}
+
 void fill_matrix_info(const MatPlan& P, es_plan_info* info) {
     if (info == nullptr) return;
     std::memset(info, 0, sizeof(*info));
@@ -262,6 +274,60 @@ es_status es_matrix_scan_f32(const float* a, const int64_t* a_shape, int a_rank,
     if (st == ES_OK) st = es::choose_matrix_path("es_matrix_scan_f32", &P);
     if (st != ES_OK || P.empty) return st;
     return es::launch_matrix("es_matrix_scan_f32", &P, reinterpret_cast<cudaStream_t>(stream));
+}
+
+es_status es_matrix_scan_workspace_f32(const int64_t* a_shape, int a_rank, const int64_t* b_shape, int b_rank,
+                                       int axis, int projective, size_t* bytes) {
+    if (bytes == nullptr) return es::api_fail(ES_E_ARG, "es_matrix_scan_workspace_f32: null result pointer");
+    es::MatPlan P{};
+    // shapes only: stand-in pointers that pass the pointer checks
+    const float* pa = reinterpret_cast<const float*>(uintptr_t(1) << 44);
+    const float* pb = reinterpret_cast<const float*>(uintptr_t(2) << 44);
+    float* po = reinterpret_cast<float*>(uintptr_t(3) << 44);
+    es_status st = es::plan_matrix("es_matrix_scan_workspace_f32", pa, a_shape, a_rank, pb, b_shape, b_rank, axis, 0,
+                                   projective, po, false, &P);
+    if (st != ES_OK) return st;
+    int64_t chunks = 0, chunk = 0;
+    *bytes = es::chunked_applies(P) ? es::chunked_workspace(P, &chunks, &chunk) : 0;
+    return ES_OK;
+}
+
+es_status es_matrix_scan_ws_f32(const float* a, const int64_t* a_shape, int a_rank, const float* b,
+                                const int64_t* b_shape, int b_rank, int axis, int reverse, int projective, float* out,
+                                void* workspace, size_t workspace_bytes, es_stream_t stream) {
+    const char* fn = "es_matrix_scan_ws_f32";
+    es::MatPlan P{};
+    es_status st = es::plan_matrix(fn, a, a_shape, a_rank, b, b_shape, b_rank, axis, reverse, projective, out, false,
+                                   &P);
+    if (st != ES_OK || P.empty) return st;
+    int64_t chunks = 0, chunk = 0;
+    const size_t need = es::chunked_applies(P) ? es::chunked_workspace(P, &chunks, &chunk) : 0;
+    const int forced = es::api_path_override();
+    const bool chunked = need > 0 && workspace != nullptr && workspace_bytes >= need &&
+                         (forced == ES_PATH_AUTO || forced == ES_PATH_MAT_CHUNKED);
+    if (!chunked) {
+        if (forced == ES_PATH_MAT_CHUNKED)
+            return es::api_fail(ES_E_UNSUPPORTED, "%s: the chunked path needs few long lanes and %zu workspace bytes",
+                                fn, need);
+        if ((st = es::choose_matrix_path(fn, &P)) != ES_OK) return st;
+        return es::launch_matrix(fn, &P, reinterpret_cast<cudaStream_t>(stream));
+    }
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return es::api_fail(ES_E_ARG, "%s: workspace not 16-byte aligned", fn);
+    const uintptr_t wlo = reinterpret_cast<uintptr_t>(workspace), whi = wlo + need;
+    const void* ops[3] = {a, b, out};
+    const int64_t cnt[3] = {P.n_a, P.n_b, P.n_out};
+    for (int k = 0; k < 3; ++k) {
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(ops[k]), hi = lo + static_cast<uintptr_t>(cnt[k]) * 4;
+        if (lo < whi && wlo < hi) return es::api_fail(ES_E_ARG, "%s: the workspace overlaps an operand", fn);
+    }
+    int dev = 0;
+    es::DeviceState* ds = nullptr;
+    if ((st = es::api_device(&dev, &ds)) != ES_OK) return st;
+    P.L.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = es::launch_mat_chunked(P.L, static_cast<float*>(workspace), chunks, chunk);
+    if (e != cudaSuccess) return es::api_fail(ES_E_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+    es::count_launch(3);
+    return ES_OK;
 }
 
 es_status es_plan_linear_scan_f32(const float* a, const int64_t* a_shape, int a_rank, const float* b,

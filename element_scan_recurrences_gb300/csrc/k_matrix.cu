@@ -449,4 +449,199 @@ cudaError_t launch_mat_tma(const MatLaunch& L, const char** err) {
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// few long lanes: a chunked scan in three launches
+//
+// The recurrence composes: over a chunk of trips s..e, h[e] = Phi h[s-1] + u[e]
+// with Phi = a[e] ... a[s] and u the chunk's scan from zero.  With few lanes
+// the sequential kernels leave most of the GPU idle, so the trips are cut
+// into chunks:
+//   1. k_mat_chunk_local, one thread per column of every (lane, chunk): the
+//      chunk's scan from zero (its last state u[e]) and, in n more column
+//      threads, its transition product Phi (the scan of the identity with no
+//      b); both go to the workspace;
+//   2. k_mat_chunk_carry, one thread per (lane, column): the chunks in scan
+//      order, carry = Phi_k carry + u_k, recording the carry into each chunk;
+//   3. k_mat_chunk_final, one thread per column of every (lane, chunk): the
+//      chunk scanned again from its carry, writing the states.
+// Every step keeps the definition's order inside a product, but the carries
+// reassociate the chain (Phi_k applied to a carry rather than step by step),
+// so results agree with the sequential scan to rounding, not bit for bit.
+// Workspace per (lane, chunk): Phi (n x n), u[e] and the carry (n x m each).
+
+namespace {
+
+// the trips of chunk k in scan order: first trip, step
+struct ChunkTrips {
+    int64_t first;
+    int64_t count;
+    int64_t step;
+};
+
+__device__ __forceinline__ ChunkTrips chunk_trips(int64_t k, int64_t chunk, int64_t T, int reverse) {
+    // chunks count in scan order: chunk 0 holds the first trips scanned
+    const int64_t lo = k * chunk;
+    const int64_t cnt = min(chunk, T - lo);
+    return reverse ? ChunkTrips{T - 1 - lo, cnt, -1} : ChunkTrips{lo, cnt, 1};
+}
+
+__device__ __forceinline__ void lane_offsets(const MatGeom& g, int64_t lane, int64_t* oa, int64_t* ob, int64_t* oo) {
+    int64_t rem = lane;
+    *oa = *ob = *oo = 0;
+    for (int d = g.nd - 1; d >= 0; --d) {
+        const int64_t q = rem % g.dim[d];
+        rem /= g.dim[d];
+        *oa += q * g.sa[d];
+        *ob += q * g.sb[d];
+        *oo += q * g.so[d];
+    }
+}
+
+template <int N>
+__global__ void __launch_bounds__(128)
+k_mat_chunk_local(const float* __restrict__ a, const float* __restrict__ b, float* __restrict__ ws, const MatGeom g,
+                  int m, int64_t chunks, int64_t chunk, int reverse) {
+    const int cols = m + N;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t unit = tid / cols;                      // (lane, chunk)
+    const int c = static_cast<int>(tid % cols);
+    if (unit >= g.lanes * chunks) return;
+    const int64_t lane = unit / chunks, k = unit % chunks;
+    int64_t oa, ob, oo;
+    lane_offsets(g, lane, &oa, &ob, &oo);
+    const bool is_h = c < m;
+    float h[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) h[i] = (!is_h && i == c - m) ? 1.0f : 0.0f;
+    const ChunkTrips ct = chunk_trips(k, chunk, g.T, reverse);
+    for (int64_t q = 0; q < ct.count; ++q) {
+        const int64_t t = ct.first + q * ct.step;
+        const float* A = a + (oa + t * g.ta) * N * N;
+        float hn[N];
+        column_step<N>(hn, h, [&](int i, float (&r)[N]) {
+#pragma unroll
+            for (int j = 0; j < N; ++j) r[j] = __ldg(A + i * N + j);
+        });
+        if (is_h) {
+            const float* B = b + (ob + t * g.tb) * N * m + c;
+#pragma unroll
+            for (int i = 0; i < N; ++i) hn[i] = __fadd_rn(hn[i], __ldg(B + i * m));
+        }
+#pragma unroll
+        for (int i = 0; i < N; ++i) h[i] = hn[i];
+    }
+    // workspace unit: Phi [N][N] (column c - m), then u [N][m] (column c)
+    float* wu = ws + unit * (static_cast<int64_t>(N) * N + 2LL * N * m);
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        if (is_h) wu[N * N + i * m + c] = h[i];
+        else wu[i * N + (c - m)] = h[i];
+    }
+}
+
+template <int N>
+__global__ void __launch_bounds__(128)
+k_mat_chunk_carry(float* __restrict__ ws, int64_t lanes, int m, int64_t chunks) {
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (tid >= lanes * m) return;
+    const int64_t lane = tid / m;
+    const int c = static_cast<int>(tid % m);
+    const int64_t unit_floats = static_cast<int64_t>(N) * N + 2LL * N * m;
+    float carry[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) carry[i] = 0.0f;
+    for (int64_t k = 0; k < chunks; ++k) {
+        float* wu = ws + (lane * chunks + k) * unit_floats;
+        float* carry_in = wu + N * N + N * m;
+#pragma unroll
+        for (int i = 0; i < N; ++i) carry_in[i * m + c] = carry[i];
+        const float* Phi = wu;
+        float hn[N];
+        column_step<N>(hn, carry, [&](int i, float (&r)[N]) {
+#pragma unroll
+            for (int j = 0; j < N; ++j) r[j] = Phi[i * N + j];
+        });
+#pragma unroll
+        for (int i = 0; i < N; ++i) carry[i] = __fadd_rn(hn[i], wu[N * N + i * m + c]);
+    }
+}
+
+template <int N>
+__global__ void __launch_bounds__(128)
+k_mat_chunk_final(const float* __restrict__ a, const float* __restrict__ b, const float* __restrict__ ws,
+                  float* __restrict__ out, const MatGeom g, int m, int64_t chunks, int64_t chunk, int reverse) {
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t unit = tid / m;
+    const int c = static_cast<int>(tid % m);
+    if (unit >= g.lanes * chunks) return;
+    const int64_t lane = unit / chunks, k = unit % chunks;
+    int64_t oa, ob, oo;
+    lane_offsets(g, lane, &oa, &ob, &oo);
+    const float* carry_in = ws + unit * (static_cast<int64_t>(N) * N + 2LL * N * m) + N * N + N * m;
+    float h[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) h[i] = carry_in[i * m + c];
+    const ChunkTrips ct = chunk_trips(k, chunk, g.T, reverse);
+    for (int64_t q = 0; q < ct.count; ++q) {
+        const int64_t t = ct.first + q * ct.step;
+        const float* A = a + (oa + t * g.ta) * N * N;
+        float hn[N];
+        column_step<N>(hn, h, [&](int i, float (&r)[N]) {
+#pragma unroll
+            for (int j = 0; j < N; ++j) r[j] = __ldg(A + i * N + j);
+        });
+        const float* B = b + (ob + t * g.tb) * N * m + c;
+        float* O = out + (oo + t * g.to) * N * m + c;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            h[i] = __fadd_rn(hn[i], __ldg(B + i * m));
+            __stcs(O + i * m, h[i]);
+        }
+    }
+}
+
+template <int N>
+cudaError_t launch_chunked_n(const MatLaunch& L, float* ws, int64_t chunks, int64_t chunk) {
+    const int64_t units = L.g.lanes * chunks;
+    const int64_t t1 = units * (L.m + N), t2 = L.g.lanes * L.m, t3 = units * L.m;
+    for (int64_t t : {t1, t2, t3})
+        if ((t + 127) / 128 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    k_mat_chunk_local<N><<<static_cast<unsigned>((t1 + 127) / 128), 128, 0, L.stream>>>(L.a, L.b, ws, L.g, L.m,
+                                                                                       chunks, chunk, L.reverse);
+    k_mat_chunk_carry<N><<<static_cast<unsigned>((t2 + 127) / 128), 128, 0, L.stream>>>(ws, L.g.lanes, L.m, chunks);
+    k_mat_chunk_final<N><<<static_cast<unsigned>((t3 + 127) / 128), 128, 0, L.stream>>>(L.a, L.b, ws, L.out, L.g,
+                                                                                       L.m, chunks, chunk, L.reverse);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+void mat_chunk_shape(int64_t lanes, int64_t T, int m, int64_t* chunks, int64_t* chunk) {
+    // about 4096 (lane, chunk) units of at least 64 trips
+    int64_t c = lanes >= 4096 ? 1 : (4096 + lanes - 1) / lanes;
+    const int64_t max_chunks = T / 64 > 1 ? T / 64 : 1;
+    if (c > max_chunks) c = max_chunks;
+    *chunk = (T + c - 1) / c;
+    *chunks = (T + *chunk - 1) / *chunk;
+    (void)m;
+}
+
+size_t mat_chunk_workspace_bytes(int n, int m, int64_t lanes, int64_t chunks) {
+    return static_cast<size_t>(lanes) * static_cast<size_t>(chunks) *
+           (static_cast<size_t>(n) * n + 2 * static_cast<size_t>(n) * m) * 4;
+}
+
+cudaError_t launch_mat_chunked(const MatLaunch& L, float* ws, int64_t chunks, int64_t chunk) {
+    switch (L.n) {
+#define ES_MAT_CASE(K) \
+    case K: return launch_chunked_n<K>(L, ws, chunks, chunk);
+        ES_MAT_CASE(1) ES_MAT_CASE(2) ES_MAT_CASE(3) ES_MAT_CASE(4) ES_MAT_CASE(5) ES_MAT_CASE(6) ES_MAT_CASE(7)
+        ES_MAT_CASE(8) ES_MAT_CASE(9) ES_MAT_CASE(10) ES_MAT_CASE(11) ES_MAT_CASE(12) ES_MAT_CASE(13)
+        ES_MAT_CASE(14) ES_MAT_CASE(15) ES_MAT_CASE(16)
+#undef ES_MAT_CASE
+    }
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace es

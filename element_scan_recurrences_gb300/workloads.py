@@ -188,6 +188,7 @@ class MatrixWorkload:
     reverse: Tuple[bool, ...] = (False,)
     projective: bool = False
     seed: int = 0
+    workspace: bool = False        # run through the workspace entry (chunked scan for few lanes)
 
     @property
     def ax(self) -> int:
@@ -226,6 +227,8 @@ MATRIX_WORKLOADS = {
     w.name: w for w in [
         # the pages' delta rule: 64 sequences x 16 heads, 1024 steps, 16 x 16 state
         MatrixWorkload("matrix_scan_delta_rule", "delta_rule", (64, 1024, 16), 1, 16, 16),
+        # the delta rule over 8 long sequences: few lanes, run as a chunked scan
+        MatrixWorkload("matrix_scan_few_lanes", "delta_rule", (8, 131072), 1, 16, 16, workspace=True),
         # linear-scan on the shape of the wide-lane element-scan case
         MatrixWorkload("linear_scan_lanes", "linear", (64, 4096, 1024), 1, 1, 1),
     ]

@@ -77,7 +77,8 @@ typedef enum es_path {
     ES_PATH_LANE_TMA = 3,  /* lanes innermost: TMA/mbarrier time-tile pipeline */
     ES_PATH_TIME_TMA = 4,  /* time innermost: TMA tiles transposed in SMEM     */
     ES_PATH_VEC_TMA = 5,   /* vector state: TMA pipeline + xor shuffles        */
-    ES_PATH_MAT_TMA = 6    /* matrix-scan, dense operands: TMA pipeline        */
+    ES_PATH_MAT_TMA = 6,   /* matrix-scan, dense operands: TMA pipeline        */
+    ES_PATH_MAT_CHUNKED = 7 /* matrix-scan, few long lanes: chunked scan (3 kernels) */
 } es_path;
 
 /*
@@ -291,6 +292,34 @@ es_status es_plan_matrix_scan_f32(const float *a, const int64_t *a_shape, int a_
                                   const float *b, const int64_t *b_shape, int b_rank,
                                   int axis, int reverse, int projective, const float *out,
                                   es_plan_info *info);
+
+/*
+ * Few long lanes.  A matrix-scan over few lanes (lanes * m < 8192) and many
+ * trips (T >= 256) leaves most of the GPU idle when run lane by lane; since
+ * the recurrence composes (over trips s..e, h[e] = (a[e]...a[s]) h[s-1] + the
+ * chunk's scan from zero), it can instead run as a chunked scan in three
+ * launches: each (lane, chunk) scans from zero and forms its transition
+ * product, one pass per lane carries the chunks' boundary states, and each
+ * chunk is scanned again from its carry.  The carries reassociate the
+ * chain, so these results agree with the sequential order to rounding
+ * (within 1e-5 * (1 + |h|) for non-expansive a), not bit for bit.  The chunks'
+ * products and boundary states need a workspace, which the caller provides
+ * (the library allocates nothing); projective scans always run sequentially.
+ *
+ * es_matrix_scan_workspace_f32: the workspace bytes a call with these shapes
+ * would use (0 when it runs sequentially and needs none).  Host logic only.
+ * es_matrix_scan_ws_f32: es_matrix_scan_f32 with a device workspace of
+ * `workspace_bytes` (16-byte aligned, not overlapping the operands): the
+ * chunked scan when it applies and the workspace suffices (ES_PATH_MAT_CHUNKED),
+ * else exactly es_matrix_scan_f32.
+ */
+es_status es_matrix_scan_workspace_f32(const int64_t *a_shape, int a_rank, const int64_t *b_shape,
+                                       int b_rank, int axis, int projective, size_t *bytes);
+
+es_status es_matrix_scan_ws_f32(const float *a, const int64_t *a_shape, int a_rank,
+                                const float *b, const int64_t *b_shape, int b_rank,
+                                int axis, int reverse, int projective, float *out,
+                                void *workspace, size_t workspace_bytes, es_stream_t stream);
 
 /*
  * es_linear_scan_f32 -- linear-scan, the matrix-scan over one-by-one matrices

@@ -175,3 +175,74 @@ def test_full_size_sampled(name):
     else:
         want = M.matrix_scan(sa, sb, axis=0)
     bitwise(got, want, name)
+
+
+def close(got, want, what, tol=1e-5):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    err = np.abs(got - want) / (1.0 + np.abs(want))
+    assert float(err.max()) <= tol, "%s: max scaled error %.3g" % (what, float(err.max()))
+
+
+@pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
+@pytest.mark.parametrize("n,m,T", [(16, 16, 3001), (4, 3, 1000), (1, 1, 5000), (7, 2, 640)])
+def test_chunked_few_lanes(n, m, T, reverse):
+    """Few long lanes through the workspace entry: the chunked scan (chunks of
+    uneven count, the last one short), within 1e-5 * (1 + |h|) of the
+    sequential oracle for non-expansive a."""
+    rng = np.random.default_rng(n * 7 + m + T)
+    a = contractive(rng, (3, T), n, norm=0.98)
+    b = rng.standard_normal((3, T, n, m)).astype(np.float32)
+    need = es.matrix_scan_workspace(a.shape, b.shape, 1)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    da, db = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    n0 = es.launch_count()
+    got = es.matrix_scan_ws(da, db, ws, axis=1, reverse=reverse)
+    es.device_status()
+    assert es.launch_count() - n0 == 3
+    close(got.cpu().numpy(), M.matrix_scan(a, b, axis=1, reverse=reverse), "chunked n=%d m=%d T=%d" % (n, m, T))
+
+
+def test_chunked_fallbacks_and_broadcast():
+    rng = np.random.default_rng(11)
+    a = contractive(rng, (2, 700), 4)
+    b = rng.standard_normal((2, 700, 4, 2)).astype(np.float32)
+    da, db = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    need = es.matrix_scan_workspace(a.shape, b.shape, 1)
+    # too small a workspace: the sequential kernels, bit for bit
+    small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    got = es.matrix_scan_ws(da, db, small, axis=1)
+    bitwise(got.cpu().numpy(), M.matrix_scan(a, b, axis=1), "fallback")
+    # forcing the chunked path without enough workspace is refused
+    es.set_path_override("mat_chunked")
+    try:
+        with pytest.raises(es.EsError) as e:
+            es.matrix_scan_ws(da, db, small, axis=1)
+        assert e.value.status == 4
+    finally:
+        es.set_path_override("auto")
+    # a shared by the lanes (broadcast), chunked
+    a1 = np.ascontiguousarray(a[:1])
+    need = es.matrix_scan_workspace(a1.shape, b.shape, 1)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    got = es.matrix_scan_ws(torch.from_numpy(a1).cuda(), db, ws, axis=1)
+    close(got.cpu().numpy(), M.matrix_scan(a1, b, axis=1), "broadcast a, chunked")
+    # projective scans never take the chunked path
+    assert es.matrix_scan_workspace(a.shape, b.shape, 1, projective=True) == 0
+    es.device_status()
+
+
+def test_chunked_full_size_sampled():
+    """The few-lanes bench workload at full size: sampled lanes checked by the
+    oracle on whole sequences (tolerance), the bench's launch configuration."""
+    from element_scan_recurrences_gb300 import workloads as wl
+    w = wl.MATRIX_WORKLOADS["matrix_scan_few_lanes"]
+    a, b = wl.make_matrix_inputs(w, "cuda")
+    ws = torch.empty(es.matrix_scan_workspace(w.a_shape, w.b_shape, w.axis), dtype=torch.uint8, device="cuda")
+    out = es.matrix_scan_ws(a, b, ws, axis=w.axis)
+    es.device_status()
+    for lane in (0, w.lead[0] - 1):
+        sa, sb = a[lane].cpu().numpy(), b[lane].cpu().numpy()
+        close(out[lane].cpu().numpy(), M.matrix_scan(sa, sb, axis=0), "lane %d" % lane)
