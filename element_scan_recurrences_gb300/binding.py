@@ -33,7 +33,8 @@ EXPORTS = ("es_scan_f32", "es_plan_f32", "es_scan_backward_f32", "es_plan_backwa
            "es_set_drop_tile", "es_body_create", "es_body_destroy", "es_body_n_seqs", "es_scan_body_f32",
            "es_plan_body_f32", "es_body_source", "es_body_prepare", "es_body_compile_count", "es_matrix_scan_f32",
            "es_plan_matrix_scan_f32", "es_linear_scan_f32", "es_plan_linear_scan_f32", "es_table_scan_i32",
-           "es_plan_table_scan_i32", "es_matrix_scan_workspace_f32", "es_matrix_scan_ws_f32")
+           "es_plan_table_scan_i32", "es_matrix_scan_workspace_f32", "es_matrix_scan_ws_f32",
+           "es_matrix_scan_static_f32")
 
 
 class LibraryMissing(ImportError):
@@ -126,6 +127,8 @@ def lib():
         L.es_matrix_scan_workspace_f32.restype = ctypes.c_int
         L.es_matrix_scan_ws_f32.argtypes = msig + [ctypes.c_int, P, P, ctypes.c_size_t, P]
         L.es_matrix_scan_ws_f32.restype = ctypes.c_int
+        L.es_matrix_scan_static_f32.argtypes = msig + [ctypes.c_int, P, P]
+        L.es_matrix_scan_static_f32.restype = ctypes.c_int
         tsig = [P, ctypes.c_int64, ctypes.c_int64, P, i64p, ctypes.c_int, ctypes.c_int, ctypes.c_int32]
         L.es_table_scan_i32.argtypes = tsig + [P, P]
         L.es_table_scan_i32.restype = ctypes.c_int
@@ -551,6 +554,29 @@ def matrix_scan_ws(a, b, workspace, axis: int = 0, reverse: bool = False, projec
     _check(lib().es_matrix_scan_ws_f32(a.data_ptr(), sa, ra, b.data_ptr(), sb, rb, int(axis), int(bool(reverse)),
                                        int(bool(projective)), out.data_ptr(), workspace.data_ptr(),
                                        workspace.numel() * workspace.element_size(), handle))
+    return out
+
+
+STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def matrix_scan_static(a, b, axis: int = 0, reverse: bool = False, projective: bool = False, out=None,
+                       stream=None):
+    """matrix-scan whose chunked path (few long lanes) runs in the library's
+    own static device scratch: no workspace argument, no allocation."""
+    import torch
+    _require_cuda_f32(a, "a")
+    _require_cuda_f32(b, "b")
+    shape = _lead_broadcast(list(a.shape[:-2]), list(b.shape[:-2])) + [int(b.shape[-2]), int(b.shape[-1])]
+    if out is None:
+        out = torch.empty(shape, device=b.device, dtype=torch.float32)
+    sa, ra = _shape_array(a.shape)
+    sb, rb = _shape_array(b.shape)
+    if stream is None:
+        stream = torch.cuda.current_stream(b.device)
+    handle = stream if isinstance(stream, int) else stream.cuda_stream
+    _check(lib().es_matrix_scan_static_f32(a.data_ptr(), sa, ra, b.data_ptr(), sb, rb, int(axis),
+                                           int(bool(reverse)), int(bool(projective)), out.data_ptr(), handle))
     return out
 
 

@@ -16,8 +16,25 @@
 #include "es_internal.h"
 #include "es_matrix.h"
 
+// Scratch the library owns for es_matrix_scan_static_f32: module scope, so no
+// call allocates device memory.
+static __device__ __align__(256) unsigned char g_es_static_scratch[ES_STATIC_SCRATCH_BYTES];
+
 namespace es {
 namespace {
+
+// the static scratch of one device: its address, fetched once, and the event
+// that orders successive uses
+struct StaticScratch {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    void* ptr = nullptr;
+    cudaEvent_t released = nullptr;
+    bool used = false;
+    std::mutex mu;
+};
+constexpr int kScratchDevices = 64;
+StaticScratch g_scratch[kScratchDevices];
 
 std::string dims_str(const int64_t* d, int r) {
     std::string s = "[";
@@ -327,6 +344,35 @@ es_status es_matrix_scan_ws_f32(const float* a, const int64_t* a_shape, int a_ra
     cudaError_t e = es::launch_mat_chunked(P.L, static_cast<float*>(workspace), chunks, chunk);
     if (e != cudaSuccess) return es::api_fail(ES_E_CUDA, "%s: %s", fn, cudaGetErrorString(e));
     es::count_launch(3);
+    return ES_OK;
+}
+
+es_status es_matrix_scan_static_f32(const float* a, const int64_t* a_shape, int a_rank, const float* b,
+                                    const int64_t* b_shape, int b_rank, int axis, int reverse, int projective,
+                                    float* out, es_stream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return es::api_fail(ES_E_CUDA, "es_matrix_scan_static_f32: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= es::kScratchDevices)
+        return es::api_fail(ES_E_UNSUPPORTED, "es_matrix_scan_static_f32: device ordinal %d too large", dev);
+    es::StaticScratch& sc = es::g_scratch[dev];
+    std::call_once(sc.once, [&]() {
+        sc.err = cudaGetSymbolAddress(&sc.ptr, g_es_static_scratch);
+        if (sc.err == cudaSuccess) sc.err = cudaEventCreateWithFlags(&sc.released, cudaEventDisableTiming);
+    });
+    if (sc.err != cudaSuccess)
+        return es::api_fail(ES_E_CUDA, "es_matrix_scan_static_f32: scratch set-up: %s", cudaGetErrorString(sc.err));
+    std::lock_guard<std::mutex> lock(sc.mu);
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the previous user of the scratch, on whatever stream, comes first
+    if (sc.used && (e = cudaStreamWaitEvent(s, sc.released, 0)) != cudaSuccess)
+        return es::api_fail(ES_E_CUDA, "es_matrix_scan_static_f32: %s", cudaGetErrorString(e));
+    es_status st = es_matrix_scan_ws_f32(a, a_shape, a_rank, b, b_shape, b_rank, axis, reverse, projective, out,
+                                         sc.ptr, ES_STATIC_SCRATCH_BYTES, stream);
+    if (st != ES_OK) return st;
+    if ((e = cudaEventRecord(sc.released, s)) != cudaSuccess)
+        return es::api_fail(ES_E_CUDA, "es_matrix_scan_static_f32: %s", cudaGetErrorString(e));
+    sc.used = true;
     return ES_OK;
 }
 

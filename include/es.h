@@ -322,6 +322,23 @@ es_status es_matrix_scan_ws_f32(const float *a, const int64_t *a_shape, int a_ra
                                 void *workspace, size_t workspace_bytes, es_stream_t stream);
 
 /*
+ * es_matrix_scan_static_f32 -- es_matrix_scan_ws_f32 without a caller
+ * workspace: the chunked scan runs in a scratch array the library owns (a
+ * static device array of ES_STATIC_SCRATCH_BYTES per device, part of the
+ * library's module, its address fetched once per device), so the call
+ * allocates nothing and takes no workspace.  A call whose chunked scan would
+ * need more runs lane by lane, exactly as es_matrix_scan_f32.  Successive
+ * calls on one device are ordered through the scratch (each waits on an
+ * event the previous one recorded), so calls on different streams do not
+ * overlap in it.
+ */
+#define ES_STATIC_SCRATCH_BYTES (32u << 20)
+es_status es_matrix_scan_static_f32(const float *a, const int64_t *a_shape, int a_rank,
+                                    const float *b, const int64_t *b_shape, int b_rank,
+                                    int axis, int reverse, int projective, float *out,
+                                    es_stream_t stream);
+
+/*
  * es_linear_scan_f32 -- linear-scan, the matrix-scan over one-by-one matrices
  * ("matrix-scan" section): h[t] = a[t] * h[t-1] + b[t] from h = 0, with a and
  * b broadcast NumPy-style to one shape (rank 0 is a number), `axis` counting
