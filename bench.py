@@ -40,6 +40,7 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 PATH_KERNEL = {"lane_tma": "k_lane_tma", "time_tma": "k_time_tma", "vec_tma": "k_vec_tma", "generic": "k_generic"}
 PATH_KERNEL_BWD = {"lane_tma": "k_lane_bwd", "generic": "k_generic_bwd"}
+PATH_KERNEL_BODY_BWD = {"generic": "k_body_generic_bwd"}
 # kernels compiled at run time from a body program
 PATH_KERNEL_BODY = {"lane_tma": "k_body_lane", "time_tma": "k_body_time", "vec_tma": "k_body_vec",
                     "generic": "k_body_generic"}
@@ -181,6 +182,7 @@ KERNEL_SOURCES = {
     "k_vec_bwd": ["k_vec_bwd.cu"], "k_time_bwd": ["k_time_bwd.cu"],
     "k_body_lane": ["skel_lane.cuh"] + _BODY_SOURCES, "k_body_time": ["skel_time.cuh"] + _BODY_SOURCES,
     "k_body_vec": ["skel_vec.cuh"] + _BODY_SOURCES, "k_body_generic": ["skel_generic.cuh"] + _BODY_SOURCES,
+    "k_body_generic_bwd": ["skel_generic_bwd.cuh"] + _BODY_SOURCES,
 }
 
 
@@ -226,6 +228,17 @@ def oracle_scan(w, init, seqs, reverse):
         return scan_body(w.text, init, seqs, axis=w.axis, state_axis=w.state_axis, reverse=reverse)
     import oracle
     return oracle.scan(w.body, init, seqs, axis=w.axis, state_axis=w.state_axis, reverse=reverse)
+
+
+def oracle_backward(w, init, seqs, states, grad_out, reverse):
+    """The CPU gradient oracle on host arrays (fixed body or body program)."""
+    if w.text is not None:
+        from oracle.body_grad import scan_body_backward
+        return scan_body_backward(w.text, init, seqs, states, grad_out, axis=w.axis, state_axis=w.state_axis,
+                                  reverse=reverse)
+    import oracle
+    return oracle.scan_backward(w.body, init, seqs, states, grad_out, axis=w.axis, state_axis=w.state_axis,
+                                reverse=reverse)
 
 
 def take_sample(w, init, seqs, target_elems: int):
@@ -274,8 +287,7 @@ def cpu_oracle_rate(w, init, seqs, budget_s: float, backward: bool = False):
         t0 = time.perf_counter()
         for k, reverse in enumerate(w.reverse):
             if backward:
-                oracle.scan_backward(w.body, ins, ss, prep[k][0], prep[k][1], axis=w.axis,
-                                     state_axis=w.state_axis, reverse=reverse)
+                oracle_backward(w, ins, ss, prep[k][0], prep[k][1], reverse)
             else:
                 oracle_scan(w, ins, ss, reverse)
         return time.perf_counter() - t0, elems * len(w.reverse), desc
@@ -301,20 +313,38 @@ def run_reference(args, w):
     init, seqs = wl.make_inputs(w, "cpu")
     # each step scans a bounded sample so that the whole run stays short
     step_budget = max(0.05, min(1.0, 120.0 / max(1, args.steps + args.warmup)))
-    ins, ss, elems, _ = take_sample(w, init, seqs, 1 << 18)
+    backward = args.pass_ == "backward"
+
+    def sample(target):
+        ins, ss, elems, desc = take_sample(w, init, seqs, target)
+        prep = []
+        if backward:
+            # the sample's saved states and an all-ones output gradient (untimed)
+            import numpy as np
+            for r in w.reverse:
+                st = oracle_scan(w, ins, ss, r)
+                prep.append((st, np.ones_like(st)))
+        return ins, ss, elems, desc, prep
+
+    def one_step(ins, ss, prep):
+        for k, r in enumerate(w.reverse):
+            if backward:
+                oracle_backward(w, ins, ss, prep[k][0], prep[k][1], r)
+            else:
+                oracle_scan(w, ins, ss, r)
+
+    calib = 1 << 18 if not backward or w.text is None else 1 << 14
+    ins, ss, elems, _, prep = sample(calib)
     t0 = time.perf_counter()
-    for r in w.reverse:
-        oracle_scan(w, ins, ss, r)
+    one_step(ins, ss, prep)
     t_cal = time.perf_counter() - t0
-    target = max(1, int((1 << 18) * step_budget / max(t_cal, 1e-4)))
-    ins, ss, elems, desc = take_sample(w, init, seqs, target)
+    target = max(1, int(calib * step_budget / max(t_cal, 1e-4)))
+    ins, ss, elems, desc, prep = sample(target)
     for _ in range(args.warmup):
-        for r in w.reverse:
-            oracle_scan(w, ins, ss, r)
+        one_step(ins, ss, prep)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        for r in w.reverse:
-            oracle_scan(w, ins, ss, r)
+        one_step(ins, ss, prep)
     dt = time.perf_counter() - t0
     elems *= len(w.reverse)
     value = elems * args.steps / dt
@@ -323,7 +353,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config_of(w),
+        "config": config_of(w, backward),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample_desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -448,24 +478,33 @@ def run_ours(args, w):
             es.scan_into(w.body, init, seqs, o, axis=w.axis, state_axis=w.state_axis, reverse=r, stream=stream)
 
     backward = args.pass_ == "backward"
-    if backward and program is not None:
-        raise SystemExit("--pass backward: body programs have no backward kernels yet")
+
+    def scan_backward(o, g, gr, r):
+        if program is not None:
+            program.scan_backward(init, seqs, o, g, axis=w.axis, state_axis=w.state_axis, reverse=r, grads=gr,
+                                  stream=stream)
+        else:
+            es.scan_backward(w.body, init, seqs, o, g, axis=w.axis, state_axis=w.state_axis, reverse=r, grads=gr,
+                             stream=stream)
+
     if backward:
         # saved states and an output gradient per direction (untimed set-up)
         gen = torch.Generator(device=device)
         gen.manual_seed(1000 + rank)
         for o, r in zip(outs, w.reverse):
-            es.scan_into(w.body, init, seqs, o, axis=w.axis, state_axis=w.state_axis, reverse=r, stream=stream)
+            scan_into(o, r)
         gouts = [torch.randn(w.shape, generator=gen, device=device) for _ in w.reverse]
         grads = [(torch.empty_like(init), [torch.empty_like(t) for t in seqs]) for _ in w.reverse]
-        plans = [es.plan_backward(w.body, w.shape, w.axis, w.shape[-1] if w.state_axis else 0,
-                                  w.seq_widths if w.state_axis else None, r) for r in w.reverse]
+        sw_, widths_ = (w.shape[-1], w.seq_widths) if w.state_axis else (0, None)
+        if program is not None:
+            plans = [program.plan_backward(w.shape, w.axis, sw_, widths_, r) for r in w.reverse]
+        else:
+            plans = [es.plan_backward(w.body, w.shape, w.axis, sw_, widths_, r) for r in w.reverse]
 
     def step():
         if backward:
             for o, g, gr, r in zip(outs, gouts, grads, w.reverse):
-                es.scan_backward(w.body, init, seqs, o, g, axis=w.axis, state_axis=w.state_axis, reverse=r,
-                                 grads=gr, stream=stream)
+                scan_backward(o, g, gr, r)
             return
         for o, r in zip(outs, w.reverse):
             scan_into(o, r)
@@ -478,7 +517,10 @@ def run_ours(args, w):
 
     # roofline of the dominant kernel (every launch of a step is the same kernel)
     alg_bytes = w.backward_algorithmic_bytes() if backward else w.algorithmic_bytes()
-    kernels = PATH_KERNEL_BWD if backward else PATH_KERNEL_BODY if program is not None else PATH_KERNEL
+    if backward:
+        kernels = PATH_KERNEL_BODY_BWD if program is not None else PATH_KERNEL_BWD
+    else:
+        kernels = PATH_KERNEL_BODY if program is not None else PATH_KERNEL
     kernel = kernels.get(plans[0]["path"], plans[0]["path"])
     roofline = roofline_of(kernel, w.name + ("_backward" if backward else ""), alg_bytes, kernel_ms)
 
@@ -511,8 +553,7 @@ def run_ours(args, w):
                             d.copy_(hh, non_blocking=True)
                         od.copy_(sh, non_blocking=True)
                         gd.copy_(gh, non_blocking=True)
-                        es.scan_backward(w.body, init, seqs, od, gd, axis=w.axis, state_axis=w.state_axis,
-                                         reverse=r, grads=gr_d, stream=stream)
+                        scan_backward(od, gd, gr_d, r)
                         gr_h[0].copy_(gr_d[0], non_blocking=True)
                         for hh, d in zip(gr_h[1], gr_d[1]):
                             hh.copy_(d, non_blocking=True)

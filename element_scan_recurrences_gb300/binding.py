@@ -34,7 +34,8 @@ EXPORTS = ("es_scan_f32", "es_plan_f32", "es_scan_backward_f32", "es_plan_backwa
            "es_plan_body_f32", "es_body_source", "es_body_prepare", "es_body_compile_count", "es_matrix_scan_f32",
            "es_plan_matrix_scan_f32", "es_linear_scan_f32", "es_plan_linear_scan_f32", "es_table_scan_i32",
            "es_plan_table_scan_i32", "es_matrix_scan_workspace_f32", "es_matrix_scan_ws_f32",
-           "es_matrix_scan_static_f32")
+           "es_matrix_scan_static_f32", "es_scan_body_backward_f32", "es_plan_body_backward_f32",
+           "es_body_source_backward", "es_body_prepare_backward")
 
 
 class LibraryMissing(ImportError):
@@ -111,6 +112,15 @@ def lib():
         L.es_body_source.restype = ctypes.c_int
         L.es_body_prepare.argtypes = [P, ctypes.c_int, ctypes.c_int, i64p, ctypes.c_int]
         L.es_body_prepare.restype = ctypes.c_int
+        L.es_scan_body_backward_f32.argtypes = [P] + bsig[1:] + [P]
+        L.es_scan_body_backward_f32.restype = ctypes.c_int
+        L.es_plan_body_backward_f32.argtypes = [P] + bsig[1:] + [ctypes.POINTER(PlanInfo)]
+        L.es_plan_body_backward_f32.restype = ctypes.c_int
+        L.es_body_source_backward.argtypes = [P, ctypes.c_int, ctypes.c_int, i64p, ctypes.c_char_p, ctypes.c_size_t,
+                                              ctypes.POINTER(ctypes.c_size_t)]
+        L.es_body_source_backward.restype = ctypes.c_int
+        L.es_body_prepare_backward.argtypes = [P, ctypes.c_int, ctypes.c_int, i64p]
+        L.es_body_prepare_backward.restype = ctypes.c_int
         L.es_body_compile_count.argtypes = []
         L.es_body_compile_count.restype = ctypes.c_uint64
         msig = [P, i64p, ctypes.c_int, P, i64p, ctypes.c_int, ctypes.c_int, ctypes.c_int]   # a, b, axis, reverse
@@ -379,6 +389,78 @@ class Body:
         buf = ctypes.create_string_buffer(need.value + 1)
         _check(lib().es_body_source(self._h, int(state_width), n, sw, buf, need.value + 1, ctypes.byref(need)))
         return buf.value.decode()
+
+    def source_backward(self, state_width: int = 0, seq_widths=None) -> str:
+        """The functor with its vector-Jacobian product for a signature."""
+        n = self.n_seqs
+        sw = _widths_array(seq_widths)
+        need = ctypes.c_size_t()
+        _check(lib().es_body_source_backward(self._h, int(state_width), n, sw, None, 0, ctypes.byref(need)))
+        buf = ctypes.create_string_buffer(need.value + 1)
+        _check(lib().es_body_source_backward(self._h, int(state_width), n, sw, buf, need.value + 1,
+                                             ctypes.byref(need)))
+        return buf.value.decode()
+
+    def prepare_backward(self, state_width: int = 0, seq_widths=None) -> None:
+        """Compile ahead of time the backward kernel of a signature (no GPU needed)."""
+        _check(lib().es_body_prepare_backward(self._h, int(state_width), self.n_seqs, _widths_array(seq_widths)))
+
+    def plan_backward(self, shape: Sequence[int], axis: int, state_width: int = 0, seq_widths=None,
+                      reverse: bool = False, ptrs: Optional[Sequence[int]] = None) -> dict:
+        """Validate and plan a backward call without a GPU.  ``ptrs`` are
+        (initial, seq 0 .. seq n-1, states, grad_out, grad_initial, grad seq
+        0 .. n-1); by default 16-byte aligned, non-overlapping stand-ins."""
+        n = self.n_seqs
+        rank = len(shape)
+        shp = (ctypes.c_int64 * max(rank, 1))(*shape)
+        if ptrs is None:
+            ptrs = [(k + 1) << 44 for k in range(2 * n + 4)]
+        seqs = (ctypes.c_void_p * n)(*ptrs[1:n + 1])
+        gseqs = (ctypes.c_void_p * n)(*ptrs[n + 4:2 * n + 4])
+        info = PlanInfo()
+        _check(lib().es_plan_body_backward_f32(self._h, ptrs[0], seqs, n, shp, rank, int(axis), int(state_width),
+                                               _widths_array(seq_widths), int(bool(reverse)), ptrs[n + 1],
+                                               ptrs[n + 2], ptrs[n + 3], gseqs, ctypes.byref(info)))
+        return {"O": info.O, "T": info.T, "J": info.J, "W": info.W,
+                "seq_width": tuple(info.seq_width[k] for k in range(n)), "elements": info.elements,
+                "path": PATHS[info.path], "reverse": bool(info.reverse)}
+
+    def scan_backward(self, initial, seqs, states, grad_out, axis: int = 0, state_axis: bool = False,
+                      reverse: bool = False, grads=None, stream=None):
+        """Gradients of sum(grad_out * scan(...)) on CUDA tensors.
+
+        ``states`` is the forward output.  Returns (grad_initial, [grad seq
+        k]) shaped like initial and the sequences; ``grads`` may supply those
+        buffers.  Asynchronous on ``stream``."""
+        import torch
+        seqs = list(seqs)
+        _require_cuda_f32(initial, "initial")
+        for k, t in enumerate(seqs):
+            _require_cuda_f32(t, "sequence %d" % k)
+        _require_cuda_f32(states, "states")
+        _require_cuda_f32(grad_out, "grad_out")
+        shape = list(states.shape)
+        if list(grad_out.shape) != shape:
+            raise EsError(1, "grad_out shape %s does not match the states %s" % (list(grad_out.shape), shape))
+        if grads is None:
+            grads = (torch.empty_like(initial), [torch.empty_like(t) for t in seqs])
+        g_init, g_seqs = grads
+        for t in [g_init] + list(g_seqs):
+            _require_cuda_f32(t, "gradient buffer")
+        n = len(seqs)
+        rank = len(shape)
+        shp = (ctypes.c_int64 * max(rank, 1))(*shape)
+        state_width = shape[-1] if state_axis else 0
+        sw = _widths_array([int(t.shape[-1]) for t in seqs]) if state_axis else None
+        sp = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in seqs])
+        gp = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in g_seqs])
+        if stream is None:
+            stream = torch.cuda.current_stream(states.device)
+        handle = stream if isinstance(stream, int) else stream.cuda_stream
+        _check(lib().es_scan_body_backward_f32(self._h, initial.data_ptr(), sp, n, shp, rank, int(axis),
+                                               int(state_width), sw, int(bool(reverse)), states.data_ptr(),
+                                               grad_out.data_ptr(), g_init.data_ptr(), gp, handle))
+        return g_init, list(g_seqs)
 
     def prepare(self, state_width: int = 0, seq_widths=None, path="auto") -> None:
         """Compile ahead of time the kernels a signature may use (no GPU needed)."""

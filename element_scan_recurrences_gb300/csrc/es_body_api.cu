@@ -27,8 +27,9 @@
 struct es_body_program {
     std::unique_ptr<es::body::Program> prog;
     std::mutex mu;
-    // generated functor per (state width, vector state, wide mask)
-    std::map<std::tuple<int, bool, unsigned>, std::string> functors;
+    // generated functor per (state width, vector state, wide mask, with the
+    // vector-Jacobian product)
+    std::map<std::tuple<int, bool, unsigned, bool>, std::string> functors;
 };
 
 namespace es {
@@ -39,13 +40,14 @@ using body::Error;
 es_status body_fail(const Error& e) { return api_fail(ES_E_BODY, "%s: %s", e.code.c_str(), e.msg.c_str()); }
 
 // the functor for a signature, generated once per program
-es_status functor_for(es_body_program* b, int W, bool vector, unsigned wide_mask, std::string* out) {
+es_status functor_for(es_body_program* b, int W, bool vector, unsigned wide_mask, std::string* out,
+                      bool with_vjp = false) {
     std::lock_guard<std::mutex> lock(b->mu);
-    const auto key = std::make_tuple(W, vector, wide_mask);
+    const auto key = std::make_tuple(W, vector, wide_mask, with_vjp);
     auto it = b->functors.find(key);
     if (it == b->functors.end()) {
         try {
-            it = b->functors.emplace(key, b->prog->generate(W, vector, wide_mask)).first;
+            it = b->functors.emplace(key, b->prog->generate(W, vector, wide_mask, with_vjp)).first;
         } catch (const Error& e) {
             return body_fail(e);
         }
@@ -292,7 +294,7 @@ bool launch_body_lane(const BodyLaunch& L, std::string* err) {
 
 // the functor of a signature given by widths (no shapes)
 es_status signature_functor(const char* fn, es_body_t body, int state_width, int n_seqs, const int64_t* seq_widths,
-                            std::string* functor, int* W_out) {
+                            std::string* functor, int* W_out, bool with_vjp = false) {
     if (body == nullptr || !body->prog) return api_fail(ES_E_ARG, "%s: null body program", fn);
     if (n_seqs != body->prog->n_seqs())
         return api_fail(ES_E_BODY, "arity: the body takes %d sequence(s), not %d", body->prog->n_seqs(), n_seqs);
@@ -308,7 +310,7 @@ es_status signature_functor(const char* fn, es_body_t body, int state_width, int
         if (w == W) mask |= 1u << k;
     }
     *W_out = W;
-    return functor_for(body, W, state_width != 0, mask, functor);
+    return functor_for(body, W, state_width != 0, mask, functor, with_vjp);
 }
 
 bool launch_body_time(const BodyLaunch& L, std::string* err) {
@@ -398,6 +400,100 @@ bool launch_body_vec(const BodyLaunch& L, std::string* err) {
     return jit_launch(k, static_cast<unsigned>(ctas), 32 + 128 / vec_values(W), smem, L.stream, args, err);
 }
 
+// ---------------------------------------------------------------------------
+// backward ("Precision and gradients"): the body's vector-Jacobian product
+// scanned in the opposite trip order, one thread per lane
+
+KernelText generic_bwd_text(const std::string& functor, int W) {
+    return {"#include \"skel_generic_bwd.cuh\"\n" + functor,
+            "&es::k_body_generic_bwd<EsBody, " + std::to_string(W) + ">"};
+}
+
+struct BodyBwdCall {
+    BodyCall C;           // the forward call's plan (shapes, signature)
+    std::string functor;  // the functor with its `vjp`
+};
+
+// The forward plan for the shapes (the saved states have the output shape),
+// then the gradient buffers: present, 4-byte aligned, disjoint from every
+// input and from each other.
+es_status plan_body_backward(es_body_t body, const float* initial, const float* const* seqs, int n_seqs,
+                             const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
+                             int reverse, const float* states, const float* grad_out, const float* grad_initial,
+                             float* const* grad_seqs, BodyBwdCall* B) {
+    static const char* const kFn = "es_scan_body_backward_f32";
+    // the forced-path check comes after the plan (any forward path is fine)
+    BodyCall& C = B->C;
+    es_status st = plan_body(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths, reverse, states,
+                             &C);
+    if (st != ES_OK) return st;
+    if ((st = functor_for(body, static_cast<int>(C.S.W), C.vector, C.wide_mask, &B->functor, true)) != ES_OK)
+        return st;
+    const int forced = api_path_override();
+    if (forced != ES_PATH_AUTO && forced != ES_PATH_GENERIC)
+        return api_fail(ES_E_UNSUPPORTED, "%s: the forced kernel path %d cannot serve this call", kFn, forced);
+    if (C.S.empty) {
+        C.path = ES_PATH_EMPTY;
+        return ES_OK;
+    }
+    if (grad_out == nullptr || grad_initial == nullptr || grad_seqs == nullptr)
+        return api_fail(ES_E_ARG, "%s: null gradient pointer", kFn);
+    for (int k = 0; k < n_seqs; ++k)
+        if (grad_seqs[k] == nullptr) return api_fail(ES_E_ARG, "%s: null gradient pointer", kFn);
+    // every buffer of the call: inputs first, then the written gradients
+    const int nb = 2 * n_seqs + 4;
+    std::vector<const void*> ptr(nb);
+    std::vector<int64_t> cnt(nb);
+    std::vector<std::string> nm(nb);
+    ptr[0] = initial, cnt[0] = C.S.n_init, nm[0] = "initial";
+    for (int k = 0; k < n_seqs; ++k) ptr[1 + k] = seqs[k], cnt[1 + k] = C.S.n_seq[k], nm[1 + k] = "seq " + std::to_string(k);
+    ptr[n_seqs + 1] = states, cnt[n_seqs + 1] = C.S.n_out, nm[n_seqs + 1] = "states";
+    ptr[n_seqs + 2] = grad_out, cnt[n_seqs + 2] = C.S.n_out, nm[n_seqs + 2] = "grad_out";
+    ptr[n_seqs + 3] = grad_initial, cnt[n_seqs + 3] = C.S.n_init, nm[n_seqs + 3] = "grad_initial";
+    for (int k = 0; k < n_seqs; ++k)
+        ptr[n_seqs + 4 + k] = grad_seqs[k], cnt[n_seqs + 4 + k] = C.S.n_seq[k], nm[n_seqs + 4 + k] = "grad seq " + std::to_string(k);
+    for (int k = 0; k < nb; ++k)
+        if (reinterpret_cast<uintptr_t>(ptr[k]) % 4 != 0)
+            return api_fail(ES_E_ARG, "%s: `%s` is not 4-byte aligned", kFn, nm[k].c_str());
+    for (int k = n_seqs + 3; k < nb; ++k) {
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(ptr[k]), hi = lo + static_cast<uintptr_t>(cnt[k]) * 4;
+        for (int q = 0; q < nb; ++q) {
+            if (q == k) continue;
+            const uintptr_t l2 = reinterpret_cast<uintptr_t>(ptr[q]), h2 = l2 + static_cast<uintptr_t>(cnt[q]) * 4;
+            if (lo < h2 && l2 < hi)
+                return api_fail(ES_E_ARG, "%s: `%s` overlaps `%s`", kFn, nm[k].c_str(), nm[q].c_str());
+        }
+    }
+    C.path = ES_PATH_GENERIC;
+    return ES_OK;
+}
+
+bool launch_body_generic_bwd(const BodyBwdCall& B, const float* init, const float* const* seqs, const float* states,
+                             const float* gout, float* ginit, float* const* gseqs, cudaStream_t stream,
+                             std::string* err) {
+    const BodyCall& C = B.C;
+    JitKernel k;
+    const KernelText kt = generic_bwd_text(B.functor, static_cast<int>(C.S.W));
+    if (!jit_kernel(kt.source, kt.name, &k, err)) return false;
+    SeqPtrs sp{};
+    GradPtrs gp{};
+    for (int q = 0; q < C.S.n_seqs; ++q) {
+        sp.p[q] = seqs[q];
+        gp.p[q] = gseqs[q];
+    }
+    const int64_t lanes = C.S.O * C.S.J;
+    const int threads = 128;
+    const int64_t blocks = (lanes + threads - 1) / threads;
+    if (blocks > 0x7fffffffLL) {
+        *err = "too many lanes for one launch";
+        return false;
+    }
+    int64_t O = C.S.O, T = C.S.T, J = C.S.J;
+    int reverse = C.reverse;
+    void* args[] = {&sp, &init, &states, &gout, &gp, &ginit, &O, &T, &J, &reverse};
+    return jit_launch(k, static_cast<unsigned>(blocks), threads, 0, stream, args, err);
+}
+
 void fill_info(const BodyCall& C, es_plan_info* info) {
     if (info == nullptr) return;
     std::memset(info, 0, sizeof(*info));
@@ -474,6 +570,69 @@ es_status es_body_prepare(es_body_t body, int state_width, int n_seqs, const int
         std::string err;
         if (!es::jit_compile(kt.source, kt.name, &err)) return es::api_fail(ES_E_CUDA, "es_body_prepare: %s", err.c_str());
     }
+    return ES_OK;
+}
+
+es_status es_body_prepare_backward(es_body_t body, int state_width, int n_seqs, const int64_t* seq_widths) {
+    std::string functor;
+    int W = 1;
+    es_status st = es::signature_functor("es_body_prepare_backward", body, state_width, n_seqs, seq_widths, &functor,
+                                         &W, true);
+    if (st != ES_OK) return st;
+    const es::KernelText kt = es::generic_bwd_text(functor, W);
+    std::string err;
+    if (!es::jit_compile(kt.source, kt.name, &err))
+        return es::api_fail(ES_E_CUDA, "es_body_prepare_backward: %s", err.c_str());
+    return ES_OK;
+}
+
+es_status es_body_source_backward(es_body_t body, int state_width, int n_seqs, const int64_t* seq_widths, char* buf,
+                                  size_t cap, size_t* needed) {
+    std::string src;
+    int W = 1;
+    es_status st = es::signature_functor("es_body_source_backward", body, state_width, n_seqs, seq_widths, &src, &W,
+                                         true);
+    if (st != ES_OK) return st;
+    if (needed != nullptr) *needed = src.size();
+    if (buf != nullptr && cap > 0) {
+        const size_t n = src.size() < cap - 1 ? src.size() : cap - 1;
+        std::memcpy(buf, src.data(), n);
+        buf[n] = '\0';
+    }
+    return ES_OK;
+}
+
+es_status es_plan_body_backward_f32(es_body_t body, const float* initial, const float* const* seqs, int n_seqs,
+                                    const int64_t* shape, int rank, int axis, int state_width,
+                                    const int64_t* seq_widths, int reverse, const float* states,
+                                    const float* grad_out, const float* grad_initial, float* const* grad_seqs,
+                                    es_plan_info* info) {
+    es::BodyBwdCall B{};
+    es_status st = es::plan_body_backward(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths,
+                                          reverse, states, grad_out, grad_initial, grad_seqs, &B);
+    if (st != ES_OK) return st;
+    es::fill_info(B.C, info);
+    return ES_OK;
+}
+
+es_status es_scan_body_backward_f32(es_body_t body, const float* initial, const float* const* seqs, int n_seqs,
+                                    const int64_t* shape, int rank, int axis, int state_width,
+                                    const int64_t* seq_widths, int reverse, const float* states,
+                                    const float* grad_out, float* grad_initial, float* const* grad_seqs,
+                                    es_stream_t stream) {
+    es::BodyBwdCall B{};
+    es_status st = es::plan_body_backward(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths,
+                                          reverse, states, grad_out, grad_initial, grad_seqs, &B);
+    if (st != ES_OK) return st;
+    if (B.C.path == ES_PATH_EMPTY) return ES_OK;
+    int dev = 0;
+    es::DeviceState* ds = nullptr;
+    if ((st = es::api_device(&dev, &ds)) != ES_OK) return st;
+    std::string err;
+    if (!es::launch_body_generic_bwd(B, initial, seqs, states, grad_out, grad_initial, grad_seqs,
+                                     reinterpret_cast<cudaStream_t>(stream), &err))
+        return es::api_fail(ES_E_CUDA, "es_scan_body_backward_f32: %s", err.c_str());
+    es::count_launch();
     return ES_OK;
 }
 

@@ -31,6 +31,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <set>
 #include <sstream>
 
 namespace es {
@@ -146,6 +147,15 @@ struct Val {
     std::string name;     // tensor: an expression naming it (array name if wide)
     bool is_bool = false; // tensor dtype: bool or f32
     bool wide = false;    // tensor width: the state's W (array of E) or one
+    bool diff = false;    // depends on the state or a sequence through differentiable operations
+};
+
+// One differentiable operation of the trace (the tape the VJP sweeps back).
+struct Node {
+    std::string op;
+    Val out;
+    std::vector<Val> args;
+    Val mask;             // `where`'s condition
 };
 
 Val number(double v) {
@@ -212,12 +222,20 @@ public:
         return t;
     }
 
-    Val emit(bool is_bool, bool wide, const std::string& expr) {
+    // A statement computing a new value.  `op` names a differentiable
+    // operation of `args` (recorded on the tape when one of them is
+    // differentiable); without it the value has no gradient.
+    Val emit(bool is_bool, bool wide, const std::string& expr, const char* op = nullptr,
+             const std::vector<Val>& args = {}, const Val& mask = Val()) {
         Val r;
         r.kind = Val::kTensor;
         r.is_bool = is_bool;
         r.wide = wide;
         r.name = "v" + std::to_string(next_++);
+        if (op != nullptr && !is_bool) {
+            for (const Val& a : args) r.diff = r.diff || a.diff;
+            if (r.diff) tape.push_back(Node{op, r, args, mask});
+        }
         const char* type = is_bool ? "bool" : "float";
         if (wide) {
             code += std::string("        ") + type + " " + r.name + "[E];\n#pragma unroll\n        for (int e = 0; e < E; ++e) " +
@@ -229,6 +247,8 @@ public:
     }
 
     int W() const { return W_; }
+
+    std::vector<Node> tape;
 
 private:
     Val reduce(const std::string& op, const std::vector<Val>& pos, const std::map<std::string, Form>& kws);
@@ -251,6 +271,14 @@ template <size_t N>
 const char* lookup(const char* (&table)[N][2], const std::string& key) {
     for (size_t i = 0; i < N; ++i)
         if (key == table[i][0]) return table[i][1];
+    return nullptr;
+}
+
+// the table's own spelling of an operation (a name that outlives the call)
+template <size_t N>
+const char* lookup_name(const char* (&table)[N][2], const std::string& key) {
+    for (size_t i = 0; i < N; ++i)
+        if (key == table[i][0]) return table[i][0];
     return nullptr;
 }
 
@@ -298,7 +326,7 @@ Val Tracer::reduce(const std::string& op, const std::vector<Val>& pos, const std
     // a one-value vector (or an empty axis list) reduces to itself
     if (empty_axes || !t.wide) return t;
     return emit(false, false, std::string(op == "sum" ? "es::group_sum" : "es::group_max") + "<E, G>(" + t.name +
-                                  ", mask)");
+                                  ", mask)", op == "sum" ? "sum" : "rmax", {t});
 }
 
 Val Tracer::eval(const Form& f, const Env& env) {
@@ -372,7 +400,7 @@ Val Tracer::eval(const Form& f, const Env& env) {
         if (v.kind != Val::kTensor) return v;
         const auto& dims = args[1].items;
         if (head == "broadcast-to" && !dims.empty() && !v.wide && vector_ && dims.back().num == W_)
-            return emit(v.is_bool, true, ref(v));
+            return emit(v.is_bool, true, ref(v), "bcast", {v});
         return v;
     }
 
@@ -393,8 +421,8 @@ Val Tracer::eval(const Form& f, const Env& env) {
                 return v;
             }
             const Val t = f32(v, head);
-            if (head == "-") return emit(false, t.wide, "(-" + ref(t) + ")");
-            if (head == "/") return emit(false, t.wide, "__fdiv_rn(1.0f, " + ref(t) + ")");
+            if (head == "-") return emit(false, t.wide, "(-" + ref(t) + ")", "neg", {t});
+            if (head == "/") return emit(false, t.wide, "__fdiv_rn(1.0f, " + ref(t) + ")", "div", {tensor(number(1.0)), t});
             return t;
         }
         Val acc = vals[0];
@@ -404,7 +432,8 @@ Val Tracer::eval(const Form& f, const Env& env) {
                 acc = number(number_arith(head, acc.num, v.num));
             } else {
                 const Val a = f32(acc, head), b = f32(v, head);
-                acc = emit(false, a.wide || b.wide, std::string(fn) + "(" + ref(a) + ", " + ref(b) + ")");
+                const char* nm = head == "+" ? "add" : head == "-" ? "sub" : head == "*" ? "mul" : "div";
+                acc = emit(false, a.wide || b.wide, std::string(fn) + "(" + ref(a) + ", " + ref(b) + ")", nm, {a, b});
             }
         }
         return acc;
@@ -435,12 +464,13 @@ Val Tracer::eval(const Form& f, const Env& env) {
         const Val m = boolean(vals[0], "where mask");
         const Val a = tensor(vals[1]), b = tensor(vals[2]);
         if (a.is_bool != b.is_bool) fail("E-DIM-002", "where: branches of different dtypes");
-        return emit(a.is_bool, m.wide || a.wide || b.wide, "(" + ref(m) + " ? " + ref(a) + " : " + ref(b) + ")");
+        return emit(a.is_bool, m.wide || a.wide || b.wide, "(" + ref(m) + " ? " + ref(a) + " : " + ref(b) + ")",
+                    "where", {a, b}, m);
     }
     if (head == "neg") {
         arity(1, 1);
         const Val a = f32(vals[0], head);
-        return emit(false, a.wide, "(-" + ref(a) + ")");
+        return emit(false, a.wide, "(-" + ref(a) + ")", "neg", {a});
     }
     if (const char* fn = lookup(kUnary, head)) {
         arity(1, 1);
@@ -450,17 +480,176 @@ Val Tracer::eval(const Form& f, const Env& env) {
             return number(head == "sqrt" ? std::sqrt(x) : head == "exp" ? std::exp(x) : std::log(x));
         }
         const Val a = f32(vals[0], head);
-        return emit(false, a.wide, std::string(fn) + "(" + ref(a) + ")");
+        return emit(false, a.wide, std::string(fn) + "(" + ref(a) + ")", lookup_name(kUnary, head), {a});
     }
     if (const char* fn = lookup(kBinaryFn, head)) {
         arity(2, 2);
         if (head == "pow" && vals[0].kind == Val::kNumber && vals[1].kind == Val::kNumber)
             return number(std::pow(vals[0].num, vals[1].num));
         const Val a = f32(vals[0], head), b = f32(vals[1], head);
-        return emit(false, a.wide || b.wide, std::string(fn) + "(" + ref(a) + ", " + ref(b) + ")");
+        return emit(false, a.wide || b.wide, std::string(fn) + "(" + ref(a) + ", " + ref(b) + ")",
+                    lookup_name(kBinaryFn, head), {a, b});
     }
     fail("op", "`" + head + "` is not an operation a body may use");
 }
+
+// ---------------------------------------------------------------------------
+// the vector-Jacobian product: the tape swept backwards
+//
+// Derivatives ("Precision and gradients": comparisons and casts have none,
+// `where` follows the selected branch, the usual tie rules apply), each an
+// f32 expression rounded step by step:
+//   a+b: (g, g)   a-b: (g, -g)   a*b: (g*b, g*a)   a/b: (g/b, -(g*q)/b), q = a/b
+//   -a: -g   |a|: g*sign(a) (0 at 0)   sqrt: (g*0.5)/out   exp: g*out
+//   log: g/a   tanh: g*(1-out*out)   sin: g*cos(a)   cos: -(g*sin(a))
+//   rsqrt: g*((out*out*out)*-0.5)   acos: -(g/sqrt(1-a*a))   asin: g/sqrt(1-a*a)
+//   atan2(y, x): ((g*x)/(x*x+y*y), -(g*y)/(x*x+y*y))
+//   pow(a, b): (g*(b*pow(a, b-1)), 0 if out == 0 else g*(out*log(a)))
+//   maximum / minimum: the larger (smaller) operand takes g, a tie or NaN
+//   splits g*0.5 each; where: g to the selected branch; sum: g to every
+//   value; max: g/count to each of its count equal maxima.
+// Contributions reach an operand in reverse tape order, a node's operands in
+// argument order, the first assigned and later ones added; a width-one
+// operand of a wide operation receives the sum of the wide contribution over
+// the state (this thread's values in order, then the lane's threads).
+class Adjoint {
+public:
+    explicit Adjoint(const Tracer& tr) : tr_(tr) {}
+
+    std::string code;
+
+    static std::string gname(const Val& v) {
+        std::string g = "g_";
+        for (char ch : v.name)
+            if (ch != '[' && ch != ']') g += ch;
+        return g;
+    }
+
+    bool has(const Val& v) const { return assigned_.count(gname(v)) != 0; }
+
+    // the seed: the cotangent of the body's result is the state's cotangent
+    // (a width-one result, spread over the state, takes its sum)
+    void seed(const Val& r) {
+        if (r.kind != Val::kTensor || !r.diff) return;
+        contribute(r, "lam[e]", true);
+    }
+
+    void sweep() {
+        const std::vector<Node>& tape = tr_.tape;
+        for (auto it = tape.rbegin(); it != tape.rend(); ++it) {
+            const Node& n = *it;
+            if (!has(n.out)) continue;
+            const bool w = n.out.wide;
+            const std::string G = w ? gname(n.out) + "[e]" : gname(n.out);
+            const std::string OUT = tr_.ref(n.out);
+            const Val& a = n.args[0];
+            const std::string A = tr_.ref(a);
+            const Val* b = n.args.size() > 1 ? &n.args[1] : nullptr;
+            const std::string B = b ? tr_.ref(*b) : "";
+            const std::string& op = n.op;
+            auto half = "__fmul_rn(" + G + ", 0.5f)";
+            if (op == "add") {
+                contribute(a, G, w);
+                contribute(*b, G, w);
+            } else if (op == "sub") {
+                contribute(a, G, w);
+                contribute(*b, "(-" + G + ")", w);
+            } else if (op == "mul") {
+                contribute(a, "__fmul_rn(" + G + ", " + B + ")", w);
+                contribute(*b, "__fmul_rn(" + G + ", " + A + ")", w);
+            } else if (op == "div") {
+                contribute(a, "__fdiv_rn(" + G + ", " + B + ")", w);
+                contribute(*b, "(-__fdiv_rn(__fmul_rn(" + G + ", " + OUT + "), " + B + "))", w);
+            } else if (op == "neg") {
+                contribute(a, "(-" + G + ")", w);
+            } else if (op == "abs") {
+                contribute(a, "(" + A + " > 0.0f ? " + G + " : (" + A + " < 0.0f ? (-" + G + ") : 0.0f))", w);
+            } else if (op == "sqrt") {
+                contribute(a, "__fdiv_rn(" + half + ", " + OUT + ")", w);
+            } else if (op == "exp") {
+                contribute(a, "__fmul_rn(" + G + ", " + OUT + ")", w);
+            } else if (op == "log") {
+                contribute(a, "__fdiv_rn(" + G + ", " + A + ")", w);
+            } else if (op == "tanh") {
+                contribute(a, "__fmul_rn(" + G + ", __fsub_rn(1.0f, __fmul_rn(" + OUT + ", " + OUT + ")))", w);
+            } else if (op == "sin") {
+                contribute(a, "__fmul_rn(" + G + ", cosf(" + A + "))", w);
+            } else if (op == "cos") {
+                contribute(a, "(-__fmul_rn(" + G + ", sinf(" + A + ")))", w);
+            } else if (op == "rsqrt") {
+                contribute(a, "__fmul_rn(" + G + ", __fmul_rn(__fmul_rn(__fmul_rn(" + OUT + ", " + OUT + "), " + OUT +
+                                  "), -0.5f))", w);
+            } else if (op == "acos" || op == "asin") {
+                const std::string q = "__fdiv_rn(" + G + ", __fsqrt_rn(__fsub_rn(1.0f, __fmul_rn(" + A + ", " + A + "))))";
+                contribute(a, op == "acos" ? "(-" + q + ")" : q, w);
+            } else if (op == "atan2") {
+                const std::string den = "__fadd_rn(__fmul_rn(" + B + ", " + B + "), __fmul_rn(" + A + ", " + A + "))";
+                contribute(a, "__fdiv_rn(__fmul_rn(" + G + ", " + B + "), " + den + ")", w);
+                contribute(*b, "(-__fdiv_rn(__fmul_rn(" + G + ", " + A + "), " + den + "))", w);
+            } else if (op == "pow") {
+                contribute(a, "__fmul_rn(" + G + ", __fmul_rn(" + B + ", powf(" + A + ", __fsub_rn(" + B + ", 1.0f))))", w);
+                contribute(*b, "(" + OUT + " == 0.0f ? 0.0f : __fmul_rn(" + G + ", __fmul_rn(" + OUT + ", logf(" + A +
+                                   "))))", w);
+            } else if (op == "maximum" || op == "minimum") {
+                const char* cmp = op == "maximum" ? " > " : " < ";
+                contribute(a, "(" + A + cmp + B + " ? " + G + " : (" + B + cmp + A + " ? 0.0f : " + half + "))", w);
+                contribute(*b, "(" + B + cmp + A + " ? " + G + " : (" + A + cmp + B + " ? 0.0f : " + half + "))", w);
+            } else if (op == "where") {
+                const std::string M = tr_.ref(n.mask);
+                contribute(a, "(" + M + " ? " + G + " : 0.0f)", w);
+                contribute(*b, "(" + M + " ? 0.0f : " + G + ")", w);
+            } else if (op == "sum") {
+                contribute(a, G, true);     // every value of the reduced vector
+            } else if (op == "rmax") {
+                const std::string cnt = "cnt" + std::to_string(tmp_++);
+                code += "        float " + cnt + "_v[E];\n#pragma unroll\n        for (int e = 0; e < E; ++e) " + cnt +
+                        "_v[e] = (" + A + " == " + OUT + ") ? 1.0f : 0.0f;\n        const float " + cnt +
+                        " = es::group_sum<E, G>(" + cnt + "_v, mask);\n";
+                contribute(a, "(" + A + " == " + OUT + " ? __fdiv_rn(" + G + ", " + cnt + ") : 0.0f)", true);
+            } else if (op == "bcast") {
+                contribute(a, G, true);
+            }
+        }
+    }
+
+    // the gradient of a leaf, or zero
+    std::string grad_or_zero(const Val& v) const {
+        if (!has(v)) return "0.0f";
+        return v.wide ? gname(v) + "[e]" : gname(v);
+    }
+
+private:
+    // add `expr` (wide: an expression of e) to the gradient of `target`
+    void contribute(const Val& target, const std::string& expr, bool expr_wide) {
+        if (target.kind != Val::kTensor || !target.diff) return;
+        const std::string gv = gname(target);
+        std::string value = expr;
+        bool value_wide = expr_wide;
+        if (expr_wide && !target.wide) {
+            // a width-one operand of a wide operation: the sum over the state
+            const std::string c = "c" + std::to_string(tmp_++);
+            code += "        float " + c + "[E];\n#pragma unroll\n        for (int e = 0; e < E; ++e) " + c + "[e] = " +
+                    expr + ";\n        const float " + c + "_s = es::group_sum<E, G>(" + c + ", mask);\n";
+            value = c + "_s";
+            value_wide = false;
+        }
+        const bool first = assigned_.insert(gv).second;
+        if (target.wide) {
+            // a wide target takes a wide value, or a width-one one on every value
+            const std::string rhs = first ? value : "__fadd_rn(" + gv + "[e], " + value + ")";
+            if (first) code += "        float " + gv + "[E];\n";
+            code += "#pragma unroll\n        for (int e = 0; e < E; ++e) " + gv + "[e] = " + rhs + ";\n";
+        } else {
+            (void)value_wide;
+            if (first) code += "        float " + gv + " = " + value + ";\n";
+            else code += "        " + gv + " = __fadd_rn(" + gv + ", " + value + ");\n";
+        }
+    }
+
+    const Tracer& tr_;
+    std::set<std::string> assigned_;
+    int tmp_ = 0;
+};
 
 std::string comment_safe(const std::string& s) {
     std::string r;
@@ -495,7 +684,7 @@ std::unique_ptr<Program> Program::parse(const std::string& text) {
     return p;
 }
 
-std::string Program::generate(int W, bool vector, unsigned wide_mask) const {
+std::string Program::generate(int W, bool vector, unsigned wide_mask, bool with_vjp) const {
     const int ns = n_seqs();
     Tracer tr(W, vector);
     Env env;
@@ -503,14 +692,18 @@ std::string Program::generate(int W, bool vector, unsigned wide_mask) const {
     h.kind = Val::kTensor;
     h.name = "h";
     h.wide = true;
+    h.diff = true;
     env[params_[0]] = h;
     int nw = 0, nn = 0;
+    std::vector<Val> leaves;
     for (int k = 0; k < ns; ++k) {
         Val s;
         s.kind = Val::kTensor;
         s.wide = (wide_mask >> k) & 1u;
+        s.diff = true;
         s.name = s.wide ? "sw[" + std::to_string(nw++) + "]" : "sn[" + std::to_string(nn++) + "]";
         env[params_[k + 1]] = s;
+        leaves.push_back(s);
     }
     Val r;
     for (const Form& e : exprs_) r = tr.eval(e, env);
@@ -539,7 +732,36 @@ std::string Program::generate(int W, bool vector, unsigned wide_mask) const {
     o << "        (void)h;\n        (void)sw;\n        (void)sn;\n        (void)mask;\n";
     o << tr.code;
     o << "#pragma unroll\n        for (int e = 0; e < E; ++e) r[e] = " << tr.ref(r) << ";\n";
-    o << "    }\n};\n";
+    o << "    }\n";
+    if (with_vjp) {
+        // the trip's vector-Jacobian product: the body again from the state
+        // before the trip (`h`), then the tape backwards from the cotangent
+        // `lam` of the state after it; dp is the previous state's cotangent,
+        // dsw / dsn the sequences' (a width-one one summed over the state)
+        Adjoint adj(tr);
+        adj.seed(r);
+        adj.sweep();
+        o << "    template <int E, int G>\n";
+        o << "    __device__ __forceinline__ static void vjp(float (&dp)[E], float (&dsw)[kSW][E], float (&dsn)[kSN],\n"
+             "                                               const float (&lam)[E], const float (&h)[E],\n"
+             "                                               const float (&sw)[kSW][E], const float (&sn)[kSN],\n"
+             "                                               const unsigned mask) {\n";
+        o << "        (void)lam;\n        (void)h;\n        (void)sw;\n        (void)sn;\n        (void)mask;\n";
+        o << tr.code << adj.code;
+        o << "#pragma unroll\n        for (int e = 0; e < E; ++e) dp[e] = " << adj.grad_or_zero(h) << ";\n";
+        int qw = 0, qn = 0;
+        for (const Val& s : leaves) {
+            if (s.wide)
+                o << "#pragma unroll\n        for (int e = 0; e < E; ++e) dsw[" << qw++ << "][e] = " << adj.grad_or_zero(s)
+                  << ";\n";
+            else
+                o << "        dsn[" << qn++ << "] = " << adj.grad_or_zero(s) << ";\n";
+        }
+        if (nw == 0) o << "#pragma unroll\n        for (int e = 0; e < E; ++e) dsw[0][e] = 0.0f;\n";
+        if (nn == 0) o << "        dsn[0] = 0.0f;\n";
+        o << "    }\n";
+    }
+    o << "};\n";
     return o.str();
 }
 

@@ -37,8 +37,9 @@ public:
 
     // The functor for one call signature: state width W (1 for a scalar
     // state), whether the state is a vector (`:state-axis`), and which
-    // sequences are as wide as the state (bit k of wide_mask).  Throws Error.
-    std::string generate(int W, bool vector, unsigned wide_mask) const;
+    // sequences are as wide as the state (bit k of wide_mask).  With
+    // `with_vjp` it also has the trip's vector-Jacobian product.  Throws Error.
+    std::string generate(int W, bool vector, unsigned wide_mask, bool with_vjp = false) const;
 
     // Throws Error when the text is not a body.
     static std::unique_ptr<Program> parse(const std::string& text);

@@ -37,6 +37,11 @@ struct SeqPtrs {
     const float* p[kMaxBodySeqs];
 };
 
+// gradient outputs of a backward launch, one per sequence
+struct GradPtrs {
+    float* p[kMaxBodySeqs];
+};
+
 // one TMA descriptor per sequence, passed by value (__grid_constant__)
 template <int NS>
 struct TmaMaps {

@@ -250,6 +250,71 @@ es_status es_body_prepare(es_body_t body, int state_width, int n_seqs, const int
 uint64_t es_body_compile_count(void);
 
 /*
+ * es_scan_body_backward_f32 -- gradients of a body-program scan
+ * ("Nonlinear element scans", "Precision and gradients": gradients flow to
+ * `initial` and to every sequence; the gradient of a scan is another element
+ * scan over the same lanes in the opposite trip order that applies the
+ * body's vector-Jacobian product once a trip; comparisons and casts carry no
+ * derivative, `where` passes it to the selected branch, and ties of
+ * maximum / minimum and of the reduction `max` split it evenly).
+ *
+ * The VJP is derived from the body at compile time by reverse-mode
+ * differentiation of its operations.  Per trip, with p the state before it
+ * and lam the state's cotangent (the carried one plus grad_out of the trip),
+ * the body is evaluated again at p, then its operations are swept backwards:
+ * each one's derivative is formed in f32 with every operation rounded, the
+ * contributions to a value are added in the reverse order of the operations
+ * (a node's operands in argument order), and a width-one sequence, or any
+ * width-one value a wide operation used, receives the sum of its wide
+ * contribution over w = 0..W-1.  The rules per operation:
+ *   a+b (g, g); a-b (g, -g); a*b (g*b, g*a); a/b (g/b, -(g*(a/b))/b);
+ *   -a -g; |a| g*sign(a), 0 at 0; sqrt (g*0.5)/out; exp g*out; log g/a;
+ *   tanh g*(1-out*out); sin g*cos(a); cos -(g*sin(a));
+ *   rsqrt g*((out*out*out)*-0.5); acos -(g/sqrt(1-a*a)); asin g/sqrt(1-a*a);
+ *   atan2(y, x) ((g*x)/(x*x+y*y), -(g*y)/(x*x+y*y));
+ *   pow(a, b) (g*(b*pow(a, b-1)), 0 if out == 0 else g*(out*log(a)));
+ *   maximum / minimum: the winner takes g, a tie (or NaN) gives g*0.5 each;
+ *   where: g to the selected branch; sum: g to every value; max: g/count to
+ *   each of its count equal maxima.
+ *
+ *   body .. reverse  exactly the arguments of the forward call.
+ *   states           device f32 of `shape`: the forward output.
+ *   grad_out         device f32 of `shape`: dL/d(states).
+ *   grad_initial     device f32, the shape of `initial` (written).
+ *   grad_seqs        HOST array of n_seqs DEVICE pointers, each with its
+ *                    sequence's shape (written).
+ * The written buffers may not overlap any input or each other (ES_E_ARG).
+ * The kernel is one thread per lane (ES_PATH_GENERIC), compiled with NVRTC
+ * on first use of a signature.  Asynchronous on `stream`; no allocation;
+ * statuses as for es_scan_body_f32.
+ */
+es_status es_scan_body_backward_f32(es_body_t body, const float *initial, const float *const *seqs,
+                                    int n_seqs, const int64_t *shape, int rank, int axis,
+                                    int state_width, const int64_t *seq_widths, int reverse,
+                                    const float *states, const float *grad_out,
+                                    float *grad_initial, float *const *grad_seqs,
+                                    es_stream_t stream);
+
+/* Plan of a body-program backward call (validation, body check and kernel
+ * path; no CUDA call, nothing compiled). */
+es_status es_plan_body_backward_f32(es_body_t body, const float *initial, const float *const *seqs,
+                                    int n_seqs, const int64_t *shape, int rank, int axis,
+                                    int state_width, const int64_t *seq_widths, int reverse,
+                                    const float *states, const float *grad_out,
+                                    const float *grad_initial, float *const *grad_seqs,
+                                    es_plan_info *info);
+
+/* The functor with its vector-Jacobian product `vjp` for a signature
+ * (arguments and output as in es_body_source).  No CUDA call. */
+es_status es_body_source_backward(es_body_t body, int state_width, int n_seqs,
+                                  const int64_t *seq_widths, char *buf, size_t cap, size_t *needed);
+
+/* Compile ahead of time the backward kernel of a signature (as in
+ * es_body_source).  No device needed. */
+es_status es_body_prepare_backward(es_body_t body, int state_width, int n_seqs,
+                                   const int64_t *seq_widths);
+
+/*
  * es_matrix_scan_f32 -- matrix-scan ("Tensor operations", the `matrix-scan`
  * row of the operations table and the section "matrix-scan"):
  *

@@ -1,0 +1,105 @@
+"""Body-program gradients through the C ABI without a GPU: every backward
+kernel compiles for sm_103a (NVRTC on the host), the plan validates the
+gradient buffers, and the generated vector-Jacobian product has the
+documented derivative rules."""
+import pytest
+
+import body_cases
+import body_grad_pins
+from element_scan_recurrences_gb300 import binding as es
+
+
+@pytest.mark.parametrize("cid", body_cases.CASE_IDS)
+def test_backward_kernel_compiles(cid):
+    c = body_cases.case(cid)
+    es.Body(c[1]).prepare_backward(c[2], c[3])
+
+
+def test_backward_kernels_compile_for_autograd_bodies():
+    for case in body_grad_pins.AUTOGRAD_CASES:
+        es.Body(case[0]).prepare_backward(case[2], case[3])
+
+
+def _ptrs(n):
+    return [(k + 1) << 44 for k in range(2 * n + 4)]
+
+
+def test_backward_plan():
+    b = es.Body("(lambda (h x a) (tanh (+ x (* a h))))")
+    p = b.plan_backward([3, 100, 64], 1)
+    assert p["path"] == "generic" and (p["O"], p["T"], p["J"], p["W"]) == (3, 100, 64, 1)
+    assert b.plan_backward([3, 100, 64], 1, reverse=True)["reverse"]
+    v = es.Body(body_cases.NORMCAP_TEXT)
+    p = v.plan_backward([2, 10, 5, 16], 1, 16, [16, 1])
+    assert p["path"] == "generic" and p["W"] == 16 and p["seq_width"] == (16, 1)
+    # no lanes: nothing to do
+    assert b.plan_backward([0, 100, 64], 1)["path"] == "empty"
+
+
+def test_backward_plan_rejects_bad_buffers():
+    b = es.Body("(lambda (h x a) (tanh (+ x (* a h))))")
+    shape = [3, 100, 64]
+    n = 2
+    for k in range(n + 3, 2 * n + 4):           # each written buffer onto `states`
+        ptrs = _ptrs(n)
+        ptrs[k] = ptrs[n + 1] + 64
+        with pytest.raises(es.EsError) as e:
+            b.plan_backward(shape, 1, ptrs=ptrs)
+        assert e.value.status == 3 and "overlaps" in str(e.value)
+    ptrs = _ptrs(n)
+    ptrs[n + 4] = ptrs[n + 5]                     # two gradients on one buffer
+    with pytest.raises(es.EsError) as e:
+        b.plan_backward(shape, 1, ptrs=ptrs)
+    assert e.value.status == 3
+    for k in (n + 2, n + 3, n + 4):               # grad_out, grad_initial, a gradient: null
+        ptrs = _ptrs(n)
+        ptrs[k] = 0
+        with pytest.raises(es.EsError) as e:
+            b.plan_backward(shape, 1, ptrs=ptrs)
+        assert e.value.status == 3
+    ptrs = _ptrs(n)
+    ptrs[n + 5] += 2                              # misaligned gradient
+    with pytest.raises(es.EsError) as e:
+        b.plan_backward(shape, 1, ptrs=ptrs)
+    assert e.value.status == 3 and "aligned" in str(e.value)
+
+
+def test_backward_forced_path():
+    b = es.Body("(lambda (h x a) (tanh (+ x (* a h))))")
+    es.set_path_override("lane_tma")
+    try:
+        with pytest.raises(es.EsError) as e:
+            b.plan_backward([3, 100, 64], 1)
+        assert e.value.status == 4
+    finally:
+        es.set_path_override("auto")
+    es.set_path_override("generic")
+    try:
+        assert b.plan_backward([3, 100, 64], 1)["path"] == "generic"
+    finally:
+        es.set_path_override("auto")
+
+
+def test_backward_rejects_what_the_forward_rejects():
+    with pytest.raises(es.EsError) as e:
+        es.Body("(lambda (h x) (+ h (sum x)))").plan_backward([2, 5, 3], 1)
+    assert e.value.status == 7 and "reduce" in str(e.value)
+
+
+def test_vjp_source_has_the_derivative_rules():
+    src = es.Body("(lambda (h x a) (tanh (+ x (* a h))))").source_backward()
+    assert "static void vjp(" in src
+    # tanh: g * (1 - out * out); the product's operands swap
+    assert "__fmul_rn(g_v2[e], __fsub_rn(1.0f, __fmul_rn(v2[e], v2[e])))" in src
+    assert "g_sw1[e] = __fmul_rn(g_v0[e], h[e])" in src and "g_h[e] = __fmul_rn(g_v0[e], sw[1][e])" in src
+    # a width-one gate of a vector state takes the sum over the state
+    src = es.Body("(lambda (h g) (* h g))").source_backward(8, [1])
+    assert "es::group_sum<E, G>(c0, mask)" in src and "dsn[0] = g_sn0" in src
+    # maximum: the winner takes g, a tie splits it
+    src = es.Body("(lambda (h x c) (maximum (- h c) x))").source_backward()
+    assert "__fmul_rn(g_v1[e], 0.5f)" in src
+    # comparisons and casts carry no gradient; a constant result none at all
+    src = es.Body("(lambda (h x) (+ h (cast (> x 0.5) :f32)))").source_backward()
+    assert "dsw[0][e] = 0.0f" in src
+    src = es.Body("(lambda (h x) 3.0)").source_backward()
+    assert "dp[e] = 0.0f" in src
