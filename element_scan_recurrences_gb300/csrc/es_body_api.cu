@@ -409,6 +409,45 @@ KernelText generic_bwd_text(const std::string& functor, int W) {
             "&es::k_body_generic_bwd<EsBody, " + std::to_string(W) + ">"};
 }
 
+KernelText lane_bwd_text(const std::string& functor, int LI, int TT) {
+    return {"#include \"skel_lane_bwd.cuh\"\n" + functor,
+            "&es::k_body_lane_bwd<EsBody, " + std::to_string(LI) + ", " + std::to_string(TT) + ">"};
+}
+
+// Trips per tile of the lanes-innermost backward: the sequences, the shifted
+// states and the output gradient of a tile sit in registers.  With at most
+// one CTA per SM (four consumer warps, one per SM sub-partition) the longer
+// tile of the forward's size pays off: the per-tile barrier and wait are
+// latency no other warp hides (GB300, 128 lanes x 128 rows x 16384 trips of
+// the MAXPLUS body: 0.70 -> 0.77 of HBM peak; with two CTAs per SM the
+// shorter tile stays ahead, 0.997 vs 0.948 on 64 x 1024 lanes).
+int lane_bwd_trips(int n_seqs, bool one_cta_per_sm) {
+    return one_cta_per_sm ? lane_trips(n_seqs) : lane_trips(n_seqs + 2);
+}
+
+// values of a lane's state per thread in the vector-state backward
+int vec_bwd_values(int) { return 1; }
+
+KernelText vec_bwd_text(const std::string& functor, int W, int TT) {
+    return {"#include \"skel_vec_bwd.cuh\"\n" + functor, "&es::k_body_vec_bwd<EsBody, " + std::to_string(W) + ", " +
+                                                               std::to_string(vec_bwd_values(W)) + ", " +
+                                                               std::to_string(TT) + ">"};
+}
+
+// bytes of one vector-state backward stage: every sequence's tile, the
+// shifted states' and the output gradient's
+int64_t vec_bwd_stage_bytes(int W, int TT, int n_wide, int n_narrow) {
+    return vec_stage_bytes(W, TT, n_wide + 2, n_narrow);
+}
+
+// trips per vector-state backward tile: 32 unless a stage would pass 32 KB
+// (two or three CTAs share an SM)
+int vec_bwd_trips(int W, int n_wide, int n_narrow) {
+    int TT = 32;
+    while (TT > 8 && vec_bwd_stage_bytes(W, TT, n_wide, n_narrow) > 32 * 1024) TT /= 2;
+    return TT;
+}
+
 struct BodyBwdCall {
     BodyCall C;           // the forward call's plan (shapes, signature)
     std::string functor;  // the functor with its `vjp`
@@ -430,7 +469,7 @@ es_status plan_body_backward(es_body_t body, const float* initial, const float* 
     if ((st = functor_for(body, static_cast<int>(C.S.W), C.vector, C.wide_mask, &B->functor, true)) != ES_OK)
         return st;
     const int forced = api_path_override();
-    if (forced != ES_PATH_AUTO && forced != ES_PATH_GENERIC)
+    if (forced != ES_PATH_AUTO && forced != ES_PATH_GENERIC && forced != ES_PATH_LANE_TMA && forced != ES_PATH_VEC_TMA)
         return api_fail(ES_E_UNSUPPORTED, "%s: the forced kernel path %d cannot serve this call", kFn, forced);
     if (C.S.empty) {
         C.path = ES_PATH_EMPTY;
@@ -464,8 +503,20 @@ es_status plan_body_backward(es_body_t body, const float* initial, const float* 
                 return api_fail(ES_E_ARG, "%s: `%s` overlaps `%s`", kFn, nm[k].c_str(), nm[q].c_str());
         }
     }
-    C.path = ES_PATH_GENERIC;
-    return ES_OK;
+    // the forward's tile rules for every buffer TMA reads or writes
+    bool grads16 = aligned16(grad_out);
+    for (int k = 0; k < n_seqs; ++k) grads16 = grads16 && aligned16(grad_seqs[k]);
+    const bool lane_ok = grads16 && body_lane_ok(C.S, seqs, states);
+    const bool vec_ok = grads16 && body_vec_ok(C.S, seqs, states);
+    if (forced == ES_PATH_AUTO) {
+        C.path = vec_ok ? ES_PATH_VEC_TMA : lane_ok ? ES_PATH_LANE_TMA : ES_PATH_GENERIC;
+        return ES_OK;
+    }
+    if (forced == ES_PATH_GENERIC || (forced == ES_PATH_LANE_TMA && lane_ok) || (forced == ES_PATH_VEC_TMA && vec_ok)) {
+        C.path = forced;
+        return ES_OK;
+    }
+    return api_fail(ES_E_UNSUPPORTED, "%s: the forced kernel path %d cannot serve this call", kFn, forced);
 }
 
 bool launch_body_generic_bwd(const BodyBwdCall& B, const float* init, const float* const* seqs, const float* states,
@@ -492,6 +543,103 @@ bool launch_body_generic_bwd(const BodyBwdCall& B, const float* init, const floa
     int reverse = C.reverse;
     void* args[] = {&sp, &init, &states, &gout, &gp, &ginit, &O, &T, &J, &reverse};
     return jit_launch(k, static_cast<unsigned>(blocks), threads, 0, stream, args, err);
+}
+
+bool launch_body_lane_bwd(const BodyBwdCall& B, const float* init, const float* const* seqs, const float* states,
+                          const float* gout, float* ginit, float* const* gseqs, cudaStream_t stream,
+                          DeviceState* dev, EncodeTiledFn encode, std::string* err) {
+    const BodyCall& C = B.C;
+    const int NS = C.S.n_seqs;
+    const int NM = NS + 2;
+    const int64_t I = C.S.J;
+    int LI = 32;
+    for (int cand : {128, 64}) {
+        if (I >= cand && 5 * C.S.O * ((I + cand - 1) / cand) >= 4LL * dev->num_sms) {
+            LI = cand;
+            break;
+        }
+    }
+    const int64_t tiles_i = (I + LI - 1) / LI;
+    const bool one_per_sm = C.S.O * tiles_i <= dev->num_sms;
+    const int TT = lane_bwd_trips(NS, one_per_sm);
+    const int64_t stage_bytes = static_cast<int64_t>(NM) * TT * LI * 4;
+    const int64_t out_bytes = 2LL * NS * TT * LI * 4;       // two gradient tiles
+    const int64_t smem_cap = one_per_sm ? 200 * 1024 : 100 * 1024;
+    int stages = 96 / TT;
+    if (stages > 8) stages = 8;
+    while (stages > 2 && stages * stage_bytes + out_bytes > smem_cap) --stages;
+    // the sequences, the saved states, the output gradient, then the gradients
+    alignas(64) CUtensorMap maps[2 * ES_MAX_SEQS + 2];
+    for (int q = 0; q < 2 * NS + 2; ++q) {
+        const float* base = q < NS ? seqs[q] : q == NS ? states : q == NS + 1 ? gout : gseqs[q - NM];
+        if (!encode_rows(encode, &maps[q], base, C.S.O, C.S.T, I, LI, TT)) {
+            *err = "cuTensorMapEncodeTiled failed for a lane-innermost backward tile map";
+            return false;
+        }
+    }
+    JitKernel k;
+    const KernelText kt = lane_bwd_text(B.functor, LI, TT);
+    if (!jit_kernel(kt.source, kt.name, &k, err)) return false;
+    int T = static_cast<int>(C.S.T), Ii = static_cast<int>(I), ti = static_cast<int>(tiles_i);
+    int reverse = C.reverse;
+    unsigned int* status = dev->status;
+    uint64_t wait_ns = api_wait_ns();
+    int64_t drop = api_drop_tile();
+    void* args[] = {maps, &init, &ginit, &T, &Ii, &ti, &stages, &reverse, &status, &wait_ns, &drop};
+    const size_t smem = static_cast<size_t>(stages * stage_bytes + out_bytes) + 1024;
+    return jit_launch(k, static_cast<unsigned>(C.S.O * tiles_i), 32 + LI, smem, stream, args, err);
+}
+
+bool launch_body_vec_bwd(const BodyBwdCall& B, const float* init, const float* const* seqs, const float* states,
+                         const float* gout, float* ginit, float* const* gseqs, cudaStream_t stream, DeviceState* dev,
+                         EncodeTiledFn encode, std::string* err) {
+    const BodyCall& C = B.C;
+    const int NS = C.S.n_seqs;
+    const int W = static_cast<int>(C.S.W);
+    const int LV = 128 / W;
+    int n_wide = 0;
+    for (int q = 0; q < NS; ++q) n_wide += C.S.sw[q] == W ? 1 : 0;
+    const int TT = vec_bwd_trips(W, n_wide, NS - n_wide);
+    const int64_t stage_bytes = vec_bwd_stage_bytes(W, TT, n_wide, NS - n_wide);
+    const int64_t out_bytes = 2 * vec_stage_bytes(W, TT, n_wide, NS - n_wide);   // two gradient tiles
+    const int64_t tiles_j = (C.S.J + LV - 1) / LV;
+    const int64_t ctas = C.S.O * tiles_j;
+    int64_t per_sm = (ctas + dev->num_sms - 1) / dev->num_sms;
+    per_sm = per_sm < 1 ? 1 : per_sm > 8 ? 8 : per_sm;
+    int64_t budget = (200 * 1024) / per_sm;
+    if (budget > 160 * 1024) budget = 160 * 1024;
+    int64_t st = (budget - out_bytes) / stage_bytes;
+    const int stages = static_cast<int>(st < 2 ? 2 : st > 8 ? 8 : st);
+    // the sequences, the saved states, the output gradient, then the gradients
+    alignas(64) CUtensorMap maps[2 * ES_MAX_SEQS + 2];
+    for (int q = 0; q < 2 * NS + 2; ++q) {
+        const int qs = q < NS ? q : q >= NS + 2 ? q - NS - 2 : -1;   // the sequence a map follows
+        const bool wide = qs < 0 || C.S.sw[qs] == W;
+        const float* basep = q < NS ? seqs[q] : q == NS ? states : q == NS + 1 ? gout : gseqs[q - NS - 2];
+        const int64_t row = wide ? C.S.J * W : C.S.J;
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(row), static_cast<cuuint64_t>(C.S.T),
+                                    static_cast<cuuint64_t>(C.S.O)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row) * 4, static_cast<cuuint64_t>(row) * C.S.T * 4};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(wide ? 128 : LV), static_cast<cuuint32_t>(TT), 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (encode(&maps[q], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(basep), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            *err = "cuTensorMapEncodeTiled failed for a vector-state backward tile map";
+            return false;
+        }
+    }
+    JitKernel k;
+    const KernelText kt = vec_bwd_text(B.functor, W, TT);
+    if (!jit_kernel(kt.source, kt.name, &k, err)) return false;
+    int T = static_cast<int>(C.S.T), J = static_cast<int>(C.S.J), tj = static_cast<int>(tiles_j);
+    int stg = stages, reverse = C.reverse;
+    unsigned int* status = dev->status;
+    uint64_t wait_ns = api_wait_ns();
+    int64_t drop = api_drop_tile();
+    void* args[] = {maps, &init, &ginit, &T, &J, &tj, &stg, &reverse, &status, &wait_ns, &drop};
+    const size_t smem = static_cast<size_t>(stages * stage_bytes + out_bytes) + 1024;
+    return jit_launch(k, static_cast<unsigned>(ctas), 32 + 128 / vec_bwd_values(W), smem, stream, args, err);
 }
 
 void fill_info(const BodyCall& C, es_plan_info* info) {
@@ -579,10 +727,24 @@ es_status es_body_prepare_backward(es_body_t body, int state_width, int n_seqs, 
     es_status st = es::signature_functor("es_body_prepare_backward", body, state_width, n_seqs, seq_widths, &functor,
                                          &W, true);
     if (st != ES_OK) return st;
-    const es::KernelText kt = es::generic_bwd_text(functor, W);
-    std::string err;
-    if (!es::jit_compile(kt.source, kt.name, &err))
-        return es::api_fail(ES_E_CUDA, "es_body_prepare_backward: %s", err.c_str());
+    std::vector<es::KernelText> todo = {es::generic_bwd_text(functor, W)};
+    if (W == 1)
+        for (int LI : {32, 64, 128})
+            for (bool one : {false, true}) {
+                const int TT = es::lane_bwd_trips(n_seqs, one);
+                if (one && TT == es::lane_bwd_trips(n_seqs, false)) continue;
+                todo.push_back(es::lane_bwd_text(functor, LI, TT));
+            }
+    if (W == 2 || W == 4 || W == 8 || W == 16) {
+        int n_wide = 0;
+        for (int k = 0; k < n_seqs; ++k) n_wide += (seq_widths == nullptr || seq_widths[k] == W) ? 1 : 0;
+        todo.push_back(es::vec_bwd_text(functor, W, es::vec_bwd_trips(W, n_wide, n_seqs - n_wide)));
+    }
+    for (const es::KernelText& kt : todo) {
+        std::string err;
+        if (!es::jit_compile(kt.source, kt.name, &err))
+            return es::api_fail(ES_E_CUDA, "es_body_prepare_backward: %s", err.c_str());
+    }
     return ES_OK;
 }
 
@@ -629,9 +791,21 @@ es_status es_scan_body_backward_f32(es_body_t body, const float* initial, const 
     es::DeviceState* ds = nullptr;
     if ((st = es::api_device(&dev, &ds)) != ES_OK) return st;
     std::string err;
-    if (!es::launch_body_generic_bwd(B, initial, seqs, states, grad_out, grad_initial, grad_seqs,
-                                     reinterpret_cast<cudaStream_t>(stream), &err))
-        return es::api_fail(ES_E_CUDA, "es_scan_body_backward_f32: %s", err.c_str());
+    bool ok;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (B.C.path == ES_PATH_LANE_TMA || B.C.path == ES_PATH_VEC_TMA) {
+        es::EncodeTiledFn encode = nullptr;
+        if ((st = es::api_encoder(&encode)) != ES_OK) return st;
+        if (B.C.path == ES_PATH_LANE_TMA)
+            ok = es::launch_body_lane_bwd(B, initial, seqs, states, grad_out, grad_initial, grad_seqs, s, ds, encode,
+                                          &err);
+        else
+            ok = es::launch_body_vec_bwd(B, initial, seqs, states, grad_out, grad_initial, grad_seqs, s, ds, encode,
+                                         &err);
+    } else {
+        ok = es::launch_body_generic_bwd(B, initial, seqs, states, grad_out, grad_initial, grad_seqs, s, &err);
+    }
+    if (!ok) return es::api_fail(ES_E_CUDA, "es_scan_body_backward_f32: %s", err.c_str());
     es::count_launch();
     return ES_OK;
 }

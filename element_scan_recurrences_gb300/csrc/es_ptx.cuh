@@ -175,6 +175,13 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t c0,
                  : "memory");
 }
 
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2,
+                                             const void* src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 template <int N>

@@ -27,7 +27,22 @@ def _ptrs(n):
 def test_backward_plan():
     b = es.Body("(lambda (h x a) (tanh (+ x (* a h))))")
     p = b.plan_backward([3, 100, 64], 1)
-    assert p["path"] == "generic" and (p["O"], p["T"], p["J"], p["W"]) == (3, 100, 64, 1)
+    assert p["path"] == "lane_tma" and (p["O"], p["T"], p["J"], p["W"]) == (3, 100, 64, 1)
+    # lanes innermost need 32 or more lanes in rows of 16 bytes, 16-byte aligned TMA-read buffers
+    assert b.plan_backward([3, 100, 66], 1)["path"] == "generic"
+    assert b.plan_backward([3, 100, 16], 1)["path"] == "generic"
+    assert b.plan_backward([64, 100], 0)["path"] == "lane_tma"
+    assert b.plan_backward([100, 64], -1)["path"] == "generic"      # one lane per row
+    for k in (1, 3, 4):                                   # a sequence, the states, grad_out
+        ptrs = _ptrs(2)
+        ptrs[k] += 4
+        assert b.plan_backward([3, 100, 64], 1, ptrs=ptrs)["path"] == "generic"
+    ptrs = _ptrs(2)
+    ptrs[6] += 4                                          # a gradient: written by TMA tensor stores
+    assert b.plan_backward([3, 100, 64], 1, ptrs=ptrs)["path"] == "generic"
+    ptrs = _ptrs(2)
+    ptrs[5] += 4                                          # grad_initial: plain stores
+    assert b.plan_backward([3, 100, 64], 1, ptrs=ptrs)["path"] == "lane_tma"
     assert b.plan_backward([3, 100, 64], 1, reverse=True)["reverse"]
     v = es.Body(body_cases.NORMCAP_TEXT)
     p = v.plan_backward([2, 10, 5, 16], 1, 16, [16, 1])
@@ -66,18 +81,21 @@ def test_backward_plan_rejects_bad_buffers():
 
 def test_backward_forced_path():
     b = es.Body("(lambda (h x a) (tanh (+ x (* a h))))")
-    es.set_path_override("lane_tma")
-    try:
-        with pytest.raises(es.EsError) as e:
-            b.plan_backward([3, 100, 64], 1)
-        assert e.value.status == 4
-    finally:
-        es.set_path_override("auto")
-    es.set_path_override("generic")
-    try:
-        assert b.plan_backward([3, 100, 64], 1)["path"] == "generic"
-    finally:
-        es.set_path_override("auto")
+    for path, shape, status in (("time_tma", [3, 100, 64], 4), ("vec_tma", [3, 100, 64], 4),
+                                ("lane_tma", [3, 100, 66], 4)):
+        es.set_path_override(path)
+        try:
+            with pytest.raises(es.EsError) as e:
+                b.plan_backward(shape, 1)
+            assert e.value.status == status
+        finally:
+            es.set_path_override("auto")
+    for path in ("generic", "lane_tma"):
+        es.set_path_override(path)
+        try:
+            assert b.plan_backward([3, 100, 64], 1)["path"] == path
+        finally:
+            es.set_path_override("auto")
 
 
 def test_backward_rejects_what_the_forward_rejects():

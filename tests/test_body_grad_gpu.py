@@ -48,16 +48,20 @@ def compare(got, want, exact, what):
         what, float(err.max()), np.unravel_index(err.argmax(), err.shape))
 
 
-def backward_pair(text, initial, seqs, axis, state_axis, reverse, seed):
+def backward_pair(text, initial, seqs, axis, state_axis, reverse, seed, path="auto"):
     """(GPU gradients, oracle gradients) from the oracle's forward states."""
     states = scan_body(text, initial, seqs, axis=axis, state_axis=state_axis, reverse=reverse)
     G = np.random.default_rng(seed).standard_normal(states.shape).astype(np.float32)
     want = scan_body_backward(text, initial, seqs, states, G, axis=axis, state_axis=state_axis, reverse=reverse)
     body = es.Body(text)
     d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    gi, gs = body.scan_backward(d(initial), [d(s) for s in seqs], d(states), d(G), axis=axis,
-                                state_axis=state_axis, reverse=reverse)
-    es.device_status()
+    es.set_path_override(path)
+    try:
+        gi, gs = body.scan_backward(d(initial), [d(s) for s in seqs], d(states), d(G), axis=axis,
+                                    state_axis=state_axis, reverse=reverse)
+        es.device_status()
+    finally:
+        es.set_path_override("auto")
     return (gi.cpu().numpy(), [g.cpu().numpy() for g in gs]), want
 
 
@@ -70,11 +74,67 @@ def check(got, want, exact, what):
 @pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
 @pytest.mark.parametrize("cid", body_cases.CASE_IDS)
 def test_body_backward(cid, reverse):
-    """Every test body, several blocks of lanes with a ragged last block."""
+    """Every test body on the any-layout kernel: several blocks of lanes with
+    a ragged last block."""
     c = body_cases.case(cid)
     initial, seqs, state_axis = body_cases.make_inputs(c, 3, 45, 50, seed=7)
-    got, want = backward_pair(c[1], initial, seqs, 1, state_axis, reverse, 11)
+    got, want = backward_pair(c[1], initial, seqs, 1, state_axis, reverse, 11, path="generic")
     check(got, want, c[6], "%s reverse=%s" % (cid, reverse))
+
+
+SCALAR_IDS = [c[0] for c in body_cases.CASES if c[2] == 0]
+
+
+@pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
+@pytest.mark.parametrize("cid", SCALAR_IDS)
+def test_body_backward_lane_tiles(cid, reverse):
+    """Scalar-state bodies on the lanes-innermost backward: a ragged lane
+    tile (40 lanes: 32 + 8) and a ragged time tile; the same operations per
+    trip as the oracle, so exact bodies stay bit-identical."""
+    c = body_cases.case(cid)
+    initial, seqs, state_axis = body_cases.make_inputs(c, 3, 45, 40, seed=8)
+    assert es.Body(c[1]).plan_backward([3, 45, 40], 1, reverse=reverse)["path"] == "lane_tma"
+    got, want = backward_pair(c[1], initial, seqs, 1, state_axis, reverse, 12, path="lane_tma")
+    check(got, want, c[6], "%s reverse=%s" % (cid, reverse))
+
+
+VECTOR_IDS = [c[0] for c in body_cases.CASES if c[2] in (2, 4, 8, 16)]
+
+
+def _vjp_sums_over_state(text, W, widths):
+    """Whether the VJP sums over the state (an explicit sum, a width-one
+    operand of a wide operation, the tie count of `max`): those sums run as
+    shuffle butterflies on the tiled kernel, in another order than the
+    oracle's w = 0..W-1."""
+    src = es.Body(text).source_backward(W, widths)
+    return "group_sum" in src[src.index("static void vjp("):]
+
+
+@pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
+@pytest.mark.parametrize("cid", VECTOR_IDS)
+def test_body_backward_vec_tiles(cid, reverse):
+    """Vector-state bodies on the vector-state backward: a ragged lane tile
+    and a ragged time tile.  Bit-identical unless the VJP sums over the
+    state (then within the tolerance)."""
+    c = body_cases.case(cid)
+    W = c[2]
+    J = 128 // W * 2 + 4
+    initial, seqs, state_axis = body_cases.make_inputs(c, 3, 45, J, seed=9)
+    assert es.Body(c[1]).plan_backward([3, 45, J, W], 1, W, c[3], reverse=reverse)["path"] == "vec_tma"
+    got, want = backward_pair(c[1], initial, seqs, 1, state_axis, reverse, 13, path="vec_tma")
+    exact = c[6] and not _vjp_sums_over_state(c[1], W, c[3])
+    check(got, want, exact, "%s reverse=%s" % (cid, reverse))
+
+
+@pytest.mark.parametrize("T", [1, 2, 17, 200])
+def test_body_backward_lane_trip_counts(T):
+    """One trip (the shifted-state box entirely outside), a partial tile,
+    a tile and one, and many tiles."""
+    c = body_cases.case("five_seqs")
+    initial, seqs, _ = body_cases.make_inputs(c, 2, T, 36, seed=T)
+    for reverse in (False, True):
+        got, want = backward_pair(c[1], initial, seqs, 1, False, reverse, T, path="lane_tma")
+        check(got, want, True, "T=%d reverse=%s" % (T, reverse))
 
 
 @pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
@@ -83,7 +143,7 @@ def test_body_backward_autograd_bodies(ci, reverse):
     case = body_grad_pins.AUTOGRAD_CASES[ci]
     text, W, widths, ranges, irng = case[0], case[2], case[3], case[4], case[5]
     c = ("ag", text, W, widths, ranges, irng, False, False)
-    initial, seqs, state_axis = body_cases.make_inputs(c, 2, 33, 70, seed=ci)
+    initial, seqs, state_axis = body_cases.make_inputs(c, 2, 33, 68, seed=ci)
     got, want = backward_pair(text, initial, seqs, 1, state_axis, reverse, 100 + ci)
     check(got, want, False, "%s reverse=%s" % (text, reverse))
 
@@ -110,9 +170,13 @@ TIE_BODIES = [
 def test_body_backward_ties_bitwise(ti, reverse):
     text, W, widths, ranges, irng = TIE_BODIES[ti]
     c = ("tie", text, W, widths, ranges, irng, True, True)
-    initial, seqs, sa = _quantised(c, 2, 40, 33, ti)
-    got, want = backward_pair(text, initial, seqs, 1, sa, reverse, ti)
+    initial, seqs, sa = _quantised(c, 2, 40, 36, ti)
+    # the one-thread-per-lane kernel: its sums over the state run in state order
+    got, want = backward_pair(text, initial, seqs, 1, sa, reverse, ti, path="generic")
     check(got, want, True, "%s reverse=%s" % (text, reverse))
+    if W == 0:
+        got, want = backward_pair(text, initial, seqs, 1, sa, reverse, ti, path="lane_tma")
+        check(got, want, True, "%s reverse=%s lane tiles" % (text, reverse))
 
 
 @pytest.mark.parametrize("axis", [0, -1])
@@ -178,7 +242,7 @@ def test_body_backward_rejects_overlap_on_device():
     assert e.value.status == 3
 
 
-@pytest.mark.parametrize("name", ["body_tanh_decay_lanes", "body_normcap_vector"])
+@pytest.mark.parametrize("name", ["body_tanh_decay_lanes", "body_normcap_vector", "body_maxplus_reverse"])
 def test_body_backward_full_size_sampled(name):
     """The backward of a body workload at full size in the bench's launch
     configuration, checked on sampled lanes against the gradient oracle."""
@@ -203,7 +267,8 @@ def test_body_backward_full_size_sampled(name):
         s_init = init[o:o + 1][:, jj].cpu().numpy()
         wi, ws = scan_body_backward(w.text, s_init, s_seqs, s_states, s_G, axis=1, state_axis=w.state_axis,
                                     reverse=reverse)
-        exact = name == "body_normcap_vector"
+        # the vector-state kernel sums over the state as a butterfly
+        exact = name == "body_maxplus_reverse"
         compare(gi[o:o + 1][:, jj].cpu().numpy(), wi, exact, "%s grad_initial o=%d" % (name, o))
         for k in range(len(seqs)):
             compare(gs[k][sl].cpu().numpy(), ws[k], exact, "%s grad seq %d o=%d" % (name, k, o))

@@ -84,3 +84,28 @@ def test_table_scan_pipelines(shape, axis, path):
     want = TS.table_scan(table, sym, axis=axis)
     drop_then_recover(lambda: es.table_scan(dt, ds, axis=axis),
                       lambda out: np.testing.assert_array_equal(out.cpu().numpy(), want))
+
+
+def test_body_backward_lane_pipeline():
+    """The lanes-innermost backward gives up a missing tile, then recovers."""
+    from oracle.body_grad import scan_body_backward
+    c = body_cases.case("maxplus")
+    initial, seqs, _ = body_cases.make_inputs(c, 2, 400, 64)
+    states = scan_body(c[1], initial, seqs, axis=1)
+    G = np.random.default_rng(1).standard_normal(states.shape).astype(np.float32)
+    want = scan_body_backward(c[1], initial, seqs, states, G, axis=1)
+    body = es.Body(c[1])
+    d = lambda a: torch.from_numpy(a).cuda()
+    di, ds, dst, dg = d(initial), [d(s) for s in seqs], d(states), d(G)
+    es.set_path_override("lane_tma")
+
+    def run():
+        return body.scan_backward(di, ds, dst, dg, axis=1)
+
+    def check(out):
+        gi, gs = out
+        assert np.array_equal(gi.cpu().numpy(), want[0])
+        for g, w in zip(gs, want[1]):
+            assert np.array_equal(g.cpu().numpy(), w)
+
+    drop_then_recover(run, check)
