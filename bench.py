@@ -40,7 +40,8 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 PATH_KERNEL = {"lane_tma": "k_lane_tma", "time_tma": "k_time_tma", "vec_tma": "k_vec_tma", "generic": "k_generic"}
 PATH_KERNEL_BWD = {"lane_tma": "k_lane_bwd", "generic": "k_generic_bwd"}
-PATH_KERNEL_BODY_BWD = {"generic": "k_body_generic_bwd", "lane_tma": "k_body_lane_bwd", "vec_tma": "k_body_vec_bwd"}
+PATH_KERNEL_BODY_BWD = {"generic": "k_body_generic_bwd", "lane_tma": "k_body_lane_bwd", "vec_tma": "k_body_vec_bwd",
+                        "time_tma": "k_body_time_bwd"}
 # kernels compiled at run time from a body program
 PATH_KERNEL_BODY = {"lane_tma": "k_body_lane", "time_tma": "k_body_time", "vec_tma": "k_body_vec",
                     "generic": "k_body_generic"}
@@ -185,6 +186,7 @@ KERNEL_SOURCES = {
     "k_body_generic_bwd": ["skel_generic_bwd.cuh"] + _BODY_SOURCES,
     "k_body_lane_bwd": ["skel_lane_bwd.cuh"] + _BODY_SOURCES,
     "k_body_vec_bwd": ["skel_vec_bwd.cuh", "skel_vec.cuh"] + _BODY_SOURCES,
+    "k_body_time_bwd": ["skel_time_bwd.cuh"] + _BODY_SOURCES,
 }
 
 

@@ -425,6 +425,15 @@ int lane_bwd_trips(int n_seqs, bool one_cta_per_sm) {
     return one_cta_per_sm ? lane_trips(n_seqs) : lane_trips(n_seqs + 2);
 }
 
+// rows per CTA of the time-innermost backward: 64, or 32 with more than three
+// sequences (every sequence's tile and its gradient's stay in shared memory)
+int time_bwd_rows(int n_seqs) { return n_seqs <= 3 ? 64 : 32; }
+
+KernelText time_bwd_text(const std::string& functor, int n_seqs) {
+    return {"#include \"skel_time_bwd.cuh\"\n" + functor,
+            "&es::k_body_time_bwd<EsBody, " + std::to_string(time_bwd_rows(n_seqs)) + ">"};
+}
+
 // values of a lane's state per thread in the vector-state backward
 int vec_bwd_values(int) { return 1; }
 
@@ -469,7 +478,8 @@ es_status plan_body_backward(es_body_t body, const float* initial, const float* 
     if ((st = functor_for(body, static_cast<int>(C.S.W), C.vector, C.wide_mask, &B->functor, true)) != ES_OK)
         return st;
     const int forced = api_path_override();
-    if (forced != ES_PATH_AUTO && forced != ES_PATH_GENERIC && forced != ES_PATH_LANE_TMA && forced != ES_PATH_VEC_TMA)
+    if (forced != ES_PATH_AUTO && forced != ES_PATH_GENERIC && forced != ES_PATH_LANE_TMA && forced != ES_PATH_VEC_TMA &&
+        forced != ES_PATH_TIME_TMA)
         return api_fail(ES_E_UNSUPPORTED, "%s: the forced kernel path %d cannot serve this call", kFn, forced);
     if (C.S.empty) {
         C.path = ES_PATH_EMPTY;
@@ -508,11 +518,14 @@ es_status plan_body_backward(es_body_t body, const float* initial, const float* 
     for (int k = 0; k < n_seqs; ++k) grads16 = grads16 && aligned16(grad_seqs[k]);
     const bool lane_ok = grads16 && body_lane_ok(C.S, seqs, states);
     const bool vec_ok = grads16 && body_vec_ok(C.S, seqs, states);
+    // the 36-trip state boxes want at least two tiles of trips
+    const bool time_ok = grads16 && C.S.T >= 64 && body_time_ok(C.S, seqs, states);
     if (forced == ES_PATH_AUTO) {
-        C.path = vec_ok ? ES_PATH_VEC_TMA : lane_ok ? ES_PATH_LANE_TMA : ES_PATH_GENERIC;
+        C.path = vec_ok ? ES_PATH_VEC_TMA : time_ok ? ES_PATH_TIME_TMA : lane_ok ? ES_PATH_LANE_TMA : ES_PATH_GENERIC;
         return ES_OK;
     }
-    if (forced == ES_PATH_GENERIC || (forced == ES_PATH_LANE_TMA && lane_ok) || (forced == ES_PATH_VEC_TMA && vec_ok)) {
+    if (forced == ES_PATH_GENERIC || (forced == ES_PATH_LANE_TMA && lane_ok) || (forced == ES_PATH_VEC_TMA && vec_ok) ||
+        (forced == ES_PATH_TIME_TMA && time_ok)) {
         C.path = forced;
         return ES_OK;
     }
@@ -642,6 +655,50 @@ bool launch_body_vec_bwd(const BodyBwdCall& B, const float* init, const float* c
     return jit_launch(k, static_cast<unsigned>(ctas), 32 + 128 / vec_bwd_values(W), smem, stream, args, err);
 }
 
+bool launch_body_time_bwd(const BodyBwdCall& B, const float* init, const float* const* seqs, const float* states,
+                          const float* gout, float* ginit, float* const* gseqs, cudaStream_t stream,
+                          DeviceState* dev, EncodeTiledFn encode, std::string* err) {
+    const BodyCall& C = B.C;
+    const int NS = C.S.n_seqs;
+    const int LO = time_bwd_rows(NS);
+    const int64_t stage_bytes = ((NS + 1) * LO * 128LL + LO * 144LL + 1023) & ~1023LL;
+    const int64_t out_bytes = 2LL * NS * LO * 128;
+    const int64_t ctas = (C.S.O + LO - 1) / LO;
+    int64_t per_sm = (ctas + dev->num_sms - 1) / dev->num_sms;
+    per_sm = per_sm < 1 ? 1 : per_sm > 2 ? 2 : per_sm;
+    const int64_t budget = (220 * 1024) / per_sm - out_bytes - 2048;
+    int64_t st = budget / stage_bytes;
+    const int stages = static_cast<int>(st < 2 ? 2 : st > 4 ? 4 : st);
+    // the sequences, the saved states (36-trip unswizzled boxes), the output
+    // gradient, then the gradients
+    alignas(64) CUtensorMap maps[2 * ES_MAX_SEQS + 2];
+    for (int q = 0; q < 2 * NS + 2; ++q) {
+        const bool hbox = q == NS;
+        const float* basep = q < NS ? seqs[q] : q == NS ? states : q == NS + 1 ? gout : gseqs[q - NS - 2];
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(C.S.T), static_cast<cuuint64_t>(C.S.O)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(C.S.T) * 4};
+        const cuuint32_t box[2] = {hbox ? 36u : 32u, static_cast<cuuint32_t>(LO)};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode(&maps[q], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(basep), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, hbox ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            *err = "cuTensorMapEncodeTiled failed for a time-innermost backward tile map";
+            return false;
+        }
+    }
+    JitKernel k;
+    const KernelText kt = time_bwd_text(B.functor, NS);
+    if (!jit_kernel(kt.source, kt.name, &k, err)) return false;
+    int O = static_cast<int>(C.S.O), T = static_cast<int>(C.S.T);
+    int stg = stages, reverse = C.reverse;
+    unsigned int* status = dev->status;
+    uint64_t wait_ns = api_wait_ns();
+    int64_t drop = api_drop_tile();
+    void* args[] = {maps, &init, &ginit, &O, &T, &stg, &reverse, &status, &wait_ns, &drop};
+    const size_t smem = static_cast<size_t>(stages * stage_bytes + out_bytes) + 1024;
+    return jit_launch(k, static_cast<unsigned>(ctas), 32 + LO, smem, stream, args, err);
+}
+
 void fill_info(const BodyCall& C, es_plan_info* info) {
     if (info == nullptr) return;
     std::memset(info, 0, sizeof(*info));
@@ -735,6 +792,7 @@ es_status es_body_prepare_backward(es_body_t body, int state_width, int n_seqs, 
                 if (one && TT == es::lane_bwd_trips(n_seqs, false)) continue;
                 todo.push_back(es::lane_bwd_text(functor, LI, TT));
             }
+    if (W == 1) todo.push_back(es::time_bwd_text(functor, n_seqs));
     if (W == 2 || W == 4 || W == 8 || W == 16) {
         int n_wide = 0;
         for (int k = 0; k < n_seqs; ++k) n_wide += (seq_widths == nullptr || seq_widths[k] == W) ? 1 : 0;
@@ -793,11 +851,14 @@ es_status es_scan_body_backward_f32(es_body_t body, const float* initial, const 
     std::string err;
     bool ok;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (B.C.path == ES_PATH_LANE_TMA || B.C.path == ES_PATH_VEC_TMA) {
+    if (B.C.path != ES_PATH_GENERIC) {
         es::EncodeTiledFn encode = nullptr;
         if ((st = es::api_encoder(&encode)) != ES_OK) return st;
         if (B.C.path == ES_PATH_LANE_TMA)
             ok = es::launch_body_lane_bwd(B, initial, seqs, states, grad_out, grad_initial, grad_seqs, s, ds, encode,
+                                          &err);
+        else if (B.C.path == ES_PATH_TIME_TMA)
+            ok = es::launch_body_time_bwd(B, initial, seqs, states, grad_out, grad_initial, grad_seqs, s, ds, encode,
                                           &err);
         else
             ok = es::launch_body_vec_bwd(B, initial, seqs, states, grad_out, grad_initial, grad_seqs, s, ds, encode,

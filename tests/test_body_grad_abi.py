@@ -9,15 +9,23 @@ import body_grad_pins
 from element_scan_recurrences_gb300 import binding as es
 
 
-@pytest.mark.parametrize("cid", body_cases.CASE_IDS)
+# scalar and vector states, width-one sequences, the most sequences, `max`
+# over the state and most operations of the body language
+COMPILE_IDS = ["identities", "angle", "eight_seqs", "normcap_w16", "row_max_w8"]
+
+
+@pytest.mark.parametrize("cid", COMPILE_IDS)
 def test_backward_kernel_compiles(cid):
+    """NVRTC compiles every backward kernel variant of the signature."""
     c = body_cases.case(cid)
     es.Body(c[1]).prepare_backward(c[2], c[3])
 
 
-def test_backward_kernels_compile_for_autograd_bodies():
+def test_backward_source_for_every_test_body():
+    for c in body_cases.CASES:
+        assert "static void vjp(" in es.Body(c[1]).source_backward(c[2], c[3])
     for case in body_grad_pins.AUTOGRAD_CASES:
-        es.Body(case[0]).prepare_backward(case[2], case[3])
+        assert "static void vjp(" in es.Body(case[0]).source_backward(case[2], case[3])
 
 
 def _ptrs(n):
@@ -32,7 +40,9 @@ def test_backward_plan():
     assert b.plan_backward([3, 100, 66], 1)["path"] == "generic"
     assert b.plan_backward([3, 100, 16], 1)["path"] == "generic"
     assert b.plan_backward([64, 100], 0)["path"] == "lane_tma"
-    assert b.plan_backward([100, 64], -1)["path"] == "generic"      # one lane per row
+    assert b.plan_backward([100, 64], -1)["path"] == "time_tma"     # the sequence axis last
+    assert b.plan_backward([100, 32], -1)["path"] == "generic"      # one tile of trips only
+    assert b.plan_backward([100, 66], -1)["path"] == "generic"      # rows of 16 bytes
     for k in (1, 3, 4):                                   # a sequence, the states, grad_out
         ptrs = _ptrs(2)
         ptrs[k] += 4
@@ -82,7 +92,7 @@ def test_backward_plan_rejects_bad_buffers():
 def test_backward_forced_path():
     b = es.Body("(lambda (h x a) (tanh (+ x (* a h))))")
     for path, shape, status in (("time_tma", [3, 100, 64], 4), ("vec_tma", [3, 100, 64], 4),
-                                ("lane_tma", [3, 100, 66], 4)):
+                                ("lane_tma", [3, 100, 66], 4), ("mat_tma", [3, 100, 64], 4)):
         es.set_path_override(path)
         try:
             with pytest.raises(es.EsError) as e:

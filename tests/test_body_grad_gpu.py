@@ -98,6 +98,28 @@ def test_body_backward_lane_tiles(cid, reverse):
     check(got, want, c[6], "%s reverse=%s" % (cid, reverse))
 
 
+@pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
+@pytest.mark.parametrize("cid", SCALAR_IDS)
+def test_body_backward_time_tiles(cid, reverse):
+    """Scalar-state bodies with the sequence axis last on the time-innermost
+    backward: 150 rows (a ragged row tile) of 100 trips (a ragged time tile)."""
+    c = body_cases.case(cid)
+    initial, seqs, state_axis = body_cases.make_inputs(c, 3, 100, 50, seed=10, axis=2)
+    assert es.Body(c[1]).plan_backward([3, 50, 100], 2, reverse=reverse)["path"] == "time_tma"
+    got, want = backward_pair(c[1], initial, seqs, 2, state_axis, reverse, 14, path="time_tma")
+    check(got, want, c[6], "%s reverse=%s" % (cid, reverse))
+
+
+@pytest.mark.parametrize("T", [64, 68, 96, 260])
+def test_body_backward_time_trip_counts(T):
+    """Exactly two tiles, a 4-trip ragged tile, three tiles, many tiles."""
+    c = body_cases.case("eight_seqs")
+    initial, seqs, _ = body_cases.make_inputs(c, 2, T, 40, seed=T, axis=2)
+    for reverse in (False, True):
+        got, want = backward_pair(c[1], initial, seqs, 2, False, reverse, T, path="time_tma")
+        check(got, want, True, "T=%d reverse=%s" % (T, reverse))
+
+
 VECTOR_IDS = [c[0] for c in body_cases.CASES if c[2] in (2, 4, 8, 16)]
 
 

@@ -86,21 +86,25 @@ def test_table_scan_pipelines(shape, axis, path):
                       lambda out: np.testing.assert_array_equal(out.cpu().numpy(), want))
 
 
-def test_body_backward_lane_pipeline():
-    """The lanes-innermost backward gives up a missing tile, then recovers."""
+@pytest.mark.parametrize("path,axis", [("lane_tma", 1), ("time_tma", 2), ("vec_tma", 1)])
+def test_body_backward_pipelines(path, axis):
+    """Each tiled backward gives up a missing tile, then recovers."""
     from oracle.body_grad import scan_body_backward
+    # a body with no sum over the state: bit-exact on every path
     c = body_cases.case("maxplus")
-    initial, seqs, _ = body_cases.make_inputs(c, 2, 400, 64)
-    states = scan_body(c[1], initial, seqs, axis=1)
+    if path == "vec_tma":
+        c = ("maxplus_w8", c[1], 8, [8, 8]) + tuple(c[4:])
+    initial, seqs, sa = body_cases.make_inputs(c, 2, 400, 64, axis=axis)
+    states = scan_body(c[1], initial, seqs, axis=axis, state_axis=sa)
     G = np.random.default_rng(1).standard_normal(states.shape).astype(np.float32)
-    want = scan_body_backward(c[1], initial, seqs, states, G, axis=1)
+    want = scan_body_backward(c[1], initial, seqs, states, G, axis=axis, state_axis=sa)
     body = es.Body(c[1])
     d = lambda a: torch.from_numpy(a).cuda()
     di, ds, dst, dg = d(initial), [d(s) for s in seqs], d(states), d(G)
-    es.set_path_override("lane_tma")
+    es.set_path_override(path)
 
     def run():
-        return body.scan_backward(di, ds, dst, dg, axis=1)
+        return body.scan_backward(di, ds, dst, dg, axis=axis, state_axis=sa)
 
     def check(out):
         gi, gs = out
