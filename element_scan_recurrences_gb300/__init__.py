@@ -18,6 +18,9 @@ _BINDING_NAMES = {
 
 
 def __getattr__(name):
+    if name == "element_scan":
+        from .autograd import element_scan
+        return element_scan
     if name in _BINDING_NAMES:
         from . import binding
         return getattr(binding, name)

@@ -131,3 +131,14 @@ def test_vjp_source_has_the_derivative_rules():
     assert "dsw[0][e] = 0.0f" in src
     src = es.Body("(lambda (h x) 3.0)").source_backward()
     assert "dp[e] = 0.0f" in src
+
+
+def test_autograd_refuses_cpu_tensors():
+    """No CPU fallback: the differentiable scan wants CUDA tensors."""
+    torch = pytest.importorskip("torch")
+    from element_scan_recurrences_gb300.autograd import element_scan
+    x = torch.zeros(2, 5, 3)
+    with pytest.raises(TypeError):
+        element_scan("(lambda (h x) (+ h x))", torch.zeros(2, 3), [x], axis=1)
+    with pytest.raises(TypeError):
+        element_scan("tanh_decay", torch.zeros(2, 3), [x, x], axis=1)
