@@ -28,12 +28,24 @@ notes): the computation is f32 (the table row: "computed in f32"); a matrix
 product is the plain definition, each product and each sum rounded, the
 terms added in the order j = 0..n-1, then b added; the division by s is
 an IEEE f32 division.
+
+Gradients (same section: "its gradient is the same scan run backwards on
+a's transposes"; a projective scan "has no gradient"): with g[t] the
+gradient of the states, the cotangent of h[t] is
+
+    lam[t] = a[t+1]^T @ lam[t+1] + g[t]       (a reverse scan: a[t-1], lam[t-1])
+
+run from zero in the opposite trip order (past the last trip the
+coefficient is the zero matrix), so db[t] = lam[t] and
+da[t] = lam[t] @ h[t-1]^T (h before the scan's first trip is zero).  Each
+product is the plain definition in f32: a^T's rows in order j, then g
+added; da[i][j] = sum over k = 0..m-1 in order of lam[i][k] * h[j][k].
 """
 from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["matrix_scan", "linear_scan", "broadcast_lead"]
+__all__ = ["matrix_scan", "linear_scan", "broadcast_lead", "matrix_scan_backward", "linear_scan_backward"]
 
 
 def broadcast_lead(sa, sb):
@@ -114,3 +126,70 @@ def linear_scan(a, b, axis=0, reverse=False):
     r = matrix_scan(np.broadcast_to(a, shape)[..., None, None], np.broadcast_to(b, shape)[..., None, None],
                     axis=axis, reverse=reverse)
     return r[..., 0, 0]
+
+
+def _outer_sum(lam, hp):
+    """lam @ hp^T in f32: [L, n, m] x [L, n, m] -> [L, n, n], the sum over
+    k = 0..m-1 in order, each product and each sum rounded."""
+    m = lam.shape[-1]
+    acc = np.multiply(lam[:, :, None, 0], hp[:, None, :, 0], dtype=np.float32)
+    for k in range(1, m):
+        acc = np.add(acc, np.multiply(lam[:, :, None, k], hp[:, None, :, k], dtype=np.float32), dtype=np.float32)
+    return acc
+
+
+def matrix_scan_backward(a, b, states, grad_out, axis=0, reverse=False, projective=False):
+    """Gradients of sum(grad_out * matrix_scan(a, b)) with respect to a and b,
+    from the forward states.  a and b have one leading shape (a broadcast
+    operand's gradient is the caller's sum).  Returns (da, db), f32."""
+    if projective:
+        raise ValueError("E-ARG: a projective matrix-scan has no gradient")
+    a = np.asarray(a, np.float32)
+    b = np.asarray(b, np.float32)
+    states = np.asarray(states, np.float32)
+    grad_out = np.asarray(grad_out, np.float32)
+    if a.ndim < 3 or b.ndim < 3 or a.shape[:-2] != b.shape[:-2]:
+        raise ValueError("E-DIM-001: the backward wants a [..., n, n] and b [..., n, m] of one leading shape")
+    n, m = b.shape[-2], b.shape[-1]
+    if a.shape[-2:] != (n, n) or states.shape != b.shape or grad_out.shape != b.shape:
+        raise ValueError("E-DIM-001: shapes do not fit")
+    lead = b.shape[:-2]
+    ax = axis + len(lead) if axis < 0 else axis
+    if not 0 <= ax < len(lead):
+        raise ValueError("E-DIM-001: axis %d out of range for leading shape %s" % (axis, lead))
+    T = lead[ax]
+    am = np.moveaxis(a, ax, 0).reshape(T, -1, n, n)
+    hm = np.moveaxis(states, ax, 0).reshape(T, -1, n, m)
+    gm = np.moveaxis(grad_out, ax, 0).reshape(T, -1, n, m)
+    L = am.shape[1]
+    da = np.empty((T, L, n, n), np.float32)
+    db = np.empty((T, L, n, m), np.float32)
+    lam = np.zeros((L, n, m), np.float32)
+    zero_a = np.zeros((L, n, n), np.float32)
+    zero_h = np.zeros((L, n, m), np.float32)
+    # the opposite of the scan's trip order
+    order = range(T) if reverse else range(T - 1, -1, -1)
+    with np.errstate(all="ignore"):
+        for t in order:
+            tn = t - 1 if reverse else t + 1          # the trip after t in scan order
+            tp = t + 1 if reverse else t - 1          # the trip before t in scan order
+            aT = np.ascontiguousarray(np.swapaxes(am[tn], 1, 2)) if 0 <= tn < T else zero_a
+            lam = np.add(_product(aT, lam), gm[t], dtype=np.float32)
+            db[t] = lam
+            hp = hm[tp] if 0 <= tp < T else zero_h
+            da[t] = _outer_sum(lam, hp)
+    moved = tuple(lead[i] for i in range(len(lead)) if i != ax)
+    da = np.moveaxis(da.reshape((T,) + moved + (n, n)), 0, ax)
+    db = np.moveaxis(db.reshape((T,) + moved + (n, m)), 0, ax)
+    return da, db
+
+
+def linear_scan_backward(a, b, states, grad_out, axis=0, reverse=False):
+    """Gradients of a linear-scan with a and b of one shape: (da, db)."""
+    a = np.asarray(a, np.float32)
+    b = np.asarray(b, np.float32)
+    if a.shape != b.shape:
+        raise ValueError("E-DIM-001: the backward wants a and b of one shape")
+    da, db = matrix_scan_backward(a[..., None, None], b[..., None, None], np.asarray(states)[..., None, None],
+                                  np.asarray(grad_out)[..., None, None], axis=axis, reverse=reverse)
+    return da[..., 0, 0], db[..., 0, 0]

@@ -24,6 +24,19 @@ The facts:
     h_t = h_{t-1} + b_t / c exactly for c a power of two; with b zero after
     its first step, h_t points along (a_t ... a_1) b_0 with a positive factor;
   * shapes the contract rejects.
+
+Gradients ("its gradient is the same scan run backwards on a's
+transposes"; a projective scan has none):
+  * a = identity makes the cotangent a reverse running sum of the state
+    gradients (``np.add.accumulate`` on the flipped sequence, bit for bit),
+    and da[t] = db[t] h[t-1]^T against an f64 ``np.einsum``;
+  * a general scan's gradients agree with PyTorch autograd of an f64 loop
+    over ``torch.matmul``, forward and reverse;
+  * linear-scan: the cotangent of a constant-coefficient scan is
+    ``scipy.signal.lfilter`` run backwards, and da[t] is the one product
+    lam[t] h[t-1];
+  * reverse = flip-backward-flip, axis placement, zero state gradients give
+    zero gradients; a projective scan and broadcast operands are refused.
 """
 from __future__ import annotations
 
@@ -231,7 +244,97 @@ def pin_rejected_shapes(M):
         raise AssertionError("accepted shapes the contract rejects: %s %s axis %d" % (sa, sb, axis))
 
 
+def pin_backward_identity_is_reverse_running_sum(M):
+    rng = _rng(20)
+    L, T, n, m = 3, 9, 3, 2
+    a = np.broadcast_to(np.eye(n, dtype=f32), (L, T, n, n)).copy()
+    b = rng.standard_normal((L, T, n, m)).astype(f32)
+    G = rng.standard_normal((L, T, n, m)).astype(f32)
+    h = M.matrix_scan(a, b, axis=1)
+    da, db = M.matrix_scan_backward(a, b, h, G, axis=1)
+    want = np.flip(np.add.accumulate(np.flip(G, 1), axis=1, dtype=f32), 1)
+    assert np.array_equal(_bits(db), _bits(want)), "db is not the reverse running sum of G"
+    hp = np.concatenate([np.zeros_like(h[:, :1]), h[:, :-1]], axis=1).astype(np.float64)
+    want_a = np.einsum("ltik,ltjk->ltij", db.astype(np.float64), hp)
+    assert np.allclose(da, want_a, rtol=1e-6, atol=1e-6), "da is not db h_prev^T"
+    assert not np.any(da[:, 0]), "da of the first trip (h before it is zero)"
+
+
+def _torch_matrix_grads(a, b, G, axis_t, reverse):
+    import torch
+    ta = torch.tensor(a, dtype=torch.float64, requires_grad=True)
+    tb = torch.tensor(b, dtype=torch.float64, requires_grad=True)
+    T = a.shape[axis_t]
+    h = torch.zeros(b.shape[0], *b.shape[2:], dtype=torch.float64)
+    outs = [None] * T
+    for t in (range(T - 1, -1, -1) if reverse else range(T)):
+        h = ta[:, t] @ h + tb[:, t]
+        outs[t] = h
+    (torch.stack(outs, 1) * torch.tensor(G, dtype=torch.float64)).sum().backward()
+    return ta.grad.numpy(), tb.grad.numpy()
+
+
+def pin_backward_matches_autograd(M):
+    rng = _rng(21)
+    L, T, n, m = 2, 11, 4, 3
+    a = (rng.standard_normal((L, T, n, n)) * 0.45).astype(f32)
+    b = rng.standard_normal((L, T, n, m)).astype(f32)
+    for reverse in (False, True):
+        G = rng.standard_normal((L, T, n, m)).astype(f32)
+        h = M.matrix_scan(a, b, axis=1, reverse=reverse)
+        da, db = M.matrix_scan_backward(a, b, h, G, axis=1, reverse=reverse)
+        wa, wb = _torch_matrix_grads(a, b, G, 1, reverse)
+        for got, want, nm in ((da, wa, "da"), (db, wb, "db")):
+            err = np.abs(got - want) / (1.0 + np.abs(want))
+            assert float(err.max()) < 1e-5, "%s reverse=%s: %g" % (nm, reverse, float(err.max()))
+
+
+def pin_backward_linear_scan(M):
+    rng = _rng(22)
+    T, c = 40, 0.8
+    a = np.full((2, T), c, f32)
+    b = rng.standard_normal((2, T)).astype(f32)
+    G = rng.standard_normal((2, T)).astype(f32)
+    h = M.linear_scan(a, b, axis=1)
+    da, db = M.linear_scan_backward(a, b, h, G, axis=1)
+    want = np.flip(scipy.signal.lfilter([1.0], [1.0, -float(f32(c))], np.flip(G.astype(np.float64), 1), axis=1), 1)
+    assert np.allclose(db, want, rtol=1e-5, atol=1e-5), "linear-scan cotangent"
+    hp = np.concatenate([np.zeros((2, 1), f32), h[:, :-1]], axis=1)
+    assert np.array_equal(_bits(da), _bits(np.multiply(db, hp, dtype=f32))), "da[t] = lam[t] h[t-1]"
+
+
+def pin_backward_structure(M):
+    rng = _rng(23)
+    a = (rng.standard_normal((3, 8, 2, 3, 3)) * 0.5).astype(f32)
+    b = rng.standard_normal((3, 8, 2, 3, 2)).astype(f32)
+    G = rng.standard_normal(b.shape).astype(f32)
+    h = M.matrix_scan(a, b, axis=1)
+    da, db = M.matrix_scan_backward(a, b, h, G, axis=1)
+    # reverse = flip-backward-flip
+    hr = M.matrix_scan(np.flip(a, 1), np.flip(b, 1), axis=1, reverse=True)
+    ra, rb = M.matrix_scan_backward(np.flip(a, 1), np.flip(b, 1), hr, np.flip(G, 1), axis=1, reverse=True)
+    assert np.array_equal(_bits(np.flip(ra, 1)), _bits(da)) and np.array_equal(_bits(np.flip(rb, 1)), _bits(db))
+    # axis placement
+    ma, mb = M.matrix_scan_backward(np.moveaxis(a, 1, 0), np.moveaxis(b, 1, 0), np.moveaxis(h, 1, 0),
+                                    np.moveaxis(G, 1, 0), axis=0)
+    assert np.array_equal(_bits(np.moveaxis(ma, 0, 1)), _bits(da))
+    # no state gradient, no gradient
+    za, zb = M.matrix_scan_backward(a, b, h, np.zeros_like(G), axis=1)
+    assert not np.any(za) and not np.any(zb)
+    # refused: a projective scan, broadcast operands
+    for kw, aa in (({"projective": True}, a), ({}, a[:1])):
+        try:
+            M.matrix_scan_backward(aa, b, h, G, axis=1, **kw)
+        except ValueError:
+            continue
+        raise AssertionError("the backward accepted %s" % kw)
+
+
 ALL_PINS = [
+    pin_backward_identity_is_reverse_running_sum,
+    pin_backward_matches_autograd,
+    pin_backward_linear_scan,
+    pin_backward_structure,
     pin_identity_is_running_sum,
     pin_matches_f64_matmul_loop,
     pin_delta_rule_stores_values,

@@ -29,6 +29,17 @@ MUTATIONS = [
     ("broadcast_to_first_lane", "a = np.broadcast_to(a, lead + (n, n))",
      "a = np.broadcast_to(a.reshape((-1, n, n))[:1].reshape((1,) * len(lead) + (n, n)), lead + (n, n))", 0),
     ("n_limit_dropped", "if n > 16:", "if n > 64:", 0),
+    ("bwd_not_transposed", "aT = np.ascontiguousarray(np.swapaxes(am[tn], 1, 2)) if 0 <= tn < T else zero_a",
+     "aT = np.ascontiguousarray(am[tn]) if 0 <= tn < T else zero_a", 0),
+    ("bwd_a_not_shifted", "tn = t - 1 if reverse else t + 1", "tn = t", 0),
+    ("bwd_g_scaled", "lam = np.add(_product(aT, lam), gm[t], dtype=np.float32)",
+     "lam = np.add(_product(aT, lam), gm[t] * np.float32(0.5), dtype=np.float32)", 0),
+    ("bwd_h_not_previous", "tp = t + 1 if reverse else t - 1", "tp = t", 0),
+    ("bwd_da_transposed", "da[t] = _outer_sum(lam, hp)", "da[t] = np.swapaxes(_outer_sum(lam, hp), 1, 2)", 0),
+    ("bwd_wrong_direction", "order = range(T) if reverse else range(T - 1, -1, -1)",
+     "order = range(T - 1, -1, -1) if reverse else range(T)", 0),
+    ("bwd_projective_allowed", "    if projective:\n        raise", "    if False:\n        raise", 0),
+    ("bwd_last_k_dropped", "for k in range(1, m):", "for k in range(1, m - 1 if m > 1 else 1):", 0),
     ("linear_scan_swapped", "r = matrix_scan(np.broadcast_to(a, shape)[..., None, None], np.broadcast_to(b, shape)[..., None, None],",
      "r = matrix_scan(np.broadcast_to(b, shape)[..., None, None], np.broadcast_to(a, shape)[..., None, None],", 0),
 ]
