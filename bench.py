@@ -627,9 +627,10 @@ def table_config(w):
             "l2": "no flush: symbols and states (%.2f GB) exceed the 129 MB L2" % (alg / 1e9)}
 
 
-def matrix_config(w):
-    alg = w.algorithmic_bytes()
-    return {"workload": w.name, "pass": "forward", "op": "linear-scan" if w.kind == "linear" else "matrix-scan",
+def matrix_config(w, backward=False):
+    alg = w.backward_algorithmic_bytes() if backward else w.algorithmic_bytes()
+    return {"workload": w.name + (" (backward pass)" if backward else ""),
+            "pass": "backward" if backward else "forward", "op": "linear-scan" if w.kind == "linear" else "matrix-scan",
             "a_shape": list(w.a_shape), "b_shape": list(w.b_shape), "axis": w.axis, "n": w.n, "m": w.m,
             "projective": w.projective, "workspace": getattr(w, "workspace", False),
             "directions": ["reverse" if r else "forward" for r in w.reverse],
@@ -659,6 +660,34 @@ def matrix_oracle(w, a, b, reverse):
     return M.matrix_scan(a, b, axis=w.axis, reverse=reverse, projective=w.projective)
 
 
+def matrix_oracle_backward(w, a, b, states, grad_out, reverse):
+    import oracle.matrix as M
+    if w.kind == "linear":
+        return M.linear_scan_backward(a, b, states, grad_out, axis=w.axis, reverse=reverse)
+    return M.matrix_scan_backward(a, b, states, grad_out, axis=w.axis, reverse=reverse)
+
+
+def matrix_backward_call(es, w, a, b, states, grad_out, grads, reverse, stream):
+    if w.kind == "linear":
+        es.linear_scan_backward(a, b, states, grad_out, axis=w.axis, reverse=reverse, grads=grads, stream=stream)
+    else:
+        es.matrix_scan_backward(a, b, states, grad_out, axis=w.axis, reverse=reverse, grads=grads, stream=stream)
+
+
+def matrix_backward_plan(es, w, reverse):
+    if w.kind == "linear":
+        return es.plan_linear_scan_backward(w.a_shape, w.b_shape, w.axis, reverse)
+    return es.plan_matrix_scan_backward(w.a_shape, w.b_shape, w.axis, reverse)
+
+
+# the backward's dominant kernels: linear-scan runs the element-scan backward
+# skeletons of its body; matrix-scan two launches (the cotangent scan on a's
+# transposes, then grad_a), timed as one call
+MATRIX_BWD_KERNEL = {"mat_tma": "k_mat_tma_bwd", "generic": "k_mat_generic_bwd",
+                     "lane_tma": "k_body_lane_bwd", "time_tma": "k_body_time_bwd"}
+KERNEL_SOURCES.update({k: ["k_matrix.cu", "es_matrix_api.cu"] for k in ("k_mat_tma_bwd", "k_mat_generic_bwd")})
+
+
 def op_sample(w, inputs, target_elems):
     """A bounded sample of an op workload for the oracle: (inputs, elements,
     description)."""
@@ -681,12 +710,31 @@ def op_oracle(w, inputs, reverse):
     return matrix_oracle(w, inputs[0], inputs[1], reverse)
 
 
-def op_cpu_rate(w, inputs, budget_s):
+def op_backward_prep(w, sample):
+    """The sample's saved states and an all-ones state gradient per
+    direction (made before any timing)."""
+    import numpy as np
+    prep = []
+    for r in w.reverse:
+        st = op_oracle(w, sample, r)
+        prep.append((st, np.ones_like(st)))
+    return prep
+
+
+def op_oracle_step(w, sample, prep, backward):
+    for k, r in enumerate(w.reverse):
+        if backward:
+            matrix_oracle_backward(w, sample[0], sample[1], prep[k][0], prep[k][1], r)
+        else:
+            op_oracle(w, sample, r)
+
+
+def op_cpu_rate(w, inputs, budget_s, backward=False):
     def run(target):
         sample, elems, desc = op_sample(w, inputs, target)
+        prep = op_backward_prep(w, sample) if backward else None
         t0 = time.perf_counter()
-        for r in w.reverse:
-            op_oracle(w, sample, r)
+        op_oracle_step(w, sample, prep, backward)
         return time.perf_counter() - t0, elems * len(w.reverse), desc
 
     target = 1 << 18
@@ -750,8 +798,22 @@ def run_ours_op(args, w):
     outs = [torch.empty(job.out_shape, device=device, dtype=dtype) for _ in w.reverse]
     stream = torch.cuda.current_stream(device)
     plans = [job.plan(r) for r in w.reverse]
+    backward = args.pass_ == "backward"
+    if backward:
+        # saved states and a state gradient per direction (untimed set-up)
+        for o, r in zip(outs, w.reverse):
+            job.call(job.inputs, o, r, stream)
+        gen = torch.Generator(device=device)
+        gen.manual_seed(1000 + rank)
+        gouts = [torch.randn(job.out_shape, generator=gen, device=device) for _ in w.reverse]
+        grads = [(torch.empty_like(job.inputs[0]), torch.empty_like(job.inputs[1])) for _ in w.reverse]
+        plans = [matrix_backward_plan(es, w, r) for r in w.reverse]
 
     def step():
+        if backward:
+            for o, g, gr, r in zip(outs, gouts, grads, w.reverse):
+                matrix_backward_call(es, w, job.inputs[0], job.inputs[1], o, g, gr, r, stream)
+            return
         for o, r in zip(outs, w.reverse):
             job.call(job.inputs, o, r, stream)
 
@@ -759,9 +821,20 @@ def run_ours_op(args, w):
     elems_step = w.elements * len(w.reverse)
     value = sum_over_ranks(dist, float(elems_step * args.steps), device) / (region_ms / 1e3)
     kernel_ms = sum(per_step_ms) / len(per_step_ms) / len(w.reverse)
-    kernel = job.kernels.get(plans[0]["path"], plans[0]["path"])
-    roofline = roofline_of(kernel, w.name, w.algorithmic_bytes(), kernel_ms)
-    if plans[0]["path"] == "mat_chunked":
+    if backward:
+        kernel = MATRIX_BWD_KERNEL.get(plans[0]["path"], plans[0]["path"])
+        roofline = roofline_of(kernel, w.name + "_backward", w.backward_algorithmic_bytes(), kernel_ms)
+        if w.kind != "linear":
+            roofline["kernel"] = "k_mat_%s (transposed) + k_mat_da" % ("tma" if plans[0]["path"] == "mat_tma"
+                                                                      else "generic")
+            roofline["note"] = ("a call of two launches timed as one: the cotangent scan on a's transposes, then "
+                                "grad_a from the cotangent and the saved states; the cotangent is written and read "
+                                "again, so its DRAM traffic is about (2n^2 + 4nm) / (2n^2 + 3nm) of the "
+                                "algorithmic bytes")
+    else:
+        kernel = job.kernels.get(plans[0]["path"], plans[0]["path"])
+        roofline = roofline_of(kernel, w.name, w.algorithmic_bytes(), kernel_ms)
+    if not backward and plans[0]["path"] == "mat_chunked":
         # three launches make one call: `achieved` is the whole call's
         # algorithmic bytes over its time (the final pass alone is ~60%)
         roofline["kernel"] = "k_mat_chunk_local + k_mat_chunk_carry + k_mat_chunk_final"
@@ -775,8 +848,30 @@ def run_ours_op(args, w):
         out_h = [torch.empty(job.out_shape, dtype=dtype).pin_memory() for _ in w.reverse]
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
 
+        h2d = sum(t.numel() for t in hosts) * 4 * len(w.reverse)
+        d2h = sum(o.numel() for o in out_h) * 4
+        if backward:
+            states_h = [o.cpu().pin_memory() for o in outs]
+            gout_h = [g.cpu().pin_memory() for g in gouts]
+            grads_h = [(torch.empty(job.inputs[0].shape).pin_memory(), torch.empty(job.inputs[1].shape).pin_memory())
+                       for _ in w.reverse]
+            h2d = (sum(t.numel() for t in hosts) + 2 * w.elements) * 4 * len(w.reverse)
+            d2h = (job.inputs[0].numel() + job.inputs[1].numel()) * 4 * len(w.reverse)
+
         def e2e_step():
             with torch.cuda.stream(stream):
+                if backward:
+                    # inputs, saved states and state gradient in; both gradients out
+                    for sh, gh, od, gd, gr_h, gr_d, r in zip(states_h, gout_h, outs, gouts, grads_h, grads,
+                                                              w.reverse):
+                        for d, hh in zip(job.inputs, hosts):
+                            d.copy_(hh, non_blocking=True)
+                        od.copy_(sh, non_blocking=True)
+                        gd.copy_(gh, non_blocking=True)
+                        matrix_backward_call(es, w, job.inputs[0], job.inputs[1], od, gd, gr_d, r, stream)
+                        gr_h[0].copy_(gr_d[0], non_blocking=True)
+                        gr_h[1].copy_(gr_d[1], non_blocking=True)
+                    return
                 for oh, od, r in zip(out_h, outs, w.reverse):
                     for d, hh in zip(job.inputs, hosts):
                         d.copy_(hh, non_blocking=True)
@@ -785,18 +880,18 @@ def run_ours_op(args, w):
 
         e_ms = time_e2e(e2e_step, e2e_steps, stream, device, dist)
         e2e = {"value": sum_over_ranks(dist, float(elems_step * e2e_steps), device) / (e_ms / 1e3), "unit": UNIT,
-               "h2d_bytes_per_step": sum(t.numel() for t in hosts) * 4 * len(w.reverse),
-               "d2h_bytes_per_step": sum(o.numel() for o in out_h) * 4, "steps": e2e_steps,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "ms_per_step": e_ms / e2e_steps}
         del hosts, out_h
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, desc, cores = op_cpu_rate(w, job.inputs, args.cpu_budget)
+        rate, desc, cores = op_cpu_rate(w, job.inputs, args.cpu_budget, backward=backward)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
     if rank == 0:
-        config = dict(job.config(), parallelism="replicas: each GPU scans its own batch"
-                      if world > 1 else "single GPU", path=plans[0]["path"])
+        config = dict(matrix_config(w, True) if backward else job.config(),
+                      parallelism="replicas: each GPU scans its own batch" if world > 1 else "single GPU",
+                      path=plans[0]["path"])
         emit_line(args, world, value, region_ms, config, roofline, cpu, e2e, launches, clocks)
     if dist is not None:
         dist.destroy_process_group()
@@ -816,20 +911,22 @@ def run_reference_op(args, w):
     else:
         inputs = list(wl.make_matrix_inputs(w, "cpu"))
         config = matrix_config(w)
+    backward = args.pass_ == "backward"
+    if backward:
+        config = matrix_config(w, True)
     step_budget = max(0.05, min(1.0, 120.0 / max(1, args.steps + args.warmup)))
     sample, elems, _ = op_sample(w, inputs, 1 << 14)
+    prep = op_backward_prep(w, sample) if backward else None
     t0 = time.perf_counter()
-    for r in w.reverse:
-        op_oracle(w, sample, r)
+    op_oracle_step(w, sample, prep, backward)
     t_cal = time.perf_counter() - t0
     sample, elems, desc = op_sample(w, inputs, max(1, int((1 << 14) * step_budget / max(t_cal, 1e-4))))
+    prep = op_backward_prep(w, sample) if backward else None
     for _ in range(args.warmup):
-        for r in w.reverse:
-            op_oracle(w, sample, r)
+        op_oracle_step(w, sample, prep, backward)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        for r in w.reverse:
-            op_oracle(w, sample, r)
+        op_oracle_step(w, sample, prep, backward)
     dt = time.perf_counter() - t0
     elems *= len(w.reverse)
     value = elems * args.steps / dt
@@ -872,8 +969,9 @@ def main(argv=None):
         w = ops[args.workload]
         if args.trips:
             w = w.with_trips(args.trips)
-        if args.pass_ == "backward":
-            ap.error("--pass backward: only the element-scan workloads have backward kernels")
+        if args.pass_ == "backward" and (w.name in wl.TABLE_WORKLOADS or getattr(w, "workspace", False)):
+            ap.error("--pass backward: table-scan states have no gradient, and the chunked matrix-scan has no "
+                     "backward path")
         return run_reference_op(args, w) if args.impl == "reference" else run_ours_op(args, w)
     w = wl.WORKLOADS[args.workload]
     if args.trips:

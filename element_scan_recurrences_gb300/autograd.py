@@ -8,6 +8,10 @@ vector-Jacobian product over the saved states).  This module only marshals
 arguments between autograd and the library: both passes run in the CUDA
 kernels, and CPU tensors are refused (no fallback).
 
+``matrix_scan(a, b, ...)`` and ``linear_scan(a, b, ...)`` are differentiable
+the same way ("matrix-scan": the gradient is the same scan run backwards on
+a's transposes; a projective scan has none, and its backward raises).
+
 A parameter shared along time or lanes is broadcast to the sequence shape
 before the call, as the pages ask ("Arguments and body": parameters enter
 through the sequence list).  Done with ``expand`` (then made contiguous for
@@ -78,3 +82,54 @@ def element_scan(body, initial: torch.Tensor, sequences: Sequence[torch.Tensor],
         body = _program(body)
     seqs = [s.contiguous() for s in sequences]
     return _Scan.apply(body, int(axis), bool(state_axis), bool(reverse), initial.contiguous(), *seqs)
+
+
+class _MatrixScan(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, linear, axis, reverse, projective, a, b):
+        if linear:
+            out = es.linear_scan(a, b, axis=axis, reverse=reverse)
+        else:
+            out = es.matrix_scan(a, b, axis=axis, reverse=reverse, projective=projective)
+        ctx.linear, ctx.axis, ctx.reverse, ctx.projective = linear, axis, reverse, projective
+        ctx.save_for_backward(a, b, out)
+        return out
+
+    @staticmethod
+    @once_differentiable
+    def backward(ctx, grad_out):
+        a, b, out = ctx.saved_tensors
+        grad_out = grad_out.contiguous()
+        if ctx.linear:
+            ga, gb = es.linear_scan_backward(a, b, out, grad_out, axis=ctx.axis, reverse=ctx.reverse)
+        else:
+            ga, gb = es.matrix_scan_backward(a, b, out, grad_out, axis=ctx.axis, reverse=ctx.reverse,
+                                             projective=ctx.projective)
+        return None, None, None, None, ga, gb
+
+
+def _one_shape(a, b, lead_a, lead_b):
+    """Broadcast the leading dims of a and b to one shape (autograd sums a
+    broadcast operand's gradient back)."""
+    r = max(len(lead_a), len(lead_b))
+    la = [1] * (r - len(lead_a)) + list(lead_a)
+    lb = [1] * (r - len(lead_b)) + list(lead_b)
+    lead = [y if x == 1 else x for x, y in zip(la, lb)]
+    a = a.reshape(la + list(a.shape[len(lead_a):])).expand(lead + list(a.shape[len(lead_a):]))
+    b = b.reshape(lb + list(b.shape[len(lead_b):])).expand(lead + list(b.shape[len(lead_b):]))
+    return a.contiguous(), b.contiguous()
+
+
+def matrix_scan(a: torch.Tensor, b: torch.Tensor, axis: int = 0, reverse: bool = False,
+                projective: bool = False) -> torch.Tensor:
+    """The states of a matrix-scan, differentiable with respect to a and b
+    (leading dims broadcast first, so autograd sums a shared operand's
+    gradient)."""
+    a, b = _one_shape(a, b, a.shape[:-2], b.shape[:-2])
+    return _MatrixScan.apply(False, int(axis), bool(reverse), bool(projective), a, b)
+
+
+def linear_scan(a: torch.Tensor, b: torch.Tensor, axis: int = 0, reverse: bool = False) -> torch.Tensor:
+    """The states of a linear-scan, differentiable with respect to a and b."""
+    a, b = _one_shape(a, b, a.shape, b.shape)
+    return _MatrixScan.apply(True, int(axis), bool(reverse), False, a, b)

@@ -35,7 +35,8 @@ EXPORTS = ("es_scan_f32", "es_plan_f32", "es_scan_backward_f32", "es_plan_backwa
            "es_plan_matrix_scan_f32", "es_linear_scan_f32", "es_plan_linear_scan_f32", "es_table_scan_i32",
            "es_plan_table_scan_i32", "es_matrix_scan_workspace_f32", "es_matrix_scan_ws_f32",
            "es_matrix_scan_static_f32", "es_scan_body_backward_f32", "es_plan_body_backward_f32",
-           "es_body_source_backward", "es_body_prepare_backward")
+           "es_body_source_backward", "es_body_prepare_backward", "es_matrix_scan_backward_f32",
+           "es_plan_matrix_scan_backward_f32", "es_linear_scan_backward_f32", "es_plan_linear_scan_backward_f32")
 
 
 class LibraryMissing(ImportError):
@@ -138,6 +139,15 @@ def lib():
         L.es_matrix_scan_ws_f32.argtypes = msig + [ctypes.c_int, P, P, ctypes.c_size_t, P]
         L.es_matrix_scan_ws_f32.restype = ctypes.c_int
         L.es_matrix_scan_static_f32.argtypes = msig + [ctypes.c_int, P, P]
+        # ..., projective, states, grad_out, grad_a, grad_b
+        L.es_matrix_scan_backward_f32.argtypes = msig + [ctypes.c_int, P, P, P, P, P]
+        L.es_matrix_scan_backward_f32.restype = ctypes.c_int
+        L.es_plan_matrix_scan_backward_f32.argtypes = msig + [ctypes.c_int, P, P, P, P, ctypes.POINTER(PlanInfo)]
+        L.es_plan_matrix_scan_backward_f32.restype = ctypes.c_int
+        L.es_linear_scan_backward_f32.argtypes = msig + [P, P, P, P, P]
+        L.es_linear_scan_backward_f32.restype = ctypes.c_int
+        L.es_plan_linear_scan_backward_f32.argtypes = msig + [P, P, P, P, ctypes.POINTER(PlanInfo)]
+        L.es_plan_linear_scan_backward_f32.restype = ctypes.c_int
         L.es_matrix_scan_static_f32.restype = ctypes.c_int
         tsig = [P, ctypes.c_int64, ctypes.c_int64, P, i64p, ctypes.c_int, ctypes.c_int, ctypes.c_int32]
         L.es_table_scan_i32.argtypes = tsig + [P, P]
@@ -698,6 +708,79 @@ def linear_scan(a, b, axis: int = 0, reverse: bool = False, out=None, stream=Non
     _check(lib().es_linear_scan_f32(a.data_ptr(), sa, ra, b.data_ptr(), sb, rb, int(axis), int(bool(reverse)),
                                     out.data_ptr(), handle))
     return out
+
+
+def plan_matrix_scan_backward(a_shape, b_shape, axis: int = 0, reverse: bool = False, projective: bool = False,
+                              ptrs: Optional[Sequence[int]] = None) -> dict:
+    """Validate and plan a matrix-scan backward without a GPU.  ``ptrs`` =
+    (a, b, states, grad_out, grad_a, grad_b)."""
+    if ptrs is None:
+        ptrs = [(k + 1) << 44 for k in range(6)]
+    sa, ra = _shape_array(a_shape)
+    sb, rb = _shape_array(b_shape)
+    info = PlanInfo()
+    _check(lib().es_plan_matrix_scan_backward_f32(ptrs[0], sa, ra, ptrs[1], sb, rb, int(axis), int(bool(reverse)),
+                                                  int(bool(projective)), ptrs[2], ptrs[3], ptrs[4], ptrs[5],
+                                                  ctypes.byref(info)))
+    return _info(info)
+
+
+def _backward_args(a, b, states, grad_out, grads):
+    import torch
+    for t, nm in ((a, "a"), (b, "b"), (states, "states"), (grad_out, "grad_out")):
+        _require_cuda_f32(t, nm)
+    if list(grad_out.shape) != list(states.shape):
+        raise EsError(1, "grad_out shape %s does not match the states %s" % (list(grad_out.shape),
+                                                                             list(states.shape)))
+    if grads is None:
+        grads = (torch.empty_like(a), torch.empty_like(b))
+    for t in grads:
+        _require_cuda_f32(t, "gradient buffer")
+    return grads
+
+
+def matrix_scan_backward(a, b, states, grad_out, axis: int = 0, reverse: bool = False, projective: bool = False,
+                         grads=None, stream=None):
+    """Gradients (grad_a, grad_b) of sum(grad_out * matrix_scan(a, b)) on CUDA
+    tensors, from the forward's states; ``grads`` may supply the buffers."""
+    import torch
+    ga, gb = _backward_args(a, b, states, grad_out, grads)
+    sa, ra = _shape_array(a.shape)
+    sb, rb = _shape_array(b.shape)
+    if stream is None:
+        stream = torch.cuda.current_stream(b.device)
+    handle = stream if isinstance(stream, int) else stream.cuda_stream
+    _check(lib().es_matrix_scan_backward_f32(a.data_ptr(), sa, ra, b.data_ptr(), sb, rb, int(axis),
+                                             int(bool(reverse)), int(bool(projective)), states.data_ptr(),
+                                             grad_out.data_ptr(), ga.data_ptr(), gb.data_ptr(), handle))
+    return ga, gb
+
+
+def plan_linear_scan_backward(a_shape, b_shape, axis: int = 0, reverse: bool = False,
+                              ptrs: Optional[Sequence[int]] = None) -> dict:
+    if ptrs is None:
+        ptrs = [(k + 1) << 44 for k in range(6)]
+    sa, ra = _shape_array(a_shape)
+    sb, rb = _shape_array(b_shape)
+    info = PlanInfo()
+    _check(lib().es_plan_linear_scan_backward_f32(ptrs[0], sa, ra, ptrs[1], sb, rb, int(axis), int(bool(reverse)),
+                                                  ptrs[2], ptrs[3], ptrs[4], ptrs[5], ctypes.byref(info)))
+    return _info(info)
+
+
+def linear_scan_backward(a, b, states, grad_out, axis: int = 0, reverse: bool = False, grads=None, stream=None):
+    """Gradients (grad_a, grad_b) of a linear-scan whose a and b share one shape."""
+    import torch
+    ga, gb = _backward_args(a, b, states, grad_out, grads)
+    sa, ra = _shape_array(a.shape)
+    sb, rb = _shape_array(b.shape)
+    if stream is None:
+        stream = torch.cuda.current_stream(b.device)
+    handle = stream if isinstance(stream, int) else stream.cuda_stream
+    _check(lib().es_linear_scan_backward_f32(a.data_ptr(), sa, ra, b.data_ptr(), sb, rb, int(axis),
+                                             int(bool(reverse)), states.data_ptr(), grad_out.data_ptr(),
+                                             ga.data_ptr(), gb.data_ptr(), handle))
+    return ga, gb
 
 
 # ---------------------------------------------------------------------------

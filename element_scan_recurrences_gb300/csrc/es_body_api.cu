@@ -468,12 +468,12 @@ struct BodyBwdCall {
 es_status plan_body_backward(es_body_t body, const float* initial, const float* const* seqs, int n_seqs,
                              const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
                              int reverse, const float* states, const float* grad_out, const float* grad_initial,
-                             float* const* grad_seqs, BodyBwdCall* B) {
+                             float* const* grad_seqs, BodyBwdCall* B, bool zero_initial = false) {
     static const char* const kFn = "es_scan_body_backward_f32";
     // the forced-path check comes after the plan (any forward path is fine)
     BodyCall& C = B->C;
     es_status st = plan_body(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths, reverse, states,
-                             &C);
+                             &C, zero_initial);
     if (st != ES_OK) return st;
     if ((st = functor_for(body, static_cast<int>(C.S.W), C.vector, C.wide_mask, &B->functor, true)) != ES_OK)
         return st;
@@ -485,7 +485,8 @@ es_status plan_body_backward(es_body_t body, const float* initial, const float* 
         C.path = ES_PATH_EMPTY;
         return ES_OK;
     }
-    if (grad_out == nullptr || grad_initial == nullptr || grad_seqs == nullptr)
+    // from zero (an internal caller): no initial and no initial gradient
+    if (grad_out == nullptr || (grad_initial == nullptr) != zero_initial || grad_seqs == nullptr)
         return api_fail(ES_E_ARG, "%s: null gradient pointer", kFn);
     for (int k = 0; k < n_seqs; ++k)
         if (grad_seqs[k] == nullptr) return api_fail(ES_E_ARG, "%s: null gradient pointer", kFn);
@@ -505,9 +506,10 @@ es_status plan_body_backward(es_body_t body, const float* initial, const float* 
         if (reinterpret_cast<uintptr_t>(ptr[k]) % 4 != 0)
             return api_fail(ES_E_ARG, "%s: `%s` is not 4-byte aligned", kFn, nm[k].c_str());
     for (int k = n_seqs + 3; k < nb; ++k) {
+        if (ptr[k] == nullptr) continue;        // no initial gradient (a scan from zero)
         const uintptr_t lo = reinterpret_cast<uintptr_t>(ptr[k]), hi = lo + static_cast<uintptr_t>(cnt[k]) * 4;
         for (int q = 0; q < nb; ++q) {
-            if (q == k) continue;
+            if (q == k || ptr[q] == nullptr) continue;
             const uintptr_t l2 = reinterpret_cast<uintptr_t>(ptr[q]), h2 = l2 + static_cast<uintptr_t>(cnt[q]) * 4;
             if (lo < h2 && l2 < hi)
                 return api_fail(ES_E_ARG, "%s: `%s` overlaps `%s`", kFn, nm[k].c_str(), nm[q].c_str());
@@ -827,12 +829,8 @@ es_status es_plan_body_backward_f32(es_body_t body, const float* initial, const 
                                     const int64_t* seq_widths, int reverse, const float* states,
                                     const float* grad_out, const float* grad_initial, float* const* grad_seqs,
                                     es_plan_info* info) {
-    es::BodyBwdCall B{};
-    es_status st = es::plan_body_backward(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths,
-                                          reverse, states, grad_out, grad_initial, grad_seqs, &B);
-    if (st != ES_OK) return st;
-    es::fill_info(B.C, info);
-    return ES_OK;
+    return es::plan_body_backward_impl(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths,
+                                       reverse, states, grad_out, grad_initial, grad_seqs, info, false);
 }
 
 es_status es_scan_body_backward_f32(es_body_t body, const float* initial, const float* const* seqs, int n_seqs,
@@ -840,9 +838,36 @@ es_status es_scan_body_backward_f32(es_body_t body, const float* initial, const 
                                     const int64_t* seq_widths, int reverse, const float* states,
                                     const float* grad_out, float* grad_initial, float* const* grad_seqs,
                                     es_stream_t stream) {
+    return es::scan_body_backward_impl(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths,
+                                       reverse, states, grad_out, grad_initial, grad_seqs,
+                                       reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+}  // extern "C"
+
+namespace es {
+
+es_status plan_body_backward_impl(es_body_t body, const float* initial, const float* const* seqs, int n_seqs,
+                                  const int64_t* shape, int rank, int axis, int state_width,
+                                  const int64_t* seq_widths, int reverse, const float* states, const float* grad_out,
+                                  const float* grad_initial, float* const* grad_seqs, es_plan_info* info,
+                                  bool zero_initial) {
+    BodyBwdCall B{};
+    es_status st = plan_body_backward(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths,
+                                      reverse, states, grad_out, grad_initial, grad_seqs, &B, zero_initial);
+    if (st != ES_OK) return st;
+    fill_info(B.C, info);
+    return ES_OK;
+}
+
+es_status scan_body_backward_impl(es_body_t body, const float* initial, const float* const* seqs, int n_seqs,
+                                  const int64_t* shape, int rank, int axis, int state_width,
+                                  const int64_t* seq_widths, int reverse, const float* states, const float* grad_out,
+                                  float* grad_initial, float* const* grad_seqs, cudaStream_t stream,
+                                  bool zero_initial) {
     es::BodyBwdCall B{};
     es_status st = es::plan_body_backward(body, initial, seqs, n_seqs, shape, rank, axis, state_width, seq_widths,
-                                          reverse, states, grad_out, grad_initial, grad_seqs, &B);
+                                          reverse, states, grad_out, grad_initial, grad_seqs, &B, zero_initial);
     if (st != ES_OK) return st;
     if (B.C.path == ES_PATH_EMPTY) return ES_OK;
     int dev = 0;
@@ -850,7 +875,7 @@ es_status es_scan_body_backward_f32(es_body_t body, const float* initial, const 
     if ((st = es::api_device(&dev, &ds)) != ES_OK) return st;
     std::string err;
     bool ok;
-    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const cudaStream_t s = stream;
     if (B.C.path != ES_PATH_GENERIC) {
         es::EncodeTiledFn encode = nullptr;
         if ((st = es::api_encoder(&encode)) != ES_OK) return st;
@@ -870,6 +895,10 @@ es_status es_scan_body_backward_f32(es_body_t body, const float* initial, const 
     es::count_launch();
     return ES_OK;
 }
+
+}  // namespace es
+
+extern "C" {
 
 uint64_t es_body_compile_count(void) { return es::jit_compile_count(); }
 

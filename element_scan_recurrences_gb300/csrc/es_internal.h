@@ -99,6 +99,20 @@ es_status plan_body_impl(struct es_body_program* body, const float* initial, con
                          const int64_t* shape, int rank, int axis, int state_width, const int64_t* seq_widths,
                          int reverse, const float* out, es_plan_info* info, bool zero_initial);
 
+// Gradients of a body-program scan (es_scan_body_backward_f32); with
+// `zero_initial` the forward started from zero: `initial` and
+// `grad_initial` are null.
+es_status scan_body_backward_impl(struct es_body_program* body, const float* initial, const float* const* seqs, int n_seqs,
+                                  const int64_t* shape, int rank, int axis, int state_width,
+                                  const int64_t* seq_widths, int reverse, const float* states, const float* grad_out,
+                                  float* grad_initial, float* const* grad_seqs, cudaStream_t stream,
+                                  bool zero_initial);
+es_status plan_body_backward_impl(struct es_body_program* body, const float* initial, const float* const* seqs, int n_seqs,
+                                  const int64_t* shape, int rank, int axis, int state_width,
+                                  const int64_t* seq_widths, int reverse, const float* states, const float* grad_out,
+                                  const float* grad_initial, float* const* grad_seqs, es_plan_info* info,
+                                  bool zero_initial);
+
 // Each launcher enqueues exactly one kernel; it returns cudaSuccess or the
 // launch error.  `err` receives a message for non-CUDA failures (tensor-map
 // encoding).

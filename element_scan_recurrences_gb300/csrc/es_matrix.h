@@ -27,6 +27,8 @@ struct MatLaunch {
     int gp;              // threads per lane group: a power of two >= the columns carried
     bool projective;
     int reverse;
+    bool trans;          // the gradient's cotangent scan: a[t + a_shift]^T (zero off the axis)
+    int a_shift;
     MatGeom g;           // any layout (generic kernel)
     int64_t O, T, J;     // dense canonical view [O, T, J] of the leading dims (TMA kernel)
     unsigned int* status;
@@ -38,6 +40,11 @@ struct MatLaunch {
 };
 
 cudaError_t launch_mat_generic(const MatLaunch& L);
+
+// da[t] = lam[t] @ h_prev^T over the dense view [O, T, J] of n x m blocks
+// (h_prev: the state before trip t in scan order, zero before the first).
+cudaError_t launch_mat_da(const float* lam, const float* states, float* da, int n, int64_t O, int64_t T,
+                          int64_t J, int m, int reverse, cudaStream_t stream);
 cudaError_t launch_mat_tma(const MatLaunch& L, const char** err);
 
 // The chunked scan for few long lanes (three launches, a caller workspace):

@@ -265,6 +265,85 @@ bool same_shape(const int64_t* a_shape, int a_rank, const int64_t* b_shape, int 
     return true;
 }
 
+bool overlaps(const void* p, int64_t n, const void* q, int64_t k) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return a < b + static_cast<uintptr_t>(k) * 4 && b < a + static_cast<uintptr_t>(n) * 4;
+}
+
+// ---------------------------------------------------------------------------
+// gradients ("matrix-scan": "its gradient is the same scan run backwards on
+// a's transposes"; a projective scan "has no gradient")
+//
+// The cotangent lam[t] = a[t+1]^T lam[t+1] + g[t] (a reverse scan: a[t-1],
+// lam[t-1]) is the matrix-scan kernel run in the opposite direction on the
+// state gradients with the transposed coefficient one trip off (the zero
+// matrix past the end); it is db.  A second kernel forms
+// da[t] = lam[t] h[t-1]^T from it and the saved states.
+
+struct MatBwdPlan {
+    MatPlan P;           // the cotangent scan: b = grad_out, out = grad_b
+    const float* states;
+    float* grad_a;
+};
+
+es_status plan_matrix_backward(const char* fn, const float* a, const int64_t* a_shape, int a_rank, const float* b,
+                               const int64_t* b_shape, int b_rank, int axis, int reverse, int projective,
+                               const float* states, const float* grad_out, const float* grad_a,
+                               const float* grad_b, MatBwdPlan* Q) {
+    if (projective) return api_fail(ES_E_ARG, "%s: a projective matrix-scan has no gradient", fn);
+    MatPlan& P = Q->P;
+    es_status st = plan_matrix(fn, a, a_shape, a_rank, b, b_shape, b_rank, axis, reverse, 0, states, false, &P);
+    if (st != ES_OK) return st;
+    if (!P.dense)
+        return api_fail(ES_E_UNSUPPORTED,
+                        "%s: a %s and b %s: the gradient wants one leading shape (broadcast the operands first)", fn,
+                        dims_str(a_shape, a_rank).c_str(), dims_str(b_shape, b_rank).c_str());
+    Q->states = states;
+    Q->grad_a = const_cast<float*>(grad_a);
+    if (P.empty) return ES_OK;
+    if (grad_out == nullptr || grad_a == nullptr || grad_b == nullptr)
+        return api_fail(ES_E_ARG, "%s: null gradient pointer", fn);
+    const void* buf[6] = {a, b, states, grad_out, grad_a, grad_b};
+    const int64_t cnt[6] = {P.n_a, P.n_b, P.n_out, P.n_out, P.n_a, P.n_b};
+    const char* nm[6] = {"a", "b", "states", "grad_out", "grad_a", "grad_b"};
+    for (int k = 3; k < 6; ++k)
+        if (reinterpret_cast<uintptr_t>(buf[k]) % 4 != 0)
+            return api_fail(ES_E_ARG, "%s: `%s` is not 4-byte aligned", fn, nm[k]);
+    for (int k = 4; k < 6; ++k)
+        for (int q = 0; q < 6; ++q)
+            if (q != k && overlaps(buf[k], cnt[k], buf[q], cnt[q]))
+                return api_fail(ES_E_ARG, "%s: `%s` overlaps `%s`", fn, nm[k], nm[q]);
+    // the cotangent scan
+    MatLaunch& L = P.L;
+    L.b = grad_out;
+    L.out = const_cast<float*>(grad_b);
+    L.trans = true;
+    L.a_shift = reverse ? -1 : 1;       // the trip after t in the forward's order
+    L.reverse = reverse ? 0 : 1;        // the opposite direction
+    const bool tma = mat_tma_ok(L.n, L.m, L.gp, false, L.O, L.T, L.J, true, L.a, L.b) &&
+                     reinterpret_cast<uintptr_t>(L.out) % 16 == 0;
+    const int forced = api_path_override();
+    if (forced == ES_PATH_AUTO) {
+        P.path = tma ? ES_PATH_MAT_TMA : ES_PATH_GENERIC;
+        return ES_OK;
+    }
+    if (forced == ES_PATH_GENERIC || (forced == ES_PATH_MAT_TMA && tma)) {
+        P.path = forced;
+        return ES_OK;
+    }
+    return api_fail(ES_E_UNSUPPORTED, "%s: the forced kernel path %d cannot serve this call", fn, forced);
+}
+
+es_status launch_matrix_backward(const char* fn, MatBwdPlan* Q, int reverse, cudaStream_t stream) {
+    es_status st = launch_matrix(fn, &Q->P, stream);
+    if (st != ES_OK) return st;
+    const MatLaunch& L = Q->P.L;
+    cudaError_t e = launch_mat_da(L.out, Q->states, Q->grad_a, L.n, L.O, L.T, L.J, L.m, reverse ? 1 : 0, stream);
+    if (e != cudaSuccess) return api_fail(ES_E_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+    count_launch();
+    return ES_OK;
+}
+
 }  // namespace
 }  // namespace es
 
@@ -407,6 +486,66 @@ es_status es_linear_scan_f32(const float* a, const int64_t* a_shape, int a_rank,
     }
     if ((st = es::choose_matrix_path("es_linear_scan_f32", &P)) != ES_OK) return st;
     return es::launch_matrix("es_linear_scan_f32", &P, reinterpret_cast<cudaStream_t>(stream));
+}
+
+es_status es_plan_matrix_scan_backward_f32(const float* a, const int64_t* a_shape, int a_rank, const float* b,
+                                           const int64_t* b_shape, int b_rank, int axis, int reverse, int projective,
+                                           const float* states, const float* grad_out, const float* grad_a,
+                                           const float* grad_b, es_plan_info* info) {
+    es::MatBwdPlan Q{};
+    es_status st = es::plan_matrix_backward("es_matrix_scan_backward_f32", a, a_shape, a_rank, b, b_shape, b_rank,
+                                            axis, reverse, projective, states, grad_out, grad_a, grad_b, &Q);
+    if (st != ES_OK) return st;
+    es::fill_matrix_info(Q.P, info);
+    if (info != nullptr) info->reverse = reverse ? 1 : 0;
+    return ES_OK;
+}
+
+es_status es_matrix_scan_backward_f32(const float* a, const int64_t* a_shape, int a_rank, const float* b,
+                                      const int64_t* b_shape, int b_rank, int axis, int reverse, int projective,
+                                      const float* states, const float* grad_out, float* grad_a, float* grad_b,
+                                      es_stream_t stream) {
+    const char* fn = "es_matrix_scan_backward_f32";
+    es::MatBwdPlan Q{};
+    es_status st = es::plan_matrix_backward(fn, a, a_shape, a_rank, b, b_shape, b_rank, axis, reverse, projective,
+                                            states, grad_out, grad_a, grad_b, &Q);
+    if (st != ES_OK || Q.P.empty) return st;
+    return es::launch_matrix_backward(fn, &Q, reverse, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// linear-scan's gradient is the element-scan backward of its body, from zero
+static es_status linear_backward(bool plan_only, const float* a, const int64_t* a_shape, int a_rank, const float* b,
+                                 const int64_t* b_shape, int b_rank, int axis, int reverse, const float* states,
+                                 const float* grad_out, float* grad_a, float* grad_b, es_plan_info* info,
+                                 cudaStream_t stream) {
+    const char* fn = "es_linear_scan_backward_f32";
+    if (a_shape == nullptr || b_shape == nullptr) return es::api_fail(ES_E_ARG, "%s: null shape", fn);
+    if (!es::same_shape(a_shape, a_rank, b_shape, b_rank))
+        return es::api_fail(ES_E_UNSUPPORTED,
+                            "%s: a %s and b %s: the gradient wants one shape (broadcast the operands first)", fn,
+                            es::dims_str(a_shape, a_rank).c_str(), es::dims_str(b_shape, b_rank).c_str());
+    const float* seqs[2] = {a, b};
+    float* gseqs[2] = {grad_a, grad_b};
+    if (plan_only)
+        return es::plan_body_backward_impl(es::linear_body(), nullptr, seqs, 2, a_shape, a_rank, axis, 0, nullptr,
+                                           reverse, states, grad_out, nullptr, gseqs, info, true);
+    return es::scan_body_backward_impl(es::linear_body(), nullptr, seqs, 2, a_shape, a_rank, axis, 0, nullptr,
+                                       reverse, states, grad_out, nullptr, gseqs, stream, true);
+}
+
+es_status es_plan_linear_scan_backward_f32(const float* a, const int64_t* a_shape, int a_rank, const float* b,
+                                           const int64_t* b_shape, int b_rank, int axis, int reverse,
+                                           const float* states, const float* grad_out, const float* grad_a,
+                                           const float* grad_b, es_plan_info* info) {
+    return linear_backward(true, a, a_shape, a_rank, b, b_shape, b_rank, axis, reverse, states, grad_out,
+                           const_cast<float*>(grad_a), const_cast<float*>(grad_b), info, nullptr);
+}
+
+es_status es_linear_scan_backward_f32(const float* a, const int64_t* a_shape, int a_rank, const float* b,
+                                      const int64_t* b_shape, int b_rank, int axis, int reverse, const float* states,
+                                      const float* grad_out, float* grad_a, float* grad_b, es_stream_t stream) {
+    return linear_backward(false, a, a_shape, a_rank, b, b_shape, b_rank, axis, reverse, states, grad_out, grad_a,
+                           grad_b, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

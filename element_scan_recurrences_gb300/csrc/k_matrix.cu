@@ -93,10 +93,12 @@ __device__ __forceinline__ float group_max_abs(float v, int gp, unsigned mask) {
 // ---------------------------------------------------------------------------
 // any layout
 
-template <int N, bool PROJ>
+// TRANS (the gradient's cotangent scan): the step's coefficient is
+// a[t + a_shift]^T, the zero matrix where t + a_shift falls outside the axis.
+template <int N, bool PROJ, bool TRANS>
 __global__ void __launch_bounds__(128)
 k_mat_generic(const float* __restrict__ a, const float* __restrict__ b, float* __restrict__ out, const MatGeom g,
-              int m, int gp, int reverse) {
+              int m, int gp, int reverse, int a_shift) {
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     // projective: a lane is a group of gp threads (columns of h, then of P);
     // else one thread per column of h
@@ -124,10 +126,17 @@ k_mat_generic(const float* __restrict__ a, const float* __restrict__ b, float* _
         const int64_t t = reverse ? g.T - 1 - s : s;
         float hn[N];
         if (live) {
-            const float* A = a + (oa + t * g.ta) * N * N;
+            const int64_t tc = t + a_shift;
+            const bool a_in = tc >= 0 && tc < g.T;
+            const float* A = a + (oa + (a_in ? tc : 0) * g.ta) * N * N;
             column_step<N>(hn, h, [&](int i, float (&r)[N]) {
 #pragma unroll
-                for (int q = 0; q < N; ++q) r[q] = __ldg(A + i * N + q);
+                for (int q = 0; q < N; ++q) {
+                    if constexpr (TRANS)
+                        r[q] = a_in ? __ldg(A + q * N + i) : 0.0f;
+                    else
+                        r[q] = __ldg(A + i * N + q);
+                }
             });
             if (is_h) {
                 const float* B = b + (ob + t * g.tb) * N * m + c;
@@ -176,11 +185,15 @@ k_mat_generic(const float* __restrict__ a, const float* __restrict__ b, float* _
 constexpr int kMatMaxStages = 4;
 constexpr int kMatConsumers = 128;
 
-template <int N, int R, bool PROJ>
+// TRANS (the gradient's cotangent scan): the step's coefficient is
+// a[t + a_shift]^T; the a tile is loaded a_shift trips off the b tile, and
+// TMA's zero fill past either end of the axis is the zero matrix.
+template <int N, int R, bool PROJ, bool TRANS>
 __global__ void __launch_bounds__(32 + kMatConsumers)
 k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
           float* __restrict__ out, int T, int J, int m, int gp, int LPC, int tiles_j, int TT, int stages,
-          int reverse, unsigned int* status, uint64_t wait_ns, int64_t drop_tile) {
+          int reverse, int a_shift, unsigned int* status, uint64_t wait_ns, int64_t drop_tile) {
+    static_assert(!(PROJ && TRANS), "a projective scan has no gradient");
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMatMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kMatMaxStages];
@@ -230,7 +243,7 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
                 const int jt = reverse ? ntiles - 1 - k : k;
                 float* st = tiles + static_cast<size_t>(s) * stage_floats;
                 mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
-                tma_load_4d(st, &map_a, 0, j0, jt * TT, o, &full_bar[s], pol);
+                tma_load_4d(st, &map_a, 0, j0, jt * TT + a_shift, o, &full_bar[s], pol);
                 tma_load_4d(st + a_pad, &map_b, 0, j0, jt * TT, o, &full_bar[s], pol);
             }
             for (int k = max(0, issued - stages); k < issued; ++k) {
@@ -283,7 +296,13 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
             for (int r = 0; r < RPT; ++r) {
                 const int i = r * R + g;
                 float row[N];
-                smem_row<N>(A, i, row);
+                if constexpr (TRANS) {
+                    // column i of a: the row groups read neighbouring words
+#pragma unroll
+                    for (int j = 0; j < N; ++j) row[j] = A[j * N + i];
+                } else {
+                    smem_row<N>(A, i, row);
+                }
                 float prod[N];
 #pragma unroll
                 for (int j = 0; j < N; j += 2) mul2_rn(prod[j], prod[j + 1], row[j], row[j + 1], h[j], h[j + 1]);
@@ -325,30 +344,131 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
     }
 }
 
+// ---------------------------------------------------------------------------
+// the gradient of a: da[t] = lam[t] @ h_prev^T
+//
+// One unit is one (lane, trip) of the dense view [O, T, J]; h_prev is the
+// state before the trip in scan order (zero before the first).  Each thread
+// forms a B x B block of da, every entry the sum over k = 0..m-1 in order of
+// lam[i][k] * h_prev[j][k], each product and sum rounded (the first product
+// starts the sum).  Rows come straight from global memory (16-byte loads when
+// m is a multiple of 4); the rows a unit's threads share meet in L1.
+template <int N, int B, int KV>
+__global__ void __launch_bounds__(128)
+k_mat_da(const float* __restrict__ lam, const float* __restrict__ states, float* __restrict__ da, int64_t O,
+         int64_t T, int64_t J, int m, int reverse) {
+    constexpr int NB = N / B;
+    constexpr int TPU = NB * NB;                 // threads per unit
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t u = tid / TPU;
+    if (u >= O * T * J) return;
+    const int w = static_cast<int>(tid % TPU);
+    const int bi = w / NB, bj = w % NB;
+    const int64_t j = u % J;
+    const int64_t t = (u / J) % T;
+    const int64_t o = u / (J * T);
+    const int64_t tp = reverse ? t + 1 : t - 1;
+    const bool has_prev = tp >= 0 && tp < T;
+    const float* Lr = lam + (u * N + bi * B) * m;
+    const float* Hr = states + (((o * T + (has_prev ? tp : 0)) * J + j) * N + bj * B) * m;
+    float acc[B][B];
+    auto load = [&](const float* p, int k, float (&d)[KV]) {
+        if constexpr (KV == 4) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(p + k));
+            d[0] = v.x;
+            d[1] = v.y;
+            d[2] = v.z;
+            d[3] = v.w;
+        } else {
+            d[0] = __ldg(p + k);
+        }
+    };
+    for (int k = 0; k < m; k += KV) {
+        float lv[B][KV], hv[B][KV];
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            load(Lr + b * m, k, lv[b]);
+            if (has_prev) {
+                load(Hr + b * m, k, hv[b]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < KV; ++q) hv[b][q] = 0.0f;
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < KV; ++q) {
+#pragma unroll
+            for (int x = 0; x < B; ++x)
+#pragma unroll
+                for (int y = 0; y < B; ++y) {
+                    const float p = __fmul_rn(lv[x][q], hv[y][q]);
+                    acc[x][y] = (k + q == 0) ? p : __fadd_rn(acc[x][y], p);
+                }
+        }
+    }
+    float* D = da + u * N * N + (bi * B) * N + bj * B;
+#pragma unroll
+    for (int x = 0; x < B; ++x) {
+        if constexpr (B == 4) {
+            __stcs(reinterpret_cast<float4*>(D + x * N), make_float4(acc[x][0], acc[x][1], acc[x][2], acc[x][3]));
+        } else {
+#pragma unroll
+            for (int y = 0; y < B; ++y) __stcs(D + x * N + y, acc[x][y]);
+        }
+    }
+}
+
+template <int N>
+cudaError_t launch_da_n(const float* lam, const float* states, float* da, int64_t O, int64_t T, int64_t J, int m,
+                        int reverse, cudaStream_t stream) {
+    const int64_t units = O * T * J;
+    auto go = [&](auto kern, int tpu) {
+        const int64_t blocks = (units * tpu + 127) / 128;
+        if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        kern<<<static_cast<unsigned>(blocks), 128, 0, stream>>>(lam, states, da, O, T, J, m, reverse);
+        return cudaGetLastError();
+    };
+    const bool vec = m % 4 == 0 && reinterpret_cast<uintptr_t>(lam) % 16 == 0 &&
+                     reinterpret_cast<uintptr_t>(states) % 16 == 0;
+    if constexpr (N % 4 == 0) {
+        if (vec && reinterpret_cast<uintptr_t>(da) % 16 == 0) return go(k_mat_da<N, 4, 4>, (N / 4) * (N / 4));
+        return go(k_mat_da<N, 4, 1>, (N / 4) * (N / 4));
+    } else if constexpr (N % 2 == 0) {
+        if (vec) return go(k_mat_da<N, 2, 4>, (N / 2) * (N / 2));
+        return go(k_mat_da<N, 2, 1>, (N / 2) * (N / 2));
+    } else {
+        if (vec) return go(k_mat_da<N, 1, 4>, N * N);
+        return go(k_mat_da<N, 1, 1>, N * N);
+    }
+}
+
 template <int N>
 cudaError_t launch_generic_n(const MatLaunch& L) {
     const int gp = L.gp;
     const int64_t threads_total = L.projective ? L.g.lanes * gp : L.g.lanes * L.m;
     const int64_t blocks = (threads_total + 127) / 128;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const unsigned grid = static_cast<unsigned>(blocks);
     if (L.projective)
-        k_mat_generic<N, true><<<static_cast<unsigned>(blocks), 128, 0, L.stream>>>(L.a, L.b, L.out, L.g, L.m, gp,
-                                                                                   L.reverse);
+        k_mat_generic<N, true, false><<<grid, 128, 0, L.stream>>>(L.a, L.b, L.out, L.g, L.m, gp, L.reverse, 0);
+    else if (L.trans)
+        k_mat_generic<N, false, true><<<grid, 128, 0, L.stream>>>(L.a, L.b, L.out, L.g, L.m, gp, L.reverse,
+                                                                   L.a_shift);
     else
-        k_mat_generic<N, false><<<static_cast<unsigned>(blocks), 128, 0, L.stream>>>(L.a, L.b, L.out, L.g, L.m, gp,
-                                                                                    L.reverse);
+        k_mat_generic<N, false, false><<<grid, 128, 0, L.stream>>>(L.a, L.b, L.out, L.g, L.m, gp, L.reverse, 0);
     return cudaGetLastError();
 }
 
 template <int N, int R>
 cudaError_t launch_tma_nr(const MatLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb, int lpc, int tiles_j,
                           int TT, int stages, size_t smem) {
-    auto kern = L.projective ? k_mat_tma<N, R, true> : k_mat_tma<N, R, false>;
+    auto kern = L.projective ? k_mat_tma<N, R, true, false> : L.trans ? k_mat_tma<N, R, false, true>
+                                                                      : k_mat_tma<N, R, false, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(L.O * tiles_j), 32 + lpc * L.gp * R, smem, L.stream>>>(
         ma, mb, L.out, static_cast<int>(L.T), static_cast<int>(L.J), L.m, L.gp, lpc, tiles_j, TT, stages,
-        L.reverse, L.status, L.wait_ns, L.drop_tile);
+        L.reverse, L.trans ? L.a_shift : 0, L.status, L.wait_ns, L.drop_tile);
     return cudaGetLastError();
 }
 
@@ -397,6 +517,19 @@ bool encode_blocks(EncodeTiledFn encode, CUtensorMap* map, const float* base, in
 }
 
 }  // namespace
+
+cudaError_t launch_mat_da(const float* lam, const float* states, float* da, int n, int64_t O, int64_t T,
+                          int64_t J, int m, int reverse, cudaStream_t stream) {
+    switch (n) {
+#define ES_DA_CASE(K) \
+    case K: return launch_da_n<K>(lam, states, da, O, T, J, m, reverse, stream);
+        ES_DA_CASE(1) ES_DA_CASE(2) ES_DA_CASE(3) ES_DA_CASE(4) ES_DA_CASE(5) ES_DA_CASE(6) ES_DA_CASE(7)
+        ES_DA_CASE(8) ES_DA_CASE(9) ES_DA_CASE(10) ES_DA_CASE(11) ES_DA_CASE(12) ES_DA_CASE(13)
+        ES_DA_CASE(14) ES_DA_CASE(15) ES_DA_CASE(16)
+#undef ES_DA_CASE
+    }
+    return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_mat_generic(const MatLaunch& L) {
     switch (L.n) {

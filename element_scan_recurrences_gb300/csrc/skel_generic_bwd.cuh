@@ -97,8 +97,10 @@ k_body_generic_bwd(const SeqPtrs seqs, const float* __restrict__ init, const flo
             load(reverse ? t + 1 : t - 1, cur);
         }
     }
+    if (ginit != nullptr) {   // null: the scan started from zero and wants no initial gradient
 #pragma unroll
-    for (int w = 0; w < W; ++w) ginit[lane * W + w] = lam[w];
+        for (int w = 0; w < W; ++w) ginit[lane * W + w] = lam[w];
+    }
 }
 
 }  // namespace es

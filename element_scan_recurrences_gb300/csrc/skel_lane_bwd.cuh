@@ -183,7 +183,7 @@ k_body_lane_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
         }
     }
     if (storer) bulk_wait_all();
-    if (valid) ginit[static_cast<int64_t>(o) * I + i] = lam;
+    if (valid && ginit != nullptr) ginit[static_cast<int64_t>(o) * I + i] = lam;   // null: not wanted
 }
 
 }  // namespace es

@@ -199,7 +199,7 @@ k_body_time_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
         if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
     if (storer) bulk_wait_all();
-    if (valid) ginit[o0 + r] = lam;
+    if (valid && ginit != nullptr) ginit[o0 + r] = lam;   // null: not wanted
 }
 
 }  // namespace es

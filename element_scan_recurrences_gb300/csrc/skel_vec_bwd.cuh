@@ -216,7 +216,7 @@ k_body_vec_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const fl
         if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
     if (storer) bulk_wait_all();
-    if (valid) {
+    if (valid && ginit != nullptr) {   // null: not wanted
 #pragma unroll
         for (int e = 0; e < E; ++e) ginit[(static_cast<int64_t>(o) * J + j0 + v) * W + w0 + e] = lam[e];
     }

@@ -223,6 +223,12 @@ class MatrixWorkload:
         """f32 bytes of one launch: a and b read, the states written."""
         return 4 * (math.prod(self.a_shape) + 2 * math.prod(self.b_shape))
 
+    def backward_algorithmic_bytes(self) -> int:
+        """f32 bytes of one backward call: a, the saved states and the state
+        gradients read; the gradients of a and of b written."""
+        na, nb = math.prod(self.a_shape), math.prod(self.b_shape)
+        return 4 * (2 * na + 3 * nb)
+
     def with_trips(self, T: int, name: Optional[str] = None) -> "MatrixWorkload":
         lead = tuple(T if i == self.ax else d for i, d in enumerate(self.lead))
         return dataclasses.replace(self, lead=lead, name=name or "%s_T%d" % (self.name, T))

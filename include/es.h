@@ -420,6 +420,65 @@ es_status es_plan_linear_scan_f32(const float *a, const int64_t *a_shape, int a_
                                   int axis, int reverse, const float *out, es_plan_info *info);
 
 /*
+ * es_matrix_scan_backward_f32 -- gradients of a matrix-scan ("matrix-scan"
+ * section: its gradient is the same scan run backwards on a's transposes; a
+ * projective scan has no gradient).  With g[t] = dL/dh[t] (`grad_out`), the
+ * cotangent
+ *
+ *     lam[t] = a[t+1]^T @ lam[t+1] + g[t]    (reverse: a[t-1]^T @ lam[t-1])
+ *
+ * runs from zero in the opposite trip order, past the last trip with the
+ * zero matrix as coefficient; grad_b = lam and grad_a[t] = lam[t] @ h^T of
+ * the state before trip t (zero before the first).  Every product is the
+ * plain definition in f32: a^T's rows in order then g added; grad_a[i][j]
+ * sums lam[i][k] * h[j][k] over k = 0..m-1 in order.
+ *
+ *   a .. projective  the forward call's arguments; a and b must have one
+ *                    leading shape (no broadcasting: ES_E_UNSUPPORTED), and
+ *                    a projective scan is ES_E_ARG.
+ *   states           device f32: the forward's output.
+ *   grad_out         device f32 of the output's shape.
+ *   grad_a, grad_b   device f32 of a's and b's shapes (written); they may
+ *                    not overlap any input or each other (ES_E_ARG).
+ * Two kernels on `stream` (the cotangent scan, then grad_a); no allocation.
+ */
+es_status es_matrix_scan_backward_f32(const float *a, const int64_t *a_shape, int a_rank,
+                                      const float *b, const int64_t *b_shape, int b_rank,
+                                      int axis, int reverse, int projective,
+                                      const float *states, const float *grad_out,
+                                      float *grad_a, float *grad_b, es_stream_t stream);
+
+/* Plan of a matrix-scan backward call (validation and the cotangent scan's
+ * kernel path; no CUDA call). */
+es_status es_plan_matrix_scan_backward_f32(const float *a, const int64_t *a_shape, int a_rank,
+                                           const float *b, const int64_t *b_shape, int b_rank,
+                                           int axis, int reverse, int projective,
+                                           const float *states, const float *grad_out,
+                                           const float *grad_a, const float *grad_b,
+                                           es_plan_info *info);
+
+/*
+ * es_linear_scan_backward_f32 -- gradients of a linear-scan whose a and b
+ * have one shape (ES_E_UNSUPPORTED otherwise): lam[t] = a[t+1] * lam[t+1] +
+ * g[t] in the opposite trip order, grad_b = lam, grad_a[t] = lam[t] * h[t-1]
+ * (zero before the first trip), one product and one sum a trip, rounded.  It
+ * runs as the element-scan backward of the body (+ (* a h) b) from zero, on
+ * the element-scan backward kernels.  Arguments as for the matrix form.
+ */
+es_status es_linear_scan_backward_f32(const float *a, const int64_t *a_shape, int a_rank,
+                                      const float *b, const int64_t *b_shape, int b_rank,
+                                      int axis, int reverse, const float *states,
+                                      const float *grad_out, float *grad_a, float *grad_b,
+                                      es_stream_t stream);
+
+/* Plan of a linear-scan backward call (no CUDA call). */
+es_status es_plan_linear_scan_backward_f32(const float *a, const int64_t *a_shape, int a_rank,
+                                           const float *b, const int64_t *b_shape, int b_rank,
+                                           int axis, int reverse, const float *states,
+                                           const float *grad_out, const float *grad_a,
+                                           const float *grad_b, es_plan_info *info);
+
+/*
  * es_table_scan_i32 -- table-scan ("Tensor operations", the `table-scan` row
  * of the operations table and the section "table-scan"): a deterministic
  * automaton run along `axis` of `symbols`,

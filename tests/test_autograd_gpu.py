@@ -137,3 +137,64 @@ def test_vector_state_and_upstream_graph():
     want = np.einsum("otjk,otjn->kn", z.cpu().numpy().astype(np.float64), gx.astype(np.float64))
     err = np.abs(Wt.grad.cpu().numpy() - want) / (1 + np.abs(want))
     assert float(err.max()) <= 1e-4, float(err.max())
+
+
+def test_matrix_scan_gradients_and_shared_operand():
+    """matrix-scan through autograd: the delta rule's a and b built from
+    k, v, beta; gradients reach k, v and beta (checked against an f64 torch
+    loop), and a shared `a` (broadcast over the batch) sums its gradient."""
+    from element_scan_recurrences_gb300.autograd import matrix_scan
+    torch.manual_seed(6)
+    B, T, n, m = 2, 33, 8, 4
+    k = torch.nn.functional.normalize(torch.randn(B, T, n, device="cuda"), dim=-1).requires_grad_(True)
+    v = torch.randn(B, T, m, device="cuda", requires_grad=True)
+    beta = torch.rand(B, T, 1, 1, device="cuda", requires_grad=True)
+    eye = torch.eye(n, device="cuda")
+    a = eye - beta * k.unsqueeze(-1) * k.unsqueeze(-2)
+    b = beta * k.unsqueeze(-1) * v.unsqueeze(-2)
+    S = matrix_scan(a, b, axis=1)
+    G = torch.randn_like(S)
+    (S * G).sum().backward()
+    # the same in f64 with torch.matmul
+    k64, v64, b64 = (t.detach().double().requires_grad_(True) for t in (k, v, beta))
+    a64 = torch.eye(n, dtype=torch.float64, device="cuda") - b64 * k64.unsqueeze(-1) * k64.unsqueeze(-2)
+    bb64 = b64 * k64.unsqueeze(-1) * v64.unsqueeze(-2)
+    h = torch.zeros(B, n, m, dtype=torch.float64, device="cuda")
+    outs = []
+    for t in range(T):
+        h = a64[:, t] @ h + bb64[:, t]
+        outs.append(h)
+    (torch.stack(outs, 1) * G.double()).sum().backward()
+    for got, want, nm in ((k.grad, k64.grad, "k"), (v.grad, v64.grad, "v"), (beta.grad, b64.grad, "beta")):
+        err = (got.double() - want).abs() / (1 + want.abs())
+        assert float(err.max()) < 1e-4, (nm, float(err.max()))
+    # a shared by both sequences: its gradient is the sum of theirs
+    a1 = (torch.randn(1, T, n, n, device="cuda") * 0.3).requires_grad_(True)
+    bb = torch.randn(B, T, n, m, device="cuda")
+    out = matrix_scan(a1, bb, axis=1)
+    Gs = torch.randn_like(out)
+    (out * Gs).sum().backward()
+    A = a1.detach().expand(B, T, n, n).contiguous()
+    ga, _ = es.matrix_scan_backward(A, bb, es.matrix_scan(A, bb, axis=1), Gs.contiguous(), axis=1)
+    assert torch.allclose(a1.grad[0], ga.sum(0), rtol=1e-5, atol=1e-5)
+    # a projective scan has no gradient
+    ap = a1.detach().expand(B, T, n, n).contiguous().requires_grad_(True)
+    outp = matrix_scan(ap, bb, axis=1, projective=True)
+    with pytest.raises(es.EsError):
+        outp.sum().backward()
+
+
+def test_linear_scan_gradients():
+    from element_scan_recurrences_gb300.autograd import linear_scan
+    import oracle.matrix as M
+    rng = np.random.default_rng(7)
+    a = rng.uniform(0.5, 0.99, (3, 50, 40)).astype(np.float32)
+    b = rng.standard_normal((3, 50, 40)).astype(np.float32)
+    G = rng.standard_normal((3, 50, 40)).astype(np.float32)
+    ta, tb = _leaf(a), _leaf(b)
+    out = linear_scan(ta, tb, axis=1)
+    (out * torch.from_numpy(G).cuda()).sum().backward()
+    st = M.linear_scan(a, b, axis=1)
+    wa, wb = M.linear_scan_backward(a, b, st, G, axis=1)
+    close(ta.grad.cpu(), wa, "a", exact=True)
+    close(tb.grad.cpu(), wb, "b", exact=True)

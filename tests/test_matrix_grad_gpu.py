@@ -1,0 +1,142 @@
+"""matrix-scan and linear-scan gradients on the GPU against the gradient
+oracle (``oracle.matrix.matrix_scan_backward``), element by element.
+
+"matrix-scan": the gradient is the same scan run backwards on a's
+transposes.  The kernels form every product in the definition's order, so
+the bar is bit-identical, on the TMA and on the any-layout cotangent scan,
+forward and reverse, with ragged lane and time tiles."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.matrix as M
+from element_scan_recurrences_gb300 import binding as es
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_ready():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    es.lib()
+    yield
+    es.set_path_override("auto")
+
+
+def bitwise(got, want, what):
+    got = np.asarray(got, np.float32)
+    want = np.asarray(want, np.float32)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    bad = got.view(np.uint32) != want.view(np.uint32)
+    assert not bad.any(), "%s: %d of %d differ; first at %s: %r vs %r" % (
+        what, int(bad.sum()), bad.size, np.argwhere(bad)[0], got[bad][0], want[bad][0])
+
+
+def contractive(rng, lead, n):
+    return (rng.standard_normal(tuple(lead) + (n, n)) * (0.9 / np.sqrt(n))).astype(np.float32)
+
+
+def run_pair(a, b, axis, reverse, path, seed):
+    states = M.matrix_scan(a, b, axis=axis, reverse=reverse)
+    G = np.random.default_rng(seed).standard_normal(states.shape).astype(np.float32)
+    want = M.matrix_scan_backward(a, b, states, G, axis=axis, reverse=reverse)
+    d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    es.set_path_override(path)
+    try:
+        ga, gb = es.matrix_scan_backward(d(a), d(b), d(states), d(G), axis=axis, reverse=reverse)
+        es.device_status()
+    finally:
+        es.set_path_override("auto")
+    return (ga.cpu().numpy(), gb.cpu().numpy()), want
+
+
+@pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
+@pytest.mark.parametrize("n,m", [(16, 16), (16, 4), (8, 8), (4, 3), (2, 4), (7, 2), (1, 1), (3, 5)])
+@pytest.mark.parametrize("path", ["auto", "generic"])
+def test_matrix_backward(n, m, reverse, path):
+    rng = np.random.default_rng(n * 100 + m)
+    a = contractive(rng, (3, 37, 5), n)
+    b = rng.standard_normal((3, 37, 5, n, m)).astype(np.float32)
+    got, want = run_pair(a, b, 1, reverse, path, n + m)
+    plan = es.plan_matrix_scan_backward(a.shape, b.shape, 1, reverse)
+    if path == "auto" and n in (2, 4, 8, 16) and (n * m) % 4 == 0:
+        assert plan["path"] == "mat_tma", plan
+    bitwise(got[1], want[1], "grad_b n=%d m=%d" % (n, m))
+    bitwise(got[0], want[0], "grad_a n=%d m=%d" % (n, m))
+
+
+@pytest.mark.parametrize("axis", [0, -1])
+def test_matrix_backward_axes(axis):
+    rng = np.random.default_rng(5)
+    lead = (29, 6) if axis == 0 else (6, 29)
+    a = contractive(rng, lead, 4)
+    b = rng.standard_normal(lead + (4, 4)).astype(np.float32)
+    for reverse in (False, True):
+        got, want = run_pair(a, b, axis, reverse, "auto", 7)
+        bitwise(got[0], want[0], "grad_a axis=%d" % axis)
+        bitwise(got[1], want[1], "grad_b axis=%d" % axis)
+
+
+@pytest.mark.parametrize("T", [1, 2, 65])
+def test_matrix_backward_trip_counts(T):
+    rng = np.random.default_rng(T)
+    a = contractive(rng, (2, T, 33), 16)
+    b = rng.standard_normal((2, T, 33, 16, 16)).astype(np.float32)
+    for reverse in (False, True):
+        got, want = run_pair(a, b, 1, reverse, "auto", T)
+        bitwise(got[0], want[0], "grad_a T=%d" % T)
+        bitwise(got[1], want[1], "grad_b T=%d" % T)
+
+
+def test_matrix_backward_refusals():
+    a = torch.rand(2, 7, 4, 4, device="cuda")
+    b = torch.rand(2, 7, 4, 2, device="cuda")
+    h = es.matrix_scan(a, b, axis=1)
+    with pytest.raises(es.EsError) as e:
+        es.matrix_scan_backward(a, b, h, h.clone(), axis=1, projective=True)
+    assert e.value.status == 3
+    with pytest.raises(es.EsError) as e:
+        es.matrix_scan_backward(a[:1].contiguous(), b, h, h.clone(), axis=1)
+    assert e.value.status == 4
+    with pytest.raises(es.EsError) as e:       # a gradient written over the states
+        es.matrix_scan_backward(a, b, h, h.clone(), axis=1, grads=(torch.empty_like(a), h))
+    assert e.value.status == 3
+
+
+@pytest.mark.parametrize("shape,axis,path", [((3, 45, 40), 1, "lane_tma"), ((150, 100), -1, "time_tma"),
+                                             ((3, 45, 50), 1, "generic")])
+def test_linear_backward(shape, axis, path):
+    rng = np.random.default_rng(11)
+    a = rng.uniform(0.5, 0.99, shape).astype(np.float32)
+    b = rng.standard_normal(shape).astype(np.float32)
+    assert es.plan_linear_scan_backward(shape, shape, axis)["path"] == path
+    for reverse in (False, True):
+        states = M.linear_scan(a, b, axis=axis, reverse=reverse)
+        G = rng.standard_normal(shape).astype(np.float32)
+        wa, wb = M.linear_scan_backward(a, b, states, G, axis=axis, reverse=reverse)
+        d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+        ga, gb = es.linear_scan_backward(d(a), d(b), d(states), d(G), axis=axis, reverse=reverse)
+        es.device_status()
+        bitwise(ga.cpu(), wa, "linear grad_a %s" % path)
+        bitwise(gb.cpu(), wb, "linear grad_b %s" % path)
+
+
+def test_delta_rule_backward_full_size_sampled():
+    """The delta-rule workload's backward at full size in the bench's launch
+    configuration; sampled lanes checked bit for bit by the oracle."""
+    from element_scan_recurrences_gb300 import workloads as wl
+    w = wl.MATRIX_WORKLOADS["matrix_scan_delta_rule"]
+    a, b = wl.make_matrix_inputs(w, "cuda")
+    h = es.matrix_scan(a, b, axis=w.axis)
+    G = torch.randn(h.shape, device="cuda", generator=torch.Generator("cuda").manual_seed(3))
+    ga, gb = es.matrix_scan_backward(a, b, h, G, axis=w.axis)
+    es.device_status()
+    for o, j in ((0, 0), (w.lead[0] - 1, w.lead[2] - 1), (17, 5)):
+        sa = a[o:o + 1, :, j:j + 1].cpu().numpy()
+        sb = b[o:o + 1, :, j:j + 1].cpu().numpy()
+        sh = h[o:o + 1, :, j:j + 1].cpu().numpy()
+        sg = G[o:o + 1, :, j:j + 1].cpu().numpy()
+        wa, wb = M.matrix_scan_backward(sa, sb, sh, sg, axis=1)
+        bitwise(ga[o:o + 1, :, j:j + 1].cpu(), wa, "grad_a lane (%d, %d)" % (o, j))
+        bitwise(gb[o:o + 1, :, j:j + 1].cpu(), wb, "grad_b lane (%d, %d)" % (o, j))

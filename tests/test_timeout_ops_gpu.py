@@ -74,6 +74,26 @@ def test_matrix_scan_pipeline():
                       lambda out: np.testing.assert_array_equal(out.cpu().numpy(), want))
 
 
+def test_matrix_scan_backward_pipeline():
+    """The cotangent scan (the TMA kernel on a's transposes) gives up a
+    missing tile, then recovers."""
+    rng = np.random.default_rng(3)
+    a = (rng.standard_normal((2, 400, 8, 4, 4)) * 0.4).astype(np.float32)
+    b = rng.standard_normal((2, 400, 8, 4, 4)).astype(np.float32)
+    assert es.plan_matrix_scan_backward(a.shape, b.shape, 1)["path"] == "mat_tma"
+    h = M.matrix_scan(a, b, axis=1)
+    G = rng.standard_normal(h.shape).astype(np.float32)
+    wa, wb = M.matrix_scan_backward(a, b, h, G, axis=1)
+    d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    da, db, dh, dg = d(a), d(b), d(h), d(G)
+
+    def check(out):
+        np.testing.assert_array_equal(out[0].cpu().numpy(), wa)
+        np.testing.assert_array_equal(out[1].cpu().numpy(), wb)
+
+    drop_then_recover(lambda: es.matrix_scan_backward(da, db, dh, dg, axis=1), check)
+
+
 @pytest.mark.parametrize("shape,axis,path", [((130, 400), -1, "time_tma"), ((2, 400, 64), 1, "lane_tma")])
 def test_table_scan_pipelines(shape, axis, path):
     rng = np.random.default_rng(2)
