@@ -306,6 +306,19 @@ def cpu_oracle_rate(w, init, seqs, budget_s: float, backward: bool = False):
     return elems / t, desc, 1
 
 
+def body_live_mask(w):
+    """The sequences a body workload's backward reads (for its algorithmic
+    bytes), from the library's generated VJP; None without the library."""
+    if w.text is None:
+        return None
+    try:
+        from element_scan_recurrences_gb300 import binding as es
+        return es.Body(w.text).vjp_live_mask(w.shape[-1] if w.state_axis else 0,
+                                             w.seq_widths if w.state_axis else None)
+    except Exception:   # noqa: BLE001 -- metadata only
+        return None
+
+
 def run_reference(args, w):
     """--impl reference: the CPU oracle as the comparison arm."""
     rank, world, _ = dist_env()
@@ -357,7 +370,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config_of(w, backward),
+        "config": config_of(w, backward, body_live_mask(w) if backward else None),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample_desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -366,8 +379,8 @@ def run_reference(args, w):
     return 0
 
 
-def config_of(w, backward=False):
-    alg = w.backward_algorithmic_bytes() if backward else w.algorithmic_bytes()
+def config_of(w, backward=False, live=None):
+    alg = w.backward_algorithmic_bytes(live) if backward else w.algorithmic_bytes()
     body = w.text if w.text is not None else ["TANH_DECAY", "NORMCAP", "MAXPLUS"][w.body]
     return {"workload": w.name + (" (backward pass)" if backward else ""),
             "pass": "backward" if backward else "forward", "body": body, "shape": list(w.shape),
@@ -520,7 +533,10 @@ def run_ours(args, w):
     kernel_ms = sum(per_step_ms) / len(per_step_ms) / len(w.reverse)
 
     # roofline of the dominant kernel (every launch of a step is the same kernel)
-    alg_bytes = w.backward_algorithmic_bytes() if backward else w.algorithmic_bytes()
+    live = None
+    if backward and program is not None:
+        live = program.vjp_live_mask(w.shape[-1] if w.state_axis else 0, w.seq_widths if w.state_axis else None)
+    alg_bytes = w.backward_algorithmic_bytes(live) if backward else w.algorithmic_bytes()
     if backward:
         kernels = PATH_KERNEL_BODY_BWD if program is not None else PATH_KERNEL_BWD
     else:
@@ -582,7 +598,7 @@ def run_ours(args, w):
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
 
     if rank == 0:
-        config = dict(config_of(w, backward), parallelism="replicas: each GPU scans its own batch"
+        config = dict(config_of(w, backward, live), parallelism="replicas: each GPU scans its own batch"
                       if world > 1 else "single GPU", path=plans[0]["path"])
         emit_line(args, world, value, region_ms, config, roofline, cpu, e2e, launches, clocks)
     if dist is not None:

@@ -411,6 +411,14 @@ class Body:
                                              ctypes.byref(need)))
         return buf.value.decode()
 
+    def vjp_live_mask(self, state_width: int = 0, seq_widths=None) -> int:
+        """Bit k set when the body's vector-Jacobian product reads sequence k
+        (the others are not streamed by the backward kernels)."""
+        src = self.source_backward(state_width, seq_widths)
+        key = "kVjpSeqs = 0x"
+        at = src.index(key) + len(key)
+        return int(src[at:src.index("u", at)], 16)
+
     def prepare_backward(self, state_width: int = 0, seq_widths=None) -> None:
         """Compile ahead of time the backward kernel of a signature (no GPU needed)."""
         _check(lib().es_body_prepare_backward(self._h, int(state_width), self.n_seqs, _widths_array(seq_widths)))

@@ -10,6 +10,7 @@
 //   * ES_PATH_VEC_TMA   vector state of 2, 4, 8 or 16 values: the TMA
 //     pipeline with a lane's state over G threads (skel_vec.cuh);
 //   * ES_PATH_GENERIC   any shape or alignment (skel_generic.cuh).
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <memory>
@@ -443,10 +444,11 @@ KernelText vec_bwd_text(const std::string& functor, int W, int TT) {
                                                                std::to_string(TT) + ">"};
 }
 
-// bytes of one vector-state backward stage: every sequence's tile, the
-// shifted states' and the output gradient's
+// bytes of one vector-state backward stage: the tiles of the sequences the
+// VJP reads (n_wide, n_narrow of them), the output gradient's and TT+1 rows
+// of the saved states
 int64_t vec_bwd_stage_bytes(int W, int TT, int n_wide, int n_narrow) {
-    return vec_stage_bytes(W, TT, n_wide + 2, n_narrow);
+    return vec_stage_bytes(W, TT, n_wide + 1, n_narrow) + (TT + 1) * 128LL * 4;
 }
 
 // trips per vector-state backward tile: 32 unless a stage would pass 32 KB
@@ -455,6 +457,30 @@ int vec_bwd_trips(int W, int n_wide, int n_narrow) {
     int TT = 32;
     while (TT > 8 && vec_bwd_stage_bytes(W, TT, n_wide, n_narrow) > 32 * 1024) TT /= 2;
     return TT;
+}
+
+// the sequences a backward functor's VJP reads (its kVjpSeqs)
+unsigned vjp_live_mask(const std::string& functor) {
+    const std::string key = "kVjpSeqs = 0x";
+    const size_t at = functor.find(key);
+    if (at == std::string::npos) return ~0u;
+    return static_cast<unsigned>(std::strtoul(functor.c_str() + at + key.size(), nullptr, 16));
+}
+
+int popcount(unsigned x) {
+    int n = 0;
+    for (; x != 0; x &= x - 1) ++n;
+    return n;
+}
+
+// the live sequences of a signature, wide and width-one
+void live_counts(unsigned live, int n_seqs, const int64_t* widths, int W, int* n_wide, int* n_narrow) {
+    *n_wide = *n_narrow = 0;
+    for (int k = 0; k < n_seqs; ++k) {
+        if (!((live >> k) & 1u)) continue;
+        if (widths == nullptr || widths[k] == W) ++*n_wide;
+        else ++*n_narrow;
+    }
 }
 
 struct BodyBwdCall {
@@ -576,8 +602,10 @@ bool launch_body_lane_bwd(const BodyBwdCall& B, const float* init, const float* 
     }
     const int64_t tiles_i = (I + LI - 1) / LI;
     const bool one_per_sm = C.S.O * tiles_i <= dev->num_sms;
-    const int TT = lane_bwd_trips(NS, one_per_sm);
-    const int64_t stage_bytes = static_cast<int64_t>(NM) * TT * LI * 4;
+    const int NL = popcount(vjp_live_mask(B.functor) & ((1u << NS) - 1u));   // sequences streamed
+    const int TT = lane_bwd_trips(NL, one_per_sm);
+    // the live sequences' tiles, the output gradient's, TT+1 rows of states
+    const int64_t stage_bytes = ((NL + 1) * static_cast<int64_t>(TT) + TT + 1) * LI * 4;
     const int64_t out_bytes = 2LL * NS * TT * LI * 4;       // two gradient tiles
     const int64_t smem_cap = one_per_sm ? 200 * 1024 : 100 * 1024;
     int stages = 96 / TT;
@@ -587,7 +615,7 @@ bool launch_body_lane_bwd(const BodyBwdCall& B, const float* init, const float* 
     alignas(64) CUtensorMap maps[2 * ES_MAX_SEQS + 2];
     for (int q = 0; q < 2 * NS + 2; ++q) {
         const float* base = q < NS ? seqs[q] : q == NS ? states : q == NS + 1 ? gout : gseqs[q - NM];
-        if (!encode_rows(encode, &maps[q], base, C.S.O, C.S.T, I, LI, TT)) {
+        if (!encode_rows(encode, &maps[q], base, C.S.O, C.S.T, I, LI, q == NS ? TT + 1 : TT)) {
             *err = "cuTensorMapEncodeTiled failed for a lane-innermost backward tile map";
             return false;
         }
@@ -614,8 +642,10 @@ bool launch_body_vec_bwd(const BodyBwdCall& B, const float* init, const float* c
     const int LV = 128 / W;
     int n_wide = 0;
     for (int q = 0; q < NS; ++q) n_wide += C.S.sw[q] == W ? 1 : 0;
-    const int TT = vec_bwd_trips(W, n_wide, NS - n_wide);
-    const int64_t stage_bytes = vec_bwd_stage_bytes(W, TT, n_wide, NS - n_wide);
+    int lw = 0, ln = 0;
+    live_counts(vjp_live_mask(B.functor), NS, C.S.sw, W, &lw, &ln);
+    const int TT = vec_bwd_trips(W, lw, ln);
+    const int64_t stage_bytes = vec_bwd_stage_bytes(W, TT, lw, ln);
     const int64_t out_bytes = 2 * vec_stage_bytes(W, TT, n_wide, NS - n_wide);   // two gradient tiles
     const int64_t tiles_j = (C.S.J + LV - 1) / LV;
     const int64_t ctas = C.S.O * tiles_j;
@@ -635,7 +665,8 @@ bool launch_body_vec_bwd(const BodyBwdCall& B, const float* init, const float* c
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(row), static_cast<cuuint64_t>(C.S.T),
                                     static_cast<cuuint64_t>(C.S.O)};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row) * 4, static_cast<cuuint64_t>(row) * C.S.T * 4};
-        const cuuint32_t box[3] = {static_cast<cuuint32_t>(wide ? 128 : LV), static_cast<cuuint32_t>(TT), 1};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(wide ? 128 : LV),
+                                   static_cast<cuuint32_t>(q == NS ? TT + 1 : TT), 1};   // states: TT+1 rows
         const cuuint32_t estr[3] = {1, 1, 1};
         if (encode(&maps[q], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(basep), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -663,7 +694,8 @@ bool launch_body_time_bwd(const BodyBwdCall& B, const float* init, const float* 
     const BodyCall& C = B.C;
     const int NS = C.S.n_seqs;
     const int LO = time_bwd_rows(NS);
-    const int64_t stage_bytes = ((NS + 1) * LO * 128LL + LO * 144LL + 1023) & ~1023LL;
+    const int NL = popcount(vjp_live_mask(B.functor) & ((1u << NS) - 1u));   // sequences streamed
+    const int64_t stage_bytes = ((NL + 1) * LO * 128LL + LO * 144LL + 1023) & ~1023LL;
     const int64_t out_bytes = 2LL * NS * LO * 128;
     const int64_t ctas = (C.S.O + LO - 1) / LO;
     int64_t per_sm = (ctas + dev->num_sms - 1) / dev->num_sms;
@@ -787,18 +819,22 @@ es_status es_body_prepare_backward(es_body_t body, int state_width, int n_seqs, 
                                          &W, true);
     if (st != ES_OK) return st;
     std::vector<es::KernelText> todo = {es::generic_bwd_text(functor, W)};
+    const unsigned live = es::vjp_live_mask(functor);
+    const int NL = es::popcount(live & ((1u << n_seqs) - 1u));
     if (W == 1)
         for (int LI : {32, 64, 128})
             for (bool one : {false, true}) {
-                const int TT = es::lane_bwd_trips(n_seqs, one);
-                if (one && TT == es::lane_bwd_trips(n_seqs, false)) continue;
+                const int TT = es::lane_bwd_trips(NL, one);
+                if (one && TT == es::lane_bwd_trips(NL, false)) continue;
                 todo.push_back(es::lane_bwd_text(functor, LI, TT));
             }
     if (W == 1) todo.push_back(es::time_bwd_text(functor, n_seqs));
     if (W == 2 || W == 4 || W == 8 || W == 16) {
-        int n_wide = 0;
-        for (int k = 0; k < n_seqs; ++k) n_wide += (seq_widths == nullptr || seq_widths[k] == W) ? 1 : 0;
-        todo.push_back(es::vec_bwd_text(functor, W, es::vec_bwd_trips(W, n_wide, n_seqs - n_wide)));
+        int lw = 0, ln = 0;
+        std::vector<int64_t> widths(n_seqs);
+        for (int k = 0; k < n_seqs; ++k) widths[k] = seq_widths == nullptr ? W : seq_widths[k];
+        es::live_counts(live, n_seqs, widths.data(), W, &lw, &ln);
+        todo.push_back(es::vec_bwd_text(functor, W, es::vec_bwd_trips(W, lw, ln)));
     }
     for (const es::KernelText& kt : todo) {
         std::string err;

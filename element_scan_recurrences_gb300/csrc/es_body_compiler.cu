@@ -30,6 +30,8 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
+#include <cctype>
 #include <map>
 #include <set>
 #include <sstream>
@@ -237,13 +239,56 @@ public:
             if (r.diff) tape.push_back(Node{op, r, args, mask});
         }
         const char* type = is_bool ? "bool" : "float";
+        std::string stmt;
         if (wide) {
-            code += std::string("        ") + type + " " + r.name + "[E];\n#pragma unroll\n        for (int e = 0; e < E; ++e) " +
-                    r.name + "[e] = " + expr + ";\n";
+            stmt = std::string("        ") + type + " " + r.name + "[E];\n#pragma unroll\n        for (int e = 0; e < E; ++e) " +
+                   r.name + "[e] = " + expr + ";\n";
         } else {
-            code += std::string("        const ") + type + " " + r.name + " = " + expr + ";\n";
+            stmt = std::string("        const ") + type + " " + r.name + " = " + expr + ";\n";
         }
+        code += stmt;
+        stmts.push_back(Stmt{r.name, stmt, names_in(expr)});
         return r;
+    }
+
+    // one emitted statement: the value it defines, its text, the values and
+    // arguments (`h`, `sw[k]`, `sn[k]`) its expression reads
+    struct Stmt {
+        std::string name;
+        std::string code;
+        std::vector<std::string> deps;
+    };
+    std::vector<Stmt> stmts;
+
+    // the value and argument names an expression of generated code reads
+    static std::vector<std::string> names_in(const std::string& x) {
+        std::vector<std::string> out;
+        size_t i = 0;
+        auto word = [](char ch) { return std::isalnum(static_cast<unsigned char>(ch)) || ch == '_'; };
+        while (i < x.size()) {
+            if (!word(x[i])) {
+                ++i;
+                continue;
+            }
+            size_t j = i;
+            while (j < x.size() && word(x[j])) ++j;
+            const std::string id = x.substr(i, j - i);
+            const bool after_scope = i >= 2 && x[i - 1] == ':' && x[i - 2] == ':';
+            if (!after_scope && !std::isdigit(static_cast<unsigned char>(id[0]))) {
+                if (id.size() > 1 && id[0] == 'v' && std::all_of(id.begin() + 1, id.end(), [](char ch) {
+                        return std::isdigit(static_cast<unsigned char>(ch));
+                    })) {
+                    out.push_back(id);
+                } else if (id == "h") {
+                    out.push_back("h");
+                } else if ((id == "sw" || id == "sn") && j < x.size() && x[j] == '[') {
+                    const size_t k = x.find(']', j);
+                    out.push_back(x.substr(i, k + 1 - i));
+                }
+            }
+            i = j;
+        }
+        return out;
     }
 
     int W() const { return W_; }
@@ -514,9 +559,24 @@ Val Tracer::eval(const Form& f, const Env& env) {
 // the state (this thread's values in order, then the lane's threads).
 class Adjoint {
 public:
-    explicit Adjoint(const Tracer& tr) : tr_(tr) {}
+    // `result`: the body's value; when `from_saved` its derivative formulas
+    // read the trip's output from the saved states (`res`), which hold it
+    Adjoint(const Tracer& tr, const Val& result, bool from_saved)
+        : tr_(tr), res_name_(result.name), from_saved_(from_saved) {}
 
     std::string code;
+    std::set<std::string> used;     // forward values the derivatives read
+    bool reads_res = false;
+
+    // a forward value as a derivative formula reads it
+    std::string val(const Val& x) {
+        if (x.kind == Val::kTensor && from_saved_ && x.name == res_name_) {
+            reads_res = true;
+            return "res[e]";
+        }
+        if (x.kind == Val::kTensor) used.insert(x.name);
+        return tr_.ref(x);
+    }
 
     static std::string gname(const Val& v) {
         std::string g = "g_";
@@ -541,12 +601,17 @@ public:
             if (!has(n.out)) continue;
             const bool w = n.out.wide;
             const std::string G = w ? gname(n.out) + "[e]" : gname(n.out);
-            const std::string OUT = tr_.ref(n.out);
             const Val& a = n.args[0];
-            const std::string A = tr_.ref(a);
             const Val* b = n.args.size() > 1 ? &n.args[1] : nullptr;
-            const std::string B = b ? tr_.ref(*b) : "";
             const std::string& op = n.op;
+            // the operands' and the result's values, only where a formula reads them
+            static const std::set<std::string> kReadsA = {"mul", "abs", "log", "sin", "cos", "acos", "asin",
+                                                          "atan2", "pow", "maximum", "minimum", "rmax"};
+            static const std::set<std::string> kReadsB = {"mul", "div", "atan2", "pow", "maximum", "minimum"};
+            static const std::set<std::string> kReadsOut = {"div", "sqrt", "exp", "tanh", "rsqrt", "pow", "rmax"};
+            const std::string A = kReadsA.count(op) ? val(a) : "";
+            const std::string B = b && kReadsB.count(op) ? val(*b) : "";
+            const std::string OUT = kReadsOut.count(op) ? val(n.out) : "";
             auto half = "__fmul_rn(" + G + ", 0.5f)";
             if (op == "add") {
                 contribute(a, G, w);
@@ -595,7 +660,7 @@ public:
                 contribute(a, "(" + A + cmp + B + " ? " + G + " : (" + B + cmp + A + " ? 0.0f : " + half + "))", w);
                 contribute(*b, "(" + B + cmp + A + " ? " + G + " : (" + A + cmp + B + " ? 0.0f : " + half + "))", w);
             } else if (op == "where") {
-                const std::string M = tr_.ref(n.mask);
+                const std::string M = val(n.mask);
                 contribute(a, "(" + M + " ? " + G + " : 0.0f)", w);
                 contribute(*b, "(" + M + " ? 0.0f : " + G + ")", w);
             } else if (op == "sum") {
@@ -610,6 +675,26 @@ public:
                 contribute(a, G, true);
             }
         }
+    }
+
+    // the forward statements the derivatives need: the values they read and
+    // everything those are computed from, in the trace's order
+    std::string live_forward(std::set<std::string>* live) const {
+        std::map<std::string, const Tracer::Stmt*> def;
+        for (const Tracer::Stmt& st : tr_.stmts) def[st.name] = &st;
+        std::vector<std::string> todo(used.begin(), used.end());
+        while (!todo.empty()) {
+            const std::string nm = todo.back();
+            todo.pop_back();
+            if (!live->insert(nm).second) continue;
+            auto it = def.find(nm);
+            if (it != def.end())
+                for (const std::string& d : it->second->deps) todo.push_back(d);
+        }
+        std::string out;
+        for (const Tracer::Stmt& st : tr_.stmts)
+            if (live->count(st.name)) out += st.code;
+        return out;
     }
 
     // the gradient of a leaf, or zero
@@ -647,6 +732,8 @@ private:
     }
 
     const Tracer& tr_;
+    std::string res_name_;
+    bool from_saved_;
     std::set<std::string> assigned_;
     int tmp_ = 0;
 };
@@ -736,18 +823,40 @@ std::string Program::generate(int W, bool vector, unsigned wide_mask, bool with_
     if (with_vjp) {
         // the trip's vector-Jacobian product: the body again from the state
         // before the trip (`h`), then the tape backwards from the cotangent
-        // `lam` of the state after it; dp is the previous state's cotangent,
-        // dsw / dsn the sequences' (a width-one one summed over the state)
-        Adjoint adj(tr);
+        // `lam` of the state after it (`res`); dp is the previous state's
+        // cotangent, dsw / dsn the sequences' (a width-one one summed over
+        // the state)
+        // The trip's result is read from the saved states (they hold it);
+        // the other values the derivatives read are computed again, and only
+        // those.  A sequence no needed value reads is not needed at all.
+        const bool computed_result = r.kind == Val::kTensor && r.wide && r.name.size() > 1 && r.name[0] == 'v';
+        Adjoint adj(tr, r, computed_result);
         adj.seed(r);
         adj.sweep();
+        std::set<std::string> live;
+        const std::string forward = adj.live_forward(&live);
+        unsigned seq_mask = 0;
+        {
+            int kw = 0, kn = 0;
+            for (int k = 0; k < ns; ++k) {
+                const bool wide = (wide_mask >> k) & 1u;
+                const std::string nm = wide ? "sw[" + std::to_string(kw++) + "]" : "sn[" + std::to_string(kn++) + "]";
+                if (live.count(nm)) seq_mask |= 1u << k;
+            }
+        }
+        o << "    // sequences the vector-Jacobian product reads (bit k), and whether it\n"
+             "    // reads the trip's result from the saved states\n";
+        o << "    static constexpr unsigned kVjpSeqs = 0x" << std::hex << seq_mask << std::dec << "u;\n";
+        o << "    static constexpr bool kVjpRes = " << (adj.reads_res ? "true" : "false") << ";\n";
         o << "    template <int E, int G>\n";
         o << "    __device__ __forceinline__ static void vjp(float (&dp)[E], float (&dsw)[kSW][E], float (&dsn)[kSN],\n"
              "                                               const float (&lam)[E], const float (&h)[E],\n"
+             "                                               const float (&res)[E],\n"
              "                                               const float (&sw)[kSW][E], const float (&sn)[kSN],\n"
              "                                               const unsigned mask) {\n";
-        o << "        (void)lam;\n        (void)h;\n        (void)sw;\n        (void)sn;\n        (void)mask;\n";
-        o << tr.code << adj.code;
+        o << "        (void)lam;\n        (void)h;\n        (void)res;\n        (void)sw;\n        (void)sn;\n"
+             "        (void)mask;\n";
+        o << forward << adj.code;
         o << "#pragma unroll\n        for (int e = 0; e < E; ++e) dp[e] = " << adj.grad_or_zero(h) << ";\n";
         int qw = 0, qn = 0;
         for (const Val& s : leaves) {

@@ -57,6 +57,16 @@ __host__ __device__ constexpr int wide_slot(unsigned wide_mask, int k) {
 __host__ __device__ constexpr int narrow_slot(unsigned wide_mask, int k) { return k - wide_slot(wide_mask, k); }
 __host__ __device__ constexpr bool is_wide(unsigned wide_mask, int k) { return ((wide_mask >> k) & 1u) != 0; }
 
+// the sequences a backward kernel streams (those the body's vector-Jacobian
+// product reads): their number, and sequence k's place among them
+__host__ __device__ constexpr int live_count(unsigned live_mask, int ns) {
+    int n = 0;
+    for (int q = 0; q < ns; ++q) n += (live_mask >> q) & 1u;
+    return n;
+}
+__host__ __device__ constexpr int live_slot(unsigned live_mask, int k) { return live_count(live_mask, k); }
+__host__ __device__ constexpr bool is_live(unsigned live_mask, int k) { return ((live_mask >> k) & 1u) != 0; }
+
 // `sum` over a lane's state: this thread's E values in order, then a
 // butterfly over the lane's G threads.  Every thread of the group ends with
 // the same bits (each level adds the same two operands).  With G = 1 the

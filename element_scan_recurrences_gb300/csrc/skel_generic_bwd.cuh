@@ -11,8 +11,10 @@
 // state's cotangent on.  After the last trip lam is the gradient of `init`.
 // A forward scan's gradient walks t = T-1 .. 0, a reverse scan's t = 0 ..
 // T-1.  One thread holds the whole state (G = 1), so the sums over the state
-// run w = 0..W-1 in order.  Loads for the next trip are issued one trip
-// ahead when the registers allow.
+// run w = 0..W-1 in order.  Only the sequences the VJP reads are loaded, and
+// the trip's result comes from the saved states where the VJP reads it.
+// Loads for the next trip are issued one trip ahead when the registers
+// allow.
 #pragma once
 
 #include "skel_common.cuh"
@@ -27,7 +29,7 @@ k_body_generic_bwd(const SeqPtrs seqs, const float* __restrict__ init, const flo
     constexpr int NS = Body::kNS;
     constexpr int kSW = Body::kSW, kSN = Body::kSN;
     // one trip ahead while a trip's loads take at most 64 registers
-    constexpr bool kAhead = W * (kSW + 2) + kSN <= 64;
+    constexpr bool kAhead = W * (kSW + 3) + kSN <= 64;
     const int64_t lane = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (lane >= O * J) return;
     const int64_t o = lane / J;
@@ -37,13 +39,21 @@ k_body_generic_bwd(const SeqPtrs seqs, const float* __restrict__ init, const flo
         float sw[kSW][W];
         float sn[kSN];
         float p[W];    // the state before the trip
+        float res[W];  // the trip's result (its saved state)
         float g[W];    // the output gradient of the trip
     };
     auto load = [&](int64_t t, Trip& d) {
         const int64_t row = (o * T + t) * J + j;
 #pragma unroll
         for (int k = 0; k < NS; ++k) {
-            if (is_wide(Body::kWideMask, k)) {
+            if (!is_live(Body::kVjpSeqs, k)) {
+                if (is_wide(Body::kWideMask, k)) {
+#pragma unroll
+                    for (int w = 0; w < W; ++w) d.sw[wide_slot(Body::kWideMask, k)][w] = 0.0f;
+                } else {
+                    d.sn[narrow_slot(Body::kWideMask, k)] = 0.0f;
+                }
+            } else if (is_wide(Body::kWideMask, k)) {
 #pragma unroll
                 for (int w = 0; w < W; ++w) d.sw[wide_slot(Body::kWideMask, k)][w] = __ldg(seqs.p[k] + row * W + w);
             } else {
@@ -56,6 +66,7 @@ k_body_generic_bwd(const SeqPtrs seqs, const float* __restrict__ init, const flo
 #pragma unroll
         for (int w = 0; w < W; ++w) {
             d.p[w] = first ? (init != nullptr ? __ldg(init + lane * W + w) : 0.0f) : __ldg(states + prow * W + w);
+            d.res[w] = Body::kVjpRes ? __ldg(states + row * W + w) : 0.0f;
             d.g[w] = __ldcs(gout + row * W + w);
         }
     };
@@ -78,7 +89,7 @@ k_body_generic_bwd(const SeqPtrs seqs, const float* __restrict__ init, const flo
         float dp[W];
         float dsw[kSW][W];
         float dsn[kSN];
-        Body::template vjp<W, 1>(dp, dsw, dsn, lam, cur.p, cur.sw, cur.sn, 0xffffffffu);
+        Body::template vjp<W, 1>(dp, dsw, dsn, lam, cur.p, cur.res, cur.sw, cur.sn, 0xffffffffu);
         const int64_t row = (o * T + t) * J + j;
 #pragma unroll
         for (int k = 0; k < NS; ++k) {

@@ -5,11 +5,12 @@
 // element scan in the opposite trip order applying the body's
 // vector-Jacobian product once a trip.  One CTA owns LI adjacent lanes of
 // one o and walks the time tiles of TT trips backwards in scan order:
-//   * warp 0, lane 0 streams, per tile, TT trips of every sequence, of the
-//     output gradient and of the saved states shifted by one trip (the state
-//     before each trip: rows t0-1 .. t0+TT-2 of a forward scan, t0+1 ..
-//     t0+TT of a reverse one; the row outside [0, T) arrives zero-filled
-//     and is replaced by `init`) into an S-stage SMEM ring with TMA;
+//   * warp 0, lane 0 streams, per tile, TT trips of every sequence the VJP
+//     reads (`kVjpSeqs`), of the output gradient, and TT+1 rows of the saved
+//     states (rows t0-1 .. t0+TT-1 of a forward scan, t0 .. t0+TT of a
+//     reverse one: every trip's previous state and its own result; the row
+//     outside [0, T) arrives zero-filled and the scan's first trip takes
+//     `init`) into an S-stage SMEM ring with TMA;
 //   * LI consumer threads (one per lane) copy the tile into registers, hand
 //     the stage back, then run the VJP over the tile with the cotangent in a
 //     register.  The serial chain is only the cotangent's (the body itself
@@ -33,19 +34,24 @@ k_body_lane_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
                 float* __restrict__ ginit, int T, int I, int tiles_i, int stages, int reverse, unsigned int* status,
                 uint64_t wait_ns, int64_t drop_tile) {
     constexpr int NS = Body::kNS;
-    constexpr int NM = NS + 2;     // the sequences, the shifted states, the output gradient
-    constexpr int kP = NS, kG = NS + 1;
+    constexpr unsigned kLive = Body::kVjpSeqs;
+    constexpr int NL = live_count(kLive, NS);    // sequences streamed
+    constexpr int kP = NS, kG = NS + 1;          // map slots of the states and the output gradient
     static_assert(Body::kWideMask == (1u << NS) - 1u, "a scalar state has no width-one sequences");
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kLaneBwdMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kLaneBwdMaxStages];
     __shared__ int abort_flag;
 
+    // a stage: the live sequences' tiles, the output gradient's, then TT+1
+    // rows of the saved states
     constexpr int kTileFloats = TT * LI;
-    constexpr uint32_t kStageBytes = NM * kTileFloats * 4u;
-    float* tiles = reinterpret_cast<float*>(smem_raw + smem_align_pad(smem_raw));   // [stages][NM][TT][LI]
-    float* outs = tiles + static_cast<size_t>(stages) * NM * kTileFloats;           // [2][NS][TT][LI]
-    const CUtensorMap* gmaps = &maps.m[NM];                                          // the gradients' maps
+    constexpr int kOffG = NL * kTileFloats, kOffH = (NL + 1) * kTileFloats;
+    constexpr int kStageFloats = kOffH + (TT + 1) * LI;
+    constexpr uint32_t kStageBytes = kStageFloats * 4u;
+    float* tiles = reinterpret_cast<float*>(smem_raw + smem_align_pad(smem_raw));   // [stages][kStageFloats]
+    float* outs = tiles + static_cast<size_t>(stages) * kStageFloats;               // [2][NS][TT][LI]
+    const CUtensorMap* gmaps = &maps.m[NS + 2];                                      // the gradients' maps
 
     const int o = blockIdx.x / tiles_i;
     const int i0 = (blockIdx.x % tiles_i) * LI;
@@ -65,7 +71,8 @@ k_body_lane_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
 
     if (warp == 0) {
         if (lane == 0) {
-            for (int q = 0; q < NM; ++q) tma_prefetch_desc(&maps.m[q]);
+            for (int q = 0; q < NS + 2; ++q)
+                if (q >= NS || is_live(kLive, q)) tma_prefetch_desc(&maps.m[q]);
             const uint64_t pol = l2_policy_stream();
             int issued = 0;
             for (int k = 0; k < ntiles; ++k) {
@@ -79,14 +86,15 @@ k_body_lane_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
                 if (k == drop_tile) continue;   // testing hook: this tile never arrives
                 const int j = reverse ? k : ntiles - 1 - k;
                 const int t0 = j * TT;
-                float* st = tiles + s * NM * kTileFloats;
+                float* st = tiles + static_cast<size_t>(s) * kStageFloats;
                 mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
 #pragma unroll
                 for (int q = 0; q < NS; ++q)
-                    tma_load_3d(st + q * kTileFloats, &maps.m[q], i0, t0, o, &full_bar[s], pol);
-                // the state before each trip: one row back (forward) or ahead (reverse)
-                tma_load_3d(st + kP * kTileFloats, &maps.m[kP], i0, reverse ? t0 + 1 : t0 - 1, o, &full_bar[s], pol);
-                tma_load_3d(st + kG * kTileFloats, &maps.m[kG], i0, t0, o, &full_bar[s], pol);
+                    if (is_live(kLive, q))
+                        tma_load_3d(st + live_slot(kLive, q) * kTileFloats, &maps.m[q], i0, t0, o, &full_bar[s], pol);
+                tma_load_3d(st + kOffG, &maps.m[kG], i0, t0, o, &full_bar[s], pol);
+                // the states from the row before the tile (forward) or from the tile's first (reverse)
+                tma_load_3d(st + kOffH, &maps.m[kP], i0, reverse ? t0 : t0 - 1, o, &full_bar[s], pol);
             }
             for (int k = max(0, issued - stages); k < issued; ++k) {
                 if (k == drop_tile) continue;
@@ -129,33 +137,45 @@ k_body_lane_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
         const int j = reverse ? k : ntiles - 1 - k;
         const int t0 = j * TT;
         const int n = min(TT, T - t0);
-        const float* st = tiles + s * NM * kTileFloats + c;
-        float vr[NM][TT];
+        const float* st = tiles + static_cast<size_t>(s) * kStageFloats + c;
+        float vr[NL > 0 ? NL : 1][TT], vg[TT], vh[TT + 1];
 #pragma unroll
-        for (int q = 0; q < NM; ++q)
+        for (int q = 0; q < NL; ++q)
 #pragma unroll
             for (int tt = 0; tt < TT; ++tt) vr[q][tt] = st[q * kTileFloats + tt * LI];
+#pragma unroll
+        for (int tt = 0; tt < TT; ++tt) vg[tt] = st[kOffG + tt * LI];
+#pragma unroll
+        for (int tt = 0; tt <= TT; ++tt) vh[tt] = st[kOffH + tt * LI];
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
-        // the scan's first trip takes `init` as its previous state (one tile)
+        // the scan's first trip takes `init` as its previous state (one tile;
+        // the row it replaces is outside [0, T), no trip's result)
         if (t_first >= t0 && t_first < t0 + TT) {
 #pragma unroll
             for (int tt = 0; tt < TT; ++tt)
-                if (t0 + tt == t_first) vr[kP][tt] = h0;
+                if (t0 + tt == t_first) {
+                    if (!reverse)
+                        vh[tt] = h0;
+                    else
+                        vh[tt + 1] = h0;
+                }
         }
         float* ob = outs + static_cast<size_t>(k & 1) * NS * kTileFloats + c;
-        auto trip = [&](const int tt) {
-            lam = __fadd_rn(lam, vr[kG][tt]);
+        // trip tt with its previous state in row pi and its result in row ri
+        auto trip = [&](const int tt, const int pi, const int ri) {
+            lam = __fadd_rn(lam, vg[tt]);
             const float lm[1] = {lam};
-            const float hp[1] = {vr[kP][tt]};
+            const float hp[1] = {vh[pi]};
+            const float hr[1] = {vh[ri]};
             float sw[Body::kSW][1];
             const float sn[Body::kSN] = {};
 #pragma unroll
-            for (int q = 0; q < NS; ++q) sw[q][0] = vr[q][tt];
+            for (int q = 0; q < NS; ++q) sw[q][0] = is_live(kLive, q) ? vr[live_slot(kLive, q)][tt] : 0.0f;
             float dp[1];
             float dsw[Body::kSW][1];
             float dsn[Body::kSN];
-            Body::template vjp<1, 1>(dp, dsw, dsn, lm, hp, sw, sn, 0xffffffffu);
+            Body::template vjp<1, 1>(dp, dsw, dsn, lm, hp, hr, sw, sn, 0xffffffffu);
 #pragma unroll
             for (int q = 0; q < NS; ++q) ob[q * kTileFloats + tt * LI] = dsw[q][0];
             lam = dp[0];
@@ -165,20 +185,20 @@ k_body_lane_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
         if (n == TT) {
             if (!reverse) {
 #pragma unroll
-                for (int tt = TT - 1; tt >= 0; --tt) trip(tt);
+                for (int tt = TT - 1; tt >= 0; --tt) trip(tt, tt, tt + 1);
             } else {
 #pragma unroll
-                for (int tt = 0; tt < TT; ++tt) trip(tt);
+                for (int tt = 0; tt < TT; ++tt) trip(tt, tt + 1, tt);
             }
         } else {
             if (!reverse) {
 #pragma unroll
                 for (int tt = TT - 1; tt >= 0; --tt)
-                    if (tt < n) trip(tt);
+                    if (tt < n) trip(tt, tt, tt + 1);
             } else {
 #pragma unroll
                 for (int tt = 0; tt < TT; ++tt)
-                    if (tt < n) trip(tt);
+                    if (tt < n) trip(tt, tt + 1, tt);
             }
         }
     }

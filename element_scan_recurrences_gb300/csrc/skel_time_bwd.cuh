@@ -5,12 +5,14 @@
 // element scan in the opposite trip order applying the body's
 // vector-Jacobian product once a trip.  Each lane is one row of T values.
 // Per tile of LO rows x 32 trips the producer streams, with TMA, every
-// sequence and the output gradient as 128-byte-swizzled boxes {32, LO}
+// sequence the VJP reads (`kVjpSeqs`) and the output gradient as
+// 128-byte-swizzled boxes {32, LO}
 // (conflict-free 16-byte reads of a thread's own row) and the saved states as
 // an unswizzled box {36, LO} whose 144-byte rows also read conflict-free:
 // trips t0-4 .. t0+31 for a forward scan, t0 .. t0+35 for a reverse one, so
-// the state before every trip of the tile is in the same box (columns outside
-// 0..T-1 are zero-filled and `init` takes the scan's first trip's place).
+// the state before every trip of the tile, and its result, are in the same
+// box (columns outside 0..T-1 are zero-filled and `init` takes the scan's
+// first trip's place).
 // Each consumer thread owns one row.  It walks its 32 trips in backward order
 // four at a time (one 16-byte vector of every tile, read one group ahead),
 // runs the VJP with the cotangent in a register, and writes the sequences'
@@ -33,11 +35,14 @@ k_body_time_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
                 float* __restrict__ ginit, int O, int T, int stages, int reverse, unsigned int* status,
                 uint64_t wait_ns, int64_t drop_tile) {
     constexpr int NS = Body::kNS;
+    constexpr unsigned kLive = Body::kVjpSeqs;
+    constexpr int NL = live_count(kLive, NS);   // sequences streamed
     constexpr int kP = NS, kG = NS + 1;      // map slots of the states and the output gradient
     static_assert(Body::kWideMask == (1u << NS) - 1u, "a scalar state has no width-one sequences");
     constexpr uint32_t kTile = LO * 128u;                          // one swizzled {32, LO} tile
     constexpr uint32_t kHTile = LO * kTimeBwdHCols * 4u;
-    constexpr uint32_t kOffH = (NS + 1) * kTile;                   // sequences, then the output gradient
+    constexpr uint32_t kOffG = NL * kTile;                         // the live sequences, then the output gradient
+    constexpr uint32_t kOffH = (NL + 1) * kTile;
     constexpr uint32_t kStage = (kOffH + kHTile + 1023u) & ~1023u;
     constexpr uint32_t kOut = NS * kTile;                           // one output buffer
     extern __shared__ unsigned char smem_raw[];
@@ -65,7 +70,8 @@ k_body_time_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
 
     if (warp == 0) {
         if (lane == 0) {
-            for (int q = 0; q < NS + 2; ++q) tma_prefetch_desc(&maps.m[q]);
+            for (int q = 0; q < NS + 2; ++q)
+                if (q >= NS || is_live(kLive, q)) tma_prefetch_desc(&maps.m[q]);
             const uint64_t pol = l2_policy_stream();
             int issued = 0;
             for (int k = 0; k < ntiles; ++k) {
@@ -81,8 +87,10 @@ k_body_time_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
                 unsigned char* st = base + static_cast<size_t>(s) * kStage;
                 mbar_arrive_expect_tx(&full_bar[s], kOffH + kHTile);
 #pragma unroll
-                for (int q = 0; q < NS; ++q) tma_load_2d(st + q * kTile, &maps.m[q], t0, o0, &full_bar[s], pol);
-                tma_load_2d(st + NS * kTile, &maps.m[kG], t0, o0, &full_bar[s], pol);
+                for (int q = 0; q < NS; ++q)
+                    if (is_live(kLive, q))
+                        tma_load_2d(st + live_slot(kLive, q) * kTile, &maps.m[q], t0, o0, &full_bar[s], pol);
+                tma_load_2d(st + kOffG, &maps.m[kG], t0, o0, &full_bar[s], pol);
                 // the states four trips back (forward) or from the tile (reverse): x stays 16-byte aligned
                 tma_load_2d(st + kOffH, &maps.m[kP], reverse ? t0 : t0 - 4, o0, &full_bar[s], pol);
             }
@@ -138,8 +146,11 @@ k_body_time_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
         auto chunk = [&](int q) { return (static_cast<uint32_t>(q) ^ swz) << 4; };
         auto readq = [&](int q, Quad& d) {
 #pragma unroll
-            for (int p = 0; p < NS; ++p) d.s[p] = *reinterpret_cast<const float4*>(st + p * kTile + row_off + chunk(q));
-            d.g = *reinterpret_cast<const float4*>(st + NS * kTile + row_off + chunk(q));
+            for (int p = 0; p < NS; ++p)
+                d.s[p] = is_live(kLive, p)
+                             ? *reinterpret_cast<const float4*>(st + live_slot(kLive, p) * kTile + row_off + chunk(q))
+                             : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            d.g = *reinterpret_cast<const float4*>(st + kOffG + row_off + chunk(q));
             d.h0 = *reinterpret_cast<const float4*>(hrow + 16 * q);
             d.h1 = *reinterpret_cast<const float4*>(hrow + 16 * (q + 1));
         };
@@ -154,6 +165,8 @@ k_body_time_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
                 const int hc = reverse ? i + 1 : i + 3;
                 float p = hc < 4 ? comp(d.h0, hc) : comp(d.h1, hc - 4);
                 if (t0 + 4 * q + i == t_first) p = h0;
+                // the trip's result: column 4q+i+4 (forward), 4q+i (reverse)
+                const float hr[1] = {reverse ? comp(d.h0, i) : comp(d.h1, i)};
                 lam = __fadd_rn(lam, comp(d.g, i));
                 const float lm[1] = {lam};
                 const float hp[1] = {p};
@@ -164,7 +177,7 @@ k_body_time_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
                 float dp[1];
                 float dsw[Body::kSW][1];
                 float dsn[Body::kSN];
-                Body::template vjp<1, 1>(dp, dsw, dsn, lm, hp, sw, sn, 0xffffffffu);
+                Body::template vjp<1, 1>(dp, dsw, dsn, lm, hp, hr, sw, sn, 0xffffffffu);
 #pragma unroll
                 for (int pq = 0; pq < NS; ++pq) res[pq][i] = dsw[pq][0];
                 lam = dp[0];

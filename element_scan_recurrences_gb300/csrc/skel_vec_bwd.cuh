@@ -8,10 +8,11 @@
 // sequence are [O, T, J*W], a width-one sequence is [O, T, J]; one CTA owns
 // LV = 128 / W adjacent lanes of one o (128 contiguous values per trip).
 // Warp 0's lane 0 streams time tiles of TT trips, last tile first for a
-// forward scan, of every sequence, of the output gradient and of the saved
-// states shifted by one trip (the state before each trip; the row outside
-// [0, T) arrives zero-filled and the scan's first trip takes `init`) into an
-// S-stage SMEM ring with TMA.  Each of the 128 / E consumer threads holds E
+// forward scan, of every sequence the VJP reads (`kVjpSeqs`), of the output
+// gradient and TT+1 rows of the saved states (rows t0-1 .. t0+TT-1 of a
+// forward scan, t0 .. t0+TT of a reverse one: every trip's previous state
+// and its result; the row outside [0, T) arrives zero-filled and the scan's
+// first trip takes `init`) into an S-stage SMEM ring with TMA.  Each of the 128 / E consumer threads holds E
 // consecutive values of one lane's cotangent (a lane is G = W / E threads;
 // the VJP's sums over the state combine them with xor shuffles).  Per trip
 // it reads its operands from SMEM, adds the trip's output gradient to the
@@ -42,20 +43,29 @@ k_body_vec_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const fl
     constexpr int G = W / E;                      // threads per lane
     constexpr unsigned kMask = 0xffffffffu;
     static_assert(NC % 32 == 0, "the consumer barrier counts whole warps");
+    constexpr unsigned kLive = Body::kVjpSeqs;
     constexpr uint32_t kWideBytes = TT * kVecRow * 4u;
     constexpr uint32_t kNarrowBytes = TT * LV * 4u;   // a multiple of 128 bytes
-    auto tile_bytes = [](int q) -> uint32_t {
-        return q >= NS || is_wide(kWide, q) ? kWideBytes : kNarrowBytes;
-    };
-    // byte offset of map slot q's tile inside a stage (sequences, states,
-    // output gradient) or, for q < NS, inside an output buffer
-    auto tile_off = [&](int q) -> uint32_t {
+    constexpr uint32_t kHBytes = (TT + 1) * kVecRow * 4u;
+    auto seq_bytes = [](int q) -> uint32_t { return is_wide(kWide, q) ? kWideBytes : kNarrowBytes; };
+    // byte offsets in a stage: the live sequences' tiles, the output
+    // gradient's, then TT+1 rows of the saved states
+    auto in_off = [&](int q) -> uint32_t {
         uint32_t off = 0;
-        for (int k = 0; k < q; ++k) off += tile_bytes(k);
+        for (int k = 0; k < q; ++k)
+            if (is_live(kLive, k)) off += seq_bytes(k);
         return off;
     };
-    const uint32_t stage_bytes = tile_off(NS + 2);
-    const uint32_t out_bytes = tile_off(NS);
+    const uint32_t off_g = in_off(NS);
+    const uint32_t off_h = off_g + kWideBytes;
+    const uint32_t stage_bytes = off_h + kHBytes;
+    // byte offset of sequence q's gradient tile in an output buffer
+    auto out_off = [&](int q) -> uint32_t {
+        uint32_t off = 0;
+        for (int k = 0; k < q; ++k) off += seq_bytes(k);
+        return off;
+    };
+    const uint32_t out_bytes = out_off(NS);
 
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kVecBwdMaxStages];
@@ -83,7 +93,8 @@ k_body_vec_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const fl
 
     if (warp == 0) {
         if (lane == 0) {
-            for (int q = 0; q < NS + 2; ++q) tma_prefetch_desc(&maps.m[q]);
+            for (int q = 0; q < NS + 2; ++q)
+                if (q >= NS || is_live(kLive, q)) tma_prefetch_desc(&maps.m[q]);
             const uint64_t pol = l2_policy_stream();
             int issued = 0;
             for (int k = 0; k < ntiles; ++k) {
@@ -101,11 +112,12 @@ k_body_vec_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const fl
                 mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
 #pragma unroll
                 for (int q = 0; q < NS; ++q)
-                    tma_load_3d(st + tile_off(q), &maps.m[q], is_wide(kWide, q) ? j0 * W : j0, t0, o, &full_bar[s],
-                                pol);
-                // the state before each trip: one row back (forward) or ahead (reverse)
-                tma_load_3d(st + tile_off(kP), &maps.m[kP], j0 * W, reverse ? t0 + 1 : t0 - 1, o, &full_bar[s], pol);
-                tma_load_3d(st + tile_off(kG), &maps.m[kG], j0 * W, t0, o, &full_bar[s], pol);
+                    if (is_live(kLive, q))
+                        tma_load_3d(st + in_off(q), &maps.m[q], is_wide(kWide, q) ? j0 * W : j0, t0, o, &full_bar[s],
+                                    pol);
+                tma_load_3d(st + off_g, &maps.m[kG], j0 * W, t0, o, &full_bar[s], pol);
+                // the states from the row before the tile (forward) or from the tile's first (reverse)
+                tma_load_3d(st + off_h, &maps.m[kP], j0 * W, reverse ? t0 : t0 - 1, o, &full_bar[s], pol);
             }
             for (int k = max(0, issued - stages); k < issued; ++k) {
                 if (k == drop_tile) continue;
@@ -145,7 +157,7 @@ k_body_vec_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const fl
             const unsigned char* ob = outs + static_cast<size_t>((k - 1) & 1) * out_bytes;
 #pragma unroll
             for (int q = 0; q < NS; ++q)
-                tma_store_3d(&gmaps[q], is_wide(kWide, q) ? j0 * W : j0, jp * TT, o, ob + tile_off(q));
+                tma_store_3d(&gmaps[q], is_wide(kWide, q) ? j0 * W : j0, jp * TT, o, ob + out_off(q));
             bulk_commit();
             // the buffer written at the next tile is the one this store reads
             bulk_wait_read<0>();
@@ -157,17 +169,26 @@ k_body_vec_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const fl
         const unsigned char* st = base + static_cast<size_t>(s) * stage_bytes;
         unsigned char* ob = outs + static_cast<size_t>(k & 1) * out_bytes;
         auto trip = [&](const int tt) {
-            float dw[Body::kSW][E], dn[Body::kSN], p[E], g[E];
+            float dw[Body::kSW][E], dn[Body::kSN], p[E], hr[E], g[E];
 #pragma unroll
             for (int q = 0; q < NS; ++q) {
-                const float* tile = reinterpret_cast<const float*>(st + tile_off(q));
-                if (is_wide(kWide, q))
-                    vec_load<E>(dw[wide_slot(kWide, q)], tile + tt * kVecRow + c * E);
-                else
-                    dn[narrow_slot(kWide, q)] = tile[tt * LV + v];
+                const float* tile = reinterpret_cast<const float*>(st + in_off(q));
+                if (is_wide(kWide, q)) {
+                    if (is_live(kLive, q)) {
+                        vec_load<E>(dw[wide_slot(kWide, q)], tile + tt * kVecRow + c * E);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < E; ++e) dw[wide_slot(kWide, q)][e] = 0.0f;
+                    }
+                } else {
+                    dn[narrow_slot(kWide, q)] = is_live(kLive, q) ? tile[tt * LV + v] : 0.0f;
+                }
             }
-            vec_load<E>(p, reinterpret_cast<const float*>(st + tile_off(kP)) + tt * kVecRow + c * E);
-            vec_load<E>(g, reinterpret_cast<const float*>(st + tile_off(kG)) + tt * kVecRow + c * E);
+            // rows of the states box: the previous state and the trip's result
+            const float* hb = reinterpret_cast<const float*>(st + off_h) + c * E;
+            vec_load<E>(p, hb + (tt + reverse) * kVecRow);
+            vec_load<E>(hr, hb + (tt + 1 - reverse) * kVecRow);
+            vec_load<E>(g, reinterpret_cast<const float*>(st + off_g) + tt * kVecRow + c * E);
             const bool first = t0 + tt == t_first;
 #pragma unroll
             for (int e = 0; e < E; ++e) {
@@ -175,10 +196,10 @@ k_body_vec_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const fl
                 lam[e] = __fadd_rn(lam[e], g[e]);
             }
             float dp[E], dsw[Body::kSW][E], dsn[Body::kSN];
-            Body::template vjp<E, G>(dp, dsw, dsn, lam, p, dw, dn, kMask);
+            Body::template vjp<E, G>(dp, dsw, dsn, lam, p, hr, dw, dn, kMask);
 #pragma unroll
             for (int q = 0; q < NS; ++q) {
-                float* tile = reinterpret_cast<float*>(ob + tile_off(q));
+                float* tile = reinterpret_cast<float*>(ob + out_off(q));
                 if (is_wide(kWide, q)) {
                     float* d = tile + tt * kVecRow + c * E;
 #pragma unroll

@@ -89,17 +89,18 @@ class Workload:
         reads = sum(math.prod(self.seq_shape(k)) for k in range(self.n_seqs))
         return 4 * (reads + math.prod(self.init_shape) + self.elements)
 
-    def backward_algorithmic_bytes(self) -> int:
+    def backward_algorithmic_bytes(self, live_mask: Optional[int] = None) -> int:
         """f32 bytes of one backward launch: the output gradient, the saved
         states, the second sequence, x (not for TANH_DECAY, whose gradient
         never reads it) and initial read; both sequence gradients and the
-        initial gradient written.  A body program's backward reads every
-        sequence and writes every sequence's gradient."""
+        initial gradient written.  A body program's backward reads the
+        sequences its vector-Jacobian product reads (bit k of `live_mask`;
+        all when None) and writes every sequence's gradient."""
         ni = math.prod(self.init_shape)
         if self.text is not None:
-            # a body program's VJP evaluates the body again: every sequence is read
-            ns = sum(math.prod(self.seq_shape(k)) for k in range(self.n_seqs))
-            return 4 * (2 * self.elements + ns + ni + ns + ni)
+            sizes = [math.prod(self.seq_shape(k)) for k in range(self.n_seqs)]
+            live = sum(n for k, n in enumerate(sizes) if live_mask is None or (live_mask >> k) & 1)
+            return 4 * (2 * self.elements + live + ni + sum(sizes) + ni)
         n0, n1 = (math.prod(self.seq_shape(k)) for k in range(2))
         reads = 2 * self.elements + n1 + ni + (0 if self.body == TANH_DECAY else n0)
         return 4 * (reads + n0 + n1 + ni)

@@ -2,6 +2,8 @@
 kernel compiles for sm_103a (NVRTC on the host), the plan validates the
 gradient buffers, and the generated vector-Jacobian product has the
 documented derivative rules."""
+import re
+
 import pytest
 
 import body_cases
@@ -117,9 +119,21 @@ def test_backward_rejects_what_the_forward_rejects():
 def test_vjp_source_has_the_derivative_rules():
     src = es.Body("(lambda (h x a) (tanh (+ x (* a h))))").source_backward()
     assert "static void vjp(" in src
-    # tanh: g * (1 - out * out); the product's operands swap
-    assert "__fmul_rn(g_v2[e], __fsub_rn(1.0f, __fmul_rn(v2[e], v2[e])))" in src
+    # tanh: g * (1 - out * out), the trip's result read from the saved states;
+    # the product's operands swap
+    assert "__fmul_rn(g_v2[e], __fsub_rn(1.0f, __fmul_rn(res[e], res[e])))" in src
     assert "g_sw1[e] = __fmul_rn(g_v0[e], h[e])" in src and "g_h[e] = __fmul_rn(g_v0[e], sw[1][e])" in src
+    # nothing of the body is computed again, and x is never read
+    vjp = src[src.index("static void vjp("):]
+    assert "tanhf" not in vjp and not re.search(r"(?<!d)sw\[0\]", vjp)
+    assert "kVjpSeqs = 0x2u" in src and "kVjpRes = true" in src
+    # linear-scan's body: the gradient never reads b
+    src = es.Body("(lambda (h a b) (+ (* a h) b))").source_backward()
+    assert "kVjpSeqs = 0x1u" in src and "kVjpRes = false" in src
+    # a body whose derivatives read an intermediate recomputes it (and what it needs)
+    src = es.Body("(lambda (h x a g) (where (> g 0.5) (tanh (+ x (* a h))) h))").source_backward()
+    vjp = src[src.index("static void vjp("):]
+    assert "tanhf" in vjp and "kVjpSeqs = 0x7u" in src
     # a width-one gate of a vector state takes the sum over the state
     src = es.Body("(lambda (h g) (* h g))").source_backward(8, [1])
     assert "es::group_sum<E, G>(c0, mask)" in src and "dsn[0] = g_sn0" in src
