@@ -39,7 +39,8 @@ UNIT = "elements/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 PATH_KERNEL = {"lane_tma": "k_lane_tma", "time_tma": "k_time_tma", "vec_tma": "k_vec_tma", "generic": "k_generic"}
-PATH_KERNEL_BWD = {"lane_tma": "k_lane_bwd", "generic": "k_generic_bwd"}
+PATH_KERNEL_BWD = {"lane_tma": "k_lane_bwd", "generic": "k_generic_bwd", "vec_tma": "k_vec_bwd",
+                   "time_tma": "k_time_bwd"}
 PATH_KERNEL_BODY_BWD = {"generic": "k_body_generic_bwd", "lane_tma": "k_body_lane_bwd", "vec_tma": "k_body_vec_bwd",
                         "time_tma": "k_body_time_bwd"}
 # kernels compiled at run time from a body program
