@@ -36,7 +36,8 @@ EXPORTS = ("es_scan_f32", "es_plan_f32", "es_scan_backward_f32", "es_plan_backwa
            "es_plan_table_scan_i32", "es_matrix_scan_workspace_f32", "es_matrix_scan_ws_f32",
            "es_matrix_scan_static_f32", "es_scan_body_backward_f32", "es_plan_body_backward_f32",
            "es_body_source_backward", "es_body_prepare_backward", "es_matrix_scan_backward_f32",
-           "es_plan_matrix_scan_backward_f32", "es_linear_scan_backward_f32", "es_plan_linear_scan_backward_f32")
+           "es_plan_matrix_scan_backward_f32", "es_linear_scan_backward_f32", "es_plan_linear_scan_backward_f32",
+           "es_scan_host_f32", "es_scan_body_host_f32")
 
 
 class LibraryMissing(ImportError):
@@ -113,6 +114,11 @@ def lib():
         L.es_body_source.restype = ctypes.c_int
         L.es_body_prepare.argtypes = [P, ctypes.c_int, ctypes.c_int, i64p, ctypes.c_int]
         L.es_body_prepare.restype = ctypes.c_int
+        hsig = sig[:-1] + [P, P, ctypes.POINTER(P), P, ctypes.c_int, P]   # ..., out_h, init_d, seqs_d, out_d, chunks, stream
+        L.es_scan_host_f32.argtypes = hsig
+        L.es_scan_host_f32.restype = ctypes.c_int
+        L.es_scan_body_host_f32.argtypes = [P] + hsig[1:]
+        L.es_scan_body_host_f32.restype = ctypes.c_int
         L.es_scan_body_backward_f32.argtypes = [P] + bsig[1:] + [P]
         L.es_scan_body_backward_f32.restype = ctypes.c_int
         L.es_plan_body_backward_f32.argtypes = [P] + bsig[1:] + [ctypes.POINTER(PlanInfo)]
@@ -256,24 +262,42 @@ def scan_into(body, initial, seqs, out, axis: int = 0, state_axis: bool = False,
     return out
 
 
+def _host_args(initial_h, seqs_h, out_h, dev_bufs):
+    init_d, seqs_d, out_d = dev_bufs
+    for t, nm in [(initial_h, "initial_h"), (out_h, "out_h")] + [(h, "sequence %d" % k) for k, h in enumerate(seqs_h)]:
+        if t.is_cuda or not t.is_contiguous() or str(t.dtype) != "torch.float32":
+            raise TypeError("%s must be a contiguous float32 host tensor" % nm)
+    _require_cuda_f32(init_d, "initial_d")
+    _require_cuda_f32(out_d, "out_d")
+    for k, d in enumerate(seqs_d):
+        _require_cuda_f32(d, "device sequence %d" % k)
+    n = len(seqs_h)
+    hp = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in seqs_h])
+    dp = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in seqs_d])
+    return init_d, out_d, hp, dp
+
+
 def scan_host(body, initial_h, seqs_h, out_h, dev_bufs, axis: int = 0, state_axis: bool = False,
-              reverse: bool = False, stream=None):
-    """End-to-end call on host tensors: copy the inputs from (pinned) host
-    memory into the caller's device buffers, scan, copy the states back.
+              reverse: bool = False, stream=None, chunks: int = 0):
+    """End-to-end call on host tensors (es_scan_host_f32): the library copies
+    the inputs from (pinned) host memory into the caller's device buffers,
+    scans and copies the states back, in row pieces that overlap.
 
     ``dev_bufs`` = (initial_d, [x_d, a_d], out_d), preallocated by the caller.
     Asynchronous on ``stream``; synchronise before reading ``out_h``.
     """
     import torch
-    init_d, seqs_d, out_d = dev_bufs
+    init_d, out_d, hp, dp = _host_args(initial_h, seqs_h, out_h, dev_bufs)
+    shape = list(out_h.shape)
+    state_width = shape[-1] if state_axis else 0
+    seq_widths = [int(t.shape[-1]) for t in seqs_h] if state_axis else None
+    b, shp, rank, ax, sw_, widths = _args(body, shape, axis, state_width, seq_widths)
     if stream is None:
         stream = torch.cuda.current_stream(out_d.device)
-    with torch.cuda.stream(stream):
-        init_d.copy_(initial_h, non_blocking=True)
-        for d, h in zip(seqs_d, seqs_h):
-            d.copy_(h, non_blocking=True)
-        scan_into(body, init_d, seqs_d, out_d, axis=axis, state_axis=state_axis, reverse=reverse, stream=stream)
-        out_h.copy_(out_d, non_blocking=True)
+    handle = stream if isinstance(stream, int) else stream.cuda_stream
+    _check(lib().es_scan_host_f32(b, initial_h.data_ptr(), hp, len(seqs_h), shp, rank, ax, sw_, widths,
+                                  int(bool(reverse)), out_h.data_ptr(), init_d.data_ptr(), dp, out_d.data_ptr(),
+                                  int(chunks), handle))
     return out_h
 
 
@@ -544,20 +568,24 @@ class Body:
         return out
 
     def scan_host(self, initial_h, seqs_h, out_h, dev_bufs, axis: int = 0, state_axis: bool = False,
-                  reverse: bool = False, stream=None):
-        """End-to-end call on host tensors (see ``scan_host``): copy the inputs
-        into the caller's device buffers, scan, copy the states back.
-        Asynchronous on ``stream``; synchronise before reading ``out_h``."""
+                  reverse: bool = False, stream=None, chunks: int = 0):
+        """End-to-end call on host tensors (es_scan_body_host_f32; see the
+        module's ``scan_host``).  Asynchronous on ``stream``; synchronise
+        before reading ``out_h``."""
         import torch
-        init_d, seqs_d, out_d = dev_bufs
+        init_d, out_d, hp, dp = _host_args(initial_h, seqs_h, out_h, dev_bufs)
+        shape = list(out_h.shape)
+        n = len(seqs_h)
+        rank = len(shape)
+        shp = (ctypes.c_int64 * max(rank, 1))(*shape)
+        state_width = shape[-1] if state_axis else 0
+        sw = _widths_array([int(t.shape[-1]) for t in seqs_h]) if state_axis else None
         if stream is None:
             stream = torch.cuda.current_stream(out_d.device)
-        with torch.cuda.stream(stream):
-            init_d.copy_(initial_h, non_blocking=True)
-            for d, h in zip(seqs_d, seqs_h):
-                d.copy_(h, non_blocking=True)
-            self.scan_into(init_d, seqs_d, out_d, axis=axis, state_axis=state_axis, reverse=reverse, stream=stream)
-            out_h.copy_(out_d, non_blocking=True)
+        handle = stream if isinstance(stream, int) else stream.cuda_stream
+        _check(lib().es_scan_body_host_f32(self._h, initial_h.data_ptr(), hp, n, shp, rank, int(axis),
+                                           int(state_width), sw, int(bool(reverse)), out_h.data_ptr(),
+                                           init_d.data_ptr(), dp, out_d.data_ptr(), int(chunks), handle))
         return out_h
 
 

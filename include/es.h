@@ -166,6 +166,36 @@ es_status es_scan_backward_f32(es_body body, const float *initial, const float *
                                const float *states, const float *grad_out, float *grad_initial,
                                float *const *grad_seqs, es_stream_t stream);
 
+/*
+ * es_scan_host_f32 -- es_scan_f32 end to end on HOST buffers: the inputs are
+ * copied into the caller's device buffers, scanned, and the states copied
+ * back to `out_h`.  Lanes are independent ("Storage and execution"), so when
+ * the sequence axis is not the first dimension the call splits along the
+ * first dimension into `chunks` row pieces (0: the library's default, 8; at
+ * most 64; never more than the rows), each a complete smaller scan, and
+ * pipelines them on three library-owned streams: one piece's host-to-device
+ * copies, another's scan and a third's device-to-host copy run at once.  The
+ * results are those of es_scan_f32 on the whole call, bit for bit.
+ *
+ *   body .. reverse   as for es_scan_f32.
+ *   initial_h, seqs_h (a HOST array of host pointers), out_h
+ *                     host buffers of the call's shapes; page-locked memory
+ *                     lets the copies overlap.
+ *   initial_d, seqs_d (a HOST array of device pointers), out_d
+ *                     caller-owned device buffers of the same shapes.
+ *   chunks            pieces (see above).
+ *   stream            the call starts after earlier work on `stream`, and
+ *                     work enqueued on `stream` after it waits for all of it
+ *                     (events); read out_h after synchronising `stream`.
+ * No allocation per call (the streams and events are created once per
+ * device).  Statuses as for es_scan_f32.
+ */
+es_status es_scan_host_f32(es_body body, const float *initial_h, const float *const *seqs_h,
+                           int n_seqs, const int64_t *shape, int rank, int axis,
+                           int state_width, const int64_t *seq_widths, int reverse,
+                           float *out_h, float *initial_d, float *const *seqs_d, float *out_d,
+                           int chunks, es_stream_t stream);
+
 /* Plan of a backward call (validation and kernel path, no CUDA call). */
 es_status es_plan_backward_f32(es_body body, const float *initial, const float *const *seqs,
                                int n_seqs, const int64_t *shape, int rank, int axis,
@@ -245,6 +275,14 @@ es_status es_body_source(es_body_t body, int state_width, int n_seqs, const int6
  * compiler's log. */
 es_status es_body_prepare(es_body_t body, int state_width, int n_seqs, const int64_t *seq_widths,
                           int path);
+
+/* es_scan_host_f32 with a body program (arguments as for es_scan_host_f32,
+ * with the program in place of the body id). */
+es_status es_scan_body_host_f32(es_body_t body, const float *initial_h, const float *const *seqs_h,
+                                int n_seqs, const int64_t *shape, int rank, int axis,
+                                int state_width, const int64_t *seq_widths, int reverse,
+                                float *out_h, float *initial_d, float *const *seqs_d, float *out_d,
+                                int chunks, es_stream_t stream);
 
 /* NVRTC compilations so far in this process (kernel cache misses). */
 uint64_t es_body_compile_count(void);
