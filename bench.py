@@ -611,9 +611,10 @@ def run_ours(args, w):
 # matrix-scan / linear-scan workloads
 
 MATRIX_KERNEL = {"mat_tma": "k_mat_tma", "generic": "k_mat_generic", "lane_tma": "k_body_lane",
-                 "time_tma": "k_body_time", "mat_chunked": "k_mat_chunk_final"}
+                 "time_tma": "k_body_time", "mat_chunked": "k_mat_chunk_final",
+                 "mat_chunked_tma": "k_mat_tma_chunked"}
 KERNEL_SOURCES.update({k: ["k_matrix.cu", "es_matrix_api.cu"]
-                       for k in ("k_mat_tma", "k_mat_generic", "k_mat_chunk_final")})
+                       for k in ("k_mat_tma", "k_mat_generic", "k_mat_chunk_final", "k_mat_tma_chunked")})
 
 
 def matrix_scan_call(es, w, a, b, out, reverse, stream, workspace=None):
@@ -795,12 +796,13 @@ class OpJob:
         es, w = self.es, self.w
         if self.table:
             return es.plan_table_scan(w.n_states, w.n_syms, w.shape, w.axis)
-        if self.workspace is not None and es.matrix_scan_workspace(w.a_shape, w.b_shape, w.axis, w.projective):
-            return {"path": "mat_chunked"}
+        if self.workspace is not None:
+            return es.plan_matrix_scan_ws(w.a_shape, w.b_shape, self.workspace.numel(), w.axis, reverse,
+                                          w.projective)
         return matrix_plan(es, w, reverse)
 
     def launches_per_call(self):
-        return 3 if self.plan(False)["path"] == "mat_chunked" else 1
+        return 3 if self.plan(False)["path"] in ("mat_chunked", "mat_chunked_tma") else 1
 
     def config(self):
         return table_config(self.w) if self.table else matrix_config(self.w)
@@ -851,10 +853,12 @@ def run_ours_op(args, w):
     else:
         kernel = job.kernels.get(plans[0]["path"], plans[0]["path"])
         roofline = roofline_of(kernel, w.name, w.algorithmic_bytes(), kernel_ms)
-    if not backward and plans[0]["path"] == "mat_chunked":
+    if not backward and plans[0]["path"] in ("mat_chunked", "mat_chunked_tma"):
         # three launches make one call: `achieved` is the whole call's
-        # algorithmic bytes over its time (the final pass alone is ~60%)
-        roofline["kernel"] = "k_mat_chunk_local + k_mat_chunk_carry + k_mat_chunk_final"
+        # algorithmic bytes over its time
+        roofline["kernel"] = ("k_mat_tma (chunk pass) + k_mat_chunk_link + k_mat_tma (final pass)"
+                              if plans[0]["path"] == "mat_chunked_tma" else
+                              "k_mat_chunk_local + k_mat_chunk_carry + k_mat_chunk_final")
         roofline["kernel_ms"] = kernel_ms
         roofline["note"] = ("a call of three launches timed as one; its DRAM traffic is about 5/3 of the "
                             "algorithmic bytes (a and b are read in the first and the last pass)")

@@ -12,7 +12,7 @@ _BINDING_NAMES = {
     "TANH_DECAY", "NORMCAP", "MAXPLUS", "device_status", "plan", "status_string",
     "launch_count", "set_path_override", "set_wait_limit_ns", "set_drop_tile", "scan_backward", "plan_backward",
     "Body", "body_compile_count", "matrix_scan", "plan_matrix_scan", "linear_scan", "plan_linear_scan",
-    "table_scan", "plan_table_scan", "matrix_scan_workspace", "matrix_scan_ws",
+    "table_scan", "plan_table_scan", "matrix_scan_workspace", "matrix_scan_ws", "plan_matrix_scan_ws",
     "matrix_scan_static", "matrix_scan_backward", "plan_matrix_scan_backward", "linear_scan_backward",
     "plan_linear_scan_backward",
 }

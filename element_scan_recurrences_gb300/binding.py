@@ -24,7 +24,7 @@ STATUS = {0: "ES_OK", 1: "ES_E_DIM_001", 2: "ES_E_DIM_002", 3: "ES_E_ARG", 4: "E
           5: "ES_E_CUDA", 6: "ES_E_TIMEOUT", 7: "ES_E_BODY"}
 MAX_SEQS = 8
 PATHS = {0: "auto", 1: "empty", 2: "generic", 3: "lane_tma", 4: "time_tma", 5: "vec_tma", 6: "mat_tma",
-         7: "mat_chunked"}
+         7: "mat_chunked", 8: "mat_chunked_tma"}
 PATH_IDS = {v: k for k, v in PATHS.items()}
 
 # every function include/es.h declares
@@ -34,6 +34,7 @@ EXPORTS = ("es_scan_f32", "es_plan_f32", "es_scan_backward_f32", "es_plan_backwa
            "es_plan_body_f32", "es_body_source", "es_body_prepare", "es_body_compile_count", "es_matrix_scan_f32",
            "es_plan_matrix_scan_f32", "es_linear_scan_f32", "es_plan_linear_scan_f32", "es_table_scan_i32",
            "es_plan_table_scan_i32", "es_matrix_scan_workspace_f32", "es_matrix_scan_ws_f32",
+           "es_plan_matrix_scan_ws_f32",
            "es_matrix_scan_static_f32", "es_scan_body_backward_f32", "es_plan_body_backward_f32",
            "es_body_source_backward", "es_body_prepare_backward", "es_matrix_scan_backward_f32",
            "es_plan_matrix_scan_backward_f32", "es_linear_scan_backward_f32", "es_plan_linear_scan_backward_f32",
@@ -144,6 +145,9 @@ def lib():
         L.es_matrix_scan_workspace_f32.restype = ctypes.c_int
         L.es_matrix_scan_ws_f32.argtypes = msig + [ctypes.c_int, P, P, ctypes.c_size_t, P]
         L.es_matrix_scan_ws_f32.restype = ctypes.c_int
+        L.es_plan_matrix_scan_ws_f32.argtypes = msig + [ctypes.c_int, P, P, ctypes.c_size_t,
+                                                        ctypes.POINTER(PlanInfo)]
+        L.es_plan_matrix_scan_ws_f32.restype = ctypes.c_int
         L.es_matrix_scan_static_f32.argtypes = msig + [ctypes.c_int, P, P]
         # ..., projective, states, grad_out, grad_a, grad_b
         L.es_matrix_scan_backward_f32.argtypes = msig + [ctypes.c_int, P, P, P, P, P]
@@ -660,6 +664,22 @@ def matrix_scan_workspace(a_shape, b_shape, axis: int = 0, projective: bool = Fa
     n = ctypes.c_size_t()
     _check(lib().es_matrix_scan_workspace_f32(sa, ra, sb, rb, int(axis), int(bool(projective)), ctypes.byref(n)))
     return int(n.value)
+
+
+def plan_matrix_scan_ws(a_shape, b_shape, workspace_bytes: int, axis: int = 0, reverse: bool = False,
+                        projective: bool = False, ptrs: Optional[Sequence[int]] = None) -> dict:
+    """The checks and the kernel path of ``matrix_scan_ws`` with a workspace
+    of ``workspace_bytes``, without a GPU.  ``ptrs`` = (a, b, out, workspace),
+    by default 16-byte aligned, non-overlapping stand-ins."""
+    if ptrs is None:
+        ptrs = [(k + 1) << 44 for k in range(4)]
+    sa, ra = _shape_array(a_shape)
+    sb, rb = _shape_array(b_shape)
+    info = PlanInfo()
+    _check(lib().es_plan_matrix_scan_ws_f32(ptrs[0], sa, ra, ptrs[1], sb, rb, int(axis), int(bool(reverse)),
+                                            int(bool(projective)), ptrs[2], ptrs[3] if workspace_bytes else None,
+                                            int(workspace_bytes), ctypes.byref(info)))
+    return _info(info)
 
 
 def matrix_scan_ws(a, b, workspace, axis: int = 0, reverse: bool = False, projective: bool = False, out=None,

@@ -498,7 +498,8 @@ uint64_t es_launch_count(void) { return g_launches.load(); }
 
 es_status es_set_path_override(int path) {
     if (path != ES_PATH_AUTO && path != ES_PATH_GENERIC && path != ES_PATH_LANE_TMA && path != ES_PATH_TIME_TMA &&
-        path != ES_PATH_VEC_TMA && path != ES_PATH_MAT_TMA && path != ES_PATH_MAT_CHUNKED)
+        path != ES_PATH_VEC_TMA && path != ES_PATH_MAT_TMA && path != ES_PATH_MAT_CHUNKED &&
+        path != ES_PATH_MAT_CHUNKED_TMA)
         return fail(ES_E_ARG, "es_set_path_override: unknown path %d", path);
     g_path_override.store(path);
     return ES_OK;

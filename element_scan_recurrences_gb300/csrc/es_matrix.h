@@ -52,6 +52,11 @@ cudaError_t launch_mat_tma(const MatLaunch& L, const char** err);
 void mat_chunk_shape(int64_t lanes, int64_t T, int m, int64_t* chunks, int64_t* chunk);
 size_t mat_chunk_workspace_bytes(int n, int m, int64_t lanes, int64_t chunks);
 cudaError_t launch_mat_chunked(const MatLaunch& L, float* ws, int64_t chunks, int64_t chunk);
+// The same chunked scan with its two scan passes on the TMA kernel (dense
+// operands as the TMA kernel takes them, n + m <= 32) and a pipelined link
+// pass; the same workspace layout, the same results bit for bit.
+bool mat_chunked_tma_ok(const MatLaunch& L, bool dense, int64_t chunks, int64_t chunk);
+cudaError_t launch_mat_chunked_tma(const MatLaunch& L, float* ws, int64_t chunks, int64_t chunk, const char** err);
 
 // The TMA kernel serves dense operands with n in {2, 4, 8, 16}, 16-byte
 // aligned bases, n*m a multiple of 4 and at most 256, and a lane group of at

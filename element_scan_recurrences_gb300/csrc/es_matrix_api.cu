@@ -388,6 +388,63 @@ es_status es_matrix_scan_workspace_f32(const int64_t* a_shape, int a_rank, const
     return ES_OK;
 }
 
+}  // extern "C"
+
+namespace es {
+
+// the path es_matrix_scan_ws_f32 takes with this workspace: the chunked scan
+// (on the TMA kernel where it takes the operands, else the direct-load chunk
+// kernels, the same arithmetic) or the sequential choice of
+// es_matrix_scan_f32; ws_chunked set for the former
+es_status plan_matrix_ws(const char* fn, MatPlan* P, const void* workspace, size_t workspace_bytes,
+                         int64_t* chunks, int64_t* chunk, bool* ws_chunked) {
+    *ws_chunked = false;
+    if (P->empty) return ES_OK;
+    const size_t need = chunked_applies(*P) ? chunked_workspace(*P, chunks, chunk) : 0;
+    const int forced = api_path_override();
+    const bool want = forced == ES_PATH_AUTO || forced == ES_PATH_MAT_CHUNKED || forced == ES_PATH_MAT_CHUNKED_TMA;
+    if (!(need > 0 && workspace != nullptr && workspace_bytes >= need && want)) {
+        if (forced == ES_PATH_MAT_CHUNKED || forced == ES_PATH_MAT_CHUNKED_TMA)
+            return api_fail(ES_E_UNSUPPORTED, "%s: the chunked path needs few long lanes and %zu workspace bytes",
+                            fn, need);
+        return choose_matrix_path(fn, P);
+    }
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return api_fail(ES_E_ARG, "%s: workspace not 16-byte aligned", fn);
+    const uintptr_t wlo = reinterpret_cast<uintptr_t>(workspace), whi = wlo + need;
+    const void* ops[3] = {P->L.a, P->L.b, P->L.out};
+    const int64_t cnt[3] = {P->n_a, P->n_b, P->n_out};
+    for (int k = 0; k < 3; ++k) {
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(ops[k]), hi = lo + static_cast<uintptr_t>(cnt[k]) * 4;
+        if (lo < whi && wlo < hi) return api_fail(ES_E_ARG, "%s: the workspace overlaps an operand", fn);
+    }
+    const bool tma = forced != ES_PATH_MAT_CHUNKED && mat_chunked_tma_ok(P->L, P->dense, *chunks, *chunk);
+    if (forced == ES_PATH_MAT_CHUNKED_TMA && !tma)
+        return api_fail(ES_E_UNSUPPORTED, "%s: the forced kernel path %d cannot serve this call", fn, forced);
+    P->path = tma ? ES_PATH_MAT_CHUNKED_TMA : ES_PATH_MAT_CHUNKED;
+    *ws_chunked = true;
+    return ES_OK;
+}
+
+}  // namespace es
+
+extern "C" {
+
+es_status es_plan_matrix_scan_ws_f32(const float* a, const int64_t* a_shape, int a_rank, const float* b,
+                                     const int64_t* b_shape, int b_rank, int axis, int reverse, int projective,
+                                     const float* out, const void* workspace, size_t workspace_bytes,
+                                     es_plan_info* info) {
+    const char* fn = "es_matrix_scan_ws_f32";
+    es::MatPlan P{};
+    es_status st = es::plan_matrix(fn, a, a_shape, a_rank, b, b_shape, b_rank, axis, reverse, projective,
+                                   const_cast<float*>(out), false, &P);
+    int64_t chunks = 0, chunk = 0;
+    bool ws_chunked = false;
+    if (st == ES_OK) st = es::plan_matrix_ws(fn, &P, workspace, workspace_bytes, &chunks, &chunk, &ws_chunked);
+    if (st != ES_OK) return st;
+    es::fill_matrix_info(P, info);
+    return ES_OK;
+}
+
 es_status es_matrix_scan_ws_f32(const float* a, const int64_t* a_shape, int a_rank, const float* b,
                                 const int64_t* b_shape, int b_rank, int axis, int reverse, int projective, float* out,
                                 void* workspace, size_t workspace_bytes, es_stream_t stream) {
@@ -397,31 +454,28 @@ es_status es_matrix_scan_ws_f32(const float* a, const int64_t* a_shape, int a_ra
                                    &P);
     if (st != ES_OK || P.empty) return st;
     int64_t chunks = 0, chunk = 0;
-    const size_t need = es::chunked_applies(P) ? es::chunked_workspace(P, &chunks, &chunk) : 0;
-    const int forced = es::api_path_override();
-    const bool chunked = need > 0 && workspace != nullptr && workspace_bytes >= need &&
-                         (forced == ES_PATH_AUTO || forced == ES_PATH_MAT_CHUNKED);
-    if (!chunked) {
-        if (forced == ES_PATH_MAT_CHUNKED)
-            return es::api_fail(ES_E_UNSUPPORTED, "%s: the chunked path needs few long lanes and %zu workspace bytes",
-                                fn, need);
-        if ((st = es::choose_matrix_path(fn, &P)) != ES_OK) return st;
-        return es::launch_matrix(fn, &P, reinterpret_cast<cudaStream_t>(stream));
-    }
-    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return es::api_fail(ES_E_ARG, "%s: workspace not 16-byte aligned", fn);
-    const uintptr_t wlo = reinterpret_cast<uintptr_t>(workspace), whi = wlo + need;
-    const void* ops[3] = {a, b, out};
-    const int64_t cnt[3] = {P.n_a, P.n_b, P.n_out};
-    for (int k = 0; k < 3; ++k) {
-        const uintptr_t lo = reinterpret_cast<uintptr_t>(ops[k]), hi = lo + static_cast<uintptr_t>(cnt[k]) * 4;
-        if (lo < whi && wlo < hi) return es::api_fail(ES_E_ARG, "%s: the workspace overlaps an operand", fn);
-    }
+    bool ws_chunked = false;
+    if ((st = es::plan_matrix_ws(fn, &P, workspace, workspace_bytes, &chunks, &chunk, &ws_chunked)) != ES_OK)
+        return st;
+    if (!ws_chunked) return es::launch_matrix(fn, &P, reinterpret_cast<cudaStream_t>(stream));
     int dev = 0;
     es::DeviceState* ds = nullptr;
     if ((st = es::api_device(&dev, &ds)) != ES_OK) return st;
-    P.L.stream = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = es::launch_mat_chunked(P.L, static_cast<float*>(workspace), chunks, chunk);
-    if (e != cudaSuccess) return es::api_fail(ES_E_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+    es::MatLaunch& L = P.L;
+    L.stream = reinterpret_cast<cudaStream_t>(stream);
+    L.status = ds->status;
+    L.wait_ns = es::api_wait_ns();
+    L.drop_tile = es::api_drop_tile();
+    L.num_sms = ds->num_sms;
+    const char* msg = nullptr;
+    cudaError_t e;
+    if (P.path == ES_PATH_MAT_CHUNKED_TMA) {
+        if ((st = es::api_encoder(&L.encode)) != ES_OK) return st;
+        e = es::launch_mat_chunked_tma(L, static_cast<float*>(workspace), chunks, chunk, &msg);
+    } else {
+        e = es::launch_mat_chunked(L, static_cast<float*>(workspace), chunks, chunk);
+    }
+    if (e != cudaSuccess) return es::api_fail(ES_E_CUDA, "%s: %s", fn, msg != nullptr ? msg : cudaGetErrorString(e));
     es::count_launch(3);
     return ES_OK;
 }

@@ -185,15 +185,34 @@ k_mat_generic(const float* __restrict__ a, const float* __restrict__ b, float* _
 constexpr int kMatMaxStages = 4;
 constexpr int kMatConsumers = 128;
 
+// What a launch of the row-group kernel computes:
+//   kMatFull   the whole scan of each lane, every state stored;
+//   kMatLocal  the first pass of the chunked scan: each CTA lane is one
+//              chunk of trips of one scan lane, scanned from zero, with its
+//              transition product (the chunk's a, from the identity, no b) in
+//              n more column threads; only the chunk's last state and product
+//              are written, to the workspace;
+//   kMatFinal  the last pass: each chunk scanned again from its carry (read
+//              from the workspace), every state stored.
+// In the chunk modes a CTA's LPC lanes are LPC consecutive chunks of one scan
+// lane, each streamed as its own {block, 1, TT} box.  A chunk's trips that
+// fall outside the axis (the short chunk) arrive zero-filled and leave the
+// state as it was.
+enum : int { kMatFull = 0, kMatLocal = 1, kMatFinal = 2 };
+
 // TRANS (the gradient's cotangent scan): the step's coefficient is
 // a[t + a_shift]^T; the a tile is loaded a_shift trips off the b tile, and
 // TMA's zero fill past either end of the axis is the zero matrix.
-template <int N, int R, bool PROJ, bool TRANS>
-__global__ void __launch_bounds__(32 + kMatConsumers)
+template <int N, int R, bool PROJ, bool TRANS, int MODE>
+__global__ void __launch_bounds__(32 + kMatConsumers, 1)
 k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-          float* __restrict__ out, int T, int J, int m, int gp, int LPC, int tiles_j, int TT, int stages,
-          int reverse, int a_shift, unsigned int* status, uint64_t wait_ns, int64_t drop_tile) {
+          float* __restrict__ out, float* __restrict__ ws, int T, int J, int m, int gp, int LPC, int tiles_j, int TT,
+          int stages, int reverse, int a_shift, int chunks, int chunk, int chunk_off, unsigned int* status,
+          uint64_t wait_ns, int64_t drop_tile) {
+    constexpr bool kChunk = MODE != kMatFull;
+    constexpr bool kIdent = PROJ || MODE == kMatLocal;     // columns that carry a product from the identity
     static_assert(!(PROJ && TRANS), "a projective scan has no gradient");
+    static_assert(!kChunk || (!PROJ && !TRANS), "the chunked passes are plain scans");
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMatMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kMatMaxStages];
@@ -201,17 +220,32 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
 
     const int TPL = gp * R;                                 // threads per lane
     const int consumers = LPC * TPL;                        // a multiple of 32, at most kMatConsumers
-    const uint32_t a_floats = static_cast<uint32_t>(TT) * LPC * N * N;
-    const uint32_t b_floats = static_cast<uint32_t>(TT) * LPC * N * m;
-    // every tile starts on a 128-byte boundary
-    const uint32_t a_pad = (a_floats + 31u) & ~31u;
-    const uint32_t stage_floats = (a_pad + b_floats + 31u) & ~31u;
-    const uint32_t stage_bytes = (a_floats + b_floats) * 4u;   // bytes the two copies bring
+    // a stage: the a region, then the b region, each on a 128-byte boundary;
+    // in the chunk modes each lane's box also starts on one
+    const uint32_t la = kChunk ? (static_cast<uint32_t>(TT) * N * N + 31u) & ~31u : 0u;
+    const uint32_t lb = kChunk ? (static_cast<uint32_t>(TT) * N * m + 31u) & ~31u : 0u;
+    const uint32_t a_region = kChunk ? LPC * la : static_cast<uint32_t>(TT) * LPC * N * N;
+    const uint32_t b_region = kChunk ? LPC * lb : static_cast<uint32_t>(TT) * LPC * N * m;
+    const uint32_t a_pad = (a_region + 31u) & ~31u;
+    const uint32_t stage_floats = (a_pad + b_region + 31u) & ~31u;
+    const uint32_t stage_bytes = static_cast<uint32_t>(TT) * LPC * (N * N + N * m) * 4u;   // bytes the copies bring
     float* tiles = reinterpret_cast<float*>(smem_raw + smem_align_pad(smem_raw));
 
-    const int o = blockIdx.x / tiles_j;
-    const int j0 = (blockIdx.x % tiles_j) * LPC;
-    const int ntiles = (T + TT - 1) / TT;
+    // full: CTA = (o, a tile of LPC lanes along J); chunk modes: CTA = (scan
+    // lane o * J + j, a group of LPC chunks)
+    int o, jj, c0;
+    if constexpr (kChunk) {
+        const int lane_id = blockIdx.x / tiles_j;
+        o = lane_id / J;
+        jj = lane_id % J;
+        c0 = (blockIdx.x % tiles_j) * LPC;
+    } else {
+        o = blockIdx.x / tiles_j;
+        jj = (blockIdx.x % tiles_j) * LPC;
+        c0 = 0;
+    }
+    const int span = kChunk ? chunk : T;                   // trips a CTA lane scans
+    const int ntiles = (span + TT - 1) / TT;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -243,8 +277,19 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
                 const int jt = reverse ? ntiles - 1 - k : k;
                 float* st = tiles + static_cast<size_t>(s) * stage_floats;
                 mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
-                tma_load_4d(st, &map_a, 0, j0, jt * TT + a_shift, o, &full_bar[s], pol);
-                tma_load_4d(st + a_pad, &map_b, 0, j0, jt * TT, o, &full_bar[s], pol);
+                if constexpr (kChunk) {
+                    for (int l = 0; l < LPC; ++l) {
+                        // the chunk's trips from jt * TT; past the axis (and
+                        // for lanes past the last chunk) the box is zero-filled
+                        const int64_t t = static_cast<int64_t>(c0 + l) * chunk - chunk_off + jt * TT;
+                        const int ct = static_cast<int>(t < T ? t : T);
+                        tma_load_4d(st + l * la, &map_a, 0, jj, ct, o, &full_bar[s], pol);
+                        tma_load_4d(st + a_pad + l * lb, &map_b, 0, jj, ct, o, &full_bar[s], pol);
+                    }
+                } else {
+                    tma_load_4d(st, &map_a, 0, jj, jt * TT + a_shift, o, &full_bar[s], pol);
+                    tma_load_4d(st + a_pad, &map_b, 0, jj, jt * TT, o, &full_bar[s], pol);
+                }
             }
             for (int k = max(0, issued - stages); k < issued; ++k) {
                 if (k == drop_tile) continue;
@@ -255,25 +300,36 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
         return;
     }
 
-    // consumers: thread (l, g, c) is row group g of column c of lane j0 + l
+    // consumers: thread (l, g, c) is row group g of column c of CTA lane l
     const int ct = threadIdx.x - 32;
     const int l = ct / TPL;
     const int w = ct % TPL;
     const int g = w / gp;
     const int c = w % gp;
-    const bool valid = j0 + l < J;
+    const bool valid = kChunk ? c0 + l < chunks : jj + l < J;
     const bool is_h = c < m;
-    const bool is_p = PROJ && !is_h && c < m + N;
+    const bool is_p = kIdent && !is_h && c < m + N;
     constexpr int RPT = N / R;                              // rows per thread
     // warp lane of this column's row group 0
     const int col_base = (lane & ~(TPL - 1)) + c;
     const int64_t lane_block = static_cast<int64_t>(N) * m;          // floats of h per lane and trip
-    float* obase = out + (static_cast<int64_t>(o) * T * J + j0 + l) * lane_block + c;
+    float* obase = out + (static_cast<int64_t>(o) * T * J + (kChunk ? jj : jj + l)) * lane_block + c;
     const int64_t trip_stride = static_cast<int64_t>(J) * lane_block;
+    // chunk modes: the chunk's first trip on the axis and its workspace unit
+    // (units of a scan lane in scan order)
+    const int64_t tbase = kChunk ? static_cast<int64_t>(c0 + l) * chunk - chunk_off : 0;
+    const int64_t unit = static_cast<int64_t>(blockIdx.x / tiles_j) * chunks + (reverse ? chunks - 1 - (c0 + l) : c0 + l);
+    const int64_t unit_floats = static_cast<int64_t>(N) * N + 2LL * N * m;
     // the column's whole state (every row), the same in all its row groups
     float h[N];
+    if constexpr (MODE == kMatFinal) {
+        const float* carry = ws + unit * unit_floats + N * N + N * m;
 #pragma unroll
-    for (int i = 0; i < N; ++i) h[i] = (is_p && i == c - m) ? 1.0f : 0.0f;
+        for (int i = 0; i < N; ++i) h[i] = (valid && is_h) ? carry[i * m + c] : 0.0f;
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) h[i] = (is_p && i == c - m) ? 1.0f : 0.0f;
+    }
 
     for (int k = 0; k < ntiles; ++k) {
         const int s = k % stages;
@@ -284,14 +340,18 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
         }
         const int jt = reverse ? ntiles - 1 - k : k;
         const int t0 = jt * TT;
-        const int n = min(TT, T - t0);
+        const int n = min(TT, span - t0);
         const float* sa = tiles + static_cast<size_t>(s) * stage_floats;
         const float* sb = sa + a_pad;
         // one trip: this thread's rows of a @ h + b (scaled when projective),
         // stored, then the whole new column gathered into h
         auto trip = [&](const int tt, float (&mine)[RPT]) {
-            const float* A = sa + (static_cast<uint32_t>(tt) * LPC + l) * (N * N);
-            const float* B = sb + (static_cast<uint32_t>(tt) * LPC + l) * (N * m) + c;
+            const float* A = kChunk ? sa + l * la + tt * (N * N) : sa + (static_cast<uint32_t>(tt) * LPC + l) * (N * N);
+            // columns past m (a product's) read no b: their pointer stays in the block
+            const float* B = (kChunk ? sb + l * lb + tt * (N * m) : sb + (static_cast<uint32_t>(tt) * LPC + l) * (N * m)) +
+                             (is_h ? c : 0);
+            const int64_t t = kChunk ? tbase + t0 + tt : t0 + tt;
+            const bool live = !kChunk || (t >= 0 && t < T);
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
                 const int i = r * R + g;
@@ -321,14 +381,18 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
 #pragma unroll
                 for (int r = 0; r < RPT; ++r) mine[r] = __fdiv_rn(mine[r], sc);
             }
-            if (valid && is_h) {
-                float* op = obase + static_cast<int64_t>(t0 + tt) * trip_stride;
+            if (MODE != kMatLocal && valid && is_h && live) {
+                float* op = obase + t * trip_stride;
 #pragma unroll
                 for (int r = 0; r < RPT; ++r) __stcs(op + (r * R + g) * m, mine[r]);
             }
-            // row i lives in row group i % R at position i / R
+            // row i lives in row group i % R at position i / R (a trip off
+            // the axis keeps the state: the same for the whole lane group)
 #pragma unroll
-            for (int i = 0; i < N; ++i) h[i] = __shfl_sync(0xffffffffu, mine[i / R], col_base + (i % R) * gp);
+            for (int i = 0; i < N; ++i) {
+                const float v = __shfl_sync(0xffffffffu, mine[i / R], col_base + (i % R) * gp);
+                h[i] = live ? v : h[i];
+            }
         };
         // two register sets by trip parity: a trip never overwrites the
         // registers the previous trip's stores may still be reading
@@ -341,6 +405,18 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
         if (q < n) trip(reverse ? n - 1 - q : q, ma);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
+    }
+    if constexpr (MODE == kMatLocal) {
+        // the chunk's last state (u) and transition product (Phi), written
+        // once by row group 0
+        if (valid && g == 0 && (is_h || is_p)) {
+            float* wu = ws + unit * unit_floats;
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                if (is_h) wu[N * N + i * m + c] = h[i];
+                else wu[i * N + (c - m)] = h[i];
+            }
+        }
     }
 }
 
@@ -459,33 +535,53 @@ cudaError_t launch_generic_n(const MatLaunch& L) {
     return cudaGetLastError();
 }
 
-template <int N, int R>
-cudaError_t launch_tma_nr(const MatLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb, int lpc, int tiles_j,
-                          int TT, int stages, size_t smem) {
-    auto kern = L.projective ? k_mat_tma<N, R, true, false> : L.trans ? k_mat_tma<N, R, false, true>
-                                                                      : k_mat_tma<N, R, false, false>;
+// the chunk modes' extra arguments (unused by a full scan)
+struct MatChunkArgs {
+    float* ws;
+    int chunks, chunk, chunk_off;
+};
+
+template <int N, int R, int MODE>
+cudaError_t launch_tma_nr(const MatLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb, int gp, int lpc,
+                          int tiles_j, int TT, int stages, size_t smem, const MatChunkArgs& C) {
+    auto kern = MODE != kMatFull ? k_mat_tma<N, R, false, false, MODE>
+                : L.projective   ? k_mat_tma<N, R, true, false, kMatFull>
+                : L.trans        ? k_mat_tma<N, R, false, true, kMatFull>
+                                 : k_mat_tma<N, R, false, false, kMatFull>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(L.O * tiles_j), 32 + lpc * L.gp * R, smem, L.stream>>>(
-        ma, mb, L.out, static_cast<int>(L.T), static_cast<int>(L.J), L.m, L.gp, lpc, tiles_j, TT, stages,
-        L.reverse, L.trans ? L.a_shift : 0, L.status, L.wait_ns, L.drop_tile);
+    const int64_t grid = (MODE != kMatFull ? L.g.lanes : L.O) * tiles_j;
+    kern<<<static_cast<unsigned>(grid), 32 + lpc * gp * R, smem, L.stream>>>(
+        ma, mb, L.out, C.ws, static_cast<int>(L.T), static_cast<int>(L.J), L.m, gp, lpc, tiles_j, TT, stages,
+        L.reverse, L.trans ? L.a_shift : 0, C.chunks, C.chunk, C.chunk_off, L.status, L.wait_ns, L.drop_tile);
     return cudaGetLastError();
 }
 
-template <int N>
-cudaError_t launch_tma_n(const MatLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb, int R, int lpc,
-                         int tiles_j, int TT, int stages, size_t smem) {
+template <int N, int MODE>
+cudaError_t launch_tma_n(const MatLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb, int gp, int R, int lpc,
+                         int tiles_j, int TT, int stages, size_t smem, const MatChunkArgs& C) {
     if constexpr (N >= 16) {
-        if (R == 16) return launch_tma_nr<N, 16>(L, ma, mb, lpc, tiles_j, TT, stages, smem);
+        if (R == 16) return launch_tma_nr<N, 16, MODE>(L, ma, mb, gp, lpc, tiles_j, TT, stages, smem, C);
     }
     if constexpr (N >= 8) {
-        if (R == 8) return launch_tma_nr<N, 8>(L, ma, mb, lpc, tiles_j, TT, stages, smem);
+        if (R == 8) return launch_tma_nr<N, 8, MODE>(L, ma, mb, gp, lpc, tiles_j, TT, stages, smem, C);
     }
     if constexpr (N >= 4) {
-        if (R == 4) return launch_tma_nr<N, 4>(L, ma, mb, lpc, tiles_j, TT, stages, smem);
+        if (R == 4) return launch_tma_nr<N, 4, MODE>(L, ma, mb, gp, lpc, tiles_j, TT, stages, smem, C);
     }
-    if (R == 2) return launch_tma_nr<N, 2>(L, ma, mb, lpc, tiles_j, TT, stages, smem);
-    return launch_tma_nr<N, 1>(L, ma, mb, lpc, tiles_j, TT, stages, smem);
+    if (R == 2) return launch_tma_nr<N, 2, MODE>(L, ma, mb, gp, lpc, tiles_j, TT, stages, smem, C);
+    return launch_tma_nr<N, 1, MODE>(L, ma, mb, gp, lpc, tiles_j, TT, stages, smem, C);
+}
+
+template <int MODE>
+cudaError_t launch_tma_mode(const MatLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb, int gp, int R, int lpc,
+                            int tiles_j, int TT, int stages, size_t smem, const MatChunkArgs& C) {
+    switch (L.n) {
+        case 2: return launch_tma_n<2, MODE>(L, ma, mb, gp, R, lpc, tiles_j, TT, stages, smem, C);
+        case 4: return launch_tma_n<4, MODE>(L, ma, mb, gp, R, lpc, tiles_j, TT, stages, smem, C);
+        case 8: return launch_tma_n<8, MODE>(L, ma, mb, gp, R, lpc, tiles_j, TT, stages, smem, C);
+        default: return launch_tma_n<16, MODE>(L, ma, mb, gp, R, lpc, tiles_j, TT, stages, smem, C);
+    }
 }
 
 // Row groups per column: enough to fill a warp with one lane's threads (at
@@ -500,6 +596,16 @@ void mat_tile_shape(int n, int m, int gp, int* R, int* lpc, int* TT) {
     while (l * tpl > 32 && per_trip(l) > 32 * 1024) l /= 2;
     *lpc = l;
     *TT = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(64, (32 * 1024) / per_trip(l))));
+}
+
+// floats of one pipeline stage as the kernel lays it out (the a region, then
+// the b region, each on a 128-byte boundary; per lane in the chunk modes)
+int64_t mat_stage_floats(int n, int m, int lpc, int TT, bool chunked) {
+    auto up = [](int64_t v) { return (v + 31) & ~int64_t(31); };
+    const int64_t na = static_cast<int64_t>(TT) * n * n, nb = static_cast<int64_t>(TT) * n * m;
+    const int64_t a_region = chunked ? lpc * up(na) : lpc * na;
+    const int64_t b_region = chunked ? lpc * up(nb) : lpc * nb;
+    return up(up(a_region) + b_region);
 }
 
 bool encode_blocks(EncodeTiledFn encode, CUtensorMap* map, const float* base, int64_t block, int64_t J, int64_t T,
@@ -562,9 +668,6 @@ cudaError_t launch_mat_tma(const MatLaunch& L, const char** err) {
     int R = 0, LPC = 0, TT = 0;
     mat_tile_shape(n, m, L.gp, &R, &LPC, &TT);
     const int stages = 3;
-    // a stage as the kernel lays it out: each tile on a 128-byte boundary
-    const int64_t a_pad = (static_cast<int64_t>(TT) * LPC * n * n + 31) & ~int64_t(31);
-    const int64_t stage_floats = (a_pad + static_cast<int64_t>(TT) * LPC * n * m + 31) & ~int64_t(31);
     const int64_t tiles_j = (L.J + LPC - 1) / LPC;
     CUtensorMap ma, mb;
     if (!encode_blocks(L.encode, &ma, L.a, static_cast<int64_t>(n) * n, L.J, L.T, L.O, LPC, TT) ||
@@ -572,14 +675,9 @@ cudaError_t launch_mat_tma(const MatLaunch& L, const char** err) {
         *err = "cuTensorMapEncodeTiled failed for a matrix-scan tile map";
         return cudaErrorInvalidValue;
     }
-    const size_t smem = static_cast<size_t>(stages) * stage_floats * 4 + 1024;
-    const int tj = static_cast<int>(tiles_j);
-    switch (n) {
-        case 2: return launch_tma_n<2>(L, ma, mb, R, LPC, tj, TT, stages, smem);
-        case 4: return launch_tma_n<4>(L, ma, mb, R, LPC, tj, TT, stages, smem);
-        case 8: return launch_tma_n<8>(L, ma, mb, R, LPC, tj, TT, stages, smem);
-        default: return launch_tma_n<16>(L, ma, mb, R, LPC, tj, TT, stages, smem);
-    }
+    const size_t smem = static_cast<size_t>(stages) * mat_stage_floats(n, m, LPC, TT, false) * 4 + 1024;
+    return launch_tma_mode<kMatFull>(L, ma, mb, L.gp, R, LPC, static_cast<int>(tiles_j), TT, stages, smem,
+                                     MatChunkArgs{nullptr, 0, 0, 0});
 }
 
 
@@ -748,6 +846,100 @@ cudaError_t launch_chunked_n(const MatLaunch& L, float* ws, int64_t chunks, int6
     return cudaGetLastError();
 }
 
+// The link pass of the chunked scan on the TMA kernels: one CTA per scan
+// lane, thread (i, c) holding row i of column c of the carry.  The chunks'
+// Phi and u (contiguous at the head of each workspace unit) stream into a
+// ring of kLinkDepth shared-memory slots with 16-byte cp.async copies issued
+// kLinkDepth - 1 chunks ahead; the carry's columns are exchanged through
+// shared memory (two buffers alternate), one CTA barrier per chunk.  The
+// arithmetic is k_mat_chunk_carry's: row i of Phi times the column, products
+// rounded and added in order, then u.
+constexpr int kLinkDepth = 16;
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int K>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(K) : "memory");
+}
+
+template <int N>
+__global__ void __launch_bounds__(256)
+k_mat_chunk_link(float* __restrict__ ws, int m, int chunks) {
+    extern __shared__ float4 link_smem[];
+    const int head = N * N + N * m;                        // Phi and u: the part read (a multiple of 4)
+    const int64_t unit_floats = head + static_cast<int64_t>(N) * m;
+    float* wl = ws + static_cast<int64_t>(blockIdx.x) * chunks * unit_floats;
+    float* ring = reinterpret_cast<float*>(link_smem);     // [kLinkDepth][head]
+    float* cb = ring + kLinkDepth * head;                  // [2][N][m]
+    const int tid = threadIdx.x, nt = blockDim.x;          // N * m threads
+    const int i = tid / m, c = tid % m;
+    auto issue = [&](int k) {
+        if (k < chunks) {
+            const float* src = wl + k * unit_floats;
+            float* dst = ring + (k % kLinkDepth) * head;
+            for (int q = tid; q < head / 4; q += nt) cp_async16(dst + 4 * q, src + 4 * q);
+        }
+        cp_async_commit();   // an empty group past the end keeps the count uniform
+    };
+    for (int k = 0; k < kLinkDepth - 1; ++k) issue(k);
+    float cv = 0.0f;
+    cb[tid] = 0.0f;          // the carry into the first chunk
+    for (int k = 0; k < chunks; ++k) {
+        cp_async_wait<kLinkDepth - 2>();   // this thread's copies of chunk k
+        __syncthreads();                   // everyone's, and the carry of chunk k - 1
+        issue(k + kLinkDepth - 1);         // into the slot chunk k - 1 used
+        const float* Phi = ring + (k % kLinkDepth) * head;
+        const float* cur = cb + (k & 1) * (N * m);
+        wl[k * unit_floats + head + tid] = cv;   // the carry into chunk k
+        float acc = __fmul_rn(Phi[i * N], cur[c]);
+#pragma unroll
+        for (int j = 1; j < N; ++j) acc = __fadd_rn(acc, __fmul_rn(Phi[i * N + j], cur[j * m + c]));
+        cv = __fadd_rn(acc, Phi[N * N + tid]);
+        cb[((k + 1) & 1) * (N * m) + tid] = cv;
+    }
+    cp_async_wait<0>();
+}
+
+template <int N>
+cudaError_t launch_chunked_tma_n(const MatLaunch& L, float* ws, int64_t chunks, int64_t chunk, const char** err) {
+    const int m = L.m;
+    const int stages = 3;
+    MatChunkArgs C{ws, static_cast<int>(chunks), static_cast<int>(chunk),
+                   static_cast<int>(L.reverse ? chunks * chunk - L.T : 0)};
+    // pass 1 carries the m state columns and the product's N; pass 3 the m
+    int gp1 = 1;
+    while (gp1 < m + N) gp1 <<= 1;
+    const int gp3 = L.gp;
+    int R1 = 0, lpc1 = 0, TT1 = 0, R3 = 0, lpc3 = 0, TT3 = 0;
+    mat_tile_shape(N, m, gp1, &R1, &lpc1, &TT1);
+    mat_tile_shape(N, m, gp3, &R3, &lpc3, &TT3);
+    CUtensorMap ma1, mb1, ma3, mb3;
+    if (!encode_blocks(L.encode, &ma1, L.a, N * N, L.J, L.T, L.O, 1, TT1) ||
+        !encode_blocks(L.encode, &mb1, L.b, static_cast<int64_t>(N) * m, L.J, L.T, L.O, 1, TT1) ||
+        !encode_blocks(L.encode, &ma3, L.a, N * N, L.J, L.T, L.O, 1, TT3) ||
+        !encode_blocks(L.encode, &mb3, L.b, static_cast<int64_t>(N) * m, L.J, L.T, L.O, 1, TT3)) {
+        *err = "cuTensorMapEncodeTiled failed for a matrix-scan chunk map";
+        return cudaErrorInvalidValue;
+    }
+    const size_t smem1 = static_cast<size_t>(stages) * mat_stage_floats(N, m, lpc1, TT1, true) * 4 + 1024;
+    const size_t smem3 = static_cast<size_t>(stages) * mat_stage_floats(N, m, lpc3, TT3, true) * 4 + 1024;
+    const int groups1 = static_cast<int>((chunks + lpc1 - 1) / lpc1);
+    const int groups3 = static_cast<int>((chunks + lpc3 - 1) / lpc3);
+    cudaError_t e = launch_tma_n<N, kMatLocal>(L, ma1, mb1, gp1, R1, lpc1, groups1, TT1, stages, smem1, C);
+    if (e != cudaSuccess) return e;
+    const size_t smem_link = (static_cast<size_t>(kLinkDepth) * (N * N + N * m) + 2 * N * m) * 4;
+    e = cudaFuncSetAttribute(k_mat_chunk_link<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem_link));
+    if (e != cudaSuccess) return e;
+    k_mat_chunk_link<N><<<static_cast<unsigned>(L.g.lanes), N * m, smem_link, L.stream>>>(ws, m,
+                                                                                     static_cast<int>(chunks));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_tma_n<N, kMatFinal>(L, ma3, mb3, gp3, R3, lpc3, groups3, TT3, stages, smem3, C);
+}
+
 }  // namespace
 
 void mat_chunk_shape(int64_t lanes, int64_t T, int m, int64_t* chunks, int64_t* chunk) {
@@ -763,6 +955,27 @@ void mat_chunk_shape(int64_t lanes, int64_t T, int m, int64_t* chunks, int64_t* 
 size_t mat_chunk_workspace_bytes(int n, int m, int64_t lanes, int64_t chunks) {
     return static_cast<size_t>(lanes) * static_cast<size_t>(chunks) *
            (static_cast<size_t>(n) * n + 2 * static_cast<size_t>(n) * m) * 4;
+}
+
+bool mat_chunked_tma_ok(const MatLaunch& L, bool dense, int64_t chunks, int64_t chunk) {
+    int gp1 = 1;
+    while (gp1 < L.m + L.n) gp1 <<= 1;
+    if (L.projective || L.trans || L.m + L.n > 32) return false;
+    if (!mat_tma_ok(L.n, L.m, gp1, false, L.O, L.T, L.J, dense, L.a, L.b)) return false;
+    if (reinterpret_cast<uintptr_t>(L.out) % 16 != 0) return false;
+    // chunk coordinates, counts and grids in 32-bit
+    const int64_t lim = int64_t(1) << 30;
+    return chunks * chunk < lim && L.T < lim && L.g.lanes * chunks < lim && L.g.lanes == L.O * L.J;
+}
+
+cudaError_t launch_mat_chunked_tma(const MatLaunch& L, float* ws, int64_t chunks, int64_t chunk, const char** err) {
+    switch (L.n) {
+        case 2: return launch_chunked_tma_n<2>(L, ws, chunks, chunk, err);
+        case 4: return launch_chunked_tma_n<4>(L, ws, chunks, chunk, err);
+        case 8: return launch_chunked_tma_n<8>(L, ws, chunks, chunk, err);
+        case 16: return launch_chunked_tma_n<16>(L, ws, chunks, chunk, err);
+    }
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_mat_chunked(const MatLaunch& L, float* ws, int64_t chunks, int64_t chunk) {

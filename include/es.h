@@ -78,7 +78,8 @@ typedef enum es_path {
     ES_PATH_TIME_TMA = 4,  /* time innermost: TMA tiles transposed in SMEM     */
     ES_PATH_VEC_TMA = 5,   /* vector state: TMA pipeline + xor shuffles        */
     ES_PATH_MAT_TMA = 6,   /* matrix-scan, dense operands: TMA pipeline        */
-    ES_PATH_MAT_CHUNKED = 7 /* matrix-scan, few long lanes: chunked scan (3 kernels) */
+    ES_PATH_MAT_CHUNKED = 7, /* matrix-scan, few long lanes: chunked scan (3 kernels) */
+    ES_PATH_MAT_CHUNKED_TMA = 8 /* the same chunked scan, its scan passes on the TMA pipeline */
 } es_path;
 
 /*
@@ -408,16 +409,30 @@ es_status es_plan_matrix_scan_f32(const float *a, const int64_t *a_shape, int a_
  * (within 1e-5 * (1 + |h|) for non-expansive a), not bit for bit.  The chunks'
  * products and boundary states need a workspace, which the caller provides
  * (the library allocates nothing); projective scans always run sequentially.
+ * Dense operands with n in {2, 4, 8, 16}, n*m a multiple of 4, n + m <= 32
+ * and 16-byte aligned bases run the two scan passes on the TMA pipeline
+ * (ES_PATH_MAT_CHUNKED_TMA); anything else on direct-load kernels
+ * (ES_PATH_MAT_CHUNKED).  Both take the same chunks and the same arithmetic
+ * step for step, so they agree bit for bit.
  *
  * es_matrix_scan_workspace_f32: the workspace bytes a call with these shapes
  * would use (0 when it runs sequentially and needs none).  Host logic only.
  * es_matrix_scan_ws_f32: es_matrix_scan_f32 with a device workspace of
  * `workspace_bytes` (16-byte aligned, not overlapping the operands): the
- * chunked scan when it applies and the workspace suffices (ES_PATH_MAT_CHUNKED),
- * else exactly es_matrix_scan_f32.
+ * chunked scan when it applies and the workspace suffices, else exactly
+ * es_matrix_scan_f32.  Forcing ES_PATH_MAT_CHUNKED or ES_PATH_MAT_CHUNKED_TMA
+ * (es_set_path_override) on a call that cannot take it is ES_E_UNSUPPORTED.
+ * es_plan_matrix_scan_ws_f32: the checks and the path of that call without a
+ * GPU (info->path: ES_PATH_MAT_CHUNKED_TMA, ES_PATH_MAT_CHUNKED or the
+ * sequential path); the pointers are only checked, never read.
  */
 es_status es_matrix_scan_workspace_f32(const int64_t *a_shape, int a_rank, const int64_t *b_shape,
                                        int b_rank, int axis, int projective, size_t *bytes);
+
+es_status es_plan_matrix_scan_ws_f32(const float *a, const int64_t *a_shape, int a_rank,
+                                     const float *b, const int64_t *b_shape, int b_rank,
+                                     int axis, int reverse, int projective, const float *out,
+                                     const void *workspace, size_t workspace_bytes, es_plan_info *info);
 
 es_status es_matrix_scan_ws_f32(const float *a, const int64_t *a_shape, int a_rank,
                                 const float *b, const int64_t *b_shape, int b_rank,

@@ -49,3 +49,53 @@ def test_linear_plans():
     assert es.plan_linear_scan([64, 1, 1024], [64, 4096, 1024], axis=1)["path"] == "generic"
     with pytest.raises(es.EsError):
         es.plan_linear_scan([3, 4], [4, 4], axis=0)
+
+
+def test_workspace_plans():
+    """Few long lanes with a workspace: the chunked scan on the TMA passes
+    where they take the operands, else on the direct-load chunk kernels;
+    without enough workspace the sequential path; forcing checked."""
+    sa, sb = [8, 131072, 16, 16], [8, 131072, 16, 16]
+    need = es.matrix_scan_workspace(sa, sb, 1)
+    assert need == 8 * 512 * (16 * 16 + 2 * 16 * 16) * 4      # 512 chunks of 256 trips per lane
+    assert es.plan_matrix_scan_ws(sa, sb, need, axis=1)["path"] == "mat_chunked_tma"
+    assert es.plan_matrix_scan_ws(sa, sb, need, axis=1, reverse=True)["path"] == "mat_chunked_tma"
+    assert es.plan_matrix_scan_ws(sa, sb, need - 16, axis=1)["path"] == "mat_tma"
+    assert es.plan_matrix_scan_ws(sa, sb, 0, axis=1)["path"] == "mat_tma"
+    # odd n, n + m > 32, n*m not a multiple of 4, a broadcast a: direct-load chunk kernels
+    for a_shape, b_shape in (([3, 2000, 7, 7], [3, 2000, 7, 2]), ([3, 2000, 16, 16], [3, 2000, 16, 17]),
+                             ([3, 2000, 2, 2], [3, 2000, 2, 1]), ([1, 2000, 4, 4], [3, 2000, 4, 4])):
+        n = es.matrix_scan_workspace(a_shape, b_shape, 1)
+        assert n > 0
+        assert es.plan_matrix_scan_ws(a_shape, b_shape, n, axis=1)["path"] == "mat_chunked", (a_shape, b_shape)
+    # an `out` off the 16-byte grid takes the direct-load kernels too
+    p = es.plan_matrix_scan_ws(sa, sb, need, axis=1, ptrs=[1 << 44, 2 << 44, (3 << 44) + 4, 4 << 44])
+    assert p["path"] == "mat_chunked"
+    # many lanes: no chunking
+    assert es.matrix_scan_workspace([64, 1024, 16, 16, 16], [64, 1024, 16, 16, 16], 1) == 0
+    assert es.plan_matrix_scan_ws([64, 1024, 16, 16, 16], [64, 1024, 16, 16, 16], 1 << 20, axis=1)["path"] == "mat_tma"
+    # forcing
+    es.set_path_override("mat_chunked")
+    try:
+        assert es.plan_matrix_scan_ws(sa, sb, need, axis=1)["path"] == "mat_chunked"
+        with pytest.raises(es.EsError) as e:
+            es.plan_matrix_scan_ws(sa, sb, need - 16, axis=1)
+        assert e.value.status == 4
+    finally:
+        es.set_path_override("auto")
+    es.set_path_override("mat_chunked_tma")
+    try:
+        assert es.plan_matrix_scan_ws(sa, sb, need, axis=1)["path"] == "mat_chunked_tma"
+        n = es.matrix_scan_workspace([3, 2000, 7, 7], [3, 2000, 7, 2], 1)
+        with pytest.raises(es.EsError) as e:
+            es.plan_matrix_scan_ws([3, 2000, 7, 7], [3, 2000, 7, 2], n, axis=1)
+        assert e.value.status == 4
+    finally:
+        es.set_path_override("auto")
+    # the workspace may not overlap an operand, and sits on the 16-byte grid
+    with pytest.raises(es.EsError) as e:
+        es.plan_matrix_scan_ws(sa, sb, need, axis=1, ptrs=[1 << 44, 2 << 44, 3 << 44, (1 << 44) + 64])
+    assert e.value.status == 3
+    with pytest.raises(es.EsError) as e:
+        es.plan_matrix_scan_ws(sa, sb, need, axis=1, ptrs=[1 << 44, 2 << 44, 3 << 44, (4 << 44) + 4])
+    assert e.value.status == 3

@@ -205,6 +205,49 @@ def test_chunked_few_lanes(n, m, T, reverse):
     close(got.cpu().numpy(), M.matrix_scan(a, b, axis=1, reverse=reverse), "chunked n=%d m=%d T=%d" % (n, m, T))
 
 
+CHUNK_TMA_CASES = [
+    # n, m, a's leading dims (axis 1 is T), T
+    (16, 16, (3,), 3001),       # the last chunk short
+    (16, 8, (1,), 256),         # four chunks of 64
+    (8, 24, (2,), 2000),        # n + m = 32: pass 1 carries 32 columns
+    (8, 4, (2, 3), 777),        # lanes after the axis (J = 3)
+    (4, 4, (2,), 1000),
+    (4, 3, (2,), 1300),
+    (2, 2, (5,), 5000),
+]
+
+
+@pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
+@pytest.mark.parametrize("n,m,lead,T", CHUNK_TMA_CASES,
+                         ids=["n%dm%d_%s_T%d" % (c[0], c[1], "x".join(map(str, c[2])), c[3]) for c in CHUNK_TMA_CASES])
+def test_chunked_tma_matches_chunk_kernels(n, m, lead, T, reverse):
+    """The chunked scan with its scan passes on the TMA kernel takes the same
+    chunks and the same arithmetic as the direct-load chunk kernels: bit for
+    bit the same states, and within 1e-5 * (1 + |h|) of the sequential oracle."""
+    rng = np.random.default_rng(n * 1000 + m * 10 + T)
+    a_lead = (lead[0], T) + lead[1:]
+    a = contractive(rng, a_lead, n, norm=0.97)
+    b = rng.standard_normal(a_lead + (n, m)).astype(np.float32)
+    need = es.matrix_scan_workspace(a.shape, b.shape, 1)
+    assert need > 0
+    assert es.plan_matrix_scan_ws(a.shape, b.shape, need, axis=1, reverse=reverse)["path"] == "mat_chunked_tma"
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    da, db = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    got = {}
+    for path in ("mat_chunked_tma", "mat_chunked"):
+        es.set_path_override(path)
+        try:
+            ws.fill_(0xFF)          # no value may leak from an earlier call's workspace
+            n0 = es.launch_count()
+            got[path] = es.matrix_scan_ws(da, db, ws, axis=1, reverse=reverse).cpu().numpy()
+            es.device_status()
+            assert es.launch_count() - n0 == 3
+        finally:
+            es.set_path_override("auto")
+    bitwise(got["mat_chunked_tma"], got["mat_chunked"], "chunked tma vs direct n=%d m=%d" % (n, m))
+    close(got["mat_chunked_tma"], M.matrix_scan(a, b, axis=1, reverse=reverse), "chunked tma n=%d m=%d" % (n, m))
+
+
 def test_chunked_fallbacks_and_broadcast():
     rng = np.random.default_rng(11)
     a = contractive(rng, (2, 700), 4)

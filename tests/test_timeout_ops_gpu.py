@@ -74,6 +74,26 @@ def test_matrix_scan_pipeline():
                       lambda out: np.testing.assert_array_equal(out.cpu().numpy(), want))
 
 
+def test_matrix_scan_chunked_pipeline():
+    """Both TMA passes of the chunked scan give up on the missing tile; the
+    next call is correct."""
+    rng = np.random.default_rng(2)
+    # 16 x 16 blocks: tiles of 4 trips, so a chunk (66 trips) has a tile 3
+    a = (rng.standard_normal((2, 3000, 16, 16)) * 0.1).astype(np.float32)
+    b = rng.standard_normal((2, 3000, 16, 16)).astype(np.float32)
+    need = es.matrix_scan_workspace(a.shape, b.shape, 1)
+    assert es.plan_matrix_scan_ws(a.shape, b.shape, need, axis=1)["path"] == "mat_chunked_tma"
+    da, db = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    want = M.matrix_scan(a, b, axis=1)
+
+    def check(out):
+        err = np.abs(out.cpu().numpy().astype(np.float64) - want) / (1 + np.abs(want.astype(np.float64)))
+        assert err.max() <= 1e-5
+
+    drop_then_recover(lambda: es.matrix_scan_ws(da, db, ws, axis=1), check)
+
+
 def test_matrix_scan_backward_pipeline():
     """The cotangent scan (the TMA kernel on a's transposes) gives up a
     missing tile, then recovers."""
