@@ -49,7 +49,7 @@ cudaError_t launch_mat_tma(const MatLaunch& L, const char** err);
 
 // The chunked scan for few long lanes (three launches, a caller workspace):
 // how to cut T, the workspace it needs, and the launch.
-void mat_chunk_shape(int64_t lanes, int64_t T, int m, int64_t* chunks, int64_t* chunk);
+void mat_chunk_shape(int n, int m, bool dense, int64_t lanes, int64_t T, int64_t* chunks, int64_t* chunk);
 size_t mat_chunk_workspace_bytes(int n, int m, int64_t lanes, int64_t chunks);
 cudaError_t launch_mat_chunked(const MatLaunch& L, float* ws, int64_t chunks, int64_t chunk);
 // The same chunked scan with its two scan passes on the TMA kernel (dense

@@ -204,7 +204,7 @@ bool chunked_applies(const MatPlan& P) {
 }
 
 size_t chunked_workspace(const MatPlan& P, int64_t* chunks, int64_t* chunk) {
-    mat_chunk_shape(P.L.g.lanes, P.L.T, P.L.m, chunks, chunk);
+    mat_chunk_shape(P.L.n, P.L.m, P.dense, P.L.g.lanes, P.L.T, chunks, chunk);
     return mat_chunk_workspace_bytes(P.L.n, P.L.m, P.L.g.lanes, *chunks);
 }
 

@@ -942,14 +942,57 @@ cudaError_t launch_chunked_tma_n(const MatLaunch& L, float* ws, int64_t chunks, 
 
 }  // namespace
 
-void mat_chunk_shape(int64_t lanes, int64_t T, int m, int64_t* chunks, int64_t* chunk) {
-    // about 4096 (lane, chunk) units of at least 64 trips
-    int64_t c = lanes >= 4096 ? 1 : (4096 + lanes - 1) / lanes;
-    const int64_t max_chunks = T / 64 > 1 ? T / 64 : 1;
+namespace {
+
+// The TMA passes take the chunked scan's operands by shape: n in
+// {2, 4, 8, 16}, n*m a multiple of 4 and at most 256, n + m <= 32 (pass 1
+// carries m state columns and n product columns), dense leading dims.
+bool chunked_tma_shape(int n, int m, bool dense) {
+    return dense && (n == 2 || n == 4 || n == 8 || n == 16) && (n * m) % 4 == 0 && n * m <= 256 && n + m <= 32;
+}
+
+// GB300: 152 SMs of 228 KB shared memory.  Plan-time constants, so that the
+// chunk shape (and with it the workspace size) needs no GPU to compute.
+constexpr int64_t kPlanSMs = 152;
+constexpr int64_t kPlanSmemPerSM = 228 * 1024;
+
+// CTAs of one chunk pass resident per SM: shared memory (with the 1 KB the
+// runtime reserves per CTA), and registers at up to 128 per thread
+int64_t chunk_pass_ctas_per_sm(int n, int m, int gp) {
+    int R = 0, lpc = 0, TT = 0;
+    mat_tile_shape(n, m, gp, &R, &lpc, &TT);
+    const int64_t smem = 3 * mat_stage_floats(n, m, lpc, TT, true) * 4 + 1024 + 1024;
+    const int64_t threads = 32 + static_cast<int64_t>(lpc) * gp * R;
+    return std::max<int64_t>(1, std::min(kPlanSmemPerSM / smem, 65536 / (threads * 128)));
+}
+
+}  // namespace
+
+void mat_chunk_shape(int n, int m, bool dense, int64_t lanes, int64_t T, int64_t* chunks, int64_t* chunk) {
+    const int64_t max_chunks = T / 64 > 1 ? T / 64 : 1;      // chunks of at least 64 trips
+    int64_t c;
+    if (chunked_tma_shape(n, m, dense)) {
+        // the TMA passes: one CTA scans LPC chunks of one lane, so
+        // lanes * ceil(chunks / LPC) CTAs; as many chunks as fill one wave of
+        // resident CTAs, which leaves no ragged last wave and keeps the link
+        // pass (one step per chunk) short
+        int gp1 = 1, gp3 = 1;
+        while (gp1 < m + n) gp1 <<= 1;
+        while (gp3 < m) gp3 <<= 1;
+        int R = 0, lpc1 = 0, lpc3 = 0, TT = 0;
+        mat_tile_shape(n, m, gp1, &R, &lpc1, &TT);
+        mat_tile_shape(n, m, gp3, &R, &lpc3, &TT);
+        const int64_t lpc = std::min(lpc1, lpc3);
+        const int64_t slots = kPlanSMs * std::min(chunk_pass_ctas_per_sm(n, m, gp1), chunk_pass_ctas_per_sm(n, m, gp3));
+        const int64_t groups = std::max<int64_t>(1, slots / lanes);
+        c = groups * lpc;
+    } else {
+        // the direct-load kernels: about 4096 (lane, chunk) units
+        c = lanes >= 4096 ? 1 : (4096 + lanes - 1) / lanes;
+    }
     if (c > max_chunks) c = max_chunks;
     *chunk = (T + c - 1) / c;
     *chunks = (T + *chunk - 1) / *chunk;
-    (void)m;
 }
 
 size_t mat_chunk_workspace_bytes(int n, int m, int64_t lanes, int64_t chunks) {
@@ -960,7 +1003,7 @@ size_t mat_chunk_workspace_bytes(int n, int m, int64_t lanes, int64_t chunks) {
 bool mat_chunked_tma_ok(const MatLaunch& L, bool dense, int64_t chunks, int64_t chunk) {
     int gp1 = 1;
     while (gp1 < L.m + L.n) gp1 <<= 1;
-    if (L.projective || L.trans || L.m + L.n > 32) return false;
+    if (L.projective || L.trans || !chunked_tma_shape(L.n, L.m, dense)) return false;
     if (!mat_tma_ok(L.n, L.m, gp1, false, L.O, L.T, L.J, dense, L.a, L.b)) return false;
     if (reinterpret_cast<uintptr_t>(L.out) % 16 != 0) return false;
     // chunk coordinates, counts and grids in 32-bit

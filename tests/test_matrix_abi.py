@@ -57,7 +57,9 @@ def test_workspace_plans():
     without enough workspace the sequential path; forcing checked."""
     sa, sb = [8, 131072, 16, 16], [8, 131072, 16, 16]
     need = es.matrix_scan_workspace(sa, sb, 1)
-    assert need == 8 * 512 * (16 * 16 + 2 * 16 * 16) * 4      # 512 chunks of 256 trips per lane
+    # 8 lanes x 38 CTAs of 4 chunks: one wave of 152 SMs x 2 CTAs, so 152
+    # chunks of 863 trips per lane
+    assert need == 8 * 152 * (16 * 16 + 2 * 16 * 16) * 4
     assert es.plan_matrix_scan_ws(sa, sb, need, axis=1)["path"] == "mat_chunked_tma"
     assert es.plan_matrix_scan_ws(sa, sb, need, axis=1, reverse=True)["path"] == "mat_chunked_tma"
     assert es.plan_matrix_scan_ws(sa, sb, need - 16, axis=1)["path"] == "mat_tma"
