@@ -685,16 +685,21 @@ def matrix_oracle_backward(w, a, b, states, grad_out, reverse):
     return M.matrix_scan_backward(a, b, states, grad_out, axis=w.axis, reverse=reverse)
 
 
-def matrix_backward_call(es, w, a, b, states, grad_out, grads, reverse, stream):
+def matrix_backward_call(es, w, a, b, states, grad_out, grads, reverse, stream, workspace=None):
     if w.kind == "linear":
         es.linear_scan_backward(a, b, states, grad_out, axis=w.axis, reverse=reverse, grads=grads, stream=stream)
+    elif workspace is not None:
+        es.matrix_scan_backward_ws(a, b, states, grad_out, workspace, axis=w.axis, reverse=reverse, grads=grads,
+                                   stream=stream)
     else:
         es.matrix_scan_backward(a, b, states, grad_out, axis=w.axis, reverse=reverse, grads=grads, stream=stream)
 
 
-def matrix_backward_plan(es, w, reverse):
+def matrix_backward_plan(es, w, reverse, workspace=None):
     if w.kind == "linear":
         return es.plan_linear_scan_backward(w.a_shape, w.b_shape, w.axis, reverse)
+    if workspace is not None:
+        return es.plan_matrix_scan_backward_ws(w.a_shape, w.b_shape, workspace.numel(), w.axis, reverse)
     return es.plan_matrix_scan_backward(w.a_shape, w.b_shape, w.axis, reverse)
 
 
@@ -702,8 +707,10 @@ def matrix_backward_plan(es, w, reverse):
 # skeletons of its body; matrix-scan two launches (the cotangent scan on a's
 # transposes, then grad_a), timed as one call
 MATRIX_BWD_KERNEL = {"mat_tma": "k_mat_tma_bwd", "generic": "k_mat_generic_bwd",
-                     "lane_tma": "k_body_lane_bwd", "time_tma": "k_body_time_bwd"}
-KERNEL_SOURCES.update({k: ["k_matrix.cu", "es_matrix_api.cu"] for k in ("k_mat_tma_bwd", "k_mat_generic_bwd")})
+                     "lane_tma": "k_body_lane_bwd", "time_tma": "k_body_time_bwd",
+                     "mat_chunked_tma": "k_mat_tma_chunked_bwd"}
+KERNEL_SOURCES.update({k: ["k_matrix.cu", "es_matrix_api.cu"]
+                       for k in ("k_mat_tma_bwd", "k_mat_generic_bwd", "k_mat_tma_chunked_bwd")})
 
 
 def op_sample(w, inputs, target_elems):
@@ -826,12 +833,12 @@ def run_ours_op(args, w):
         gen.manual_seed(1000 + rank)
         gouts = [torch.randn(job.out_shape, generator=gen, device=device) for _ in w.reverse]
         grads = [(torch.empty_like(job.inputs[0]), torch.empty_like(job.inputs[1])) for _ in w.reverse]
-        plans = [matrix_backward_plan(es, w, r) for r in w.reverse]
+        plans = [matrix_backward_plan(es, w, r, job.workspace) for r in w.reverse]
 
     def step():
         if backward:
             for o, g, gr, r in zip(outs, gouts, grads, w.reverse):
-                matrix_backward_call(es, w, job.inputs[0], job.inputs[1], o, g, gr, r, stream)
+                matrix_backward_call(es, w, job.inputs[0], job.inputs[1], o, g, gr, r, stream, job.workspace)
             return
         for o, r in zip(outs, w.reverse):
             job.call(job.inputs, o, r, stream)
@@ -843,7 +850,12 @@ def run_ours_op(args, w):
     if backward:
         kernel = MATRIX_BWD_KERNEL.get(plans[0]["path"], plans[0]["path"])
         roofline = roofline_of(kernel, w.name + "_backward", w.backward_algorithmic_bytes(), kernel_ms)
-        if w.kind != "linear":
+        if w.kind != "linear" and plans[0]["path"] == "mat_chunked_tma":
+            roofline["kernel"] = ("k_mat_tma (transposed, chunk pass) + k_mat_chunk_link + k_mat_tma (transposed, "
+                                  "final pass) + k_mat_da")
+            roofline["note"] = ("a call of four launches timed as one: the cotangent scan chunked (a and grad_out read "
+                                "by both scan passes), then grad_a from the cotangent and the saved states")
+        elif w.kind != "linear":
             roofline["kernel"] = "k_mat_%s (transposed) + k_mat_da" % ("tma" if plans[0]["path"] == "mat_tma"
                                                                       else "generic")
             roofline["note"] = ("a call of two launches timed as one: the cotangent scan on a's transposes, then "
@@ -889,7 +901,8 @@ def run_ours_op(args, w):
                             d.copy_(hh, non_blocking=True)
                         od.copy_(sh, non_blocking=True)
                         gd.copy_(gh, non_blocking=True)
-                        matrix_backward_call(es, w, job.inputs[0], job.inputs[1], od, gd, gr_d, r, stream)
+                        matrix_backward_call(es, w, job.inputs[0], job.inputs[1], od, gd, gr_d, r, stream,
+                                             job.workspace)
                         gr_h[0].copy_(gr_d[0], non_blocking=True)
                         gr_h[1].copy_(gr_d[1], non_blocking=True)
                     return
@@ -990,9 +1003,8 @@ def main(argv=None):
         w = ops[args.workload]
         if args.trips:
             w = w.with_trips(args.trips)
-        if args.pass_ == "backward" and (w.name in wl.TABLE_WORKLOADS or getattr(w, "workspace", False)):
-            ap.error("--pass backward: table-scan states have no gradient, and the chunked matrix-scan has no "
-                     "backward path")
+        if args.pass_ == "backward" and w.name in wl.TABLE_WORKLOADS:
+            ap.error("--pass backward: table-scan states have no gradient")
         return run_reference_op(args, w) if args.impl == "reference" else run_ours_op(args, w)
     w = wl.WORKLOADS[args.workload]
     if args.trips:

@@ -14,7 +14,7 @@ _BINDING_NAMES = {
     "Body", "body_compile_count", "matrix_scan", "plan_matrix_scan", "linear_scan", "plan_linear_scan",
     "table_scan", "plan_table_scan", "matrix_scan_workspace", "matrix_scan_ws", "plan_matrix_scan_ws",
     "matrix_scan_static", "matrix_scan_backward", "plan_matrix_scan_backward", "linear_scan_backward",
-    "plan_linear_scan_backward",
+    "plan_linear_scan_backward", "matrix_scan_backward_ws", "plan_matrix_scan_backward_ws",
 }
 
 

@@ -38,7 +38,8 @@ EXPORTS = ("es_scan_f32", "es_plan_f32", "es_scan_backward_f32", "es_plan_backwa
            "es_matrix_scan_static_f32", "es_scan_body_backward_f32", "es_plan_body_backward_f32",
            "es_body_source_backward", "es_body_prepare_backward", "es_matrix_scan_backward_f32",
            "es_plan_matrix_scan_backward_f32", "es_linear_scan_backward_f32", "es_plan_linear_scan_backward_f32",
-           "es_scan_host_f32", "es_scan_body_host_f32")
+           "es_scan_host_f32", "es_scan_body_host_f32", "es_matrix_scan_backward_ws_f32",
+           "es_plan_matrix_scan_backward_ws_f32")
 
 
 class LibraryMissing(ImportError):
@@ -154,6 +155,11 @@ def lib():
         L.es_matrix_scan_backward_f32.restype = ctypes.c_int
         L.es_plan_matrix_scan_backward_f32.argtypes = msig + [ctypes.c_int, P, P, P, P, ctypes.POINTER(PlanInfo)]
         L.es_plan_matrix_scan_backward_f32.restype = ctypes.c_int
+        L.es_matrix_scan_backward_ws_f32.argtypes = msig + [ctypes.c_int, P, P, P, P, P, ctypes.c_size_t, P]
+        L.es_matrix_scan_backward_ws_f32.restype = ctypes.c_int
+        L.es_plan_matrix_scan_backward_ws_f32.argtypes = msig + [ctypes.c_int, P, P, P, P, P, ctypes.c_size_t,
+                                                                 ctypes.POINTER(PlanInfo)]
+        L.es_plan_matrix_scan_backward_ws_f32.restype = ctypes.c_int
         L.es_linear_scan_backward_f32.argtypes = msig + [P, P, P, P, P]
         L.es_linear_scan_backward_f32.restype = ctypes.c_int
         L.es_plan_linear_scan_backward_f32.argtypes = msig + [P, P, P, P, ctypes.POINTER(PlanInfo)]
@@ -809,6 +815,44 @@ def matrix_scan_backward(a, b, states, grad_out, axis: int = 0, reverse: bool = 
     _check(lib().es_matrix_scan_backward_f32(a.data_ptr(), sa, ra, b.data_ptr(), sb, rb, int(axis),
                                              int(bool(reverse)), int(bool(projective)), states.data_ptr(),
                                              grad_out.data_ptr(), ga.data_ptr(), gb.data_ptr(), handle))
+    return ga, gb
+
+
+def plan_matrix_scan_backward_ws(a_shape, b_shape, workspace_bytes: int, axis: int = 0, reverse: bool = False,
+                                 projective: bool = False, ptrs: Optional[Sequence[int]] = None) -> dict:
+    """The checks and the kernel path of ``matrix_scan_backward_ws`` without a
+    GPU.  ``ptrs`` = (a, b, states, grad_out, grad_a, grad_b, workspace)."""
+    if ptrs is None:
+        ptrs = [(k + 1) << 44 for k in range(7)]
+    sa, ra = _shape_array(a_shape)
+    sb, rb = _shape_array(b_shape)
+    info = PlanInfo()
+    _check(lib().es_plan_matrix_scan_backward_ws_f32(ptrs[0], sa, ra, ptrs[1], sb, rb, int(axis),
+                                                     int(bool(reverse)), int(bool(projective)), ptrs[2], ptrs[3],
+                                                     ptrs[4], ptrs[5], ptrs[6] if workspace_bytes else None,
+                                                     int(workspace_bytes), ctypes.byref(info)))
+    return _info(info)
+
+
+def matrix_scan_backward_ws(a, b, states, grad_out, workspace, axis: int = 0, reverse: bool = False,
+                            projective: bool = False, grads=None, stream=None):
+    """matrix_scan_backward with a caller workspace (a CUDA tensor of at least
+    ``matrix_scan_workspace`` bytes of the same shapes): few long lanes run the
+    cotangent scan chunked."""
+    import torch
+    ga, gb = _backward_args(a, b, states, grad_out, grads)
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA tensor")
+    sa, ra = _shape_array(a.shape)
+    sb, rb = _shape_array(b.shape)
+    if stream is None:
+        stream = torch.cuda.current_stream(b.device)
+    handle = stream if isinstance(stream, int) else stream.cuda_stream
+    _check(lib().es_matrix_scan_backward_ws_f32(a.data_ptr(), sa, ra, b.data_ptr(), sb, rb, int(axis),
+                                                int(bool(reverse)), int(bool(projective)), states.data_ptr(),
+                                                grad_out.data_ptr(), ga.data_ptr(), gb.data_ptr(),
+                                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                                handle))
     return ga, gb
 
 

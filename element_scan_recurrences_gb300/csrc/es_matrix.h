@@ -54,7 +54,8 @@ size_t mat_chunk_workspace_bytes(int n, int m, int64_t lanes, int64_t chunks);
 cudaError_t launch_mat_chunked(const MatLaunch& L, float* ws, int64_t chunks, int64_t chunk);
 // The same chunked scan with its two scan passes on the TMA kernel (dense
 // operands as the TMA kernel takes them, n + m <= 32) and a pipelined link
-// pass; the same workspace layout, the same results bit for bit.
+// pass; the same workspace layout, the same results bit for bit.  With
+// `trans` set it runs the gradient's cotangent scan, chunked the same way.
 bool mat_chunked_tma_ok(const MatLaunch& L, bool dense, int64_t chunks, int64_t chunk);
 cudaError_t launch_mat_chunked_tma(const MatLaunch& L, float* ws, int64_t chunks, int64_t chunk, const char** err);
 

@@ -289,7 +289,7 @@ struct MatBwdPlan {
 es_status plan_matrix_backward(const char* fn, const float* a, const int64_t* a_shape, int a_rank, const float* b,
                                const int64_t* b_shape, int b_rank, int axis, int reverse, int projective,
                                const float* states, const float* grad_out, const float* grad_a,
-                               const float* grad_b, MatBwdPlan* Q) {
+                               const float* grad_b, MatBwdPlan* Q, bool chunk_forcible = false) {
     if (projective) return api_fail(ES_E_ARG, "%s: a projective matrix-scan has no gradient", fn);
     MatPlan& P = Q->P;
     es_status st = plan_matrix(fn, a, a_shape, a_rank, b, b_shape, b_rank, axis, reverse, 0, states, false, &P);
@@ -323,7 +323,9 @@ es_status plan_matrix_backward(const char* fn, const float* a, const int64_t* a_
     const bool tma = mat_tma_ok(L.n, L.m, L.gp, false, L.O, L.T, L.J, true, L.a, L.b) &&
                      reinterpret_cast<uintptr_t>(L.out) % 16 == 0;
     const int forced = api_path_override();
-    if (forced == ES_PATH_AUTO) {
+    // a forced chunked path is decided by the workspace entry (its sequential
+    // choice is then the automatic one)
+    if (forced == ES_PATH_AUTO || (chunk_forcible && forced == ES_PATH_MAT_CHUNKED_TMA)) {
         P.path = tma ? ES_PATH_MAT_TMA : ES_PATH_GENERIC;
         return ES_OK;
     }
@@ -332,6 +334,43 @@ es_status plan_matrix_backward(const char* fn, const float* a, const int64_t* a_
         return ES_OK;
     }
     return api_fail(ES_E_UNSUPPORTED, "%s: the forced kernel path %d cannot serve this call", fn, forced);
+}
+
+// es_matrix_scan_backward_ws_f32's path: the cotangent scan chunked on the TMA
+// passes (the forward's chunks and workspace size: the geometry is the same)
+// when the lanes are few, the operands suit it and the workspace suffices;
+// else the sequential path of es_matrix_scan_backward_f32.  ws_chunked set
+// for the former.
+es_status plan_matrix_backward_ws(const char* fn, MatBwdPlan* Q, const float* b, const float* grad_out,
+                                  const void* workspace, size_t workspace_bytes, int64_t* chunks, int64_t* chunk,
+                                  bool* ws_chunked) {
+    *ws_chunked = false;
+    MatPlan& P = Q->P;
+    if (P.empty) return ES_OK;
+    const int forced = api_path_override();
+    if (forced == ES_PATH_MAT_CHUNKED)
+        return api_fail(ES_E_UNSUPPORTED, "%s: the direct-load chunk kernels have no gradient", fn);
+    const size_t need = chunked_applies(P) ? chunked_workspace(P, chunks, chunk) : 0;
+    const bool tma = need > 0 && mat_chunked_tma_ok(P.L, P.dense, *chunks, *chunk);
+    if (!(tma && workspace != nullptr && workspace_bytes >= need)) {
+        if (forced == ES_PATH_MAT_CHUNKED_TMA)
+            return api_fail(ES_E_UNSUPPORTED,
+                            "%s: the chunked gradient needs few long lanes, operands the TMA passes take and %zu "
+                            "workspace bytes", fn, need);
+        return ES_OK;
+    }
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+        return api_fail(ES_E_ARG, "%s: workspace not 16-byte aligned", fn);
+    const void* ops[6] = {P.L.a, b, Q->states, grad_out, Q->grad_a, P.L.out};
+    const int64_t cnt[6] = {P.n_a, P.n_b, P.n_out, P.n_out, P.n_a, P.n_b};
+    const uintptr_t wlo = reinterpret_cast<uintptr_t>(workspace), whi = wlo + need;
+    for (int k = 0; k < 6; ++k) {
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(ops[k]), hi = lo + static_cast<uintptr_t>(cnt[k]) * 4;
+        if (lo < whi && wlo < hi) return api_fail(ES_E_ARG, "%s: the workspace overlaps an operand", fn);
+    }
+    P.path = ES_PATH_MAT_CHUNKED_TMA;
+    *ws_chunked = true;
+    return ES_OK;
 }
 
 es_status launch_matrix_backward(const char* fn, MatBwdPlan* Q, int reverse, cudaStream_t stream) {
@@ -565,6 +604,62 @@ es_status es_matrix_scan_backward_f32(const float* a, const int64_t* a_shape, in
                                             states, grad_out, grad_a, grad_b, &Q);
     if (st != ES_OK || Q.P.empty) return st;
     return es::launch_matrix_backward(fn, &Q, reverse, reinterpret_cast<cudaStream_t>(stream));
+}
+
+es_status es_plan_matrix_scan_backward_ws_f32(const float* a, const int64_t* a_shape, int a_rank, const float* b,
+                                              const int64_t* b_shape, int b_rank, int axis, int reverse,
+                                              int projective, const float* states, const float* grad_out,
+                                              const float* grad_a, const float* grad_b, const void* workspace,
+                                              size_t workspace_bytes, es_plan_info* info) {
+    const char* fn = "es_matrix_scan_backward_ws_f32";
+    es::MatBwdPlan Q{};
+    es_status st = es::plan_matrix_backward(fn, a, a_shape, a_rank, b, b_shape, b_rank, axis, reverse, projective,
+                                            states, grad_out, grad_a, grad_b, &Q, true);
+    int64_t chunks = 0, chunk = 0;
+    bool ws_chunked = false;
+    if (st == ES_OK)
+        st = es::plan_matrix_backward_ws(fn, &Q, b, grad_out, workspace, workspace_bytes, &chunks, &chunk,
+                                         &ws_chunked);
+    if (st != ES_OK) return st;
+    es::fill_matrix_info(Q.P, info);
+    if (info != nullptr) info->reverse = reverse ? 1 : 0;
+    return ES_OK;
+}
+
+es_status es_matrix_scan_backward_ws_f32(const float* a, const int64_t* a_shape, int a_rank, const float* b,
+                                         const int64_t* b_shape, int b_rank, int axis, int reverse, int projective,
+                                         const float* states, const float* grad_out, float* grad_a, float* grad_b,
+                                         void* workspace, size_t workspace_bytes, es_stream_t stream) {
+    const char* fn = "es_matrix_scan_backward_ws_f32";
+    es::MatBwdPlan Q{};
+    es_status st = es::plan_matrix_backward(fn, a, a_shape, a_rank, b, b_shape, b_rank, axis, reverse, projective,
+                                            states, grad_out, grad_a, grad_b, &Q, true);
+    if (st != ES_OK || Q.P.empty) return st;
+    int64_t chunks = 0, chunk = 0;
+    bool ws_chunked = false;
+    if ((st = es::plan_matrix_backward_ws(fn, &Q, b, grad_out, workspace, workspace_bytes, &chunks, &chunk,
+                                          &ws_chunked)) != ES_OK)
+        return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!ws_chunked) return es::launch_matrix_backward(fn, &Q, reverse, s);
+    int dev = 0;
+    es::DeviceState* ds = nullptr;
+    if ((st = es::api_device(&dev, &ds)) != ES_OK) return st;
+    es::MatLaunch& L = Q.P.L;
+    L.stream = s;
+    L.status = ds->status;
+    L.wait_ns = es::api_wait_ns();
+    L.drop_tile = es::api_drop_tile();
+    L.num_sms = ds->num_sms;
+    if ((st = es::api_encoder(&L.encode)) != ES_OK) return st;
+    const char* msg = nullptr;
+    // the cotangent scan, chunked (grad_b), then grad_a from it and the states
+    cudaError_t e = es::launch_mat_chunked_tma(L, static_cast<float*>(workspace), chunks, chunk, &msg);
+    if (e == cudaSuccess)
+        e = es::launch_mat_da(L.out, Q.states, Q.grad_a, L.n, L.O, L.T, L.J, L.m, reverse ? 1 : 0, s);
+    if (e != cudaSuccess) return es::api_fail(ES_E_CUDA, "%s: %s", fn, msg != nullptr ? msg : cudaGetErrorString(e));
+    es::count_launch(4);
+    return ES_OK;
 }
 
 // linear-scan's gradient is the element-scan backward of its body, from zero

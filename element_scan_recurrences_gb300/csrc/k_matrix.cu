@@ -202,7 +202,9 @@ enum : int { kMatFull = 0, kMatLocal = 1, kMatFinal = 2 };
 
 // TRANS (the gradient's cotangent scan): the step's coefficient is
 // a[t + a_shift]^T; the a tile is loaded a_shift trips off the b tile, and
-// TMA's zero fill past either end of the axis is the zero matrix.
+// TMA's zero fill past either end of the axis is the zero matrix.  The chunk
+// modes run it too (a chunk's product is then the product of the transposed,
+// shifted coefficients).
 template <int N, int R, bool PROJ, bool TRANS, int MODE>
 __global__ void __launch_bounds__(32 + kMatConsumers, 1)
 k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
@@ -212,7 +214,7 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
     constexpr bool kChunk = MODE != kMatFull;
     constexpr bool kIdent = PROJ || MODE == kMatLocal;     // columns that carry a product from the identity
     static_assert(!(PROJ && TRANS), "a projective scan has no gradient");
-    static_assert(!kChunk || (!PROJ && !TRANS), "the chunked passes are plain scans");
+    static_assert(!kChunk || !PROJ, "a projective scan is not chunked");
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMatMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kMatMaxStages];
@@ -283,7 +285,7 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
                         // for lanes past the last chunk) the box is zero-filled
                         const int64_t t = static_cast<int64_t>(c0 + l) * chunk - chunk_off + jt * TT;
                         const int ct = static_cast<int>(t < T ? t : T);
-                        tma_load_4d(st + l * la, &map_a, 0, jj, ct, o, &full_bar[s], pol);
+                        tma_load_4d(st + l * la, &map_a, 0, jj, ct + a_shift, o, &full_bar[s], pol);
                         tma_load_4d(st + a_pad + l * lb, &map_b, 0, jj, ct, o, &full_bar[s], pol);
                     }
                 } else {
@@ -544,7 +546,7 @@ struct MatChunkArgs {
 template <int N, int R, int MODE>
 cudaError_t launch_tma_nr(const MatLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb, int gp, int lpc,
                           int tiles_j, int TT, int stages, size_t smem, const MatChunkArgs& C) {
-    auto kern = MODE != kMatFull ? k_mat_tma<N, R, false, false, MODE>
+    auto kern = MODE != kMatFull ? (L.trans ? k_mat_tma<N, R, false, true, MODE> : k_mat_tma<N, R, false, false, MODE>)
                 : L.projective   ? k_mat_tma<N, R, true, false, kMatFull>
                 : L.trans        ? k_mat_tma<N, R, false, true, kMatFull>
                                  : k_mat_tma<N, R, false, false, kMatFull>;
@@ -1003,7 +1005,7 @@ size_t mat_chunk_workspace_bytes(int n, int m, int64_t lanes, int64_t chunks) {
 bool mat_chunked_tma_ok(const MatLaunch& L, bool dense, int64_t chunks, int64_t chunk) {
     int gp1 = 1;
     while (gp1 < L.m + L.n) gp1 <<= 1;
-    if (L.projective || L.trans || !chunked_tma_shape(L.n, L.m, dense)) return false;
+    if (L.projective || !chunked_tma_shape(L.n, L.m, dense)) return false;
     if (!mat_tma_ok(L.n, L.m, gp1, false, L.O, L.T, L.J, dense, L.a, L.b)) return false;
     if (reinterpret_cast<uintptr_t>(L.out) % 16 != 0) return false;
     // chunk coordinates, counts and grids in 32-bit

@@ -511,6 +511,40 @@ es_status es_plan_matrix_scan_backward_f32(const float *a, const int64_t *a_shap
                                            es_plan_info *info);
 
 /*
+ * es_matrix_scan_backward_ws_f32 -- es_matrix_scan_backward_f32 with a
+ * device workspace, for few long lanes.  The cotangent recurrence composes
+ * over chunks of trips exactly as the forward scan does, so it runs as the
+ * same chunked scan (chunk pass, link pass, final pass on the TMA kernel,
+ * section "Few long lanes" above) with the transposed, one-trip-shifted
+ * coefficient, then grad_a as before: four kernels.  It applies when the
+ * forward call would be chunked on the TMA passes (ES_PATH_MAT_CHUNKED_TMA)
+ * and `workspace_bytes` covers es_matrix_scan_workspace_f32 of the same
+ * shapes (the geometry is the forward's); otherwise the call is exactly
+ * es_matrix_scan_backward_f32.  The chunks reassociate the cotangent chain,
+ * so grad_b and grad_a agree with the sequential gradient to rounding
+ * (within 1e-5 * (1 + |value|) for non-expansive a), not bit for bit.
+ *   workspace  device, 16-byte aligned, not overlapping any operand (ES_E_ARG).
+ * Forcing ES_PATH_MAT_CHUNKED_TMA on a call that cannot take it, or
+ * ES_PATH_MAT_CHUNKED (the direct-load chunk kernels have no gradient), is
+ * ES_E_UNSUPPORTED.  es_plan_matrix_scan_backward_ws_f32: the checks and
+ * the path without a GPU.
+ */
+es_status es_matrix_scan_backward_ws_f32(const float *a, const int64_t *a_shape, int a_rank,
+                                         const float *b, const int64_t *b_shape, int b_rank,
+                                         int axis, int reverse, int projective,
+                                         const float *states, const float *grad_out,
+                                         float *grad_a, float *grad_b,
+                                         void *workspace, size_t workspace_bytes, es_stream_t stream);
+
+es_status es_plan_matrix_scan_backward_ws_f32(const float *a, const int64_t *a_shape, int a_rank,
+                                              const float *b, const int64_t *b_shape, int b_rank,
+                                              int axis, int reverse, int projective,
+                                              const float *states, const float *grad_out,
+                                              const float *grad_a, const float *grad_b,
+                                              const void *workspace, size_t workspace_bytes,
+                                              es_plan_info *info);
+
+/*
  * es_linear_scan_backward_f32 -- gradients of a linear-scan whose a and b
  * have one shape (ES_E_UNSUPPORTED otherwise): lam[t] = a[t+1] * lam[t+1] +
  * g[t] in the opposite trip order, grad_b = lam, grad_a[t] = lam[t] * h[t-1]

@@ -101,3 +101,47 @@ def test_workspace_plans():
     with pytest.raises(es.EsError) as e:
         es.plan_matrix_scan_ws(sa, sb, need, axis=1, ptrs=[1 << 44, 2 << 44, 3 << 44, (4 << 44) + 4])
     assert e.value.status == 3
+
+
+def test_backward_workspace_plans():
+    """The gradient with a workspace: the cotangent scan chunked on the TMA
+    passes where the forward would be, with the forward's workspace size;
+    else the sequential gradient; forcing checked."""
+    sa, sb = [8, 131072, 16, 16], [8, 131072, 16, 16]
+    need = es.matrix_scan_workspace(sa, sb, 1)
+    for reverse in (False, True):
+        p = es.plan_matrix_scan_backward_ws(sa, sb, need, axis=1, reverse=reverse)
+        assert p["path"] == "mat_chunked_tma" and p["reverse"] == reverse
+    assert es.plan_matrix_scan_backward_ws(sa, sb, need - 16, axis=1)["path"] == "mat_tma"
+    assert es.plan_matrix_scan_backward_ws(sa, sb, 0, axis=1)["path"] == "mat_tma"
+    # operands the TMA passes do not take: the sequential gradient
+    n = es.matrix_scan_workspace([3, 2000, 7, 7], [3, 2000, 7, 2], 1)
+    assert es.plan_matrix_scan_backward_ws([3, 2000, 7, 7], [3, 2000, 7, 2], n, axis=1)["path"] == "generic"
+    # a projective scan has no gradient
+    with pytest.raises(es.EsError) as e:
+        es.plan_matrix_scan_backward_ws(sa, sb, need, axis=1, projective=True)
+    assert e.value.status == 3
+    # the workspace may not overlap an operand (here grad_b)
+    with pytest.raises(es.EsError) as e:
+        es.plan_matrix_scan_backward_ws(sa, sb, need, axis=1, ptrs=[(k + 1) << 44 for k in range(6)] + [(6 << 44) + 64])
+    assert e.value.status == 3
+    es.set_path_override("mat_chunked_tma")
+    try:
+        assert es.plan_matrix_scan_backward_ws(sa, sb, need, axis=1)["path"] == "mat_chunked_tma"
+        for args in ((sa, sb, need - 16), ([3, 2000, 7, 7], [3, 2000, 7, 2], n)):
+            with pytest.raises(es.EsError) as e:
+                es.plan_matrix_scan_backward_ws(*args, axis=1)
+            assert e.value.status == 4
+        # the entry without a workspace cannot take it
+        with pytest.raises(es.EsError) as e:
+            es.plan_matrix_scan_backward(sa, sb, axis=1)
+        assert e.value.status == 4
+    finally:
+        es.set_path_override("auto")
+    es.set_path_override("mat_chunked")   # the direct-load chunk kernels have no gradient
+    try:
+        with pytest.raises(es.EsError) as e:
+            es.plan_matrix_scan_backward_ws(sa, sb, need, axis=1)
+        assert e.value.status == 4
+    finally:
+        es.set_path_override("auto")

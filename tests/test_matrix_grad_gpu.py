@@ -140,3 +140,72 @@ def test_delta_rule_backward_full_size_sampled():
         wa, wb = M.matrix_scan_backward(sa, sb, sh, sg, axis=1)
         bitwise(ga[o:o + 1, :, j:j + 1].cpu(), wa, "grad_a lane (%d, %d)" % (o, j))
         bitwise(gb[o:o + 1, :, j:j + 1].cpu(), wb, "grad_b lane (%d, %d)" % (o, j))
+
+
+def spectral(rng, lead, n, norm=0.97):
+    a = rng.standard_normal(tuple(lead) + (n, n))
+    s = np.linalg.norm(a, ord=2, axis=(-2, -1))[..., None, None]
+    return (a / s * norm).astype(np.float32)
+
+
+def close(got, want, what, tol=1e-5):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    err = np.abs(got - want) / (1.0 + np.abs(want))
+    assert float(err.max()) <= tol, "%s: max scaled error %.3g" % (what, float(err.max()))
+
+
+CHUNK_GRAD_CASES = [(16, 16, (3,), 3001), (16, 8, (1,), 256), (8, 4, (2, 3), 777), (4, 4, (2,), 1000),
+                    (2, 2, (5,), 5000)]
+
+
+@pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
+@pytest.mark.parametrize("n,m,lead,T", CHUNK_GRAD_CASES,
+                         ids=["n%dm%d_%s_T%d" % (c[0], c[1], "x".join(map(str, c[2])), c[3]) for c in CHUNK_GRAD_CASES])
+def test_chunked_backward(n, m, lead, T, reverse):
+    """Few long lanes: the cotangent scan chunked on the TMA passes (four
+    launches), within 1e-5 * (1 + |value|) of the gradient oracle and of the
+    sequential gradient (the chunks reassociate the cotangent chain)."""
+    rng = np.random.default_rng(n * 1000 + m * 10 + T + 1)
+    a_lead = (lead[0], T) + lead[1:]
+    a = spectral(rng, a_lead, n)
+    b = rng.standard_normal(a_lead + (n, m)).astype(np.float32)
+    states = M.matrix_scan(a, b, axis=1, reverse=reverse)
+    G = rng.standard_normal(states.shape).astype(np.float32)
+    want = M.matrix_scan_backward(a, b, states, G, axis=1, reverse=reverse)
+    need = es.matrix_scan_workspace(a.shape, b.shape, 1)
+    assert es.plan_matrix_scan_backward_ws(a.shape, b.shape, need, 1, reverse)["path"] == "mat_chunked_tma"
+    d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    da, db, dh, dg = d(a), d(b), d(states), d(G)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    n0 = es.launch_count()
+    ga, gb = es.matrix_scan_backward_ws(da, db, dh, dg, ws, axis=1, reverse=reverse)
+    es.device_status()
+    assert es.launch_count() - n0 == 4
+    sa, sb = es.matrix_scan_backward(da, db, dh, dg, axis=1, reverse=reverse)
+    es.device_status()
+    what = "n=%d m=%d T=%d rev=%d" % (n, m, T, reverse)
+    close(gb.cpu().numpy(), want[1], "grad_b " + what)
+    close(ga.cpu().numpy(), want[0], "grad_a " + what)
+    close(gb.cpu().numpy(), sb.cpu().numpy(), "grad_b vs sequential " + what)
+    close(ga.cpu().numpy(), sa.cpu().numpy(), "grad_a vs sequential " + what)
+
+
+def test_chunked_backward_falls_back():
+    """Without enough workspace, or with operands the TMA passes do not take,
+    the workspace entry is the sequential gradient, bit for bit."""
+    rng = np.random.default_rng(5)
+    for n, m in ((4, 4), (7, 2)):
+        a = spectral(rng, (2, 700), n)
+        b = rng.standard_normal((2, 700, n, m)).astype(np.float32)
+        states = M.matrix_scan(a, b, axis=1)
+        G = rng.standard_normal(states.shape).astype(np.float32)
+        want = M.matrix_scan_backward(a, b, states, G, axis=1)
+        need = es.matrix_scan_workspace(a.shape, b.shape, 1)
+        ws = torch.empty(max(16, need - 16 if n == 4 else need), dtype=torch.uint8, device="cuda")
+        d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+        ga, gb = es.matrix_scan_backward_ws(d(a), d(b), d(states), d(G), ws, axis=1)
+        es.device_status()
+        bitwise(gb.cpu().numpy(), want[1], "grad_b fallback n=%d" % n)
+        bitwise(ga.cpu().numpy(), want[0], "grad_a fallback n=%d" % n)

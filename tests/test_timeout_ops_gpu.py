@@ -94,6 +94,28 @@ def test_matrix_scan_chunked_pipeline():
     drop_then_recover(lambda: es.matrix_scan_ws(da, db, ws, axis=1), check)
 
 
+def test_matrix_scan_chunked_backward_pipeline():
+    """The chunked cotangent scan's TMA passes give up on the missing tile;
+    the next call is correct."""
+    rng = np.random.default_rng(3)
+    a = (rng.standard_normal((2, 3000, 16, 16)) * 0.1).astype(np.float32)
+    b = rng.standard_normal((2, 3000, 16, 16)).astype(np.float32)
+    h = M.matrix_scan(a, b, axis=1)
+    G = rng.standard_normal(h.shape).astype(np.float32)
+    wa, wb = M.matrix_scan_backward(a, b, h, G, axis=1)
+    need = es.matrix_scan_workspace(a.shape, b.shape, 1)
+    assert es.plan_matrix_scan_backward_ws(a.shape, b.shape, need, 1)["path"] == "mat_chunked_tma"
+    da, db, dh, dg = (torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (a, b, h, G))
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+
+    def check(out):
+        for got, want in zip(out, (wa, wb)):
+            err = np.abs(got.cpu().numpy().astype(np.float64) - want) / (1 + np.abs(want.astype(np.float64)))
+            assert err.max() <= 1e-5
+
+    drop_then_recover(lambda: es.matrix_scan_backward_ws(da, db, dh, dg, ws, axis=1), check)
+
+
 def test_matrix_scan_backward_pipeline():
     """The cotangent scan (the TMA kernel on a's transposes) gives up a
     missing tile, then recovers."""
