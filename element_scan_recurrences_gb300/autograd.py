@@ -86,12 +86,19 @@ def element_scan(body, initial: torch.Tensor, sequences: Sequence[torch.Tensor],
 
 class _MatrixScan(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, linear, axis, reverse, projective, a, b):
+    def forward(ctx, linear, axis, reverse, projective, chunked, a, b):
+        ws = None
+        if chunked and not linear:
+            nbytes = es.matrix_scan_workspace(a.shape, b.shape, axis, projective)
+            if nbytes:
+                ws = torch.empty(nbytes, dtype=torch.uint8, device=a.device)
         if linear:
             out = es.linear_scan(a, b, axis=axis, reverse=reverse)
+        elif ws is not None:
+            out = es.matrix_scan_ws(a, b, ws, axis=axis, reverse=reverse, projective=projective)
         else:
             out = es.matrix_scan(a, b, axis=axis, reverse=reverse, projective=projective)
-        ctx.linear, ctx.axis, ctx.reverse, ctx.projective = linear, axis, reverse, projective
+        ctx.linear, ctx.axis, ctx.reverse, ctx.projective, ctx.ws = linear, axis, reverse, projective, ws
         ctx.save_for_backward(a, b, out)
         return out
 
@@ -102,10 +109,13 @@ class _MatrixScan(torch.autograd.Function):
         grad_out = grad_out.contiguous()
         if ctx.linear:
             ga, gb = es.linear_scan_backward(a, b, out, grad_out, axis=ctx.axis, reverse=ctx.reverse)
+        elif ctx.ws is not None:
+            ga, gb = es.matrix_scan_backward_ws(a, b, out, grad_out, ctx.ws, axis=ctx.axis, reverse=ctx.reverse,
+                                                projective=ctx.projective)
         else:
             ga, gb = es.matrix_scan_backward(a, b, out, grad_out, axis=ctx.axis, reverse=ctx.reverse,
                                              projective=ctx.projective)
-        return None, None, None, None, ga, gb
+        return None, None, None, None, None, ga, gb
 
 
 def _one_shape(a, b, lead_a, lead_b):
@@ -121,15 +131,17 @@ def _one_shape(a, b, lead_a, lead_b):
 
 
 def matrix_scan(a: torch.Tensor, b: torch.Tensor, axis: int = 0, reverse: bool = False,
-                projective: bool = False) -> torch.Tensor:
+                projective: bool = False, chunked: bool = False) -> torch.Tensor:
     """The states of a matrix-scan, differentiable with respect to a and b
     (leading dims broadcast first, so autograd sums a shared operand's
-    gradient)."""
+    gradient).  ``chunked``: few long lanes run the chunked scan and the
+    chunked gradient in a workspace allocated here (results within rounding
+    of the sequential scan, not bit for bit); other shapes are unaffected."""
     a, b = _one_shape(a, b, a.shape[:-2], b.shape[:-2])
-    return _MatrixScan.apply(False, int(axis), bool(reverse), bool(projective), a, b)
+    return _MatrixScan.apply(False, int(axis), bool(reverse), bool(projective), bool(chunked), a, b)
 
 
 def linear_scan(a: torch.Tensor, b: torch.Tensor, axis: int = 0, reverse: bool = False) -> torch.Tensor:
     """The states of a linear-scan, differentiable with respect to a and b."""
     a, b = _one_shape(a, b, a.shape, b.shape)
-    return _MatrixScan.apply(True, int(axis), bool(reverse), False, a, b)
+    return _MatrixScan.apply(True, int(axis), bool(reverse), False, False, a, b)

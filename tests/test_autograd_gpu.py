@@ -198,3 +198,33 @@ def test_linear_scan_gradients():
     wa, wb = M.linear_scan_backward(a, b, st, G, axis=1)
     close(ta.grad.cpu(), wa, "a", exact=True)
     close(tb.grad.cpu(), wb, "b", exact=True)
+
+
+def test_matrix_scan_chunked_gradients():
+    """matrix-scan through autograd with ``chunked=True`` on few long lanes:
+    the delta rule's k, v, beta gradients within tolerance of the sequential
+    autograd gradients (the chunked forward and gradient reassociate the
+    chains), with the chunked paths actually taken."""
+    from element_scan_recurrences_gb300.autograd import matrix_scan
+    torch.manual_seed(7)
+    B, T, n, m = 2, 3000, 16, 16
+    assert es.matrix_scan_workspace((B, T, n, n), (B, T, n, m), 1) > 0
+    k0 = torch.nn.functional.normalize(torch.randn(B, T, n, device="cuda"), dim=-1)
+    v0 = torch.randn(B, T, m, device="cuda")
+    beta0 = torch.rand(B, T, 1, 1, device="cuda")
+    G = torch.randn(B, T, n, m, device="cuda")
+    grads = []
+    for chunked in (False, True):
+        k, v, beta = (t.clone().requires_grad_(True) for t in (k0, v0, beta0))
+        a = torch.eye(n, device="cuda") - beta * k.unsqueeze(-1) * k.unsqueeze(-2)
+        b = beta * k.unsqueeze(-1) * v.unsqueeze(-2)
+        n0 = es.launch_count()
+        S = matrix_scan(a, b, axis=1, chunked=chunked)
+        (S * G).sum().backward()
+        es.device_status()
+        launches = es.launch_count() - n0
+        assert launches == (3 + 4 if chunked else 1 + 2), launches
+        grads.append((S.detach().cpu().numpy(), k.grad.cpu().numpy(), v.grad.cpu().numpy(),
+                      beta.grad.cpu().numpy()))
+    for seq, chk, nm in zip(grads[0], grads[1], ("states", "k", "v", "beta")):
+        close(chk, seq, "chunked %s" % nm)
