@@ -84,6 +84,32 @@ __device__ __forceinline__ void mul2_rn(float& p0, float& p1, float a0, float a1
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// K consecutive floats of shared memory (16-byte aligned when K % 4 == 0,
+// 8-byte when K % 2 == 0)
+template <int K>
+__device__ __forceinline__ void smem_seg(const float* p, float (&d)[K]) {
+    if constexpr (K % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < K; q += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(p + q);
+            d[q] = v.x;
+            d[q + 1] = v.y;
+            d[q + 2] = v.z;
+            d[q + 3] = v.w;
+        }
+    } else if constexpr (K % 2 == 0) {
+#pragma unroll
+        for (int q = 0; q < K; q += 2) {
+            const float2 v = *reinterpret_cast<const float2*>(p + q);
+            d[q] = v.x;
+            d[q + 1] = v.y;
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < K; ++q) d[q] = p[q];
+    }
+}
+
 // the largest |value| over the lane group of `gp` threads (a power of two)
 __device__ __forceinline__ float group_max_abs(float v, int gp, unsigned mask) {
     for (int off = gp / 2; off >= 1; off >>= 1) v = ieee_maximum(v, __shfl_xor_sync(mask, v, off));
@@ -354,24 +380,39 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
                              (is_h ? c : 0);
             const int64_t t = kChunk ? tbase + t0 + tt : t0 + tt;
             const bool live = !kChunk || (t >= 0 && t < T);
+            if constexpr (TRANS) {
+                // row i of a^T h is sum_j a[j][i] h[j]: over j in order, this
+                // thread's contiguous rows i = g*RPT + r take the segment
+                // a[j][g*RPT ..] of row j (vector loads) times h[j], the
+                // same rounded products added in the same order as a dot
+                // product of column i
+                float acc[RPT];
 #pragma unroll
-            for (int r = 0; r < RPT; ++r) {
-                const int i = r * R + g;
-                float row[N];
-                if constexpr (TRANS) {
-                    // column i of a: the row groups read neighbouring words
+                for (int j = 0; j < N; ++j) {
+                    float seg[RPT], prod[RPT];
+                    smem_seg<RPT>(A + j * N + g * RPT, seg);
 #pragma unroll
-                    for (int j = 0; j < N; ++j) row[j] = A[j * N + i];
-                } else {
-                    smem_row<N>(A, i, row);
+                    for (int r = 0; r + 1 < RPT; r += 2) mul2_rn(prod[r], prod[r + 1], seg[r], seg[r + 1], h[j], h[j]);
+                    if constexpr (RPT % 2 == 1) prod[RPT - 1] = __fmul_rn(seg[RPT - 1], h[j]);
+#pragma unroll
+                    for (int r = 0; r < RPT; ++r) acc[r] = j == 0 ? prod[r] : __fadd_rn(acc[r], prod[r]);
                 }
-                float prod[N];
 #pragma unroll
-                for (int j = 0; j < N; j += 2) mul2_rn(prod[j], prod[j + 1], row[j], row[j + 1], h[j], h[j + 1]);
-                float acc = prod[0];
+                for (int r = 0; r < RPT; ++r) mine[r] = is_h ? __fadd_rn(acc[r], B[(g * RPT + r) * m]) : acc[r];
+            } else {
 #pragma unroll
-                for (int j = 1; j < N; ++j) acc = __fadd_rn(acc, prod[j]);
-                mine[r] = is_h ? __fadd_rn(acc, B[i * m]) : acc;
+                for (int r = 0; r < RPT; ++r) {
+                    const int i = r * R + g;
+                    float row[N];
+                    smem_row<N>(A, i, row);
+                    float prod[N];
+#pragma unroll
+                    for (int j = 0; j < N; j += 2) mul2_rn(prod[j], prod[j + 1], row[j], row[j + 1], h[j], h[j + 1]);
+                    float acc = prod[0];
+#pragma unroll
+                    for (int j = 1; j < N; ++j) acc = __fadd_rn(acc, prod[j]);
+                    mine[r] = is_h ? __fadd_rn(acc, B[i * m]) : acc;
+                }
             }
             if constexpr (PROJ) {
                 float mx = 0.0f;
@@ -386,13 +427,15 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
             if (MODE != kMatLocal && valid && is_h && live) {
                 float* op = obase + t * trip_stride;
 #pragma unroll
-                for (int r = 0; r < RPT; ++r) __stcs(op + (r * R + g) * m, mine[r]);
+                for (int r = 0; r < RPT; ++r) __stcs(op + (TRANS ? g * RPT + r : r * R + g) * m, mine[r]);
             }
-            // row i lives in row group i % R at position i / R (a trip off
-            // the axis keeps the state: the same for the whole lane group)
+            // row i lives in row group i % R at position i / R (TRANS: group
+            // i / RPT at position i % RPT); a trip off the axis keeps the
+            // state (the same for the whole lane group)
 #pragma unroll
             for (int i = 0; i < N; ++i) {
-                const float v = __shfl_sync(0xffffffffu, mine[i / R], col_base + (i % R) * gp);
+                const float v = TRANS ? __shfl_sync(0xffffffffu, mine[i % RPT], col_base + (i / RPT) * gp)
+                                      : __shfl_sync(0xffffffffu, mine[i / R], col_base + (i % R) * gp);
                 h[i] = live ? v : h[i];
             }
         };
@@ -430,11 +473,14 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
 // forms a B x B block of da, every entry the sum over k = 0..m-1 in order of
 // lam[i][k] * h_prev[j][k], each product and sum rounded (the first product
 // starts the sum).  Rows come straight from global memory (16-byte loads when
-// m is a multiple of 4); the rows a unit's threads share meet in L1.
-template <int N, int B, int KV>
+// m is a multiple of 4); the rows a unit's threads share meet in L1.  MC > 0
+// is m known at compile time: the loop over k unrolls and every load of the
+// unit can be in flight at once.
+template <int N, int B, int KV, int MC>
 __global__ void __launch_bounds__(128)
 k_mat_da(const float* __restrict__ lam, const float* __restrict__ states, float* __restrict__ da, int64_t O,
-         int64_t T, int64_t J, int m, int reverse) {
+         int64_t T, int64_t J, int m_rt, int reverse) {
+    const int m = MC > 0 ? MC : m_rt;
     constexpr int NB = N / B;
     constexpr int TPU = NB * NB;                 // threads per unit
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -461,6 +507,7 @@ k_mat_da(const float* __restrict__ lam, const float* __restrict__ states, float*
             d[0] = __ldg(p + k);
         }
     };
+#pragma unroll(MC > 0 ? MC / KV : 1)
     for (int k = 0; k < m; k += KV) {
         float lv[B][KV], hv[B][KV];
 #pragma unroll
@@ -509,14 +556,17 @@ cudaError_t launch_da_n(const float* lam, const float* states, float* da, int64_
     const bool vec = m % 4 == 0 && reinterpret_cast<uintptr_t>(lam) % 16 == 0 &&
                      reinterpret_cast<uintptr_t>(states) % 16 == 0;
     if constexpr (N % 4 == 0) {
-        if (vec && reinterpret_cast<uintptr_t>(da) % 16 == 0) return go(k_mat_da<N, 4, 4>, (N / 4) * (N / 4));
-        return go(k_mat_da<N, 4, 1>, (N / 4) * (N / 4));
+        if (vec && reinterpret_cast<uintptr_t>(da) % 16 == 0) {
+            if (m == 16) return go(k_mat_da<N, 4, 4, 16>, (N / 4) * (N / 4));
+            return go(k_mat_da<N, 4, 4, 0>, (N / 4) * (N / 4));
+        }
+        return go(k_mat_da<N, 4, 1, 0>, (N / 4) * (N / 4));
     } else if constexpr (N % 2 == 0) {
-        if (vec) return go(k_mat_da<N, 2, 4>, (N / 2) * (N / 2));
-        return go(k_mat_da<N, 2, 1>, (N / 2) * (N / 2));
+        if (vec) return go(k_mat_da<N, 2, 4, 0>, (N / 2) * (N / 2));
+        return go(k_mat_da<N, 2, 1, 0>, (N / 2) * (N / 2));
     } else {
-        if (vec) return go(k_mat_da<N, 1, 4>, N * N);
-        return go(k_mat_da<N, 1, 1>, N * N);
+        if (vec) return go(k_mat_da<N, 1, 4, 0>, N * N);
+        return go(k_mat_da<N, 1, 1, 0>, N * N);
     }
 }
 
