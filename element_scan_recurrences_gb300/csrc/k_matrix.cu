@@ -485,16 +485,19 @@ k_mat_da(const float* __restrict__ lam, const float* __restrict__ states, float*
     constexpr int TPU = NB * NB;                 // threads per unit
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t u = tid / TPU;
-    if (u >= O * T * J) return;
+    const int64_t units = O * T * J;
+    if (u >= units) return;
     const int w = static_cast<int>(tid % TPU);
     const int bi = w / NB, bj = w % NB;
-    const int64_t j = u % J;
-    const int64_t t = (u / J) % T;
-    const int64_t o = u / (J * T);
-    const int64_t tp = reverse ? t + 1 : t - 1;
-    const bool has_prev = tp >= 0 && tp < T;
+    // the unit's trip t (the state before it is unit u - J, or u + J in
+    // reverse); 32-bit division while the units fit
+    const int64_t t = units < (int64_t(1) << 31)
+                          ? static_cast<int64_t>((static_cast<uint32_t>(u) / static_cast<uint32_t>(J)) %
+                                                 static_cast<uint32_t>(T))
+                          : (u / J) % T;
+    const bool has_prev = reverse ? t + 1 < T : t > 0;
     const float* Lr = lam + (u * N + bi * B) * m;
-    const float* Hr = states + (((o * T + (has_prev ? tp : 0)) * J + j) * N + bj * B) * m;
+    const float* Hr = states + ((has_prev ? (reverse ? u + J : u - J) : u) * N + bj * B) * m;
     float acc[B][B];
     auto load = [&](const float* p, int k, float (&d)[KV]) {
         if constexpr (KV == 4) {
@@ -523,24 +526,111 @@ k_mat_da(const float* __restrict__ lam, const float* __restrict__ states, float*
 #pragma unroll
         for (int q = 0; q < KV; ++q) {
 #pragma unroll
-            for (int x = 0; x < B; ++x)
+            for (int x = 0; x < B; ++x) {
+                float p[B];
+                if constexpr (B % 2 == 0) {
+                    // two products at a time (each still one rounded product)
 #pragma unroll
-                for (int y = 0; y < B; ++y) {
-                    const float p = __fmul_rn(lv[x][q], hv[y][q]);
-                    acc[x][y] = (k + q == 0) ? p : __fadd_rn(acc[x][y], p);
+                    for (int y = 0; y < B; y += 2) mul2_rn(p[y], p[y + 1], lv[x][q], lv[x][q], hv[y][q], hv[y + 1][q]);
+                } else {
+#pragma unroll
+                    for (int y = 0; y < B; ++y) p[y] = __fmul_rn(lv[x][q], hv[y][q]);
                 }
+#pragma unroll
+                for (int y = 0; y < B; ++y) acc[x][y] = (k + q == 0) ? p[y] : __fadd_rn(acc[x][y], p[y]);
+            }
         }
     }
     float* D = da + u * N * N + (bi * B) * N + bj * B;
 #pragma unroll
     for (int x = 0; x < B; ++x) {
-        if constexpr (B == 4) {
-            __stcs(reinterpret_cast<float4*>(D + x * N), make_float4(acc[x][0], acc[x][1], acc[x][2], acc[x][3]));
+        if constexpr (B % 4 == 0) {
+#pragma unroll
+            for (int y = 0; y < B; y += 4)
+                __stcs(reinterpret_cast<float4*>(D + x * N + y),
+                       make_float4(acc[x][y], acc[x][y + 1], acc[x][y + 2], acc[x][y + 3]));
         } else {
 #pragma unroll
             for (int y = 0; y < B; ++y) __stcs(D + x * N + y, acc[x][y]);
         }
     }
+}
+
+// n = m = 16 (the delta rule's blocks): one warp per unit.  Reading rows of
+// lam and of the state straight from global memory left each 16-byte load
+// of a warp spread over 8 rows, one L1 wavefront per 16 bytes, and L1 bound
+// the kernel (ncu: L1TEX throughput 93%).  Here the warp reads the unit's two
+// 1 KB blocks with coalesced 16-byte loads into shared memory, each row's
+// four 16-byte chunks XOR-swizzled by (row / 2) % 4 so that the reads below
+// are free of bank conflicts, then lane (bi, bj) forms rows bi + 4x and
+// columns bj + 8y of da, each entry the sum over k = 0..15 in order of
+// lam[i][k] * h_prev[j][k] (the same rounded products and sums as k_mat_da).
+constexpr int kDa16Warps = 4;
+
+__device__ __forceinline__ int da16_off(int row, int chunk) { return row * 16 + ((chunk ^ ((row >> 1) & 3)) << 2); }
+
+__global__ void __launch_bounds__(32 * kDa16Warps)
+k_mat_da16(const float* __restrict__ lam, const float* __restrict__ states, float* __restrict__ da, int64_t units,
+           int64_t T, int64_t J, int reverse) {
+    __shared__ __align__(16) float sm[kDa16Warps][2][256];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t u = static_cast<int64_t>(blockIdx.x) * kDa16Warps + warp;
+    if (u >= units) return;   // the whole warp
+    const int64_t t = units < (int64_t(1) << 31)
+                          ? static_cast<int64_t>((static_cast<uint32_t>(u) / static_cast<uint32_t>(J)) %
+                                                 static_cast<uint32_t>(T))
+                          : (u / J) % T;
+    const bool has_prev = reverse ? t + 1 < T : t > 0;
+    const float4* L4 = reinterpret_cast<const float4*>(lam + u * 256);
+    const float4* H4 = reinterpret_cast<const float4*>(states + (has_prev ? (reverse ? u + J : u - J) : u) * 256);
+    float* sl = sm[warp][0];
+    float* sh = sm[warp][1];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int f = lane + 32 * q;             // 16-byte piece: row f / 4, chunk f % 4
+        const float4 lv = __ldg(L4 + f);
+        const float4 hv = has_prev ? __ldg(H4 + f) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        *reinterpret_cast<float4*>(sl + da16_off(f >> 2, f & 3)) = lv;
+        *reinterpret_cast<float4*>(sh + da16_off(f >> 2, f & 3)) = hv;
+    }
+    __syncwarp();
+    const int bi = lane & 3, bj = lane >> 2;
+    float acc[4][2];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        float lv[4][4], hv[2][4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const float4 v = *reinterpret_cast<const float4*>(sl + da16_off(bi + 4 * x, c));
+            lv[x][0] = v.x;
+            lv[x][1] = v.y;
+            lv[x][2] = v.z;
+            lv[x][3] = v.w;
+        }
+#pragma unroll
+        for (int y = 0; y < 2; ++y) {
+            const float4 v = *reinterpret_cast<const float4*>(sh + da16_off(bj + 8 * y, c));
+            hv[y][0] = v.x;
+            hv[y][1] = v.y;
+            hv[y][2] = v.z;
+            hv[y][3] = v.w;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                float p0, p1;
+                mul2_rn(p0, p1, lv[x][q], lv[x][q], hv[0][q], hv[1][q]);
+                acc[x][0] = (c + q == 0) ? p0 : __fadd_rn(acc[x][0], p0);
+                acc[x][1] = (c + q == 0) ? p1 : __fadd_rn(acc[x][1], p1);
+            }
+    }
+    float* D = da + u * 256;
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 2; ++y) __stcs(D + (bi + 4 * x) * 16 + bj + 8 * y, acc[x][y]);
 }
 
 template <int N>
@@ -555,6 +645,15 @@ cudaError_t launch_da_n(const float* lam, const float* states, float* da, int64_
     };
     const bool vec = m % 4 == 0 && reinterpret_cast<uintptr_t>(lam) % 16 == 0 &&
                      reinterpret_cast<uintptr_t>(states) % 16 == 0;
+    if constexpr (N == 16) {
+        if (m == 16 && vec) {
+            const int64_t blocks = (units + kDa16Warps - 1) / kDa16Warps;
+            if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+            k_mat_da16<<<static_cast<unsigned>(blocks), 32 * kDa16Warps, 0, stream>>>(lam, states, da, units, T, J,
+                                                                                     reverse);
+            return cudaGetLastError();
+        }
+    }
     if constexpr (N % 4 == 0) {
         if (vec && reinterpret_cast<uintptr_t>(da) % 16 == 0) {
             if (m == 16) return go(k_mat_da<N, 4, 4, 16>, (N / 4) * (N / 4));
