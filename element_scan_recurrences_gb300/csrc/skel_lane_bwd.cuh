@@ -119,6 +119,10 @@ k_body_lane_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
         const int s = k % stages;
         bool ok = true;
         if (k < ntiles) ok = mbar_wait_bounded(&full_bar[s], (k / stages) & 1, wait_ns, &abort_flag);
+        // the buffer this tile writes was last read by the store issued a tile
+        // ago (long done): the storer waits for that read before the barrier
+        // rather than for each store right after issuing it
+        if (storer) bulk_wait_read<0>();
         if (k > 0) fence_proxy_async_smem();     // this thread's gradient writes of tile k-1
         if (consumer_vote_any_failed(!ok, LI)) {
             if (!ok) report_timeout(status, &abort_flag);
@@ -130,8 +134,6 @@ k_body_lane_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
 #pragma unroll
             for (int q = 0; q < NS; ++q) tma_store_3d(&gmaps[q], i0, jp * TT, o, ob + q * kTileFloats);
             bulk_commit();
-            // the buffer written at the next tile is the one this store reads
-            bulk_wait_read<0>();
         }
         if (k == ntiles) break;
         const int j = reverse ? k : ntiles - 1 - k;

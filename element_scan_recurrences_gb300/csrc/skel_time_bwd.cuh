@@ -123,6 +123,10 @@ k_body_time_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
         const int s = k % stages;
         bool ok = true;
         if (k < ntiles) ok = mbar_wait_bounded(&full_bar[s], (k / stages) & 1, wait_ns, &abort_flag);
+        // the buffer this tile writes was last read by the store issued a tile
+        // ago (long done): the storer waits for that read before the barrier
+        // rather than for each store right after issuing it
+        if (storer) bulk_wait_read<0>();
         if (k > 0) fence_proxy_async_smem();     // this thread's gradient writes of tile k-1
         if (consumer_vote_any_failed(!ok, LO)) {
             if (!ok) report_timeout(status, &abort_flag);
@@ -134,8 +138,6 @@ k_body_time_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
 #pragma unroll
             for (int q = 0; q < NS; ++q) tma_store_2d(&gmaps[q], tp, o0, ob + q * kTile);
             bulk_commit();
-            // the buffer written at the next tile is the one this store reads
-            bulk_wait_read<0>();
         }
         if (k == ntiles) break;
         const int t0 = (reverse ? k : ntiles - 1 - k) * kTimeBwdTT;
