@@ -18,14 +18,19 @@
 // magnitude is an xor-shuffle maximum over the group (IEEE maximum, so a NaN
 // propagates), and every column is divided by it (IEEE division).
 //
-// Two kernels:
+// Kernels:
 //   * k_mat_generic: any broadcast of the leading dims (per-dim strides, a
 //     stride of 0 repeats an operand), loads straight from global memory;
 //   * k_mat_tma: dense operands; a producer thread streams {lanes x trips}
 //     tiles of a and b with TMA into an mbarrier ring, the lane's column
 //     threads read a's rows from shared memory (broadcast reads) and their own
 //     column of b, and store their column of h.  Waits are bounded as in the
-//     element-scan pipelines.
+//     element-scan pipelines.  Its chunk modes are the two scan passes of the
+//     chunked scan for few long lanes, linked by k_mat_chunk_link; the
+//     direct-load chunk kernels (k_mat_chunk_*) serve other operands;
+//   * the gradient ("its gradient is the same scan run backwards on a's
+//     transposes"): the same kernels with a transposed, one-trip-shifted
+//     coefficient for the cotangent, then k_mat_da / k_mat_da16 for grad_a.
 #include <algorithm>
 
 #include "es_device.cuh"
