@@ -145,3 +145,22 @@ def test_backward_workspace_plans():
         assert e.value.status == 4
     finally:
         es.set_path_override("auto")
+
+
+@pytest.mark.parametrize("n,m,lead,T,chunks", [
+    # TMA passes: lanes * ceil(chunks / LPC) CTAs fill one wave of 152 SMs x 2
+    (16, 16, (8,), 131072, 152),        # LPC 4: 38 CTAs a lane
+    (16, 16, (400,), 100000, 4),        # more lanes than a wave's CTAs: one CTA a lane
+    (4, 4, (2,), 100000, 607),          # LPC 4: 152 CTAs a lane, 608 asked; chunks of 165 trips need 607
+    (16, 16, (3,), 3001, 46),           # capped at chunks of 64 trips
+    # direct-load kernels (n = 7): about 4096 (lane, chunk) units, capped the same way
+    (7, 2, (3,), 2000, 31),
+    (7, 2, (1,), 1 << 20, 4096),
+])
+def test_chunk_count(n, m, lead, T, chunks):
+    """The chunk count behind es_matrix_scan_workspace_f32 (host logic): the
+    workspace is lanes x chunks units of n*n + 2*n*m floats."""
+    a_shape = [lead[0], T] + list(lead[1:]) + [n, n]
+    b_shape = [lead[0], T] + list(lead[1:]) + [n, m]
+    lanes = int(np.prod(lead))
+    assert es.matrix_scan_workspace(a_shape, b_shape, 1) == lanes * chunks * (n * n + 2 * n * m) * 4
