@@ -189,7 +189,8 @@ es_status es_scan_backward_f32(es_body body, const float *initial, const float *
  *                     work enqueued on `stream` after it waits for all of it
  *                     (events); read out_h after synchronising `stream`.
  * No allocation per call (the streams and events are created once per
- * device).  Statuses as for es_scan_f32.
+ * device).  Statuses as for es_scan_f32, and ES_E_ARG for a null host
+ * pointer or `chunks` outside 0..64 (checked before any CUDA call).
  */
 es_status es_scan_host_f32(es_body body, const float *initial_h, const float *const *seqs_h,
                            int n_seqs, const int64_t *shape, int rank, int axis,
