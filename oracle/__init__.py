@@ -6,13 +6,15 @@ library and its Python binding) never imports it and shares no code with it.
 
 The arithmetic lives in ``es_oracle.c`` (a plain lane-by-lane loop, built with
 ``gcc -O2 -ffp-contract=off``); this module only compiles it and marshals numpy
-arrays across ctypes.  Semantics follow "Nonlinear element scans"
+arrays across ctypes.  ``scan_threads`` / ``scan_backward_threads`` run that
+same loop on every host core, one contiguous block of lanes per thread.  Semantics follow "Nonlinear element scans"
 (sx.041.io/docs/element-scan.md): intro (forward recurrence, output holds the
 state after every trip), the `:state-axis` example (NORMCAP), the `:reverse`
 paragraph (MAXPLUS, reverse order) and "Arguments and body" (shapes).
 """
 from __future__ import annotations
 
+import concurrent.futures
 import ctypes
 import os
 import subprocess
@@ -105,13 +107,15 @@ def _c_array(a, dtype):
 
 
 def scan(body, initial, seqs, axis: int = 0, state_axis: bool = False,
-         reverse: bool = False, dtype=np.float32, _lib=None) -> np.ndarray:
+         reverse: bool = False, dtype=np.float32, _lib=None, out=None) -> np.ndarray:
     """Run the oracle on host arrays and return the states after every trip.
 
     ``initial`` has the output shape with ``axis`` removed; ``seqs`` is a list
     of two arrays.  Without ``state_axis`` both have the output shape; with it,
     each may have its own last width (1 or the state width W).
-    ``dtype=np.float64`` runs the double-precision diagnostic twin.
+    ``dtype=np.float64`` runs the double-precision diagnostic twin.  ``out``,
+    when given, is a C-contiguous array of the output shape and dtype that
+    receives the states (and is returned).
     """
     lib = _lib if _lib is not None else _load()
     ft = ctypes.c_float if dtype == np.float32 else ctypes.c_double
@@ -144,7 +148,10 @@ def scan(body, initial, seqs, axis: int = 0, state_axis: bool = False,
     widths = None
     if state_axis:
         widths = (ctypes.c_int64 * 2)(*[s.shape[-1] for s in seqs])
-    out = np.empty(shape, dtype=dtype)
+    if out is None:
+        out = np.empty(shape, dtype=dtype)
+    elif list(out.shape) != shape or out.dtype != dtype or not out.flags.c_contiguous:
+        raise ValueError("out must be a C-contiguous %s array of shape %r" % (np.dtype(dtype).name, shape))
     ptrs = (ctypes.POINTER(ft) * 2)(*[s.ctypes.data_as(ctypes.POINTER(ft)) for s in seqs])
     rc = fn(_body_id(body), initial.ctypes.data_as(ctypes.POINTER(ft)), ptrs, 2,
             (ctypes.c_int64 * rank)(*shape), rank, int(axis), int(W), widths,
@@ -156,10 +163,12 @@ def scan(body, initial, seqs, axis: int = 0, state_axis: bool = False,
 
 
 def scan_backward(body, initial, seqs, states, grad_out, axis: int = 0, state_axis: bool = False,
-                  reverse: bool = False, _lib=None):
+                  reverse: bool = False, _lib=None, out=None):
     """Gradients of sum(grad_out * scan(...)) with respect to initial and both
     sequences, from the forward states.  Returns (grad_initial, [gx, ga]) with
-    the shapes of initial and of each sequence."""
+    the shapes of initial and of each sequence.  ``out``, when given, is
+    (grad_initial, [gx, ga]): C-contiguous f32 arrays of those shapes that
+    receive the gradients."""
     lib = _lib if _lib is not None else _load()
     ft = ctypes.c_float
     fp = ctypes.POINTER(ft)
@@ -184,8 +193,14 @@ def scan_backward(body, initial, seqs, states, grad_out, axis: int = 0, state_ax
         if list(s.shape) != want:
             raise ValueError("sequence shape %r, expected %r" % (list(s.shape), want))
     widths = (ctypes.c_int64 * 2)(*[s.shape[-1] for s in seqs]) if state_axis else None
-    g_init = np.empty_like(initial)
-    g_seqs = [np.empty_like(s) for s in seqs]
+    if out is None:
+        g_init = np.empty_like(initial)
+        g_seqs = [np.empty_like(s) for s in seqs]
+    else:
+        g_init, g_seqs = out[0], list(out[1])
+        for g, ref in zip([g_init] + g_seqs, [initial] + seqs):
+            if g.shape != ref.shape or g.dtype != np.float32 or not g.flags.c_contiguous:
+                raise ValueError("gradient buffers must be C-contiguous f32 arrays of the operands' shapes")
     sp = (fp * 2)(*[s.ctypes.data_as(fp) for s in seqs])
     gp = (fp * 2)(*[g.ctypes.data_as(fp) for g in g_seqs])
     rc = lib.es_oracle_backward_f32(_body_id(body), initial.ctypes.data_as(fp), sp, 2, (ctypes.c_int64 * rank)(*shape),
@@ -220,3 +235,89 @@ def scan_lanes(body, initial, x, a, reverse: bool = False) -> np.ndarray:
     is [L]; the scan axis is 1.
     """
     return scan(body, initial, [x, a], axis=1, state_axis=False, reverse=reverse)
+
+
+# ---------------------------------------------------------------------------
+# all host cores: the same loop on contiguous blocks of lanes
+
+def host_threads() -> int:
+    """The host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def _lane_blocks(dim0: int, threads: int):
+    """Split [0, dim0) into at most `threads` contiguous blocks of nearly equal size."""
+    k = max(1, min(threads, dim0))
+    bounds = [dim0 * i // k for i in range(k + 1)]
+    return [(bounds[i], bounds[i + 1]) for i in range(k) if bounds[i + 1] > bounds[i]]
+
+
+def _run_blocks(jobs, threads: int):
+    if len(jobs) == 1:
+        jobs[0]()
+        return
+    # ctypes releases the interpreter lock for the duration of each call, so
+    # the blocks run at the same time
+    with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as pool:
+        for f in [pool.submit(j) for j in jobs]:
+            f.result()
+
+
+def scan_threads(body, initial, seqs, axis: int = 0, state_axis: bool = False, reverse: bool = False,
+                 threads: int = 0) -> np.ndarray:
+    """`scan` on every host core (f32): the lanes are split along dim 0 into
+    contiguous blocks, and each block is scanned by the unchanged single-thread
+    loop in a thread of its own, writing its slice of one output array.  Lanes
+    are independent ("Nonlinear element scans", intro), so the result is the
+    single-thread result bit for bit.  When the sequence axis is dim 0 (or
+    there is one block) it is exactly `scan`.  ``threads`` = 0 takes
+    `host_threads()`."""
+    threads = threads or host_threads()
+    seqs = [_c_array(s, np.float32) for s in seqs]
+    initial = _c_array(initial, np.float32)
+    rank = seqs[0].ndim
+    ax = axis + rank if axis < 0 else axis
+    if ax <= 0 or threads <= 1 or seqs[0].shape[0] <= 1:
+        return scan(body, initial, seqs, axis=axis, state_axis=state_axis, reverse=reverse)
+    shape = list(seqs[0].shape)
+    if state_axis:
+        shape[-1] = initial.shape[-1]
+    # the whole call is checked once, on a view of no lanes along dim 0
+    scan(body, initial[:0], [s[:0] for s in seqs], axis=axis, state_axis=state_axis, reverse=reverse)
+    out = np.empty(shape, np.float32)
+    lib = _load()
+    jobs = [lambda lo=lo, hi=hi: scan(body, initial[lo:hi], [s[lo:hi] for s in seqs], axis=axis,
+                                      state_axis=state_axis, reverse=reverse, _lib=lib, out=out[lo:hi])
+            for lo, hi in _lane_blocks(shape[0], threads)]
+    _run_blocks(jobs, threads)
+    return out
+
+
+def scan_backward_threads(body, initial, seqs, states, grad_out, axis: int = 0, state_axis: bool = False,
+                          reverse: bool = False, threads: int = 0):
+    """`scan_backward` on every host core, split into contiguous blocks of
+    lanes along dim 0 exactly as `scan_threads`; each lane's gradient is its
+    own reverse scan, so the result is the single-thread result bit for bit."""
+    threads = threads or host_threads()
+    seqs = [_c_array(s, np.float32) for s in seqs]
+    initial = _c_array(initial, np.float32)
+    states = _c_array(states, np.float32)
+    grad_out = _c_array(grad_out, np.float32)
+    rank = states.ndim
+    ax = axis + rank if axis < 0 else axis
+    if ax <= 0 or threads <= 1 or states.shape[0] <= 1:
+        return scan_backward(body, initial, seqs, states, grad_out, axis=axis, state_axis=state_axis,
+                             reverse=reverse)
+    g_init = np.empty_like(initial)
+    g_seqs = [np.empty_like(s) for s in seqs]
+    lib = _load()
+    jobs = [lambda lo=lo, hi=hi: scan_backward(body, initial[lo:hi], [s[lo:hi] for s in seqs], states[lo:hi],
+                                               grad_out[lo:hi], axis=axis, state_axis=state_axis,
+                                               reverse=reverse, _lib=lib,
+                                               out=(g_init[lo:hi], [g[lo:hi] for g in g_seqs]))
+            for lo, hi in _lane_blocks(states.shape[0], threads)]
+    _run_blocks(jobs, threads)
+    return g_init, g_seqs
