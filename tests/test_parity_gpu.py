@@ -1,9 +1,9 @@
 """CUDA library vs the CPU oracle, element by element, on seeded inputs.
 
 Small cases cover every kernel path with several tiles and ragged tails in
-both directions; the full-size workloads run in the launch configuration the
-bench times and are checked on sampled lanes plus properties that hold at any
-size.  MAXPLUS must be bit-exact; TANH_DECAY and NORMCAP within
+both directions; the five measured workloads run at full size in the launch
+configuration the bench times and are checked element by element (against the
+oracle on all host cores) plus properties that hold at any size.  MAXPLUS must be bit-exact; TANH_DECAY and NORMCAP within
 1e-5 * (1 + |oracle|).
 """
 import math
@@ -15,7 +15,7 @@ import torch
 import oracle
 from element_scan_recurrences_gb300 import binding as es
 from element_scan_recurrences_gb300 import workloads as wl
-from parity_helpers import check_workload, compare, run_gpu, run_oracle, sampled_lane_parity
+from parity_helpers import check_workload, compare, compare_blocks, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -147,19 +147,28 @@ def test_streams_are_respected():
 
 
 # ---------------------------------------------------------------------------
-# full-size workloads, as the bench launches them
+# the five measured workloads at full size, as the bench launches them
 
-FULL = ["tanh_decay_lanes", "normcap_vector", "maxplus_reverse", "tanh_decay_time_inner"]
+FULL = ["tanh_decay_small", "tanh_decay_lanes", "normcap_vector", "maxplus_reverse", "tanh_decay_time_inner"]
 
 
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled_lanes_and_properties(name):
+def test_full_size_every_element_and_properties(name):
+    """Every output value of the workload (each direction it names) against
+    the oracle run on all host cores on the same seeded inputs: MAXPLUS bit for
+    bit, the float bodies within 1e-5 * (1 + |oracle|); then properties that
+    hold at any size (tanh range, the norm cap, the max-plus sweep's tight
+    bound)."""
     w = wl.WORKLOADS[name]
     init, seqs = wl.make_inputs(w, "cuda")
+    init_h = init.cpu().numpy()
+    seqs_h = [s.cpu().numpy() for s in seqs]
     for reverse in w.reverse:
         out = es.scan(w.body, init, seqs, axis=w.axis, state_axis=w.state_axis, reverse=reverse)
         es.device_status()
-        sampled_lane_parity(w, init, seqs, out, reverse)
+        want = oracle.scan_threads(w.body, init_h, seqs_h, axis=w.axis, state_axis=w.state_axis, reverse=reverse)
+        compare_blocks(w.body, out.cpu().numpy(), want, "%s reverse=%s, every element" % (name, reverse))
+        del want
         assert bool(torch.isfinite(out).all())
         x, a = seqs
         if w.body == T_:
