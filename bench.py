@@ -97,33 +97,118 @@ def sum_over_ranks(dist, value: float, device=None) -> float:
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 
+class NvmlReader:
+    """Read-only NVML queries through ctypes (SM clock, its maximum, power
+    draw, the active clock-event reasons) for the GPU a process runs on.
+    Nothing here changes a setting of the GPU."""
+    SM = 1                                  # NVML_CLOCK_SM
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40}
+
+    def __init__(self, local_index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.handle = ctypes.c_void_p()
+        bus = self._pci_bus_id(local_index)
+        rc = 1
+        if bus is not None:
+            rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.handle))
+        if rc != 0:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(self._physical_index(local_index), ctypes.byref(self.handle))
+        if rc != 0:
+            raise OSError("no NVML handle for the device")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+
+    @staticmethod
+    def _pci_bus_id(local_index):
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(local_index)
+            return "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        except Exception:   # noqa: BLE001 -- older torch: fall back to the index
+            return None
+
+    @staticmethod
+    def _physical_index(local_index):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_index < len(ids) and ids[local_index].isdigit():
+            return int(ids[local_index])
+        return local_index
+
+    def sample(self):
+        ct = self.ct
+        sm, mx, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        self.lib.nvmlDeviceGetClockInfo(self.handle, self.SM, ct.byref(sm))
+        self.lib.nvmlDeviceGetMaxClockInfo(self.handle, self.SM, ct.byref(mx))
+        self.lib.nvmlDeviceGetPowerUsage(self.handle, ct.byref(mw))
+        self.reasons_fn(self.handle, ct.byref(rs))
+        return float(sm.value), float(mx.value), mw.value / 1e3, int(rs.value)
+
+
 class ClockSampler:
+    """SM clock and throttle reasons sampled in a background thread while the
+    bench runs: in-process NVML every `period_ms` (fast enough to land inside
+    a timed region of a few milliseconds), else `nvidia-smi -lms`."""
     FIELDS = ("clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap")
     REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 50):
-        self.samples = []
+    def __init__(self, gpu_index: int, period_ms: float = 0.5):
+        self.samples = []            # (time, sm MHz, max MHz, watts, set of reasons)
         self.proc = None
         self.thread = None
+        self.source = None
+        self._stop = threading.Event()
+        try:
+            self.nvml = NvmlReader(gpu_index)
+            self.nvml.sample()
+            self.source = "nvml every %.1f ms" % period_ms
+            self.thread = threading.Thread(target=self._poll, args=(period_ms / 1e3,), daemon=True)
+            self.thread.start()
+            return
+        except Exception:   # noqa: BLE001 -- no NVML here: nvidia-smi instead
+            self.nvml = None
         cmd = ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + ",".join(self.FIELDS),
-               "--format=csv,noheader,nounits", "-lms", str(period_ms)]
+               "--format=csv,noheader,nounits", "-lms", "50"]
         try:
             self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
             return
+        self.source = "nvidia-smi -lms 50"
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
 
+    def _poll(self, period):
+        while not self._stop.is_set():
+            try:
+                sm, mx, w, bits = self.nvml.sample()
+            except Exception:   # noqa: BLE001
+                return
+            names = {n for n, b in NvmlReader.REASON_BITS.items() if bits & b}
+            self.samples.append((time.time(), sm, mx, w, names))
+            time.sleep(period)
+
     def _read(self):
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) == len(self.FIELDS):
-                self.samples.append((time.time(), parts))
+                names = {n for n, v in zip(self.REASONS, parts[4:8]) if v.lower() == "active"}
+                self.samples.append((time.time(), num(parts[0]), num(parts[1]), num(parts[2]), names))
 
     def stop(self):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -134,32 +219,23 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self, t0: float, t1: float):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "nvidia-smi unavailable"}
-        inside = [p for t, p in self.samples if t0 <= t <= t1]
-        used = inside
-        note = "samples inside the timed region"
-        if len(inside) < 3:
-            # a short timed region: widen to the whole measurement window
-            used = [p for _, p in self.samples]
-            note = "timed region shorter than the sampling period; samples over warm-up and timed steps"
-
-        def num(s):
-            try:
-                return float(s)
-            except ValueError:
-                return None
-
-        sm = sorted(v for v in (num(p[0]) for p in used) if v is not None)
-        mx = [v for v in (num(p[1]) for p in used) if v is not None]
+        if self.source is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "neither NVML nor nvidia-smi available"}
+        inside = [p for p in self.samples if t0 <= p[0] <= t1]
+        used, note = inside, "samples inside the timed region"
+        if not inside:
+            used = list(self.samples)
+            note = "no sample inside the timed region; samples over warm-up and timed steps"
+        sm = sorted(p[1] for p in used if p[1] is not None)
+        mx = [p[2] for p in used if p[2] is not None]
+        pw = [p[3] for p in used if p[3] is not None]
         reasons = set()
         for p in used:
-            for name, val in zip(self.REASONS, p[4:8]):
-                if val.strip().lower() == "active":
-                    reasons.add(name)
+            reasons |= p[4]
         return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(used), "samples_in_timed_region": len(inside),
-                "note": note}
+                "reasons": sorted(reasons), "power_w_max": max(pw) if pw else None, "samples": len(used),
+                "samples_in_timed_region": len(inside), "source": self.source, "note": note}
 
 
 # ---------------------------------------------------------------------------
@@ -246,16 +322,18 @@ def oracle_backward(w, init, seqs, states, grad_out, reverse):
                                 reverse=reverse)
 
 
-def take_sample(w, init, seqs, target_elems: int):
+def take_sample(w, init, seqs, target_elems: int, min_rows: int = 1):
     """Whole sequences of a leading block of lanes, about `target_elems` output
-    values per direction: the first rows along dim 0 (or, when one row is
-    already larger, the first positions of the last lane axis of row 0).
+    values per direction: the first rows along dim 0, at least `min_rows` of
+    them where dim 0 has that many (or, when one row is already larger and one
+    row is asked for, the first positions of the last lane axis of row 0).
     Returns (initial, [sequences], elements, description)."""
     if w.ax == 0:
         raise ValueError("sampling needs a dimension before the sequence axis")
     per_row = w.elements // w.shape[0]
-    if per_row <= target_elems:
-        k = max(1, min(w.shape[0], target_elems // per_row))
+    if per_row <= target_elems or min_rows > 1:
+        k = max(1, min_rows, min(w.shape[0], target_elems // per_row))
+        k = min(k, w.shape[0])
         pick = lambda t: t[:k]
         desc = "first %d of %d rows along dim 0" % (k, w.shape[0])
         elems = k * per_row
@@ -273,38 +351,152 @@ def take_sample(w, init, seqs, target_elems: int):
     return cpu(init), [cpu(t) for t in seqs], elems, desc
 
 
-def cpu_oracle_rate(w, init, seqs, budget_s: float, backward: bool = False):
-    """Time the oracle (as it stands, one thread) on a leading block of lanes
-    of the workload; return (elements/s, description, threads).  For the
-    backward pass the oracle's forward states of the sample are made first,
-    untimed."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def run_row_blocks(fn, n_rows: int, threads: int) -> int:
+    """fn(lo, hi) over contiguous blocks of rows [0, n_rows), one thread a
+    block (the oracles' foreign calls and numpy's array operations release the
+    interpreter lock); returns the number of blocks."""
+    k = max(1, min(threads, n_rows))
+    bounds = [n_rows * i // k for i in range(k + 1)]
+    blocks = [(bounds[i], bounds[i + 1]) for i in range(k) if bounds[i + 1] > bounds[i]]
+    if len(blocks) == 1:
+        fn(*blocks[0])
+        return 1
+    import concurrent.futures
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(blocks)) as pool:
+        for f in [pool.submit(fn, lo, hi) for lo, hi in blocks]:
+            f.result()
+    return len(blocks)
+
+
+def _timed(fn):
+    t0 = time.perf_counter()
+    r = fn()
+    return time.perf_counter() - t0, r
+
+
+def oracle_baseline(sample, step, budget_s: float, threads: int):
+    """Both CPU figures of the oracle, each the median of 3 runs on a bounded
+    sample of the workload: one thread, and every host core (lanes split into
+    contiguous blocks, one per thread, each block the unchanged loop).
+    ``sample(target_elems, min_rows)`` returns (ctx, elements, description);
+    ``step(ctx, threads)`` runs the oracle once over the sample and returns
+    the threads it used.  The two runs' sample sizes are chosen so that the
+    whole measurement takes about `budget_s`."""
+    per_run = max(0.05, budget_s / 7.0)
+    ctx, e, _ = sample(1 << 18, 1)
+    t, _ = _timed(lambda: step(ctx, 1))
+    rate = e / max(t, 1e-6)
+    ctx, e1, d1 = sample(max(1, int(rate * per_run)), 1)
+    t1 = sorted(_timed(lambda: step(ctx, 1))[0] for _ in range(3))[1]
+    r1 = e1 / t1
+    ctx, en, dn = sample(max(1, int(r1 * threads * per_run)), threads)
+    t, _ = _timed(lambda: step(ctx, threads))
+    if t > 3 * per_run:
+        # one block of lanes per thread is too much work: fewer, smaller rows
+        ctx, en, dn = sample(max(1, int(en * per_run / t)), 1)
+    runs = sorted(_timed(lambda: step(ctx, threads)) for _ in range(3))
+    tn, used = runs[1]
+    return {"value": en / tn, "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": "%s (%d elements), %d threads on contiguous blocks of lanes, median of 3" % (dn, en, used),
+            "cpu_model": cpu_model(), "host_cores": threads, "median_of": 3,
+            "one_thread": {"value": r1, "unit": UNIT, "cores": 1,
+                           "sample": "%s (%d elements), one thread, median of 3" % (d1, e1)}}
+
+
+def scan_sampler(w, init, seqs, backward: bool):
+    """sample() and step() of `oracle_baseline` for an element-scan workload
+    (fixed body or body program), forward or backward (the sample's forward
+    states and an all-ones output gradient are made untimed)."""
     import numpy as np
     import oracle
     oracle.build()
 
-    def run(target):
-        ins, ss, elems, desc = take_sample(w, init, seqs, target)
+    def sample(target, min_rows):
+        ins, ss, elems, desc = take_sample(w, init, seqs, target, min_rows)
         prep = []
         if backward:
             for reverse in w.reverse:
-                st = oracle_scan(w, ins, ss, reverse)
+                st = oracle_scan_threads(w, ins, ss, reverse, host_threads())
                 prep.append((st, np.ones_like(st)))
-        t0 = time.perf_counter()
+        dirs = "+".join("reverse" if r else "forward" for r in w.reverse)
+        return (ins, ss, prep), elems * len(w.reverse), "%s of the same workload, %s" % (desc, dirs)
+
+    def step(ctx, threads):
+        ins, ss, prep = ctx
         for k, reverse in enumerate(w.reverse):
             if backward:
-                oracle_backward(w, ins, ss, prep[k][0], prep[k][1], reverse)
+                oracle_backward_threads(w, ins, ss, prep[k][0], prep[k][1], reverse, threads)
             else:
-                oracle_scan(w, ins, ss, reverse)
-        return time.perf_counter() - t0, elems * len(w.reverse), desc
+                oracle_scan_threads(w, ins, ss, reverse, threads)
+        return max(1, min(threads, ins.shape[0] if ins.ndim else 1))
+    return sample, step
 
-    target = 1 << 20
-    t, elems, desc = run(target)
-    if t < budget_s / 4:
-        target = int(target * budget_s / max(t, 1e-3))
-        t, elems, desc = run(target)
-    desc = "%s of the same workload (%d elements, %s), one thread" % (
-        desc, elems, "+".join("reverse" if r else "forward" for r in w.reverse))
-    return elems / t, desc, 1
+
+def oracle_scan_threads(w, init, seqs, reverse, threads):
+    """The oracle on `threads` contiguous blocks of lanes along dim 0."""
+    if w.text is None:
+        import oracle
+        return oracle.scan_threads(w.body, init, seqs, axis=w.axis, state_axis=w.state_axis, reverse=reverse,
+                                   threads=threads)
+    import numpy as np
+    from oracle.body import scan_body
+    shape = list(seqs[0].shape)
+    if w.state_axis:
+        shape[-1] = init.shape[-1]
+    out = np.empty(shape, np.float32)
+
+    def blk(lo, hi):
+        out[lo:hi] = scan_body(w.text, init[lo:hi], [s[lo:hi] for s in seqs], axis=w.axis,
+                               state_axis=w.state_axis, reverse=reverse)
+    run_row_blocks(blk, out.shape[0], threads)
+    return out
+
+
+def oracle_backward_threads(w, init, seqs, states, grad_out, reverse, threads):
+    """The gradient oracle on `threads` contiguous blocks of lanes along dim 0."""
+    if w.text is None:
+        import oracle
+        return oracle.scan_backward_threads(w.body, init, seqs, states, grad_out, axis=w.axis,
+                                            state_axis=w.state_axis, reverse=reverse, threads=threads)
+    from oracle.body_grad import scan_body_backward
+
+    def blk(lo, hi):
+        scan_body_backward(w.text, init[lo:hi], [s[lo:hi] for s in seqs], states[lo:hi], grad_out[lo:hi],
+                           axis=w.axis, state_axis=w.state_axis, reverse=reverse)
+    run_row_blocks(blk, states.shape[0], threads)
+
+
+def cpu_oracle_rate(w, init, seqs, budget_s: float, backward: bool = False):
+    """`cpu_baseline` of an element-scan workload: the oracle as it stands on
+    bounded samples, one thread and all host cores."""
+    sample, step = scan_sampler(w, init, seqs, backward)
+    return oracle_baseline(sample, step, budget_s, host_threads())
 
 
 def body_live_mask(w):
@@ -320,64 +512,53 @@ def body_live_mask(w):
         return None
 
 
-def run_reference(args, w):
-    """--impl reference: the CPU oracle as the comparison arm."""
-    rank, world, _ = dist_env()
-    if rank != 0:
-        return 0
-    import oracle
-    from element_scan_recurrences_gb300 import workloads as wl
-    oracle.build()
-    init, seqs = wl.make_inputs(w, "cpu")
-    # each step scans a bounded sample so that the whole run stays short
+def reference_steps(args, sample, step, config):
+    """--impl reference: the oracle on every host core as the comparison arm;
+    each of the K timed steps (after W untimed ones) scans the same bounded
+    sample of the workload, sized so that the whole run takes a few minutes."""
+    threads = host_threads()
     step_budget = max(0.05, min(1.0, 120.0 / max(1, args.steps + args.warmup)))
-    backward = args.pass_ == "backward"
-
-    def sample(target):
-        ins, ss, elems, desc = take_sample(w, init, seqs, target)
-        prep = []
-        if backward:
-            # the sample's saved states and an all-ones output gradient (untimed)
-            import numpy as np
-            for r in w.reverse:
-                st = oracle_scan(w, ins, ss, r)
-                prep.append((st, np.ones_like(st)))
-        return ins, ss, elems, desc, prep
-
-    def one_step(ins, ss, prep):
-        for k, r in enumerate(w.reverse):
-            if backward:
-                oracle_backward(w, ins, ss, prep[k][0], prep[k][1], r)
-            else:
-                oracle_scan(w, ins, ss, r)
-
-    calib = 1 << 18 if not backward or w.text is None else 1 << 14
-    ins, ss, elems, _, prep = sample(calib)
-    t0 = time.perf_counter()
-    one_step(ins, ss, prep)
-    t_cal = time.perf_counter() - t0
-    target = max(1, int(calib * step_budget / max(t_cal, 1e-4)))
-    ins, ss, elems, desc, prep = sample(target)
+    ctx, e, _ = sample(1 << 18, 1)
+    t, _ = _timed(lambda: step(ctx, threads))
+    rate = e / max(t, 1e-6)
+    ctx, elems, desc = sample(max(1, int(rate * step_budget)), threads)
+    t, _ = _timed(lambda: step(ctx, threads))
+    if t > 3 * step_budget:
+        ctx, elems, desc = sample(max(1, int(elems * step_budget / t)), 1)
+    used = 1
     for _ in range(args.warmup):
-        one_step(ins, ss, prep)
+        used = step(ctx, threads)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        one_step(ins, ss, prep)
+        step(ctx, threads)
     dt = time.perf_counter() - t0
-    elems *= len(w.reverse)
     value = elems * args.steps / dt
-    sample_desc = "%s of the same workload (%d elements per step), one thread" % (desc, elems)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config_of(w, backward, body_live_mask(w) if backward else None),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample_desc},
+        "config": config,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                         "sample": "%s (%d elements per step), %d threads on contiguous blocks of lanes" % (
+                             desc, elems, used), "cpu_model": cpu_model(), "host_cores": threads},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def run_reference(args, w):
+    """--impl reference for an element-scan workload (the fixed-body oracle,
+    or the body-program oracle for a body given as text)."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from element_scan_recurrences_gb300 import workloads as wl
+    init, seqs = wl.make_inputs(w, "cpu")
+    backward = args.pass_ == "backward"
+    sample, step = scan_sampler(w, init, seqs, backward)
+    return reference_steps(args, sample, step, config_of(w, backward, body_live_mask(w) if backward else None))
 
 
 def config_of(w, backward=False, live=None):
@@ -452,11 +633,14 @@ def roofline_of(kernel, prof_name, alg_bytes, kernel_ms):
             if peak_kind == "measured" else "fallback 6.8 TB/s"}
 
 
-def emit_line(args, world, value, region_ms, config, roofline, cpu, e2e, launches, clocks):
+def emit_line(args, world, value, region_ms, config, roofline, cpu, e2e, launches, clocks, path):
+    """Rank 0's JSON line.  `config` is the same object the reference arm
+    prints; the kernel path and the multi-GPU arrangement sit beside it."""
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": region_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
+        "path": path, "parallelism": "replicas: each GPU scans its own batch" if world > 1 else "single GPU",
         "achieved_gbs": roofline["achieved"], "hbm_frac": roofline["frac"],
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
     }
@@ -595,13 +779,11 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, desc, cores = cpu_oracle_rate(w, init, seqs, args.cpu_budget, backward=backward)
-        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        cpu = cpu_oracle_rate(w, init, seqs, args.cpu_budget, backward=backward)
 
     if rank == 0:
-        config = dict(config_of(w, backward, live), parallelism="replicas: each GPU scans its own batch"
-                      if world > 1 else "single GPU", path=plans[0]["path"])
-        emit_line(args, world, value, region_ms, config, roofline, cpu, e2e, launches, clocks)
+        emit_line(args, world, value, region_ms, config_of(w, backward, live), roofline, cpu, e2e, launches,
+                  clocks, plans[0]["path"])
     if dist is not None:
         dist.destroy_process_group()
     return 0
@@ -656,19 +838,21 @@ def matrix_config(w, backward=False):
             "l2": "no flush: inputs and outputs (%.2f GB) exceed the 129 MB L2" % (alg / 1e9)}
 
 
-def matrix_sample(w, a, b, target_elems):
+def matrix_sample(w, a, b, target_elems, min_rows=1):
     """The first rows along dim 0 (every lane of them, whole sequences) of a
-    and b, about `target_elems` output values; when one row is already
-    larger (few long lanes, the scan along dim 1), the first trips of row 0."""
+    and b, about `target_elems` output values and at least `min_rows` rows
+    where dim 0 has them; when that is already larger and the scan runs along
+    dim 1 (few long lanes), the first trips of those rows."""
     per_row = w.elements // w.lead[0]
-    if per_row <= target_elems or w.ax != 1:
-        k = max(1, min(w.lead[0], target_elems // per_row))
+    rows = max(1, min(w.lead[0], min_rows))
+    if w.ax != 1 or per_row * rows <= target_elems:
+        k = max(rows, min(w.lead[0], target_elems // per_row))
         return (a[:k].contiguous().cpu().numpy(), b[:k].contiguous().cpu().numpy(), k * per_row,
                 "first %d of %d rows along dim 0" % (k, w.lead[0]))
     per_trip = per_row // w.T
-    t = max(1, min(w.T, target_elems // per_trip))
-    return (a[:1, :t].contiguous().cpu().numpy(), b[:1, :t].contiguous().cpu().numpy(), t * per_trip,
-            "row 0 along dim 0, its first %d of %d trips" % (t, w.T))
+    t = max(1, min(w.T, target_elems // (per_trip * rows)))
+    return (a[:rows, :t].contiguous().cpu().numpy(), b[:rows, :t].contiguous().cpu().numpy(), rows * t * per_trip,
+            "first %d of %d rows along dim 0, their first %d of %d trips" % (rows, w.lead[0], t, w.T))
 
 
 def matrix_oracle(w, a, b, reverse):
@@ -713,17 +897,17 @@ KERNEL_SOURCES.update({k: ["k_matrix.cu", "es_matrix_api.cu"]
                        for k in ("k_mat_tma_bwd", "k_mat_generic_bwd", "k_mat_tma_chunked_bwd")})
 
 
-def op_sample(w, inputs, target_elems):
+def op_sample(w, inputs, target_elems, min_rows=1):
     """A bounded sample of an op workload for the oracle: (inputs, elements,
     description)."""
     from element_scan_recurrences_gb300 import workloads as wl
     if isinstance(w, wl.TableWorkload):
         table, sym = inputs
         per_row = w.elements // w.shape[0]
-        k = max(1, min(w.shape[0], target_elems // per_row))
+        k = min(w.shape[0], max(1, min_rows, target_elems // per_row))
         return ([table.cpu().numpy(), sym[:k].contiguous().cpu().numpy()], k * per_row,
                 "first %d of %d rows along dim 0" % (k, w.shape[0]))
-    sa, sb, elems, desc = matrix_sample(w, inputs[0], inputs[1], target_elems)
+    sa, sb, elems, desc = matrix_sample(w, inputs[0], inputs[1], target_elems, min_rows)
     return [sa, sb], elems, desc
 
 
@@ -746,27 +930,46 @@ def op_backward_prep(w, sample):
     return prep
 
 
-def op_oracle_step(w, sample, prep, backward):
-    for k, r in enumerate(w.reverse):
-        if backward:
-            matrix_oracle_backward(w, sample[0], sample[1], prep[k][0], prep[k][1], r)
-        else:
-            op_oracle(w, sample, r)
+def op_sampler(w, inputs, backward):
+    """sample() and step() of `oracle_baseline` for a matrix-scan,
+    linear-scan or table-scan workload; the threads split the sample's rows
+    along dim 0 into contiguous blocks (one thread when the scan runs along
+    dim 0)."""
+    from element_scan_recurrences_gb300 import workloads as wl
+    table = isinstance(w, wl.TableWorkload)
+
+    def sample(target, min_rows):
+        smp, elems, desc = op_sample(w, inputs, target, min_rows)
+        prep = op_backward_prep(w, smp) if backward else None
+        return (smp, prep), elems * len(w.reverse), "%s of the same workload" % desc
+
+    def step(ctx, threads):
+        smp, prep = ctx
+        rows = smp[1].shape[0]
+        if w.ax == 0 or rows <= 1:
+            threads = 1
+        used = 1
+        for k, r in enumerate(w.reverse):
+            if table:
+                fn = lambda lo, hi: op_oracle(w, [smp[0], smp[1][lo:hi]], r)
+            elif backward:
+                fn = lambda lo, hi: matrix_oracle_backward(w, smp[0][lo:hi], smp[1][lo:hi], prep[k][0][lo:hi],
+                                                           prep[k][1][lo:hi], r)
+            else:
+                fn = lambda lo, hi: matrix_oracle(w, smp[0][lo:hi], smp[1][lo:hi], r)
+            if threads > 1:
+                used = run_row_blocks(fn, rows, threads)
+            else:
+                fn(0, rows)
+        return used
+    return sample, step
 
 
 def op_cpu_rate(w, inputs, budget_s, backward=False):
-    def run(target):
-        sample, elems, desc = op_sample(w, inputs, target)
-        prep = op_backward_prep(w, sample) if backward else None
-        t0 = time.perf_counter()
-        op_oracle_step(w, sample, prep, backward)
-        return time.perf_counter() - t0, elems * len(w.reverse), desc
-
-    target = 1 << 18
-    t, elems, desc = run(target)
-    if t < budget_s / 4:
-        t, elems, desc = run(int(target * budget_s / max(t, 1e-3)))
-    return elems / t, "%s of the same workload (%d elements), one thread" % (desc, elems), 1
+    """`cpu_baseline` of an op workload: its oracle on bounded samples, one
+    thread and all host cores."""
+    sample, step = op_sampler(w, inputs, backward)
+    return oracle_baseline(sample, step, budget_s, host_threads())
 
 
 class OpJob:
@@ -920,13 +1123,10 @@ def run_ours_op(args, w):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, desc, cores = op_cpu_rate(w, job.inputs, args.cpu_budget, backward=backward)
-        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        cpu = op_cpu_rate(w, job.inputs, args.cpu_budget, backward=backward)
     if rank == 0:
-        config = dict(matrix_config(w, True) if backward else job.config(),
-                      parallelism="replicas: each GPU scans its own batch" if world > 1 else "single GPU",
-                      path=plans[0]["path"])
-        emit_line(args, world, value, region_ms, config, roofline, cpu, e2e, launches, clocks)
+        emit_line(args, world, value, region_ms, matrix_config(w, True) if backward else job.config(), roofline,
+                  cpu, e2e, launches, clocks, plans[0]["path"])
     if dist is not None:
         dist.destroy_process_group()
     return 0
@@ -934,7 +1134,8 @@ def run_ours_op(args, w):
 
 def run_reference_op(args, w):
     """--impl reference for a matrix-scan, linear-scan or table-scan
-    workload: its oracle on a bounded sample of the same workload, each step."""
+    workload: its oracle on every host core over a bounded sample of the same
+    workload, each step."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
@@ -948,34 +1149,8 @@ def run_reference_op(args, w):
     backward = args.pass_ == "backward"
     if backward:
         config = matrix_config(w, True)
-    step_budget = max(0.05, min(1.0, 120.0 / max(1, args.steps + args.warmup)))
-    sample, elems, _ = op_sample(w, inputs, 1 << 14)
-    prep = op_backward_prep(w, sample) if backward else None
-    t0 = time.perf_counter()
-    op_oracle_step(w, sample, prep, backward)
-    t_cal = time.perf_counter() - t0
-    sample, elems, desc = op_sample(w, inputs, max(1, int((1 << 14) * step_budget / max(t_cal, 1e-4))))
-    prep = op_backward_prep(w, sample) if backward else None
-    for _ in range(args.warmup):
-        op_oracle_step(w, sample, prep, backward)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        op_oracle_step(w, sample, prep, backward)
-    dt = time.perf_counter() - t0
-    elems *= len(w.reverse)
-    value = elems * args.steps / dt
-    sample = "%s of the same workload (%d elements per step), one thread" % (desc, elems)
-    line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config,
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "gpu_launches": 0,
-    }
-    print(json.dumps(line), flush=True)
-    return 0
+    sample, step = op_sampler(w, inputs, backward)
+    return reference_steps(args, sample, step, config)
 
 
 def main(argv=None):
