@@ -605,6 +605,64 @@ def time_device_steps(step, stream, device, dist, args, rank, local, es):
     return region_ms, per_step_ms, launches, clocks
 
 
+def chain_bound(es, w, program, stream, device, backward, sm_mhz):
+    """The serial bound of a workload with few lanes: the same kernel on one
+    CTA's worth of lanes (the first lanes of row 0, every trip), timed alone,
+    where no other CTA competes for bandwidth.  Its time is T trips x the
+    cycles one trip of the chain takes; the full launch cannot be faster than
+    that however much bandwidth is left."""
+    import torch
+    from element_scan_recurrences_gb300 import workloads as wl
+    W = w.shape[-1]
+    per_warp = 32 * min(W, 4) // W if w.state_axis else 32
+    lanes = 2 * per_warp                       # one CTA of two consumer warps
+    shape = list(w.shape)
+    shape[0] = 1
+    shape[w.rank - 2 if w.state_axis else w.rank - 1] = lanes
+    probe = w.with_shape(shape, name=w.name + "_one_cta")
+    init, seqs = wl.make_inputs(probe, device)
+    out = torch.empty(probe.shape, device=device)
+    r = probe.reverse[0]
+    if backward:
+        if program is not None:
+            program.scan_into(init, seqs, out, axis=w.axis, state_axis=w.state_axis, reverse=r, stream=stream)
+        else:
+            es.scan_into(w.body, init, seqs, out, axis=w.axis, state_axis=w.state_axis, reverse=r, stream=stream)
+        g = torch.ones_like(out)
+        grads = (torch.empty_like(init), [torch.empty_like(t) for t in seqs])
+
+    def once():
+        if backward:
+            if program is not None:
+                program.scan_backward(init, seqs, out, g, axis=w.axis, state_axis=w.state_axis, reverse=r,
+                                      grads=grads, stream=stream)
+            else:
+                es.scan_backward(w.body, init, seqs, out, g, axis=w.axis, state_axis=w.state_axis, reverse=r,
+                                 grads=grads, stream=stream)
+        elif program is not None:
+            program.scan_into(init, seqs, out, axis=w.axis, state_axis=w.state_axis, reverse=r, stream=stream)
+        else:
+            es.scan_into(w.body, init, seqs, out, axis=w.axis, state_axis=w.state_axis, reverse=r, stream=stream)
+
+    for _ in range(3):
+        once()
+    times = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        once()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        times.append(e0.elapsed_time(e1))
+    es.device_status(stream)
+    ms = sorted(times)[len(times) // 2]
+    res = {"latency_bound_ms": ms, "latency_probe": "the same kernel on %d lanes (one CTA), shape %s, median of 5"
+           % (lanes, shape)}
+    if sm_mhz:
+        res["cycles_per_trip"] = ms * 1e-3 * sm_mhz * 1e6 / w.T
+    return res
+
+
 def time_e2e(e2e_step, steps, stream, device, dist):
     """One untimed end-to-end step, then `steps` timed ones (events on the
     stream the copies and kernels run on); ms over the slowest rank."""
@@ -728,6 +786,9 @@ def run_ours(args, w):
         kernels = PATH_KERNEL_BODY if program is not None else PATH_KERNEL
     kernel = kernels.get(plans[0]["path"], plans[0]["path"])
     roofline = roofline_of(kernel, w.name + ("_backward" if backward else ""), alg_bytes, kernel_ms)
+    if plans[0]["path"] == "vec_tma" and w.ax > 0 and rank == 0:
+        roofline.update(chain_bound(es, w, program, stream, device, backward,
+                                    clocks["sm_mhz"] if clocks and clocks.get("sm_mhz") else None))
 
     # end to end through the public API with host buffers
     e2e = None

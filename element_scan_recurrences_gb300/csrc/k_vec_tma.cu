@@ -43,7 +43,6 @@ namespace {
 
 constexpr int kTT = 32;       // trips per tile
 constexpr int kMaxStages = 8;
-constexpr int kRow = 128;        // values of x per CTA per trip
 
 template <int E>
 struct Vec;
@@ -51,6 +50,7 @@ template <>
 struct Vec<1> {
     static __device__ __forceinline__ void load(float* d, const float* p) { d[0] = p[0]; }
     static __device__ __forceinline__ void store(float* p, const float* v) { __stcs(p, v[0]); }
+    static __device__ __forceinline__ void put(float* p, const float* v) { p[0] = v[0]; }
 };
 template <>
 struct Vec<2> {
@@ -61,6 +61,9 @@ struct Vec<2> {
     }
     static __device__ __forceinline__ void store(float* p, const float* v) {
         __stcs(reinterpret_cast<float2*>(p), make_float2(v[0], v[1]));
+    }
+    static __device__ __forceinline__ void put(float* p, const float* v) {
+        *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
     }
 };
 template <>
@@ -75,6 +78,9 @@ struct Vec<4> {
     static __device__ __forceinline__ void store(float* p, const float* v) {
         __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
     }
+    static __device__ __forceinline__ void put(float* p, const float* v) {
+        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    }
 };
 template <int E>
 struct VecN {   // E = 8 or 16 values as 16-byte pieces
@@ -85,6 +91,10 @@ struct VecN {   // E = 8 or 16 values as 16-byte pieces
     static __device__ __forceinline__ void store(float* p, const float* v) {
 #pragma unroll
         for (int i = 0; i < E; i += 4) Vec<4>::store(p + i, v + i);
+    }
+    static __device__ __forceinline__ void put(float* p, const float* v) {
+#pragma unroll
+        for (int i = 0; i < E; i += 4) Vec<4>::put(p + i, v + i);
     }
 };
 template <>
@@ -102,26 +112,26 @@ __device__ __forceinline__ float normcap_scale(float ss) {
     return ieee_minimum(r, 1.0f);
 }
 
-template <int W, int E, bool GW>
-__global__ void __launch_bounds__(32 + kRow / E)
+template <int W, int E, bool GW, int CW>
+__global__ void __launch_bounds__(32 * (CW + 2))
 k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_g,
-          const float* __restrict__ init, float* __restrict__ out, int T, int J, int gw, int tiles_j, int stages,
-          int reverse, unsigned int* status, uint64_t wait_ns, int64_t drop_tile) {
-    constexpr int LV = kRow / W;                   // lanes per CTA
-    constexpr int NC = kRow / E;                   // consumer threads
+          const __grid_constant__ CUtensorMap map_o, const float* __restrict__ init, int T, int J, int gw,
+          int tiles_j, int stages, int reverse, unsigned int* status, uint64_t wait_ns, int64_t drop_tile) {
+    constexpr int NC = 32 * CW;                    // consumer threads
+    constexpr int R = NC * E;                      // values of x per CTA per trip
+    constexpr int LV = R / W;                      // lanes per CTA
     constexpr int G = W / E;                       // threads per lane
-    // active consumer lanes of a warp (fewer than 32 when E is large)
-    constexpr unsigned kMask = NC >= 32 ? 0xffffffffu : ((1u << NC) - 1u);
     constexpr int GE = GW ? E : 1;                 // staged gate values per trip
     // whole-tile staging while the tile's operands fit in about 160 registers
     constexpr bool kStageTile = ES_VEC_STAGE_TILE < 0 ? (kTT * (E + GE) <= 160) : (ES_VEC_STAGE_TILE != 0);
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+    __shared__ __align__(8) uint64_t done_bar[kMaxStages];
     __shared__ int abort_flag;
 
     const int gl = LV * gw;                        // gate floats per trip row
-    const uint32_t x_bytes = kTT * kRow * 4;
+    const uint32_t x_bytes = kTT * R * 4;
     const uint32_t g_bytes = static_cast<uint32_t>(kTT * gl * 4);
     const uint32_t g_pad = (g_bytes + 1023u) & ~1023u;
     const uint32_t stage_bytes = x_bytes + g_pad;
@@ -136,14 +146,16 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], (NC + 31) / 32);
+            mbar_init(&done_bar[s], CW);
+            mbar_init(&empty_bar[s], 1);
         }
         abort_flag = 0;
         mbar_fence_init();
     }
     __syncthreads();
 
-    if (warp == 0) {
+    if (warp == CW) {
+        // producer: time tiles of x and of the gate into the stage ring
         if (lane == 0) {
             tma_prefetch_desc(&map_x);
             tma_prefetch_desc(&map_g);
@@ -172,18 +184,40 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
         }
         return;
     }
+    if (warp == CW + 1) {
+        // storer: the consumers leave each tile's states in place of its x
+        // values; the tile leaves shared memory as one TMA tensor store (rows
+        // past T and lanes past J are clipped by the tensor map), and the
+        // stage goes back to the producer once the store has read it
+        if (lane == 0) {
+            tma_prefetch_desc(&map_o);
+            for (int k = 0; k < ntiles; ++k) {
+                const int s = k % stages;
+                if (!mbar_wait_bounded(&done_bar[s], (k / stages) & 1, wait_ns, &abort_flag)) {
+                    report_timeout(status, &abort_flag);
+                    break;
+                }
+                const int j = reverse ? ntiles - 1 - k : k;
+                tma_store_3d(&map_o, j0 * W, j * kTT, o, base + static_cast<size_t>(s) * stage_bytes);
+                bulk_commit();
+                bulk_wait_read<0>();
+                mbar_arrive(&empty_bar[s]);
+            }
+            bulk_wait_all();
+        }
+        return;
+    }
 
     // consumers: thread c holds values w0 .. w0+E-1 of lane j0 + v
-    const int c = threadIdx.x - 32;
+    constexpr unsigned kMask = 0xffffffffu;
+    const int c = threadIdx.x;
     const int v = (c * E) / W;
     const int w0 = (c * E) % W;
     const bool valid = j0 + v < J;
-    const int64_t row = static_cast<int64_t>(J) * W;           // values per trip row
     float h[E];
 #pragma unroll
     for (int e = 0; e < E; ++e)
         h[e] = valid ? init[(static_cast<int64_t>(o) * J + j0 + v) * W + w0 + e] : 0.0f;
-    float* obase = out + static_cast<int64_t>(o) * T * row + static_cast<int64_t>(j0) * W + c * E;
     const int gi = v * gw + (GW ? w0 : 0);
 
     for (int k = 0; k < ntiles; ++k) {
@@ -196,11 +230,13 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
         const int j = reverse ? ntiles - 1 - k : k;
         const int t0 = j * kTT;
         const int n = min(kTT, T - t0);
-        const float* xs = reinterpret_cast<const float*>(base + static_cast<size_t>(s) * stage_bytes) + c * E;
+        // a thread writes each state over its own x values of that trip,
+        // after it has read them
+        float* xs = reinterpret_cast<float*>(base + static_cast<size_t>(s) * stage_bytes) + c * E;
         const float* gs = reinterpret_cast<const float*>(base + static_cast<size_t>(s) * stage_bytes + x_bytes) + gi;
-        float* op = obase + static_cast<int64_t>(t0) * row;
+        float* op = xs;
         auto load = [&](const int tt, float* xd, float* gd) {
-            Vec<E>::load(xd, xs + tt * kRow);
+            Vec<E>::load(xd, xs + tt * R);
 #pragma unroll
             for (int e = 0; e < GE; ++e) gd[e] = gs[tt * gl + e];
         };
@@ -223,7 +259,7 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
             const float scale = normcap_scale(ss);
 #pragma unroll
             for (int e = 0; e < E; ++e) h[e] = __fmul_rn(y[e], scale);
-            if (valid) Vec<E>::store(op + static_cast<int64_t>(tt) * row, h);
+            Vec<E>::put(op + tt * R, h);
         };
         // Sum over the lane's W values of u[e]*v[e]: this thread's E products
         // pairwise, then the xor-shuffle butterfly of the lane's group.
@@ -237,31 +273,42 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
                 for (int e = 0; e + span < E; e += 2 * span) p[e] = __fadd_rn(p[e], p[e + span]);
             return p[0];
         };
+        // the same sum with the products folded into two fused partial sums
+        auto fused_dot = [&](const float* u, const float* v) {
+            float p0 = __fmul_rn(u[0], v[0]);
+            if constexpr (E == 1) {
+                return p0;
+            } else {
+                float p1 = __fmul_rn(u[1], v[1]);
+#pragma unroll
+                for (int e = 2; e < E; e += 2) {
+                    p0 = __fmaf_rn(u[e], v[e], p0);
+                    p1 = __fmaf_rn(u[e + 1], v[e + 1], p1);
+                }
+                return __fadd_rn(p0, p1);
+            }
+        };
         if constexpr (kStageTile) {
             // the whole tile goes to registers before the chain starts
             float xr[kTT][E], gr[kTT][GE];
 #pragma unroll
             for (int tt = 0; tt < kTT; ++tt) load(tt, xr[tt], gr[tt]);
-            // the stage is free as soon as the tile sits in registers
-            __syncwarp(kMask);
-            if (lane == 0) mbar_arrive(&empty_bar[s]);
             // A full tile with a width-one gate, trips in scan order.  With
             // h = s*y and a = g'*s, the next trip's y' = g'*h + x' has
-            //     ||y'||^2 = a^2 ||y||^2 + 2a (y . x') + ||x'||^2,
-            // and all three sums depend only on this trip's y and the staged x',
-            // so they are reduced while this trip's scale s is still being formed.
-            // The scale of the next trip then needs a few scalar operations after
-            // s instead of a whole y' -> ||y'||^2 reduction: the serial chain per
-            // trip roughly halves.  The sum is clamped at zero (rounding could
-            // make a vanishing norm slightly negative).  The first trip of a tile
-            // reduces its ||y||^2 directly.
+            //     ||y'||^2 = a^2 ||y||^2 + 2a (y . x') + ||x'||^2.
+            // ||y||^2 is the value this trip's scale s came from, and the two
+            // dot products depend only on this trip's y and the staged x', so
+            // they are reduced while s is still being formed: the next scale
+            // needs a few scalar operations after s instead of a whole
+            // y' -> ||y'||^2 reduction.  While the cap acts, a^2 ||y||^2 is
+            // g'^2 whatever the rounding of ||y||^2, so rounding errors do not
+            // build up along the tile; the sum is clamped at zero (rounding
+            // could make a vanishing norm slightly negative), and each tile's
+            // first trip reduces its ||y||^2 directly.  The dot products fold
+            // their products into two fused partial sums.
             auto propagated_tile = [&](auto fwd_tag) {
                 constexpr bool FWD = decltype(fwd_tag)::value;
                 constexpr int first = FWD ? 0 : kTT - 1;
-                // the state alternates between two register sets, so a trip
-                // never overwrites registers the previous trip's store may
-                // still be reading
-                float hr[2][E];
                 float y[E];
 #pragma unroll
                 for (int e = 0; e < E; ++e) y[e] = __fadd_rn(__fmul_rn(gr[first][0], h[e]), xr[first][e]);
@@ -271,36 +318,31 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
 #pragma unroll
                 for (int q = 0; q < kTT; ++q) {
                     const int tt = FWD ? q : kTT - 1 - q;
-                    float* hs = hr[q & 1];
                     const float sc = normcap_scale(qf);
                     if (q + 1 < kTT) {
                         const int tn = FWD ? tt + 1 : tt - 1;
-                        float Q = local_dot(y, y);
-                        float D = local_dot(y, xr[tn]);
-                        float P = local_dot(xr[tn], xr[tn]);
+                        float D = fused_dot(y, xr[tn]);
+                        float P = fused_dot(xr[tn], xr[tn]);
 #pragma unroll
                         for (int off = G / 2; off >= 1; off >>= 1) {
-                            Q = __fadd_rn(Q, __shfl_xor_sync(kMask, Q, off));
                             D = __fadd_rn(D, __shfl_xor_sync(kMask, D, off));
                             P = __fadd_rn(P, __shfl_xor_sync(kMask, P, off));
                         }
 #pragma unroll
-                        for (int e = 0; e < E; ++e) hs[e] = __fmul_rn(y[e], sc);
-                        if (valid) Vec<E>::store(op + static_cast<int64_t>(tt) * row, hs);
+                        for (int e = 0; e < E; ++e) h[e] = __fmul_rn(y[e], sc);
+                        Vec<E>::put(op + tt * R, h);
                         const float gn = gr[tn][0];
 #pragma unroll
-                        for (int e = 0; e < E; ++e) y[e] = __fadd_rn(__fmul_rn(gn, hs[e]), xr[tn][e]);
+                        for (int e = 0; e < E; ++e) y[e] = __fadd_rn(__fmul_rn(gn, h[e]), xr[tn][e]);
                         const float a = __fmul_rn(gn, sc);
-                        qf = __fmaf_rn(__fmul_rn(a, a), Q, __fmaf_rn(__fadd_rn(a, a), D, P));
+                        qf = __fmaf_rn(__fmul_rn(a, a), qf, __fmaf_rn(__fadd_rn(a, a), D, P));
                         qf = ieee_maximum(qf, 0.0f);
                     } else {
 #pragma unroll
-                        for (int e = 0; e < E; ++e) hs[e] = __fmul_rn(y[e], sc);
-                        if (valid) Vec<E>::store(op + static_cast<int64_t>(tt) * row, hs);
+                        for (int e = 0; e < E; ++e) h[e] = __fmul_rn(y[e], sc);
+                        Vec<E>::put(op + tt * R, h);
                     }
                 }
-#pragma unroll
-                for (int e = 0; e < E; ++e) h[e] = hr[(kTT - 1) & 1][e];
             };
             // full tiles run unguarded (one basic block, so consecutive trips
             // overlap); only the ragged last tile checks every trip
@@ -348,45 +390,70 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
                     if (tt - 1 < n) trip(tt - 1, xb, gb);
                 }
             }
-            __syncwarp(kMask);
-            if (lane == 0) mbar_arrive(&empty_bar[s]);
         }
+        // the tile's states are in shared memory: make them visible to the
+        // tensor store and hand the stage to the storer
+        fence_proxy_async_smem();
+        __syncwarp(kMask);
+        if (lane == 0) mbar_arrive(&done_bar[s]);
     }
 }
 
-template <int W, int E>
-cudaError_t launch_we(const Launch& L, const CUtensorMap& mx, const CUtensorMap& mg, int gw, int tiles_j,
-                      int stages, size_t stage_bytes) {
-    const size_t smem = static_cast<size_t>(stages) * stage_bytes + 1024;
-    auto kern = gw == 1 ? k_vec_tma<W, E, false> : k_vec_tma<W, E, true>;
+// values per consumer thread and consumer warps per CTA for a state width
+struct VecShape {
+    int E, CW;
+};
+
+template <int W, int E, int CW>
+cudaError_t launch_wec(const Launch& L, const CUtensorMap& mx, const CUtensorMap& mg, const CUtensorMap& mo,
+                       int gw, int tiles_j, int stages, size_t smem) {
+    auto kern = gw == 1 ? k_vec_tma<W, E, false, CW> : k_vec_tma<W, E, true, CW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int64_t grid = L.O * tiles_j;
-    kern<<<static_cast<unsigned>(grid), 32 + kRow / E, smem, L.stream>>>(
-        mx, mg, L.init, L.out, static_cast<int>(L.T), static_cast<int>(L.J), gw, tiles_j, stages, L.reverse,
-        L.status, L.wait_ns, L.drop_tile);
+    kern<<<static_cast<unsigned>(grid), 32 * (CW + 2), smem, L.stream>>>(
+        mx, mg, mo, L.init, static_cast<int>(L.T), static_cast<int>(L.J), gw, tiles_j, stages, L.reverse, L.status,
+        L.wait_ns, L.drop_tile);
     return cudaGetLastError();
 }
 
-template <int W>
-cudaError_t launch_w(const Launch& L, const CUtensorMap& mx, const CUtensorMap& mg, int gw, int tiles_j,
-                     int stages, size_t stage_bytes) {
-    // values per thread: each halving of a lane's thread group takes one
-    // shuffle off the serial chain and adds one add to the thread's own tree
+template <int W, int E>
+cudaError_t launch_we(const Launch& L, const CUtensorMap& mx, const CUtensorMap& mg, const CUtensorMap& mo, int gw,
+                      int tiles_j, int stages, size_t smem, int CW) {
+    if (CW == 2) return launch_wec<W, E, 2>(L, mx, mg, mo, gw, tiles_j, stages, smem);
+    return launch_wec<W, E, 1>(L, mx, mg, mo, gw, tiles_j, stages, smem);
+}
+
+// values per thread: each halving of a lane's thread group takes one shuffle
+// off the serial chain and adds one add to the thread's own tree
+int vec_values_per_thread(int W) {
     int E = ES_VEC_VALUES_PER_THREAD;
     if (E == 0) E = W >= 4 ? 4 : W;
-    if (E > W) E = W;
+    return E > W ? W : E;
+}
+
+// Consumer warps per CTA: two (on two schedulers of the SM) where the row of
+// lanes is wide enough, so that one CTA a SM drives two independent chains.
+int vec_consumer_warps(int W, int64_t J) {
+    const int lanes_per_warp = 32 * vec_values_per_thread(W) / W;
+    return J >= 2 * lanes_per_warp ? 2 : 1;
+}
+
+template <int W>
+cudaError_t launch_w(const Launch& L, const CUtensorMap& mx, const CUtensorMap& mg, const CUtensorMap& mo, int gw,
+                     int tiles_j, int stages, size_t smem, int CW) {
+    const int E = vec_values_per_thread(W);
     if constexpr (W >= 16) {
-        if (E == 16) return launch_we<W, 16>(L, mx, mg, gw, tiles_j, stages, stage_bytes);
+        if (E == 16) return launch_we<W, 16>(L, mx, mg, mo, gw, tiles_j, stages, smem, CW);
     }
     if constexpr (W >= 8) {
-        if (E == 8) return launch_we<W, 8>(L, mx, mg, gw, tiles_j, stages, stage_bytes);
+        if (E == 8) return launch_we<W, 8>(L, mx, mg, mo, gw, tiles_j, stages, smem, CW);
     }
     if constexpr (W >= 4) {
-        if (E == 4) return launch_we<W, 4>(L, mx, mg, gw, tiles_j, stages, stage_bytes);
+        if (E == 4) return launch_we<W, 4>(L, mx, mg, mo, gw, tiles_j, stages, smem, CW);
     }
-    if (E == 2) return launch_we<W, 2>(L, mx, mg, gw, tiles_j, stages, stage_bytes);
-    return launch_we<W, 1>(L, mx, mg, gw, tiles_j, stages, stage_bytes);
+    if (E == 2) return launch_we<W, 2>(L, mx, mg, mo, gw, tiles_j, stages, smem, CW);
+    return launch_we<W, 1>(L, mx, mg, mo, gw, tiles_j, stages, smem, CW);
 }
 
 bool encode_vec(const Launch& L, CUtensorMap* m, const float* base, int64_t row, int box_inner, const char** err) {
@@ -412,7 +479,7 @@ bool vec_tma_ok(int body, int64_t O, int64_t T, int64_t J, int64_t W, const int6
     if (body != ES_BODY_NORMCAP) return false;
     if (W != 2 && W != 4 && W != 8 && W != 16) return false;
     if (sw[0] != W || (sw[1] != 1 && sw[1] != W)) return false;
-    const int64_t LV = kRow / W;
+    const int64_t LV = 32 * vec_values_per_thread(static_cast<int>(W)) / W;     // lanes of one consumer warp
     if (J < LV) return false;                               // a tile never exceeds the row
     if ((J * W) % 4 != 0 || (J * sw[1]) % 4 != 0 || (LV * sw[1]) % 4 != 0) return false;   // 16-byte strides, boxes
     if (O >= (int64_t(1) << 31) || T >= (int64_t(1) << 31) || J * W >= (int64_t(1) << 31)) return false;
@@ -425,25 +492,32 @@ bool vec_tma_ok(int body, int64_t O, int64_t T, int64_t J, int64_t W, const int6
 cudaError_t launch_vec_tma(const Launch& L, const char** err) {
     const int W = static_cast<int>(L.W);
     const int gw = static_cast<int>(L.sw[1]);
-    const int LV = kRow / W;
+    const int E = vec_values_per_thread(W);
+    const int CW = vec_consumer_warps(W, L.J);
+    const int R = 32 * CW * E;                  // values of a trip row per CTA
+    const int LV = R / W;                       // lanes per CTA
     const int64_t tiles_j = (L.J + LV - 1) / LV;
     const int64_t ctas = L.O * tiles_j;
-    const size_t x_bytes = static_cast<size_t>(kTT) * kRow * 4;
+    const size_t x_bytes = static_cast<size_t>(kTT) * R * 4;
     const size_t g_bytes = static_cast<size_t>(kTT) * LV * gw * 4;
     const size_t stage_bytes = x_bytes + ((g_bytes + 1023) & ~size_t(1023));
+    // a stage is held from its load through the chain to the store of its
+    // states: 3 or more stages, as many as the CTAs a SM holds leave room for
     const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>(8, (ctas + L.num_sms - 1) / L.num_sms));
-    const int64_t budget = std::min<int64_t>(96 * 1024, (200 * 1024) / per_sm);
+    const int64_t budget = (200 * 1024) / per_sm;
     const int stages = static_cast<int>(
-        std::max<int64_t>(2, std::min<int64_t>(kMaxStages, budget / static_cast<int64_t>(stage_bytes))));
-    CUtensorMap mx, mg;
-    if (!encode_vec(L, &mx, L.x, L.J * W, kRow, err) || !encode_vec(L, &mg, L.a, L.J * gw, LV * gw, err))
+        std::max<int64_t>(3, std::min<int64_t>(kMaxStages, budget / static_cast<int64_t>(stage_bytes))));
+    const size_t smem = static_cast<size_t>(stages) * stage_bytes + 1024;
+    CUtensorMap mx, mg, mo;
+    if (!encode_vec(L, &mx, L.x, L.J * W, R, err) || !encode_vec(L, &mg, L.a, L.J * gw, LV * gw, err) ||
+        !encode_vec(L, &mo, L.out, L.J * W, R, err))
         return cudaErrorInvalidValue;
     const int tj = static_cast<int>(tiles_j);
     switch (W) {
-        case 2: return launch_w<2>(L, mx, mg, gw, tj, stages, stage_bytes);
-        case 4: return launch_w<4>(L, mx, mg, gw, tj, stages, stage_bytes);
-        case 8: return launch_w<8>(L, mx, mg, gw, tj, stages, stage_bytes);
-        default: return launch_w<16>(L, mx, mg, gw, tj, stages, stage_bytes);
+        case 2: return launch_w<2>(L, mx, mg, mo, gw, tj, stages, smem, CW);
+        case 4: return launch_w<4>(L, mx, mg, mo, gw, tj, stages, smem, CW);
+        case 8: return launch_w<8>(L, mx, mg, mo, gw, tj, stages, smem, CW);
+        default: return launch_w<16>(L, mx, mg, mo, gw, tj, stages, smem, CW);
     }
 }
 
