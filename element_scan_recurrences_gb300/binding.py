@@ -716,8 +716,12 @@ STATIC_SCRATCH_BYTES = 32 << 20
 
 def matrix_scan_static(a, b, axis: int = 0, reverse: bool = False, projective: bool = False, out=None,
                        stream=None):
-    """matrix-scan whose chunked path (few long lanes) runs in the library's
-    own static device scratch: no workspace argument, no allocation."""
+    """es_matrix_scan_static_f32: matrix-scan whose chunked path (few long
+    lanes) runs in the library's own static device scratch of
+    STATIC_SCRATCH_BYTES, for callers that cannot allocate device memory.  A
+    scan that would need more scratch raises EsError (ES_E_UNSUPPORTED).
+    When ``out`` is None this wrapper allocates it with torch; a caller that
+    may not allocate passes ``out``."""
     import torch
     _require_cuda_f32(a, "a")
     _require_cuda_f32(b, "b")

@@ -17,7 +17,9 @@
 #include "es_matrix.h"
 
 // Scratch the library owns for es_matrix_scan_static_f32: module scope, so no
-// call allocates device memory.
+// call allocates device memory.  In host code this name stands for the array
+// but is no device address; the address comes from cudaGetSymbolAddress, once
+// per device, with that device current.
 static __device__ __align__(256) unsigned char g_es_static_scratch[ES_STATIC_SCRATCH_BYTES];
 
 namespace es {
@@ -534,13 +536,23 @@ es_status es_matrix_scan_static_f32(const float* a, const int64_t* a_shape, int 
     });
     if (sc.err != cudaSuccess)
         return es::api_fail(ES_E_CUDA, "es_matrix_scan_static_f32: scratch set-up: %s", cudaGetErrorString(sc.err));
+    // the chunked scan of this call must fit the library's array
+    size_t need = 0;
+    es_status st = es_matrix_scan_workspace_f32(a_shape, a_rank, b_shape, b_rank, axis, projective, &need);
+    if (st != ES_OK) return st;
+    if (need > ES_STATIC_SCRATCH_BYTES)
+        return es::api_fail(ES_E_UNSUPPORTED,
+                            "es_matrix_scan_static_f32: this scan needs %zu bytes of scratch, more than the %zu "
+                            "bytes (ES_STATIC_SCRATCH_BYTES) the library holds; call es_matrix_scan_ws_f32 with a "
+                            "workspace of es_matrix_scan_workspace_f32 bytes instead",
+                            need, static_cast<size_t>(ES_STATIC_SCRATCH_BYTES));
     std::lock_guard<std::mutex> lock(sc.mu);
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // the previous user of the scratch, on whatever stream, comes first
     if (sc.used && (e = cudaStreamWaitEvent(s, sc.released, 0)) != cudaSuccess)
         return es::api_fail(ES_E_CUDA, "es_matrix_scan_static_f32: %s", cudaGetErrorString(e));
-    es_status st = es_matrix_scan_ws_f32(a, a_shape, a_rank, b, b_shape, b_rank, axis, reverse, projective, out,
-                                         sc.ptr, ES_STATIC_SCRATCH_BYTES, stream);
+    st = es_matrix_scan_ws_f32(a, a_shape, a_rank, b, b_shape, b_rank, axis, reverse, projective, out, sc.ptr,
+                               ES_STATIC_SCRATCH_BYTES, stream);
     if (st != ES_OK) return st;
     if ((e = cudaEventRecord(sc.released, s)) != cudaSuccess)
         return es::api_fail(ES_E_CUDA, "es_matrix_scan_static_f32: %s", cudaGetErrorString(e));

@@ -10,20 +10,29 @@
 //   dx = mu,  da = mu * p (summed over the state for a width-one gate),
 //   lam <- a * mu.
 // Only (h . lam) sits on the serial chain: |y| and the gate gradient depend
-// on the saved states and inputs alone.  1/|y| comes from the hardware
-// reciprocal square root of |y|^2 (relative error below 2^-22) and is
-// multiplied in, the same value as the division up to rounding; sums over a
-// lane are pairwise within a thread, then xor-shuffles across the lane's W/E
-// threads, as in the forward vector kernel.
+// on the saved states, the inputs and mu alone.  1/|y| comes from the
+// hardware reciprocal square root of |y|^2 (relative error below 2^-22) and
+// is multiplied in, the same value as the division up to rounding; sums over
+// a lane are pairwise within a thread, then xor-shuffles across the lane's
+// W/E threads, as in the forward vector kernel.
 //
 // Layout as in the forward vector kernel (x, states, grad_out, grad_x are
-// [O, T, J*W]; the gate and its gradient [O, T, J*gw]); one CTA owns
-// LV = 128/W lanes of one o.  Per time tile of TT trips the producer streams
-// grad_out, x, the gate and TT+1 rows of saved states (the tile's outputs and
-// the state before its first trip in scan order, from a box that may start
-// at row -1 or end at row T, zero-filled there; `initial` replaces it).
-// Consumers prefetch each trip's operands one trip ahead from SMEM and hand
-// the stage back at the end of the tile.  Waits are bounded.
+// [O, T, J*W]; the gate and its gradient [O, T, J*gw]).  A CTA owns the
+// lanes of CW consumer warps (E values a thread, 32*CW*E values a trip row)
+// and its warps split the work of each time tile of TT trips:
+//   * the producer streams grad_out, x, the gate and TT+1 rows of saved
+//     states (the tile's outputs and the state before its first trip in scan
+//     order, from a box that may start at row -1 or end at row T, zero-filled
+//     there; `initial` replaces it) into a stage ring with TMA;
+//   * a helper warp per chain warp forms each trip's 1/|y| and cap flag ahead
+//     of the chain (written over the trip's x values in the stage), and after
+//     the chain the gate gradients sum(mu * p) (written over the gate);
+//   * the chain warps run the cotangent recurrence alone, reading each trip's
+//     operands one trip ahead and writing mu over the trip's grad_out;
+//   * a store warp sends the tile's grad_x and grad_gate out with two TMA
+//     tensor stores (rows past T and lanes past J are clipped by the tensor
+//     maps) and hands the stage back once they have read it.
+// The roles hand a stage on with mbarriers only.  Waits are bounded.
 #include <algorithm>
 
 #include "es_device.cuh"
@@ -32,8 +41,7 @@ namespace es {
 namespace {
 
 constexpr int kTT = 16;
-constexpr int kMaxStages = 8;
-constexpr int kRow = 128;        // values per CTA per trip
+constexpr int kMaxStages = 6;
 
 template <int E>
 __device__ __forceinline__ void ld_vec(float* d, const float* p) {
@@ -56,40 +64,53 @@ __device__ __forceinline__ void ld_vec(float* d, const float* p) {
 }
 
 template <int E>
-__device__ __forceinline__ void st_vec(float* p, const float* v) {
+__device__ __forceinline__ void put_vec(float* p, const float* v) {
     if constexpr (E % 4 == 0) {
 #pragma unroll
-        for (int i = 0; i < E; i += 4) __stcs(reinterpret_cast<float4*>(p + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+        for (int i = 0; i < E; i += 4)
+            *reinterpret_cast<float4*>(p + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
     } else if constexpr (E == 2) {
-        __stcs(reinterpret_cast<float2*>(p), make_float2(v[0], v[1]));
+        *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
     } else {
-        __stcs(p, v[0]);
+        p[0] = v[0];
     }
 }
 
-template <int W, int E, bool GW>
-__global__ void __launch_bounds__(32 + kRow / E)
+// shared-memory layout of one stage, in bytes
+template <int W, int E, bool GW, int CW>
+struct VbLayout {
+    static constexpr int R = 32 * CW * E;          // values of a trip row per CTA
+    static constexpr int LV = R / W;               // lanes per CTA
+    static constexpr int GW_ = GW ? W : 1;         // gate width
+    static constexpr uint32_t kSeq = kTT * R * 4;  // grad_out or x
+    static constexpr uint32_t kH = (kTT + 1) * R * 4;
+    static constexpr uint32_t kA = kTT * LV * GW_ * 4;
+    static constexpr uint32_t kOffX = kSeq;
+    static constexpr uint32_t kOffH = 2 * kSeq;
+    static constexpr uint32_t kOffA = (kOffH + kH + 1023u) & ~1023u;
+    static constexpr uint32_t kStage = (kOffA + kA + 1023u) & ~1023u;
+};
+
+template <int W, int E, bool GW, int CW>
+__global__ void __launch_bounds__(32 * (2 * CW + 2))
 k_vec_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_x,
           const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_h,
-          const float* __restrict__ init, float* __restrict__ ginit, float* __restrict__ gx, float* __restrict__ ga,
-          int T, int J, int tiles_j, int stages, int reverse, unsigned int* status, uint64_t wait_ns,
-          int64_t drop_tile) {
-    constexpr int LV = kRow / W;
-    constexpr int NC = kRow / E;
+          const __grid_constant__ CUtensorMap map_gx, const __grid_constant__ CUtensorMap map_ga,
+          const float* __restrict__ init, float* __restrict__ ginit, int T, int J, int tiles_j, int stages,
+          int reverse, unsigned int* status, uint64_t wait_ns, int64_t drop_tile) {
+    using Lay = VbLayout<W, E, GW, CW>;
+    constexpr int R = Lay::R;
+    constexpr int LV = Lay::LV;
+    constexpr int gw = Lay::GW_;
     constexpr int G = W / E;
     constexpr int GE = GW ? E : 1;
-    constexpr int gw = GW ? W : 1;
-    constexpr unsigned kMask = NC >= 32 ? 0xffffffffu : ((1u << NC) - 1u);
-    constexpr uint32_t kSeqBytes = kTT * kRow * 4;                 // grad_out or x
-    constexpr uint32_t kHBytes = (kTT + 1) * kRow * 4;             // states
-    constexpr uint32_t kABytes = kTT * LV * gw * 4;                // gate
-    constexpr uint32_t kOffX = kSeqBytes;
-    constexpr uint32_t kOffH = 2 * kSeqBytes;
-    constexpr uint32_t kOffA = (kOffH + kHBytes + 1023u) & ~1023u;
-    constexpr uint32_t kStageBytes = (kOffA + kABytes + 1023u) & ~1023u;
+    constexpr unsigned kMask = 0xffffffffu;
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
-    __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+    __shared__ __align__(8) uint64_t rn_bar[kMaxStages];    // helpers: the tile's 1/|y| are in place
+    __shared__ __align__(8) uint64_t mu_bar[kMaxStages];    // chain warps: the tile's mu are in place
+    __shared__ __align__(8) uint64_t done_bar[kMaxStages];  // helpers: the gate gradients are in place
+    __shared__ __align__(8) uint64_t empty_bar[kMaxStages]; // storer: the stores have read the stage
     __shared__ int abort_flag;
 
     unsigned char* base = smem_raw + smem_align_pad(smem_raw);
@@ -98,19 +119,25 @@ k_vec_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUt
     const int ntiles = (T + kTT - 1) / kTT;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const bool desc = !reverse;
+    const bool desc = !reverse;                      // the gradient runs the trips backwards
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], (NC + 31) / 32);
+            mbar_init(&rn_bar[s], CW);
+            mbar_init(&mu_bar[s], CW);
+            mbar_init(&done_bar[s], CW);
+            mbar_init(&empty_bar[s], 1);
         }
         abort_flag = 0;
         mbar_fence_init();
     }
     __syncthreads();
 
-    if (warp == 0) {
+    auto tile_t0 = [&](int k) { return (desc ? ntiles - 1 - k : k) * kTT; };
+
+    if (warp == 2 * CW) {
+        // producer
         if (lane == 0) {
             tma_prefetch_desc(&map_g);
             tma_prefetch_desc(&map_x);
@@ -127,13 +154,13 @@ k_vec_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUt
                 }
                 issued = k + 1;
                 if (k == drop_tile) continue;   // testing hook: this tile never arrives
-                const int t0 = (desc ? ntiles - 1 - k : k) * kTT;
-                unsigned char* st = base + static_cast<size_t>(s) * kStageBytes;
-                mbar_arrive_expect_tx(&full_bar[s], 2 * kSeqBytes + kHBytes + kABytes);
+                const int t0 = tile_t0(k);
+                unsigned char* st = base + static_cast<size_t>(s) * Lay::kStage;
+                mbar_arrive_expect_tx(&full_bar[s], 2 * Lay::kSeq + Lay::kH + Lay::kA);
                 tma_load_3d(st, &map_g, j0 * W, t0, o, &full_bar[s], pol);
-                tma_load_3d(st + kOffX, &map_x, j0 * W, t0, o, &full_bar[s], pol);
-                tma_load_3d(st + kOffH, &map_h, j0 * W, reverse ? t0 : t0 - 1, o, &full_bar[s], pol);
-                tma_load_3d(st + kOffA, &map_a, j0 * gw, t0, o, &full_bar[s], pol);
+                tma_load_3d(st + Lay::kOffX, &map_x, j0 * W, t0, o, &full_bar[s], pol);
+                tma_load_3d(st + Lay::kOffH, &map_h, j0 * W, reverse ? t0 : t0 - 1, o, &full_bar[s], pol);
+                tma_load_3d(st + Lay::kOffA, &map_a, j0 * gw, t0, o, &full_bar[s], pol);
             }
             for (int k = max(0, issued - stages); k < issued; ++k) {
                 if (k == drop_tile) continue;
@@ -143,23 +170,42 @@ k_vec_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUt
         }
         return;
     }
+    if (warp == 2 * CW + 1) {
+        // storer: grad_x from the grad_out rows, grad_gate from the gate rows
+        if (lane == 0) {
+            tma_prefetch_desc(&map_gx);
+            tma_prefetch_desc(&map_ga);
+            for (int k = 0; k < ntiles; ++k) {
+                const int s = k % stages;
+                if (!mbar_wait_bounded(&done_bar[s], (k / stages) & 1, wait_ns, &abort_flag)) {
+                    report_timeout(status, &abort_flag);
+                    break;
+                }
+                const int t0 = tile_t0(k);
+                unsigned char* st = base + static_cast<size_t>(s) * Lay::kStage;
+                tma_store_3d(&map_gx, j0 * W, t0, o, st);
+                tma_store_3d(&map_ga, j0 * gw, t0, o, st + Lay::kOffA);
+                bulk_commit();
+                bulk_wait_read<0>();
+                mbar_arrive(&empty_bar[s]);
+            }
+            bulk_wait_all();
+        }
+        return;
+    }
 
-    // consumers: thread c holds values w0 .. w0+E-1 of lane j0 + v
-    const int c = threadIdx.x - 32;
+    // chain warp w (< CW) and helper warp CW + w own the same lanes: thread c
+    // holds values w0 .. w0+E-1 of lane j0 + v
+    const bool helper = warp >= CW;
+    const int c = (helper ? warp - CW : warp) * 32 + lane;
     const int v = (c * E) / W;
     const int w0 = (c * E) % W;
     const bool valid = j0 + v < J;
-    const bool lead = (w0 == 0);                       // writes the lane's summed gate gradient
-    const int64_t row = static_cast<int64_t>(J) * W;
-    const int64_t grow = static_cast<int64_t>(J) * gw;
-    float p0[E], lam[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        p0[e] = valid ? init[(static_cast<int64_t>(o) * J + j0 + v) * W + w0 + e] : 0.0f;
-        lam[e] = 0.0f;
-    }
     const int t_first = reverse ? T - 1 : 0;
     const int gi = v * gw + (GW ? w0 : 0);
+    float p0[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) p0[e] = valid ? init[(static_cast<int64_t>(o) * J + j0 + v) * W + w0 + e] : 0.0f;
 
     auto lane_sum = [&](float s) {
 #pragma unroll
@@ -173,138 +219,167 @@ k_vec_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUt
             for (int e = 0; e + span < E; e += 2 * span) q[e] = __fadd_rn(q[e], q[e + span]);
         return q[0];
     };
-
-    for (int k = 0; k < ntiles; ++k) {
-        const int s = k % stages;
-        const bool ok = mbar_wait_bounded(&full_bar[s], (k / stages) & 1, wait_ns, &abort_flag);
-        if (!__all_sync(kMask, ok)) {
-            if (!ok) report_timeout(status, &abort_flag);
-            break;
+    struct Rows {
+        float* g;          // grad_out; mu replaces it
+        float* x;          // x; the signed 1/|y| replaces its first value
+        const float* h;    // states
+        float* a;          // gate; its gradient replaces it
+    };
+    auto rows = [&](int s) {
+        unsigned char* st = base + static_cast<size_t>(s) * Lay::kStage;
+        return Rows{reinterpret_cast<float*>(st) + c * E, reinterpret_cast<float*>(st + Lay::kOffX) + c * E,
+                    reinterpret_cast<const float*>(st + Lay::kOffH) + c * E,
+                    reinterpret_cast<float*>(st + Lay::kOffA) + gi};
+    };
+    // the state before trip tt of the tile starting at t0 (initial before the first trip)
+    auto before = [&](const Rows& rw, int t0, int tt, float* p) {
+        if (t0 + tt == t_first) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) p[e] = p0[e];
+        } else {
+            ld_vec<E>(p, rw.h + (reverse ? tt + 1 : tt) * R);
         }
-        const int t0 = (desc ? ntiles - 1 - k : k) * kTT;
-        const int n = min(kTT, T - t0);
-        const unsigned char* st = base + static_cast<size_t>(s) * kStageBytes;
-        const float* gs = reinterpret_cast<const float*>(st) + c * E;
-        const float* xs = reinterpret_cast<const float*>(st + kOffX) + c * E;
-        const float* hs = reinterpret_cast<const float*>(st + kOffH) + c * E;
-        const float* as = reinterpret_cast<const float*>(st + kOffA) + gi;
-        float* gxp = gx + static_cast<int64_t>(o) * T * row + static_cast<int64_t>(j0) * W + c * E;
-        float* gap = ga + static_cast<int64_t>(o) * T * grow + static_cast<int64_t>(j0) * gw + gi;
+    };
 
-        struct Ops {
-            float g[E], x[E], h[E], p[E], a[GE];
-        };
-        // operands of trip tt: its own state row and the row of the state before it
-        auto load = [&](const int tt, Ops& d) {
-            ld_vec<E>(d.g, gs + tt * kRow);
-            ld_vec<E>(d.x, xs + tt * kRow);
-            const int hr = reverse ? tt : tt + 1;
-            const int pr = reverse ? tt + 1 : tt;
-            ld_vec<E>(d.h, hs + hr * kRow);
-            ld_vec<E>(d.p, hs + pr * kRow);
-            if (t0 + tt == t_first) {
-#pragma unroll
-                for (int e = 0; e < E; ++e) d.p[e] = p0[e];
+    if (helper) {
+        // pass 1 of tile k: 1/|y| with its cap flag for every trip, the lane
+        // sums level by level over all trips so their shuffles overlap
+        auto norms = [&](int k) -> bool {
+            const int s = k % stages;
+            const bool ok = mbar_wait_bounded(&full_bar[s], (k / stages) & 1, wait_ns, &abort_flag);
+            if (!__all_sync(kMask, ok)) {
+                if (!ok) report_timeout(status, &abort_flag);
+                return false;
             }
-#pragma unroll
-            for (int e = 0; e < GE; ++e) d.a[e] = as[tt * LV * gw + e];
-        };
-        auto trip = [&](const int tt, const Ops& d) {
-            // off the chain: |y| from the saved state before the trip
-            float y[E], q[E];
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                y[e] = __fadd_rn(__fmul_rn(d.a[GW ? e : 0], d.p[e]), d.x[e]);
-                q[e] = __fmul_rn(y[e], y[e]);
-            }
-            const float ss = lane_sum(local_sum(q));
-            const bool capped = ss > 1.0f;
-            const float rn = rsqrt_approx(ss);
-            // the chain: lam -> (h . lam) -> mu -> a * mu
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                lam[e] = __fadd_rn(lam[e], d.g[e]);
-                q[e] = __fmul_rn(d.h[e], lam[e]);
-            }
-            const float hl = lane_sum(local_sum(q));
-            float mu[E], da[E];
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const float m = __fmul_rn(__fsub_rn(lam[e], __fmul_rn(d.h[e], hl)), rn);
-                mu[e] = capped ? m : lam[e];
-                da[e] = __fmul_rn(mu[e], d.p[e]);
-                lam[e] = __fmul_rn(d.a[GW ? e : 0], mu[e]);
-            }
-            if (valid) {
-                st_vec<E>(gxp + static_cast<int64_t>(t0 + tt) * row, mu);
-                if constexpr (GW) {
-                    st_vec<E>(gap + static_cast<int64_t>(t0 + tt) * grow, da);
-                }
-            }
-            if constexpr (!GW) {
-                const float dsum = lane_sum(local_sum(da));
-                if (valid && lead) __stcs(gap + static_cast<int64_t>(t0 + tt) * grow, dsum);
-            }
-        };
-        Ops A;
-        if (n == kTT) {
-            // Full tile in three passes so the serial chain runs alone:
-            // (1) every trip's 1/|y| and cap flag (they need only saved states
-            //     and inputs), (2) the cotangent chain, keeping each mu,
-            // (3) the gate gradients sum(mu * p) over each lane.  The lane
-            // sums of passes 1 and 3 go level by level over all trips of the
-            // tile, so their shuffles overlap instead of forming 16 chains.
-            float rn[kTT], ssl[kTT];
-            bool capped[kTT];
+            const int t0 = tile_t0(k);
+            const Rows rw = rows(s);
+            float ss[kTT];
 #pragma unroll
             for (int tt = 0; tt < kTT; ++tt) {
-                Ops d;
-                load(tt, d);
-                float q[E];
+                float p[E], x[E], a[GE], q[E];
+                before(rw, t0, tt, p);
+                ld_vec<E>(x, rw.x + tt * R);
+#pragma unroll
+                for (int e = 0; e < GE; ++e) a[e] = rw.a[tt * LV * gw + e];
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
-                    const float y = __fadd_rn(__fmul_rn(d.a[GW ? e : 0], d.p[e]), d.x[e]);
+                    const float y = __fadd_rn(__fmul_rn(a[GW ? e : 0], p[e]), x[e]);
                     q[e] = __fmul_rn(y, y);
                 }
-                ssl[tt] = local_sum(q);
+                ss[tt] = local_sum(q);
             }
 #pragma unroll
             for (int off = G / 2; off >= 1; off >>= 1)
 #pragma unroll
-                for (int tt = 0; tt < kTT; ++tt) ssl[tt] = __fadd_rn(ssl[tt], __shfl_xor_sync(kMask, ssl[tt], off));
+                for (int tt = 0; tt < kTT; ++tt) ss[tt] = __fadd_rn(ss[tt], __shfl_xor_sync(kMask, ss[tt], off));
+            // a positive value is 1/|y| of a capped trip; -1 marks |y| <= 1
+#pragma unroll
+            for (int tt = 0; tt < kTT; ++tt) rw.x[tt * R] = ss[tt] > 1.0f ? rsqrt_approx(ss[tt]) : -1.0f;
+            __syncwarp(kMask);
+            if (lane == 0) mbar_arrive(&rn_bar[s]);
+            return true;
+        };
+        // pass 3 of tile k: the gate gradients sum(mu * p), over the lane for
+        // a width-one gate, written over the gate
+        auto gate_grads = [&](int k) -> bool {
+            const int s = k % stages;
+            const bool ok = mbar_wait_bounded(&mu_bar[s], (k / stages) & 1, wait_ns, &abort_flag);
+            if (!__all_sync(kMask, ok)) {
+                if (!ok) report_timeout(status, &abort_flag);
+                return false;
+            }
+            const int t0 = tile_t0(k);
+            const Rows rw = rows(s);
+            float dl[kTT];
 #pragma unroll
             for (int tt = 0; tt < kTT; ++tt) {
-                capped[tt] = ssl[tt] > 1.0f;
-                rn[tt] = rsqrt_approx(ssl[tt]);
+                float mu[E], p[E], da[E];
+                ld_vec<E>(mu, rw.g + tt * R);
+                before(rw, t0, tt, p);
+#pragma unroll
+                for (int e = 0; e < E; ++e) da[e] = __fmul_rn(mu[e], p[e]);
+                if constexpr (GW) {
+                    put_vec<E>(rw.a + tt * LV * gw, da);
+                } else {
+                    dl[tt] = local_sum(da);
+                }
             }
-            float mus[kTT][E];
-            float gn[E], hn[E];            // the next trip's operands, read one trip ahead
-            auto fetch = [&](const int tt) {
-                ld_vec<E>(gn, gs + tt * kRow);
-                ld_vec<E>(hn, hs + (reverse ? tt : tt + 1) * kRow);
-            };
-            auto chain = [&](const int tt, const int next) {
-                float g[E], h[E], q[E];
+            if constexpr (!GW) {
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    g[e] = gn[e];
-                    h[e] = hn[e];
-                }
-                if (next >= 0) fetch(next);
+                for (int off = G / 2; off >= 1; off >>= 1)
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    lam[e] = __fadd_rn(lam[e], g[e]);
-                    q[e] = __fmul_rn(h[e], lam[e]);
-                }
-                const float hl = lane_sum(local_sum(q));
+                    for (int tt = 0; tt < kTT; ++tt) dl[tt] = __fadd_rn(dl[tt], __shfl_xor_sync(kMask, dl[tt], off));
+                if (w0 == 0) {
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float m = __fmul_rn(__fsub_rn(lam[e], __fmul_rn(h[e], hl)), rn[tt]);
-                    mus[tt][e] = capped[tt] ? m : lam[e];
-                    lam[e] = __fmul_rn(as[tt * LV * gw + (GW ? e : 0)], mus[tt][e]);
+                    for (int tt = 0; tt < kTT; ++tt) rw.a[tt * LV] = dl[tt];
                 }
-                if (valid) st_vec<E>(gxp + static_cast<int64_t>(t0 + tt) * row, mus[tt]);
-            };
+            }
+            fence_proxy_async_smem();
+            __syncwarp(kMask);
+            if (lane == 0) mbar_arrive(&done_bar[s]);
+            return true;
+        };
+        // the norms run one tile ahead of the chain, the gate gradients one behind
+        if (!norms(0)) return;
+        for (int k = 0; k < ntiles; ++k) {
+            if (k + 1 < ntiles && !norms(k + 1)) return;
+            if (!gate_grads(k)) return;
+        }
+        return;
+    }
+
+    // chain warp: lam -> (h . lam) -> mu -> a * mu, trip after trip
+    float lam[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) lam[e] = 0.0f;
+    for (int k = 0; k < ntiles; ++k) {
+        const int s = k % stages;
+        const bool ok = mbar_wait_bounded(&rn_bar[s], (k / stages) & 1, wait_ns, &abort_flag);
+        if (!__all_sync(kMask, ok)) {
+            if (!ok) report_timeout(status, &abort_flag);
+            break;
+        }
+        const int t0 = tile_t0(k);
+        const int n = min(kTT, T - t0);
+        const Rows rw = rows(s);
+        // the next trip's operands are read while a trip runs
+        float gn[E], hn[E], an[GE], rnn;
+        auto fetch = [&](const int tt) {
+            ld_vec<E>(gn, rw.g + tt * R);
+            ld_vec<E>(hn, rw.h + (reverse ? tt : tt + 1) * R);
+#pragma unroll
+            for (int e = 0; e < GE; ++e) an[e] = rw.a[tt * LV * gw + e];
+            rnn = rw.x[tt * R];
+        };
+        auto chain = [&](const int tt, const int next) {
+            float g[E], h[E], a[GE], q[E], mu[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                g[e] = gn[e];
+                h[e] = hn[e];
+            }
+#pragma unroll
+            for (int e = 0; e < GE; ++e) a[e] = an[e];
+            const float rn = rnn;
+            if (next >= 0) fetch(next);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                lam[e] = __fadd_rn(lam[e], g[e]);
+                q[e] = __fmul_rn(h[e], lam[e]);
+            }
+            const float hl = lane_sum(local_sum(q));
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const float m = __fmul_rn(__fsub_rn(lam[e], __fmul_rn(h[e], hl)), rn);
+                mu[e] = rn > 0.0f ? m : lam[e];
+                lam[e] = __fmul_rn(a[GW ? e : 0], mu[e]);
+            }
+            put_vec<E>(rw.g + tt * R, mu);
+        };
+        if (n == kTT) {
+            // full tile: one basic block, so consecutive trips overlap (with
+            // the whole tile's operands staged in registers instead, the
+            // burst of loads at each tile start measured slower)
             if (desc) {
                 fetch(kTT - 1);
 #pragma unroll
@@ -314,43 +389,16 @@ k_vec_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUt
 #pragma unroll
                 for (int tt = 0; tt < kTT; ++tt) chain(tt, tt + 1 < kTT ? tt + 1 : -1);
             }
-            float dl[kTT][GW ? E : 1];
-#pragma unroll
-            for (int tt = 0; tt < kTT; ++tt) {
-                Ops d;
-                load(tt, d);
-                float da[E];
-#pragma unroll
-                for (int e = 0; e < E; ++e) da[e] = __fmul_rn(mus[tt][e], d.p[e]);
-                if constexpr (GW) {
-                    if (valid) st_vec<E>(gap + static_cast<int64_t>(t0 + tt) * grow, da);
-                } else {
-                    dl[tt][0] = local_sum(da);
-                }
-            }
-            if constexpr (!GW) {
-#pragma unroll
-                for (int off = G / 2; off >= 1; off >>= 1)
-#pragma unroll
-                    for (int tt = 0; tt < kTT; ++tt)
-                        dl[tt][0] = __fadd_rn(dl[tt][0], __shfl_xor_sync(kMask, dl[tt][0], off));
-#pragma unroll
-                for (int tt = 0; tt < kTT; ++tt)
-                    if (valid && lead) __stcs(gap + static_cast<int64_t>(t0 + tt) * grow, dl[tt][0]);
-            }
         } else if (desc) {
-            for (int tt = n - 1; tt >= 0; --tt) {
-                load(tt, A);
-                trip(tt, A);
-            }
+            fetch(n - 1);
+            for (int tt = n - 1; tt >= 0; --tt) chain(tt, tt - 1);
         } else {
-            for (int tt = 0; tt < n; ++tt) {
-                load(tt, A);
-                trip(tt, A);
-            }
+            fetch(0);
+            for (int tt = 0; tt < n; ++tt) chain(tt, tt + 1 < n ? tt + 1 : -1);
         }
+        fence_proxy_async_smem();
         __syncwarp(kMask);
-        if (lane == 0) mbar_arrive(&empty_bar[s]);
+        if (lane == 0) mbar_arrive(&mu_bar[s]);
     }
     if (valid) {
 #pragma unroll
@@ -358,31 +406,39 @@ k_vec_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUt
     }
 }
 
-template <int W, int E, bool GW>
-cudaError_t launch_vb(const BackwardLaunch& B, const CUtensorMap* maps, int tiles_j, int stages) {
+// consumer warps per CTA: two where the row of lanes is wide enough
+int vb_consumer_warps(int W, int64_t J) {
+    const int E = W >= 4 ? 4 : W;
+    return J >= 2 * (32 * E / W) ? 2 : 1;
+}
+
+template <int W, int E, bool GW, int CW>
+cudaError_t launch_vb(const BackwardLaunch& B, const CUtensorMap* maps, int stages) {
+    using Lay = VbLayout<W, E, GW, CW>;
     const Launch& L = B.fwd;
-    constexpr int LV = kRow / W;
-    constexpr uint32_t kSeqBytes = kTT * kRow * 4;
-    constexpr uint32_t kHBytes = (kTT + 1) * kRow * 4;
-    constexpr uint32_t kABytes = kTT * LV * (GW ? W : 1) * 4;
-    constexpr uint32_t kOffA = (2 * kSeqBytes + kHBytes + 1023u) & ~1023u;
-    constexpr uint32_t kStageBytes = (kOffA + kABytes + 1023u) & ~1023u;
-    const size_t smem = static_cast<size_t>(stages) * kStageBytes + 1024;
-    auto kern = k_vec_bwd<W, E, GW>;
+    const int64_t tiles_j = (L.J + Lay::LV - 1) / Lay::LV;
+    const size_t smem = static_cast<size_t>(stages) * Lay::kStage + 1024;
+    auto kern = k_vec_bwd<W, E, GW, CW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int64_t grid = L.O * tiles_j;
-    kern<<<static_cast<unsigned>(grid), 32 + kRow / E, smem, L.stream>>>(
-        maps[0], maps[1], maps[2], maps[3], L.init, B.ginit, B.gx, B.ga, static_cast<int>(L.T), static_cast<int>(L.J),
-        tiles_j, stages, L.reverse, L.status, L.wait_ns, L.drop_tile);
+    kern<<<static_cast<unsigned>(grid), 32 * (2 * CW + 2), smem, L.stream>>>(
+        maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], L.init, B.ginit, static_cast<int>(L.T),
+        static_cast<int>(L.J), static_cast<int>(tiles_j), stages, L.reverse, L.status, L.wait_ns, L.drop_tile);
     return cudaGetLastError();
 }
 
-template <int W>
-cudaError_t launch_vb_w(const BackwardLaunch& B, const CUtensorMap* maps, int tiles_j, int stages) {
+template <int W, int CW>
+cudaError_t launch_vb_wc(const BackwardLaunch& B, const CUtensorMap* maps, int stages) {
     constexpr int E = W >= 4 ? 4 : W;
-    if (B.fwd.sw[1] == 1) return launch_vb<W, E, false>(B, maps, tiles_j, stages);
-    return launch_vb<W, E, true>(B, maps, tiles_j, stages);
+    if (B.fwd.sw[1] == 1) return launch_vb<W, E, false, CW>(B, maps, stages);
+    return launch_vb<W, E, true, CW>(B, maps, stages);
+}
+
+template <int W>
+cudaError_t launch_vb_w(const BackwardLaunch& B, const CUtensorMap* maps, int CW, int stages) {
+    if (CW == 2) return launch_vb_wc<W, 2>(B, maps, stages);
+    return launch_vb_wc<W, 1>(B, maps, stages);
 }
 
 bool encode_vb(const Launch& L, CUtensorMap* m, const float* base, int64_t row, int box_inner, int rows,
@@ -408,22 +464,35 @@ cudaError_t launch_vec_tma_bwd(const BackwardLaunch& B, const char** err) {
     const Launch& L = B.fwd;
     const int W = static_cast<int>(L.W);
     const int gw = static_cast<int>(L.sw[1]);
-    const int LV = kRow / W;
+    const int E = W >= 4 ? 4 : W;
+    const int CW = vb_consumer_warps(W, L.J);
+    const int R = 32 * CW * E;
+    const int LV = R / W;
     const int64_t tiles_j = (L.J + LV - 1) / LV;
-    // four stages of the four streams (about 100 KB): two CTAs per SM
-    const int stages = 4;
-    CUtensorMap maps[4];
-    if (!encode_vb(L, &maps[0], B.gout, L.J * W, kRow, kTT, err) ||
-        !encode_vb(L, &maps[1], L.x, L.J * W, kRow, kTT, err) ||
+    const int64_t ctas = L.O * tiles_j;
+    // a stage is held from its load through the norms, the chain and the
+    // gate gradients to its stores: four stages where one CTA a SM runs,
+    // fewer where more CTAs share a SM
+    const size_t seq = static_cast<size_t>(kTT) * R * 4;
+    const size_t stage_bytes = ((2 * seq + (kTT + 1) * R * 4 + 1023) & ~size_t(1023)) +
+                               ((static_cast<size_t>(kTT) * LV * gw * 4 + 1023) & ~size_t(1023));
+    const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>(8, (ctas + L.num_sms - 1) / L.num_sms));
+    const int stages = static_cast<int>(std::max<int64_t>(
+        3, std::min<int64_t>(std::min<int64_t>(4, kMaxStages),
+                             static_cast<int64_t>(210 * 1024 / per_sm) / static_cast<int64_t>(stage_bytes))));
+    CUtensorMap maps[6];
+    if (!encode_vb(L, &maps[0], B.gout, L.J * W, R, kTT, err) ||
+        !encode_vb(L, &maps[1], L.x, L.J * W, R, kTT, err) ||
         !encode_vb(L, &maps[2], L.a, L.J * gw, LV * gw, kTT, err) ||
-        !encode_vb(L, &maps[3], B.states, L.J * W, kRow, kTT + 1, err))
+        !encode_vb(L, &maps[3], B.states, L.J * W, R, kTT + 1, err) ||
+        !encode_vb(L, &maps[4], B.gx, L.J * W, R, kTT, err) ||
+        !encode_vb(L, &maps[5], B.ga, L.J * gw, LV * gw, kTT, err))
         return cudaErrorInvalidValue;
-    const int tj = static_cast<int>(tiles_j);
     switch (W) {
-        case 2: return launch_vb_w<2>(B, maps, tj, stages);
-        case 4: return launch_vb_w<4>(B, maps, tj, stages);
-        case 8: return launch_vb_w<8>(B, maps, tj, stages);
-        default: return launch_vb_w<16>(B, maps, tj, stages);
+        case 2: return launch_vb_w<2>(B, maps, CW, stages);
+        case 4: return launch_vb_w<4>(B, maps, CW, stages);
+        case 8: return launch_vb_w<8>(B, maps, CW, stages);
+        default: return launch_vb_w<16>(B, maps, CW, stages);
     }
 }
 

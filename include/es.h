@@ -441,15 +441,33 @@ es_status es_matrix_scan_ws_f32(const float *a, const int64_t *a_shape, int a_ra
                                 void *workspace, size_t workspace_bytes, es_stream_t stream);
 
 /*
- * es_matrix_scan_static_f32 -- es_matrix_scan_ws_f32 without a caller
- * workspace: the chunked scan runs in a scratch array the library owns (a
- * static device array of ES_STATIC_SCRATCH_BYTES per device, part of the
- * library's module, its address fetched once per device), so the call
- * allocates nothing and takes no workspace.  A call whose chunked scan would
- * need more runs lane by lane, exactly as es_matrix_scan_f32.  Successive
- * calls on one device are ordered through the scratch (each waits on an
- * event the previous one recorded), so calls on different streams do not
- * overlap in it.
+ * es_matrix_scan_static_f32 -- es_matrix_scan_ws_f32 for callers that cannot
+ * allocate device memory: code that runs where cudaMalloc is unavailable or
+ * not allowed (an allocator-free real-time or embedded host, a plug-in whose
+ * host application owns every allocation, a call made while a memory pool
+ * may not grow).  The pages have no counterpart: this is an interface choice
+ * of the library.  The chunked scan for few long lanes runs in a scratch array
+ * the library owns: a static device array of ES_STATIC_SCRATCH_BYTES, part of
+ * the library's module, so every GPU that has loaded it holds it until the
+ * process exits.  The call allocates nothing; the caller still passes a,
+ * b and out (device, as for es_matrix_scan_ws_f32).
+ *   set-up     the first call on a device, with that device current, loads
+ *              the module that holds the array (its device memory is taken
+ *              then), fetches the array's address (cudaGetSymbolAddress) and
+ *              creates one event; make that first call before any stream
+ *              capture.
+ *   limit      a scan whose chunked form needs more than
+ *              ES_STATIC_SCRATCH_BYTES (es_matrix_scan_workspace_f32) is
+ *              refused with ES_E_UNSUPPORTED and a message giving both sizes;
+ *              such a caller passes its own workspace to es_matrix_scan_ws_f32.
+ *              Scans that need no scratch (many lanes) run as
+ *              es_matrix_scan_f32.
+ *   sharing    every call uses the same array, which keeps the last call's
+ *              values; the scan writes every scratch value before reading
+ *              it, so nothing needs clearing.  Calls that overlapped on the
+ *              GPU would race in the array, so the library orders them: each
+ *              call's kernels wait on an event the previous call recorded,
+ *              whatever stream either was issued on.
  */
 #define ES_STATIC_SCRATCH_BYTES (32u << 20)
 es_status es_matrix_scan_static_f32(const float *a, const int64_t *a_shape, int a_rank,
