@@ -203,6 +203,13 @@ int64_t vec_stage_bytes(int W, int TT, int n_wide, int n_narrow) {
     return static_cast<int64_t>(TT) * (n_wide * 128LL * 4 + n_narrow * (128LL / W) * 4);
 }
 
+// bytes of one forward vector-state stage: the sequences' tiles, then the
+// tile of states the store warp sends out (as laid out by k_body_vec)
+int64_t vec_fwd_stage_bytes(int W, int TT, int n_wide, int n_narrow) {
+    const int64_t in = (vec_stage_bytes(W, TT, n_wide, n_narrow) + 127) & ~int64_t(127);
+    return (in + static_cast<int64_t>(TT) * 128 * 4 + 1023) & ~int64_t(1023);
+}
+
 // trips per vector-state tile: 32 unless a stage of every sequence would
 // pass 64 KB
 int vec_trips(int W, int n_wide, int n_narrow) {
@@ -361,15 +368,20 @@ bool launch_body_vec(const BodyLaunch& L, std::string* err) {
     int n_wide = 0;
     for (int q = 0; q < NS; ++q) n_wide += C.S.sw[q] == W ? 1 : 0;
     const int TT = vec_trips(W, n_wide, NS - n_wide);
-    const int64_t stage_bytes = vec_stage_bytes(W, TT, n_wide, NS - n_wide);
+    const int64_t stage_bytes = vec_fwd_stage_bytes(W, TT, n_wide, NS - n_wide);
     const int64_t tiles_j = (C.S.J + LV - 1) / LV;
     const int64_t ctas = C.S.O * tiles_j;
     int64_t per_sm = (ctas + L.dev->num_sms - 1) / L.dev->num_sms;
     per_sm = per_sm < 1 ? 1 : per_sm > 8 ? 8 : per_sm;
+    // a stage is held from its load through the chain to the store of its
+    // states: three or more where shared memory allows
     int64_t budget = (200 * 1024) / per_sm;
     if (budget > 160 * 1024) budget = 160 * 1024;
     int64_t st = budget / stage_bytes;
-    const int stages = static_cast<int>(st < 2 ? 2 : st > 8 ? 8 : st);
+    st = st < 3 ? 3 : st > 8 ? 8 : st;
+    const int64_t fit = (226 * 1024) / stage_bytes;
+    if (st > fit) st = fit < 2 ? 2 : fit;
+    const int stages = static_cast<int>(st);
     alignas(64) CUtensorMap maps[ES_MAX_SEQS];
     for (int q = 0; q < NS; ++q) {
         const bool wide = C.S.sw[q] == W;
@@ -386,19 +398,35 @@ bool launch_body_vec(const BodyLaunch& L, std::string* err) {
             return false;
         }
     }
+    alignas(64) CUtensorMap omap;
+    {
+        const int64_t row = C.S.J * W;
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(row), static_cast<cuuint64_t>(C.S.T),
+                                    static_cast<cuuint64_t>(C.S.O)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row) * 4, static_cast<cuuint64_t>(row) * C.S.T * 4};
+        const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(TT), 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (L.encode(&omap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, L.out, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            *err = "cuTensorMapEncodeTiled failed for the vector-state output map";
+            return false;
+        }
+    }
     JitKernel k;
     const KernelText kt = vec_text(C.functor, W, TT);
     if (!jit_kernel(kt.source, kt.name, &k, err)) return false;
     const float* init = L.init;
-    float* out = L.out;
     int T = static_cast<int>(C.S.T), J = static_cast<int>(C.S.J), tj = static_cast<int>(tiles_j);
     int stg = stages, reverse = C.reverse;
     unsigned int* status = L.dev->status;
     uint64_t wait_ns = api_wait_ns();
     int64_t drop = api_drop_tile();
-    void* args[] = {maps, &init, &out, &T, &J, &tj, &stg, &reverse, &status, &wait_ns, &drop};
+    void* args[] = {maps, &omap, &init, &T, &J, &tj, &stg, &reverse, &status, &wait_ns, &drop};
     const size_t smem = static_cast<size_t>(stages * stage_bytes) + 1024;
-    return jit_launch(k, static_cast<unsigned>(ctas), 32 + 128 / vec_values(W), smem, L.stream, args, err);
+    const int consumer_threads = 128 / vec_values(W);
+    return jit_launch(k, static_cast<unsigned>(ctas), 32 * ((consumer_threads + 31) / 32) + 64, smem, L.stream, args,
+                      err);
 }
 
 // ---------------------------------------------------------------------------

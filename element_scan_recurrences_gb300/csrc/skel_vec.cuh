@@ -4,16 +4,18 @@
 // Canonical view: the output and every full-width sequence are [O, T, J*W],
 // a width-one sequence is [O, T, J].  One CTA owns LV = 128 / W adjacent
 // lanes of one o (128 contiguous values per trip) and walks all T trips.
-// Warp 0's lane 0 streams time tiles of TT trips of every sequence (box
-// {128, TT} of a full-width sequence, {LV, TT} of a width-one one) into an
-// S-stage SMEM ring with TMA, each stage guarded by a full / empty mbarrier
-// pair.  Each of the 128 / E consumer threads holds E consecutive values of
-// one lane's state; a lane is G = W / E threads, and the body's reductions
-// combine them with xor shuffles.  A consumer reads a trip's operands from
-// SMEM one trip ahead of its use, runs the body, and stores its E values with
-// one vector store (a coalesced 512-byte row per trip and CTA); the stage goes
-// back to the producer after the tile.  Waits are bounded as in the other
-// pipelines.
+// Warp roles: the consumer warps first (one per scheduler), then a producer
+// and a store warp.  The producer streams time tiles of TT trips of every
+// sequence (box {128, TT} of a full-width sequence, {LV, TT} of a width-one
+// one) into an S-stage SMEM ring with TMA.  Each of the 128 / E consumer
+// threads holds E consecutive values of one lane's state; a lane is G = W / E
+// threads, and the body's reductions combine them with xor shuffles.  A
+// consumer reads a trip's operands from SMEM one trip ahead of its use, runs
+// the body, and writes its E values into the stage's tile of states; the
+// store warp sends each finished tile out with one TMA tensor store and hands
+// the stage back to the producer once the store has read it (full, done and
+// empty mbarriers; the consumers issue no global store).  Waits are bounded
+// as in the other pipelines.
 #pragma once
 
 #include "skel_common.cuh"
@@ -56,29 +58,48 @@ __device__ __forceinline__ void vec_store(float* p, const float (&v)[E]) {
     }
 }
 
+// E values into shared memory (16-byte pieces where E allows)
+template <int E>
+__device__ __forceinline__ void vec_put(float* p, const float (&v)[E]) {
+    if constexpr (E % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < E; i += 4)
+            *reinterpret_cast<float4*>(p + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    } else if constexpr (E == 2) {
+        *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+    } else {
+        p[0] = v[0];
+    }
+}
+
 template <class Body, int W, int E, int TT>
-__global__ void __launch_bounds__(32 + kVecRow / E)
-k_body_vec(const __grid_constant__ TmaMaps<Body::kNS> maps, const float* __restrict__ init, float* __restrict__ out,
-           int T, int J, int tiles_j, int stages, int reverse, unsigned int* status, uint64_t wait_ns,
-           int64_t drop_tile) {
+__global__ void __launch_bounds__(32 * ((kVecRow / E + 31) / 32) + 64)
+k_body_vec(const __grid_constant__ TmaMaps<Body::kNS> maps, const __grid_constant__ CUtensorMap map_out,
+           const float* __restrict__ init, int T, int J, int tiles_j, int stages, int reverse, unsigned int* status,
+           uint64_t wait_ns, int64_t drop_tile) {
     constexpr int NS = Body::kNS;
     constexpr unsigned kWide = Body::kWideMask;
     constexpr int LV = kVecRow / W;                // lanes per CTA
     constexpr int NC = kVecRow / E;                // consumer threads
+    constexpr int CWN = (NC + 31) / 32;            // consumer warps
     constexpr int G = W / E;                       // threads per lane
     constexpr unsigned kMask = NC >= 32 ? 0xffffffffu : ((1u << NC) - 1u);
     constexpr uint32_t kWideBytes = TT * kVecRow * 4u;
     constexpr uint32_t kNarrowBytes = TT * LV * 4u;   // a multiple of 128 bytes
-    // byte offset of sequence q's tile inside a stage, and the stage size
+    // byte offset of sequence q's tile inside a stage (the states' tile
+    // follows the sequences'), and the stage size
     auto tile_off = [](int q) -> uint32_t {
         uint32_t off = 0;
         for (int k = 0; k < q; ++k) off += is_wide(kWide, k) ? kWideBytes : kNarrowBytes;
         return off;
     };
-    const uint32_t stage_bytes = tile_off(NS);
+    const uint32_t in_bytes = tile_off(NS);
+    const uint32_t out_off = (in_bytes + 127u) & ~127u;
+    const uint32_t stage_bytes = (out_off + kWideBytes + 1023u) & ~1023u;
 
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kVecMaxStages];
+    __shared__ __align__(8) uint64_t done_bar[kVecMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kVecMaxStages];
     __shared__ int abort_flag;
     unsigned char* base = smem_raw + smem_align_pad(smem_raw);
@@ -92,14 +113,16 @@ k_body_vec(const __grid_constant__ TmaMaps<Body::kNS> maps, const float* __restr
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], (NC + 31) / 32);
+            mbar_init(&done_bar[s], CWN);
+            mbar_init(&empty_bar[s], 1);
         }
         abort_flag = 0;
         mbar_fence_init();
     }
     __syncthreads();
 
-    if (warp == 0) {
+    if (warp == CWN) {
+        // producer: time tiles of every sequence into the stage ring
         if (lane == 0) {
             for (int q = 0; q < NS; ++q) tma_prefetch_desc(&maps.m[q]);
             const uint64_t pol = l2_policy_stream();
@@ -115,7 +138,7 @@ k_body_vec(const __grid_constant__ TmaMaps<Body::kNS> maps, const float* __restr
                 if (k == drop_tile) continue;   // testing hook: this tile never arrives
                 const int j = reverse ? ntiles - 1 - k : k;
                 unsigned char* st = base + static_cast<size_t>(s) * stage_bytes;
-                mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
+                mbar_arrive_expect_tx(&full_bar[s], in_bytes);
 #pragma unroll
                 for (int q = 0; q < NS; ++q)
                     tma_load_3d(st + tile_off(q), &maps.m[q], is_wide(kWide, q) ? j0 * W : j0, j * TT, o,
@@ -129,18 +152,40 @@ k_body_vec(const __grid_constant__ TmaMaps<Body::kNS> maps, const float* __restr
         }
         return;
     }
+    if (warp == CWN + 1) {
+        // storer: each tile of states leaves shared memory as one TMA tensor
+        // store (rows past T and lanes past J clipped by the tensor map); the
+        // stage goes back to the producer once the store has read it
+        if (lane == 0) {
+            tma_prefetch_desc(&map_out);
+            for (int k = 0; k < ntiles; ++k) {
+                const int s = k % stages;
+                if (!mbar_wait_bounded(&done_bar[s], (k / stages) & 1, wait_ns, &abort_flag)) {
+                    report_timeout(status, &abort_flag);
+                    break;
+                }
+                const int j = reverse ? ntiles - 1 - k : k;
+                tma_store_3d(&map_out, j0 * W, j * TT, o, base + static_cast<size_t>(s) * stage_bytes + out_off);
+                bulk_commit();
+                bulk_wait_read<0>();
+                mbar_arrive(&empty_bar[s]);
+            }
+            bulk_wait_all();
+        }
+        return;
+    }
 
-    // consumers: thread c holds values w0 .. w0+E-1 of lane j0 + v
-    const int c = threadIdx.x - 32;
+    // consumers (the first warps, one per scheduler): thread c holds values
+    // w0 .. w0+E-1 of lane j0 + v
+    const int c = threadIdx.x;
+    if (c >= NC) return;
     const int v = (c * E) / W;
     const int w0 = (c * E) % W;
     const bool valid = j0 + v < J;
-    const int64_t row = static_cast<int64_t>(J) * W;
     float h[E];
 #pragma unroll
     for (int e = 0; e < E; ++e)   // a null `init`: from zero
         h[e] = valid && init != nullptr ? init[(static_cast<int64_t>(o) * J + j0 + v) * W + w0 + e] : 0.0f;
-    float* obase = out + static_cast<int64_t>(o) * T * row + static_cast<int64_t>(j0) * W + c * E;
 
     for (int k = 0; k < ntiles; ++k) {
         const int s = k % stages;
@@ -152,8 +197,8 @@ k_body_vec(const __grid_constant__ TmaMaps<Body::kNS> maps, const float* __restr
         const int j = reverse ? ntiles - 1 - k : k;
         const int t0 = j * TT;
         const int n = min(TT, T - t0);
-        const unsigned char* st = base + static_cast<size_t>(s) * stage_bytes;
-        float* op = obase + static_cast<int64_t>(t0) * row;
+        unsigned char* st = base + static_cast<size_t>(s) * stage_bytes;
+        float* op = reinterpret_cast<float*>(st + out_off) + c * E;
         auto load = [&](const int tt, float (&dw)[Body::kSW][E], float (&dn)[Body::kSN]) {
 #pragma unroll
             for (int q = 0; q < NS; ++q) {
@@ -173,7 +218,7 @@ k_body_vec(const __grid_constant__ TmaMaps<Body::kNS> maps, const float* __restr
         for (int e = 0; e < E; ++e) hr[0][e] = hr[1][e] = h[e];
         auto trip = [&](const int tt, const float (&dw)[Body::kSW][E], const float (&dn)[Body::kSN]) {
             Body::template step<E, G>(hr[tt & 1], hr[(tt & 1) ^ 1], dw, dn, kMask);
-            if (valid) vec_store<E>(op + static_cast<int64_t>(tt) * row, hr[tt & 1]);
+            vec_put<E>(op + tt * kVecRow, hr[tt & 1]);
         };
         // the next trip's operands are read while a trip runs; rows past the
         // valid trips of a ragged tile hold TMA's zero fill and are not used
@@ -200,8 +245,11 @@ k_body_vec(const __grid_constant__ TmaMaps<Body::kNS> maps, const float* __restr
         const int last = reverse ? 0 : n - 1;
 #pragma unroll
         for (int e = 0; e < E; ++e) h[e] = hr[last & 1][e];
+        // the tile's states are in shared memory: visible to the tensor
+        // store, then handed to the storer
+        fence_proxy_async_smem();
         __syncwarp(kMask);
-        if (lane == 0) mbar_arrive(&empty_bar[s]);
+        if (lane == 0) mbar_arrive(&done_bar[s]);
     }
 }
 
