@@ -330,7 +330,9 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
                         }
 #pragma unroll
                         for (int e = 0; e < E; ++e) h[e] = __fmul_rn(y[e], sc);
-                        Vec<E>::put(op + tt * R, h);
+                        // the state replaces this trip's x, no longer read
+#pragma unroll
+                        for (int e = 0; e < E; ++e) xr[tt][e] = h[e];
                         const float gn = gr[tn][0];
 #pragma unroll
                         for (int e = 0; e < E; ++e) y[e] = __fadd_rn(__fmul_rn(gn, h[e]), xr[tn][e]);
@@ -340,9 +342,14 @@ k_vec_tma(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUt
                     } else {
 #pragma unroll
                         for (int e = 0; e < E; ++e) h[e] = __fmul_rn(y[e], sc);
-                        Vec<E>::put(op + tt * R, h);
+#pragma unroll
+                        for (int e = 0; e < E; ++e) xr[tt][e] = h[e];
                     }
                 }
+                // the tile's states leave the registers in one burst, off the
+                // chain (shared-memory stores queue with the shuffles)
+#pragma unroll
+                for (int tt = 0; tt < kTT; ++tt) Vec<E>::put(op + tt * R, xr[tt]);
             };
             // full tiles run unguarded (one basic block, so consecutive trips
             // overlap); only the ragged last tile checks every trip
