@@ -385,7 +385,33 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
                              (is_h ? c : 0);
             const int64_t t = kChunk ? tbase + t0 + tt : t0 + tt;
             const bool live = !kChunk || (t >= 0 && t < T);
-            if constexpr (TRANS) {
+            if constexpr (kChunk && TRANS) {
+                // the chunked passes: row i of a^T h + b as one fused sum
+                // started from b (0 for a product column), j in order
+                float acc[RPT];
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) acc[r] = is_h ? B[(g * RPT + r) * m] : 0.0f;
+#pragma unroll
+                for (int j = 0; j < N; ++j) {
+                    float seg[RPT];
+                    smem_seg<RPT>(A + j * N + g * RPT, seg);
+#pragma unroll
+                    for (int r = 0; r < RPT; ++r) acc[r] = __fmaf_rn(seg[r], h[j], acc[r]);
+                }
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) mine[r] = acc[r];
+            } else if constexpr (kChunk) {
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    const int i = r * R + g;
+                    float row[N];
+                    smem_row<N>(A, i, row);
+                    float acc = is_h ? B[i * m] : 0.0f;
+#pragma unroll
+                    for (int j = 0; j < N; ++j) acc = __fmaf_rn(row[j], h[j], acc);
+                    mine[r] = acc;
+                }
+            } else if constexpr (TRANS) {
                 // row i of a^T h is sum_j a[j][i] h[j]: over j in order, this
                 // thread's contiguous rows i = g*RPT + r take the segment
                 // a[j][g*RPT ..] of row j (vector loads) times h[j], the
@@ -439,8 +465,12 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
             // state (the same for the whole lane group)
 #pragma unroll
             for (int i = 0; i < N; ++i) {
-                const float v = TRANS ? __shfl_sync(0xffffffffu, mine[i % RPT], col_base + (i / RPT) * gp)
-                                      : __shfl_sync(0xffffffffu, mine[i / R], col_base + (i % R) * gp);
+                float v;
+                if constexpr (R == 1)
+                    v = mine[i];    // the thread holds its whole column
+                else
+                    v = TRANS ? __shfl_sync(0xffffffffu, mine[i % RPT], col_base + (i / RPT) * gp)
+                              : __shfl_sync(0xffffffffu, mine[i / R], col_base + (i % R) * gp);
                 h[i] = live ? v : h[i];
             }
         };
@@ -885,6 +915,23 @@ __device__ __forceinline__ void lane_offsets(const MatGeom& g, int64_t lane, int
     }
 }
 
+// one step of a chunked pass for one column: hn[i] = sum_j a[i][j] h[j]
+// + b[i] as one fused sum started from b[i] (0 without b), j in order: the
+// arithmetic of the TMA kernel's chunk modes.  hn may alias h.
+template <int N>
+__device__ __forceinline__ void chunk_step(float (&hn)[N], const float (&h)[N], const float* A, const float* B,
+                                           int m) {
+    float acc[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        acc[i] = B != nullptr ? __ldg(B + i * m) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < N; ++j) acc[i] = __fmaf_rn(__ldg(A + i * N + j), h[j], acc[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i) hn[i] = acc[i];
+}
+
 template <int N>
 __global__ void __launch_bounds__(128)
 k_mat_chunk_local(const float* __restrict__ a, const float* __restrict__ b, float* __restrict__ ws, const MatGeom g,
@@ -905,16 +952,9 @@ k_mat_chunk_local(const float* __restrict__ a, const float* __restrict__ b, floa
     for (int64_t q = 0; q < ct.count; ++q) {
         const int64_t t = ct.first + q * ct.step;
         const float* A = a + (oa + t * g.ta) * N * N;
+        const float* B = b + (ob + t * g.tb) * N * m + c;
         float hn[N];
-        column_step<N>(hn, h, [&](int i, float (&r)[N]) {
-#pragma unroll
-            for (int j = 0; j < N; ++j) r[j] = __ldg(A + i * N + j);
-        });
-        if (is_h) {
-            const float* B = b + (ob + t * g.tb) * N * m + c;
-#pragma unroll
-            for (int i = 0; i < N; ++i) hn[i] = __fadd_rn(hn[i], __ldg(B + i * m));
-        }
+        chunk_step<N>(hn, h, A, is_h ? B : nullptr, m);
 #pragma unroll
         for (int i = 0; i < N; ++i) h[i] = hn[i];
     }
@@ -973,18 +1013,11 @@ k_mat_chunk_final(const float* __restrict__ a, const float* __restrict__ b, cons
     for (int64_t q = 0; q < ct.count; ++q) {
         const int64_t t = ct.first + q * ct.step;
         const float* A = a + (oa + t * g.ta) * N * N;
-        float hn[N];
-        column_step<N>(hn, h, [&](int i, float (&r)[N]) {
-#pragma unroll
-            for (int j = 0; j < N; ++j) r[j] = __ldg(A + i * N + j);
-        });
         const float* B = b + (ob + t * g.tb) * N * m + c;
         float* O = out + (oo + t * g.to) * N * m + c;
+        chunk_step<N>(h, h, A, B, m);
 #pragma unroll
-        for (int i = 0; i < N; ++i) {
-            h[i] = __fadd_rn(hn[i], __ldg(B + i * m));
-            __stcs(O + i * m, h[i]);
-        }
+        for (int i = 0; i < N; ++i) __stcs(O + i * m, h[i]);
     }
 }
 
