@@ -89,6 +89,17 @@ __device__ __forceinline__ void mul2_rn(float& p0, float& p1, float a0, float a1
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// two IEEE fused multiply-adds in one packed instruction (sm_100 and
+// later): (d0, d1) = (a0 * b0 + c0, a1 * b1 + c1), each rounded once, so the
+// result is that of two __fmaf_rn
+__device__ __forceinline__ void fma2_rn(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                        float c1) {
+    asm("{\n\t.reg .b64 x, y, z, w;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+        "mov.b64 z, {%6, %7};\n\tfma.rn.f32x2 w, x, y, z;\n\tmov.b64 {%0, %1}, w;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 // K consecutive floats of shared memory (16-byte aligned when K % 4 == 0,
 // 8-byte when K % 2 == 0)
 template <int K>
@@ -387,7 +398,8 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
             const bool live = !kChunk || (t >= 0 && t < T);
             if constexpr (kChunk && TRANS) {
                 // the chunked passes: row i of a^T h + b as one fused sum
-                // started from b (0 for a product column), j in order
+                // started from b (0 for a product column), j in order; two
+                // rows a packed instruction
                 float acc[RPT];
 #pragma unroll
                 for (int r = 0; r < RPT; ++r) acc[r] = is_h ? B[(g * RPT + r) * m] : 0.0f;
@@ -396,20 +408,26 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
                     float seg[RPT];
                     smem_seg<RPT>(A + j * N + g * RPT, seg);
 #pragma unroll
-                    for (int r = 0; r < RPT; ++r) acc[r] = __fmaf_rn(seg[r], h[j], acc[r]);
+                    for (int r = 0; r + 1 < RPT; r += 2)
+                        fma2_rn(acc[r], acc[r + 1], seg[r], seg[r + 1], h[j], h[j], acc[r], acc[r + 1]);
+                    if constexpr (RPT % 2 == 1) acc[RPT - 1] = __fmaf_rn(seg[RPT - 1], h[j], acc[RPT - 1]);
                 }
 #pragma unroll
                 for (int r = 0; r < RPT; ++r) mine[r] = acc[r];
             } else if constexpr (kChunk) {
+                // the chunked passes: row i of a h + b as two fused partial
+                // sums over the even and the odd j (the even one started
+                // from b, 0 for a product column), j in order within each,
+                // one packed instruction a pair of j, then their sum
 #pragma unroll
                 for (int r = 0; r < RPT; ++r) {
                     const int i = r * R + g;
                     float row[N];
                     smem_row<N>(A, i, row);
-                    float acc = is_h ? B[i * m] : 0.0f;
+                    float p0 = is_h ? B[i * m] : 0.0f, p1 = 0.0f;
 #pragma unroll
-                    for (int j = 0; j < N; ++j) acc = __fmaf_rn(row[j], h[j], acc);
-                    mine[r] = acc;
+                    for (int j = 0; j < N; j += 2) fma2_rn(p0, p1, row[j], row[j + 1], h[j], h[j + 1], p0, p1);
+                    mine[r] = __fadd_rn(p0, p1);
                 }
             } else if constexpr (TRANS) {
                 // row i of a^T h is sum_j a[j][i] h[j]: over j in order, this
@@ -916,17 +934,24 @@ __device__ __forceinline__ void lane_offsets(const MatGeom& g, int64_t lane, int
 }
 
 // one step of a chunked pass for one column: hn[i] = sum_j a[i][j] h[j]
-// + b[i] as one fused sum started from b[i] (0 without b), j in order: the
-// arithmetic of the TMA kernel's chunk modes.  hn may alias h.
+// + b[i] as two fused partial sums over the even and the odd j (the even
+// one started from b[i], 0 without b), j in order within each, then their
+// sum; an odd N's last term joins the even sum.  The arithmetic of the TMA
+// kernel's chunk modes.  hn may alias h.
 template <int N>
 __device__ __forceinline__ void chunk_step(float (&hn)[N], const float (&h)[N], const float* A, const float* B,
                                            int m) {
     float acc[N];
 #pragma unroll
     for (int i = 0; i < N; ++i) {
-        acc[i] = B != nullptr ? __ldg(B + i * m) : 0.0f;
+        float p0 = B != nullptr ? __ldg(B + i * m) : 0.0f, p1 = 0.0f;
 #pragma unroll
-        for (int j = 0; j < N; ++j) acc[i] = __fmaf_rn(__ldg(A + i * N + j), h[j], acc[i]);
+        for (int j = 0; j + 1 < N; j += 2) {
+            p0 = __fmaf_rn(__ldg(A + i * N + j), h[j], p0);
+            p1 = __fmaf_rn(__ldg(A + i * N + j + 1), h[j + 1], p1);
+        }
+        if constexpr (N % 2 == 1) p0 = __fmaf_rn(__ldg(A + i * N + N - 1), h[N - 1], p0);
+        acc[i] = N == 1 ? p0 : __fadd_rn(p0, p1);
     }
 #pragma unroll
     for (int i = 0; i < N; ++i) hn[i] = acc[i];
