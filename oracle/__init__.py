@@ -266,6 +266,16 @@ def _run_blocks(jobs, threads: int):
             f.result()
 
 
+def split_rows(fn, n_rows: int, threads: int = 0) -> int:
+    """Call fn(lo, hi) on contiguous blocks of rows [0, n_rows), one thread a
+    block (`host_threads()` blocks by default); for running any of the oracles
+    on independent lanes at once.  Returns the number of blocks."""
+    threads = threads or host_threads()
+    blocks = _lane_blocks(n_rows, threads)
+    _run_blocks([lambda lo=lo, hi=hi: fn(lo, hi) for lo, hi in blocks], threads)
+    return len(blocks)
+
+
 def scan_threads(body, initial, seqs, axis: int = 0, state_axis: bool = False, reverse: bool = False,
                  threads: int = 0) -> np.ndarray:
     """`scan` on every host core (f32): the lanes are split along dim 0 into

@@ -177,53 +177,38 @@ def test_body_misaligned_falls_back_to_generic():
     compare(got.cpu().numpy(), scan_body(c[1], initial, seqs, axis=1), True, "misaligned")
 
 
-def _sampled_lanes(w, init, seqs, out, reverse, n_lanes=48, seed=1):
-    """Oracle on sampled lanes of a full-size run: the lanes are independent,
-    so the sampled lanes gathered into one batch scan to the same states."""
-    rng = np.random.default_rng(seed)
-    ax = w.ax
-    W = w.shape[-1] if w.state_axis else 1
-    O = int(np.prod(w.shape[:ax]))
-    T = w.T
-    J = int(np.prod(w.shape[ax + 1:])) // W
-    widths = list(w.seq_widths) if w.state_axis else [1] * len(seqs)
-    views = [t.reshape(O, T, J, wd) for t, wd in zip(seqs, widths)]
-    ov = out.reshape(O, T, J, W)
-    iv = init.reshape(O, J, W)
-    lanes = [(0, 0), (O - 1, J - 1)] + [(int(rng.integers(O)), int(rng.integers(J))) for _ in range(n_lanes - 2)]
-    oi = torch.tensor([l[0] for l in lanes], device=out.device)
-    ji = torch.tensor([l[1] for l in lanes], device=out.device)
-    # [n, T, w] -> [1, T, n, w]
-    g = lambda v: v[oi, :, ji, :].permute(1, 0, 2).unsqueeze(0).contiguous().cpu().numpy()
-    s_seqs = [g(v) for v in views]
-    s_init = iv[oi, ji, :].unsqueeze(0).contiguous().cpu().numpy()
-    got = g(ov)
-    if not w.state_axis:
-        s_seqs = [s[..., 0] for s in s_seqs]
-        s_init = s_init[..., 0]
-        got = got[..., 0]
-    want = scan_body(w.text, s_init, s_seqs, axis=1, state_axis=w.state_axis, reverse=reverse)
-    return got, want
-
-
 @pytest.mark.parametrize("name", ["body_tanh_decay_lanes", "body_gated_lanes", "body_normcap_vector",
                                   "body_maxplus_reverse", "body_tanh_decay_time_inner"])
-def test_body_full_size_sampled(name):
-    """The body workloads at full size in the bench's launch configuration,
-    checked on sampled lanes (always the first and the last) against the
-    oracle, plus the bound every state of the body obeys."""
+def test_body_full_size_every_element(name):
+    """The body workloads at full size in the bench's launch configuration:
+    every output value (each direction the workload names) against the
+    body-program oracle run on every host core (lanes split into contiguous
+    blocks of rows), bit for bit for the IEEE-exact max-plus body and within
+    1e-5 * (1 + |oracle|) otherwise, plus the bound every state of the body
+    obeys."""
+    import oracle
     from element_scan_recurrences_gb300 import workloads as wl
+    from parity_helpers import compare_blocks
     w = wl.WORKLOADS[name]
     init, seqs = wl.make_inputs(w, "cuda")
     body = es.Body(w.text)
     exact = name == "body_maxplus_reverse"
+    init_h, seqs_h = init.cpu().numpy(), [s.cpu().numpy() for s in seqs]
     for reverse in w.reverse:
         out = body.scan(init, seqs, axis=w.axis, state_axis=w.state_axis, reverse=reverse)
         es.device_status()
-        got, want = _sampled_lanes(w, init, seqs, out, reverse)
-        compare(got, want, exact, "%s reverse=%s" % (name, reverse))
+        want = np.empty(tuple(out.shape), np.float32)
+
+        def rows(lo, hi):
+            want[lo:hi] = scan_body(w.text, init_h[lo:hi], [s[lo:hi] for s in seqs_h], axis=w.axis,
+                                    state_axis=w.state_axis, reverse=reverse)
+        oracle.split_rows(rows, w.shape[0])
+        compare_blocks(wl.MAXPLUS if exact else wl.TANH_DECAY, out.cpu().numpy(), want,
+                       "%s reverse=%s, every element" % (name, reverse), exact=exact)
+        del want
         if "tanh" in name or "gated" in name:
             assert float(out.abs().max()) <= 1.0
         if "normcap" in name:
             assert float(out.square().sum(-1).sqrt().max()) <= 1.0 + 1e-6
         del out
+    es.device_status()

@@ -151,9 +151,11 @@ def test_linear_scan_paths():
 
 
 @pytest.mark.parametrize("name", ["matrix_scan_delta_rule", "linear_scan_lanes"])
-def test_full_size_sampled(name):
+def test_full_size_every_element(name):
     """The bench workloads at full size in the bench's launch configuration,
-    checked bit for bit on sampled lanes (the first and the last included)."""
+    every state against the oracle (run on every host core over contiguous
+    blocks of rows), bit for bit."""
+    import oracle
     from element_scan_recurrences_gb300 import workloads as wl
     w = wl.MATRIX_WORKLOADS[name]
     a, b = wl.make_matrix_inputs(w, "cuda")
@@ -162,19 +164,19 @@ def test_full_size_sampled(name):
     else:
         out = es.matrix_scan(a, b, axis=w.axis)
     es.device_status()
-    rng = np.random.default_rng(2)
-    B, T, J = w.lead
-    lanes = [(0, 0), (B - 1, J - 1)] + [(int(rng.integers(B)), int(rng.integers(J))) for _ in range(30)]
-    bi = torch.tensor([l[0] for l in lanes], device="cuda")
-    ji = torch.tensor([l[1] for l in lanes], device="cuda")
-    # [lanes, T, ...] -> [T, lanes, ...], scanned along axis 0
-    take = lambda t: t[bi, :, ji].transpose(0, 1).contiguous().cpu().numpy()
-    sa, sb, got = take(a), take(b), take(out)
-    if w.kind == "linear":
-        want = M.linear_scan(sa, sb, axis=0)
-    else:
-        want = M.matrix_scan(sa, sb, axis=0)
-    bitwise(got, want, name)
+    ah, bh = a.cpu().numpy(), b.cpu().numpy()
+    del a, b
+    want = np.empty(tuple(out.shape), np.float32)
+
+    def rows(lo, hi):
+        if w.kind == "linear":
+            want[lo:hi] = M.linear_scan(ah[lo:hi], bh[lo:hi], axis=w.axis)
+        else:
+            want[lo:hi] = M.matrix_scan(ah[lo:hi], bh[lo:hi], axis=w.axis)
+    oracle.split_rows(rows, w.lead[0])
+    got = out.cpu().numpy()
+    for lo in range(0, w.lead[0], 8):
+        bitwise(got[lo:lo + 8], want[lo:lo + 8], "%s rows %d.." % (name, lo))
 
 
 def close(got, want, what, tol=1e-5):
@@ -277,15 +279,23 @@ def test_chunked_fallbacks_and_broadcast():
     es.device_status()
 
 
-def test_chunked_full_size_sampled():
-    """The few-lanes bench workload at full size: sampled lanes checked by the
-    oracle on whole sequences (tolerance), the bench's launch configuration."""
+def test_chunked_full_size_every_lane():
+    """The few-lanes bench workload at full size in the bench's launch
+    configuration: every lane's whole sequence of states against the oracle
+    (run on every host core, one lane a thread), within tolerance."""
+    import oracle
     from element_scan_recurrences_gb300 import workloads as wl
     w = wl.MATRIX_WORKLOADS["matrix_scan_few_lanes"]
     a, b = wl.make_matrix_inputs(w, "cuda")
     ws = torch.empty(es.matrix_scan_workspace(w.a_shape, w.b_shape, w.axis), dtype=torch.uint8, device="cuda")
     out = es.matrix_scan_ws(a, b, ws, axis=w.axis)
     es.device_status()
-    for lane in (0, w.lead[0] - 1):
-        sa, sb = a[lane].cpu().numpy(), b[lane].cpu().numpy()
-        close(out[lane].cpu().numpy(), M.matrix_scan(sa, sb, axis=0), "lane %d" % lane)
+    ah, bh = a.cpu().numpy(), b.cpu().numpy()
+    want = np.empty(tuple(out.shape), np.float32)
+
+    def rows(lo, hi):
+        want[lo:hi] = M.matrix_scan(ah[lo:hi], bh[lo:hi], axis=w.axis)
+    oracle.split_rows(rows, w.lead[0])
+    got = out.cpu().numpy()
+    for lane in range(w.lead[0]):
+        close(got[lane], want[lane], "lane %d" % lane)

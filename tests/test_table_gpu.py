@@ -87,15 +87,20 @@ def test_clamping_on_every_path():
     assert got.min() >= 0 and got.max() < states
 
 
-def test_full_size_sampled():
-    """The bench workload at full size, bit for bit on sampled rows."""
+@pytest.mark.parametrize("name", ["table_scan_time_inner", "table_scan_lanes"])
+def test_full_size_every_element(name):
+    """The bench workloads at full size, every state against the oracle (run
+    on every host core over contiguous blocks of rows), bit for bit."""
+    import oracle
     from element_scan_recurrences_gb300 import workloads as wl
-    w = wl.TABLE_WORKLOADS["table_scan_time_inner"]
+    w = wl.TABLE_WORKLOADS[name]
     table, sym = wl.make_table_inputs(w, "cuda")
     out = es.table_scan(table, sym, axis=w.axis)
     es.device_status()
-    rng = np.random.default_rng(3)
-    rows = np.concatenate([[0, w.shape[0] - 1], rng.integers(0, w.shape[0], 62)])
-    r = torch.from_numpy(rows).cuda()
-    want = TS.table_scan(table.cpu().numpy(), sym[r].cpu().numpy(), axis=-1)
-    assert np.array_equal(out[r].cpu().numpy(), want)
+    th, sh = table.cpu().numpy(), sym.cpu().numpy()
+    want = np.empty(tuple(out.shape), np.int32)
+
+    def rows(lo, hi):
+        want[lo:hi] = TS.table_scan(th, sh[lo:hi], axis=w.axis)
+    oracle.split_rows(rows, w.shape[0])
+    assert np.array_equal(out.cpu().numpy(), want)
