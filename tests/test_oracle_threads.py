@@ -72,3 +72,27 @@ def test_threaded_oracle_rejects_what_the_oracle_rejects():
 
 def test_host_threads_is_positive():
     assert oracle.host_threads() >= 1
+
+
+def test_split_rows_runs_each_block_once():
+    for n, t in ((1, 4), (10, 3), (64, 16), (5, 64)):
+        seen = []
+        used = oracle.split_rows(lambda lo, hi: seen.append((lo, hi)), n, t)
+        seen.sort()
+        assert used == len(seen) == min(n, t)
+        assert seen[0][0] == 0 and seen[-1][1] == n and all(a[1] == b[0] for a, b in zip(seen, seen[1:]))
+
+
+def test_body_oracle_on_row_blocks_is_bit_identical():
+    """The body-program oracle run over row blocks in threads (as the GPU
+    tests run it at full size) gives the whole-array result bit for bit."""
+    from oracle.body import scan_body
+    text = "(lambda (h x a) (tanh (+ x (* a h))))"
+    init, (x, a) = _inputs(oracle.TANH_DECAY, (9, 21, 6), 1, False, None, 8)
+    whole = scan_body(text, init, [x, a], axis=1)
+    out = np.empty_like(whole)
+
+    def rows(lo, hi):
+        out[lo:hi] = scan_body(text, init[lo:hi], [x[lo:hi], a[lo:hi]], axis=1)
+    oracle.split_rows(rows, 9, 4)
+    assert np.array_equal(out.view(np.uint32), whole.view(np.uint32))
