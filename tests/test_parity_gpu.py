@@ -42,6 +42,9 @@ SMALL = [
     ("lane_tma", wl.custom(M_, (2, 37, 96), 1, name="maxplus_lane", **MAXPLUS_DISTS)),
     ("lane_tma", wl.custom(M_, (5, 64, 1000), 1, name="maxplus_lane_wide", **MAXPLUS_DISTS)),
     ("lane_tma", wl.custom(T_, (300, 40), 0, name="tanh_lane_axis0")),
+    # enough lanes for 256-lane tiles: a ragged last lane tile (1000 = 3 x 256 + 232) and trip tile
+    ("lane_tma", wl.custom(T_, (40, 70, 1000), 1, name="tanh_lane_256")),
+    ("lane_tma", wl.custom(M_, (40, 70, 1000), 1, name="maxplus_lane_256", **MAXPLUS_DISTS)),
     ("lane_tma", wl.custom(T_, (4, 33, 8, 16), 1, state_axis=True, seq_widths=(16, 16), name="tanh_vec_full")),
     # time innermost, transposed through SMEM
     ("time_tma", wl.custom(T_, (300, 100), -1, name="tanh_time")),
