@@ -16,29 +16,44 @@
 // rows of saved states: the tile's own outputs plus the state before its
 // first trip in scan order (a TMA box that may start at row -1 or end at row
 // T; TMA fills those rows with zeros and the consumer takes `initial` there).
-// Consumers copy the tile to registers, free the stage, then run the chain
-// and store dx and da with one coalesced row store each per trip.  Waits are
-// bounded as in the forward kernels.
+// Consumers copy the tile to registers, free the stage, then run the chain.
+// Gradients go either straight to global memory (one coalesced row store of
+// dx and da per trip and warp) or, staged, into a shared-memory tile that one
+// thread sends out with two TMA tensor stores after a consumer barrier (two
+// tiles alternate; the stores also clip ragged lane and time tiles).  Waits
+// are bounded as in the forward kernels.
 #include <algorithm>
 
 #include "es_device.cuh"
 
+// Tuning overrides (0, or -1 for the flag: chosen per shape in
+// launch_lane_tma_bwd).
+#ifndef ES_LANE_BWD_TT
+#define ES_LANE_BWD_TT 0        // trips per tile: 16 or 32
+#endif
+#ifndef ES_LANE_BWD_STAGES
+#define ES_LANE_BWD_STAGES 0    // pipeline depth
+#endif
+#ifndef ES_LANE_BWD_STAGED
+#define ES_LANE_BWD_STAGED -1   // 1: gradients staged for TMA stores, 0: direct row stores
+#endif
+
 namespace es {
 namespace {
 
-constexpr int kTT = 16;          // trips per time tile
 constexpr int kMaxStages = 8;
 
-template <int BODY, int LI>
+template <int BODY, int LI, int TT, bool kStaged>
 __global__ void __launch_bounds__(32 + LI)
 k_lane_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_h,
            const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_x,
+           const __grid_constant__ CUtensorMap map_gx, const __grid_constant__ CUtensorMap map_ga,
            const float* __restrict__ init, float* __restrict__ ginit, float* __restrict__ gx,
            float* __restrict__ ga, int T, int I, int tiles_i, int stages, int reverse, unsigned int* status,
            uint64_t wait_ns, int64_t drop_tile) {
     constexpr bool kNeedX = BODY == ES_BODY_MAXPLUS;
-    constexpr int kRows = kTT + 1;                       // state rows per tile
-    constexpr int kTile = kTT * LI;                      // floats of one per-trip stream
+    constexpr int kRows = TT + 1;                        // state rows per tile
+    constexpr int kTile = TT * LI;                       // floats of one per-trip stream
     constexpr int kStageFloats = (kNeedX ? 3 : 2) * kTile + kRows * LI;
     constexpr uint32_t kStageBytes = kStageFloats * 4u;
     extern __shared__ unsigned char smem_raw[];
@@ -47,9 +62,10 @@ k_lane_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CU
     __shared__ int abort_flag;
 
     float* tiles = reinterpret_cast<float*>(smem_raw + smem_align_pad(smem_raw));
+    float* outs = tiles + static_cast<size_t>(stages) * kStageFloats;   // staged: [2][dx, da][TT][LI]
     const int o = blockIdx.x / tiles_i;
     const int i0 = (blockIdx.x % tiles_i) * LI;
-    const int ntiles = (T + kTT - 1) / kTT;
+    const int ntiles = (T + TT - 1) / TT;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // backward visits time descending for a forward scan, ascending for a reverse one
@@ -83,7 +99,7 @@ k_lane_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CU
                 issued = k + 1;
                 if (k == drop_tile) continue;   // testing hook: this tile never arrives
                 const int j = desc ? ntiles - 1 - k : k;
-                const int t0 = j * kTT;
+                const int t0 = j * TT;
                 float* st = tiles + s * kStageFloats;
                 mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
                 tma_load_3d(st, &map_g, i0, t0, o, &full_bar[s], pol);
@@ -106,23 +122,47 @@ k_lane_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CU
     const bool valid = i < I;
     const float p0 = valid ? init[static_cast<int64_t>(o) * I + i] : 0.0f;
     const int t_first = reverse ? T - 1 : 0;            // first trip in scan order: its p is initial
+    const bool storer = kStaged && threadIdx.x == 32;
     float lam = 0.0f;
     const int64_t base = static_cast<int64_t>(o) * T * I + i;
 
-    for (int k = 0; k < ntiles; ++k) {
+    // Staged: one consumer barrier per tile votes on whether any consumer gave
+    // up its wait and marks the previous tile's gradients complete in SMEM.
+    // Direct: each warp leaves on its own vote.
+    for (int k = 0; k < ntiles + (kStaged ? 1 : 0); ++k) {
         const int s = k % stages;
-        const bool ok = mbar_wait_bounded(&full_bar[s], (k / stages) & 1, wait_ns, &abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) {
-            if (!ok) report_timeout(status, &abort_flag);
-            break;
+        bool ok = true;
+        if (k < ntiles) ok = mbar_wait_bounded(&full_bar[s], (k / stages) & 1, wait_ns, &abort_flag);
+        if constexpr (kStaged) {
+            // the buffer this tile writes was last read by the store issued a
+            // tile ago: the storer waits for that read before the barrier
+            if (storer) bulk_wait_read<0>();
+            if (k > 0) fence_proxy_async_smem();     // this thread's gradient writes of tile k-1
+            if (consumer_vote_any_failed(!ok, LI)) {
+                if (!ok) report_timeout(status, &abort_flag);
+                break;
+            }
+            if (storer && k > 0) {
+                const int jp = desc ? ntiles - k : k - 1;
+                const float* ob = outs + static_cast<size_t>((k - 1) & 1) * 2 * kTile;
+                tma_store_3d(&map_gx, i0, jp * TT, o, ob);
+                tma_store_3d(&map_ga, i0, jp * TT, o, ob + kTile);
+                bulk_commit();
+            }
+            if (k == ntiles) break;
+        } else {
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (!ok) report_timeout(status, &abort_flag);
+                break;
+            }
         }
         const int j = desc ? ntiles - 1 - k : k;
-        const int t0 = j * kTT;
-        const int n = min(kTT, T - t0);
+        const int t0 = j * TT;
+        const int n = min(TT, T - t0);
         const float* st = tiles + s * kStageFloats + c;
-        float gr[kTT], ar[kTT], xr[kNeedX ? kTT : 1], hr[kRows];
+        float gr[TT], ar[TT], xr[kNeedX ? TT : 1], hr[kRows];
 #pragma unroll
-        for (int tt = 0; tt < kTT; ++tt) {
+        for (int tt = 0; tt < TT; ++tt) {
             gr[tt] = st[tt * LI];
             ar[tt] = st[kTile + tt * LI];
             if constexpr (kNeedX) xr[tt] = st[2 * kTile + tt * LI];
@@ -136,6 +176,7 @@ k_lane_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CU
         // scan); the state before it is the row next to it
         float* dxp = gx + base + static_cast<int64_t>(t0) * I;
         float* dap = ga + base + static_cast<int64_t>(t0) * I;
+        float* ob = outs + static_cast<size_t>(k & 1) * 2 * kTile + c;
         auto trip = [&](const int tt) {
             const float h = reverse ? hr[tt] : hr[tt + 1];
             float p = reverse ? hr[tt + 1] : hr[tt];
@@ -150,46 +191,79 @@ k_lane_bwd(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CU
             } else {
                 maxplus_vjp(__fsub_rn(p, ar[tt]), xr[tt], lam, dx, da);
             }
-            if (valid) {
+            if constexpr (kStaged) {
+                ob[tt * LI] = dx;
+                ob[kTile + tt * LI] = da;
+            } else if (valid) {
                 __stcs(dxp + static_cast<int64_t>(tt) * I, dx);
                 __stcs(dap + static_cast<int64_t>(tt) * I, da);
             }
         };
-        if (n == kTT) {
+        // trips past T in a ragged tile (zero-filled) must not touch the
+        // cotangent; a staged tile's TMA store clips them
+        if (n == TT) {
             if (desc) {
 #pragma unroll
-                for (int tt = kTT - 1; tt >= 0; --tt) trip(tt);
+                for (int tt = TT - 1; tt >= 0; --tt) trip(tt);
             } else {
 #pragma unroll
-                for (int tt = 0; tt < kTT; ++tt) trip(tt);
+                for (int tt = 0; tt < TT; ++tt) trip(tt);
             }
         } else if (desc) {
 #pragma unroll
-            for (int tt = kTT - 1; tt >= 0; --tt)
+            for (int tt = TT - 1; tt >= 0; --tt)
                 if (tt < n) trip(tt);
         } else {
 #pragma unroll
-            for (int tt = 0; tt < kTT; ++tt)
+            for (int tt = 0; tt < TT; ++tt)
                 if (tt < n) trip(tt);
         }
     }
+    if (storer) bulk_wait_all();
     if (valid) ginit[static_cast<int64_t>(o) * I + i] = lam;
 }
 
-template <int BODY, int LI>
-cudaError_t launch_bwd_li(const BackwardLaunch& B, const CUtensorMap* maps, int I, int tiles_i, int stages) {
+// the launch's shape: lanes per CTA, trips per tile, stages, staged stores
+struct BwdCfg {
+    int LI, TT, stages;
+    bool staged;
+};
+
+size_t bwd_smem(int body, const BwdCfg& c) {
+    const size_t tile = static_cast<size_t>(c.TT) * c.LI;
+    const size_t stage = (body == ES_BODY_MAXPLUS ? 3 : 2) * tile + static_cast<size_t>(c.TT + 1) * c.LI;
+    return (c.stages * stage + (c.staged ? 4 * tile : 0)) * 4 + 1024;
+}
+
+template <int BODY, int LI, int TT, bool kStaged>
+cudaError_t launch_bwd_cfg(const BackwardLaunch& B, const CUtensorMap* maps, int I, int tiles_i, int stages) {
     const Launch& L = B.fwd;
-    constexpr bool kNeedX = BODY == ES_BODY_MAXPLUS;
-    const size_t stage_floats = static_cast<size_t>(kNeedX ? 3 : 2) * kTT * LI + static_cast<size_t>(kTT + 1) * LI;
-    const size_t smem = static_cast<size_t>(stages) * stage_floats * 4 + 1024;
-    auto kern = k_lane_bwd<BODY, LI>;
+    const size_t smem = bwd_smem(BODY, BwdCfg{LI, TT, stages, kStaged});
+    auto kern = k_lane_bwd<BODY, LI, TT, kStaged>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int64_t grid = L.O * tiles_i;
     kern<<<static_cast<unsigned>(grid), 32 + LI, smem, L.stream>>>(
-        maps[0], maps[1], maps[2], maps[3], L.init, B.ginit, B.gx, B.ga, static_cast<int>(L.T), I, tiles_i, stages,
-        L.reverse, L.status, L.wait_ns, L.drop_tile);
+        maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], L.init, B.ginit, B.gx, B.ga, static_cast<int>(L.T), I,
+        tiles_i, stages, L.reverse, L.status, L.wait_ns, L.drop_tile);
     return cudaGetLastError();
+}
+
+template <int BODY, int LI>
+cudaError_t launch_bwd_li(const BackwardLaunch& B, const CUtensorMap* maps, int I, int tiles_i, const BwdCfg& c) {
+    if (c.staged) {
+        if (c.TT == 32) return launch_bwd_cfg<BODY, LI, 32, true>(B, maps, I, tiles_i, c.stages);
+        return launch_bwd_cfg<BODY, LI, 16, true>(B, maps, I, tiles_i, c.stages);
+    }
+    if (c.TT == 32) return launch_bwd_cfg<BODY, LI, 32, false>(B, maps, I, tiles_i, c.stages);
+    return launch_bwd_cfg<BODY, LI, 16, false>(B, maps, I, tiles_i, c.stages);
+}
+
+template <int BODY>
+cudaError_t launch_bwd_body(const BackwardLaunch& B, const CUtensorMap* maps, int I, int tiles_i, const BwdCfg& c) {
+    if (c.LI == 128) return launch_bwd_li<BODY, 128>(B, maps, I, tiles_i, c);
+    if (c.LI == 64) return launch_bwd_li<BODY, 64>(B, maps, I, tiles_i, c);
+    return launch_bwd_li<BODY, 32>(B, maps, I, tiles_i, c);
 }
 
 bool encode_bwd(const Launch& L, CUtensorMap* m, const float* base, int64_t I, int LI, int rows, const char** err) {
@@ -221,22 +295,29 @@ cudaError_t launch_lane_tma_bwd(const BackwardLaunch& B, const char** err) {
         }
     }
     const int64_t tiles_i = (I + LI - 1) / LI;
-    // about 64 trips of every stream in flight per CTA
-    const int stages = 4;
-    CUtensorMap maps[4];
+    const bool one_per_sm = L.O * tiles_i <= L.num_sms;
+    // Where several CTAs share an SM, 16-trip tiles with the gradients staged
+    // for TMA stores, as many stages as keep a CTA within about 100 KB (two a
+    // SM); where there is at most one CTA a SM, direct row stores and four
+    // 16-trip stages.
+    BwdCfg c{LI, 16, 4, !one_per_sm};
+    if (c.staged) {
+        c.stages = 6;
+        while (c.stages > 2 && bwd_smem(L.body, c) > 100 * 1024) --c.stages;
+    }
+    if (ES_LANE_BWD_TT != 0) c.TT = ES_LANE_BWD_TT;
+    if (ES_LANE_BWD_STAGES != 0) c.stages = ES_LANE_BWD_STAGES;
+    if (ES_LANE_BWD_STAGED >= 0) c.staged = ES_LANE_BWD_STAGED != 0;
+    CUtensorMap maps[6];
     const float* x = L.body == ES_BODY_MAXPLUS ? L.x : L.a;   // TANH needs no x: map something valid
-    if (!encode_bwd(L, &maps[0], B.gout, I, LI, kTT, err) || !encode_bwd(L, &maps[1], B.states, I, LI, kTT + 1, err) ||
-        !encode_bwd(L, &maps[2], L.a, I, LI, kTT, err) || !encode_bwd(L, &maps[3], x, I, LI, kTT, err))
+    if (!encode_bwd(L, &maps[0], B.gout, I, LI, c.TT, err) ||
+        !encode_bwd(L, &maps[1], B.states, I, LI, c.TT + 1, err) || !encode_bwd(L, &maps[2], L.a, I, LI, c.TT, err) ||
+        !encode_bwd(L, &maps[3], x, I, LI, c.TT, err) || !encode_bwd(L, &maps[4], B.gx, I, LI, c.TT, err) ||
+        !encode_bwd(L, &maps[5], B.ga, I, LI, c.TT, err))
         return cudaErrorInvalidValue;
     const int Ii = static_cast<int>(I), ti = static_cast<int>(tiles_i);
-    if (L.body == ES_BODY_TANH_DECAY) {
-        if (LI == 128) return launch_bwd_li<ES_BODY_TANH_DECAY, 128>(B, maps, Ii, ti, stages);
-        if (LI == 64) return launch_bwd_li<ES_BODY_TANH_DECAY, 64>(B, maps, Ii, ti, stages);
-        return launch_bwd_li<ES_BODY_TANH_DECAY, 32>(B, maps, Ii, ti, stages);
-    }
-    if (LI == 128) return launch_bwd_li<ES_BODY_MAXPLUS, 128>(B, maps, Ii, ti, stages);
-    if (LI == 64) return launch_bwd_li<ES_BODY_MAXPLUS, 64>(B, maps, Ii, ti, stages);
-    return launch_bwd_li<ES_BODY_MAXPLUS, 32>(B, maps, Ii, ti, stages);
+    if (L.body == ES_BODY_TANH_DECAY) return launch_bwd_body<ES_BODY_TANH_DECAY>(B, maps, Ii, ti, c);
+    return launch_bwd_body<ES_BODY_MAXPLUS>(B, maps, Ii, ti, c);
 }
 
 }  // namespace es

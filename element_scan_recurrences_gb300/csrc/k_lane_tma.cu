@@ -241,7 +241,6 @@ cudaError_t launch_lane_tma(const Launch& L, const char** err) {
     }
     if (ES_LANE_LI != 0 && I >= ES_LANE_LI) LI = ES_LANE_LI;
     const int64_t tiles_i = (I + LI - 1) / LI;
-    const int64_t ctas = L.O * tiles_i;
     // Pipeline depth: about 96 trips of both sequences in flight per CTA
     // (three 32-trip stages), measured best on GB300 for both one CTA per
     // SM (few lanes) and several (many lanes, even when not all CTAs fit at
@@ -249,7 +248,6 @@ cudaError_t launch_lane_tma(const Launch& L, const char** err) {
     // 256-lane tiles (1 KB row segments, one CTA a SM) measured best with two
     // 32-trip stages: 0.502 against 0.517 ms for 128-lane tiles on
     // [64, 4096, 1024], three stages 0.511.
-    (void)ctas;
     int TT = 32;
     int stages = 3;
     if (LI == 256) {

@@ -131,6 +131,8 @@ SCAN_CASES = [
     ("lane_tma", wl.custom(T_, (3, 50, 200), 1, name="tanh_lane")),
     ("lane_tma", wl.custom(M_, (2, 37, 96), 1, name="maxplus_lane", **MAXPLUS_DISTS)),
     ("lane_tma", wl.custom(T_, (40, 70, 1000), 1, name="tanh_lane_256")),
+    ("lane_tma", wl.custom(M_, (40, 45, 1000), 1, name="maxplus_lane_staged", **MAXPLUS_DISTS)),
+    ("lane_tma", wl.custom(T_, (200, 37, 40), 1, name="tanh_lane_staged_32")),
     ("lane_tma", wl.custom(T_, (4, 33, 8, 16), 1, state_axis=True, seq_widths=(16, 16), name="tanh_vec_full")),
     ("time_tma", wl.custom(T_, (300, 100), -1, name="tanh_time")),
     ("time_tma", wl.custom(M_, (129, 68), 1, name="maxplus_time", **MAXPLUS_DISTS)),
