@@ -260,9 +260,10 @@ bool launch_body_lane(const BodyLaunch& L, std::string* err) {
     const BodyCall& C = *L.C;
     const int NS = C.S.n_seqs;
     const int64_t I = C.S.J;
-    // lanes per CTA: the widest tile that still puts a CTA on most SMs
+    // lanes per CTA: the widest tile (the longest contiguous row segment per
+    // TMA box row) that still puts a CTA on most SMs
     int LI = 32;
-    for (int cand : {128, 64}) {
+    for (int cand : {256, 128, 64}) {
         if (I >= cand && 5 * C.S.O * ((I + cand - 1) / cand) >= 4LL * L.dev->num_sms) {
             LI = cand;
             break;
@@ -824,7 +825,7 @@ es_status es_body_prepare(es_body_t body, int state_width, int n_seqs, const int
     std::vector<es::KernelText> todo;
     if (path == ES_PATH_AUTO || path == ES_PATH_GENERIC) todo.push_back(es::generic_text(functor, W));
     if ((path == ES_PATH_AUTO || path == ES_PATH_LANE_TMA) && W == 1)
-        for (int LI : {32, 64, 128}) todo.push_back(es::lane_text(functor, LI, es::lane_trips(n_seqs)));
+        for (int LI : {32, 64, 128, 256}) todo.push_back(es::lane_text(functor, LI, es::lane_trips(n_seqs)));
     if ((path == ES_PATH_AUTO || path == ES_PATH_TIME_TMA) && W == 1) todo.push_back(es::time_text(functor));
     if ((path == ES_PATH_AUTO || path == ES_PATH_VEC_TMA) && (W == 2 || W == 4 || W == 8 || W == 16)) {
         int n_wide = 0;

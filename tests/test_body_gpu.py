@@ -104,6 +104,18 @@ SCALAR_IDS = [c[0] for c in body_cases.CASES if c[2] == 0]
 
 @pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
 @pytest.mark.parametrize("cid", SCALAR_IDS)
+def test_body_wide_lane_tiles(cid, reverse):
+    """Rows wide and a batch deep enough for 256-lane tiles: a ragged last
+    lane tile (1000 = 3 x 256 + 232) and a ragged last trip tile."""
+    c = body_cases.case(cid)
+    O, T, J = 40, 70, 1000
+    assert tiled_path(c, O, T, J, 1) == "lane_tma"
+    got, want = run(c, O, T, J, 1, reverse, "auto")
+    compare(got, want, c[7], "%s wide lane tiles reverse=%s" % (cid, reverse))
+
+
+@pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
+@pytest.mark.parametrize("cid", SCALAR_IDS)
 def test_body_time_path(cid, reverse):
     """The sequence axis last: rows of T trips transposed through shared
     memory; a ragged last row tile and a ragged last trip tile."""

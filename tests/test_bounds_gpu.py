@@ -201,6 +201,7 @@ def test_host_pipeline_stays_in_bounds():
 GATED = "(lambda (h x a g) (where (> g 0.5) (tanh (+ x (* a h))) h))"
 BODY_CASES = [
     ("lane_tma", GATED, (3, 50, 200), 1, False, None),
+    ("lane_tma", GATED, (40, 45, 1000), 1, False, None),
     ("time_tma", GATED, (300, 100), -1, False, None),
     ("generic", GATED, (5, 7, 3), 0, False, None),
     ("vec_tma", wl.NORMCAP_TEXT, (3, 45, 20, 16), 1, True, (16, 1)),
@@ -208,7 +209,7 @@ BODY_CASES = [
 
 
 @pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
-@pytest.mark.parametrize("case", BODY_CASES, ids=[c[0] for c in BODY_CASES])
+@pytest.mark.parametrize("case", BODY_CASES, ids=["%s_%s" % (c[0], "x".join(map(str, c[2]))) for c in BODY_CASES])
 def test_body_program_stays_in_bounds(case, reverse):
     path, text, shape, axis, state_axis, widths = case
     body = es.Body(text)
