@@ -576,21 +576,38 @@ k_mat_da(const float* __restrict__ lam, const float* __restrict__ states, float*
                 for (int q = 0; q < KV; ++q) hv[b][q] = 0.0f;
             }
         }
+        if constexpr (KV % 2 == 0) {
+            // two consecutive k of one entry per packed multiply (each still
+            // one rounded product; the operands sit side by side as loaded)
 #pragma unroll
-        for (int q = 0; q < KV; ++q) {
+            for (int q = 0; q < KV; q += 2)
 #pragma unroll
-            for (int x = 0; x < B; ++x) {
-                float p[B];
-                if constexpr (B % 2 == 0) {
-                    // two products at a time (each still one rounded product)
+                for (int x = 0; x < B; ++x)
 #pragma unroll
-                    for (int y = 0; y < B; y += 2) mul2_rn(p[y], p[y + 1], lv[x][q], lv[x][q], hv[y][q], hv[y + 1][q]);
-                } else {
+                    for (int y = 0; y < B; ++y) {
+                        float p0, p1;
+                        mul2_rn(p0, p1, lv[x][q], lv[x][q + 1], hv[y][q], hv[y][q + 1]);
+                        const float a = (k + q == 0) ? p0 : __fadd_rn(acc[x][y], p0);
+                        acc[x][y] = __fadd_rn(a, p1);
+                    }
+        } else {
 #pragma unroll
-                    for (int y = 0; y < B; ++y) p[y] = __fmul_rn(lv[x][q], hv[y][q]);
+            for (int q = 0; q < KV; ++q) {
+#pragma unroll
+                for (int x = 0; x < B; ++x) {
+                    float p[B];
+                    if constexpr (B % 2 == 0) {
+                        // two products at a time (each still one rounded product)
+#pragma unroll
+                        for (int y = 0; y < B; y += 2)
+                            mul2_rn(p[y], p[y + 1], lv[x][q], lv[x][q], hv[y][q], hv[y + 1][q]);
+                    } else {
+#pragma unroll
+                        for (int y = 0; y < B; ++y) p[y] = __fmul_rn(lv[x][q], hv[y][q]);
+                    }
+#pragma unroll
+                    for (int y = 0; y < B; ++y) acc[x][y] = (k + q == 0) ? p[y] : __fadd_rn(acc[x][y], p[y]);
                 }
-#pragma unroll
-                for (int y = 0; y < B; ++y) acc[x][y] = (k + q == 0) ? p[y] : __fadd_rn(acc[x][y], p[y]);
             }
         }
     }
@@ -614,13 +631,22 @@ k_mat_da(const float* __restrict__ lam, const float* __restrict__ states, float*
 // of a warp spread over 8 rows, one L1 wavefront per 16 bytes, and L1 bound
 // the kernel (ncu: L1TEX throughput 93%).  Here the warp reads the unit's two
 // 1 KB blocks with coalesced 16-byte loads into shared memory, each row's
-// four 16-byte chunks XOR-swizzled by (row / 2) % 4 so that the reads below
-// are free of bank conflicts, then lane (bi, bj) forms rows bi + 4x and
-// columns bj + 8y of da, each entry the sum over k = 0..15 in order of
+// four 16-byte chunks XOR-swizzled (da16_off) so that the reads below are
+// free of bank conflicts.  Lane (ri, cj) forms rows ri and ri + 8, columns
+// 4cj .. 4cj + 3 of da, each entry the sum over k = 0..15 in order of
 // lam[i][k] * h_prev[j][k] (the same rounded products and sums as k_mat_da).
+// A packed multiply takes two consecutive k of one entry, whose operands sit
+// side by side in the 16-byte chunks read, and each finished row of four
+// entries leaves in one 16-byte store (a warp's store covers 512 contiguous
+// bytes).
 constexpr int kDa16Warps = 4;
 
-__device__ __forceinline__ int da16_off(int row, int chunk) { return row * 16 + ((chunk ^ ((row >> 1) & 3)) << 2); }
+// chunk slot of (row, chunk): XOR by ((row >> 1) + (row >> 3)) % 4.  Rows 0..7
+// (or 8..15) read at one chunk land on eight different bank groups, and so do
+// rows {y, y + 4, y + 8, y + 12} (row parity picks the half of the banks).
+__device__ __forceinline__ int da16_off(int row, int chunk) {
+    return row * 16 + ((chunk ^ (((row >> 1) + (row >> 3)) & 3)) << 2);
+}
 
 __global__ void __launch_bounds__(32 * kDa16Warps)
 k_mat_da16(const float* __restrict__ lam, const float* __restrict__ states, float* __restrict__ da, int64_t units,
@@ -648,42 +674,33 @@ k_mat_da16(const float* __restrict__ lam, const float* __restrict__ states, floa
         *reinterpret_cast<float4*>(sh + da16_off(f >> 2, f & 3)) = hv;
     }
     __syncwarp();
-    const int bi = lane & 3, bj = lane >> 2;
-    float acc[4][2];
+    const int ri = lane & 7, cj = lane >> 3;
+    float acc[2][4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        float lv[4][4], hv[2][4];
+        float4 lv[2], hv[4];
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-            const float4 v = *reinterpret_cast<const float4*>(sl + da16_off(bi + 4 * x, c));
-            lv[x][0] = v.x;
-            lv[x][1] = v.y;
-            lv[x][2] = v.z;
-            lv[x][3] = v.w;
-        }
+        for (int x = 0; x < 2; ++x) lv[x] = *reinterpret_cast<const float4*>(sl + da16_off(ri + 8 * x, c));
 #pragma unroll
-        for (int y = 0; y < 2; ++y) {
-            const float4 v = *reinterpret_cast<const float4*>(sh + da16_off(bj + 8 * y, c));
-            hv[y][0] = v.x;
-            hv[y][1] = v.y;
-            hv[y][2] = v.z;
-            hv[y][3] = v.w;
-        }
+        for (int y = 0; y < 4; ++y) hv[y] = *reinterpret_cast<const float4*>(sh + da16_off(4 * cj + y, c));
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int x = 0; x < 2; ++x)
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                float p0, p1;
-                mul2_rn(p0, p1, lv[x][q], lv[x][q], hv[0][q], hv[1][q]);
-                acc[x][0] = (c + q == 0) ? p0 : __fadd_rn(acc[x][0], p0);
-                acc[x][1] = (c + q == 0) ? p1 : __fadd_rn(acc[x][1], p1);
+            for (int y = 0; y < 4; ++y) {
+                float p0, p1, p2, p3;
+                mul2_rn(p0, p1, lv[x].x, lv[x].y, hv[y].x, hv[y].y);
+                mul2_rn(p2, p3, lv[x].z, lv[x].w, hv[y].z, hv[y].w);
+                float a = c == 0 ? p0 : __fadd_rn(acc[x][y], p0);
+                a = __fadd_rn(a, p1);
+                a = __fadd_rn(a, p2);
+                acc[x][y] = __fadd_rn(a, p3);
             }
     }
     float* D = da + u * 256;
 #pragma unroll
-    for (int x = 0; x < 4; ++x)
-#pragma unroll
-        for (int y = 0; y < 2; ++y) __stcs(D + (bi + 4 * x) * 16 + bj + 8 * y, acc[x][y]);
+    for (int x = 0; x < 2; ++x)
+        __stcs(reinterpret_cast<float4*>(D + (ri + 8 * x) * 16 + 4 * cj),
+               make_float4(acc[x][0], acc[x][1], acc[x][2], acc[x][3]));
 }
 
 template <int N>
@@ -699,7 +716,7 @@ cudaError_t launch_da_n(const float* lam, const float* states, float* da, int64_
     const bool vec = m % 4 == 0 && reinterpret_cast<uintptr_t>(lam) % 16 == 0 &&
                      reinterpret_cast<uintptr_t>(states) % 16 == 0;
     if constexpr (N == 16) {
-        if (m == 16 && vec) {
+        if (m == 16 && vec && reinterpret_cast<uintptr_t>(da) % 16 == 0) {
             const int64_t blocks = (units + kDa16Warps - 1) / kDa16Warps;
             if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
             k_mat_da16<<<static_cast<unsigned>(blocks), 32 * kDa16Warps, 0, stream>>>(lam, states, da, units, T, J,
