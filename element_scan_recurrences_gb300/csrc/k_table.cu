@@ -38,20 +38,27 @@ __device__ __forceinline__ int clamp_symbol(int s, int n_syms) { return min(max(
 // entries q = row * n_syms + symbol: the next state, clamped (`state_of`),
 // and that state's row offset (`next_off`).  A step is then
 //     off' = next_off[off + s]      (one add and one load on the chain)
-// with the state read beside it, off the chain: state_of[off + s].
+// with the state read beside it, off the chain: state_of[off + s].  When
+// n_syms is a power of two the state is off' >> log2(n_syms) and only
+// next_off is staged: one shared-memory lookup a step, not two (the lookups,
+// at random rows, are what the kernels' shared-memory traffic is made of).
+//
+// TAB: 0 the table read from global memory, 1 staged as both arrays, 2
+// staged as next_off alone (n_syms a power of two).
 struct TableSmem {
     const int* next_off;
     const int* state_of;
 };
 
 // copy and prepare the table (every thread of the CTA takes part)
+template <int TAB>
 __device__ __forceinline__ TableSmem stage_table(int* dst, const int* __restrict__ src, int n_states, int n_syms) {
     const int entries = n_states * n_syms;
     int* next_off = dst;
     int* state_of = dst + entries;
     for (int q = threadIdx.x; q < entries; q += blockDim.x) {
         const int e = min(max(__ldg(src + q), 0), n_states - 1);
-        state_of[q] = e;
+        if constexpr (TAB == 1) state_of[q] = e;
         next_off[q] = e * n_syms;
     }
     return TableSmem{next_off, state_of};
@@ -59,12 +66,16 @@ __device__ __forceinline__ TableSmem stage_table(int* dst, const int* __restrict
 
 // One step of a row-offset-carrying run: returns the state after symbol `s`
 // (already clamped) and advances `off`.  A table left in global memory is
-// read through the read-only path and clamped on the way.
-template <bool SMEM>
+// read through the read-only path and clamped on the way.  `sh` is
+// log2(n_syms) (TAB 2).
+template <int TAB>
 __device__ __forceinline__ int table_step(int& off, int s, const TableSmem& ts, const int* __restrict__ table,
-                                          int n_syms, int hi) {
+                                          int n_syms, int hi, int sh) {
     const int q = off + s;
-    if constexpr (SMEM) {
+    if constexpr (TAB == 2) {
+        off = ts.next_off[q];
+        return off >> sh;
+    } else if constexpr (TAB == 1) {
         off = ts.next_off[q];
         return ts.state_of[q];
     } else {
@@ -74,22 +85,28 @@ __device__ __forceinline__ int table_step(int& off, int s, const TableSmem& ts, 
     }
 }
 
-// shared memory a staged table takes
+// shared memory a staged table takes (both arrays)
 __host__ __device__ constexpr size_t staged_table_bytes(int64_t n_states, int64_t n_syms) {
     return static_cast<size_t>(n_states) * static_cast<size_t>(n_syms) * 8;
+}
+
+// the staging a launch uses, and the shared memory it takes
+int table_mode(bool smem, int n_syms) { return !smem ? 0 : (n_syms & (n_syms - 1)) == 0 ? 2 : 1; }
+size_t table_mode_bytes(int tab, int64_t n_states, int64_t n_syms) {
+    return tab == 0 ? 0 : tab == 2 ? staged_table_bytes(n_states, n_syms) / 2 : staged_table_bytes(n_states, n_syms);
 }
 
 // ---------------------------------------------------------------------------
 // any layout
 
-template <bool SMEM>
+template <int TAB>
 __global__ void __launch_bounds__(128)
 k_table_generic(const int* __restrict__ table, const int* __restrict__ sym, int* __restrict__ out, int64_t O,
                 int64_t T, int64_t J, int n_states, int n_syms, int start) {
     extern __shared__ int tab_s[];
     TableSmem ts{};
-    if constexpr (SMEM) {
-        ts = stage_table(tab_s, table, n_states, n_syms);
+    if constexpr (TAB > 0) {
+        ts = stage_table<TAB>(tab_s, table, n_states, n_syms);
         __syncthreads();
     }
     const int64_t lane = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -98,10 +115,11 @@ k_table_generic(const int* __restrict__ table, const int* __restrict__ sym, int*
     const int64_t j = lane - o * J;
     int off = start * n_syms;
     const int hi = n_states - 1;
+    const int sh = __ffs(n_syms) - 1;
     const int* sp = sym + o * T * J + j;
     int* op = out + o * T * J + j;
     for (int64_t t = 0; t < T; ++t) {
-        const int h = table_step<SMEM>(off, clamp_symbol(__ldg(sp + t * J), n_syms), ts, table, n_syms, hi);
+        const int h = table_step<TAB>(off, clamp_symbol(__ldg(sp + t * J), n_syms), ts, table, n_syms, hi, sh);
         __stcs(op + t * J, h);
     }
 }
@@ -112,7 +130,7 @@ k_table_generic(const int* __restrict__ table, const int* __restrict__ sym, int*
 constexpr int kTabMaxStages = 6;
 constexpr int kTabTT = 32;
 
-template <int LI, bool SMEM>
+template <int LI, int TAB>
 __global__ void __launch_bounds__(32 + LI)
 k_table_lane(const __grid_constant__ CUtensorMap map_s, const int* __restrict__ table, int* __restrict__ out, int T,
              int I, int tiles_i, int stages, int n_states, int n_syms, int start, unsigned int* status,
@@ -124,7 +142,7 @@ k_table_lane(const __grid_constant__ CUtensorMap map_s, const int* __restrict__ 
     constexpr int kTileInts = kTabTT * LI;
     int* tiles = reinterpret_cast<int*>(smem_raw + smem_align_pad(smem_raw));
     TableSmem ts{};
-    if constexpr (SMEM) ts = stage_table(tiles + stages * kTileInts, table, n_states, n_syms);
+    if constexpr (TAB > 0) ts = stage_table<TAB>(tiles + stages * kTileInts, table, n_states, n_syms);
 
     const int o = blockIdx.x / tiles_i;
     const int i0 = (blockIdx.x % tiles_i) * LI;
@@ -171,6 +189,7 @@ k_table_lane(const __grid_constant__ CUtensorMap map_s, const int* __restrict__ 
     const int i = i0 + c;
     const bool valid = i < I;
     const int hi = n_states - 1;
+    const int sh = __ffs(n_syms) - 1;
     int off = start * n_syms;
     int* obase = out + static_cast<int64_t>(o) * T * I + i;
     for (int k = 0; k < ntiles; ++k) {
@@ -195,7 +214,7 @@ k_table_lane(const __grid_constant__ CUtensorMap map_s, const int* __restrict__ 
         // still be reading
         int hv[2];
         auto trip = [&](const int tt) {
-            hv[tt & 1] = table_step<SMEM>(off, sr[tt], ts, table, n_syms, hi);
+            hv[tt & 1] = table_step<TAB>(off, sr[tt], ts, table, n_syms, hi, sh);
             if (valid) __stcs(op + static_cast<int64_t>(tt) * I, hv[tt & 1]);
         };
         if (n == kTabTT) {
@@ -215,7 +234,7 @@ k_table_lane(const __grid_constant__ CUtensorMap map_s, const int* __restrict__ 
 constexpr int kTabLO = 64;
 constexpr int kTabOutBufs = 3;
 
-template <bool SMEM>
+template <int TAB>
 __global__ void __launch_bounds__(32 + kTabLO)
 k_table_time(const __grid_constant__ CUtensorMap map_s, const __grid_constant__ CUtensorMap map_out,
              const int* __restrict__ table, int O, int T, int stages, int n_states, int n_syms, int start,
@@ -229,8 +248,8 @@ k_table_time(const __grid_constant__ CUtensorMap map_s, const __grid_constant__ 
     unsigned char* in_tiles = base;
     unsigned char* out_tiles = base + static_cast<size_t>(stages) * kTileBytes;
     TableSmem ts{};
-    if constexpr (SMEM)
-        ts = stage_table(reinterpret_cast<int*>(out_tiles + kTabOutBufs * kTileBytes), table, n_states, n_syms);
+    if constexpr (TAB > 0)
+        ts = stage_table<TAB>(reinterpret_cast<int*>(out_tiles + kTabOutBufs * kTileBytes), table, n_states, n_syms);
 
     const int o0 = blockIdx.x * kTabLO;
     const int ntiles = (T + 31) / 32;
@@ -274,6 +293,7 @@ k_table_time(const __grid_constant__ CUtensorMap map_s, const __grid_constant__ 
 
     const int r = threadIdx.x - 32;
     const int hi = n_states - 1;
+    const int sh = __ffs(n_syms) - 1;
     int off = start * n_syms;
     const uint32_t row_off = static_cast<uint32_t>(r) * 128u;
     const uint32_t swz = static_cast<uint32_t>(r & 7);   // 128-byte swizzle: chunk q lives at q ^ (row % 8)
@@ -306,10 +326,10 @@ k_table_time(const __grid_constant__ CUtensorMap map_s, const __grid_constant__ 
         for (int q = 0; q < 8; ++q) {
             if (q < nq) {
                 int4 v;
-                v.x = table_step<SMEM>(off, clamp_symbol(seg[q].x, n_syms), ts, table, n_syms, hi);
-                v.y = table_step<SMEM>(off, clamp_symbol(seg[q].y, n_syms), ts, table, n_syms, hi);
-                v.z = table_step<SMEM>(off, clamp_symbol(seg[q].z, n_syms), ts, table, n_syms, hi);
-                v.w = table_step<SMEM>(off, clamp_symbol(seg[q].w, n_syms), ts, table, n_syms, hi);
+                v.x = table_step<TAB>(off, clamp_symbol(seg[q].x, n_syms), ts, table, n_syms, hi, sh);
+                v.y = table_step<TAB>(off, clamp_symbol(seg[q].y, n_syms), ts, table, n_syms, hi, sh);
+                v.z = table_step<TAB>(off, clamp_symbol(seg[q].z, n_syms), ts, table, n_syms, hi, sh);
+                v.w = table_step<TAB>(off, clamp_symbol(seg[q].w, n_syms), ts, table, n_syms, hi, sh);
                 *reinterpret_cast<int4*>(orow + ((static_cast<uint32_t>(q) ^ swz) << 4)) = v;
             }
         }
@@ -317,25 +337,25 @@ k_table_time(const __grid_constant__ CUtensorMap map_s, const __grid_constant__ 
     if (storer) bulk_wait_all();
 }
 
-template <bool SMEM>
+template <int TAB>
 cudaError_t launch_generic_t(const TableLaunch& L, size_t table_bytes) {
     const int64_t lanes = L.O * L.J;
     const int64_t blocks = (lanes + 127) / 128;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    const size_t smem = SMEM ? table_bytes : 0;
+    const size_t smem = table_bytes;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k_table_generic<SMEM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(k_table_generic<TAB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    k_table_generic<SMEM><<<static_cast<unsigned>(blocks), 128, smem, L.stream>>>(
+    k_table_generic<TAB><<<static_cast<unsigned>(blocks), 128, smem, L.stream>>>(
         L.table, L.sym, L.out, L.O, L.T, L.J, L.n_states, L.n_syms, L.start);
     return cudaGetLastError();
 }
 
-template <int LI, bool SMEM>
+template <int LI, int TAB>
 cudaError_t launch_lane_t(const TableLaunch& L, const CUtensorMap& ms, int tiles_i, int stages, size_t smem) {
-    auto kern = k_table_lane<LI, SMEM>;
+    auto kern = k_table_lane<LI, TAB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(L.O * tiles_i), 32 + LI, smem, L.stream>>>(
@@ -344,10 +364,10 @@ cudaError_t launch_lane_t(const TableLaunch& L, const CUtensorMap& ms, int tiles
     return cudaGetLastError();
 }
 
-template <bool SMEM>
+template <int TAB>
 cudaError_t launch_time_t(const TableLaunch& L, const CUtensorMap& ms, const CUtensorMap& mo, int stages,
                           size_t smem) {
-    auto kern = k_table_time<SMEM>;
+    auto kern = k_table_time<TAB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>((L.O + kTabLO - 1) / kTabLO), 32 + kTabLO, smem, L.stream>>>(
@@ -375,13 +395,14 @@ bool table_time_ok(int64_t O, int64_t T, int64_t J, const void* sym, const void*
 }
 
 cudaError_t launch_table_generic(const TableLaunch& L) {
-    const size_t tb = staged_table_bytes(L.n_states, L.n_syms);
-    return table_in_smem(L.n_states, L.n_syms) ? launch_generic_t<true>(L, tb) : launch_generic_t<false>(L, tb);
+    const int tab = table_mode(table_in_smem(L.n_states, L.n_syms), L.n_syms);
+    const size_t tb = table_mode_bytes(tab, L.n_states, L.n_syms);
+    return tab == 2 ? launch_generic_t<2>(L, tb) : tab == 1 ? launch_generic_t<1>(L, tb) : launch_generic_t<0>(L, tb);
 }
 
 cudaError_t launch_table_lane(const TableLaunch& L, const char** err) {
-    const bool smem_tab = table_in_smem(L.n_states, L.n_syms);
-    const size_t tb = smem_tab ? staged_table_bytes(L.n_states, L.n_syms) : 0;
+    const int tab = table_mode(table_in_smem(L.n_states, L.n_syms), L.n_syms);
+    const size_t tb = table_mode_bytes(tab, L.n_states, L.n_syms);
     // 64 sequences per CTA and two stages: a lookup chain per thread leaves
     // latency that more CTAs per SM cover (on GB300 the lanes workload took
     // 0.49 / 0.47 / 0.41 ms at 4 / 3 / 2 stages with 128 sequences per CTA,
@@ -403,14 +424,16 @@ cudaError_t launch_table_lane(const TableLaunch& L, const char** err) {
         return cudaErrorInvalidValue;
     }
     const int ti = static_cast<int>(tiles_i);
-    if (smem_tab) return LI == 64 ? launch_lane_t<64, true>(L, ms, ti, stages, smem)
-                                  : launch_lane_t<32, true>(L, ms, ti, stages, smem);
-    return LI == 64 ? launch_lane_t<64, false>(L, ms, ti, stages, smem) : launch_lane_t<32, false>(L, ms, ti, stages, smem);
+    if (tab == 2) return LI == 64 ? launch_lane_t<64, 2>(L, ms, ti, stages, smem)
+                                  : launch_lane_t<32, 2>(L, ms, ti, stages, smem);
+    if (tab == 1) return LI == 64 ? launch_lane_t<64, 1>(L, ms, ti, stages, smem)
+                                  : launch_lane_t<32, 1>(L, ms, ti, stages, smem);
+    return LI == 64 ? launch_lane_t<64, 0>(L, ms, ti, stages, smem) : launch_lane_t<32, 0>(L, ms, ti, stages, smem);
 }
 
 cudaError_t launch_table_time(const TableLaunch& L, const char** err) {
-    const bool smem_tab = table_in_smem(L.n_states, L.n_syms);
-    const size_t tb = smem_tab ? staged_table_bytes(L.n_states, L.n_syms) : 0;
+    const int tab = table_mode(table_in_smem(L.n_states, L.n_syms), L.n_syms);
+    const size_t tb = table_mode_bytes(tab, L.n_states, L.n_syms);
     const int stages = 2;   // more CTAs per SM beat a deeper ring (0.43 ms at 4 stages, 0.38 at 2)
     const size_t smem = (static_cast<size_t>(stages) + kTabOutBufs) * kTabLO * 128 + tb + 1024;
     CUtensorMap maps[2];
@@ -427,8 +450,9 @@ cudaError_t launch_table_time(const TableLaunch& L, const char** err) {
             return cudaErrorInvalidValue;
         }
     }
-    return smem_tab ? launch_time_t<true>(L, maps[0], maps[1], stages, smem)
-                    : launch_time_t<false>(L, maps[0], maps[1], stages, smem);
+    return tab == 2 ? launch_time_t<2>(L, maps[0], maps[1], stages, smem)
+           : tab == 1 ? launch_time_t<1>(L, maps[0], maps[1], stages, smem)
+                      : launch_time_t<0>(L, maps[0], maps[1], stages, smem);
 }
 
 }  // namespace es
