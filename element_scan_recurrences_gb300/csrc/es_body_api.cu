@@ -380,7 +380,7 @@ bool launch_body_vec(const BodyLaunch& L, std::string* err) {
     if (budget > 160 * 1024) budget = 160 * 1024;
     int64_t st = budget / stage_bytes;
     st = st < 3 ? 3 : st > 8 ? 8 : st;
-    const int64_t fit = (226 * 1024) / stage_bytes;
+    const int64_t fit = (222 * 1024) / stage_bytes;     // beside the reductions' static shared memory
     if (st > fit) st = fit < 2 ? 2 : fit;
     const int stages = static_cast<int>(st);
     alignas(64) CUtensorMap maps[ES_MAX_SEQS];

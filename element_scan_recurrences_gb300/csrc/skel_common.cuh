@@ -67,18 +67,48 @@ __host__ __device__ constexpr int live_count(unsigned live_mask, int ns) {
 __host__ __device__ constexpr int live_slot(unsigned live_mask, int k) { return live_count(live_mask, k); }
 __host__ __device__ constexpr bool is_live(unsigned live_mask, int k) { return ((live_mask >> k) & 1u) != 0; }
 
-// `sum` over a lane's state: this thread's E values in order, then a
-// butterfly over the lane's G threads.  Every thread of the group ends with
-// the same bits (each level adds the same two operands).  With G = 1 the
-// order is w = 0..W-1.
+// threads of a block that may call group_sum with G >= 8 (the vector-state
+// skeletons launch at most 192)
+constexpr int kGroupSumThreads = 256;
+
+// `sum` over a lane's state: this thread's E values in order, then over the
+// lane's G threads.  With G >= 8 the partials meet in shared memory and
+// every thread adds its group's G partials as one pairwise tree (the same
+// order in all of them): a store and one 16-byte read per four partials
+// instead of log2(G) dependent shuffles on the chain; with G = 2 or 4 a
+// butterfly.  Every thread of the group ends with the same bits.  With G = 1
+// the order is w = 0..W-1.
 template <int E, int G>
 __device__ __forceinline__ float group_sum(const float (&v)[E], unsigned mask) {
     float s = v[0];
 #pragma unroll
     for (int e = 1; e < E; ++e) s = __fadd_rn(s, v[e]);
+    if constexpr (G >= 8) {
+        __shared__ __align__(16) float partial[kGroupSumThreads];
+        const int tid = threadIdx.x;
+        __syncwarp(mask);            // the group's reads of the previous call are done
+        partial[tid] = s;
+        __syncwarp(mask);
+        const float4* g4 = reinterpret_cast<const float4*>(partial + (tid & ~(G - 1)));
+        float p[G];
 #pragma unroll
-    for (int off = G / 2; off >= 1; off >>= 1) s = __fadd_rn(s, __shfl_xor_sync(mask, s, off));
-    return s;
+        for (int q = 0; q < G / 4; ++q) {
+            const float4 w = g4[q];
+            p[4 * q] = w.x;
+            p[4 * q + 1] = w.y;
+            p[4 * q + 2] = w.z;
+            p[4 * q + 3] = w.w;
+        }
+#pragma unroll
+        for (int span = 1; span < G; span *= 2)
+#pragma unroll
+            for (int q = 0; q < G; q += 2 * span) p[q] = __fadd_rn(p[q], p[q + span]);
+        return p[0];
+    } else {
+#pragma unroll
+        for (int off = G / 2; off >= 1; off >>= 1) s = __fadd_rn(s, __shfl_xor_sync(mask, s, off));
+        return s;
+    }
 }
 
 // `max` over a lane's state (IEEE maximum: exact, so the order is free)
