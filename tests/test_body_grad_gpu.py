@@ -265,9 +265,12 @@ def test_body_backward_rejects_overlap_on_device():
 
 
 @pytest.mark.parametrize("name", ["body_tanh_decay_lanes", "body_normcap_vector", "body_maxplus_reverse"])
-def test_body_backward_full_size_sampled(name):
+def test_body_backward_full_size_every_element(name):
     """The backward of a body workload at full size in the bench's launch
-    configuration, checked on sampled lanes against the gradient oracle."""
+    configuration, every gradient against the gradient oracle (run on every
+    host core over contiguous blocks of the leading dimension, from the same
+    saved states)."""
+    import oracle
     from element_scan_recurrences_gb300 import workloads as wl
     w = wl.WORKLOADS[name]
     init, seqs = wl.make_inputs(w, "cuda")
@@ -277,21 +280,26 @@ def test_body_backward_full_size_sampled(name):
     G = torch.randn(states.shape, device="cuda", generator=torch.Generator("cuda").manual_seed(5))
     gi, gs = body.scan_backward(init, seqs, states, G, axis=w.axis, state_axis=w.state_axis, reverse=reverse)
     es.device_status()
-    O, T = w.shape[0], w.shape[1]
-    J = w.shape[2]
-    rng = np.random.default_rng(0)
-    jj = sorted(set([0, J - 1] + list(rng.integers(0, J, 6))))
-    for o in sorted(set([0, O - 1, int(rng.integers(0, O))])):
-        sl = (slice(o, o + 1), slice(None), jj)
-        s_seqs = [s[sl].cpu().numpy() for s in seqs]
-        s_states = states[sl].cpu().numpy()
-        s_G = G[sl].cpu().numpy()
-        s_init = init[o:o + 1][:, jj].cpu().numpy()
-        wi, ws = scan_body_backward(w.text, s_init, s_seqs, s_states, s_G, axis=1, state_axis=w.state_axis,
-                                    reverse=reverse)
-        # the vector-state kernel sums over the state as a butterfly
-        exact = name == "body_maxplus_reverse"
-        compare(gi[o:o + 1][:, jj].cpu().numpy(), wi, exact, "%s grad_initial o=%d" % (name, o))
-        for k in range(len(seqs)):
-            compare(gs[k][sl].cpu().numpy(), ws[k], exact, "%s grad seq %d o=%d" % (name, k, o))
-    del states, G, gi, gs
+    i_h, s_h = init.cpu().numpy(), [s.cpu().numpy() for s in seqs]
+    st_h, g_h = states.cpu().numpy(), G.cpu().numpy()
+    del states, G, seqs
+    got_i, got_s = gi.cpu().numpy(), [t.cpu().numpy() for t in gs]
+    del gi, gs
+    want_i = np.empty_like(got_i)
+    want_s = [np.empty_like(t) for t in got_s]
+
+    def rows(lo, hi):
+        wi, ws = scan_body_backward(w.text, i_h[lo:hi], [s[lo:hi] for s in s_h], st_h[lo:hi], g_h[lo:hi],
+                                    axis=w.axis, state_axis=w.state_axis, reverse=reverse)
+        want_i[lo:hi] = wi
+        for k in range(len(ws)):
+            want_s[k][lo:hi] = ws[k]
+    O = w.shape[0]
+    oracle.split_rows(rows, O)
+    # the vector-state kernel sums over the state in its own order
+    exact = name == "body_maxplus_reverse"
+    compare(got_i, want_i, exact, "%s grad_initial" % name)
+    step = max(1, O // 16)
+    for lo in range(0, O, step):
+        for k in range(len(got_s)):
+            compare(got_s[k][lo:lo + step], want_s[k][lo:lo + step], exact, "%s grad seq %d rows %d.." % (name, k, lo))

@@ -122,9 +122,11 @@ def test_linear_backward(shape, axis, path):
         bitwise(gb.cpu(), wb, "linear grad_b %s" % path)
 
 
-def test_delta_rule_backward_full_size_sampled():
+def test_delta_rule_backward_full_size_every_element():
     """The delta-rule workload's backward at full size in the bench's launch
-    configuration; sampled lanes checked bit for bit by the oracle."""
+    configuration; every gradient against the oracle (run on every host core
+    over contiguous blocks of the leading dimension), bit for bit."""
+    import oracle
     from element_scan_recurrences_gb300 import workloads as wl
     w = wl.MATRIX_WORKLOADS["matrix_scan_delta_rule"]
     a, b = wl.make_matrix_inputs(w, "cuda")
@@ -132,14 +134,19 @@ def test_delta_rule_backward_full_size_sampled():
     G = torch.randn(h.shape, device="cuda", generator=torch.Generator("cuda").manual_seed(3))
     ga, gb = es.matrix_scan_backward(a, b, h, G, axis=w.axis)
     es.device_status()
-    for o, j in ((0, 0), (w.lead[0] - 1, w.lead[2] - 1), (17, 5)):
-        sa = a[o:o + 1, :, j:j + 1].cpu().numpy()
-        sb = b[o:o + 1, :, j:j + 1].cpu().numpy()
-        sh = h[o:o + 1, :, j:j + 1].cpu().numpy()
-        sg = G[o:o + 1, :, j:j + 1].cpu().numpy()
-        wa, wb = M.matrix_scan_backward(sa, sb, sh, sg, axis=1)
-        bitwise(ga[o:o + 1, :, j:j + 1].cpu(), wa, "grad_a lane (%d, %d)" % (o, j))
-        bitwise(gb[o:o + 1, :, j:j + 1].cpu(), wb, "grad_b lane (%d, %d)" % (o, j))
+    ah, bh, hh, gh = a.cpu().numpy(), b.cpu().numpy(), h.cpu().numpy(), G.cpu().numpy()
+    del a, b, h, G
+    got_a, got_b = ga.cpu().numpy(), gb.cpu().numpy()
+    del ga, gb
+    want_a, want_b = np.empty_like(got_a), np.empty_like(got_b)
+
+    def rows(lo, hi):
+        want_a[lo:hi], want_b[lo:hi] = M.matrix_scan_backward(ah[lo:hi], bh[lo:hi], hh[lo:hi], gh[lo:hi],
+                                                              axis=w.axis)
+    oracle.split_rows(rows, w.lead[0])
+    for lo in range(0, w.lead[0], 8):
+        bitwise(got_a[lo:lo + 8], want_a[lo:lo + 8], "grad_a rows %d.." % lo)
+        bitwise(got_b[lo:lo + 8], want_b[lo:lo + 8], "grad_b rows %d.." % lo)
 
 
 def spectral(rng, lead, n, norm=0.97):
