@@ -83,6 +83,7 @@ CASES = [
     ("lane_tma", wl.custom(T_, (40, 70, 1000), 1, name="tanh_lane_staged")),
     ("lane_tma", wl.custom(M_, (40, 45, 1000), 1, name="maxplus_lane_staged", **MAXPLUS_DISTS)),
     ("lane_tma", wl.custom(T_, (200, 37, 40), 1, name="tanh_lane_staged_32")),
+    ("lane_tma", wl.custom(M_, (150, 40, 100), 1, name="maxplus_lane_staged_64", **MAXPLUS_DISTS)),
     ("lane_tma", wl.custom(T_, (4, 19, 8, 16), 1, state_axis=True, seq_widths=(16, 16), name="tanh_vec_full")),
     ("generic", wl.custom(T_, (5, 7, 3), 0, name="tanh_generic")),
     ("generic", wl.custom(M_, (5, 7, 3), 2, name="maxplus_generic", **MAXPLUS_DISTS)),
