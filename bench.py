@@ -1122,9 +1122,10 @@ def run_ours_op(args, w):
         elif w.kind != "linear":
             roofline["kernel"] = "k_mat_%s (transposed) + k_mat_da" % ("tma" if plans[0]["path"] == "mat_tma"
                                                                       else "generic")
-            roofline["note"] = ("a call of two launches timed as one: the cotangent scan on a's transposes, then "
-                                "grad_a from the cotangent and the saved states; the cotangent is written and read "
-                                "again, so its DRAM traffic is about (2n^2 + 4nm) / (2n^2 + 3nm) of the "
+            roofline["note"] = ("a call timed as one: the cotangent scan on a's transposes and grad_a from the "
+                                "cotangent and the saved states (on the TMA path in windows of trips, each window's "
+                                "grad_a beside the next scan window on a second stream); the cotangent is written "
+                                "and read again, so its DRAM traffic is about (2n^2 + 4nm) / (2n^2 + 3nm) of the "
                                 "algorithmic bytes")
     else:
         kernel = job.kernels.get(plans[0]["path"], plans[0]["path"])

@@ -31,6 +31,11 @@ struct MatLaunch {
     int a_shift;
     MatGeom g;           // any layout (generic kernel)
     int64_t O, T, J;     // dense canonical view [O, T, J] of the leading dims (TMA kernel)
+    // TMA full scan only: the trips [win0, win0 + win_len) of the axis (0
+    // length: all of it), started from the states at `carry` (the dense
+    // [O, J] view of one trip of `out`; null: from zero)
+    int64_t win0 = 0, win_len = 0;
+    const float* carry = nullptr;
     unsigned int* status;
     uint64_t wait_ns;
     int64_t drop_tile;
@@ -42,9 +47,10 @@ struct MatLaunch {
 cudaError_t launch_mat_generic(const MatLaunch& L);
 
 // da[t] = lam[t] @ h_prev^T over the dense view [O, T, J] of n x m blocks
-// (h_prev: the state before trip t in scan order, zero before the first).
+// (h_prev: the state before trip t in scan order, zero before the first), for
+// the trips [t_lo, t_lo + t_cnt) (t_cnt < 0: all of them).
 cudaError_t launch_mat_da(const float* lam, const float* states, float* da, int n, int64_t O, int64_t T,
-                          int64_t J, int m, int reverse, cudaStream_t stream);
+                          int64_t J, int m, int reverse, cudaStream_t stream, int64_t t_lo = 0, int64_t t_cnt = -1);
 cudaError_t launch_mat_tma(const MatLaunch& L, const char** err);
 
 // The chunked scan for few long lanes (three launches, a caller workspace):

@@ -8,6 +8,7 @@
 // one before the matrices); the result is that shape + [n, m].  linear-scan
 // takes a and b broadcast to one shape, numbers included: the same scan over
 // one-by-one matrices.  Shape errors are E-DIM-001.
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -21,6 +22,12 @@
 // but is no device address; the address comes from cudaGetSymbolAddress, once
 // per device, with that device current.
 static __device__ __align__(256) unsigned char g_es_static_scratch[ES_STATIC_SCRATCH_BYTES];
+
+// Tuning override: trip windows of a matrix-scan gradient on the TMA path (1:
+// one cotangent launch, then one da launch).
+#ifndef ES_MAT_BWD_WINDOWS
+#define ES_MAT_BWD_WINDOWS 8
+#endif
 
 namespace es {
 namespace {
@@ -375,14 +382,97 @@ es_status plan_matrix_backward_ws(const char* fn, MatBwdPlan* Q, const float* b,
     return ES_OK;
 }
 
+// The two launches of the gradient overlap in windows of trips.  The
+// cotangent scan is bound by its chain and leaves bandwidth that the da
+// kernel, bound by bandwidth, can use: the scan runs window by window on the
+// caller's stream (each window started from the states the previous one left
+// next to it), and each window's da runs on a library-owned stream as soon as
+// its scan window is done, beside the next scan window.  Same operations in
+// the same order as one scan then one da launch, so the same bits.
+constexpr int kBwdWindows = ES_MAT_BWD_WINDOWS;
+constexpr int kBwdDevices = 64;
+
+struct BwdPipe {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    cudaStream_t side = nullptr;
+    cudaEvent_t scanned[kBwdWindows > 1 ? kBwdWindows : 1] = {};
+    cudaEvent_t done = nullptr;
+    std::mutex mu;        // one call at a time enqueues on the side stream
+};
+BwdPipe g_bwd[kBwdDevices];
+
+cudaError_t bwd_pipe_init(BwdPipe* p) {
+    cudaError_t e = cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking);
+    for (int k = 0; k < kBwdWindows && e == cudaSuccess; ++k)
+        e = cudaEventCreateWithFlags(&p->scanned[k], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming);
+    return e;
+}
+
+// windows for a gradient: the TMA scan with at least 128 trips a window
+int bwd_windows(const MatPlan& P) {
+    if (P.path != ES_PATH_MAT_TMA || kBwdWindows < 2) return 1;
+    const int64_t k = P.L.T / 128;
+    return static_cast<int>(k < 2 ? 1 : k > kBwdWindows ? kBwdWindows : k);
+}
+
 es_status launch_matrix_backward(const char* fn, MatBwdPlan* Q, int reverse, cudaStream_t stream) {
-    es_status st = launch_matrix(fn, &Q->P, stream);
+    const int K = bwd_windows(Q->P);
+    if (K <= 1) {
+        es_status st = launch_matrix(fn, &Q->P, stream);
+        if (st != ES_OK) return st;
+        const MatLaunch& L = Q->P.L;
+        cudaError_t e = launch_mat_da(L.out, Q->states, Q->grad_a, L.n, L.O, L.T, L.J, L.m, reverse ? 1 : 0, stream);
+        if (e != cudaSuccess) return api_fail(ES_E_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+        count_launch();
+        return ES_OK;
+    }
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    es_status st = api_device(&dev, &ds);
     if (st != ES_OK) return st;
-    const MatLaunch& L = Q->P.L;
-    cudaError_t e = launch_mat_da(L.out, Q->states, Q->grad_a, L.n, L.O, L.T, L.J, L.m, reverse ? 1 : 0, stream);
-    if (e != cudaSuccess) return api_fail(ES_E_CUDA, "%s: %s", fn, cudaGetErrorString(e));
-    count_launch();
-    return ES_OK;
+    if (dev >= kBwdDevices) return api_fail(ES_E_CUDA, "%s: device %d beyond the library's table", fn, dev);
+    BwdPipe* p = &g_bwd[dev];
+    std::call_once(p->once, [p]() { p->err = bwd_pipe_init(p); });
+    if (p->err != cudaSuccess) return api_fail(ES_E_CUDA, "%s: %s", fn, cudaGetErrorString(p->err));
+    std::lock_guard<std::mutex> lock(p->mu);
+    auto check = [&](cudaError_t e) -> es_status {
+        return e == cudaSuccess ? ES_OK : api_fail(ES_E_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+    };
+    MatLaunch& L = Q->P.L;
+    L.status = ds->status;
+    L.wait_ns = api_wait_ns();
+    L.drop_tile = api_drop_tile();
+    L.stream = stream;
+    L.num_sms = ds->num_sms;
+    if ((st = api_encoder(&L.encode)) != ES_OK) return st;
+    const int64_t T = L.T, span = (T + K - 1) / K;
+    const int64_t trip_floats = L.J * L.n * L.m;      // one trip of the dense [O, T, J] view
+    // the cotangent runs descending for a forward scan's gradient
+    const bool desc = L.reverse != 0;
+    for (int w = 0; w < K; ++w) {
+        const int64_t t1 = desc ? T - w * span : std::min<int64_t>(T, (w + 1) * span);
+        const int64_t t0 = desc ? std::max<int64_t>(0, t1 - span) : w * span;
+        if (t1 <= t0) break;
+        MatLaunch Lw = L;
+        Lw.win0 = t0;
+        Lw.win_len = t1 - t0;
+        const int64_t tc = desc ? t1 : t0 - 1;            // the trip whose states start this window
+        Lw.carry = (tc >= 0 && tc < T) ? L.out + tc * trip_floats : nullptr;
+        const char* msg = nullptr;
+        cudaError_t e = launch_mat_tma(Lw, &msg);
+        if (e != cudaSuccess) return api_fail(ES_E_CUDA, "%s: %s", fn, msg != nullptr ? msg : cudaGetErrorString(e));
+        count_launch();
+        if ((st = check(cudaEventRecord(p->scanned[w], stream))) != ES_OK) return st;
+        if ((st = check(cudaStreamWaitEvent(p->side, p->scanned[w], 0))) != ES_OK) return st;
+        e = launch_mat_da(L.out, Q->states, Q->grad_a, L.n, L.O, T, L.J, L.m, reverse ? 1 : 0, p->side, t0, t1 - t0);
+        if ((st = check(e)) != ES_OK) return st;
+        count_launch();
+    }
+    // later work on the caller's stream waits for the last da window
+    if ((st = check(cudaEventRecord(p->done, p->side))) != ES_OK) return st;
+    return check(cudaStreamWaitEvent(stream, p->done, 0));
 }
 
 }  // namespace

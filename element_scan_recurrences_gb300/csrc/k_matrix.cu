@@ -251,8 +251,8 @@ template <int N, int R, bool PROJ, bool TRANS, int MODE>
 __global__ void __launch_bounds__(32 + kMatConsumers, 1)
 k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
           float* __restrict__ out, float* __restrict__ ws, int T, int J, int m, int gp, int LPC, int tiles_j, int TT,
-          int stages, int reverse, int a_shift, int chunks, int chunk, int chunk_off, unsigned int* status,
-          uint64_t wait_ns, int64_t drop_tile) {
+          int stages, int reverse, int a_shift, int chunks, int chunk, int chunk_off, int win0, int win_len,
+          const float* __restrict__ carry, unsigned int* status, uint64_t wait_ns, int64_t drop_tile) {
     constexpr bool kChunk = MODE != kMatFull;
     constexpr bool kIdent = PROJ || MODE == kMatLocal;     // columns that carry a product from the identity
     static_assert(!(PROJ && TRANS), "a projective scan has no gradient");
@@ -288,7 +288,10 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
         jj = (blockIdx.x % tiles_j) * LPC;
         c0 = 0;
     }
-    const int span = kChunk ? chunk : T;                   // trips a CTA lane scans
+    // trips a CTA lane scans: a chunk, or (full scan) the window [win0,
+    // win0 + win_len) of the axis, the whole axis unless the scan is cut into
+    // windows
+    const int span = kChunk ? chunk : win_len;
     const int ntiles = (span + TT - 1) / TT;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -331,8 +334,8 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
                         tma_load_4d(st + a_pad + l * lb, &map_b, 0, jj, ct, o, &full_bar[s], pol);
                     }
                 } else {
-                    tma_load_4d(st, &map_a, 0, jj, jt * TT + a_shift, o, &full_bar[s], pol);
-                    tma_load_4d(st + a_pad, &map_b, 0, jj, jt * TT, o, &full_bar[s], pol);
+                    tma_load_4d(st, &map_a, 0, jj, win0 + jt * TT + a_shift, o, &full_bar[s], pol);
+                    tma_load_4d(st + a_pad, &map_b, 0, jj, win0 + jt * TT, o, &full_bar[s], pol);
                 }
             }
             for (int k = max(0, issued - stages); k < issued; ++k) {
@@ -367,9 +370,17 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
     // the column's whole state (every row), the same in all its row groups
     float h[N];
     if constexpr (MODE == kMatFinal) {
-        const float* carry = ws + unit * unit_floats + N * N + N * m;
+        const float* cin = ws + unit * unit_floats + N * N + N * m;
 #pragma unroll
-        for (int i = 0; i < N; ++i) h[i] = (valid && is_h) ? carry[i * m + c] : 0.0f;
+        for (int i = 0; i < N; ++i) h[i] = (valid && is_h) ? cin[i * m + c] : 0.0f;
+    } else if constexpr (MODE == kMatFull) {
+        // a window after the first starts from the state the previous window
+        // left at the trip next to it (`carry` points at that trip's states)
+        const float* cin = carry != nullptr ? carry + (static_cast<int64_t>(o) * T * J + jj + l) * lane_block + c
+                                            : nullptr;
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            h[i] = (cin != nullptr && valid && is_h) ? cin[i * m] : (is_p && i == c - m) ? 1.0f : 0.0f;
     } else {
 #pragma unroll
         for (int i = 0; i < N; ++i) h[i] = (is_p && i == c - m) ? 1.0f : 0.0f;
@@ -394,7 +405,7 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
             // columns past m (a product's) read no b: their pointer stays in the block
             const float* B = (kChunk ? sb + l * lb + tt * (N * m) : sb + (static_cast<uint32_t>(tt) * LPC + l) * (N * m)) +
                              (is_h ? c : 0);
-            const int64_t t = kChunk ? tbase + t0 + tt : t0 + tt;
+            const int64_t t = kChunk ? tbase + t0 + tt : win0 + t0 + tt;
             const bool live = !kChunk || (t >= 0 && t < T);
             if constexpr (kChunk && TRANS) {
                 // the chunked passes: row i of a^T h + b as one fused sum
@@ -529,25 +540,42 @@ k_mat_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
 // m is a multiple of 4); the rows a unit's threads share meet in L1.  MC > 0
 // is m known at compile time: the loop over k unrolls and every load of the
 // unit can be in flight at once.
+// Unit v of a window of trips [t_lo, t_lo + t_cnt) of the dense view
+// [O, T, J]: its index u in the whole view and its trip t (32-bit divisions
+// while the view's units fit).
+__device__ __forceinline__ void window_unit(int64_t v, int64_t T, int64_t J, int64_t t_lo, int64_t t_cnt, bool small,
+                                            int64_t* u, int64_t* t) {
+    const int64_t per_o = t_cnt * J;
+    int64_t ob, r, tr;
+    if (small) {
+        ob = static_cast<uint32_t>(v) / static_cast<uint32_t>(per_o);
+        r = v - ob * per_o;
+        tr = static_cast<uint32_t>(r) / static_cast<uint32_t>(J);
+    } else {
+        ob = v / per_o;
+        r = v - ob * per_o;
+        tr = r / J;
+    }
+    *u = (ob * T + t_lo) * J + r;
+    *t = t_lo + tr;
+}
+
 template <int N, int B, int KV, int MC>
 __global__ void __launch_bounds__(128)
 k_mat_da(const float* __restrict__ lam, const float* __restrict__ states, float* __restrict__ da, int64_t O,
-         int64_t T, int64_t J, int m_rt, int reverse) {
+         int64_t T, int64_t J, int m_rt, int reverse, int64_t t_lo, int64_t t_cnt) {
     const int m = MC > 0 ? MC : m_rt;
     constexpr int NB = N / B;
     constexpr int TPU = NB * NB;                 // threads per unit
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t u = tid / TPU;
-    const int64_t units = O * T * J;
-    if (u >= units) return;
+    const int64_t v = tid / TPU;
+    if (v >= O * t_cnt * J) return;
     const int w = static_cast<int>(tid % TPU);
     const int bi = w / NB, bj = w % NB;
-    // the unit's trip t (the state before it is unit u - J, or u + J in
-    // reverse); 32-bit division while the units fit
-    const int64_t t = units < (int64_t(1) << 31)
-                          ? static_cast<int64_t>((static_cast<uint32_t>(u) / static_cast<uint32_t>(J)) %
-                                                 static_cast<uint32_t>(T))
-                          : (u / J) % T;
+    // the unit u of the whole view and its trip t (the state before it is
+    // unit u - J, or u + J in reverse)
+    int64_t u, t;
+    window_unit(v, T, J, t_lo, t_cnt, O * T * J < (int64_t(1) << 31), &u, &t);
     const bool has_prev = reverse ? t + 1 < T : t > 0;
     const float* Lr = lam + (u * N + bi * B) * m;
     const float* Hr = states + ((has_prev ? (reverse ? u + J : u - J) : u) * N + bj * B) * m;
@@ -650,16 +678,14 @@ __device__ __forceinline__ int da16_off(int row, int chunk) {
 
 __global__ void __launch_bounds__(32 * kDa16Warps)
 k_mat_da16(const float* __restrict__ lam, const float* __restrict__ states, float* __restrict__ da, int64_t units,
-           int64_t T, int64_t J, int reverse) {
+           int64_t T, int64_t J, int reverse, int64_t t_lo, int64_t t_cnt, bool small) {
     __shared__ __align__(16) float sm[kDa16Warps][2][256];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t u = static_cast<int64_t>(blockIdx.x) * kDa16Warps + warp;
-    if (u >= units) return;   // the whole warp
-    const int64_t t = units < (int64_t(1) << 31)
-                          ? static_cast<int64_t>((static_cast<uint32_t>(u) / static_cast<uint32_t>(J)) %
-                                                 static_cast<uint32_t>(T))
-                          : (u / J) % T;
+    const int64_t v = static_cast<int64_t>(blockIdx.x) * kDa16Warps + warp;
+    if (v >= units) return;   // the whole warp
+    int64_t u, t;
+    window_unit(v, T, J, t_lo, t_cnt, small, &u, &t);
     const bool has_prev = reverse ? t + 1 < T : t > 0;
     const float4* L4 = reinterpret_cast<const float4*>(lam + u * 256);
     const float4* H4 = reinterpret_cast<const float4*>(states + (has_prev ? (reverse ? u + J : u - J) : u) * 256);
@@ -705,12 +731,13 @@ k_mat_da16(const float* __restrict__ lam, const float* __restrict__ states, floa
 
 template <int N>
 cudaError_t launch_da_n(const float* lam, const float* states, float* da, int64_t O, int64_t T, int64_t J, int m,
-                        int reverse, cudaStream_t stream) {
-    const int64_t units = O * T * J;
+                        int reverse, int64_t t_lo, int64_t t_cnt, cudaStream_t stream) {
+    const int64_t units = O * t_cnt * J;
+    if (units == 0) return cudaSuccess;
     auto go = [&](auto kern, int tpu) {
         const int64_t blocks = (units * tpu + 127) / 128;
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-        kern<<<static_cast<unsigned>(blocks), 128, 0, stream>>>(lam, states, da, O, T, J, m, reverse);
+        kern<<<static_cast<unsigned>(blocks), 128, 0, stream>>>(lam, states, da, O, T, J, m, reverse, t_lo, t_cnt);
         return cudaGetLastError();
     };
     const bool vec = m % 4 == 0 && reinterpret_cast<uintptr_t>(lam) % 16 == 0 &&
@@ -719,8 +746,8 @@ cudaError_t launch_da_n(const float* lam, const float* states, float* da, int64_
         if (m == 16 && vec && reinterpret_cast<uintptr_t>(da) % 16 == 0) {
             const int64_t blocks = (units + kDa16Warps - 1) / kDa16Warps;
             if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-            k_mat_da16<<<static_cast<unsigned>(blocks), 32 * kDa16Warps, 0, stream>>>(lam, states, da, units, T, J,
-                                                                                     reverse);
+            k_mat_da16<<<static_cast<unsigned>(blocks), 32 * kDa16Warps, 0, stream>>>(
+                lam, states, da, units, T, J, reverse, t_lo, t_cnt, O * T * J < (int64_t(1) << 31));
             return cudaGetLastError();
         }
     }
@@ -756,10 +783,14 @@ cudaError_t launch_generic_n(const MatLaunch& L) {
     return cudaGetLastError();
 }
 
-// the chunk modes' extra arguments (unused by a full scan)
+// the chunk modes' extra arguments (unused by a full scan), and the full
+// scan's window of the axis with the state it starts from (unused by the
+// chunk modes)
 struct MatChunkArgs {
     float* ws;
     int chunks, chunk, chunk_off;
+    int win0, win_len;
+    const float* carry;
 };
 
 template <int N, int R, int MODE>
@@ -774,7 +805,8 @@ cudaError_t launch_tma_nr(const MatLaunch& L, const CUtensorMap& ma, const CUten
     const int64_t grid = (MODE != kMatFull ? L.g.lanes : L.O) * tiles_j;
     kern<<<static_cast<unsigned>(grid), 32 + lpc * gp * R, smem, L.stream>>>(
         ma, mb, L.out, C.ws, static_cast<int>(L.T), static_cast<int>(L.J), L.m, gp, lpc, tiles_j, TT, stages,
-        L.reverse, L.trans ? L.a_shift : 0, C.chunks, C.chunk, C.chunk_off, L.status, L.wait_ns, L.drop_tile);
+        L.reverse, L.trans ? L.a_shift : 0, C.chunks, C.chunk, C.chunk_off, C.win0, C.win_len, C.carry, L.status,
+        L.wait_ns, L.drop_tile);
     return cudaGetLastError();
 }
 
@@ -846,10 +878,11 @@ bool encode_blocks(EncodeTiledFn encode, CUtensorMap* map, const float* base, in
 }  // namespace
 
 cudaError_t launch_mat_da(const float* lam, const float* states, float* da, int n, int64_t O, int64_t T,
-                          int64_t J, int m, int reverse, cudaStream_t stream) {
+                          int64_t J, int m, int reverse, cudaStream_t stream, int64_t t_lo, int64_t t_cnt) {
+    if (t_cnt < 0) t_cnt = T;
     switch (n) {
 #define ES_DA_CASE(K) \
-    case K: return launch_da_n<K>(lam, states, da, O, T, J, m, reverse, stream);
+    case K: return launch_da_n<K>(lam, states, da, O, T, J, m, reverse, t_lo, t_cnt, stream);
         ES_DA_CASE(1) ES_DA_CASE(2) ES_DA_CASE(3) ES_DA_CASE(4) ES_DA_CASE(5) ES_DA_CASE(6) ES_DA_CASE(7)
         ES_DA_CASE(8) ES_DA_CASE(9) ES_DA_CASE(10) ES_DA_CASE(11) ES_DA_CASE(12) ES_DA_CASE(13)
         ES_DA_CASE(14) ES_DA_CASE(15) ES_DA_CASE(16)
@@ -888,7 +921,9 @@ cudaError_t launch_mat_tma(const MatLaunch& L, const char** err) {
     const int n = L.n, m = L.m;
     int R = 0, LPC = 0, TT = 0;
     mat_tile_shape(n, m, L.gp, &R, &LPC, &TT);
-    const int stages = 3;
+    // a scan cut into windows shares the SMs with the grad_a windows: two
+    // stages leave them room (delta-rule gradient 1.082 -> 1.062 ms on GB300)
+    const int stages = L.win_len > 0 ? 2 : 3;
     const int64_t tiles_j = (L.J + LPC - 1) / LPC;
     CUtensorMap ma, mb;
     if (!encode_blocks(L.encode, &ma, L.a, static_cast<int64_t>(n) * n, L.J, L.T, L.O, LPC, TT) ||
@@ -898,7 +933,8 @@ cudaError_t launch_mat_tma(const MatLaunch& L, const char** err) {
     }
     const size_t smem = static_cast<size_t>(stages) * mat_stage_floats(n, m, LPC, TT, false) * 4 + 1024;
     return launch_tma_mode<kMatFull>(L, ma, mb, L.gp, R, LPC, static_cast<int>(tiles_j), TT, stages, smem,
-                                     MatChunkArgs{nullptr, 0, 0, 0});
+                                     MatChunkArgs{nullptr, 0, 0, 0, static_cast<int>(L.win0),
+                                                  static_cast<int>(L.win_len > 0 ? L.win_len : L.T), L.carry});
 }
 
 
@@ -1139,7 +1175,7 @@ cudaError_t launch_chunked_tma_n(const MatLaunch& L, float* ws, int64_t chunks, 
     const int m = L.m;
     const int stages = 3;
     MatChunkArgs C{ws, static_cast<int>(chunks), static_cast<int>(chunk),
-                   static_cast<int>(L.reverse ? chunks * chunk - L.T : 0)};
+                   static_cast<int>(L.reverse ? chunks * chunk - L.T : 0), 0, static_cast<int>(L.T), nullptr};
     // pass 1 carries the m state columns and the product's N; pass 3 the m
     int gp1 = 1;
     while (gp1 < m + N) gp1 <<= 1;

@@ -512,7 +512,12 @@ es_status es_plan_linear_scan_f32(const float *a, const int64_t *a_shape, int a_
  *   grad_out         device f32 of the output's shape.
  *   grad_a, grad_b   device f32 of a's and b's shapes (written); they may
  *                    not overlap any input or each other (ES_E_ARG).
- * Two kernels on `stream` (the cotangent scan, then grad_a); no allocation.
+ * Two kernels: the cotangent scan, then grad_a.  On the TMA path with at
+ * least 256 trips both run in up to eight windows of trips, the scan windows
+ * on `stream` and each window's grad_a on a library-owned stream per device
+ * (created on first use, ordered after its scan window by an event) so that
+ * it overlaps the next scan window; later work on `stream` waits for all of
+ * it.  The results are the same bits either way.  No device allocation.
  */
 es_status es_matrix_scan_backward_f32(const float *a, const int64_t *a_shape, int a_rank,
                                       const float *b, const int64_t *b_shape, int b_rank,

@@ -89,6 +89,51 @@ def test_matrix_backward_trip_counts(T):
         bitwise(got[1], want[1], "grad_b T=%d" % T)
 
 
+@pytest.mark.parametrize("reverse", [False, True], ids=["fwd", "rev"])
+@pytest.mark.parametrize("n,m,lead", [(16, 16, (2, 1000, 3)), (4, 4, (3, 300, 2)), (8, 8, (1, 777, 5)),
+                                      (16, 4, (2, 256, 4))])
+def test_matrix_backward_windows(n, m, lead, reverse):
+    """Enough trips that the gradient runs in windows of trips (the scan
+    windows started from the states their neighbours left, the grad_a windows
+    on the library's second stream): the same bits as the gradient oracle,
+    with ragged last windows."""
+    rng = np.random.default_rng(n * 7 + lead[1])
+    a = contractive(rng, lead, n)
+    b = rng.standard_normal(tuple(lead) + (n, m)).astype(np.float32)
+    assert es.plan_matrix_scan_backward(a.shape, b.shape, 1, reverse)["path"] == "mat_tma"
+    got, want = run_pair(a, b, 1, reverse, "auto", 11)
+    bitwise(got[0], want[0], "grad_a windows n=%d m=%d T=%d" % (n, m, lead[1]))
+    bitwise(got[1], want[1], "grad_b windows n=%d m=%d T=%d" % (n, m, lead[1]))
+
+
+def test_matrix_backward_windows_on_a_side_stream():
+    """Work queued on the caller's stream after a windowed gradient sees all
+    of it (the library's stream joins back), on a non-default stream, twice in
+    a row into the same buffers."""
+    rng = np.random.default_rng(5)
+    lead, n, m = (2, 640, 4), 16, 16
+    a = contractive(rng, lead, n)
+    b = rng.standard_normal(tuple(lead) + (n, m)).astype(np.float32)
+    states = M.matrix_scan(a, b, axis=1)
+    G = rng.standard_normal(states.shape).astype(np.float32)
+    wa, wb = M.matrix_scan_backward(a, b, states, G, axis=1)
+    d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    da_, db_, ds_, dg_ = d(a), d(b), d(states), d(G)
+    ga, gb = torch.empty_like(da_), torch.empty_like(db_)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            ga.fill_(float("nan"))
+            gb.fill_(float("nan"))
+            es.matrix_scan_backward(da_, db_, ds_, dg_, axis=1, grads=(ga, gb), stream=side)
+            ca, cb = ga.clone(), gb.clone()        # queued on the same stream right after
+    side.synchronize()
+    es.device_status()
+    bitwise(ca.cpu(), wa, "grad_a after the join")
+    bitwise(cb.cpu(), wb, "grad_b after the join")
+
+
 def test_matrix_backward_refusals():
     a = torch.rand(2, 7, 4, 4, device="cuda")
     b = torch.rand(2, 7, 4, 2, device="cuda")
