@@ -1125,8 +1125,8 @@ def run_ours_op(args, w):
             roofline["note"] = ("a call timed as one: the cotangent scan on a's transposes and grad_a from the "
                                 "cotangent and the saved states (on the TMA path in windows of trips, each window's "
                                 "grad_a beside the next scan window on a second stream); the cotangent is written "
-                                "and read again, so its DRAM traffic is about (2n^2 + 4nm) / (2n^2 + 3nm) of the "
-                                "algorithmic bytes")
+                                "and read again, so its DRAM traffic is up to (2n^2 + 4nm) / (2n^2 + 3nm) of the "
+                                "algorithmic bytes, less where a window's cotangent is read back from L2")
     else:
         kernel = job.kernels.get(plans[0]["path"], plans[0]["path"])
         roofline = roofline_of(kernel, w.name, w.algorithmic_bytes(), kernel_ms)
