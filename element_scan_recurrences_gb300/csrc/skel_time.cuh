@@ -152,7 +152,18 @@ k_body_time(const __grid_constant__ TmaMaps<Body::kNS + 1> maps, const float* __
             // the input stage is free as soon as the segment sits in registers
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[s]);
-            if (!reverse) {
+            // full tiles run unguarded (one basic block, so the quads' loads,
+            // stores and address arithmetic overlap the chain); only a ragged
+            // last tile checks every quad
+            if (nq == kTimeTT / 4) {
+                if (!reverse) {
+#pragma unroll
+                    for (int q = 0; q < kTimeTT / 4; ++q) quad(q, seg[q], false);
+                } else {
+#pragma unroll
+                    for (int q = kTimeTT / 4 - 1; q >= 0; --q) quad(q, seg[q], true);
+                }
+            } else if (!reverse) {
 #pragma unroll
                 for (int q = 0; q < kTimeTT / 4; ++q)
                     if (q < nq) quad(q, seg[q], false);

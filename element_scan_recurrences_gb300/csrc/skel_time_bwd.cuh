@@ -191,22 +191,43 @@ k_body_time_bwd(const __grid_constant__ TmaMaps<2 * Body::kNS + 2> maps, const f
         };
         // groups past T in a ragged tile (zero-filled) must not touch the
         // cotangent; the TMA store clips them
+        // (full tiles run unguarded: one basic block, so the next group's
+        // reads and this group's stores overlap the chain)
         Quad cur, nxt;
+        const bool full = nq == kTimeBwdTT / 4;
         if (!reverse) {
             readq(kTimeBwdTT / 4 - 1, cur);
+            if (full) {
 #pragma unroll
-            for (int q = kTimeBwdTT / 4 - 1; q >= 0; --q) {
-                if (q > 0) readq(q - 1, nxt);
-                if (q < nq) quad(q, cur);
-                cur = nxt;
+                for (int q = kTimeBwdTT / 4 - 1; q >= 0; --q) {
+                    if (q > 0) readq(q - 1, nxt);
+                    quad(q, cur);
+                    cur = nxt;
+                }
+            } else {
+#pragma unroll
+                for (int q = kTimeBwdTT / 4 - 1; q >= 0; --q) {
+                    if (q > 0) readq(q - 1, nxt);
+                    if (q < nq) quad(q, cur);
+                    cur = nxt;
+                }
             }
         } else {
             readq(0, cur);
+            if (full) {
 #pragma unroll
-            for (int q = 0; q < kTimeBwdTT / 4; ++q) {
-                if (q + 1 < kTimeBwdTT / 4) readq(q + 1, nxt);
-                if (q < nq) quad(q, cur);
-                cur = nxt;
+                for (int q = 0; q < kTimeBwdTT / 4; ++q) {
+                    if (q + 1 < kTimeBwdTT / 4) readq(q + 1, nxt);
+                    quad(q, cur);
+                    cur = nxt;
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < kTimeBwdTT / 4; ++q) {
+                    if (q + 1 < kTimeBwdTT / 4) readq(q + 1, nxt);
+                    if (q < nq) quad(q, cur);
+                    cur = nxt;
+                }
             }
         }
         // every operand of the stage has been read

@@ -222,23 +222,45 @@ k_body_vec(const __grid_constant__ TmaMaps<Body::kNS> maps, const __grid_constan
         };
         // the next trip's operands are read while a trip runs; rows past the
         // valid trips of a ragged tile hold TMA's zero fill and are not used
+        // (full tiles run unguarded: one basic block, so the loads and stores
+        // of neighbouring trips overlap the chain)
         if (!reverse) {
             load(0, aw, an);
+            if (n == TT) {
 #pragma unroll
-            for (int tt = 0; tt < TT; tt += 2) {
-                load(tt + 1, bw, bn);
-                if (tt < n) trip(tt, aw, an);
-                if (tt + 2 < TT) load(tt + 2, aw, an);
-                if (tt + 1 < n) trip(tt + 1, bw, bn);
+                for (int tt = 0; tt < TT; tt += 2) {
+                    load(tt + 1, bw, bn);
+                    trip(tt, aw, an);
+                    if (tt + 2 < TT) load(tt + 2, aw, an);
+                    trip(tt + 1, bw, bn);
+                }
+            } else {
+#pragma unroll
+                for (int tt = 0; tt < TT; tt += 2) {
+                    load(tt + 1, bw, bn);
+                    if (tt < n) trip(tt, aw, an);
+                    if (tt + 2 < TT) load(tt + 2, aw, an);
+                    if (tt + 1 < n) trip(tt + 1, bw, bn);
+                }
             }
         } else {
             load(TT - 1, aw, an);
+            if (n == TT) {
 #pragma unroll
-            for (int tt = TT - 1; tt >= 0; tt -= 2) {
-                load(tt - 1, bw, bn);
-                if (tt < n) trip(tt, aw, an);
-                if (tt - 2 >= 0) load(tt - 2, aw, an);
-                if (tt - 1 < n) trip(tt - 1, bw, bn);
+                for (int tt = TT - 1; tt >= 0; tt -= 2) {
+                    load(tt - 1, bw, bn);
+                    trip(tt, aw, an);
+                    if (tt - 2 >= 0) load(tt - 2, aw, an);
+                    trip(tt - 1, bw, bn);
+                }
+            } else {
+#pragma unroll
+                for (int tt = TT - 1; tt >= 0; tt -= 2) {
+                    load(tt - 1, bw, bn);
+                    if (tt < n) trip(tt, aw, an);
+                    if (tt - 2 >= 0) load(tt - 2, aw, an);
+                    if (tt - 1 < n) trip(tt - 1, bw, bn);
+                }
             }
         }
         // the last trip of the tile: n - 1 forward, 0 in reverse
