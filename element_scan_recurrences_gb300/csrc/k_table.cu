@@ -322,16 +322,23 @@ k_table_time(const __grid_constant__ CUtensorMap map_s, const __grid_constant__ 
         for (int q = 0; q < 8; ++q) seg[q] = *reinterpret_cast<const int4*>(srow + ((static_cast<uint32_t>(q) ^ swz) << 4));
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
+        auto quad = [&](const int q) {
+            int4 v;
+            v.x = table_step<TAB>(off, clamp_symbol(seg[q].x, n_syms), ts, table, n_syms, hi, sh);
+            v.y = table_step<TAB>(off, clamp_symbol(seg[q].y, n_syms), ts, table, n_syms, hi, sh);
+            v.z = table_step<TAB>(off, clamp_symbol(seg[q].z, n_syms), ts, table, n_syms, hi, sh);
+            v.w = table_step<TAB>(off, clamp_symbol(seg[q].w, n_syms), ts, table, n_syms, hi, sh);
+            *reinterpret_cast<int4*>(orow + ((static_cast<uint32_t>(q) ^ swz) << 4)) = v;
+        };
+        // full tiles run unguarded (one basic block); only a ragged last tile
+        // checks every group of four trips
+        if (nq == 8) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            if (q < nq) {
-                int4 v;
-                v.x = table_step<TAB>(off, clamp_symbol(seg[q].x, n_syms), ts, table, n_syms, hi, sh);
-                v.y = table_step<TAB>(off, clamp_symbol(seg[q].y, n_syms), ts, table, n_syms, hi, sh);
-                v.z = table_step<TAB>(off, clamp_symbol(seg[q].z, n_syms), ts, table, n_syms, hi, sh);
-                v.w = table_step<TAB>(off, clamp_symbol(seg[q].w, n_syms), ts, table, n_syms, hi, sh);
-                *reinterpret_cast<int4*>(orow + ((static_cast<uint32_t>(q) ^ swz) << 4)) = v;
-            }
+            for (int q = 0; q < 8; ++q) quad(q);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q < nq) quad(q);
         }
     }
     if (storer) bulk_wait_all();
