@@ -264,7 +264,8 @@ def test_body_backward_rejects_overlap_on_device():
     assert e.value.status == 3
 
 
-@pytest.mark.parametrize("name", ["body_tanh_decay_lanes", "body_normcap_vector", "body_maxplus_reverse"])
+@pytest.mark.parametrize("name", ["body_tanh_decay_lanes", "body_normcap_vector", "body_maxplus_reverse",
+                                  "body_gated_lanes", "body_tanh_decay_time_inner"])
 def test_body_backward_full_size_every_element(name):
     """The backward of a body workload at full size in the bench's launch
     configuration, every gradient against the gradient oracle (run on every

@@ -167,6 +167,33 @@ def test_linear_backward(shape, axis, path):
         bitwise(gb.cpu(), wb, "linear grad_b %s" % path)
 
 
+def test_linear_scan_backward_full_size_every_element():
+    """The linear-scan workload's backward at full size in the bench's launch
+    configuration; every gradient against the oracle (run on every host core
+    over contiguous blocks of the leading dimension), bit for bit."""
+    import oracle
+    from element_scan_recurrences_gb300 import workloads as wl
+    w = wl.MATRIX_WORKLOADS["linear_scan_lanes"]
+    a, b = wl.make_matrix_inputs(w, "cuda")
+    h = es.linear_scan(a, b, axis=w.axis)
+    G = torch.randn(h.shape, device="cuda", generator=torch.Generator("cuda").manual_seed(3))
+    ga, gb = es.linear_scan_backward(a, b, h, G, axis=w.axis)
+    es.device_status()
+    ah, bh, hh, gh = a.cpu().numpy(), b.cpu().numpy(), h.cpu().numpy(), G.cpu().numpy()
+    del a, b, h, G
+    got_a, got_b = ga.cpu().numpy(), gb.cpu().numpy()
+    del ga, gb
+    want_a, want_b = np.empty_like(got_a), np.empty_like(got_b)
+
+    def rows(lo, hi):
+        want_a[lo:hi], want_b[lo:hi] = M.linear_scan_backward(ah[lo:hi], bh[lo:hi], hh[lo:hi], gh[lo:hi],
+                                                              axis=w.axis)
+    oracle.split_rows(rows, ah.shape[0])
+    for lo in range(0, ah.shape[0], 8):
+        bitwise(got_a[lo:lo + 8], want_a[lo:lo + 8], "linear grad_a rows %d.." % lo)
+        bitwise(got_b[lo:lo + 8], want_b[lo:lo + 8], "linear grad_b rows %d.." % lo)
+
+
 def test_delta_rule_backward_full_size_every_element():
     """The delta-rule workload's backward at full size in the bench's launch
     configuration; every gradient against the oracle (run on every host core
